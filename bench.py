@@ -1,0 +1,473 @@
+"""Benchmark of the fused linear-attention forward + backward on GB300.
+
+One step = la_fwd followed by la_bwd over one batch of the workload (every kernel of the
+path), inputs resident in HBM.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun with one process per GPU.  The operation has no exchange step
+between (batch, kv head) groups, so ranks run independent replicas of the workload (weak
+scaling, no data-path collective); the timing is max-over-ranks, and ``value`` counts the
+tokens of all ranks.  ``--impl reference`` times the float64 CPU oracle (the only other
+implementation of the method here) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from efficient_transformer_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "linear-attn fwd+bwd tokens/s and TFLOP/s at 1 GB300; % of roofline"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+NOMINAL_CHUNK = 64          # chunk length of the nominal FLOP count
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# CUDA-core float32 peak: 152 SMs x 128 FP32 lanes x 2 flop per FMA x 2.07 GHz max clock.
+ALU_F32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+# ---------------------------------------------------------------------------------------
+# Work counts
+
+def tensor_bytes(w: gen.Workload):
+    el = 4 if w.dtype == "f32" else 2
+    qb = w.B * w.Hq * w.N * w.D * el
+    kvb = w.B * w.Hkv * w.N * w.D * el
+    return qb, kvb
+
+
+def path_bytes(w: gen.Workload) -> int:
+    """Compulsory bytes of fwd + bwd: fwd reads q, k, v and writes out; bwd reads q, k, v,
+    grad_out and writes dq, dk, dv; position weights are read once per pass."""
+    qb, kvb = tensor_bytes(w)
+    wb = 2 * 4 * w.N if w.weights else 0
+    return (2 * qb + 2 * kvb + wb) + (3 * qb + 4 * kvb + wb)
+
+
+def path_flops(w: gen.Workload) -> float:
+    """Nominal FLOPs of fwd + bwd, counted per query head with chunk length 64 and full
+    intra-chunk tiles; P is the number of (S, z) state pairs."""
+    P = 2 if w.weights else 1
+    D = Dv = w.D
+    rows = w.B * w.Hq * w.N
+    if w.causal:
+        f = rows * (4 * P * D * Dv + 2 * NOMINAL_CHUNK * (D + Dv))
+        b = rows * (10 * P * D * Dv + 2 * NOMINAL_CHUNK * (3 * D + 2 * Dv))
+    else:
+        f = rows * 4 * D * Dv * P
+        b = rows * 10 * D * Dv * P
+    return float(f + b)
+
+
+def kernel_work(name: str, w: gen.Workload):
+    """(bound, algorithmic units per launch, unit) for one kernel of the path.
+
+    CUDA-core kernels are bounded by float32 FMA throughput: their units are the FLOPs of
+    the arithmetic they must do (state updates 2 P D (D+1) per key token; per query row
+    the readout 2 P D (D+1) plus, causal, the 16-token intra-chunk tile).  Kernels that
+    stream tensors are bounded by HBM: their units are the bytes they must move once."""
+    P = 2 if w.weights else 1
+    D = w.D
+    qb, kvb = tensor_bytes(w)
+    kv_rows = w.B * w.Hkv * w.N
+    q_rows = w.B * w.Hq * w.N
+    st = 2 * P * D * (D + 1)
+    intra = (2 * 16 * P * D + 2 * 16 * (D + 1)) if w.causal else 0
+    table = {
+        "simt_seg_state": ("alu", kv_rows * st),
+        "simt_scan": ("hbm", None),
+        "simt_fwd": ("alu", q_rows * (st + intra) + (kv_rows * st if w.causal else 0)),
+        "simt_bwd_dq": ("alu", q_rows * (2 * st + 2 * intra) + (kv_rows * st if w.causal else 0)),
+        "simt_seg_rstate": ("alu", q_rows * st),
+        "simt_bwd_dkdv": ("alu", kv_rows * 2 * st + ((q_rows * (2 * intra + st)) if w.causal else 0)),
+    }
+    bound, units = table.get(name, ("hbm", None))
+    return bound, units, ("TFLOP/s" if bound == "alu" else "GB/s")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# Clock sampling (nvidia-smi, during the timed region)
+
+def nvsmi_id(dev, local: int) -> str:
+    """nvidia-smi --id for this CUDA device (its UUID when torch exposes it)."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except (AttributeError, RuntimeError):
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    return ids[local] if local < len(ids) else str(local)
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        window = [r for r in rows if t0 <= r[0] <= t1]
+        used = window if len(window) >= 3 else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used),
+                "sm_max_mhz": max(r[2] for r in used),
+                "power_w_max": max(r[3] for r in used),
+                "reasons": reasons, "samples": len(used),
+                "window": "timed region" if used is window else "whole run"}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+
+def oracle_sample(w: gen.Workload, tokens: int):
+    """Inputs for the first ``tokens`` positions of every (batch, head) of ``w``."""
+    ws = w.with_(N=tokens)
+    inp = gen.make_inputs(ws, seed=0)
+    return ws, inp
+
+
+def time_oracle(w: gen.Workload, tokens: int):
+    import oracle
+    ws, inp = oracle_sample(w, tokens)
+    kw = dict(is_causal=ws.causal, phi=ws.phi, eps=ws.eps, cos_weight=inp["cos_weight"],
+              sin_weight=inp["sin_weight"])
+    t0 = time.perf_counter()
+    oracle.fwd(inp["q"], inp["k"], inp["v"], **kw)
+    oracle.bwd(inp["q"], inp["k"], inp["v"], inp["grad_out"], **kw)
+    return time.perf_counter() - t0
+
+
+def oracle_tokens_for(w: gen.Workload, seconds: float) -> int:
+    """Sample length (tokens per sequence) whose oracle fwd+bwd takes about ``seconds``."""
+    probe = min(w.N, 128)
+    t = max(time_oracle(w, probe), 1e-4)
+    tokens = int(probe * seconds / t)
+    return max(16, min(w.N, tokens))
+
+
+def cpu_cores():
+    import oracle
+    return oracle.num_threads()
+
+
+# ---------------------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def config_of(w: gen.Workload, world: int):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "D": w.D,
+            "causal": w.causal, "phi": w.phi, "eps": w.eps, "cos_sin_weights": w.weights,
+            "input_scale": w.scale, "global_batch": w.B * world, "seq_len": w.N,
+            "parallelism": f"replicas{world}",
+            "l2": f"no explicit flush: inputs larger than L2 ({path_bytes(w) / 2**20:.0f} MiB moved "
+                  f"per step vs {L2_BYTES / 2**20:.0f} MiB L2)"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the float64 oracle as it stands, on the host cores, rank 0 only."""
+    if rank != 0:
+        return 0
+    w = gen.WORKLOADS[args.workload]
+    budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step, whole run ~2.5 min
+    tokens = oracle_tokens_for(w, min(10.0, budget))
+    for _ in range(args.warmup):
+        time_oracle(w, tokens)
+    times = [time_oracle(w, tokens) for _ in range(args.steps)]
+    t = statistics.mean(times)
+    value = w.B * tokens / t
+    sample = (f"first {tokens} of {w.N} positions of every (batch, head), fwd+bwd, float64 oracle; "
+              f"tokens/s = B*{tokens} / mean seconds per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) inputs)", "config": config_of(w, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    from efficient_transformer_gb300 import build as la_build
+    from efficient_transformer_gb300 import la
+
+    if rank == 0 and not os.path.exists(la.LIB_PATH):
+        la_build.build()
+    barrier(world)
+    la.load()
+    w = gen.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    host = gen.make_inputs(w, seed=rank)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
+    pinned = {n: (t.pin_memory() if t is not None else None) for n, t in host.items()}
+    del host
+    out = torch.empty_like(d["q"])
+    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+    has_w = d["cos_weight"] is not None
+    ws_f = torch.empty(max(1, la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, d["q"].dtype, w.causal, has_w, False)),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(1, la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, d["q"].dtype, w.causal, has_w, True)),
+                       dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x):
+        la.fwd(x["q"], x["k"], x["v"], w.causal, w.phi, w.eps, x["cos_weight"], x["sin_weight"],
+               out=out, workspace=ws_f, stream=stream)
+        la.bwd(x["q"], x["k"], x["v"], x["grad_out"], w.causal, w.phi, w.eps, x["cos_weight"],
+               x["sin_weight"], dq=dq, dk=dk, dv=dv, workspace=ws_b, stream=stream)
+
+    clocks = ClockSampler(nvsmi_id(dev, local))
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step(d)
+    la.get_status(stream)
+
+    # Device-timed region: inputs resident in HBM; every library launch traced with events.
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    la.trace_start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(d)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    kernels = la.trace_stop()
+    t_wall1 = time.time()
+    barrier(world)
+    la.get_status(stream)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms_step = ms_total / args.steps
+
+    # End to end: pinned host inputs -> device, fwd + bwd, every output back to pinned host.
+    e2e = None
+    if not args.no_e2e:
+        h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for n, t in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv))}
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values() if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+        e2e_steps = max(1, min(args.steps, 10))
+
+        def e2e_step():
+            for n, t in pinned.items():
+                if t is not None:
+                    d[n].copy_(t, non_blocking=True)
+            step(d)
+            for n, t in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv)):
+                h_out[n].copy_(t, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+        e2e = {"value": world * w.tokens / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    tokens_per_s = world * w.tokens / (ms_step / 1e3)
+    flops = path_flops(w)
+    nbytes = path_bytes(w)
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops_sustained"] * 1e12))
+
+    # Dominant kernel: the one with the largest share of traced device time.
+    launches = sum(n for n, _ in kernels.values())
+    total_ms = sum(ms for _, ms in kernels.values())
+    top = max(kernels.items(), key=lambda kv: kv[1][1])
+    top_name, (top_n, top_ms) = top
+    bound, units, unit = kernel_work(top_name, w)
+    per_launch_s = top_ms / top_n / 1e3
+    launches_per_step = top_n / args.steps
+    if bound == "alu":
+        achieved = units / launches_per_step / per_launch_s / 1e12
+        peak = ALU_F32_TFLOPS
+        peak_note = "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"
+    elif bound == "tensor":
+        achieved = units / launches_per_step / per_launch_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        peak_note = f"{peak_src} bf16_tflops_sustained"
+    else:
+        achieved = (units or 0) / launches_per_step / per_launch_s / 1e9
+        peak = peaks["hbm_gbs"]
+        peak_note = f"{peak_src} hbm_gbs"
+    roofline = {"bound": bound, "kernel": top_name, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": None, "peak_source": peak_note,
+                "launch_ms": per_launch_s * 1e3,
+                "share_of_traced_time": top_ms / total_ms if total_ms else None}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tokens = oracle_tokens_for(w, args.cpu_seconds)
+        t = time_oracle(w, tokens)
+        cpu = {"value": w.B * tokens / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"first {tokens} of {w.N} positions of every (batch, head), one fwd+bwd "
+                         f"({t:.1f} s); tokens/s = B*{tokens} / seconds"}
+
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) inputs, scale per workload)",
+        "config": config_of(w, world),
+        "tflops": world * flops / (ms_step / 1e3) / 1e12,
+        "path_roofline": {"bytes_per_step": nbytes, "flops_per_step": flops,
+                          "t_roofline_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
+                          "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s, bf16 sustained "
+                                   f"{peaks['bf16_tflops_sustained']} TFLOP/s"},
+        "roofline": roofline,
+        "kernels": {k: {"launches": n, "ms_per_launch": ms / n, "share": ms / total_ms if total_ms else None}
+                    for k, (n, ms) in sorted(kernels.items(), key=lambda kv: -kv[1][1])},
+        "gpu_launches": launches,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=gen.BENCH_WORKLOAD, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="approximate length of the CPU-oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps; the number is not a valid measurement",
+              file=sys.stderr)
+    world, rank, local = dist_setup()
+    if world != args.gpus and rank == 0:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,299 @@
+// la_api.cu -- the C ABI of libla.so: argument checks, the work plan, dispatch to the
+// kernel families, and the device error word.
+//
+// Entry points follow linear_attn.fwd(q, k, v, is_causal, phi, eps, cos_weight,
+// sin_weight) and linear_attn.bwd(..., grad_out) -> (dq, dk, dv) (module
+// neuralops.core.triton_kernels.linear_attn), with the key/value head count taken from
+// the caller as in gqa.fwd(k, v, num_kv_heads, num_heads) (module
+// neuralops.core.triton_kernels.gqa; its rule: both counts positive and the query count a
+// multiple of the key/value count).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "la_internal.cuh"
+
+namespace la {
+
+// Latched by kernels whose bounded waits run out; read and cleared by la_get_status().
+__device__ int g_error_word;
+
+namespace {
+
+thread_local char t_last_cuda[256] = "";
+
+la_status cuda_fail(cudaError_t e) {
+    std::snprintf(t_last_cuda, sizeof t_last_cuda, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+}
+
+// Device address of g_error_word on the current device (looked up once per device).
+cudaError_t error_word(int **out) {
+    static std::mutex mu;
+    static int *cache[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_error_word);
+        if (e != cudaSuccess) return e;
+        cache[dev] = static_cast<int *>(ptr);
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Host-only argument checks shared by every entry point.
+la_status check_shape(int B, int Hq, int Hkv, int N, int D, int dtype, int phi, float eps,
+                      const float *cw, const float *sw) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || D <= 0) return LA_ERR_ARG;
+    if (Hq % Hkv != 0) return LA_ERR_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_ARG;
+    if (phi != LA_PHI_ELU1 && phi != LA_PHI_RELU) return LA_ERR_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return LA_ERR_ARG;
+    if ((cw == nullptr) != (sw == nullptr)) return LA_ERR_ARG;
+    // element counts must fit comfortably in 64 bits
+    const unsigned long long elems = (unsigned long long)B * (unsigned long long)Hq *
+                                     (unsigned long long)N * (unsigned long long)D;
+    if (elems >> 60) return LA_ERR_ARG;
+    if (D != 32 && D != 64 && D != 128) return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
+// The work plan, a pure function of the arguments.
+Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, int has_w, int is_bwd) {
+    Plan pl{};
+    pl.P = has_w ? 2 : 1;
+    pl.path = tc_supported(Hq, Hkv, N, D, dt, pl.P, causal, is_bwd) ? LA_PATH_TCGEN05 : LA_PATH_SIMT;
+    pl.chunk = 16;
+    const int bg = B * Hkv;
+    const int nchunks = (N + pl.chunk - 1) / pl.chunk;
+    int want = (2 * kPlanSms + bg - 1) / bg;        // about two CTAs per SM in total
+    if (want > nchunks) want = nchunks;
+    if (want < 1) want = 1;
+    const int chunks_per_seg = (nchunks + want - 1) / want;
+    pl.seg_len = chunks_per_seg * pl.chunk;
+    pl.nseg = (N + pl.seg_len - 1) / pl.seg_len;
+    pl.state_elems = (size_t)pl.P * D * (D + 1);
+    const size_t state_bytes = align_up((size_t)bg * pl.nseg * pl.state_elems * sizeof(float), 256);
+    pl.off_state = 0;
+    size_t off = state_bytes;
+    if (is_bwd) {
+        pl.off_rstate = off;
+        off += state_bytes;
+        const size_t row_bytes = align_up((size_t)B * Hq * N * sizeof(float), 256);
+        pl.off_den = off;
+        off += row_bytes;
+        pl.off_gd = off;
+        off += row_bytes;
+    }
+    pl.ws_bytes = off;
+    return pl;
+}
+
+la_status run(bool bwd, const void *q, const void *k, const void *v, const void *g, void *out,
+              void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int D, la_dtype dt,
+              int causal, la_phi phi, float eps, const float *cw, const float *sw, void *ws,
+              size_t ws_bytes, void *stream) {
+    la_status st = check_shape(B, Hq, Hkv, N, D, dt, phi, eps, cw, sw);
+    if (st != LA_OK) return st;
+    if (!q || !k || !v) return LA_ERR_ARG;
+    if (bwd ? (!g || !dq || !dk || !dv) : !out) return LA_ERR_ARG;
+    const void *ptrs[] = {q, k, v, g, out, dq, dk, dv, cw, sw};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned(ptr, 16)) return LA_ERR_ALIGN;
+    const Plan pl = make_plan(B, Hq, Hkv, N, D, dt, causal, cw != nullptr, bwd);
+    if (pl.ws_bytes > 0) {
+        if (!ws || ws_bytes < pl.ws_bytes) return LA_ERR_WORKSPACE;
+        if (!aligned(ws, 256)) return LA_ERR_ALIGN;
+    }
+
+    Params p{};
+    p.q = q; p.k = k; p.v = v; p.g = g;
+    p.out = out; p.dq = dq; p.dk = dk; p.dv = dv;
+    p.cw = cw; p.sw = sw;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.D = D; p.n_rep = Hq / Hkv;
+    p.P = pl.P; p.phi = phi; p.causal = causal ? 1 : 0; p.eps = eps;
+    p.chunk = pl.chunk; p.seg_len = pl.seg_len; p.nseg = pl.nseg;
+    char *base = static_cast<char *>(ws);
+    p.state = reinterpret_cast<float *>(base + pl.off_state);
+    p.rstate = bwd ? reinterpret_cast<float *>(base + pl.off_rstate) : nullptr;
+    p.den = bwd ? reinterpret_cast<float *>(base + pl.off_den) : nullptr;
+    p.gd = bwd ? reinterpret_cast<float *>(base + pl.off_gd) : nullptr;
+    cudaError_t e = error_word(&p.err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pl.path == LA_PATH_TCGEN05)
+        e = bwd ? tc_backward(p, s) : tc_forward(p, s);
+    else
+        e = bwd ? simt_backward(p, dt, s) : simt_forward(p, dt, s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+// ---- trace facility --------------------------------------------------------------------
+
+namespace {
+struct TraceRecord {
+    const char *name;
+    cudaEvent_t start, stop;
+};
+struct TraceTotal {
+    const char *name;
+    int launches;
+    double ms;
+};
+std::mutex g_trace_mu;
+std::atomic<bool> g_trace_on{false};
+std::vector<TraceRecord> g_trace_records;
+std::vector<TraceTotal> g_trace_totals;
+}  // namespace
+
+TraceScope::TraceScope(const char *name, cudaStream_t s) : name_(name), stream_(s) {
+    if (!g_trace_on.load(std::memory_order_relaxed)) return;
+    if (cudaEventCreate(&start_) != cudaSuccess || cudaEventRecord(start_, s) != cudaSuccess) {
+        if (start_) cudaEventDestroy(start_);
+        start_ = nullptr;
+    }
+}
+
+TraceScope::~TraceScope() {
+    if (!start_) return;
+    cudaEvent_t stop = nullptr;
+    if (cudaEventCreate(&stop) != cudaSuccess || cudaEventRecord(stop, stream_) != cudaSuccess) {
+        cudaEventDestroy(start_);
+        if (stop) cudaEventDestroy(stop);
+        return;
+    }
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace_records.push_back({name_, start_, stop});
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+size_t la_workspace_size(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
+                         int has_weights, int is_bwd) {
+    const float *w = has_weights ? reinterpret_cast<const float *>(16) : nullptr;
+    if (check_shape(B, Hq, Hkv, N, D, dtype, LA_PHI_ELU1, 0.f, w, w) != LA_OK) return 0;
+    return make_plan(B, Hq, Hkv, N, D, dtype, is_causal, has_weights, is_bwd).ws_bytes;
+}
+
+la_path la_kernel_path(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
+                       int has_weights, int is_bwd) {
+    const float *w = has_weights ? reinterpret_cast<const float *>(16) : nullptr;
+    if (check_shape(B, Hq, Hkv, N, D, dtype, LA_PHI_ELU1, 0.f, w, w) != LA_OK) return LA_PATH_SIMT;
+    return make_plan(B, Hq, Hkv, N, D, dtype, is_causal, has_weights, is_bwd).path;
+}
+
+la_status la_fwd(const void *q, const void *k, const void *v, void *out, int B, int Hq, int Hkv,
+                 int N, int D, la_dtype dtype, int is_causal, la_phi phi, float eps,
+                 const float *cos_weight, const float *sin_weight, void *workspace,
+                 size_t ws_bytes, void *stream) {
+    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, dtype,
+               is_causal, phi, eps, cos_weight, sin_weight, workspace, ws_bytes, stream);
+}
+
+la_status la_bwd(const void *q, const void *k, const void *v, const void *grad_out, void *dq,
+                 void *dk, void *dv, int B, int Hq, int Hkv, int N, int D, la_dtype dtype,
+                 int is_causal, la_phi phi, float eps, const float *cos_weight,
+                 const float *sin_weight, void *workspace, size_t ws_bytes, void *stream) {
+    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, dtype, is_causal,
+               phi, eps, cos_weight, sin_weight, workspace, ws_bytes, stream);
+}
+
+la_status la_get_status(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (word != kErrNone) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e);
+        return LA_ERR_TIMEOUT;
+    }
+    return LA_OK;
+}
+
+const char *la_status_str(la_status status) {
+    switch (status) {
+        case LA_OK: return "ok";
+        case LA_ERR_ARG: return "invalid argument";
+        case LA_ERR_UNSUPPORTED: return "unsupported head dimension (D must be 32, 64 or 128)";
+        case LA_ERR_ALIGN: return "misaligned pointer (16 bytes; workspace 256 bytes)";
+        case LA_ERR_CUDA: return "CUDA error";
+        case LA_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+        case LA_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char *la_last_cuda_error(void) { return t_last_cuda; }
+
+la_status la_trace_start(void) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    for (auto &r : g_trace_records) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    g_trace_records.clear();
+    g_trace_totals.clear();
+    g_trace_on.store(true);
+    return LA_OK;
+}
+
+la_status la_trace_stop(void) {
+    g_trace_on.store(false);
+    return LA_OK;
+}
+
+int la_trace_collect(void) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    for (auto &r : g_trace_records) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.stop) == cudaSuccess &&
+            cudaEventElapsedTime(&ms, r.start, r.stop) == cudaSuccess) {
+            bool found = false;
+            for (auto &t : g_trace_totals)
+                if (std::strcmp(t.name, r.name) == 0) {
+                    t.launches += 1;
+                    t.ms += ms;
+                    found = true;
+                    break;
+                }
+            if (!found) g_trace_totals.push_back({r.name, 1, (double)ms});
+        }
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    g_trace_records.clear();
+    return (int)g_trace_totals.size();
+}
+
+la_status la_trace_kernel(int index, const char **name, int *launches, double *total_ms) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (index < 0 || index >= (int)g_trace_totals.size() || !name || !launches || !total_ms)
+        return LA_ERR_ARG;
+    *name = g_trace_totals[index].name;
+    *launches = g_trace_totals[index].launches;
+    *total_ms = g_trace_totals[index].ms;
+    return LA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// la_internal.cuh -- shared definitions of the linear-attention library (not part of the
+// public ABI): launch parameters, the work plan, and small device helpers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "la.h"
+
+namespace la {
+
+// Number of SMs the work split is planned for (GB300: 152).  The split only sets how a
+// head's sequence is cut into segments; results are correct on any device, and for a
+// given set of arguments the split (and so the float summation order) never depends on
+// the device.
+constexpr int kPlanSms = 152;
+
+// Device error word values (latched by kernels, read by la_get_status).
+constexpr int kErrNone = 0;
+constexpr int kErrTimeout = 1;
+
+// Everything a kernel needs.  Tensor pointers are typed void: the element type is a
+// template parameter of each kernel.
+struct Params {
+    const void *q, *k, *v, *g;   // inputs ([B,Hq,N,D] for q, g; [B,Hkv,N,D] for k, v)
+    void *out, *dq, *dk, *dv;    // outputs
+    const float *cw, *sw;        // position weights or null
+    int B, Hq, Hkv, N, D, n_rep, P, phi, causal;
+    float eps;
+    int chunk, seg_len, nseg;    // work split along the sequence
+    float *state;                // per (b, kv head, segment) forward state partials
+    float *rstate;               // per (b, kv head, segment) backward state partials
+    float *den;                  // [B, Hq, N] row denominators (backward)
+    float *gd;                   // [B, Hq, N] denominator gradients (backward)
+    int *err;                    // device error word
+};
+
+// How one call is carried out.  Filled by make_plan() from the arguments alone.
+struct Plan {
+    la_path path;
+    int P;            // 1, or 2 with cos/sin weights
+    int chunk;        // tokens per chunk
+    int seg_len;      // tokens per segment (a multiple of chunk)
+    int nseg;         // segments per (batch, kv head)
+    size_t state_elems;   // floats of one segment state (all terms)
+    size_t off_state, off_rstate, off_den, off_gd;   // workspace byte offsets
+    size_t ws_bytes;
+};
+
+// --- device helpers --------------------------------------------------------------------
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// phi and its derivative (phi = 0: elu(x) + 1, alpha = 1; phi = 1: relu).
+__device__ __forceinline__ float feature(float x, int phi) {
+    if (phi == LA_PHI_ELU1) return x > 0.f ? x + 1.f : expf(x);
+    return x > 0.f ? x : 0.f;
+}
+__device__ __forceinline__ float feature_grad(float x, int phi) {
+    if (phi == LA_PHI_ELU1) return x > 0.f ? 1.f : expf(x);
+    return x > 0.f ? 1.f : 0.f;
+}
+
+// Position weight of term p at token t (1 when there are no weights).
+__device__ __forceinline__ float pos_weight(const Params &p, int term, int t) {
+    if (!p.cw) return 1.f;
+    return term == 0 ? p.cw[t] : p.sw[t];
+}
+
+// --- trace facility (la_trace_*) ---------------------------------------------------------
+
+// Brackets one kernel launch with CUDA events while tracing is on; a no-op otherwise.
+class TraceScope {
+  public:
+    TraceScope(const char *name, cudaStream_t s);
+    ~TraceScope();
+    TraceScope(const TraceScope &) = delete;
+    TraceScope &operator=(const TraceScope &) = delete;
+
+  private:
+    const char *name_;
+    cudaStream_t stream_;
+    cudaEvent_t start_ = nullptr;
+};
+
+// --- launchers (defined in the kernel translation units) --------------------------------
+
+cudaError_t simt_forward(const Params &p, la_dtype dt, cudaStream_t s);
+cudaError_t simt_backward(const Params &p, la_dtype dt, cudaStream_t s);
+cudaError_t tc_forward(const Params &p, cudaStream_t s);
+cudaError_t tc_backward(const Params &p, cudaStream_t s);
+bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal, int is_bwd);
+
+}  // namespace la

@@ -1,0 +1,229 @@
+"""Thin Python binding of libla.so (argument marshalling only).
+
+``fwd`` and ``bwd`` follow the signatures of the linear_attn page
+(module neuralops.core.triton_kernels.linear_attn): ``fwd(q, k, v, is_causal=False,
+phi="elu+1", eps=1e-6, cos_weight=None, sin_weight=None)`` and ``bwd(q, k, v, grad_out,
+...) -> (dq, dk, dv)``.  The key/value head count is read from ``k.shape[1]``; when it is
+smaller than ``q.shape[1]`` the call is grouped-query attention (module
+neuralops.core.triton_kernels.gqa) with the expansion fused into the kernels, and dk, dv
+come back with the key/value shape, summed over each group.
+
+PyTorch supplies device memory and the current stream; every arithmetic step runs in
+the library's CUDA kernels.  There is no fallback: if libla.so is missing or a call
+fails, an exception says why.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libla.so")
+
+LA_OK, LA_ERR_ARG, LA_ERR_UNSUPPORTED, LA_ERR_ALIGN, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(7)
+LA_F32, LA_BF16 = 0, 1
+LA_PATH_SIMT, LA_PATH_TCGEN05 = 0, 1
+PHI = {"elu+1": 0, "relu": 1}
+_NOT_BUILT = {"identity", "softmax_free"}
+
+_lib = None
+
+
+class LinearAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(what)
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Open libla.so (built by ``efficient_transformer_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libla.so not found at {p}: build it with "
+                           "`python -m efficient_transformer_gb300.build` (no fallback exists)")
+    lib = ctypes.CDLL(p)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.la_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
+    lib.la_workspace_size.restype = sz
+    lib.la_kernel_path.argtypes = [i, i, i, i, i, i, i, i, i]
+    lib.la_kernel_path.restype = i
+    lib.la_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
+    lib.la_fwd.restype = i
+    lib.la_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
+    lib.la_bwd.restype = i
+    lib.la_get_status.argtypes = [vp]
+    lib.la_get_status.restype = i
+    lib.la_status_str.argtypes = [i]
+    lib.la_status_str.restype = ctypes.c_char_p
+    lib.la_last_cuda_error.argtypes = []
+    lib.la_last_cuda_error.restype = ctypes.c_char_p
+    lib.la_trace_start.argtypes = []
+    lib.la_trace_start.restype = i
+    lib.la_trace_stop.argtypes = []
+    lib.la_trace_stop.restype = i
+    lib.la_trace_collect.argtypes = []
+    lib.la_trace_collect.restype = i
+    lib.la_trace_kernel.argtypes = [i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i),
+                                    ctypes.POINTER(ctypes.c_double)]
+    lib.la_trace_kernel.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _raise(lib, status: int, call: str):
+    what = lib.la_status_str(status).decode()
+    if status == LA_ERR_CUDA:
+        what += ": " + lib.la_last_cuda_error().decode()
+    raise LinearAttentionError(status, f"{call}: {what}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _phi_code(phi: str) -> int:
+    if phi in _NOT_BUILT:
+        raise NotImplementedError(f"phi={phi!r} is not built (only 'elu+1' and 'relu')")
+    if phi not in PHI:
+        raise ValueError(f"unknown phi {phi!r}")
+    return PHI[phi]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_inputs(q, k, v, cos_weight, sin_weight, extra=()):
+    for name, t in (("q", q), ("k", k), ("v", v)) + tuple(extra):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, N, D] tensor")
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, q has {q.dtype}")
+    B, Hq, N, D = q.shape
+    if k.shape[0] != B or k.shape[2:] != (N, D) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if (cos_weight is None) != (sin_weight is None):
+        raise ValueError("give both cos_weight and sin_weight or neither")
+    for name, w in (("cos_weight", cos_weight), ("sin_weight", sin_weight)):
+        if w is not None and (w.dtype != torch.float32 or not w.is_cuda or w.shape != (N,)
+                              or not w.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA vector of length N={N}")
+    return B, Hq, k.shape[1], N, D
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_size(B, Hq, Hkv, N, D, dtype: torch.dtype, is_causal: bool, has_weights: bool,
+                   is_bwd: bool) -> int:
+    code = LA_F32 if dtype == torch.float32 else LA_BF16
+    return int(load().la_workspace_size(B, Hq, Hkv, N, D, code, int(is_causal), int(has_weights),
+                                        int(is_bwd)))
+
+
+def kernel_path(B, Hq, Hkv, N, D, dtype: torch.dtype, is_causal: bool, has_weights: bool,
+                is_bwd: bool) -> int:
+    code = LA_F32 if dtype == torch.float32 else LA_BF16
+    return int(load().la_kernel_path(B, Hq, Hkv, N, D, code, int(is_causal), int(has_weights),
+                                     int(is_bwd)))
+
+
+def _workspace(nbytes: int, device, given):
+    if nbytes == 0:
+        return None
+    if given is not None:
+        if given.numel() * given.element_size() < nbytes:
+            raise ValueError(f"workspace holds {given.numel() * given.element_size()} bytes, "
+                             f"{nbytes} needed")
+        return given
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, is_causal: bool = False,
+        phi: str = "elu+1", eps: float = 1e-6, cos_weight: torch.Tensor | None = None,
+        sin_weight: torch.Tensor | None = None, *, out: torch.Tensor | None = None,
+        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Linear-attention forward; returns ``out`` with the shape and dtype of ``q``."""
+    lib = load()
+    B, Hq, Hkv, N, D = _check_inputs(q, k, v, cos_weight, sin_weight)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    dt = _dtype_code(q)
+    ws = _workspace(lib.la_workspace_size(B, Hq, Hkv, N, D, dt, int(is_causal),
+                                          int(cos_weight is not None), 0), q.device, workspace)
+    st = lib.la_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, D, dt, int(is_causal),
+                    _phi_code(phi), float(eps), _ptr(cos_weight), _ptr(sin_weight), _ptr(ws),
+                    0 if ws is None else ws.numel() * ws.element_size(), _stream_handle(stream))
+    if st != LA_OK:
+        _raise(lib, st, "la_fwd")
+    return out
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tensor,
+        is_causal: bool = False, phi: str = "elu+1", eps: float = 1e-6,
+        cos_weight: torch.Tensor | None = None, sin_weight: torch.Tensor | None = None, *,
+        dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
+        dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Linear-attention backward; returns ``(dq, dk, dv)`` (dk, dv with k's shape)."""
+    lib = load()
+    B, Hq, Hkv, N, D = _check_inputs(q, k, v, cos_weight, sin_weight, (("grad_out", grad_out),))
+    if grad_out.shape != q.shape:
+        raise ValueError("grad_out must have the shape of q")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor like its input")
+    dt = _dtype_code(q)
+    ws = _workspace(lib.la_workspace_size(B, Hq, Hkv, N, D, dt, int(is_causal),
+                                          int(cos_weight is not None), 1), q.device, workspace)
+    st = lib.la_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
+                    B, Hq, Hkv, N, D, dt, int(is_causal), _phi_code(phi), float(eps),
+                    _ptr(cos_weight), _ptr(sin_weight), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                    _stream_handle(stream))
+    if st != LA_OK:
+        _raise(lib, st, "la_bwd")
+    return dq, dk, dv
+
+
+def get_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel latched an error since the last check."""
+    lib = load()
+    st = lib.la_get_status(_stream_handle(stream))
+    if st != LA_OK:
+        _raise(lib, st, "la_get_status")
+
+
+def trace_start() -> None:
+    """Start bracketing every library kernel launch with CUDA events (for reports)."""
+    load().la_trace_start()
+
+
+def trace_stop() -> dict:
+    """Stop tracing; return {kernel name: (launches, total device ms)} since trace_start()."""
+    lib = load()
+    lib.la_trace_stop()
+    n = lib.la_trace_collect()
+    res = {}
+    for idx in range(n):
+        name, launches, ms = ctypes.c_char_p(), ctypes.c_int(), ctypes.c_double()
+        if lib.la_trace_kernel(idx, ctypes.byref(name), ctypes.byref(launches), ctypes.byref(ms)) == LA_OK:
+            res[name.value.decode()] = (launches.value, ms.value)
+    return res

@@ -1,0 +1,133 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) fused linear-attention library (libla.so).
+ *
+ * The operation (module neuralops.core.triton_kernels.linear_attn, functions `fwd` and
+ * `bwd`; feature list in that module's docstring: feature maps elu+1 and relu, chunked
+ * causal streaming, bidirectional parallel reduction, cosFormer cos/sin modulation):
+ *
+ *   a_i^p = w_i^p phi(q_i),  b_j^p = w_j^p phi(k_j)
+ *   S_i^p = sum_{j in J(i)} b_j^p v_j^T,  z_i^p = sum_{j in J(i)} b_j^p
+ *   out_i = (sum_p (a_i^p)^T S_i^p) / (sum_p a_i^p . z_i^p + eps)
+ *
+ * J(i) = {j <= i} (causal) or all j (bidirectional); phi(x) = elu(x) + 1 or relu(x);
+ * without position weights there is one term p with w = 1, with them there are two:
+ * w^cos = cos_weight and w^sin = sin_weight.  la_bwd returns the exact gradient of la_fwd
+ * (the page's `bwd` differentiates `fwd`).
+ *
+ * Grouped-query attention (module neuralops.core.triton_kernels.gqa, `fwd`/`bwd`): with
+ * Hkv key/value heads and Hq = n_rep * Hkv query heads, query head h reads key/value head
+ * h / n_rep, and dk, dv are the sums over the n_rep query heads of each group.  The
+ * expanded key/value tensors are never formed.
+ *
+ * Layout: q, out, grad_out, dq are contiguous [B, Hq, N, D]; k, v, dk, dv are contiguous
+ * [B, Hkv, N, D] (row-major, D fastest; Dv = D).  Elements are float32 (LA_F32) or
+ * bfloat16 (LA_BF16); outputs use the input type.  Arithmetic is float32 accumulation in
+ * both cases (bfloat16 tensor-core operands on the LA_BF16 fast path).  cos_weight and
+ * sin_weight are float32 device vectors of length N, indexed by position, applied to
+ * phi(q_i) and phi(k_i); give both or neither.
+ *
+ * Ownership: every pointer is caller-owned device memory (except where a function says
+ * host).  The library allocates no device memory: scratch comes from the caller's
+ * workspace of at least la_workspace_size() bytes, 256-byte aligned.  Outputs are fully
+ * overwritten, never accumulated into.  The workspace must not be shared by calls that
+ * can run at the same time.
+ *
+ * Execution: la_fwd and la_bwd only enqueue kernels on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and return; they never synchronise.  Their status covers
+ * argument checks and launch errors.  Errors found by a kernel while it runs (a bounded
+ * wait that ran out) are latched in a device word that la_get_status() reads.
+ *
+ * Errors: no exception crosses this ABI and no kernel traps.
+ *   LA_ERR_ARG          null required pointer, B, Hq, Hkv, N or D <= 0, Hq % Hkv != 0,
+ *                       eps negative or not finite, unknown dtype or phi, exactly one of
+ *                       cos_weight / sin_weight given, sizes whose element count
+ *                       overflows 64 bits
+ *   LA_ERR_UNSUPPORTED  D not in {32, 64, 128}
+ *   LA_ERR_ALIGN        a pointer that is not 16-byte aligned (workspace: 256-byte)
+ *   LA_ERR_WORKSPACE    ws_bytes < la_workspace_size(...) or workspace NULL while needed
+ *   LA_ERR_CUDA         a CUDA launch or runtime error (see la_last_cuda_error())
+ *   LA_ERR_TIMEOUT      (from la_get_status) a kernel's bounded wait ran out
+ * All argument checks run on the host before any CUDA call.
+ */
+#ifndef LA_H
+#define LA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_ARG = 1,
+    LA_ERR_UNSUPPORTED = 2,
+    LA_ERR_ALIGN = 3,
+    LA_ERR_CUDA = 4,
+    LA_ERR_TIMEOUT = 5,
+    LA_ERR_WORKSPACE = 6
+} la_status;
+
+/* Feature map phi: elu(x) + 1 with alpha = 1, or max(x, 0). */
+typedef enum { LA_PHI_ELU1 = 0, LA_PHI_RELU = 1 } la_phi;
+
+/* Element type of q, k, v, grad_out and of every output. */
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+/* Which kernel family a call with these arguments runs. */
+typedef enum { LA_PATH_SIMT = 0, LA_PATH_TCGEN05 = 1 } la_path;
+
+/* Bytes of workspace that la_fwd (is_bwd = 0) or la_bwd (is_bwd = 1) needs for these
+ * sizes.  Host-only, never fails: returns 0 for arguments la_fwd / la_bwd would reject.
+ * has_weights: 1 when cos_weight and sin_weight are given. */
+size_t la_workspace_size(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
+                         int has_weights, int is_bwd);
+
+/* Kernel family chosen for these arguments (host-only; for tests and reports). */
+la_path la_kernel_path(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
+                       int has_weights, int is_bwd);
+
+/* Forward, `linear_attn.fwd(q, k, v, is_causal, phi, eps, cos_weight, sin_weight)`:
+ * writes out [B, Hq, N, D]. */
+la_status la_fwd(const void *q, const void *k, const void *v, void *out, int B, int Hq,
+                 int Hkv, int N, int D, la_dtype dtype, int is_causal, la_phi phi, float eps,
+                 const float *cos_weight, const float *sin_weight, void *workspace,
+                 size_t ws_bytes, void *stream);
+
+/* Backward, `linear_attn.bwd(q, k, v, grad_out, is_causal, phi, eps, cos_weight,
+ * sin_weight) -> (dq, dk, dv)`: writes dq [B, Hq, N, D] and the group-summed dk, dv
+ * [B, Hkv, N, D].  Recomputes what it needs of the forward from q, k, v. */
+la_status la_bwd(const void *q, const void *k, const void *v, const void *grad_out, void *dq,
+                 void *dk, void *dv, int B, int Hq, int Hkv, int N, int D, la_dtype dtype,
+                 int is_causal, la_phi phi, float eps, const float *cos_weight,
+                 const float *sin_weight, void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then returns and clears the device-side error word of the
+ * current device: LA_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call,
+ * LA_ERR_CUDA if the synchronisation failed, else LA_OK. */
+la_status la_get_status(void *stream);
+
+/* Static, NUL-terminated description of a status code (host). */
+const char *la_status_str(la_status status);
+
+/* Static description of the most recent CUDA error seen by this library on the calling
+ * thread ("" if none). */
+const char *la_last_cuda_error(void);
+
+/* Kernel timing for reports.  Between la_trace_start() and la_trace_stop() the library
+ * brackets each of its kernel launches with a pair of CUDA events recorded on the
+ * launch's own stream (the kernels themselves are unchanged).  la_trace_collect()
+ * waits for those events, folds them per kernel name, frees them and returns how many
+ * distinct kernels ran; la_trace_kernel() then reads entry `index` (0-based): a static
+ * name, the number of launches and their summed device time in milliseconds.  Host-side
+ * state is process-wide and guarded by a mutex. */
+la_status la_trace_start(void);
+la_status la_trace_stop(void);
+int la_trace_collect(void);
+la_status la_trace_kernel(int index, const char **name, int *launches, double *total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H */

@@ -1,0 +1,58 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the binding, run the
+oracle on the same inputs, and compare per output tensor."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from efficient_transformer_gb300 import inputs as gen
+from efficient_transformer_gb300 import la
+
+# max|gpu - oracle| / max|oracle| per output tensor
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def to_dev(inp: dict) -> dict:
+    return {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
+
+
+def run_gpu(w: gen.Workload, dev: dict):
+    out = la.fwd(dev["q"], dev["k"], dev["v"], w.causal, w.phi, w.eps, dev["cos_weight"],
+                 dev["sin_weight"])
+    dq, dk, dv = la.bwd(dev["q"], dev["k"], dev["v"], dev["grad_out"], w.causal, w.phi, w.eps,
+                        dev["cos_weight"], dev["sin_weight"])
+    la.get_status()
+    return out, dq, dk, dv
+
+
+def run_oracle(w: gen.Workload, inp: dict):
+    args = (inp["q"], inp["k"], inp["v"])
+    kw = dict(is_causal=w.causal, phi=w.phi, eps=w.eps, cos_weight=inp["cos_weight"],
+              sin_weight=inp["sin_weight"])
+    out = oracle.fwd(*args, **kw)
+    dq, dk, dv = oracle.bwd(*args, inp["grad_out"], **kw)
+    return out, dq, dk, dv
+
+
+def rel_err(got: torch.Tensor, ref: np.ndarray) -> float:
+    g = got.detach().to("cpu", torch.float64).numpy()
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), "non-finite values in the GPU result"
+    return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def compare(w: gen.Workload, got, ref, label: str = ""):
+    tol = TOL[w.dtype]
+    errs = {n: rel_err(a, b) for n, a, b in zip(("out", "dq", "dk", "dv"), got, ref)}
+    bad = {n: e for n, e in errs.items() if not e <= tol}
+    assert not bad, f"{label} {w.name}: errors {errs} exceed {tol}"
+    return errs
+
+
+def group_rows(w: gen.Workload, results, b: int, g: int):
+    """The rows of (out, dq, dk, dv) that belong to batch b and key/value head g."""
+    n_rep = w.Hq // w.Hkv
+    out, dq, dk, dv = results
+    hs = slice(g * n_rep, (g + 1) * n_rep)
+    return out[b:b + 1, hs], dq[b:b + 1, hs], dk[b:b + 1, g:g + 1], dv[b:b + 1, g:g + 1]

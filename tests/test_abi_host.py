@@ -1,0 +1,112 @@
+"""The C-ABI library on the host: it builds, loads, exports every declared symbol, and
+rejects bad arguments before any CUDA call (so these run without a GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from efficient_transformer_gb300 import build as la_build
+from efficient_transformer_gb300 import la
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    la_build.build()
+    return la.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"\b(la_[A-Za-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_headers_declare_entry_points():
+    names = declared_functions()
+    for required in ("la_fwd", "la_bwd", "la_workspace_size", "la_get_status", "la_status_str"):
+        assert required in names
+
+
+@pytest.mark.parametrize("name", declared_functions())
+def test_symbol_exported(lib, name):
+    assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.la_status_str(code)
+    assert lib.la_status_str(99) == b"unknown status"
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails its checks
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def fwd_call(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, Hq=4, Hkv=2, N=64, D=64, dt=la.LA_BF16,
+             causal=1, phi=0, eps=1e-6, cw=None, sw=None, ws=None, ws_bytes=0, stream=None)
+    a.update(over)
+    return lib.la_fwd(a["q"], a["k"], a["v"], a["out"], a["B"], a["Hq"], a["Hkv"], a["N"], a["D"],
+                      a["dt"], a["causal"], a["phi"], a["eps"], a["cw"], a["sw"], a["ws"],
+                      a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), la.LA_ERR_ARG),
+    (dict(out=None), la.LA_ERR_ARG),
+    (dict(B=0), la.LA_ERR_ARG),
+    (dict(N=-1), la.LA_ERR_ARG),
+    (dict(Hq=3), la.LA_ERR_ARG),              # not a multiple of Hkv (gqa rule)
+    (dict(Hkv=0), la.LA_ERR_ARG),
+    (dict(eps=-1.0), la.LA_ERR_ARG),
+    (dict(eps=float("inf")), la.LA_ERR_ARG),
+    (dict(eps=float("nan")), la.LA_ERR_ARG),
+    (dict(dt=7), la.LA_ERR_ARG),
+    (dict(phi=5), la.LA_ERR_ARG),
+    (dict(cw=FAKE), la.LA_ERR_ARG),           # one weight without the other
+    (dict(D=48), la.LA_ERR_UNSUPPORTED),
+    (dict(D=256), la.LA_ERR_UNSUPPORTED),
+    (dict(k=MISALIGNED), la.LA_ERR_ALIGN),
+    (dict(ws=None, ws_bytes=0), la.LA_ERR_WORKSPACE),
+    (dict(ws=FAKE, ws_bytes=16), la.LA_ERR_WORKSPACE),
+])
+def test_fwd_rejects(lib, over, code):
+    assert fwd_call(lib, **over) == code
+
+
+def test_bwd_rejects(lib):
+    args = [FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 1, 4, 2, 64, 64, la.LA_BF16, 1, 0, 1e-6,
+            None, None, None, 0, None]
+    assert lib.la_bwd(*args) == la.LA_ERR_ARG      # grad_out missing
+    args[3] = FAKE
+    assert lib.la_bwd(*args) == la.LA_ERR_WORKSPACE
+
+
+def test_workspace_sizes(lib):
+    f = lib.la_workspace_size(1, 32, 8, 65536, 128, la.LA_BF16, 1, 0, 0)
+    b = lib.la_workspace_size(1, 32, 8, 65536, 128, la.LA_BF16, 1, 0, 1)
+    assert 0 < f < b
+    # the backward keeps two float32 values per query row on top of its states
+    assert b >= 2 * 4 * 32 * 65536
+    assert lib.la_workspace_size(1, 3, 2, 64, 64, la.LA_BF16, 1, 0, 0) == 0     # invalid
+    # deterministic plan
+    assert f == lib.la_workspace_size(1, 32, 8, 65536, 128, la.LA_BF16, 1, 0, 0)
+
+
+def test_float32_always_takes_simt(lib):
+    assert lib.la_kernel_path(1, 2, 2, 256, 32, la.LA_F32, 1, 0, 0) == la.LA_PATH_SIMT
+    assert lib.la_kernel_path(1, 32, 8, 65536, 128, la.LA_F32, 1, 0, 1) == la.LA_PATH_SIMT
+
+
+def test_python_binding_rejects_unbuilt_phi():
+    with pytest.raises(NotImplementedError):
+        la._phi_code("identity")
+    with pytest.raises(ValueError):
+        la._phi_code("gelu")

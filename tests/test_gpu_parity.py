@@ -1,0 +1,153 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Bar: max|gpu - oracle| / max|oracle| per output tensor <= 1e-4 for float32 inputs and
+<= 2e-2 for bfloat16 inputs, on the same seeded inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as H
+from efficient_transformer_gb300 import build as la_build
+from efficient_transformer_gb300 import inputs as gen
+from efficient_transformer_gb300 import la
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    la_build.build()
+    la.load()
+
+
+# Workloads small enough for the full oracle.
+SMALL = ["causal_b1_h2_n256_d32_f32", "bidir_b2_h8_n2048_d64_bf16_elu1",
+         "bidir_b2_h8_n2048_d64_bf16_relu", "causal_b4_h16_n4096_d64_bf16"]
+# Full-size workloads checked on whole key/value groups (b, g): groups are independent,
+# so the oracle on a group's slice gives exactly those rows of the full result.
+LARGE = {"cosformer_causal_b2_h16_n8192_d128_bf16": [(0, 0), (1, 15)],
+         "gqa_causal_b1_hq32_hkv8_n65536_d128_bf16": [(0, 0), (0, 7)]}
+
+
+def groups_slice(inp, w, groups):
+    """Concatenate several (b, g) slices along the head axes (one oracle call, more threads)."""
+    parts = [gen.kv_group_slice(inp, w, b, g) for b, g in groups]
+    cat = {n: torch.cat([p[n] for p in parts], dim=1) for n in ("q", "k", "v", "grad_out")}
+    cat["cos_weight"], cat["sin_weight"] = inp["cos_weight"], inp["sin_weight"]
+    return cat
+
+
+def groups_rows(w, results, groups):
+    parts = [H.group_rows(w, results, b, g) for b, g in groups]
+    return tuple(torch.cat([p[i] for p in parts], dim=1) for i in range(4))
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full(name):
+    w = gen.WORKLOADS[name]
+    inp = gen.make_inputs(w)
+    got = H.run_gpu(w, H.to_dev(inp))
+    ref = H.run_oracle(w, inp)
+    H.compare(w, got, ref)
+
+
+@pytest.mark.parametrize("name", sorted(LARGE))
+def test_workload_groups(name):
+    w = gen.WORKLOADS[name]
+    inp = gen.make_inputs(w)
+    got = H.run_gpu(w, H.to_dev(inp))
+    groups = LARGE[name]
+    ref = H.run_oracle(w, groups_slice(inp, w, groups))
+    H.compare(w, groups_rows(w, got, groups), ref, label=f"groups {groups}")
+
+
+EDGE = [
+    # B, Hq, Hkv, N, D, dtype, causal, phi, weights
+    (1, 1, 1, 1, 32, "f32", True, "elu+1", False),
+    (1, 1, 1, 1, 64, "bf16", False, "relu", False),
+    (1, 2, 2, 2, 64, "bf16", False, "relu", False),
+    (2, 2, 1, 17, 128, "f32", True, "relu", True),
+    (1, 2, 1, 63, 64, "bf16", True, "elu+1", False),
+    (1, 4, 1, 65, 128, "bf16", True, "elu+1", False),
+    (1, 8, 1, 1000, 32, "bf16", False, "elu+1", True),
+    (1, 4, 1, 1000, 128, "f32", True, "elu+1", False),
+    (2, 4, 1, 5000, 64, "bf16", True, "elu+1", False),
+    (1, 2, 2, 129, 128, "bf16", True, "relu", True),
+    (1, 16, 2, 300, 64, "bf16", True, "elu+1", False),
+    (1, 3, 3, 200, 32, "f32", False, "elu+1", True),
+]
+
+
+def edge_workload(case):
+    B, Hq, Hkv, N, D, dt, causal, phi, weights = case
+    return gen.Workload(f"edge_b{B}_hq{Hq}_hkv{Hkv}_n{N}_d{D}_{dt}", B, Hq, Hkv, N, D, dt, causal,
+                        phi, weights=weights)
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "x".join(map(str, c)))
+def test_edge_shapes(case):
+    w = edge_workload(case)
+    inp = gen.make_inputs(w, seed=11)
+    got = H.run_gpu(w, H.to_dev(inp))
+    H.compare(w, got, H.run_oracle(w, inp))
+
+
+def test_dead_relu_rows():
+    w = gen.Workload("dead_rows", 1, 2, 1, 96, 64, "bf16", True, "relu")
+    inp = gen.make_inputs(w, seed=3)
+    inp["q"][:, :, 10:20] = -inp["q"][:, :, 10:20].abs() - 0.5   # phi(q_i) = 0 on rows 10..19
+    got = H.run_gpu(w, H.to_dev(inp))
+    H.compare(w, got, H.run_oracle(w, inp))
+    out, dq = got[0].cpu(), got[1].cpu()
+    assert torch.all(out[:, :, 10:20] == 0) and torch.all(dq[:, :, 10:20] == 0)
+
+
+def test_deterministic():
+    w = gen.WORKLOADS["causal_b4_h16_n4096_d64_bf16"].with_(B=1)
+    dev = H.to_dev(gen.make_inputs(w, seed=5))
+    a = H.run_gpu(w, dev)
+    b = H.run_gpu(w, dev)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_no_writes_outside_outputs(dtype):
+    """Guard bands around every output buffer stay untouched."""
+    w = gen.Workload("guard", 1, 4, 2, 77, 64, dtype, True, "elu+1", weights=True)
+    dev = H.to_dev(gen.make_inputs(w, seed=9))
+    pad = 4096
+    canary = 1234.5
+
+    def guarded(like):
+        buf = torch.full((like.numel() + 2 * pad,), canary, dtype=like.dtype, device="cuda")
+        return buf, buf[pad:pad + like.numel()].view(like.shape)
+
+    ob, out = guarded(dev["q"])
+    qb, dq = guarded(dev["q"])
+    kb, dk = guarded(dev["k"])
+    vb, dv = guarded(dev["v"])
+    la.fwd(dev["q"], dev["k"], dev["v"], True, "elu+1", 1e-6, dev["cos_weight"], dev["sin_weight"], out=out)
+    la.bwd(dev["q"], dev["k"], dev["v"], dev["grad_out"], True, "elu+1", 1e-6, dev["cos_weight"],
+           dev["sin_weight"], dq=dq, dk=dk, dv=dv)
+    la.get_status()
+    for buf in (ob, qb, kb, vb):
+        assert torch.all(buf[:pad] == canary) and torch.all(buf[-pad:] == canary)
+    ref = H.run_oracle(w, {n: (t.cpu() if t is not None else None) for n, t in dev.items()})
+    H.compare(w, (out, dq, dk, dv), ref)
+
+
+def test_status_clean_after_runs():
+    la.get_status()
+
+
+def test_binding_errors_are_raised():
+    q = torch.zeros(1, 3, 8, 64, device="cuda", dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 8, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(la.LinearAttentionError):
+        la.fwd(q, k, k)          # 3 query heads over 2 key/value heads
+    q = torch.zeros(1, 2, 8, 48, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(la.LinearAttentionError):
+        la.fwd(q, q, q)          # unsupported head dimension
