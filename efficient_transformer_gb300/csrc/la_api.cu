@@ -240,6 +240,8 @@ const char *la_status_str(la_status status) {
         case LA_ERR_CUDA: return "CUDA error";
         case LA_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
         case LA_ERR_WORKSPACE: return "workspace missing or too small";
+        case LA_ERR_STATIC_WS_LIMIT:
+            return "problem needs more scratch than the static workspace holds (LA_STATIC_WS_BYTES)";
     }
     return "unknown status";
 }
@@ -297,3 +299,52 @@ la_status la_trace_kernel(int index, const char **name, int *launches, double *t
 }
 
 }  // extern "C"
+
+// ---- forward without a caller workspace ------------------------------------------------
+//
+// For callers that cannot allocate device memory (plugin hosts that only pass input and
+// output buffers; loops that must not call cudaMalloc/cudaFree, which can synchronise the
+// device).  The scratch is this file-scope static device array.  In host code its name is
+// only a host-side stand-in, so the device address is looked up with
+// cudaGetSymbolAddress, once per device with that device current, and passed on.
+
+static __device__ __align__(256) unsigned char g_static_ws[LA_STATIC_WS_BYTES];
+
+namespace {
+
+cudaError_t static_ws_address(void **out) {
+    static std::mutex mu;
+    static void *cache[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_ws);
+        if (e != cudaSuccess) return e;
+        cache[dev] = ptr;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" la_status la_fwd_static_ws(const void *q, const void *k, const void *v, void *out,
+                                      int B, int Hq, int Hkv, int N, int D, la_dtype dtype,
+                                      int is_causal, la_phi phi, float eps,
+                                      const float *cos_weight, const float *sin_weight,
+                                      void *stream) {
+    la_status st = check_shape(B, Hq, Hkv, N, D, dtype, phi, eps, cos_weight, sin_weight);
+    if (st != LA_OK) return st;
+    const size_t need =
+        make_plan(B, Hq, Hkv, N, D, dtype, is_causal, cos_weight != nullptr, 0).ws_bytes;
+    if (need > LA_STATIC_WS_BYTES) return LA_ERR_STATIC_WS_LIMIT;
+    void *ws = nullptr;
+    cudaError_t e = static_ws_address(&ws);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, dtype,
+               is_causal, phi, eps, cos_weight, sin_weight, ws, LA_STATIC_WS_BYTES, stream);
+}

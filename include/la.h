@@ -126,6 +126,36 @@ la_status la_trace_stop(void);
 int la_trace_collect(void);
 la_status la_trace_kernel(int index, const char **name, int *launches, double *total_ms);
 
+/* Forward for callers that cannot allocate device memory.
+ *
+ * Some callers have no way to obtain scratch memory on the GPU: a plugin host that hands
+ * a kernel library only its input and output buffers, or a latency-critical loop that may
+ * not call cudaMalloc/cudaFree because those can synchronise the whole device.  This entry
+ * point computes exactly what la_fwd computes, with the same arguments minus the
+ * workspace: its scratch lives in LA_STATIC_WS_BYTES bytes of static device memory inside
+ * this library, which every GPU that loads the library holds until the process exits.
+ * It calls no allocator (no cudaMalloc, cudaFree or allocating library routine).  The
+ * pages have no counterpart of this entry point.
+ *
+ * - Sizes whose forward needs more scratch than LA_STATIC_WS_BYTES (see
+ *   la_workspace_size(..., is_bwd = 0)) are rejected with LA_ERR_STATIC_WS_LIMIT before
+ *   any CUDA call.
+ * - The first call on each device looks up the device address of the static scratch
+ *   (cudaGetSymbolAddress, with that device current); make that first call before any
+ *   stream capture.
+ * - All calls share the one scratch array, which keeps whatever the last call left in
+ *   it; the forward writes every scratch word before reading it, so nothing needs
+ *   clearing between calls.  Calls whose work can overlap on the GPU (different streams,
+ *   or different host threads) race on the scratch and must be serialised by the caller.
+ */
+#define LA_STATIC_WS_BYTES (64u * 1024u * 1024u)
+#define LA_ERR_STATIC_WS_LIMIT ((la_status)7)
+
+la_status la_fwd_static_ws(const void *q, const void *k, const void *v, void *out, int B,
+                           int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
+                           la_phi phi, float eps, const float *cos_weight,
+                           const float *sin_weight, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
