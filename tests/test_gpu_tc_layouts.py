@@ -1,0 +1,70 @@
+"""GPU check of the tensor-core building blocks (TMA 128-byte-swizzled tile loads,
+hand-swizzled tile writes, K-major and MN-major shared-memory descriptors, the instruction
+descriptor, tcgen05.mma into TMEM and tcgen05.ld back) against a float64 matmul of the same
+bf16 values.  Each case is one operand-layout combination that a library kernel uses."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SRC = os.path.join(HERE, "tc_probe.cu")
+LIB = os.path.join(HERE, "_build", "libtcprobe.so")
+
+
+@pytest.fixture(scope="module")
+def probe():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    os.makedirs(os.path.dirname(LIB), exist_ok=True)
+    hdr = os.path.join(ROOT, "efficient_transformer_gb300", "csrc", "la_tc_ptx.cuh")
+    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(SRC), os.path.getmtime(hdr)):
+        subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17",
+                        "-Xcompiler", "-fPIC", "-shared", "-I", os.path.dirname(hdr), SRC, "-o", LIB],
+                       check=True)
+    lib = ctypes.CDLL(LIB)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.tc_probe_mma.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
+    lib.tc_probe_mma.restype = i
+    return lib
+
+
+CASES = [
+    # N, K, a_mn, b_mn, a_manual, b_manual   (M = 128)
+    (32, 128, 0, 0, 0, 0),     # scores: phi(q) rows x phi(k) rows, 32 keys
+    (128, 128, 0, 0, 0, 0),    # scores, 128 keys
+    (64, 128, 0, 0, 0, 0),
+    (128, 32, 0, 1, 1, 0),     # P (hand-written, K = 32 keys) x V (MN-major)
+    (128, 128, 0, 1, 0, 0),    # phi(q) x state (MN-major)
+    (128, 32, 1, 1, 0, 0),     # phi(k)^T (MN-major A) x V: state update
+    (128, 64, 1, 1, 0, 0),
+    (32, 128, 1, 1, 0, 1),     # phi(q)^T x dP (hand-written MN-major B, 32 keys)
+    (32, 128, 1, 0, 0, 0),     # R^T (MN-major A) x phi(k) (K-major B)
+    (64, 64, 0, 1, 0, 0),      # head dimension 64
+    (128, 128, 0, 0, 1, 1),    # both hand-written
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "N{}_K{}_amn{}_bmn{}_am{}_bm{}".format(*c))
+def test_mma_layout(probe, case):
+    N, K, a_mn, b_mn, a_man, b_man = case
+    M = 128
+    g = torch.Generator().manual_seed(N * 1000 + K + 7 * a_mn + 13 * b_mn)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)    # logical A (m, k)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)    # logical B (n, k)
+    a_store = (A.t() if a_mn else A).contiguous().cuda()
+    b_store = (B.t() if b_mn else B).contiguous().cuda()
+    d = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.tc_probe_mma(a_store.data_ptr(), b_store.data_ptr(), d.data_ptr(), N, K, a_mn, b_mn,
+                            a_man, b_man, err.data_ptr())
+    assert rc == 0, f"probe returned {rc}"
+    want = A.double() @ B.double().t()
+    got = d.cpu().double()
+    assert torch.isfinite(got).all()
+    rel = float((got - want).abs().max() / want.abs().max())
+    assert rel < 1e-5, f"max rel err {rel:.3e}"
