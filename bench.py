@@ -88,7 +88,7 @@ def kernel_work(name: str, w: gen.Workload):
     intra = (2 * 16 * P * D + 2 * 16 * (D + 1)) if w.causal else 0
     table = {
         "simt_seg_state": ("alu", kv_rows * st),
-        "simt_scan": ("hbm", None),
+        "scan": ("hbm", None),
         "simt_fwd": ("alu", q_rows * (st + intra) + (kv_rows * st if w.causal else 0)),
         "simt_bwd_dq": ("alu", q_rows * (2 * st + 2 * intra) + (kv_rows * st if w.causal else 0)),
         "simt_seg_rstate": ("alu", q_rows * st),

@@ -75,10 +75,16 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
     Plan pl{};
     pl.P = has_w ? 2 : 1;
     pl.path = tc_supported(Hq, Hkv, N, D, dt, pl.P, causal, is_bwd) ? LA_PATH_TCGEN05 : LA_PATH_SIMT;
-    pl.chunk = 16;
     const int bg = B * Hkv;
+    int want;
+    if (pl.path == LA_PATH_TCGEN05) {
+        pl.chunk = tc_chunk(Hq / Hkv);
+        want = (kPlanSms + bg - 1) / bg;            // one CTA per SM (shared memory bound)
+    } else {
+        pl.chunk = 16;
+        want = (2 * kPlanSms + bg - 1) / bg;        // about two CTAs per SM in total
+    }
     const int nchunks = (N + pl.chunk - 1) / pl.chunk;
-    int want = (2 * kPlanSms + bg - 1) / bg;        // about two CTAs per SM in total
     if (want > nchunks) want = nchunks;
     if (want < 1) want = 1;
     const int chunks_per_seg = (nchunks + want - 1) / want;

@@ -94,10 +94,15 @@ class TraceScope {
 
 // --- launchers (defined in the kernel translation units) --------------------------------
 
+// Scan of per-segment states along the sequence (fixed order, per (batch, kv head)).
+enum ScanMode { kScanPrefix = 0, kScanSuffix = 1, kScanTotal = 2 };
+cudaError_t scan_segments(float *X, const Params &p, int mode, size_t elems, cudaStream_t s);
+
 cudaError_t simt_forward(const Params &p, la_dtype dt, cudaStream_t s);
 cudaError_t simt_backward(const Params &p, la_dtype dt, cudaStream_t s);
 cudaError_t tc_forward(const Params &p, cudaStream_t s);
 cudaError_t tc_backward(const Params &p, cudaStream_t s);
 bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal, int is_bwd);
+int tc_chunk(int n_rep);   // tokens per chunk of the tensor-core kernels
 
 }  // namespace la

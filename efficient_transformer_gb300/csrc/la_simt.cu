@@ -26,8 +26,6 @@ namespace {
 constexpr int kC = 16;          // tokens per chunk
 constexpr int kThreads = 256;   // 16 x 16 threads
 
-enum ScanMode { kScanPrefix = 0, kScanSuffix = 1, kScanTotal = 2 };
-
 // Segment of this CTA.
 struct Seg {
     int bg, b, g, s, t0, t1;
@@ -496,19 +494,14 @@ cudaError_t launch(const char *name, K kernel, size_t smem, int grid, const Para
     return cudaGetLastError();
 }
 
-cudaError_t scan(float *X, const Params &p, int mode, size_t elems, cudaStream_t s) {
-    dim3 grid((unsigned)((elems + 255) / 256), (unsigned)(p.B * p.Hkv));
-    TraceScope ts("simt_scan", s);
-    k_scan<<<grid, 256, 0, s>>>(X, p.nseg, elems, mode);
-    return cudaGetLastError();
-}
+
 
 template <typename T, int D, int P>
 cudaError_t forward_impl(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
     const size_t elems = (size_t)P * D * (D + 1);
     cudaError_t e = launch("simt_seg_state", k_seg_state<T, D, P>, smem_state<D, P>() + (P + 1) * smem_row<D>(), grid, p, s);
-    if (e == cudaSuccess) e = scan(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
+    if (e == cudaSuccess) e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
     if (e == cudaSuccess)
         e = launch("simt_fwd", k_fwd<T, D, P>, smem_state<D, P>() + (2 * P + 1) * smem_row<D>() + smem_tile(), grid, p, s);
     return e;
@@ -519,12 +512,12 @@ cudaError_t backward_impl(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
     const size_t elems = (size_t)P * D * (D + 1);
     cudaError_t e = launch("simt_seg_state", k_seg_state<T, D, P>, smem_state<D, P>() + (P + 1) * smem_row<D>(), grid, p, s);
-    if (e == cudaSuccess) e = scan(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
+    if (e == cudaSuccess) e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
     if (e == cudaSuccess)
         e = launch("simt_bwd_dq", k_bwd_dq<T, D, P>, smem_state<D, P>() + (2 * P + 3) * smem_row<D>() + 2 * smem_tile(), grid, p, s);
     if (e == cudaSuccess)
         e = launch("simt_seg_rstate", k_seg_rstate<T, D, P>, smem_state<D, P>() + (P + 1) * smem_row<D>(), grid, p, s);
-    if (e == cudaSuccess) e = scan(p.rstate, p, p.causal ? kScanSuffix : kScanTotal, elems, s);
+    if (e == cudaSuccess) e = scan_segments(p.rstate, p, p.causal ? kScanSuffix : kScanTotal, elems, s);
     if (e == cudaSuccess)
         e = launch("simt_bwd_dkdv", k_bwd_dkdv<T, D, P>, smem_state<D, P>() + (2 * P + 3) * smem_row<D>() + 2 * smem_tile(), grid, p, s);
     return e;
@@ -546,6 +539,13 @@ cudaError_t dispatch_p(const Params &p, cudaStream_t s, bool bwd) {
 }
 
 }  // namespace
+
+cudaError_t scan_segments(float *X, const Params &p, int mode, size_t elems, cudaStream_t s) {
+    dim3 grid((unsigned)((elems + 255) / 256), (unsigned)(p.B * p.Hkv));
+    TraceScope ts("scan", s);
+    k_scan<<<grid, 256, 0, s>>>(X, p.nseg, elems, mode);
+    return cudaGetLastError();
+}
 
 cudaError_t simt_forward(const Params &p, la_dtype dt, cudaStream_t s) {
     return dt == LA_F32 ? dispatch_p<float>(p, s, false) : dispatch_p<__nv_bfloat16>(p, s, false);

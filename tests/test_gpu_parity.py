@@ -157,3 +157,16 @@ def test_binding_errors_are_raised():
     q = torch.zeros(1, 2, 8, 48, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(la.LinearAttentionError):
         la.fwd(q, q, q)          # unsupported head dimension
+
+
+@pytest.mark.parametrize("name,fwd_path", [
+    ("causal_b1_h2_n256_d32_f32", la.LA_PATH_SIMT),
+    ("bidir_b2_h8_n2048_d64_bf16_elu1", la.LA_PATH_TCGEN05),
+    ("causal_b4_h16_n4096_d64_bf16", la.LA_PATH_TCGEN05),
+    ("cosformer_causal_b2_h16_n8192_d128_bf16", la.LA_PATH_SIMT),
+    ("gqa_causal_b1_hq32_hkv8_n65536_d128_bf16", la.LA_PATH_TCGEN05),
+])
+def test_kernel_family(name, fwd_path):
+    """The bf16 workloads without position weights run the tcgen05 forward."""
+    w = gen.WORKLOADS[name]
+    assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, False) == fwd_path
