@@ -93,6 +93,14 @@ def kernel_work(name: str, w: gen.Workload):
         "simt_bwd_dq": ("alu", q_rows * (2 * st + 2 * intra) + (kv_rows * st if w.causal else 0)),
         "simt_seg_rstate": ("alu", q_rows * st),
         "simt_bwd_dkdv": ("alu", kv_rows * 2 * st + ((q_rows * (2 * intra + st)) if w.causal else 0)),
+        # tensor-core kernels stream tensors: bytes each must move once
+        "tc_seg_state": ("hbm", 2 * kvb),                        # k, v
+        "tc_fwd_causal": ("hbm", 2 * qb + 2 * kvb),              # q, k, v -> out
+        "tc_fwd_bidir": ("hbm", 2 * qb),                         # q -> out
+        "tc_bwd_dq_causal": ("hbm", 3 * qb + 2 * kvb),           # q, g, k, v -> dq
+        "tc_bwd_dq_bidir": ("hbm", 3 * qb),                      # q, g -> dq
+        "tc_bwd_dkdv_causal": ("hbm", 2 * qb + 4 * kvb),         # q, g, k, v -> dk, dv
+        "tc_bwd_dkdv_bidir": ("hbm", 4 * kvb),                   # k, v -> dk, dv
     }
     bound, units = table.get(name, ("hbm", None))
     return bound, units, ("TFLOP/s" if bound == "alu" else "GB/s")

@@ -20,18 +20,10 @@
 // Warp roles (512 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
 // warps 4-7 phi prologue (in place on the swizzled tiles), warps 8-11 P conversion and
 // epilogue, warps 12-15 state conversion.
-#include <cstdlib>
-#include <cudaTypedefs.h>
-
-#include "la_internal.cuh"
-#include "la_tc_ptx.cuh"
+#include "la_tc_common.cuh"
 
 namespace la {
 namespace {
-
-using namespace tc;
-
-constexpr int kSmemLimit = 227 * 1024;
 
 template <int D, int G>
 struct FwdCfg {
@@ -58,78 +50,6 @@ struct StateCfg {
     static constexpr int NS = (kSmemLimit - 1024) / STAGE > 6 ? 6 : (kSmemLimit - 1024) / STAGE;
     static constexpr int SMEM = NS * STAGE + 1024;
 };
-
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
-}
-
-// Time-bounded wait that ignores the abort flag (used to drain in-flight copies).
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kWaitNs) return;
-}
-
-// Warp-uniform bounded wait.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    const bool ok = (*abort == 0) && mbar_wait(bar, parity, abort);
-    return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ float feat(float x, int phi) {
-    return phi == LA_PHI_ELU1 ? (x > 0.f ? x + 1.f : __expf(x)) : fmaxf(x, 0.f);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
-    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&u);
-    return __bfloat1622float2(h);
-}
-
-// Self-check build (compile with -DLA_DEBUG): every shared-memory, TMEM and global access
-// of these kernels and every TMA / MMA operand range is checked first; the first failing
-// check is recorded in g_la_debug (check id, two values, block) and the access is skipped.
-#ifdef LA_DEBUG
-__device__ int g_la_debug[4];
-__device__ __noinline__ bool dbg_fail(int id, long long a, long long b) {
-    if (atomicCAS(&g_la_debug[0], 0, id) == 0) {
-        g_la_debug[1] = (int)a;
-        g_la_debug[2] = (int)b;
-        g_la_debug[3] = (int)blockIdx.x;
-    }
-    return false;
-}
-#define LA_CHECK(cond, id, a, b) ((cond) ? true : dbg_fail((id), (long long)(a), (long long)(b)))
-#else
-#define LA_CHECK(cond, id, a, b) true
-#endif
-
-// Shared-memory range [p, p + bytes) lies inside [lo, hi).
-[[maybe_unused]] __device__ __forceinline__ bool in_smem(const void *p, uint32_t bytes, uint32_t lo, uint32_t hi) {
-    const uint32_t a = smem_u32(p);
-    return a >= lo && a + bytes <= hi;
-}
-
-// phi applied to 8 bf16 values in place (or zeros for a row past the end).
-__device__ __forceinline__ void feat8_inplace(uint8_t *chunk, bool valid, int phi) {
-    uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
-    uint4 x = *ptr, y;
-    if (valid) {
-        uint32_t *xi = reinterpret_cast<uint32_t *>(&x), *yi = reinterpret_cast<uint32_t *>(&y);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = unpack_bf16x2(xi[i]);
-            yi[i] = pack_bf16x2(feat(f.x, phi), feat(f.y, phi));
-        }
-    } else {
-        y = make_uint4(0u, 0u, 0u, 0u);
-    }
-    *ptr = y;
-}
 
 // ---------------------------------------------------------------------------------------
 // Per-segment state: S = sum_j phi(k_j) v_j^T (MMA, fp32 in TMEM), z = sum_j phi(k_j)
@@ -616,39 +536,6 @@ __global__ void __launch_bounds__(512, 1) k_tc_fwd(const __grid_constant__ CUten
 // ---------------------------------------------------------------------------------------
 // Host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// 3-D map over a contiguous bf16 tensor [heads][N][D]: box {64, rows, 1}, 128-byte swizzle;
-// rows past N read as zeros.
-cudaError_t make_map(CUtensorMap *map, const void *ptr, int heads, int N, int D, int rows) {
-    auto fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-template <typename Kern>
-cudaError_t prepare(Kern kernel, int smem) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-}
-
 template <int D>
 cudaError_t launch_state(const Params &p, cudaStream_t s) {
     CUtensorMap mk{}, mv{};
@@ -711,8 +598,9 @@ int tc_chunk(int n_rep) { return 128 / n_rep; }
 bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal, int is_bwd) {
     (void)N;
     (void)causal;
-    if (dt != LA_BF16 || P != 1 || is_bwd) return false;
+    if (dt != LA_BF16 || P != 1) return false;
     const int n_rep = Hq / Hkv;
+    if (is_bwd) return tc_bwd_supported(n_rep, D);
     if (D == 128) return n_rep == 2 || n_rep == 4 || n_rep == 8;
     if (D == 64) return n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8;
     return false;
@@ -722,7 +610,9 @@ cudaError_t tc_forward(const Params &p, cudaStream_t s) {
     return p.D == 128 ? forward_d<128>(p, s) : (p.D == 64 ? forward_d<64>(p, s) : cudaErrorNotSupported);
 }
 
-cudaError_t tc_backward(const Params &, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t tc_launch_state(const Params &p, cudaStream_t s) {
+    return p.D == 128 ? launch_state<128>(p, s) : (p.D == 64 ? launch_state<64>(p, s) : cudaErrorNotSupported);
+}
 
 }  // namespace la
 
