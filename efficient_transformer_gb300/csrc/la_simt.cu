@@ -168,16 +168,26 @@ __global__ void k_scan(float *X, int nseg, size_t elems, int mode) {
     float *base = X + (size_t)blockIdx.y * nseg * elems + e;
     if (mode == kScanTotal) {
         float acc = 0.f;
+#pragma unroll 8
         for (int s = 0; s < nseg; ++s) acc += base[(size_t)s * elems];
         for (int s = 0; s < nseg; ++s) base[(size_t)s * elems] = acc;
         return;
     }
+    // batches of 8 segments: all loads of a batch are issued before its stores
     float acc = 0.f;
-    for (int k = 0; k < nseg; ++k) {
-        const int s = (mode == kScanPrefix) ? k : nseg - 1 - k;
-        const float t = base[(size_t)s * elems];
-        base[(size_t)s * elems] = acc;
-        acc += t;
+    for (int k0 = 0; k0 < nseg; k0 += 8) {
+        float t[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int k = k0 + u, s = (mode == kScanPrefix) ? k : nseg - 1 - k;
+            t[u] = k < nseg ? base[(size_t)s * elems] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int k = k0 + u, s = (mode == kScanPrefix) ? k : nseg - 1 - k;
+            if (k < nseg) base[(size_t)s * elems] = acc;
+            acc += t[u];
+        }
     }
 }
 

@@ -1,59 +1,109 @@
-// la_tc.cu -- tensor-core kernels (tcgen05 / TMEM / TMA) for bfloat16 inputs.
+// la_tc.cu -- tensor-core kernels (tcgen05 / TMEM / TMA) for bfloat16 inputs: forward.
 //
 // The dense contractions of the chunked linear attention ("chunked causal streaming" and
 // "bidirectional parallel reduction" in the linear_attn module docstring) run as
 // tcgen05.mma with bf16 operands in 128-byte-swizzled shared memory and fp32 accumulators
-// in TMEM; tiles arrive by TMA.  The query rows of one chunk are the n_rep heads of a
-// key/value group stacked on the MMA's M = 128 rows (G = n_rep heads x C = 128 / G
-// tokens), so one key/value tile serves the whole group (the gqa page's head sharing,
-// fused: no expanded k, v).
+// in TMEM; tiles arrive by TMA and the output leaves by TMA.  The query rows of one chunk
+// are the n_rep heads of a key/value group stacked on the MMA's M = 128 rows (G = n_rep
+// heads x C = 128 / G tokens), so one key/value tile serves the whole group (the gqa
+// page's head sharing, fused: no expanded k, v).
 //
-// Forward = k_tc_state (per-segment S = phi(K)^T V, z = colsum phi(K)) -> k_scan
-// (exclusive prefix, or total when bidirectional; CUDA cores) -> k_tc_fwd.  Per chunk of
-// k_tc_fwd (M = 128 query rows, C keys):
-//   MMA1  A   = phi(Q) phi(K)^T                 [128 x C]   (causal)
-//   conv  P   = bf16(A masked j <= i); den_intra = rowsum P  (CUDA cores)
-//   MMA2  O   = P V + phi(Q) S_bf                [128 x D]
-//   epi   out = O / (den_intra + phi(Q) . z + eps)           (CUDA cores, fp32)
-//   MMA3  S  += phi(K)^T V                       [D x D]     (causal)
-//   conv  S_bf = bf16(S) for the next chunk's readout; z += colsum phi(K) (fp32)
-// Warp roles (512 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
-// warps 4-7 phi prologue (in place on the swizzled tiles), warps 8-11 P conversion and
-// epilogue, warps 12-15 state conversion.
+// z and the denominator also run on the tensor cores, through N = 16 products against two
+// small constant K-major tiles: ONES (row 0 all ones) and Z (row 0 = z_bf16).
+//
+// Forward = k_tc_state (per-segment S = phi(K)^T V, z = phi(K)^T 1) -> k_scan (exclusive
+// prefix, or total when bidirectional; CUDA cores) -> k_tc_fwd.  Per chunk of k_tc_fwd
+// (M = 128 query rows, C keys):
+//   MMA1  A   = phi(Q) phi(K)^T                                [128 x C]   (causal)
+//   conv  P   = bf16(A masked j <= i)                                      (causal)
+//   MMA2  O   = phi(Q) S_bf + P V                              [128 x D]
+//         den = phi(Q) z_bf + P 1        (column D of O)       [128 x 16]
+//   epi   out = O / (den + eps)  -> staged in shared memory -> TMA store
+//   MMA3  S  += phi(K)^T V,  z += phi(K)^T 1                              (causal)
+//   conv  S_bf, z_bf = bf16(S, z) for the next chunk
+// Warp roles (640 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
+// warps 4-7 and 16-19 phi prologue (in place, bf16x2; even and odd chunks), warps 8-11
+// state and P conversion, warps 12-15 epilogue.  O is double-buffered in TMEM when it
+// fits, so the epilogue of a chunk overlaps the next chunk's MMAs.
 #include "la_tc_common.cuh"
 
 namespace la {
 namespace {
 
+__host__ __device__ constexpr int align32(int x) { return (x + 31) / 32 * 32; }
+
+constexpr int kFwdThreads = 640;
+
 template <int D, int G>
 struct FwdCfg {
     static constexpr int C = 128 / G;                  // tokens per chunk
     static constexpr int DB = D / 64;                  // 64-wide blocks per D-wide row
+    static constexpr int CB = (C + 63) / 64;           // 64-wide blocks per C-wide row
     static constexpr int Q_BYTES = 128 * D * 2;        // 128 query rows
     static constexpr int K_BYTES = C * D * 2;
     static constexpr int V_BYTES = C * D * 2;
     static constexpr int STAGE = Q_BYTES + K_BYTES + V_BYTES;
-    static constexpr int P_BYTES = ((C + 63) / 64) * 128 * 128;
-    static constexpr int S_BYTES = DB * D * 128;       // D rows (d) x D columns (e)
-    static constexpr int FIXED = 2 * P_BYTES + S_BYTES + 2 * D * 4 + 1024;
-    static constexpr int NS = (kSmemLimit - FIXED) / STAGE > 4 ? 4 : (kSmemLimit - FIXED) / STAGE;
+    static constexpr int P_BYTES = CB * 128 * 128;
+    static constexpr int S_BYTES = DB * D * 128;       // S_bf: D rows (d) x D columns (e)
+    static constexpr int Z_BYTES = DB * 16 * 128;      // z_bf: 16 rows x D columns, K-major
+    static constexpr int ONES_BYTES = CB * 16 * 128;   // ones: 16 rows x C columns, K-major
+    static constexpr int OUT_BYTES = 128 * 128;        // output staging: 128 rows x 64 columns
+    static constexpr int FIXED = P_BYTES + S_BYTES + Z_BYTES + ONES_BYTES + OUT_BYTES + 1024;
+    static constexpr int NS = (kSmemLimit - 1024 - FIXED) / STAGE > 4 ? 4 : (kSmemLimit - 1024 - FIXED) / STAGE;
     static constexpr int SMEM = NS * STAGE + FIXED;
     static_assert(NS >= 2, "not enough shared memory for two stages");
+    // TMEM columns: [S | z], O (+ den in column D) in one or two buffers, A
+    static constexpr int NW = D + 16;
+    static constexpr int T_S = 0;
+    static constexpr int T_O0 = align32(NW);
+    static constexpr bool O2 = 3 * align32(NW) + C <= 512;
+    static constexpr int T_O1 = O2 ? T_O0 + align32(NW) : T_O0;
+    static constexpr int T_A = T_O1 + align32(NW);
+    static_assert(T_A + C <= 512, "TMEM budget");
 };
 
 template <int D>
 struct StateCfg {
-    static constexpr int C = 128;
+    static constexpr int C = 64;
     static constexpr int DB = D / 64;
     static constexpr int K_BYTES = C * D * 2;
-    static constexpr int STAGE = 2 * K_BYTES;          // K then V
-    static constexpr int NS = (kSmemLimit - 1024) / STAGE > 6 ? 6 : (kSmemLimit - 1024) / STAGE;
-    static constexpr int SMEM = NS * STAGE + 1024;
+    static constexpr int STAGE = 2 * K_BYTES;                  // K, V
+    static constexpr int ONES_BYTES = 16 * 128;
+    static constexpr int NS = (kSmemLimit - 4096) / STAGE > 6 ? 6 : (kSmemLimit - 4096) / STAGE;
+    static constexpr int SMEM = NS * STAGE + ONES_BYTES + 1024;
 };
 
+// A 16-row K-major tile with `cols` columns: row 0 = 1 for columns < cols, zero elsewhere.
+__device__ __forceinline__ void fill_ones_tile(uint8_t *t, int cols) {
+    const int nblk = (cols + 63) / 64;
+    for (int idx = threadIdx.x; idx < nblk * 16 * 8; idx += blockDim.x) {
+        const int blk = idx / 128, rc = idx % 128, row = rc / 8, c = rc % 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row == 0) {
+            const int col0 = blk * 64 + c * 8;
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                w[q] = (col0 + 2 * q < cols ? 0x3F80u : 0u) | (col0 + 2 * q + 1 < cols ? 0x3F800000u : 0u);
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        *reinterpret_cast<uint4 *>(t + swz_chunk(16, row, blk * 8 + c)) = v;
+    }
+}
+
+// One 16-column slice of an S row (bf16) into the swizzled S_bf tile (D rows).
+template <int D>
+__device__ __forceinline__ void store_state_row(uint8_t *sbf, int d, const float *v, int c16) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+    *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 // ---------------------------------------------------------------------------------------
-// Per-segment state: S = sum_j phi(k_j) v_j^T (MMA, fp32 in TMEM), z = sum_j phi(k_j)
-// (CUDA cores, fp32), written to the workspace as [D][D+1] with z in column D.
+// Per-segment state: S = phi(K)^T V and z = phi(K)^T 1 over the segment's tokens (fp32 in
+// TMEM), written to the workspace as [D][D+1] (z in column D).
 template <int D>
 __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUtensorMap map_k,
                                                      const __grid_constant__ CUtensorMap map_v, Params p) {
@@ -64,6 +114,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
+    uint8_t *ones = stage0 + NS * K::STAGE;
     const uint32_t sm_lo = smem_u32(smem_raw), sm_hi = sm_lo + K::SMEM;
     (void)sm_lo;
     (void)sm_hi;
@@ -72,6 +123,8 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
     const int t0 = seg * p.seg_len, t1 = min(p.N, t0 + p.seg_len);
     const int nchunk = (t1 - t0 + C - 1) / C;
 
+    fill_ones_tile(ones, C);
+    fence_proxy_async();
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < NS; ++s) {
@@ -83,7 +136,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_base, 128);
+        tmem_alloc(&tmem_base, 256);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -93,24 +146,17 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
 
     if (warp == 0) {
         if (lane == 0) {
-            tma_prefetch(&map_k);
-            tma_prefetch(&map_v);
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 if (k >= NS && !mbar_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
+                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N, 101, smem_u32(st) - sm_lo, c0)) break;
                 mbar_arrive_expect_tx(&bar_full[s], K::STAGE);
                 for (int blk = 0; blk < K::DB; ++blk) {
-                    uint8_t *dk_ = st + blk * C * 128, *dv_ = st + K::K_BYTES + blk * C * 128;
-                    if (LA_CHECK(in_smem(dk_, C * 128, sm_lo, sm_hi) && (smem_u32(dk_) & 1023) == 0, 101,
-                                 smem_u32(dk_) - sm_lo, k) &&
-                        LA_CHECK(c0 < p.N && bg < p.B * p.Hkv, 102, c0, bg))
-                        tma_load_3d(dk_, &map_k, &bar_full[s], blk * 64, c0, bg);
-                    if (LA_CHECK(in_smem(dv_, C * 128, sm_lo, sm_hi) && (smem_u32(dv_) & 1023) == 0, 103,
-                                 smem_u32(dv_) - sm_lo, k))
-                        tma_load_3d(dv_, &map_v, &bar_full[s], blk * 64, c0, bg);
+                    tma_load_3d(st + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
+                    tma_load_3d(st + K::K_BYTES + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
                 }
                 issued = k + 1;
             }
@@ -119,99 +165,95 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(128, D, true, true);
+            constexpr uint32_t idZ = idesc_bf16(128, 16, true, false);
+            const uint32_t on = smem_u32(ones);
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
                 tc_fence_after();
                 const uint32_t ks_ = smem_u32(stage0 + s * K::STAGE), vs_ = ks_ + K::K_BYTES;
-                // A spans 2 blocks of C rows (M = 128), B spans DB blocks
-                if (LA_CHECK(ks_ >= sm_lo && ks_ + 2u * C * 128u <= sm_hi, 111, ks_ - sm_lo, k) &&
-                    LA_CHECK(vs_ + (uint32_t)K::DB * C * 128u <= sm_hi, 112, vs_ - sm_lo, k))
-                    for (int kk = 0; kk < C / 16; ++kk)
-                        mma_bf16(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs_, C, 0, kk), idS,
-                                 (k > 0 || kk > 0) ? 1u : 0u);
+                if (!LA_CHECK(ks_ >= sm_lo && ks_ + (uint32_t)K::STAGE <= sm_hi, 111, ks_ - sm_lo, k)) break;
+                for (int kk = 0; kk < C / 16; ++kk) {
+                    const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
+                    mma_bf16(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs_, C, 0, kk), idS, acc);
+                    mma_bf16(tS + D, desc_mnmajor(ks_, C, 0, kk), desc_kmajor(on, 16, 0, kk), idZ, acc);
+                }
                 mma_commit(&bar_empty[s]);
             }
             mma_commit(&bar_done);
             mbar_drain(&bar_done, 0);
         }
     } else if (warp >= 4) {
-        const int i = threadIdx.x - 128;           // 0..127: column d for z, lane of TMEM
-        float z = 0.f;
+        const int i = threadIdx.x - 128;
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
             ok = ok && warp_wait(&bar_full[s], (k / NS) & 1, &abort_flag);
-            uint8_t *kt = stage0 + s * K::STAGE;
-            const int c0 = t0 + k * C;
             if (ok) {
+                uint8_t *kt = stage0 + s * K::STAGE;
+                const int c0 = t0 + k * C;
+#pragma unroll 4
                 for (int idx = i; idx < C * (D / 8); idx += 128) {
                     const int j = idx / (D / 8), c = idx % (D / 8);
                     uint8_t *ch = kt + swz_chunk(C, j, c);
                     if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 121, smem_u32(ch) - sm_lo, idx))
-                        feat8_inplace(ch, c0 + j < t1, p.phi);
+                        feat8_inplace2(ch, c0 + j < t1, p.phi);
                 }
+                fence_proxy_async();
             }
-            named_barrier(1, 128);
-            if (ok && i < D)
-                for (int j = 0; j < C; ++j) {
-                    const uint8_t *e_ = kt + swz_offset(C, j, i);
-                    if (LA_CHECK(in_smem(e_, 2, sm_lo, sm_hi), 122, smem_u32(e_) - sm_lo, j))
-                        z += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(e_));
-                }
-            fence_proxy_async();
             mbar_arrive(&bar_ready[s]);
         }
         ok = ok && warp_wait(&bar_done, 0, &abort_flag);
         tc_fence_after();
-        float *dst = p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
         const int wq = warp % 4;
         if (ok && wq * 32 < D) {
             const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-            float *row = dst + (size_t)i * (D + 1);
-            const size_t row_idx = ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1)) + (size_t)i * (D + 1);
-            (void)row_idx;
-            const bool row_ok = LA_CHECK(row_idx + D + 1 <= (size_t)p.B * p.Hkv * p.nseg * D * (D + 1), 131,
-                                         row_idx, i);
-            for (int c16 = 0; c16 < D / 16; ++c16) {
+            float *row = p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1)) + (size_t)i * (D + 1);
+#pragma unroll 1
+            for (int c16 = 0; c16 <= D / 16; ++c16) {
                 float v[16];
-                if (LA_CHECK(c16 * 16 + 16 <= 128, 132, c16, i)) {
-                    tmem_ld16(tS + lane_off + c16 * 16, v);
-                    tmem_ld_wait();
-                }
+                tmem_ld16(tS + lane_off + c16 * 16, v);
+                tmem_ld_wait();
+                if (c16 < D / 16) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (row_ok) row[c16 * 16 + e] = nchunk > 0 ? v[e] : 0.f;
+                    for (int e = 0; e < 16; ++e) row[c16 * 16 + e] = v[e];
+                } else {
+                    row[D] = v[0];
+                }
             }
-            if (row_ok) row[D] = z;
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tS, 128);
+    if (warp == 1) tmem_dealloc(tS, 256);
     if (threadIdx.x == 0 && abort_flag) atomicExch(p.err, kErrTimeout);
 }
 
 // ---------------------------------------------------------------------------------------
 // Chunked forward (see the file comment for the per-chunk steps and warp roles).
 template <int D, int G, bool CAUSAL>
-__global__ void __launch_bounds__(512, 1) k_tc_fwd(const __grid_constant__ CUtensorMap map_q,
-                                                   const __grid_constant__ CUtensorMap map_k,
-                                                   const __grid_constant__ CUtensorMap map_v, Params p) {
+__global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant__ CUtensorMap map_q,
+                                                           const __grid_constant__ CUtensorMap map_k,
+                                                           const __grid_constant__ CUtensorMap map_v,
+                                                           const __grid_constant__ CUtensorMap map_o, Params p) {
     using K = FwdCfg<D, G>;
     constexpr int C = K::C, NS = K::NS;
+    constexpr int OFF_K = K::Q_BYTES, OFF_V = OFF_K + K::K_BYTES;
+    constexpr int NO = K::O2 ? 2 : 1;   // O buffers
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_full[NS], bar_ready[NS], bar_empty[NS];
-    __shared__ uint64_t bar_afull, bar_pready, bar_ofull, bar_ofree, bar_sfull, bar_sbf, bar_fin;
+    __shared__ uint64_t bar_full[NS], bar_ready[NS], bar_empty[NS], bar_ofull[2], bar_ofree[2];
+    __shared__ uint64_t bar_afull, bar_pready, bar_sfull, bar_sbf, bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
     const uint32_t sm_lo = smem_u32(smem_raw), sm_hi = sm_lo + K::SMEM;
     (void)sm_lo;
     (void)sm_hi;
-    uint8_t *ptile = stage0 + NS * K::STAGE;
-    uint8_t *sbf = ptile + 2 * K::P_BYTES;
-    float *zf = reinterpret_cast<float *>(sbf + K::S_BYTES);   // [2][D]
+    uint8_t *pbuf = stage0 + NS * K::STAGE;
+    uint8_t *sbf = pbuf + K::P_BYTES;
+    uint8_t *ztile = sbf + K::S_BYTES;
+    uint8_t *ones = ztile + K::Z_BYTES;
+    uint8_t *obuf = ones + K::ONES_BYTES;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
@@ -220,22 +262,25 @@ __global__ void __launch_bounds__(512, 1) k_tc_fwd(const __grid_constant__ CUten
     const int nchunk = (t1 - t0 + C - 1) / C;
     const int bh0 = b * p.Hq + g * G;
     const float *state = p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
-    const size_t state_base = ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
-    const size_t state_total = (size_t)p.B * p.Hkv * p.nseg * D * (D + 1);
-    (void)state_base;
-    (void)state_total;
 
+    // constant tiles: ones (row 0 = 1 over C columns) and the zero rows of the z tile
+    fill_ones_tile(ones, C);
+    for (int idx = threadIdx.x; idx < K::Z_BYTES / 16; idx += blockDim.x)
+        reinterpret_cast<uint4 *>(ztile)[idx] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_ready[s], 128);
-            mbar_init(&bar_empty[s], 1 + 128);
+            mbar_init(&bar_empty[s], 1);
+        }
+        for (int o = 0; o < 2; ++o) {
+            mbar_init(&bar_ofull[o], 1);
+            mbar_init(&bar_ofree[o], 128);
         }
         mbar_init(&bar_afull, 1);
         mbar_init(&bar_pready, 128);
-        mbar_init(&bar_ofull, 1);
-        mbar_init(&bar_ofree, 128);
         mbar_init(&bar_sfull, 1);
         mbar_init(&bar_sbf, 128);
         mbar_init(&bar_fin, 1);
@@ -248,16 +293,12 @@ __global__ void __launch_bounds__(512, 1) k_tc_fwd(const __grid_constant__ CUten
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = tmem_base, tO = tmem_base + 128, tA = tmem_base + 256;
+    const uint32_t tS = tmem_base + K::T_S, tA = tmem_base + K::T_A;
+    const uint32_t tO0 = tmem_base + K::T_O0, tO1 = tmem_base + K::T_O1;
 
     if (warp == 0) {
         // ---------------- TMA producer
         if (lane == 0) {
-            tma_prefetch(&map_q);
-            if (CAUSAL) {
-                tma_prefetch(&map_k);
-                tma_prefetch(&map_v);
-            }
             constexpr uint32_t bytes = CAUSAL ? K::STAGE : K::Q_BYTES;
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
@@ -265,24 +306,18 @@ __global__ void __launch_bounds__(512, 1) k_tc_fwd(const __grid_constant__ CUten
                 if (k >= NS && !mbar_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
+                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N && bh0 + G <= p.B * p.Hq, 201,
+                              smem_u32(st) - sm_lo, c0))
+                    break;
+                LA_TL(k, 0);
                 mbar_arrive_expect_tx(&bar_full[s], bytes);
                 for (int r = 0; r < G; ++r)
-                    for (int blk = 0; blk < K::DB; ++blk) {
-                        uint8_t *dq_ = st + blk * 128 * 128 + r * C * 128;
-                        if (LA_CHECK(in_smem(dq_, C * 128, sm_lo, sm_hi) && (smem_u32(dq_) & 1023) == 0, 201,
-                                     smem_u32(dq_) - sm_lo, k) &&
-                            LA_CHECK(c0 < p.N && bh0 + r < p.B * p.Hq, 202, c0, bh0 + r))
-                            tma_load_3d(dq_, &map_q, &bar_full[s], blk * 64, c0, bh0 + r);
-                    }
+                    for (int blk = 0; blk < K::DB; ++blk)
+                        tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_full[s], blk * 64, c0, bh0 + r);
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk) {
-                        uint8_t *dk_ = st + K::Q_BYTES + blk * C * 128, *dv_ = dk_ + K::K_BYTES;
-                        if (LA_CHECK(in_smem(dk_, C * 128, sm_lo, sm_hi) && in_smem(dv_, C * 128, sm_lo, sm_hi) &&
-                                         (smem_u32(dk_) & 1023) == 0 && (smem_u32(dv_) & 1023) == 0,
-                                     203, smem_u32(dk_) - sm_lo, k)) {
-                            tma_load_3d(dk_, &map_k, &bar_full[s], blk * 64, c0, bg);
-                            tma_load_3d(dv_, &map_v, &bar_full[s], blk * 64, c0, bg);
-                        }
+                        tma_load_3d(st + OFF_K + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
+                        tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
                     }
                 issued = k + 1;
             }
@@ -293,54 +328,65 @@ __global__ void __launch_bounds__(512, 1) k_tc_fwd(const __grid_constant__ CUten
         if (lane == 0) {
             constexpr uint32_t idA = idesc_bf16(128, C, false, false);
             constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+            constexpr uint32_t idDen = idesc_bf16(128, 16, false, false);
             constexpr uint32_t idS = idesc_bf16(128, D, true, true);
-            const uint32_t sbf_u = smem_u32(sbf);
+            constexpr uint32_t idZ = idesc_bf16(128, 16, true, false);
+            const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf), zt = smem_u32(ztile), on = smem_u32(ones);
             for (int k = 0; k < nchunk; ++k) {
-                const int s = k % NS;
+                const int s = k % NS, o = k % NO;
+                const uint32_t tO = o ? tO1 : tO0;
                 if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
+                LA_TL(k, 3);
                 tc_fence_after();
-                const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + K::Q_BYTES, vs = ks_ + K::K_BYTES;
-                const uint32_t pb = smem_u32(ptile + (k & 1) * K::P_BYTES);
-                const bool ranges_ok =
-                    LA_CHECK(qs >= sm_lo && qs + K::Q_BYTES <= sm_hi, 211, qs - sm_lo, k) &&
-                    LA_CHECK(ks_ + 2u * C * 128u <= sm_hi, 212, ks_ - sm_lo, k) &&
-                    LA_CHECK(vs + K::V_BYTES <= sm_hi, 213, vs - sm_lo, k) &&
-                    LA_CHECK(pb + K::P_BYTES <= sm_hi, 214, pb - sm_lo, k) &&
-                    LA_CHECK(sbf_u + K::S_BYTES <= sm_hi, 215, sbf_u - sm_lo, k);
-                if (!ranges_ok) break;
+                const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V;
+                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && smem_u32(obuf) + K::OUT_BYTES <= sm_hi, 211,
+                              qs - sm_lo, k))
+                    break;
                 if (CAUSAL) {
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_bf16(tA, desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
                     mma_commit(&bar_afull);
                     if (!mbar_wait(&bar_pready, k & 1, &abort_flag)) break;
                 }
+                LA_TL(k, 4);
                 if ((CAUSAL || k == 0) && !mbar_wait(&bar_sbf, k & 1, &abort_flag)) break;
-                if (k > 0 && !mbar_wait(&bar_ofree, (k - 1) & 1, &abort_flag)) break;
+                LA_TL(k, 5);
+                if (k >= NO && !mbar_wait(&bar_ofree[o], ((k / NO) - 1) & 1, &abort_flag)) break;
+                LA_TL(k, 6);
                 tc_fence_after();
-                uint32_t acc = 0;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    mma_bf16(tO, desc_kmajor(qs, 128, 0, kk), desc_mnmajor(sbf_u, D, 0, kk), idO, kk > 0 ? 1u : 0u);
+                    mma_bf16(tO + D, desc_kmajor(qs, 128, 0, kk), desc_kmajor(zt, 16, 0, kk), idDen, kk > 0 ? 1u : 0u);
+                }
                 if (CAUSAL)
-                    for (int kk = 0; kk < C / 16; ++kk, acc = 1)
-                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(vs, C, 0, kk), idO, acc);
-                for (int kk = 0; kk < D / 16; ++kk, acc = 1)
-                    mma_bf16(tO, desc_kmajor(qs, 128, 0, kk), desc_mnmajor(sbf_u, D, 0, kk), idO, acc);
-                mma_commit(&bar_ofull);
+                    for (int kk = 0; kk < C / 16; ++kk) {
+                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(vs, C, 0, kk), idO, 1u);
+                        mma_bf16(tO + D, desc_kmajor(pb, 128, 0, kk), desc_kmajor(on, 16, 0, kk), idDen, 1u);
+                    }
+                mma_commit(&bar_ofull[o]);
                 if (CAUSAL) {
-                    for (int kk = 0; kk < C / 16; ++kk)
+                    for (int kk = 0; kk < C / 16; ++kk) {
                         mma_bf16(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs, C, 0, kk), idS, 1u);
+                        mma_bf16(tS + D, desc_mnmajor(ks_, C, 0, kk), desc_kmajor(on, 16, 0, kk), idZ, 1u);
+                    }
                     mma_commit(&bar_sfull);
                 }
                 mma_commit(&bar_empty[s]);
+                LA_TL(k, 7);
             }
             mma_commit(&bar_fin);
             mbar_drain(&bar_fin, 0);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- phi prologue, in place on the swizzled Q and K tiles
-        const int i = threadIdx.x - 128;
+    } else if ((warp >= 4 && warp < 8) || warp >= 16) {
+        // ---------------- phi prologue, in place on the swizzled Q and K tiles; two
+        // warpgroups take alternate chunks
+        const int pg = warp >= 16 ? 1 : 0;
+        const int i = threadIdx.x - (pg ? 512 : 128);
         bool ok = true;
-        for (int k = 0; k < nchunk; ++k) {
+        for (int k = pg; k < nchunk; k += 2) {
             const int s = k % NS;
             ok = ok && warp_wait(&bar_full[s], (k / NS) & 1, &abort_flag);
+            if (i == 0) LA_TL(k, 1);
             if (ok) {
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
@@ -349,150 +395,47 @@ __global__ void __launch_bounds__(512, 1) k_tc_fwd(const __grid_constant__ CUten
                 for (int c = 0; c < D / 8; ++c) {
                     uint8_t *ch = st + swz_chunk(128, i, c);
                     if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, c))
-                        feat8_inplace(ch, qvalid, p.phi);
+                        feat8_inplace2(ch, qvalid, p.phi);
                 }
                 if (CAUSAL)
+#pragma unroll 2
                     for (int idx = i; idx < C * (D / 8); idx += 128) {
                         const int j = idx / (D / 8), c = idx % (D / 8);
-                        uint8_t *ch = st + K::Q_BYTES + swz_chunk(C, j, c);
+                        uint8_t *ch = st + OFF_K + swz_chunk(C, j, c);
                         if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 222, smem_u32(ch) - sm_lo, idx))
-                            feat8_inplace(ch, c0 + j < t1, p.phi);
+                            feat8_inplace2(ch, c0 + j < t1, p.phi);
                     }
                 fence_proxy_async();
             }
+            if (i == 0) LA_TL(k, 2);
             mbar_arrive(&bar_ready[s]);
         }
     } else if (warp >= 8 && warp < 12) {
-        // ---------------- P conversion and epilogue (thread = query row of the chunk)
+        // ---------------- state conversion (thread = d) and P conversion (thread = row i)
         const int i = threadIdx.x - 256;
         const int wq = warp % 4;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const int r = i / C, ti = i % C;
-        const int bh = bh0 + r;
-        if (i < D && LA_CHECK(state_base + (size_t)i * (D + 1) + D < state_total, 231, i, 0) &&
-            LA_CHECK(in_smem(zf + i, 4, sm_lo, sm_hi), 232, i, 0))
-            zf[i] = state[(size_t)i * (D + 1) + D];
-        named_barrier(1, 128);
-        bool ok = true;
-        for (int k = 0; k < nchunk; ++k) {
-            const int s = k % NS;
-            const int c0 = t0 + k * C, t = c0 + ti;
-            uint8_t *st = stage0 + s * K::STAGE;
-            float den_intra = 0.f;
-            if (CAUSAL) {
-                ok = ok && warp_wait(&bar_afull, k & 1, &abort_flag);
-                tc_fence_after();
-                if (ok) {
-                    uint8_t *pb = ptile + (k & 1) * K::P_BYTES;
-#pragma unroll 1
-                    for (int c16 = 0; c16 < C / 16; ++c16) {
-                        float v[16];
-                        if (LA_CHECK(256 + c16 * 16 + 16 <= 512, 241, c16, i)) {
-                            tmem_ld16(tA + lane_off + c16 * 16, v);
-                            tmem_ld_wait();
-                        }
-                        uint32_t w[8];
-#pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            const int j = c16 * 16 + e;
-                            const float x0 = (j <= ti) ? v[e] : 0.f, x1 = (j + 1 <= ti) ? v[e + 1] : 0.f;
-                            w[e / 2] = pack_bf16x2(x0, x1);
-                            const float2 f = unpack_bf16x2(w[e / 2]);
-                            den_intra += f.x + f.y;
-                        }
-                        uint8_t *p0 = pb + swz_chunk(128, i, 2 * c16), *p1 = pb + swz_chunk(128, i, 2 * c16 + 1);
-                        if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 242,
-                                     smem_u32(p0) - sm_lo, c16)) {
-                            *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
-                            *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
-                        }
-                    }
-                    fence_proxy_async();
-                }
-                tc_fence_before();
-                mbar_arrive(&bar_pready);
-            }
-            ok = ok && warp_wait(&bar_ofull, k & 1, &abort_flag);
-            tc_fence_after();
-            if (ok) {
-                // den = rowsum P + phi(q_i) . z + eps, in fp32
-                const float *z = zf + (CAUSAL ? (k & 1) * D : 0);
-                float dint = 0.f;
-#pragma unroll 4
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint8_t *ch = st + swz_chunk(128, i, c);
-                    if (!LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi) && in_smem(z + c * 8, 32, sm_lo, sm_hi), 251,
-                                  smem_u32(ch) - sm_lo, c))
-                        continue;
-                    const uint4 x = *reinterpret_cast<const uint4 *>(ch);
-                    const uint32_t *xi = reinterpret_cast<const uint32_t *>(&x);
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float2 f = unpack_bf16x2(xi[h]);
-                        dint += f.x * z[c * 8 + 2 * h] + f.y * z[c * 8 + 2 * h + 1];
-                    }
-                }
-                const float inv = 1.f / (den_intra + dint + p.eps);
-                __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + ((size_t)bh * p.N + t) * D;
-#pragma unroll 1
-                for (int c16 = 0; c16 < D / 16; ++c16) {
-                    float v[16];
-                    if (LA_CHECK(128 + c16 * 16 + 16 <= 256, 252, c16, i)) {
-                        tmem_ld16(tO + lane_off + c16 * 16, v);
-                        tmem_ld_wait();
-                    }
-                    if (t < t1 && LA_CHECK(((size_t)bh * p.N + t) * D + c16 * 16 + 16 <= (size_t)p.B * p.Hq * p.N * D,
-                                           253, bh, t)) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e] * inv, v[2 * e + 1] * inv);
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c16 * 16);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    }
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&bar_ofree);
-            if (CAUSAL && ok && i < D) {   // z for the next chunk: z += colsum phi(K) (fp32)
-                const uint8_t *kt = st + K::Q_BYTES;
-                float zs = zf[(k & 1) * D + i];
-                for (int j = 0; j < C; ++j) {
-                    const uint8_t *e_ = kt + swz_offset(C, j, i);
-                    if (LA_CHECK(in_smem(e_, 2, sm_lo, sm_hi), 261, smem_u32(e_) - sm_lo, j))
-                        zs += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(e_));
-                }
-                if (LA_CHECK(in_smem(zf + ((k + 1) & 1) * D + i, 4, sm_lo, sm_hi), 262, i, k))
-                    zf[((k + 1) & 1) * D + i] = zs;
-            }
-            mbar_arrive(&bar_empty[s]);
-            named_barrier(1, 128);
-        }
-    } else if (warp >= 12) {
-        // ---------------- state conversion: TMEM S (fp32) -> S_bf (bf16 operand tile)
-        const int d = threadIdx.x - 384;
-        const int wq = warp % 4;
-        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const int ti = i % C;
+        // initial S, z of the segment: TMEM (causal) and the bf16 operand tiles
         if (wq * 32 < D) {
-            const float *row = state + (size_t)d * (D + 1);
-            const bool row_ok = LA_CHECK(state_base + (size_t)d * (D + 1) + D + 1 <= state_total, 271, d, 0);
+            const float *row = state + (size_t)i * (D + 1);
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 float v[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = row_ok ? row[c16 * 16 + e] : 0.f;
-                if (CAUSAL && LA_CHECK(c16 * 16 + 16 <= 128, 272, c16, d)) tmem_st16(tS + lane_off + c16 * 16, v);
-                uint32_t w[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-                uint8_t *p0 = sbf + swz_chunk(D, d, 2 * c16), *p1 = sbf + swz_chunk(D, d, 2 * c16 + 1);
-                if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 273,
-                             smem_u32(p0) - sm_lo, d)) {
-                    *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
-                }
+                for (int e = 0; e < 16; ++e) v[e] = row[c16 * 16 + e];
+                if (CAUSAL) tmem_st16(tS + lane_off + c16 * 16, v);
+                store_state_row<D>(sbf, i, v, c16);
             }
-            if (CAUSAL) tmem_st_wait();
+            float zv[16];
+            zv[0] = row[D];
+#pragma unroll
+            for (int e = 1; e < 16; ++e) zv[e] = 0.f;
+            if (CAUSAL) {
+                tmem_st16(tS + lane_off + D, zv);
+                tmem_st_wait();
+            }
+            *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zv[0]);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -500,32 +443,117 @@ __global__ void __launch_bounds__(512, 1) k_tc_fwd(const __grid_constant__ CUten
         if (CAUSAL) {
             bool ok = true;
             for (int k = 0; k < nchunk; ++k) {
-                ok = ok && warp_wait(&bar_sfull, k & 1, &abort_flag);
+                // P for chunk k
+                ok = ok && warp_wait(&bar_afull, k & 1, &abort_flag);
                 tc_fence_after();
-                if (ok && wq * 32 < D) {
-#pragma unroll 1
-                    for (int c16 = 0; c16 < D / 16; ++c16) {
-                        float v[16];
-                        if (LA_CHECK(c16 * 16 + 16 <= 128, 281, c16, d)) {
-                            tmem_ld16(tS + lane_off + c16 * 16, v);
-                            tmem_ld_wait();
-                        }
-                        uint32_t w[8];
+                if (i == 0) LA_TL(k, 8);
+                if (ok) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-                        uint8_t *p0 = sbf + swz_chunk(D, d, 2 * c16), *p1 = sbf + swz_chunk(D, d, 2 * c16 + 1);
-                        if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 282,
-                                     smem_u32(p0) - sm_lo, d)) {
-                            *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
-                            *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int c32 = 0; c32 < (C + 31) / 32; ++c32) {
+                        float v[32];
+                        if (C >= 32) {
+                            tmem_ld32(tA + lane_off + c32 * 32, v);
+                        } else {
+                            tmem_ld16(tA + lane_off, v);
+                        }
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int h = 0; h < (C >= 32 ? 2 : 1); ++h) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                const int j = c32 * 32 + h * 16 + e;
+                                w[e / 2] = pack_bf16x2((j <= ti) ? v[h * 16 + e] : 0.f,
+                                                       (j + 1 <= ti) ? v[h * 16 + e + 1] : 0.f);
+                            }
+                            const int c16 = c32 * 2 + h;
+                            uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
+                            if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 241,
+                                         smem_u32(p0) - sm_lo, c16)) {
+                                *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
+                                *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
+                            }
                         }
                     }
+                    fence_proxy_async();
+                }
+                tc_fence_before();
+                if (i == 0) LA_TL(k, 9);
+                mbar_arrive(&bar_pready);
+                // S, z after chunk k -> operand tiles for chunk k + 1
+                ok = ok && warp_wait(&bar_sfull, k & 1, &abort_flag);
+                tc_fence_after();
+                if (i == 0) LA_TL(k, 10);
+                if (ok && wq * 32 < D) {
+#pragma unroll
+                    for (int c64 = 0; c64 < D / 64; ++c64) {
+                        float v[64];
+                        tmem_ld32(tS + lane_off + c64 * 64, v);
+                        tmem_ld32(tS + lane_off + c64 * 64 + 32, v + 32);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) store_state_row<D>(sbf, i, v + 16 * h, c64 * 4 + h);
+                    }
+                    const float zd = tmem_ld1(tS + lane_off + D);
+                    tmem_ld_wait();
+                    *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zd);
                 }
                 fence_proxy_async();
                 tc_fence_before();
+                if (i == 0) LA_TL(k, 11);
                 mbar_arrive(&bar_sbf);
             }
         }
+    } else if (warp >= 12 && warp < 16) {
+        // ---------------- epilogue (thread = query row of the chunk): out = O / (den + eps),
+        // staged in shared memory 64 columns at a time and written by TMA
+        const int i = threadIdx.x - 384;
+        const int wq = warp % 4;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        bool ok = true;
+        for (int k = 0; k < nchunk; ++k) {
+            const int o = k % NO;
+            const uint32_t tO = o ? tO1 : tO0;
+            const int c0 = t0 + k * C;
+            ok = ok && warp_wait(&bar_ofull[o], (k / NO) & 1, &abort_flag);
+            tc_fence_after();
+            if (i == 0) LA_TL(k, 12);
+            float den = 0.f;
+            if (ok) den = tmem_ld1(tO + lane_off + D);
+#pragma unroll
+            for (int c64 = 0; c64 < D / 64; ++c64) {
+                float v[64];
+                if (ok) {
+                    tmem_ld32(tO + lane_off + c64 * 64, v);
+                    tmem_ld32(tO + lane_off + c64 * 64 + 32, v + 32);
+                    tmem_ld_wait();
+                }
+                if (i == 0) bulk_wait_read();   // previous stores have read the staging tile
+                named_barrier(2, 128);
+                if (ok) {
+                    const float inv = 1.f / (den + p.eps);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        uint4 w;
+                        w.x = pack_bf16x2(v[8 * q + 0] * inv, v[8 * q + 1] * inv);
+                        w.y = pack_bf16x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv);
+                        w.z = pack_bf16x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv);
+                        w.w = pack_bf16x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv);
+                        *reinterpret_cast<uint4 *>(obuf + swz_chunk(128, i, q)) = w;
+                    }
+                }
+                fence_proxy_async();
+                named_barrier(2, 128);
+                if (i == 0 && ok) {
+                    for (int r = 0; r < G; ++r) tma_store_3d(&map_o, obuf + r * C * 128, c64 * 64, c0, bh0 + r);
+                    bulk_commit();
+                }
+            }
+            tc_fence_before();
+            if (i == 0) LA_TL(k, 13);
+            mbar_arrive(&bar_ofree[o]);
+        }
+        if (i == 0) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -551,14 +579,15 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
 template <int D, int G, bool CAUSAL>
 cudaError_t launch_fwd(const Params &p, cudaStream_t s) {
     using K = FwdCfg<D, G>;
-    CUtensorMap mq{}, mk{}, mv{};
+    CUtensorMap mq{}, mk{}, mv{}, mo{};
     cudaError_t e = make_map(&mq, p.q, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, K::C);
+    if (e == cudaSuccess) e = make_map(&mo, p.out, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = prepare(k_tc_fwd<D, G, CAUSAL>, K::SMEM);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_fwd_causal" : "tc_fwd_bidir", s);
-    k_tc_fwd<D, G, CAUSAL><<<p.B * p.Hkv * p.nseg, 512, K::SMEM, s>>>(mq, mk, mv, p);
+    k_tc_fwd<D, G, CAUSAL><<<p.B * p.Hkv * p.nseg, kFwdThreads, K::SMEM, s>>>(mq, mk, mv, mo, p);
     return cudaGetLastError();
 }
 
@@ -615,6 +644,13 @@ cudaError_t tc_launch_state(const Params &p, cudaStream_t s) {
 }
 
 }  // namespace la
+
+#ifdef LA_TIMELINE
+// Timeline builds only: copy out the forward kernel's event clocks ([64][16] long long).
+extern "C" int la_timeline_read(long long *out) {
+    return cudaMemcpyFromSymbol(out, la::g_la_tl, sizeof(long long) * 64 * 16) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 #ifdef LA_DEBUG
 // Debug builds only: copy out and clear the first failed self-check (id, a, b, block).

@@ -219,14 +219,14 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
                 for (int c = 0; c < D / 8; ++c) {
                     uint8_t *ch = st + swz_chunk(128, i, c);
                     if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 321, smem_u32(ch) - sm_lo, c))
-                        feat8_inplace(ch, qvalid, p.phi);
+                        feat8_inplace2(ch, qvalid, p.phi);
                 }
                 if (CAUSAL)
                     for (int idx = i; idx < C * (D / 8); idx += 128) {
                         const int j = idx / (D / 8), c = idx % (D / 8);
                         uint8_t *ch = st + OFF_K + swz_chunk(C, j, c);
                         if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 322, smem_u32(ch) - sm_lo, idx))
-                            feat8_inplace(ch, c0 + j < t1, p.phi);
+                            feat8_inplace2(ch, c0 + j < t1, p.phi);
                     }
                 fence_proxy_async();
             }
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                     for (int c = 0; c < D / 8; ++c) {
                         uint8_t *ch = st + swz_chunk(128, i, c);
                         if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 422, smem_u32(ch) - sm_lo, c))
-                            feat8_inplace(ch, qvalid, p.phi);
+                            feat8_inplace2(ch, qvalid, p.phi);
                         uint8_t *gch = st + OFF_G + swz_chunk(128, i, c);
                         if (LA_CHECK(in_smem(gch, 16, sm_lo, sm_hi), 423, smem_u32(gch) - sm_lo, c)) {
                             uint4 x = *reinterpret_cast<uint4 *>(gch);
@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                     const int j = idx / (D / 8), c = idx % (D / 8);
                     uint8_t *ch = st + OFF_K + swz_chunk(C, j, c);
                     if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 424, smem_u32(ch) - sm_lo, idx))
-                        feat8_inplace(ch, c0 + j < t1, p.phi);
+                        feat8_inplace2(ch, c0 + j < t1, p.phi);
                 }
                 fence_proxy_async();
             }

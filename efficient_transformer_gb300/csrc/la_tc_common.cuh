@@ -65,10 +65,47 @@ __device__ __noinline__ bool dbg_fail(int id, long long a, long long b) {
 #define LA_CHECK(cond, id, a, b) true
 #endif
 
+// Timeline build (compile with -DLA_TIMELINE): block 0 of a kernel records clock64() at
+// fixed events of its first 64 chunks, read back with la_timeline_read().
+#ifdef LA_TIMELINE
+__device__ long long g_la_tl[64][16];
+#define LA_TL(k, ev)                                                  \
+    do {                                                              \
+        if (blockIdx.x == 0 && (k) < 64) g_la_tl[(k)][(ev)] = clock64(); \
+    } while (0)
+#else
+#define LA_TL(k, ev) \
+    do {             \
+    } while (0)
+#endif
+
 // Shared-memory range [p, p + bytes) lies inside [lo, hi).
 [[maybe_unused]] __device__ __forceinline__ bool in_smem(const void *p, uint32_t bytes, uint32_t lo, uint32_t hi) {
     const uint32_t a = smem_u32(p);
     return a >= lo && a + bytes <= hi;
+}
+
+// phi on two bf16 values with bf16x2 arithmetic, branch-free:
+// elu(x) + 1 = max(x, 0) + exp(min(x, 0)), relu(x) = max(x, 0).
+__device__ __forceinline__ uint32_t feat_bf16x2(uint32_t u, int phi) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+    __nv_bfloat162 y = __hmax2(x, zero);
+    if (phi == LA_PHI_ELU1) y = __hadd2(y, h2exp(__hmin2(x, zero)));
+    return *reinterpret_cast<uint32_t *>(&y);
+}
+
+// phi applied to 8 bf16 values (16 bytes) in place, or zeros for a row past the end.
+__device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid, int phi) {
+    uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
+    uint4 x = valid ? *ptr : make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+        x.x = feat_bf16x2(x.x, phi);
+        x.y = feat_bf16x2(x.y, phi);
+        x.z = feat_bf16x2(x.z, phi);
+        x.w = feat_bf16x2(x.w, phi);
+    }
+    *ptr = x;
 }
 
 // phi applied to 8 bf16 values in place (or zeros for a row past the end).
