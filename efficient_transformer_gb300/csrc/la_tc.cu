@@ -30,8 +30,6 @@
 namespace la {
 namespace {
 
-__host__ __device__ constexpr int align32(int x) { return (x + 31) / 32 * 32; }
-
 constexpr int kFwdThreads = 640;
 
 template <int D, int G>
@@ -72,34 +70,6 @@ struct StateCfg {
     static constexpr int NS = (kSmemLimit - 4096) / STAGE > 6 ? 6 : (kSmemLimit - 4096) / STAGE;
     static constexpr int SMEM = NS * STAGE + ONES_BYTES + 1024;
 };
-
-// A 16-row K-major tile with `cols` columns: row 0 = 1 for columns < cols, zero elsewhere.
-__device__ __forceinline__ void fill_ones_tile(uint8_t *t, int cols) {
-    const int nblk = (cols + 63) / 64;
-    for (int idx = threadIdx.x; idx < nblk * 16 * 8; idx += blockDim.x) {
-        const int blk = idx / 128, rc = idx % 128, row = rc / 8, c = rc % 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row == 0) {
-            const int col0 = blk * 64 + c * 8;
-            uint32_t w[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                w[q] = (col0 + 2 * q < cols ? 0x3F80u : 0u) | (col0 + 2 * q + 1 < cols ? 0x3F800000u : 0u);
-            v = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        *reinterpret_cast<uint4 *>(t + swz_chunk(16, row, blk * 8 + c)) = v;
-    }
-}
-
-// One 16-column slice of an S row (bf16) into the swizzled S_bf tile (D rows).
-template <int D>
-__device__ __forceinline__ void store_state_row(uint8_t *sbf, int d, const float *v, int c16) {
-    uint32_t w[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-    *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-}
 
 // ---------------------------------------------------------------------------------------
 // Per-segment state: S = phi(K)^T V and z = phi(K)^T 1 over the segment's tokens (fp32 in
@@ -213,7 +183,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
             for (int c16 = 0; c16 <= D / 16; ++c16) {
                 float v[16];
                 tmem_ld16(tS + lane_off + c16 * 16, v);
-                tmem_ld_wait();
+                tmem_wait_regs<16>(v);
                 if (c16 < D / 16) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) row[c16 * 16 + e] = v[e];
@@ -456,7 +426,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                         } else {
                             tmem_ld16(tA + lane_off, v);
                         }
-                        tmem_ld_wait();
+                        tmem_wait_regs<(C >= 32 ? 32 : 16)>(v);
 #pragma unroll
                         for (int h = 0; h < (C >= 32 ? 2 : 1); ++h) {
                             uint32_t w[8];
@@ -490,12 +460,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                         float v[64];
                         tmem_ld32(tS + lane_off + c64 * 64, v);
                         tmem_ld32(tS + lane_off + c64 * 64 + 32, v + 32);
-                        tmem_ld_wait();
+                        tmem_wait_regs<64>(v);
 #pragma unroll
                         for (int h = 0; h < 4; ++h) store_state_row<D>(sbf, i, v + 16 * h, c64 * 4 + h);
                     }
-                    const float zd = tmem_ld1(tS + lane_off + D);
-                    tmem_ld_wait();
+                    float zd = tmem_ld1(tS + lane_off + D);
+                    tmem_wait_regs<1>(&zd);
                     *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zd);
                 }
                 fence_proxy_async();
@@ -519,14 +489,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             tc_fence_after();
             if (i == 0) LA_TL(k, 12);
             float den = 0.f;
-            if (ok) den = tmem_ld1(tO + lane_off + D);
+            if (ok) {
+                den = tmem_ld1(tO + lane_off + D);
+                tmem_wait_regs<1>(&den);
+            }
 #pragma unroll
             for (int c64 = 0; c64 < D / 64; ++c64) {
                 float v[64];
                 if (ok) {
                     tmem_ld32(tO + lane_off + c64 * 64, v);
                     tmem_ld32(tO + lane_off + c64 * 64 + 32, v + 32);
-                    tmem_ld_wait();
+                    tmem_wait_regs<64>(v);
                 }
                 if (i == 0) bulk_wait_read();   // previous stores have read the staging tile
                 named_barrier(2, 128);

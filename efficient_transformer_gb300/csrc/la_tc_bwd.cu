@@ -28,22 +28,36 @@
 namespace la {
 namespace {
 
+constexpr int kBwdThreads = 640;
+
 template <int D, int G>
 struct BwdCfg {
     static constexpr int C = 128 / G;
     static constexpr int DB = D / 64;
+    static constexpr int CB = (C + 63) / 64;
     static constexpr int Q_BYTES = 128 * D * 2;
     static constexpr int K_BYTES = C * D * 2;
     static constexpr int V_BYTES = C * D * 2;
     static constexpr int G_BYTES = 128 * D * 2;
     static constexpr int STAGE = Q_BYTES + K_BYTES + V_BYTES + G_BYTES;   // [phi(Q) | phi(K) | V | g]
     static constexpr int NS = 2;
-    static constexpr int P_BYTES = ((C + 63) / 64) * 128 * 128;
+    static constexpr int P_BYTES = CB * 128 * 128;
     static constexpr int S_BYTES = DB * D * 128;            // S_bf: D rows (d) x D columns (e)
+    static constexpr int Z_BYTES = DB * 16 * 128;           // z_bf: 16 rows x D columns
+    static constexpr int ONES_BYTES = CB * 16 * 128;        // ones: 16 rows x C columns
+    static constexpr int GD_BYTES = 2 * 16 * 128;           // gd: 16 rows x 128 columns (query rows)
     static constexpr int R_BYTES = 2 * 128 * 128;           // R_bf: 128 rows x 128 columns (padded)
-    static constexpr int DQ_SMEM = NS * STAGE + P_BYTES + S_BYTES + 2 * D * 4 + 128 * 4 + 1024;
+    static constexpr int DQ_SMEM = NS * STAGE + P_BYTES + S_BYTES + Z_BYTES + ONES_BYTES + GD_BYTES + 1024;
     static constexpr int DKDV_SMEM = NS * STAGE + 2 * P_BYTES + R_BYTES + NS * 128 * 4 + 1024;
     static constexpr bool FITS = DQ_SMEM <= kSmemLimit - 1024 && DKDV_SMEM <= kSmemLimit - 1024;
+    // dq kernel TMEM columns: [S | z], [O | den] then da, A then dA, [R | r]
+    static constexpr int NW = D + 16;
+    static constexpr int T_S = 0;
+    static constexpr int T_O = align32(NW);
+    static constexpr int T_A = T_O + align32(NW);
+    static constexpr int T_R = T_A + align32(C);
+    static constexpr bool TMEM_FITS = T_R + NW <= 512;
+    static_assert(T_S == 0, "S starts the TMEM allocation");
 };
 
 __device__ __forceinline__ float feat_grad_from_feat(float f, int phi) {
@@ -54,15 +68,16 @@ __device__ __forceinline__ float feat_grad_from_feat(float f, int phi) {
 
 // ---------------------------------------------------------------------------------------
 template <int D, int G, bool CAUSAL>
-__global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CUtensorMap map_q,
-                                                      const __grid_constant__ CUtensorMap map_k,
-                                                      const __grid_constant__ CUtensorMap map_v,
-                                                      const __grid_constant__ CUtensorMap map_g, Params p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_constant__ CUtensorMap map_q,
+                                                              const __grid_constant__ CUtensorMap map_k,
+                                                              const __grid_constant__ CUtensorMap map_v,
+                                                              const __grid_constant__ CUtensorMap map_g,
+                                                              const __grid_constant__ CUtensorMap map_dq, Params p) {
     using K = BwdCfg<D, G>;
     constexpr int C = K::C, NS = K::NS;
     constexpr int OFF_K = K::Q_BYTES, OFF_V = OFF_K + K::K_BYTES, OFF_G = OFF_V + K::V_BYTES;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_full[NS], bar_ready[NS], bar_empty[NS];
+    __shared__ uint64_t bar_full[NS], bar_ready[NS], bar_empty[NS], bar_dqready[NS];
     __shared__ uint64_t bar_afull, bar_pready, bar_ofull, bar_gnready, bar_dafull, bar_dpready, bar_dqfull,
         bar_dofree, bar_sfull, bar_sbf, bar_fin;
     __shared__ uint32_t tmem_base;
@@ -71,10 +86,11 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
     const uint32_t sm_lo = smem_u32(smem_raw), sm_hi = sm_lo + K::DQ_SMEM;
     (void)sm_lo;
     (void)sm_hi;
-    uint8_t *pbuf = stage0 + NS * K::STAGE;
-    uint8_t *sbf = pbuf + K::P_BYTES;
-    float *zf = reinterpret_cast<float *>(sbf + K::S_BYTES);   // [2][D]
-    float *gds = zf + 2 * D;                                    // [128]
+    uint8_t *pbuf = stage0 + NS * K::STAGE;        // P, then dP
+    uint8_t *sbf = pbuf + K::P_BYTES;             // S_bf [D][D]
+    uint8_t *ztile = sbf + K::S_BYTES;            // z_bf: 16 x D, row 0 = z
+    uint8_t *ones = ztile + K::Z_BYTES;           // 16 x C, row 0 = 1
+    uint8_t *gdtile = ones + K::ONES_BYTES;       // 16 x 128, row 0 = gd over the query rows
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
@@ -86,12 +102,19 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
     const float *state = p.state + seg_state;
     float *rstate = p.rstate + seg_state;
 
+    fill_ones_tile(ones, C);
+    for (int idx = threadIdx.x; idx < (K::Z_BYTES + K::GD_BYTES) / 16; idx += blockDim.x) {
+        uint8_t *t = idx < K::Z_BYTES / 16 ? ztile + idx * 16 : gdtile + (idx - K::Z_BYTES / 16) * 16;
+        *reinterpret_cast<uint4 *>(t) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_ready[s], 128);
-            mbar_init(&bar_empty[s], 1 + 128);
+            mbar_init(&bar_empty[s], 2);
+            mbar_init(&bar_dqready[s], 128);
         }
         mbar_init(&bar_afull, 1);
         mbar_init(&bar_pready, 128);
@@ -113,7 +136,8 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = tmem_base, tO = tmem_base + 128, tA = tmem_base + 256, tR = tmem_base + 384;
+    const uint32_t tS = tmem_base + K::T_S, tO = tmem_base + K::T_O, tA = tmem_base + K::T_A,
+                   tR = tmem_base + K::T_R;
 
     if (warp == 0) {
         // ---------------- TMA producer
@@ -125,7 +149,10 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
                 if (k >= NS && !mbar_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
-                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N, 301, smem_u32(st) - sm_lo, c0)) break;
+                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N && bh0 + G <= p.B * p.Hq, 301,
+                              smem_u32(st) - sm_lo, c0))
+                    break;
+                LA_TL(k, 0);
                 mbar_arrive_expect_tx(&bar_full[s], bytes);
                 for (int r = 0; r < G; ++r)
                     for (int blk = 0; blk < K::DB; ++blk) {
@@ -148,16 +175,19 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
             constexpr uint32_t idA = idesc_bf16(128, C, false, false);
             constexpr uint32_t idO = idesc_bf16(128, D, false, true);
             constexpr uint32_t idOK = idesc_bf16(128, D, false, false);
+            constexpr uint32_t idGZ = idesc_bf16(128, D, true, true);
+            constexpr uint32_t id16 = idesc_bf16(128, 16, false, false);
             constexpr uint32_t idR = idesc_bf16(128, D, true, true);
-            const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf);
+            constexpr uint32_t idR16 = idesc_bf16(128, 16, true, false);
+            const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf), zt = smem_u32(ztile), on = smem_u32(ones),
+                           gdt = smem_u32(gdtile);
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
+                LA_TL(k, 3);
                 tc_fence_after();
                 const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V, gs = qs + OFF_G;
-                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && pb + K::P_BYTES <= sm_hi &&
-                                  sbf_u + K::S_BYTES <= sm_hi,
-                              311, qs - sm_lo, k))
+                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && gdt + K::GD_BYTES <= sm_hi, 311, qs - sm_lo, k))
                     break;
                 if (CAUSAL) {
                     for (int kk = 0; kk < D / 16; ++kk)
@@ -167,15 +197,21 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
                 }
                 if ((CAUSAL || k == 0) && !mbar_wait(&bar_sbf, k & 1, &abort_flag)) break;
                 if (k > 0 && !mbar_wait(&bar_dofree, (k - 1) & 1, &abort_flag)) break;
+                LA_TL(k, 4);
                 tc_fence_after();
-                uint32_t acc = 0;
+                // O = phi(Q) S_bf (+ P V);  den = phi(Q) z_bf (+ P 1)
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    mma_bf16(tO, desc_kmajor(qs, 128, 0, kk), desc_mnmajor(sbf_u, D, 0, kk), idO, kk > 0 ? 1u : 0u);
+                    mma_bf16(tO + D, desc_kmajor(qs, 128, 0, kk), desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
+                }
                 if (CAUSAL)
-                    for (int kk = 0; kk < C / 16; ++kk, acc = 1)
-                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(vs, C, 0, kk), idO, acc);
-                for (int kk = 0; kk < D / 16; ++kk, acc = 1)
-                    mma_bf16(tO, desc_kmajor(qs, 128, 0, kk), desc_mnmajor(sbf_u, D, 0, kk), idO, acc);
+                    for (int kk = 0; kk < C / 16; ++kk) {
+                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(vs, C, 0, kk), idO, 1u);
+                        mma_bf16(tO + D, desc_kmajor(pb, 128, 0, kk), desc_kmajor(on, 16, 0, kk), id16, 1u);
+                    }
                 mma_commit(&bar_ofull);
                 if (!mbar_wait(&bar_gnready, k & 1, &abort_flag)) break;
+                LA_TL(k, 5);
                 tc_fence_after();
                 if (CAUSAL) {
                     for (int kk = 0; kk < D / 16; ++kk)
@@ -184,33 +220,64 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
                     if (!mbar_wait(&bar_dpready, k & 1, &abort_flag)) break;
                     tc_fence_after();
                 }
-                acc = 0;
+                LA_TL(k, 6);
+                // da = (dP phi(K)) + gn S_bf^T + gd z^T
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tO, desc_kmajor(gs, 128, 0, kk), desc_kmajor(sbf_u, D, 0, kk), idOK, kk > 0 ? 1u : 0u);
+                mma_bf16(tO, desc_mnmajor(gdt, 16, 0, 0), desc_mnmajor(zt, 16, 0, 0), idGZ, 1u);
                 if (CAUSAL)
-                    for (int kk = 0; kk < C / 16; ++kk, acc = 1)
-                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(ks_, C, 0, kk), idO, acc);
-                for (int kk = 0; kk < D / 16; ++kk, acc = 1)
-                    mma_bf16(tO, desc_kmajor(gs, 128, 0, kk), desc_kmajor(sbf_u, D, 0, kk), idOK, acc);
-                mma_commit(&bar_dqfull);
-                for (int kk = 0; kk < 128 / 16; ++kk)
-                    mma_bf16(tR, desc_mnmajor(qs, 128, 0, kk), desc_mnmajor(gs, 128, 0, kk), idR,
-                             (k > 0 || kk > 0) ? 1u : 0u);
-                if (CAUSAL) {
                     for (int kk = 0; kk < C / 16; ++kk)
+                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(ks_, C, 0, kk), idO, 1u);
+                // R += phi(Q)^T gn, r += phi(Q)^T gd
+                for (int kk = 0; kk < 128 / 16; ++kk) {
+                    const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
+                    mma_bf16(tR, desc_mnmajor(qs, 128, 0, kk), desc_mnmajor(gs, 128, 0, kk), idR, acc);
+                    mma_bf16(tR + D, desc_mnmajor(qs, 128, 0, kk), desc_kmajor(gdt, 16, 0, kk), idR16, acc);
+                }
+                mma_commit(&bar_dqfull);
+                if (CAUSAL) {
+                    for (int kk = 0; kk < C / 16; ++kk) {
                         mma_bf16(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs, C, 0, kk), idR, 1u);
+                        mma_bf16(tS + D, desc_mnmajor(ks_, C, 0, kk), desc_kmajor(on, 16, 0, kk), idR16, 1u);
+                    }
                     mma_commit(&bar_sfull);
                 }
                 mma_commit(&bar_empty[s]);
+                LA_TL(k, 7);
             }
             mma_commit(&bar_fin);
             mbar_drain(&bar_fin, 0);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- phi prologue (in place on phi(Q) and phi(K) tiles)
-        const int i = threadIdx.x - 128;
+    } else if (warp == 2) {
+        // ---------------- dq store: the epilogue leaves dq over the grad_out tile; TMA writes
+        // it out, and the stage is released once the copy has read it
+        if (lane == 0) {
+            for (int k = 0; k < nchunk; ++k) {
+                const int s = k % NS;
+                const bool ok = mbar_wait(&bar_dqready[s], (k / NS) & 1, &abort_flag);
+                uint8_t *st = stage0 + s * K::STAGE;
+                const int c0 = t0 + k * C;
+                if (ok) {
+                    for (int r = 0; r < G; ++r)
+                        for (int blk = 0; blk < K::DB; ++blk)
+                            tma_store_3d(&map_dq, st + OFF_G + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
+                    bulk_commit();
+                    bulk_wait_read();
+                }
+                mbar_arrive(&bar_empty[s]);
+                if (!ok) break;
+            }
+            bulk_wait_all();
+        }
+    } else if ((warp >= 4 && warp < 8) || warp >= 16) {
+        // ---------------- phi prologue (in place on phi(Q) and phi(K)); alternate chunks
+        const int pg = warp >= 16 ? 1 : 0;
+        const int i = threadIdx.x - (pg ? 512 : 128);
         bool ok = true;
-        for (int k = 0; k < nchunk; ++k) {
+        for (int k = pg; k < nchunk; k += 2) {
             const int s = k % NS;
             ok = ok && warp_wait(&bar_full[s], (k / NS) & 1, &abort_flag);
+            if (i == 0) LA_TL(k, 1);
             if (ok) {
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
@@ -222,6 +289,7 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
                         feat8_inplace2(ch, qvalid, p.phi);
                 }
                 if (CAUSAL)
+#pragma unroll 2
                     for (int idx = i; idx < C * (D / 8); idx += 128) {
                         const int j = idx / (D / 8), c = idx % (D / 8);
                         uint8_t *ch = st + OFF_K + swz_chunk(C, j, c);
@@ -230,48 +298,49 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
                     }
                 fence_proxy_async();
             }
+            if (i == 0) LA_TL(k, 2);
             mbar_arrive(&bar_ready[s]);
         }
     } else if (warp >= 8 && warp < 12) {
-        // ---------------- row work (thread = query row i) and column sums (thread = d)
+        // ---------------- row work (thread = query row i): P, gn over the grad_out tile, gd, dP
         const int i = threadIdx.x - 256;
         const int wq = warp % 4;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const int r = i / C, ti = i % C;
         const int bh = bh0 + r;
-        if (i < D) zf[i] = state[(size_t)i * (D + 1) + D];
-        float r_acc = 0.f;
-        named_barrier(1, 128);
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
-            const int c0 = t0 + k * C, t = c0 + ti;
+            const int t = t0 + k * C + ti;
             const bool valid = t < t1;
             uint8_t *st = stage0 + s * K::STAGE;
-            const float *z = zf + (CAUSAL ? (k & 1) * D : 0);
-            float den_intra = 0.f;
             if (CAUSAL) {
                 ok = ok && warp_wait(&bar_afull, k & 1, &abort_flag);
                 tc_fence_after();
+                if (i == 0) LA_TL(k, 8);
                 if (ok) {
-#pragma unroll 1
-                    for (int c16 = 0; c16 < C / 16; ++c16) {
-                        float v[16];
-                        tmem_ld16(tA + lane_off + c16 * 16, v);
-                        tmem_ld_wait();
-                        uint32_t w[8];
 #pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            const int j = c16 * 16 + e;
-                            w[e / 2] = pack_bf16x2((j <= ti) ? v[e] : 0.f, (j + 1 <= ti) ? v[e + 1] : 0.f);
-                            const float2 f = unpack_bf16x2(w[e / 2]);
-                            den_intra += f.x + f.y;
-                        }
-                        uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
-                        if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 331,
-                                     smem_u32(p0) - sm_lo, c16)) {
-                            *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
-                            *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int c32 = 0; c32 < (C + 31) / 32; ++c32) {
+                        float v[32];
+                        if (C >= 32) tmem_ld32(tA + lane_off + c32 * 32, v);
+                        else tmem_ld16(tA + lane_off, v);
+                        tmem_wait_regs<(C >= 32 ? 32 : 16)>(v);
+#pragma unroll
+                        for (int h = 0; h < (C >= 32 ? 2 : 1); ++h) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                const int j = c32 * 32 + h * 16 + e;
+                                w[e / 2] = pack_bf16x2((j <= ti) ? v[h * 16 + e] : 0.f,
+                                                       (j + 1 <= ti) ? v[h * 16 + e + 1] : 0.f);
+                            }
+                            const int c16 = c32 * 2 + h;
+                            uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
+                            if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 331,
+                                         smem_u32(p0) - sm_lo, c16)) {
+                                *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
+                                *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
+                            }
                         }
                     }
                     fence_proxy_async();
@@ -282,46 +351,36 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
             // num, den -> gn (over the grad_out tile), gd
             ok = ok && warp_wait(&bar_ofull, k & 1, &abort_flag);
             tc_fence_after();
+            if (i == 0) LA_TL(k, 9);
             float gd = 0.f;
             if (ok) {
-                float dint = 0.f;
-#pragma unroll 4
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint8_t *ch = st + swz_chunk(128, i, c);
-                    if (!LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 332, smem_u32(ch) - sm_lo, c)) continue;
-                    const uint4 x = *reinterpret_cast<const uint4 *>(ch);
-                    const uint32_t *xi = reinterpret_cast<const uint32_t *>(&x);
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float2 f = unpack_bf16x2(xi[h]);
-                        dint += f.x * z[c * 8 + 2 * h] + f.y * z[c * 8 + 2 * h + 1];
-                    }
-                }
-                const float den = den_intra + dint + p.eps;
+                float den = tmem_ld1(tO + lane_off + D);
+                tmem_wait_regs<1>(&den);
+                den += p.eps;
                 const float inv = 1.f / den;
                 float gdot = 0.f;
-#pragma unroll 1
-                for (int c16 = 0; c16 < D / 16; ++c16) {
-                    float v[16];
-                    tmem_ld16(tO + lane_off + c16 * 16, v);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint8_t *ch = st + OFF_G + swz_chunk(128, i, 2 * c16 + h);
-                        if (!LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 333, smem_u32(ch) - sm_lo, c16)) continue;
+                for (int c64 = 0; c64 < D / 64; ++c64) {
+                    float v[64];
+                    tmem_ld32(tO + lane_off + c64 * 64, v);
+                    tmem_ld32(tO + lane_off + c64 * 64 + 32, v + 32);
+                    tmem_wait_regs<64>(v);
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        uint8_t *ch = st + OFF_G + swz_chunk(128, i, c64 * 8 + q8);
                         uint4 x = *reinterpret_cast<uint4 *>(ch);
                         uint32_t *xi = reinterpret_cast<uint32_t *>(&x);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float2 gv = unpack_bf16x2(xi[q]);
-                            gdot += gv.x * v[h * 8 + 2 * q] + gv.y * v[h * 8 + 2 * q + 1];
+                            gdot += gv.x * v[q8 * 8 + 2 * q] + gv.y * v[q8 * 8 + 2 * q + 1];
                             xi[q] = valid ? pack_bf16x2(gv.x * inv, gv.y * inv) : 0u;
                         }
                         *reinterpret_cast<uint4 *>(ch) = x;
                     }
                 }
                 gd = valid ? -gdot * inv * inv : 0.f;
-                gds[i] = gd;
+                *reinterpret_cast<__nv_bfloat16 *>(gdtile + swz_offset(16, 0, i)) = __float2bfloat16_rn(gd);
                 if (valid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 334, bh, t)) {
                     p.den[(size_t)bh * p.N + t] = den;
                     p.gd[(size_t)bh * p.N + t] = gd;
@@ -329,146 +388,149 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dq(const __grid_constant__ CU
                 fence_proxy_async();
             }
             tc_fence_before();
+            if (i == 0) LA_TL(k, 12);
             mbar_arrive(&bar_gnready);
             if (CAUSAL) {   // dP = mask(dA + gd), into the P buffer (P was consumed by the O product)
                 ok = ok && warp_wait(&bar_dafull, k & 1, &abort_flag);
                 tc_fence_after();
                 if (ok) {
-#pragma unroll 1
-                    for (int c16 = 0; c16 < C / 16; ++c16) {
-                        float v[16];
-                        tmem_ld16(tA + lane_off + c16 * 16, v);
-                        tmem_ld_wait();
-                        uint32_t w[8];
 #pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            const int j = c16 * 16 + e;
-                            w[e / 2] = pack_bf16x2((j <= ti) ? v[e] + gd : 0.f, (j + 1 <= ti) ? v[e + 1] + gd : 0.f);
-                        }
-                        uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
-                        if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 335,
-                                     smem_u32(p0) - sm_lo, c16)) {
-                            *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
-                            *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int c32 = 0; c32 < (C + 31) / 32; ++c32) {
+                        float v[32];
+                        if (C >= 32) tmem_ld32(tA + lane_off + c32 * 32, v);
+                        else tmem_ld16(tA + lane_off, v);
+                        tmem_wait_regs<(C >= 32 ? 32 : 16)>(v);
+#pragma unroll
+                        for (int h = 0; h < (C >= 32 ? 2 : 1); ++h) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                const int j = c32 * 32 + h * 16 + e;
+                                w[e / 2] = pack_bf16x2((j <= ti) ? v[h * 16 + e] + gd : 0.f,
+                                                       (j + 1 <= ti) ? v[h * 16 + e + 1] + gd : 0.f);
+                            }
+                            const int c16 = c32 * 2 + h;
+                            uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
+                            if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 335,
+                                         smem_u32(p0) - sm_lo, c16)) {
+                                *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
+                                *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
+                            }
                         }
                     }
                     fence_proxy_async();
                 }
                 tc_fence_before();
+                if (i == 0) LA_TL(k, 13);
                 mbar_arrive(&bar_dpready);
             }
-            // dq = phi'(q) * (da + gd z)
-            ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
-            tc_fence_after();
-            if (ok) {
-                __nv_bfloat16 *qrow = static_cast<__nv_bfloat16 *>(p.dq) + ((size_t)bh * p.N + t) * D;
-#pragma unroll 1
-                for (int c16 = 0; c16 < D / 16; ++c16) {
-                    float v[16];
-                    tmem_ld16(tO + lane_off + c16 * 16, v);
-                    tmem_ld_wait();
-                    if (valid && LA_CHECK(((size_t)bh * p.N + t) * D + c16 * 16 + 16 <= (size_t)p.B * p.Hq * p.N * D,
-                                          336, bh, t)) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint4 x = *reinterpret_cast<const uint4 *>(st + swz_chunk(128, i, 2 * c16 + h));
-                            const uint32_t *xi = reinterpret_cast<const uint32_t *>(&x);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float2 f = unpack_bf16x2(xi[q]);
-                                const int d0 = c16 * 16 + h * 8 + 2 * q;
-                                w[h * 4 + q] =
-                                    pack_bf16x2(feat_grad_from_feat(f.x, p.phi) * (v[h * 8 + 2 * q] + gd * z[d0]),
-                                                feat_grad_from_feat(f.y, p.phi) * (v[h * 8 + 2 * q + 1] + gd * z[d0 + 1]));
-                            }
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(qrow + c16 * 16);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    }
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&bar_dofree);
-            named_barrier(1, 128);
-            if (ok && i < D) {
-                // r += sum_i gd_i phi(q_i)[d] over this chunk's rows (thread d = i)
-                for (int row = 0; row < 128; ++row) {
-                    const uint8_t *e_ = st + swz_offset(128, row, i);
-                    r_acc += gds[row] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(e_));
-                }
-                if (CAUSAL) {   // z for the next chunk
-                    float zs = zf[(k & 1) * D + i];
-                    for (int j = 0; j < C; ++j)
-                        zs += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(st + OFF_K + swz_offset(C, j, i)));
-                    zf[((k + 1) & 1) * D + i] = zs;
-                }
-            }
-            mbar_arrive(&bar_empty[s]);
-            named_barrier(1, 128);
         }
-        if (ok && i < D) rstate[(size_t)i * (D + 1) + D] = r_acc;
-    } else if (warp >= 12) {
-        // ---------------- state conversion; at the end the segment's R to the workspace
-        const int d = threadIdx.x - 384;
+    } else if (warp >= 12 && warp < 16) {
+        // ---------------- dq epilogue (thread = query row i) and state conversion (thread = d)
+        const int i = threadIdx.x - 384;
         const int wq = warp % 4;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        // initial S, z of the segment: TMEM (causal) and the bf16 operand tiles
         if (wq * 32 < D) {
-            const float *row = state + (size_t)d * (D + 1);
+            const float *row = state + (size_t)i * (D + 1);
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 float v[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) v[e] = row[c16 * 16 + e];
                 if (CAUSAL) tmem_st16(tS + lane_off + c16 * 16, v);
-                uint32_t w[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-                *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+                store_state_row<D>(sbf, i, v, c16);
             }
-            if (CAUSAL) tmem_st_wait();
+            float zv[16];
+            zv[0] = row[D];
+#pragma unroll
+            for (int e = 1; e < 16; ++e) zv[e] = 0.f;
+            if (CAUSAL) {
+                tmem_st16(tS + lane_off + D, zv);
+                tmem_st_wait();
+            }
+            *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zv[0]);
         }
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(&bar_sbf);
         bool ok = true;
-        if (CAUSAL) {
-            for (int k = 0; k < nchunk; ++k) {
+        for (int k = 0; k < nchunk; ++k) {
+            const int s = k % NS;
+            uint8_t *st = stage0 + s * K::STAGE;
+            ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
+            tc_fence_after();
+            if (i == 0) LA_TL(k, 10);
+            // dq = phi'(q) * da, written over the (dead) gn tile, then stored by TMA
+            if (ok) {
+#pragma unroll
+                for (int c64 = 0; c64 < D / 64; ++c64) {
+                    float v[64];
+                    tmem_ld32(tO + lane_off + c64 * 64, v);
+                    tmem_ld32(tO + lane_off + c64 * 64 + 32, v + 32);
+                    tmem_wait_regs<64>(v);
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(st + swz_chunk(128, i, c64 * 8 + q8));
+                        const uint32_t *xi = reinterpret_cast<const uint32_t *>(&x);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = unpack_bf16x2(xi[q]);
+                            w[q] = pack_bf16x2(feat_grad_from_feat(f.x, p.phi) * v[q8 * 8 + 2 * q],
+                                               feat_grad_from_feat(f.y, p.phi) * v[q8 * 8 + 2 * q + 1]);
+                        }
+                        *reinterpret_cast<uint4 *>(st + OFF_G + swz_chunk(128, i, c64 * 8 + q8)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bar_dofree);
+            fence_proxy_async();
+            if (i == 0) LA_TL(k, 14);
+            mbar_arrive(&bar_dqready[s]);
+            // S, z after chunk k -> operand tiles for chunk k + 1
+            if (CAUSAL) {
                 ok = ok && warp_wait(&bar_sfull, k & 1, &abort_flag);
                 tc_fence_after();
+                if (i == 0) LA_TL(k, 11);
                 if (ok && wq * 32 < D) {
-#pragma unroll 1
-                    for (int c16 = 0; c16 < D / 16; ++c16) {
-                        float v[16];
-                        tmem_ld16(tS + lane_off + c16 * 16, v);
-                        tmem_ld_wait();
-                        uint32_t w[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-                        *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16 + 1)) =
-                            make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int c64 = 0; c64 < D / 64; ++c64) {
+                        float v[64];
+                        tmem_ld32(tS + lane_off + c64 * 64, v);
+                        tmem_ld32(tS + lane_off + c64 * 64 + 32, v + 32);
+                        tmem_wait_regs<64>(v);
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) store_state_row<D>(sbf, i, v + 16 * h, c64 * 4 + h);
                     }
+                    float zd = tmem_ld1(tS + lane_off + D);
+                    tmem_wait_regs<1>(&zd);
+                    *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zd);
                 }
                 fence_proxy_async();
                 tc_fence_before();
+                if (i == 0) LA_TL(k, 15);
                 mbar_arrive(&bar_sbf);
             }
         }
+        // the segment's R, r -> workspace
         ok = ok && warp_wait(&bar_fin, 0, &abort_flag);
         tc_fence_after();
         if (ok && wq * 32 < D) {
-            float *row = rstate + (size_t)d * (D + 1);
+            float *row = rstate + (size_t)i * (D + 1);
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 float v[16];
                 tmem_ld16(tR + lane_off + c16 * 16, v);
-                tmem_ld_wait();
+                tmem_wait_regs<16>(v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) row[c16 * 16 + e] = v[e];
             }
+            float rd = tmem_ld1(tR + lane_off + D);
+            tmem_wait_regs<1>(&rd);
+            row[D] = rd;
         }
     }
     tc_fence_before();
@@ -685,7 +747,8 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                         float va[16], vd[16];
                         tmem_ld16(tA + lane_off + c16 * 16, va);
                         tmem_ld16(tD + lane_off + c16 * 16, vd);
-                        tmem_ld_wait();
+                        tmem_wait_regs<16>(va);
+                        tmem_wait_regs<16>(vd);
                         uint32_t wa[8], wd[8];
 #pragma unroll
                         for (int e = 0; e < 16; e += 2) {
@@ -721,7 +784,8 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                     float vb[16], vv[16];
                     tmem_ld16(tA + lane_off + c16 * 16, vb);
                     tmem_ld16(tD + lane_off + c16 * 16, vv);
-                    tmem_ld_wait();
+                    tmem_wait_regs<16>(vb);
+                    tmem_wait_regs<16>(vv);
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int j = c16 * 16 + e, tok = c0 + j;
@@ -777,7 +841,7 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                     for (int c16 = 0; c16 < D / 16; ++c16) {
                         float v[16];
                         tmem_ld16(tR + lane_off + c16 * 16, v);
-                        tmem_ld_wait();
+                        tmem_wait_regs<16>(v);
                         uint32_t w[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
@@ -804,18 +868,19 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
 template <int D, int G, bool CAUSAL>
 cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     using K = BwdCfg<D, G>;
-    CUtensorMap mq{}, mk{}, mv{}, mg{};
+    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{};
     cudaError_t e = make_map(&mq, p.q, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mg, p.g, p.B * p.Hq, p.N, D, K::C);
+    if (e == cudaSuccess) e = make_map(&mdq, p.dq, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = prepare(k_tc_bwd_dq<D, G, CAUSAL>, K::DQ_SMEM);
     if (e == cudaSuccess) e = prepare(k_tc_bwd_dkdv<D, G, CAUSAL>, K::DKDV_SMEM);
     if (e != cudaSuccess) return e;
     const int grid = p.B * p.Hkv * p.nseg;
     {
         TraceScope ts(CAUSAL ? "tc_bwd_dq_causal" : "tc_bwd_dq_bidir", s);
-        k_tc_bwd_dq<D, G, CAUSAL><<<grid, 512, K::DQ_SMEM, s>>>(mq, mk, mv, mg, p);
+        k_tc_bwd_dq<D, G, CAUSAL><<<grid, kBwdThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, p);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess)
@@ -828,7 +893,7 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
 
 template <int D, int G>
 cudaError_t backward_dg(const Params &p, cudaStream_t s) {
-    if constexpr (!BwdCfg<D, G>::FITS) {
+    if constexpr (!BwdCfg<D, G>::FITS || !BwdCfg<D, G>::TMEM_FITS) {
         return cudaErrorNotSupported;
     } else {
         cudaError_t e = tc_launch_state(p, s);
@@ -863,6 +928,13 @@ cudaError_t tc_backward(const Params &p, cudaStream_t s) {
 }
 
 }  // namespace la
+
+#ifdef LA_TIMELINE
+// Timeline builds only: the dq kernel's event clocks ([64][16] long long).
+extern "C" int la_timeline_read_bwd(long long *out) {
+    return cudaMemcpyFromSymbol(out, la::g_la_tl, sizeof(long long) * 64 * 16) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 #ifdef LA_DEBUG
 // Debug builds only: the first failed self-check of the backward kernels (id, a, b, block).

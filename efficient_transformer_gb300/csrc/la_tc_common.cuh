@@ -108,6 +108,36 @@ __device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid, int p
     *ptr = x;
 }
 
+__host__ __device__ constexpr int align32(int x) { return (x + 31) / 32 * 32; }
+
+// A 16-row K-major tile with `cols` columns: row 0 = 1 for columns < cols, zero elsewhere.
+__device__ __forceinline__ void fill_ones_tile(uint8_t *t, int cols) {
+    const int nblk = (cols + 63) / 64;
+    for (int idx = threadIdx.x; idx < nblk * 16 * 8; idx += blockDim.x) {
+        const int blk = idx / 128, rc = idx % 128, row = rc / 8, c = rc % 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row == 0) {
+            const int col0 = blk * 64 + c * 8;
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                w[q] = (col0 + 2 * q < cols ? 0x3F80u : 0u) | (col0 + 2 * q + 1 < cols ? 0x3F800000u : 0u);
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        *reinterpret_cast<uint4 *>(t + swz_chunk(16, row, blk * 8 + c)) = v;
+    }
+}
+
+// One 16-column slice of an S row (bf16) into the swizzled S_bf tile (D rows).
+template <int D>
+__device__ __forceinline__ void store_state_row(uint8_t *sbf, int d, const float *v, int c16) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+    *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 // phi applied to 8 bf16 values in place (or zeros for a row past the end).
 __device__ __forceinline__ void feat8_inplace(uint8_t *chunk, bool valid, int phi) {
     uint4 *ptr = reinterpret_cast<uint4 *>(chunk);

@@ -236,6 +236,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Wait for this warp's TMEM loads, then pin the N loaded registers behind the wait: the
+// empty asm "rewrites" each value, so no use of them can be scheduled before the wait.
+template <int N>
+__device__ __forceinline__ void tmem_wait_regs(float *v) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i])::"memory");
+}
+
 // Warp-wide: thread t writes TMEM lane (lane of taddr) + t, 16 consecutive columns.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
     asm volatile(

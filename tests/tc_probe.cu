@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
         for (int c0 = 0; c0 < N; c0 += 16) {
             float v[16];
             tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-            tmem_ld_wait();
+            tmem_wait_regs<16>(v);
             for (int i = 0; i < 16; ++i) d[row * N + c0 + i] = v[i];
         }
     }
