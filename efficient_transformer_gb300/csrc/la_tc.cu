@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
                 }
                 fence_proxy_async();
             }
-            mbar_arrive(&bar_ready[s]);
+            mbar_arrive_warp(&bar_ready[s]);
         }
         ok = ok && warp_wait(&bar_done, 0, &abort_flag);
         tc_fence_after();
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 fence_proxy_async();
             }
             if (i == 0) LA_TL(k, 2);
-            mbar_arrive(&bar_ready[s]);
+            mbar_arrive_warp(&bar_ready[s]);
         }
     } else if (warp >= 8 && warp < 12) {
         // ---------------- state conversion (thread = d) and P conversion (thread = row i)
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
         }
         fence_proxy_async();
         tc_fence_before();
-        mbar_arrive(&bar_sbf);
+        mbar_arrive_warp(&bar_sbf);
         if (CAUSAL) {
             bool ok = true;
             for (int k = 0; k < nchunk; ++k) {
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 }
                 tc_fence_before();
                 if (i == 0) LA_TL(k, 9);
-                mbar_arrive(&bar_pready);
+                mbar_arrive_warp(&bar_pready);
                 // S, z after chunk k -> operand tiles for chunk k + 1
                 ok = ok && warp_wait(&bar_sfull, k & 1, &abort_flag);
                 tc_fence_after();
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 fence_proxy_async();
                 tc_fence_before();
                 if (i == 0) LA_TL(k, 11);
-                mbar_arrive(&bar_sbf);
+                mbar_arrive_warp(&bar_sbf);
             }
         }
     } else if (warp >= 12 && warp < 16) {
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             }
             tc_fence_before();
             if (i == 0) LA_TL(k, 13);
-            mbar_arrive(&bar_ofree[o]);
+            mbar_arrive_warp(&bar_ofree[o]);
         }
         if (i == 0) bulk_wait_all();
     }

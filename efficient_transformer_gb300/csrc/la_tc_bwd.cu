@@ -13,16 +13,18 @@
 //   scan (suffix R)
 //   k_tc_bwd_dkdv reverse over chunks: dk, dv (summed over the n_rep heads of the group)
 //
-// Per chunk of k_tc_bwd_dq (128 stacked query rows, C keys):
-//   A = phi(Q) phi(K)^T -> P;  O = P V + phi(Q) S_bf -> num; den = rowsum P + phi(q).z + eps
-//   gn = g / den (bf16, written over the grad_out tile), gd = -(g . num) / den^2
-//   dA = gn V^T -> dP = mask(dA + gd);  da = dP phi(K) + gn S_bf^T
-//   dq = phi'(q) * (da + gd z);  R += phi(Q)^T gn;  S += phi(K)^T V
+// Per chunk of k_tc_bwd_dq (128 stacked query rows, C keys), with the raw grad_out g:
+//   A = phi(Q) phi(K)^T,  dA' = g V^T,  X = g S_bf^T,  den = phi(Q) z + rowsum mask(A) + eps
+//   g . num = phi(q) . X + sum_j mask(A) dA'      (no O product is needed)
+//   h = -(g . num) / den,  gd = h / den,  dP' = mask(dA' + h) = den * dP
+//   phi_s = phi(q) / den (bf16, in place over phi(Q))
+//   X += dP' phi(K),  den * da = X + h z (fp32),  dq = phi'(q) / den * (X + h z)
+//   R += phi_s^T g (= phi(Q)^T gn),  r += phi_s^T h (= phi(Q)^T gd),  S += phi(K)^T V
 // Per chunk of k_tc_bwd_dkdv, computed transposed so the 128 query rows stay on the MMA's
 // K dimension (and the sum over the group's heads comes for free):
 //   dk^T = phi(Q)^T dP + R_bf V^T (+ r),  dv^T = gn^T P + R_bf^T phi(K)^T,  R += phi(Q)^T gn
-// Warp roles as in the forward: warp 0 TMA, warp 1 MMA, warps 4-7 prologue, warps 8-11
-// row work and epilogues, warps 12-15 state conversion.
+// Warp roles: warp 0 TMA, warp 1 MMA, warp 2 (dq kernel) dq store; the dq kernel runs the
+// feature map on warps 4-7 and 16-19 together and its row work on a pool of warps 8-15.
 #include "la_tc_common.cuh"
 
 namespace la {
@@ -40,23 +42,29 @@ struct BwdCfg {
     static constexpr int V_BYTES = C * D * 2;
     static constexpr int G_BYTES = 128 * D * 2;
     static constexpr int STAGE = Q_BYTES + K_BYTES + V_BYTES + G_BYTES;   // [phi(Q) | phi(K) | V | g]
-    static constexpr int NS = 2;
     static constexpr int P_BYTES = CB * 128 * 128;
     static constexpr int S_BYTES = DB * D * 128;            // S_bf: D rows (d) x D columns (e)
-    static constexpr int Z_BYTES = DB * 16 * 128;           // z_bf: 16 rows x D columns
+    static constexpr int Z_BYTES = DB * 16 * 128;           // z: 16 rows x D columns (rows 0-2: hi, lo, hi)
     static constexpr int ONES_BYTES = CB * 16 * 128;        // ones: 16 rows x C columns
-    static constexpr int GD_BYTES = 2 * 16 * 128;           // gd: 16 rows x 128 columns (query rows)
+    static constexpr int H_BYTES = 2 * 16 * 128;            // h: 16 rows x 128 query rows (rows 0-2: hi, hi, lo)
+    static constexpr int XCH_BYTES = 2 * 128 * 4;           // partial row dots of the two pool halves
+    // dq kernel: stages, dP', S_bf, two z slots, ones, h, exchange
+    static constexpr int DQ_FIXED = P_BYTES + S_BYTES + 2 * Z_BYTES + ONES_BYTES + H_BYTES + XCH_BYTES + 1024;
+    static constexpr int NS_DQ = 3 * STAGE + DQ_FIXED <= kSmemLimit - 512 ? 3 : 2;
+    static constexpr int DQ_SMEM = NS_DQ * STAGE + DQ_FIXED;
+    // dk/dv kernel
+    static constexpr int NS = 2;
     static constexpr int R_BYTES = 2 * 128 * 128;           // R_bf: 128 rows x 128 columns (padded)
-    static constexpr int DQ_SMEM = NS * STAGE + P_BYTES + S_BYTES + Z_BYTES + ONES_BYTES + GD_BYTES + 1024;
     static constexpr int DKDV_SMEM = NS * STAGE + 2 * P_BYTES + R_BYTES + NS * 128 * 4 + 1024;
-    static constexpr bool FITS = DQ_SMEM <= kSmemLimit - 1024 && DKDV_SMEM <= kSmemLimit - 1024;
-    // dq kernel TMEM columns: [S | z], [O | den] then da, A then dA, [R | r]
-    static constexpr int NW = D + 16;
+    static constexpr bool FITS = DQ_SMEM <= kSmemLimit - 512 && DKDV_SMEM <= kSmemLimit - 1024;
+    // dq kernel TMEM columns: [S | z], den, A, dA', X (then den * da - h z), [R | r]
     static constexpr int T_S = 0;
-    static constexpr int T_O = align32(NW);
-    static constexpr int T_A = T_O + align32(NW);
-    static constexpr int T_R = T_A + align32(C);
-    static constexpr bool TMEM_FITS = T_R + NW <= 512;
+    static constexpr int T_DEN = D + 16;
+    static constexpr int T_A = T_DEN + 16;
+    static constexpr int T_A2 = T_A + C;
+    static constexpr int T_X = T_A2 + C;
+    static constexpr int T_R = T_X + D;
+    static constexpr bool TMEM_FITS = T_R + D + 16 <= 512;
     static_assert(T_S == 0, "S starts the TMEM allocation");
 };
 
@@ -64,6 +72,33 @@ __device__ __forceinline__ float feat_grad_from_feat(float f, int phi) {
     // elu+1: phi = x + 1 > 1 for x > 0 (derivative 1), phi = exp(x) <= 1 otherwise
     // (derivative exp(x) = phi); relu: derivative 1 where phi > 0.
     return phi == LA_PHI_ELU1 ? (f > 1.f ? 1.f : f) : (f > 0.f ? 1.f : 0.f);
+}
+
+// z (fp32) into column d of a z tile as the rows (z_hi, z_lo, z_hi), z = z_hi + z_lo.
+template <int D>
+__device__ __forceinline__ void store_split_z(uint8_t *zt, int d, float z) {
+    const __nv_bfloat16 zh = __float2bfloat16_rn(z);
+    const __nv_bfloat16 zl = __float2bfloat16_rn(z - __bfloat162float(zh));
+    *reinterpret_cast<__nv_bfloat16 *>(zt + swz_offset(16, 0, d)) = zh;
+    *reinterpret_cast<__nv_bfloat16 *>(zt + swz_offset(16, 1, d)) = zl;
+    *reinterpret_cast<__nv_bfloat16 *>(zt + swz_offset(16, 2, d)) = zh;
+}
+
+// Eight dq values from eight phi_s = phi(q) / den (bf16) and the matching den * da (fp32):
+// dq = phi'(q) / den * (den da), with phi'(q) / den = min(phi_s, 1 / den) for elu+1
+// (phi' = min(phi, 1)) and 1 / den where phi_s > 0 for relu.
+template <bool ELU>
+__device__ __forceinline__ uint4 dq_piece(uint4 u, const float *x, float inv) {
+    const uint32_t *ui = reinterpret_cast<const uint32_t *>(&u);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = unpack_bf16x2(ui[q]);
+        const float m0 = ELU ? fminf(f.x, inv) : (f.x > 0.f ? inv : 0.f);
+        const float m1 = ELU ? fminf(f.y, inv) : (f.y > 0.f ? inv : 0.f);
+        w[q] = pack_bf16x2(m0 * x[2 * q], m1 * x[2 * q + 1]);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -74,23 +109,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
                                                               const __grid_constant__ CUtensorMap map_g,
                                                               const __grid_constant__ CUtensorMap map_dq, Params p) {
     using K = BwdCfg<D, G>;
-    constexpr int C = K::C, NS = K::NS;
+    constexpr int C = K::C, NS = K::NS_DQ;
     constexpr int OFF_K = K::Q_BYTES, OFF_V = OFF_K + K::K_BYTES, OFF_G = OFF_V + K::V_BYTES;
+    constexpr int HALF = D / 2;   // feature columns per pool half
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_full[NS], bar_ready[NS], bar_empty[NS], bar_dqready[NS];
-    __shared__ uint64_t bar_afull, bar_pready, bar_ofull, bar_gnready, bar_dafull, bar_dpready, bar_dqfull,
-        bar_dofree, bar_sfull, bar_sbf, bar_fin;
+    __shared__ uint64_t bar_fulla[NS], bar_fullg[NS], bar_ready[NS], bar_empty[NS], bar_dqready[NS][2];
+    __shared__ uint64_t bar_mfull, bar_sfull, bar_gnready, bar_dqfull, bar_xfree, bar_sbf, bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
     const uint32_t sm_lo = smem_u32(smem_raw), sm_hi = sm_lo + K::DQ_SMEM;
     (void)sm_lo;
     (void)sm_hi;
-    uint8_t *pbuf = stage0 + NS * K::STAGE;        // P, then dP
-    uint8_t *sbf = pbuf + K::P_BYTES;             // S_bf [D][D]
-    uint8_t *ztile = sbf + K::S_BYTES;            // z_bf: 16 x D, row 0 = z
-    uint8_t *ones = ztile + K::Z_BYTES;           // 16 x C, row 0 = 1
-    uint8_t *gdtile = ones + K::ONES_BYTES;       // 16 x 128, row 0 = gd over the query rows
+    uint8_t *pbuf = stage0 + NS * K::STAGE;       // dP' (query rows x keys)
+    uint8_t *sbf = pbuf + K::P_BYTES;            // S_bf [D][D]
+    // z and h enter the products as two-term bf16 splits (v = v_hi + v_lo): the z tile holds
+    // rows (z_hi, z_lo, z_hi) and the h tile rows (h_hi, h_hi, h_lo), so that one K = 16
+    // product gives h_hi z_hi + h_hi z_lo + h_lo z_hi, and phi(q) . z comes out as two
+    // columns (z_hi, z_lo) that are added in fp32
+    uint8_t *ztile = sbf + K::S_BYTES;           // two slots of 16 x D
+    uint8_t *ones = ztile + 2 * K::Z_BYTES;      // 16 x C, row 0 = 1
+    uint8_t *htile = ones + K::ONES_BYTES;       // 16 x 128 (query rows)
+    float *xch = reinterpret_cast<float *>(htile + K::H_BYTES);   // [2][128] partial row dots
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
@@ -103,29 +143,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
     float *rstate = p.rstate + seg_state;
 
     fill_ones_tile(ones, C);
-    for (int idx = threadIdx.x; idx < (K::Z_BYTES + K::GD_BYTES) / 16; idx += blockDim.x) {
-        uint8_t *t = idx < K::Z_BYTES / 16 ? ztile + idx * 16 : gdtile + (idx - K::Z_BYTES / 16) * 16;
+    for (int idx = threadIdx.x; idx < (2 * K::Z_BYTES + K::H_BYTES) / 16; idx += blockDim.x) {
+        uint8_t *t = idx < 2 * K::Z_BYTES / 16 ? ztile + idx * 16 : htile + (idx - 2 * K::Z_BYTES / 16) * 16;
         *reinterpret_cast<uint4 *>(t) = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async();
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_ready[s], 128);
-            mbar_init(&bar_empty[s], 2);
-            mbar_init(&bar_dqready[s], 128);
+            mbar_init(&bar_fulla[s], 1);
+            mbar_init(&bar_fullg[s], 1);
+            mbar_init(&bar_ready[s], 256);
+            mbar_init(&bar_empty[s], 1);
+            mbar_init(&bar_dqready[s][0], 128);
+            mbar_init(&bar_dqready[s][1], 128);
         }
-        mbar_init(&bar_afull, 1);
-        mbar_init(&bar_pready, 128);
-        mbar_init(&bar_ofull, 1);
-        mbar_init(&bar_gnready, 128);
-        mbar_init(&bar_dafull, 1);
-        mbar_init(&bar_dpready, 128);
-        mbar_init(&bar_dqfull, 1);
-        mbar_init(&bar_dofree, 128);
+        mbar_init(&bar_mfull, 1);
         mbar_init(&bar_sfull, 1);
-        mbar_init(&bar_sbf, 128);
+        mbar_init(&bar_gnready, 256);
+        mbar_init(&bar_dqfull, 1);
+        mbar_init(&bar_xfree, 256);
+        mbar_init(&bar_sbf, 256);
         mbar_init(&bar_fin, 1);
         fence_barrier_init();
     }
@@ -136,13 +174,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = tmem_base + K::T_S, tO = tmem_base + K::T_O, tA = tmem_base + K::T_A,
-                   tR = tmem_base + K::T_R;
+    const uint32_t tS = tmem_base + K::T_S, tDen = tmem_base + K::T_DEN, tA = tmem_base + K::T_A,
+                   tA2 = tmem_base + K::T_A2, tX = tmem_base + K::T_X, tR = tmem_base + K::T_R;
 
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer: K, Q (and V) on one barrier, grad_out on another
         if (lane == 0) {
-            constexpr uint32_t bytes = CAUSAL ? K::STAGE : K::Q_BYTES + K::G_BYTES;
+            constexpr uint32_t bytes_a = CAUSAL ? K::Q_BYTES + K::K_BYTES + K::V_BYTES : K::Q_BYTES;
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
@@ -153,116 +191,137 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
                               smem_u32(st) - sm_lo, c0))
                     break;
                 LA_TL(k, 0);
-                mbar_arrive_expect_tx(&bar_full[s], bytes);
-                for (int r = 0; r < G; ++r)
-                    for (int blk = 0; blk < K::DB; ++blk) {
-                        tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_full[s], blk * 64, c0, bh0 + r);
-                        tma_load_3d(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_full[s], blk * 64, c0,
-                                    bh0 + r);
-                    }
+                mbar_arrive_expect_tx(&bar_fulla[s], bytes_a);
                 if (CAUSAL)
-                    for (int blk = 0; blk < K::DB; ++blk) {
-                        tma_load_3d(st + OFF_K + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
-                        tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
-                    }
+                    for (int blk = 0; blk < K::DB; ++blk)
+                        tma_load_3d(st + OFF_K + blk * C * 128, &map_k, &bar_fulla[s], blk * 64, c0, bg);
+                for (int r = 0; r < G; ++r)
+                    for (int blk = 0; blk < K::DB; ++blk)
+                        tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fulla[s], blk * 64, c0, bh0 + r);
+                if (CAUSAL)
+                    for (int blk = 0; blk < K::DB; ++blk)
+                        tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_fulla[s], blk * 64, c0, bg);
+                mbar_arrive_expect_tx(&bar_fullg[s], K::G_BYTES);
+                for (int r = 0; r < G; ++r)
+                    for (int blk = 0; blk < K::DB; ++blk)
+                        tma_load_3d(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64, c0,
+                                    bh0 + r);
                 issued = k + 1;
             }
-            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) mbar_drain(&bar_full[k % NS], (k / NS) & 1);
+            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) {
+                mbar_drain(&bar_fulla[k % NS], (k / NS) & 1);
+                mbar_drain(&bar_fullg[k % NS], (k / NS) & 1);
+            }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer.  Iteration k finishes chunk k - 1 (da, R, r) and
+        // starts chunk k (A, den, X, dA', then the state update).  Products that share an
+        // A operand are issued back to back so that A is read from shared memory once.
         if (lane == 0) {
             constexpr uint32_t idA = idesc_bf16(128, C, false, false);
-            constexpr uint32_t idO = idesc_bf16(128, D, false, true);
-            constexpr uint32_t idOK = idesc_bf16(128, D, false, false);
-            constexpr uint32_t idGZ = idesc_bf16(128, D, true, true);
+            constexpr uint32_t idX = idesc_bf16(128, D, false, false);
+            constexpr uint32_t idDK = idesc_bf16(128, D, false, true);
+            constexpr uint32_t idHZ = idesc_bf16(128, D, true, true);
             constexpr uint32_t id16 = idesc_bf16(128, 16, false, false);
             constexpr uint32_t idR = idesc_bf16(128, D, true, true);
             constexpr uint32_t idR16 = idesc_bf16(128, 16, true, false);
-            const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf), zt = smem_u32(ztile), on = smem_u32(ones),
-                           gdt = smem_u32(gdtile);
-            for (int k = 0; k < nchunk; ++k) {
+            const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf), on = smem_u32(ones), ht = smem_u32(htile);
+            for (int k = 0; k <= nchunk; ++k) {
+                if (k > 0) {
+                    const int kp = k - 1, sp = kp % NS;
+                    if (!mbar_wait(&bar_gnready, kp & 1, &abort_flag)) break;
+                    LA_TL(kp, 5);
+                    tc_fence_after();
+                    const uint32_t qs = smem_u32(stage0 + sp * K::STAGE), ks_ = qs + OFF_K, gs = qs + OFF_G;
+                    // X += dP' phi(K) + h z^T   (X becomes den * da)
+                    const uint32_t zt = smem_u32(ztile + (CAUSAL ? (kp & 1) : 0) * K::Z_BYTES);
+                    if (CAUSAL)
+                        for (int kk = 0; kk < C / 16; ++kk)
+                            mma_bf16(tX, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(ks_, C, 0, kk), idDK, 1u);
+                    mma_bf16(tX, desc_mnmajor(ht, 16, 0, 0), desc_mnmajor(zt, 16, 0, 0), idHZ, 1u);
+                    // R += phi_s^T g, r += phi_s^T h  (phi_s = phi(Q) / den)
+                    for (int kk = 0; kk < 128 / 16; ++kk) {
+                        const uint32_t acc = (kp > 0 || kk > 0) ? 1u : 0u;
+                        const uint64_t as = desc_mnmajor(qs, 128, 0, kk);
+                        mma_bf16_fill(tR, as, desc_mnmajor(gs, 128, 0, kk), idR, acc);
+                        mma_bf16_lastuse(tR + D, as, desc_kmajor(ht, 16, 0, kk), idR16, acc);
+                    }
+                    mma_commit(&bar_dqfull);
+                }
+                if (k == nchunk) break;
                 const int s = k % NS;
                 if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
+                if (!mbar_wait(&bar_fullg[s], (k / NS) & 1, &abort_flag)) break;
+                if ((CAUSAL || k == 0) && !mbar_wait(&bar_sbf, k & 1, &abort_flag)) break;
                 LA_TL(k, 3);
                 tc_fence_after();
                 const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V, gs = qs + OFF_G;
-                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && gdt + K::GD_BYTES <= sm_hi, 311, qs - sm_lo, k))
+                const uint32_t zt = smem_u32(ztile + (CAUSAL ? (k & 1) : 0) * K::Z_BYTES);
+                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && ht + K::H_BYTES <= sm_hi, 311, qs - sm_lo, k))
                     break;
-                if (CAUSAL) {
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_bf16(tA, desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
-                    mma_commit(&bar_afull);
-                    if (!mbar_wait(&bar_pready, k & 1, &abort_flag)) break;
+                // A = phi(Q) phi(K)^T and den = phi(Q) z share phi(Q)
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t aq = desc_kmajor(qs, 128, 0, kk);
+                    if (CAUSAL) {
+                        mma_bf16_fill(tA, aq, desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                        mma_bf16_lastuse(tDen, aq, desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
+                    } else {
+                        mma_bf16(tDen, aq, desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
+                    }
                 }
-                if ((CAUSAL || k == 0) && !mbar_wait(&bar_sbf, k & 1, &abort_flag)) break;
-                if (k > 0 && !mbar_wait(&bar_dofree, (k - 1) & 1, &abort_flag)) break;
+                if (k > 0 && !mbar_wait(&bar_xfree, (k - 1) & 1, &abort_flag)) break;
                 LA_TL(k, 4);
                 tc_fence_after();
-                // O = phi(Q) S_bf (+ P V);  den = phi(Q) z_bf (+ P 1)
+                // X = g S_bf^T and dA' = g V^T share g
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    mma_bf16(tO, desc_kmajor(qs, 128, 0, kk), desc_mnmajor(sbf_u, D, 0, kk), idO, kk > 0 ? 1u : 0u);
-                    mma_bf16(tO + D, desc_kmajor(qs, 128, 0, kk), desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
-                }
-                if (CAUSAL)
-                    for (int kk = 0; kk < C / 16; ++kk) {
-                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(vs, C, 0, kk), idO, 1u);
-                        mma_bf16(tO + D, desc_kmajor(pb, 128, 0, kk), desc_kmajor(on, 16, 0, kk), id16, 1u);
+                    const uint64_t ag = desc_kmajor(gs, 128, 0, kk);
+                    if (CAUSAL) {
+                        mma_bf16_fill(tX, ag, desc_kmajor(sbf_u, D, 0, kk), idX, kk > 0 ? 1u : 0u);
+                        mma_bf16_lastuse(tA2, ag, desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                    } else {
+                        mma_bf16(tX, ag, desc_kmajor(sbf_u, D, 0, kk), idX, kk > 0 ? 1u : 0u);
                     }
-                mma_commit(&bar_ofull);
-                if (!mbar_wait(&bar_gnready, k & 1, &abort_flag)) break;
-                LA_TL(k, 5);
-                tc_fence_after();
-                if (CAUSAL) {
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_bf16(tA, desc_kmajor(gs, 128, 0, kk), desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : 0u);
-                    mma_commit(&bar_dafull);
-                    if (!mbar_wait(&bar_dpready, k & 1, &abort_flag)) break;
-                    tc_fence_after();
                 }
-                LA_TL(k, 6);
-                // da = (dP phi(K)) + gn S_bf^T + gd z^T
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tO, desc_kmajor(gs, 128, 0, kk), desc_kmajor(sbf_u, D, 0, kk), idOK, kk > 0 ? 1u : 0u);
-                mma_bf16(tO, desc_mnmajor(gdt, 16, 0, 0), desc_mnmajor(zt, 16, 0, 0), idGZ, 1u);
-                if (CAUSAL)
-                    for (int kk = 0; kk < C / 16; ++kk)
-                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(ks_, C, 0, kk), idO, 1u);
-                // R += phi(Q)^T gn, r += phi(Q)^T gd
-                for (int kk = 0; kk < 128 / 16; ++kk) {
-                    const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
-                    mma_bf16(tR, desc_mnmajor(qs, 128, 0, kk), desc_mnmajor(gs, 128, 0, kk), idR, acc);
-                    mma_bf16(tR + D, desc_mnmajor(qs, 128, 0, kk), desc_kmajor(gdt, 16, 0, kk), idR16, acc);
-                }
-                mma_commit(&bar_dqfull);
-                if (CAUSAL) {
+                mma_commit(&bar_mfull);
+                if (CAUSAL) {   // S += phi(K)^T V, z += phi(K)^T 1 (one read of phi(K))
                     for (int kk = 0; kk < C / 16; ++kk) {
-                        mma_bf16(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs, C, 0, kk), idR, 1u);
-                        mma_bf16(tS + D, desc_mnmajor(ks_, C, 0, kk), desc_kmajor(on, 16, 0, kk), idR16, 1u);
+                        const uint64_t ak = desc_mnmajor(ks_, C, 0, kk);
+                        mma_bf16_fill(tS, ak, desc_mnmajor(vs, C, 0, kk), idR, 1u);
+                        mma_bf16_lastuse(tS + D, ak, desc_kmajor(on, 16, 0, kk), idR16, 1u);
                     }
                     mma_commit(&bar_sfull);
                 }
-                mma_commit(&bar_empty[s]);
-                LA_TL(k, 7);
+                LA_TL(k, 6);
             }
             mma_commit(&bar_fin);
             mbar_drain(&bar_fin, 0);
         }
     } else if (warp == 2) {
-        // ---------------- dq store: the epilogue leaves dq over the grad_out tile; TMA writes
-        // it out, and the stage is released once the copy has read it
+        // ---------------- dq store: each pool half leaves its D/2 columns of dq over the
+        // phi_s tile; TMA writes them out, and the stage is released once the copies have
+        // read it
         if (lane == 0) {
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
-                const bool ok = mbar_wait(&bar_dqready[s], (k / NS) & 1, &abort_flag);
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
+                bool ok = true;
+                // with D = 128 each half is one 64-column block and goes out on its own;
+                // with D = 64 both halves share the block
+                for (int hh = 0; hh < 2; ++hh) {
+                    ok = ok && mbar_wait(&bar_dqready[s][hh], (k / NS) & 1, &abort_flag);
+                    if (!ok) break;
+                    if (hh == 0) LA_TL(k, 13);
+                    if (K::DB == 2 || hh == 1) {
+                        const int blk = K::DB == 2 ? hh : 0;
+                        for (int r = 0; r < G; ++r)
+                            tma_store_3d(&map_dq, st + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
+                    }
+                }
                 if (ok) {
-                    for (int r = 0; r < G; ++r)
-                        for (int blk = 0; blk < K::DB; ++blk)
-                            tma_store_3d(&map_dq, st + OFF_G + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
                     bulk_commit();
                     bulk_wait_read();
+                    LA_TL(k, 14);
                 }
                 mbar_arrive(&bar_empty[s]);
                 if (!ok) break;
@@ -270,250 +329,239 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
             bulk_wait_all();
         }
     } else if ((warp >= 4 && warp < 8) || warp >= 16) {
-        // ---------------- phi prologue (in place on phi(Q) and phi(K)); alternate chunks
-        const int pg = warp >= 16 ? 1 : 0;
-        const int i = threadIdx.x - (pg ? 512 : 128);
-        bool ok = true;
-        for (int k = pg; k < nchunk; k += 2) {
-            const int s = k % NS;
-            ok = ok && warp_wait(&bar_full[s], (k / NS) & 1, &abort_flag);
-            if (i == 0) LA_TL(k, 1);
-            if (ok) {
-                uint8_t *st = stage0 + s * K::STAGE;
-                const int c0 = t0 + k * C;
-                const bool qvalid = c0 + (i % C) < t1;
-#pragma unroll 4
-                for (int c = 0; c < D / 8; ++c) {
-                    uint8_t *ch = st + swz_chunk(128, i, c);
-                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 321, smem_u32(ch) - sm_lo, c))
-                        feat8_inplace2(ch, qvalid, p.phi);
-                }
-                if (CAUSAL)
-#pragma unroll 2
-                    for (int idx = i; idx < C * (D / 8); idx += 128) {
-                        const int j = idx / (D / 8), c = idx % (D / 8);
-                        uint8_t *ch = st + OFF_K + swz_chunk(C, j, c);
-                        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 322, smem_u32(ch) - sm_lo, idx))
-                            feat8_inplace2(ch, c0 + j < t1, p.phi);
-                    }
-                fence_proxy_async();
-            }
-            if (i == 0) LA_TL(k, 2);
-            mbar_arrive(&bar_ready[s]);
-        }
-    } else if (warp >= 8 && warp < 12) {
-        // ---------------- row work (thread = query row i): P, gn over the grad_out tile, gd, dP
-        const int i = threadIdx.x - 256;
-        const int wq = warp % 4;
-        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const int r = i / C, ti = i % C;
-        const int bh = bh0 + r;
+        // ---------------- phi prologue, in place on phi(Q) and phi(K): both warpgroups share
+        // every chunk (16-byte pieces dealt round-robin)
+        const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0..255
+        // thread pi owns 16-byte column piece c of rows r0, r0 + RPP, ...; RPP is a multiple
+        // of 8, so the piece's swizzled position is the same in all of them
+        constexpr int CPR = D / 8, RPP = 256 / CPR;
+        static_assert(RPP % 8 == 0, "rows per pass");
+        const int c = pi % CPR, r0 = pi / CPR;
+        const uint32_t pos = (uint32_t)(((c & 7) ^ (r0 & 7)) << 4);
+        const uint32_t offq = (uint32_t)(c >> 3) * 128u * 128u + pos, offk = (uint32_t)(c >> 3) * C * 128u + pos;
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
-            const int t = t0 + k * C + ti;
-            const bool valid = t < t1;
-            uint8_t *st = stage0 + s * K::STAGE;
-            if (CAUSAL) {
-                ok = ok && warp_wait(&bar_afull, k & 1, &abort_flag);
-                tc_fence_after();
-                if (i == 0) LA_TL(k, 8);
-                if (ok) {
-#pragma unroll
-                    for (int c32 = 0; c32 < (C + 31) / 32; ++c32) {
-                        float v[32];
-                        if (C >= 32) tmem_ld32(tA + lane_off + c32 * 32, v);
-                        else tmem_ld16(tA + lane_off, v);
-                        tmem_wait_regs<(C >= 32 ? 32 : 16)>(v);
-#pragma unroll
-                        for (int h = 0; h < (C >= 32 ? 2 : 1); ++h) {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int e = 0; e < 16; e += 2) {
-                                const int j = c32 * 32 + h * 16 + e;
-                                w[e / 2] = pack_bf16x2((j <= ti) ? v[h * 16 + e] : 0.f,
-                                                       (j + 1 <= ti) ? v[h * 16 + e + 1] : 0.f);
-                            }
-                            const int c16 = c32 * 2 + h;
-                            uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
-                            if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 331,
-                                         smem_u32(p0) - sm_lo, c16)) {
-                                *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
-                                *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
-                            }
-                        }
-                    }
-                    fence_proxy_async();
-                }
-                tc_fence_before();
-                mbar_arrive(&bar_pready);
-            }
-            // num, den -> gn (over the grad_out tile), gd
-            ok = ok && warp_wait(&bar_ofull, k & 1, &abort_flag);
-            tc_fence_after();
-            if (i == 0) LA_TL(k, 9);
-            float gd = 0.f;
+            ok = ok && warp_wait(&bar_fulla[s], (k / NS) & 1, &abort_flag);
+            if (pi == 0) LA_TL(k, 1);
             if (ok) {
-                float den = tmem_ld1(tO + lane_off + D);
-                tmem_wait_regs<1>(&den);
-                den += p.eps;
-                const float inv = 1.f / den;
-                float gdot = 0.f;
-#pragma unroll
-                for (int c64 = 0; c64 < D / 64; ++c64) {
-                    float v[64];
-                    tmem_ld32(tO + lane_off + c64 * 64, v);
-                    tmem_ld32(tO + lane_off + c64 * 64 + 32, v + 32);
-                    tmem_wait_regs<64>(v);
-#pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        uint8_t *ch = st + OFF_G + swz_chunk(128, i, c64 * 8 + q8);
-                        uint4 x = *reinterpret_cast<uint4 *>(ch);
-                        uint32_t *xi = reinterpret_cast<uint32_t *>(&x);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 gv = unpack_bf16x2(xi[q]);
-                            gdot += gv.x * v[q8 * 8 + 2 * q] + gv.y * v[q8 * 8 + 2 * q + 1];
-                            xi[q] = valid ? pack_bf16x2(gv.x * inv, gv.y * inv) : 0u;
-                        }
-                        *reinterpret_cast<uint4 *>(ch) = x;
+                uint8_t *st = stage0 + s * K::STAGE;
+                const int c0 = t0 + k * C;
+                const int nvalid = t1 - c0;   // tokens of this chunk inside the segment
+#pragma unroll 4
+                for (int row = r0; row < 128; row += RPP) {
+                    uint8_t *ch = st + offq + row * 128;
+                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 321, smem_u32(ch) - sm_lo, row))
+                        feat8_inplace2(ch, row % C < nvalid, p.phi);
+                }
+                if (CAUSAL)
+                    for (int j = r0; j < C; j += RPP) {
+                        uint8_t *ch = st + OFF_K + offk + j * 128;
+                        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 322, smem_u32(ch) - sm_lo, j))
+                            feat8_inplace2(ch, j < nvalid, p.phi);
                     }
-                }
-                gd = valid ? -gdot * inv * inv : 0.f;
-                *reinterpret_cast<__nv_bfloat16 *>(gdtile + swz_offset(16, 0, i)) = __float2bfloat16_rn(gd);
-                if (valid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 334, bh, t)) {
-                    p.den[(size_t)bh * p.N + t] = den;
-                    p.gd[(size_t)bh * p.N + t] = gd;
-                }
                 fence_proxy_async();
             }
-            tc_fence_before();
-            if (i == 0) LA_TL(k, 12);
-            mbar_arrive(&bar_gnready);
-            if (CAUSAL) {   // dP = mask(dA + gd), into the P buffer (P was consumed by the O product)
-                ok = ok && warp_wait(&bar_dafull, k & 1, &abort_flag);
-                tc_fence_after();
-                if (ok) {
-#pragma unroll
-                    for (int c32 = 0; c32 < (C + 31) / 32; ++c32) {
-                        float v[32];
-                        if (C >= 32) tmem_ld32(tA + lane_off + c32 * 32, v);
-                        else tmem_ld16(tA + lane_off, v);
-                        tmem_wait_regs<(C >= 32 ? 32 : 16)>(v);
-#pragma unroll
-                        for (int h = 0; h < (C >= 32 ? 2 : 1); ++h) {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int e = 0; e < 16; e += 2) {
-                                const int j = c32 * 32 + h * 16 + e;
-                                w[e / 2] = pack_bf16x2((j <= ti) ? v[h * 16 + e] + gd : 0.f,
-                                                       (j + 1 <= ti) ? v[h * 16 + e + 1] + gd : 0.f);
-                            }
-                            const int c16 = c32 * 2 + h;
-                            uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
-                            if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 335,
-                                         smem_u32(p0) - sm_lo, c16)) {
-                                *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
-                                *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
-                            }
-                        }
-                    }
-                    fence_proxy_async();
-                }
-                tc_fence_before();
-                if (i == 0) LA_TL(k, 13);
-                mbar_arrive(&bar_dpready);
-            }
+            if (pi == 0) LA_TL(k, 2);
+            mbar_arrive_warp(&bar_ready[s]);
         }
-    } else if (warp >= 12 && warp < 16) {
-        // ---------------- dq epilogue (thread = query row i) and state conversion (thread = d)
-        const int i = threadIdx.x - 384;
+    } else if (warp >= 8 && warp < 16) {
+        // ---------------- row pool: two warpgroups, thread = query row i (TMEM lane), each
+        // half owning D/2 feature columns.  Per chunk: row work, state conversion, dq.
+        const int h = (warp - 8) / 4;
         const int wq = warp % 4;
+        const int i = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        // initial S, z of the segment: TMEM (causal) and the bf16 operand tiles
+        const int r = i / C, ti = i % C;
+        const int bh = bh0 + r;
+        // initial S, z of the segment: TMEM (causal) and the operand tiles (slot 0)
         if (wq * 32 < D) {
             const float *row = state + (size_t)i * (D + 1);
 #pragma unroll 1
-            for (int c16 = 0; c16 < D / 16; ++c16) {
+            for (int c16 = h * (HALF / 16); c16 < (h + 1) * (HALF / 16); ++c16) {
                 float v[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) v[e] = row[c16 * 16 + e];
                 if (CAUSAL) tmem_st16(tS + lane_off + c16 * 16, v);
                 store_state_row<D>(sbf, i, v, c16);
             }
-            float zv[16];
-            zv[0] = row[D];
+            if (h == 0) {
+                float zv[16];
+                zv[0] = row[D];
 #pragma unroll
-            for (int e = 1; e < 16; ++e) zv[e] = 0.f;
-            if (CAUSAL) {
-                tmem_st16(tS + lane_off + D, zv);
-                tmem_st_wait();
+                for (int e = 1; e < 16; ++e) zv[e] = 0.f;
+                if (CAUSAL) tmem_st16(tS + lane_off + D, zv);
+                store_split_z<D>(ztile, i, zv[0]);
             }
-            *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zv[0]);
+            if (CAUSAL) tmem_st_wait();
         }
         fence_proxy_async();
         tc_fence_before();
-        mbar_arrive(&bar_sbf);
+        mbar_arrive_warp(&bar_sbf);
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
+            const int t = t0 + k * C + ti;
+            const bool valid = t < t1;
             uint8_t *st = stage0 + s * K::STAGE;
-            ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
+            // ---- row work: den, phi_s = phi(q) / den in place, g . num, h, dP'
+            ok = ok && warp_wait(&bar_mfull, k & 1, &abort_flag);
             tc_fence_after();
-            if (i == 0) LA_TL(k, 10);
-            // dq = phi'(q) * da, written over the (dead) gn tile, then stored by TMA
+            if (i == 0 && h == 0) LA_TL(k, 7);
+            float inv = 0.f, hval = 0.f, den = 1.f;
             if (ok) {
+                float dz[2];   // phi(q) . z_hi, phi(q) . z_lo
+                tmem_ld2(tDen + lane_off, dz);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};   // g . num partials
+                if (CAUSAL) {
+                    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int c16 = 0; c16 < C / 16; ++c16) {
+                        float va[16], vd[16];
+                        tmem_ld16(tA + lane_off + c16 * 16, va);
+                        if (h == 0) tmem_ld16(tA2 + lane_off + c16 * 16, vd);
+                        tmem_wait_regs<16>(va);
+                        if (h == 0) {
+                            tmem_wait_regs<16>(vd);
 #pragma unroll
-                for (int c64 = 0; c64 < D / 64; ++c64) {
-                    float v[64];
-                    tmem_ld32(tO + lane_off + c64 * 64, v);
-                    tmem_ld32(tO + lane_off + c64 * 64 + 32, v + 32);
-                    tmem_wait_regs<64>(v);
+                            for (int e = 0; e < 16; ++e) {
+                                const float a = (c16 * 16 + e <= ti) ? va[e] : 0.f;
+                                rs[e & 3] += a;
+                                acc[e & 3] = fmaf(a, vd[e], acc[e & 3]);
+                            }
+                        } else {
 #pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        const uint4 x = *reinterpret_cast<const uint4 *>(st + swz_chunk(128, i, c64 * 8 + q8));
-                        const uint32_t *xi = reinterpret_cast<const uint32_t *>(&x);
-                        uint32_t w[4];
+                            for (int e = 0; e < 16; ++e) rs[e & 3] += (c16 * 16 + e <= ti) ? va[e] : 0.f;
+                        }
+                    }
+                    tmem_wait_regs<2>(dz);
+                    den = (dz[0] + dz[1]) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+                } else {
+                    tmem_wait_regs<2>(dz);
+                    den = dz[0] + dz[1];
+                }
+                den += p.eps;
+                inv = 1.f / den;
+                // X in 16-column pieces, the next piece loading while this one is used
+                float xb[2][16];
+                tmem_ld16(tX + lane_off + h * HALF, xb[0]);
+#pragma unroll
+                for (int c16 = 0; c16 < HALF / 16; ++c16) {
+                    const int col0 = h * HALF + c16 * 16;
+                    float *xv = xb[c16 & 1];
+                    tmem_wait_regs<16>(xv);
+                    if (c16 + 1 < HALF / 16) tmem_ld16(tX + lane_off + col0 + 16, xb[(c16 + 1) & 1]);
+#pragma unroll
+                    for (int q8 = 0; q8 < 2; ++q8) {
+                        uint8_t *ch = st + swz_chunk(128, i, col0 / 8 + q8);
+                        if (!LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 331, smem_u32(ch) - sm_lo, col0)) continue;
+                        uint4 u = *reinterpret_cast<uint4 *>(ch);
+                        uint32_t *ui = reinterpret_cast<uint32_t *>(&u);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const float2 f = unpack_bf16x2(xi[q]);
-                            w[q] = pack_bf16x2(feat_grad_from_feat(f.x, p.phi) * v[q8 * 8 + 2 * q],
-                                               feat_grad_from_feat(f.y, p.phi) * v[q8 * 8 + 2 * q + 1]);
+                            const float2 f = unpack_bf16x2(ui[q]);
+                            acc[q] = fmaf(f.x, xv[q8 * 8 + 2 * q], acc[q]);
+                            acc[q] = fmaf(f.y, xv[q8 * 8 + 2 * q + 1], acc[q]);
+                            ui[q] = pack_bf16x2(f.x * inv, f.y * inv);
                         }
-                        *reinterpret_cast<uint4 *>(st + OFF_G + swz_chunk(128, i, c64 * 8 + q8)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4 *>(ch) = u;
                     }
                 }
+                xch[h * 128 + i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            }
+            named_barrier(3, 256);
+            if (ok) {
+                const float gdot = xch[i] + xch[128 + i];
+                hval = valid ? -gdot * inv : 0.f;
+                if (CAUSAL)
+                    for (int c16 = h; c16 < C / 16; c16 += 2) {
+                        float vd[16];
+                        tmem_ld16(tA2 + lane_off + c16 * 16, vd);
+                        tmem_wait_regs<16>(vd);
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            const int j = c16 * 16 + e;
+                            w[e / 2] = pack_bf16x2((j <= ti) ? vd[e] + hval : 0.f, (j + 1 <= ti) ? vd[e + 1] + hval : 0.f);
+                        }
+                        uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
+                        if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 335,
+                                     smem_u32(p0) - sm_lo, c16)) {
+                            *reinterpret_cast<uint4 *>(p0) = make_uint4(w[0], w[1], w[2], w[3]);
+                            *reinterpret_cast<uint4 *>(p1) = make_uint4(w[4], w[5], w[6], w[7]);
+                        }
+                    }
+                if (h == 0) {
+                    const __nv_bfloat16 hh = __float2bfloat16_rn(hval);
+                    const __nv_bfloat16 hl = __float2bfloat16_rn(hval - __bfloat162float(hh));
+                    *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 0, i)) = hh;
+                    *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 1, i)) = hh;
+                    *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 2, i)) = hl;
+                    if (valid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 334, bh, t)) {
+                        p.den[(size_t)bh * p.N + t] = den;
+                        p.gd[(size_t)bh * p.N + t] = hval * inv;
+                    }
+                }
+                fence_proxy_async();
             }
             tc_fence_before();
-            mbar_arrive(&bar_dofree);
-            fence_proxy_async();
-            if (i == 0) LA_TL(k, 14);
-            mbar_arrive(&bar_dqready[s]);
-            // S, z after chunk k -> operand tiles for chunk k + 1
+            if (i == 0 && h == 0) LA_TL(k, 8);
+            mbar_arrive_warp(&bar_gnready);
+            // ---- S, z after chunk k -> operand tiles for chunk k + 1
             if (CAUSAL) {
                 ok = ok && warp_wait(&bar_sfull, k & 1, &abort_flag);
                 tc_fence_after();
-                if (i == 0) LA_TL(k, 11);
+                if (i == 0 && h == 0) LA_TL(k, 9);
                 if (ok && wq * 32 < D) {
 #pragma unroll
-                    for (int c64 = 0; c64 < D / 64; ++c64) {
-                        float v[64];
-                        tmem_ld32(tS + lane_off + c64 * 64, v);
-                        tmem_ld32(tS + lane_off + c64 * 64 + 32, v + 32);
-                        tmem_wait_regs<64>(v);
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) store_state_row<D>(sbf, i, v + 16 * h, c64 * 4 + h);
+                    for (int c16 = 0; c16 < HALF / 16; ++c16) {
+                        float v[16];
+                        tmem_ld16(tS + lane_off + h * HALF + c16 * 16, v);
+                        tmem_wait_regs<16>(v);
+                        store_state_row<D>(sbf, i, v, (h * HALF) / 16 + c16);
                     }
-                    float zd = tmem_ld1(tS + lane_off + D);
-                    tmem_wait_regs<1>(&zd);
-                    *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zd);
+                    if (h == 0) {
+                        float zd = tmem_ld1(tS + lane_off + D);
+                        tmem_wait_regs<1>(&zd);
+                        store_split_z<D>(ztile + ((k + 1) & 1) * K::Z_BYTES, i, zd);
+                    }
                 }
                 fence_proxy_async();
                 tc_fence_before();
-                if (i == 0) LA_TL(k, 15);
-                mbar_arrive(&bar_sbf);
+                if (i == 0 && h == 0) LA_TL(k, 10);
+                mbar_arrive_warp(&bar_sbf);
             }
+            // ---- dq = phi'(q) / den * (den da), written over the phi_s tile for the TMA store
+            ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
+            tc_fence_after();
+            if (i == 0 && h == 0) LA_TL(k, 11);
+            float xb[2][16];
+            if (ok) tmem_ld16(tX + lane_off + h * HALF, xb[0]);
+#pragma unroll
+            for (int c16 = 0; c16 < HALF / 16; ++c16) {
+                const int col0 = h * HALF + c16 * 16;
+                float *xv = xb[c16 & 1];
+                if (ok) {
+                    tmem_wait_regs<16>(xv);
+                    if (c16 + 1 < HALF / 16) tmem_ld16(tX + lane_off + col0 + 16, xb[(c16 + 1) & 1]);
+                }
+                if (c16 + 1 == HALF / 16) {   // every column of X is in registers
+                    tc_fence_before();
+                    mbar_arrive_warp(&bar_xfree);
+                }
+                if (!ok) continue;
+#pragma unroll
+                for (int q8 = 0; q8 < 2; ++q8) {
+                    uint8_t *ch = st + swz_chunk(128, i, col0 / 8 + q8);
+                    if (!LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 341, smem_u32(ch) - sm_lo, q8)) continue;
+                    uint4 *cp = reinterpret_cast<uint4 *>(ch);
+                    *cp = p.phi == LA_PHI_ELU1 ? dq_piece<true>(*cp, xv + q8 * 8, inv)
+                                               : dq_piece<false>(*cp, xv + q8 * 8, inv);
+                }
+            }
+            fence_proxy_async();
+            if (i == 0 && h == 0) LA_TL(k, 12);
+            mbar_arrive_warp(&bar_dqready[s][h]);
         }
         // the segment's R, r -> workspace
         ok = ok && warp_wait(&bar_fin, 0, &abort_flag);
@@ -521,16 +569,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
         if (ok && wq * 32 < D) {
             float *row = rstate + (size_t)i * (D + 1);
 #pragma unroll 1
-            for (int c16 = 0; c16 < D / 16; ++c16) {
+            for (int c16 = h * (HALF / 16); c16 < (h + 1) * (HALF / 16); ++c16) {
                 float v[16];
                 tmem_ld16(tR + lane_off + c16 * 16, v);
                 tmem_wait_regs<16>(v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) row[c16 * 16 + e] = v[e];
             }
-            float rd = tmem_ld1(tR + lane_off + D);
-            tmem_wait_regs<1>(&rd);
-            row[D] = rd;
+            if (h == 0) {
+                float rd[16];   // r = phi_s^T h_hi (column 0) + phi_s^T h_lo (column 2)
+                tmem_ld16(tR + lane_off + D, rd);
+                tmem_wait_regs<16>(rd);
+                row[D] = rd[0] + rd[2];
+            }
         }
     }
     tc_fence_before();
@@ -721,7 +772,7 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                 }
                 fence_proxy_async();
             }
-            mbar_arrive(&bar_ready[s]);
+            mbar_arrive_warp(&bar_ready[s]);
         }
     } else if (warp >= 8 && warp < 12) {
         // ---------------- P / dP conversion (thread = query row) and the dk, dv epilogue
@@ -771,7 +822,7 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                     fence_proxy_async();
                 }
                 tc_fence_before();
-                mbar_arrive(&bar_pready);
+                mbar_arrive_warp(&bar_pready);
             }
             ok = ok && warp_wait(&bar_outfull, k & 1, &abort_flag);
             tc_fence_after();
@@ -799,13 +850,13 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bar_outfree);
+            mbar_arrive_warp(&bar_outfree);
             if (CAUSAL && ok && d < D) {   // this chunk's rows join r for the earlier chunks
                 const float *gsd = gds + s * 128;
                 for (int row = 0; row < 128; ++row)
                     r_d += gsd[row] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(st + swz_offset(128, row, d)));
             }
-            mbar_arrive(&bar_empty[s]);
+            mbar_arrive_warp(&bar_empty[s]);
         }
     } else if (warp >= 12) {
         // ---------------- R conversion: TMEM R (fp32) -> R_bf (bf16 operand tile)
@@ -830,7 +881,7 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
         }
         fence_proxy_async();
         tc_fence_before();
-        mbar_arrive(&bar_rbf);
+        mbar_arrive_warp(&bar_rbf);
         if (CAUSAL) {
             bool ok = true;
             for (int k = 0; k < nchunk; ++k) {
@@ -852,7 +903,7 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
                 }
                 fence_proxy_async();
                 tc_fence_before();
-                mbar_arrive(&bar_rbf);
+                mbar_arrive_warp(&bar_rbf);
             }
         }
     }

@@ -46,14 +46,30 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival of weight `count` (for a warp that arrives as a unit).
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Warp-wide arrival, called by all 32 lanes: the lanes synchronise (which orders their
+// earlier memory operations before lane 0's release) and lane 0 arrives for all of them,
+// so the barrier's expected count stays in threads.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31u) == 0u) mbar_arrive_cnt(bar, 32u);
+}
+
+// Test the phase; the thread may be suspended inside for up to kSuspendNs waiting for it,
+// so that waiting warps do not spin on the issue slots.
+constexpr uint32_t kSuspendNs = 200000u;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return done != 0;
 }
@@ -69,14 +85,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0u) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitNs) {
-                *abort = 1;
-                return false;
-            }
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) {
+            *abort = 1;
+            return false;
         }
     }
 }
@@ -191,6 +205,30 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// The same MMA with the A operand kept in the collector buffer for the next MMA
+// (`fill`), or taken from it and released (`lastuse`): two consecutive MMAs that share A
+// read it from shared memory once.  The A descriptor of the `lastuse` MMA must describe
+// the same matrix as the `fill` before it, with the same major-ness.
+__device__ __forceinline__ void mma_bf16_fill(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16.collector::a::fill [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_lastuse(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16.collector::a::lastuse [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on *bar when every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -217,6 +255,14 @@ __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
     uint32_t r;
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
     return __uint_as_float(r);
+}
+
+// Warp-wide: thread t gets TMEM lane (lane of taddr) + t, two consecutive columns.
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, float *v) {
+    uint32_t r0, r1;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
+    v[0] = __uint_as_float(r0);
+    v[1] = __uint_as_float(r1);
 }
 
 // Warp-wide: thread t gets TMEM lane (lane of taddr) + t, 32 consecutive 32-bit columns.

@@ -4,7 +4,12 @@
 // tcgen05.ld back out.  One CTA computes D[m][n] = sum_k A(m, k) B(n, k) for M = 128.
 //
 // A is given row-major as [M][K] (K-major) or [K][M] (MN-major); B as [N][K] (K-major)
-// or [K][N] (MN-major).  Built by tests/test_gpu_tc_layouts.py into tests/_build.
+// or [K][N] (MN-major).  With `collector` = 1 every K step is issued twice, first with A
+// kept in the collector buffer and then taking A from it, into two accumulators (D is
+// then [M][2N]: both halves must equal A B^T); with `collector` = 2 the second MMA has
+// N = 16 and takes the first 16 rows (n) of B (D is [M][N + 16]).  `dcol` places the
+// accumulator at that TMEM column of a 512-column allocation.  Built by
+// tests/test_gpu_tc_layouts.py into tests/_build.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -22,7 +27,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
                                                     const __grid_constant__ CUtensorMap map_b,
                                                     const __nv_bfloat16 *a_src, const __nv_bfloat16 *b_src,
                                                     float *d, int N, int K, int a_mn, int b_mn, int a_manual,
-                                                    int b_manual, int *err) {
+                                                    int b_manual, int collector, int dcol, int *err) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[2];
     __shared__ uint32_t tmem_slot;
@@ -35,7 +40,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
     uint8_t *tile_a = smem;
     uint8_t *tile_b = smem + nblk_a * rows_a * 128;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t ncols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
+    const uint32_t ncols = 512;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -50,7 +55,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_slot;
+    const uint32_t tmem = tmem_slot + (uint32_t)dcol;
 
     // unused columns of a partial block are zeroed so nothing undefined is ever read
     for (int i = threadIdx.x; i < (nblk_a * rows_a + nblk_b * rows_b) * 32; i += blockDim.x)
@@ -89,7 +94,16 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
         for (int ks = 0; ks < K / 16; ++ks) {
             const uint64_t da = a_mn ? desc_mnmajor(ta, rows_a, 0, ks) : desc_kmajor(ta, rows_a, 0, ks);
             const uint64_t db = b_mn ? desc_mnmajor(tb, rows_b, 0, ks) : desc_kmajor(tb, rows_b, 0, ks);
-            mma_bf16(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+            if (collector == 1) {
+                mma_bf16_fill(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+                mma_bf16_lastuse(tmem + (uint32_t)N, da, db, idesc, ks > 0 ? 1u : 0u);
+            } else if (collector == 2) {   // the second MMA is N = 16 (first 16 rows of B)
+                mma_bf16_fill(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+                mma_bf16_lastuse(tmem + (uint32_t)N, da, db, idesc_bf16(M, 16, a_mn != 0, b_mn != 0),
+                                 ks > 0 ? 1u : 0u);
+            } else {
+                mma_bf16(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+            }
         }
         mma_commit(&bars[1]);
     }
@@ -98,16 +112,17 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
     tc_fence_after();
     if (ok) {
         const int row = warp * 32 + lane;
-        for (int c0 = 0; c0 < N; c0 += 16) {
+        const int nout = collector == 1 ? 2 * N : (collector == 2 ? N + 16 : N);
+        for (int c0 = 0; c0 < nout; c0 += 16) {
             float v[16];
             tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
             tmem_wait_regs<16>(v);
-            for (int i = 0; i < 16; ++i) d[row * N + c0 + i] = v[i];
+            for (int i = 0; i < 16; ++i) d[row * nout + c0 + i] = v[i];
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, ncols);
+    if (warp == 0) tmem_dealloc(tmem_slot, ncols);
     if (threadIdx.x == 0 && abort_flag) atomicExch(err, 1);
 }
 
@@ -142,9 +157,11 @@ bool make_map(CUtensorMap *map, const void *ptr, int rows, int cols) {
 // Returns 0 on success, 1 bad arguments, 2 tensor-map failure, 3 launch failure,
 // 4 a bounded wait ran out.
 extern "C" int tc_probe_mma(const void *a, const void *b, float *d, int N, int K, int a_mn, int b_mn,
-                            int a_manual, int b_manual, int *err_dev) {
+                            int a_manual, int b_manual, int collector, int dcol, int *err_dev) {
     const int M = 128;
     if (N < 16 || N > 256 || N % 16 || K < 16 || K > 256 || K % 16) return 1;
+    if (collector < 0 || collector > 2) return 1;
+    if (dcol < 0 || dcol % 16 || dcol + (collector == 1 ? 2 * N : (collector == 2 ? N + 16 : N)) > 512) return 1;
     const int rows_a = a_mn ? K : M, cols_a = a_mn ? M : K;
     const int rows_b = b_mn ? K : N, cols_b = b_mn ? N : K;
     if ((!a_manual && cols_a % 64) || (!b_manual && cols_b % 64)) return 1;   // TMA: whole blocks
@@ -156,7 +173,7 @@ extern "C" int tc_probe_mma(const void *a, const void *b, float *d, int N, int K
         return 3;
     probe_kernel<<<1, 128, kSmemBytes>>>(ma, mb, static_cast<const __nv_bfloat16 *>(a),
                                          static_cast<const __nv_bfloat16 *>(b), d, N, K, a_mn, b_mn, a_manual,
-                                         b_manual, err_dev);
+                                         b_manual, collector, dcol, err_dev);
     if (cudaGetLastError() != cudaSuccess) return 3;
     if (cudaDeviceSynchronize() != cudaSuccess) return 3;
     int err = 0;
