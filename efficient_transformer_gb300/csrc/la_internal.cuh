@@ -33,7 +33,7 @@ struct Params {
     float *state;                // per (b, kv head, segment) forward state partials
     float *rstate;               // per (b, kv head, segment) backward state partials
     float *den;                  // [B, Hq, N] row denominators (backward)
-    float *gd;                   // [B, Hq, N] denominator gradients (backward)
+    float *gd;                   // [B, Hq, N] per-row denominator terms (backward; see each kernel)
     int *err;                    // device error word
 };
 

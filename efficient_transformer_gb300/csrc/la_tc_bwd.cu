@@ -52,11 +52,18 @@ struct BwdCfg {
     static constexpr int DQ_FIXED = P_BYTES + S_BYTES + 2 * Z_BYTES + ONES_BYTES + H_BYTES + XCH_BYTES + 1024;
     static constexpr int NS_DQ = 3 * STAGE + DQ_FIXED <= kSmemLimit - 512 ? 3 : 2;
     static constexpr int DQ_SMEM = NS_DQ * STAGE + DQ_FIXED;
-    // dk/dv kernel
-    static constexpr int NS = 2;
-    static constexpr int R_BYTES = 2 * 128 * 128;           // R_bf: 128 rows x 128 columns (padded)
-    static constexpr int DKDV_SMEM = NS * STAGE + 2 * P_BYTES + R_BYTES + NS * 128 * 4 + 1024;
-    static constexpr bool FITS = DQ_SMEM <= kSmemLimit - 512 && DKDV_SMEM <= kSmemLimit - 1024;
+    // dk/dv kernel: stages, P', dP', R_bf, h (a 16 x 128 tile unless it fits as two spare
+    // columns of dP' next to the C keys)
+    static constexpr bool H_IN_DP = C % 64 != 0 && C % 64 + 16 <= 64;
+    static constexpr int RBF_BYTES = D * 128 * 2;           // R_bf: D rows x 128 columns
+    static constexpr int KV_FIXED = 2 * P_BYTES + RBF_BYTES + (H_IN_DP ? 0 : H_BYTES) + 1024;
+    static constexpr int NS = 3 * STAGE + KV_FIXED <= kSmemLimit - 512 ? 3 : 2;
+    static constexpr int DKDV_SMEM = NS * STAGE + KV_FIXED;
+    static constexpr bool FITS = DQ_SMEM <= kSmemLimit - 512 && DKDV_SMEM <= kSmemLimit - 512;
+    // dk/dv kernel TMEM columns: [R | r], then NB_KV buffers of [A_s then dk^T | dA' then dv^T]
+    static constexpr int KT_R = 0;
+    static constexpr int KT_AD = D + 16;
+    static constexpr int NB_KV = KT_AD + 4 * C <= 512 ? 2 : 1;
     // dq kernel TMEM columns: [S | z], den, A, dA', X (then den * da - h z), [R | r]
     static constexpr int T_S = 0;
     static constexpr int T_DEN = D + 16;
@@ -64,8 +71,9 @@ struct BwdCfg {
     static constexpr int T_A2 = T_A + C;
     static constexpr int T_X = T_A2 + C;
     static constexpr int T_R = T_X + D;
-    static constexpr bool TMEM_FITS = T_R + D + 16 <= 512;
-    static_assert(T_S == 0, "S starts the TMEM allocation");
+    static constexpr bool TMEM_FITS = T_R + D + 16 <= 512 && KT_AD + 2 * C <= 512;
+    static_assert(T_S == 0 && KT_R == 0, "S (dq kernel) and R (dk/dv kernel) start the TMEM allocation");
+    static_assert(NB_KV == 1 || NB_KV == 2, "one or two dk/dv TMEM buffers");
 };
 
 __device__ __forceinline__ float feat_grad_from_feat(float f, int phi) {
@@ -82,6 +90,16 @@ __device__ __forceinline__ void store_split_z(uint8_t *zt, int d, float z) {
     *reinterpret_cast<__nv_bfloat16 *>(zt + swz_offset(16, 0, d)) = zh;
     *reinterpret_cast<__nv_bfloat16 *>(zt + swz_offset(16, 1, d)) = zl;
     *reinterpret_cast<__nv_bfloat16 *>(zt + swz_offset(16, 2, d)) = zh;
+}
+
+// One 16-column slice of an R row (bf16) into the swizzled R_bf tile (D rows, 128 columns).
+template <int D>
+__device__ __forceinline__ void store_rbf_row(uint8_t *rbf, int d, const float *v, int c16) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+    *reinterpret_cast<uint4 *>(rbf + swz_chunk(D, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(rbf + swz_chunk(D, d, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // Eight dq values from eight phi_s = phi(q) / den (bf16) and the matching den * da (fp32):
@@ -178,9 +196,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
                    tA2 = tmem_base + K::T_A2, tX = tmem_base + K::T_X, tR = tmem_base + K::T_R;
 
     if (warp == 0) {
-        // ---------------- TMA producer: K, Q (and V) on one barrier, grad_out on another
+        // ---------------- TMA producer: K and Q (what the feature map needs) on one barrier,
+        // V and grad_out on another
         if (lane == 0) {
-            constexpr uint32_t bytes_a = CAUSAL ? K::Q_BYTES + K::K_BYTES + K::V_BYTES : K::Q_BYTES;
+            constexpr uint32_t bytes_a = CAUSAL ? K::Q_BYTES + K::K_BYTES : K::Q_BYTES;
+            constexpr uint32_t bytes_g = CAUSAL ? K::V_BYTES + K::G_BYTES : K::G_BYTES;
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
@@ -198,10 +218,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
                 for (int r = 0; r < G; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fulla[s], blk * 64, c0, bh0 + r);
+                mbar_arrive_expect_tx(&bar_fullg[s], bytes_g);
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_fulla[s], blk * 64, c0, bg);
-                mbar_arrive_expect_tx(&bar_fullg[s], K::G_BYTES);
+                        tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_fullg[s], blk * 64, c0, bg);
                 for (int r = 0; r < G; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64, c0,
@@ -499,7 +519,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 2, i)) = hl;
                     if (valid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 334, bh, t)) {
                         p.den[(size_t)bh * p.N + t] = den;
-                        p.gd[(size_t)bh * p.N + t] = hval * inv;
+                        p.gd[(size_t)bh * p.N + t] = hval;   // h = den * gd for the dk/dv kernel
                     }
                 }
                 fence_proxy_async();
@@ -592,26 +612,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
 
 // ---------------------------------------------------------------------------------------
 template <int D, int G, bool CAUSAL>
-__global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ CUtensorMap map_q,
-                                                        const __grid_constant__ CUtensorMap map_k,
-                                                        const __grid_constant__ CUtensorMap map_v,
-                                                        const __grid_constant__ CUtensorMap map_g, Params p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dkdv(const __grid_constant__ CUtensorMap map_q,
+                                                                const __grid_constant__ CUtensorMap map_k,
+                                                                const __grid_constant__ CUtensorMap map_v,
+                                                                const __grid_constant__ CUtensorMap map_g,
+                                                                const __grid_constant__ CUtensorMap map_dk,
+                                                                const __grid_constant__ CUtensorMap map_dv, Params p) {
     using K = BwdCfg<D, G>;
-    constexpr int C = K::C, NS = K::NS;
+    constexpr int C = K::C, NS = K::NS, NB = K::NB_KV;
     constexpr int OFF_K = K::Q_BYTES, OFF_V = OFF_K + K::K_BYTES, OFF_G = OFF_V + K::V_BYTES;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_full[NS], bar_ready[NS], bar_empty[NS];
-    __shared__ uint64_t bar_afull, bar_pready, bar_outfull, bar_outfree, bar_rfull, bar_rbf, bar_fin;
+    // each stage is two regions: [Q | g] (free once the chunk's products are done) and
+    // [K | V] (dk is written over phi(K) and dv over V, and the region is free once the TMA
+    // stores of dk and dv have read it)
+    __shared__ uint64_t bar_fullq[NS], bar_fullg[NS], bar_fullkv[NS], bar_ready[NS], bar_emptyqg[NS],
+        bar_emptykv[NS], bar_dkready[NS], bar_dvready[NS];
+    __shared__ uint64_t bar_afull[2], bar_outfull[2], bar_outfree[2];
+    __shared__ uint64_t bar_pready, bar_rbf, bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
     const uint32_t sm_lo = smem_u32(smem_raw), sm_hi = sm_lo + K::DKDV_SMEM;
     (void)sm_lo;
     (void)sm_hi;
-    uint8_t *pbuf = stage0 + NS * K::STAGE;
-    uint8_t *dpbuf = pbuf + K::P_BYTES;
-    uint8_t *rbf = dpbuf + K::P_BYTES;
-    float *gds = reinterpret_cast<float *>(rbf + K::R_BYTES);   // [NS][128]
+    uint8_t *pbuf = stage0 + NS * K::STAGE;       // P' = mask(phi_s phi(K)^T)      [query rows][keys]
+    uint8_t *dpbuf = pbuf + K::P_BYTES;          // dP' = mask(g V^T + h), then h  [query rows][keys | h_hi h_lo]
+    uint8_t *rbf = dpbuf + K::P_BYTES;           // R_bf [D rows d][128 columns e]
+    uint8_t *htile = rbf + K::RBF_BYTES;         // h as 16 x 128 (rows h_hi, h_lo) when it is not in dP'
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
@@ -621,18 +648,30 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
     const int bh0 = b * p.Hq + g * G;
     const float *rstate = p.rstate + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
 
+    for (int idx = threadIdx.x; idx < (K::P_BYTES + (K::H_IN_DP ? 0 : K::H_BYTES)) / 16; idx += blockDim.x) {
+        uint8_t *t = idx < K::P_BYTES / 16 ? dpbuf + idx * 16 : htile + (idx - K::P_BYTES / 16) * 16;
+        *reinterpret_cast<uint4 *>(t) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_ready[s], 128);
-            mbar_init(&bar_empty[s], 1 + 128);
+            mbar_init(&bar_fullq[s], 1);
+            mbar_init(&bar_fullg[s], 1);
+            mbar_init(&bar_fullkv[s], 1);
+            mbar_init(&bar_ready[s], 256);
+            mbar_init(&bar_emptyqg[s], 1);
+            mbar_init(&bar_emptykv[s], 1);
+            mbar_init(&bar_dkready[s], 128);
+            mbar_init(&bar_dvready[s], 128);
         }
-        mbar_init(&bar_afull, 1);
+        mbar_init(&bar_afull[0], 1);
+        mbar_init(&bar_afull[1], 1);
         mbar_init(&bar_pready, 128);
-        mbar_init(&bar_outfull, 1);
-        mbar_init(&bar_outfree, 128);
-        mbar_init(&bar_rfull, 1);
+        for (int bb = 0; bb < 2; ++bb) {
+            mbar_init(&bar_outfull[bb], 1);
+            mbar_init(&bar_outfree[bb], 256);
+        }
         mbar_init(&bar_rbf, 128);
         mbar_init(&bar_fin, 1);
         fence_barrier_init();
@@ -644,226 +683,215 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // tR: R (d rows x e); tA: A, then dk^T; tD: dA, then dv^T
-    const uint32_t tR = tmem_base, tA = tmem_base + 128, tD = tmem_base + 256;
+    // TMEM: [R | r (two columns: phi_s^T h_hi, phi_s^T h_lo)], then per buffer b:
+    // tA[b] = A_s then dk^T, tD[b] = dA' then dv^T (C columns each)
+    const uint32_t tR = tmem_base + K::KT_R, tAD = tmem_base + K::KT_AD;
+    auto tA = [=](int bb) { return tAD + (uint32_t)(bb * 2 * C); };
+    auto tD = [=](int bb) { return tAD + (uint32_t)(bb * 2 * C + C); };
 
     if (warp == 0) {
         // ---------------- TMA producer (chunks in reverse order)
         if (lane == 0) {
-            constexpr uint32_t bytes = CAUSAL ? K::STAGE : K::K_BYTES + K::V_BYTES;
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
-                if (k >= NS && !mbar_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + (nchunk - 1 - k) * C;
                 if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N, 401, smem_u32(st) - sm_lo, c0)) break;
-                mbar_arrive_expect_tx(&bar_full[s], bytes);
-                if (CAUSAL)
+                if (CAUSAL && k >= NS && !mbar_wait(&bar_emptyqg[s], ((k / NS) - 1) & 1, &abort_flag)) break;
+                LA_TL2(k, 0);
+                if (CAUSAL) {
+                    mbar_arrive_expect_tx(&bar_fullq[s], K::Q_BYTES);
                     for (int r = 0; r < G; ++r)
-                        for (int blk = 0; blk < K::DB; ++blk) {
-                            tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_full[s], blk * 64, c0,
+                        for (int blk = 0; blk < K::DB; ++blk)
+                            tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fullq[s], blk * 64, c0,
                                         bh0 + r);
-                            tma_load_3d(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_full[s], blk * 64,
+                    mbar_arrive_expect_tx(&bar_fullg[s], K::G_BYTES);
+                    for (int r = 0; r < G; ++r)
+                        for (int blk = 0; blk < K::DB; ++blk)
+                            tma_load_3d(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64,
                                         c0, bh0 + r);
-                        }
+                }
+                if (k >= NS && !mbar_wait(&bar_emptykv[s], ((k / NS) - 1) & 1, &abort_flag)) break;
+                mbar_arrive_expect_tx(&bar_fullkv[s], K::K_BYTES + K::V_BYTES);
                 for (int blk = 0; blk < K::DB; ++blk) {
-                    tma_load_3d(st + OFF_K + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
-                    tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
+                    tma_load_3d(st + OFF_K + blk * C * 128, &map_k, &bar_fullkv[s], blk * 64, c0, bg);
+                    tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_fullkv[s], blk * 64, c0, bg);
                 }
                 issued = k + 1;
             }
-            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) mbar_drain(&bar_full[k % NS], (k / NS) & 1);
+            // a chunk whose K, V wait gave up has Q and g in flight: wait for those too
+            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) {
+                if (CAUSAL) {
+                    mbar_drain(&bar_fullq[k % NS], (k / NS) & 1);
+                    mbar_drain(&bar_fullg[k % NS], (k / NS) & 1);
+                }
+                mbar_drain(&bar_fullkv[k % NS], (k / NS) & 1);
+            }
+            if (issued < nchunk && CAUSAL) {
+                const int k = issued;
+                mbar_drain(&bar_fullq[k % NS], (k / NS) & 1);
+                mbar_drain(&bar_fullg[k % NS], (k / NS) & 1);
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------- dk, dv stores: TMA writes the two tiles left over phi(K) and V,
+        // and the [K | V] region is released once the copies have read it
+        if (lane == 0) {
+            for (int k = 0; k < nchunk; ++k) {
+                const int s = k % NS;
+                uint8_t *st = stage0 + s * K::STAGE;
+                const int c0 = t0 + (nchunk - 1 - k) * C;
+                const bool ok = mbar_wait(&bar_dkready[s], (k / NS) & 1, &abort_flag) &&
+                                mbar_wait(&bar_dvready[s], (k / NS) & 1, &abort_flag);
+                if (ok) {
+                    LA_TL2(k, 12);
+                    for (int blk = 0; blk < K::DB; ++blk) {
+                        tma_store_3d(&map_dk, st + OFF_K + blk * C * 128, blk * 64, c0, bg);
+                        tma_store_3d(&map_dv, st + OFF_V + blk * C * 128, blk * 64, c0, bg);
+                    }
+                    bulk_commit();
+                    bulk_wait_read();
+                    LA_TL2(k, 13);
+                }
+                mbar_arrive(&bar_emptykv[s]);
+                if (!ok) break;
+            }
+            bulk_wait_all();
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer.  Iteration k starts chunk k (A_s, dA') and finishes
+        // chunk k - 1 (dk^T, dv^T, R, r).  With two TMEM buffers the start goes first when its
+        // inputs are already there, so that the tensor pipe works while the pool converts P'
+        // of chunk k - 1; otherwise (and always with one buffer, where chunk k's products
+        // overwrite chunk k - 1's outputs) the finish comes first.
         if (lane == 0) {
             constexpr uint32_t idA = idesc_bf16(128, C, false, false);
             constexpr uint32_t idMM = idesc_bf16(128, C, true, true);
             constexpr uint32_t idMK = idesc_bf16(128, C, true, false);
             constexpr uint32_t idR = idesc_bf16(128, D, true, true);
-            const uint32_t pb = smem_u32(pbuf), dpb = smem_u32(dpbuf), rb = smem_u32(rbf);
-            for (int k = 0; k < nchunk; ++k) {
-                const int s = k % NS;
-                if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
-                if (k > 0 && !mbar_wait(&bar_outfree, (k - 1) & 1, &abort_flag)) break;
+            constexpr uint32_t idH = idesc_bf16(128, 16, true, K::H_IN_DP);
+            const uint32_t pb = smem_u32(pbuf), dpb = smem_u32(dpbuf), rb = smem_u32(rbf), ht = smem_u32(htile);
+            auto start = [&](int k) -> bool {
+                if (!CAUSAL) return true;
+                const int s = k % NS, bb = k % NB;
+                if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) return false;
+                if (!mbar_wait(&bar_fullg[s], (k / NS) & 1, &abort_flag)) return false;
+                if (k >= NB && !mbar_wait(&bar_outfree[bb], ((k - NB) / NB) & 1, &abort_flag)) return false;
+                LA_TL2(k, 3);
                 tc_fence_after();
                 const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V, gs = qs + OFF_G;
-                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && rb + K::R_BYTES <= sm_hi, 411, qs - sm_lo, k))
-                    break;
-                if (CAUSAL) {
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_bf16(tA, desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_bf16(tD, desc_kmajor(gs, 128, 0, kk), desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : 0u);
-                    mma_commit(&bar_afull);
-                    if (!mbar_wait(&bar_pready, k & 1, &abort_flag)) break;
+                for (int kk = 0; kk < D / 16; ++kk)   // A_s = phi_s phi(K)^T
+                    mma_bf16(tA(bb), desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk)   // dA' = g V^T
+                    mma_bf16(tD(bb), desc_kmajor(gs, 128, 0, kk), desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                mma_commit(&bar_afull[bb]);
+                LA_TL2(k, 4);
+                return true;
+            };
+            auto finish = [&](int kp) -> bool {
+                const int sp = kp % NS, bb = kp % NB;
+                if (CAUSAL && !mbar_wait(&bar_pready, kp & 1, &abort_flag)) return false;
+                if ((CAUSAL || kp == 0) && !mbar_wait(&bar_rbf, kp & 1, &abort_flag)) return false;
+                if (!CAUSAL) {
+                    if (!mbar_wait(&bar_ready[sp], (kp / NS) & 1, &abort_flag)) return false;
+                    if (kp >= NB && !mbar_wait(&bar_outfree[bb], ((kp - NB) / NB) & 1, &abort_flag)) return false;
                 }
-                if ((CAUSAL || k == 0) && !mbar_wait(&bar_rbf, k & 1, &abort_flag)) break;
+                LA_TL2(kp, 5);
                 tc_fence_after();
-                // dk^T = phi(Q)^T dP + R_bf V^T
+                const uint32_t qs = smem_u32(stage0 + sp * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V,
+                               gs = qs + OFF_G;
+                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && rb + K::RBF_BYTES <= sm_hi, 411, qs - sm_lo, kp))
+                    return false;
                 uint32_t acc = 0;
-                if (CAUSAL)
-                    for (int kk = 0; kk < 128 / 16; ++kk, acc = 1)
-                        mma_bf16(tA, desc_mnmajor(qs, 128, 0, kk), desc_mnmajor(dpb, 128, 0, kk), idMM, acc);
-                for (int kk = 0; kk < D / 16; ++kk, acc = 1)
-                    mma_bf16(tA, desc_kmajor(rb, 128, 0, kk), desc_kmajor(vs, C, 0, kk), idA, acc);
-                // dv^T = gn^T P + R_bf^T phi(K)^T
+                if (CAUSAL)   // dk^T = phi_s^T dP', r += phi_s^T h, R += phi_s^T g
+                    for (int kk = 0; kk < 128 / 16; ++kk, acc = 1) {
+                        const uint64_t as = desc_mnmajor(qs, 128, 0, kk);
+                        const uint64_t bh = K::H_IN_DP ? desc_mnmajor(dpb + C * 2, 128, 0, kk) : desc_kmajor(ht, 16, 0, kk);
+                        mma_bf16(tA(bb), as, desc_mnmajor(dpb, 128, 0, kk), idMM, acc);
+                        mma_bf16(tR + D, as, bh, idH, 1u);
+                        mma_bf16(tR, as, desc_mnmajor(gs, 128, 0, kk), idR, 1u);
+                    }
+                for (int kk = 0; kk < D / 16; ++kk, acc = 1)   // dk^T += R_bf V^T
+                    mma_bf16(tA(bb), desc_kmajor(rb, D, 0, kk), desc_kmajor(vs, C, 0, kk), idA, acc);
                 acc = 0;
-                if (CAUSAL)
+                if (CAUSAL)   // dv^T = g^T P'
                     for (int kk = 0; kk < 128 / 16; ++kk, acc = 1)
-                        mma_bf16(tD, desc_mnmajor(gs, 128, 0, kk), desc_mnmajor(pb, 128, 0, kk), idMM, acc);
-                for (int kk = 0; kk < D / 16; ++kk, acc = 1)
-                    mma_bf16(tD, desc_mnmajor(rb, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idMK, acc);
-                mma_commit(&bar_outfull);
-                if (CAUSAL) {   // this chunk's rows join R for the earlier chunks
-                    for (int kk = 0; kk < 128 / 16; ++kk)
-                        mma_bf16(tR, desc_mnmajor(qs, 128, 0, kk), desc_mnmajor(gs, 128, 0, kk), idR, 1u);
-                    mma_commit(&bar_rfull);
-                }
-                mma_commit(&bar_empty[s]);
+                        mma_bf16(tD(bb), desc_mnmajor(gs, 128, 0, kk), desc_mnmajor(pb, 128, 0, kk), idMM, acc);
+                for (int kk = 0; kk < D / 16; ++kk, acc = 1)   // dv^T += R_bf^T phi(K)^T
+                    mma_bf16(tD(bb), desc_mnmajor(rb, D, 0, kk), desc_kmajor(ks_, C, 0, kk), idMK, acc);
+                mma_commit(&bar_outfull[bb]);
+                if (CAUSAL) mma_commit(&bar_emptyqg[sp]);
+                LA_TL2(kp, 6);
+                return true;
+            };
+            for (int k = 0; k <= nchunk; ++k) {
+                // start first only when it will not wait (its stage is ready and its buffer free)
+                const bool early = NB == 2 && k < nchunk && CAUSAL &&
+                                   mbar_test(&bar_ready[k % NS], (k / NS) & 1) &&
+                                   mbar_test(&bar_fullg[k % NS], (k / NS) & 1) &&
+                                   (k < NB || mbar_test(&bar_outfree[k % NB], ((k - NB) / NB) & 1));
+                if (early && !start(k)) break;
+                if (k > 0 && !finish(k - 1)) break;
+                if (!early && k < nchunk && !start(k)) break;
             }
             mma_commit(&bar_fin);
             mbar_drain(&bar_fin, 0);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- prologue: phi(Q), phi(K) in place; gn = g / den over the g tile
-        const int i = threadIdx.x - 128;
-        const int r = i / C, ti = i % C;
-        const int bh = bh0 + r;
-        bool ok = true;
-        for (int k = 0; k < nchunk; ++k) {
-            const int s = k % NS;
-            ok = ok && warp_wait(&bar_full[s], (k / NS) & 1, &abort_flag);
-            if (ok) {
-                uint8_t *st = stage0 + s * K::STAGE;
-                const int c0 = t0 + (nchunk - 1 - k) * C, t = c0 + ti;
-                const bool qvalid = t < t1;
-                if (CAUSAL) {
-                    float inv = 0.f, gdv = 0.f;
-                    if (qvalid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 421, bh, t)) {
-                        inv = 1.f / p.den[(size_t)bh * p.N + t];
-                        gdv = p.gd[(size_t)bh * p.N + t];
-                    }
-                    gds[s * 128 + i] = gdv;
-#pragma unroll 4
-                    for (int c = 0; c < D / 8; ++c) {
-                        uint8_t *ch = st + swz_chunk(128, i, c);
-                        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 422, smem_u32(ch) - sm_lo, c))
-                            feat8_inplace2(ch, qvalid, p.phi);
-                        uint8_t *gch = st + OFF_G + swz_chunk(128, i, c);
-                        if (LA_CHECK(in_smem(gch, 16, sm_lo, sm_hi), 423, smem_u32(gch) - sm_lo, c)) {
-                            uint4 x = *reinterpret_cast<uint4 *>(gch);
-                            uint32_t *xi = reinterpret_cast<uint32_t *>(&x);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float2 f = unpack_bf16x2(xi[q]);
-                                xi[q] = pack_bf16x2(f.x * inv, f.y * inv);
-                            }
-                            *reinterpret_cast<uint4 *>(gch) = x;
-                        }
-                    }
-                }
-                for (int idx = i; idx < C * (D / 8); idx += 128) {
-                    const int j = idx / (D / 8), c = idx % (D / 8);
-                    uint8_t *ch = st + OFF_K + swz_chunk(C, j, c);
-                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 424, smem_u32(ch) - sm_lo, idx))
-                        feat8_inplace2(ch, c0 + j < t1, p.phi);
-                }
-                fence_proxy_async();
-            }
-            mbar_arrive_warp(&bar_ready[s]);
-        }
-    } else if (warp >= 8 && warp < 12) {
-        // ---------------- P / dP conversion (thread = query row) and the dk, dv epilogue
-        // (thread = TMEM lane = feature d)
-        const int i = threadIdx.x - 256;
-        const int wq = warp % 4;
-        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const int ti = i % C;
-        const int d = i;
-        float r_d = (d < D) ? rstate[(size_t)d * (D + 1) + D] : 0.f;
+    } else if ((warp >= 4 && warp < 8) || warp >= 16) {
+        // ---------------- prologue (both warpgroups on every chunk): phi_s = phi(q) / den over
+        // the Q tile, phi(K) over the K tile, in place
+        const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0..255
+        constexpr int CPR = D / 8, RPP = 256 / CPR;
+        static_assert(RPP % 8 == 0, "rows per pass");
+        const int c = pi % CPR, r0 = pi / CPR;
+        const uint32_t pos = (uint32_t)(((c & 7) ^ (r0 & 7)) << 4);
+        const uint32_t offq = (uint32_t)(c >> 3) * 128u * 128u + pos, offk = (uint32_t)(c >> 3) * C * 128u + pos;
+        constexpr int NR = 128 / RPP;
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
             const int c0 = t0 + (nchunk - 1 - k) * C;
+            const int nvalid = t1 - c0;
+            // this thread's rows' denominators, loaded while the chunk's tiles arrive
+            float den[NR];
+            if (CAUSAL)
+#pragma unroll
+                for (int n = 0; n < NR; ++n) {
+                    const int row = r0 + n * RPP, ti = row % C;
+                    const size_t at = (size_t)(bh0 + row / C) * p.N + c0 + ti;
+                    den[n] = (ti < nvalid && LA_CHECK(at < (size_t)p.B * p.Hq * p.N, 423, row, c0)) ? p.den[at] : 1.f;
+                }
+            if (CAUSAL) ok = ok && warp_wait(&bar_fullq[s], (k / NS) & 1, &abort_flag);
+            if (pi == 0) LA_TL2(k, 1);
             uint8_t *st = stage0 + s * K::STAGE;
-            if (CAUSAL) {
-                ok = ok && warp_wait(&bar_afull, k & 1, &abort_flag);
-                tc_fence_after();
-                if (ok) {
-                    const float gdi = gds[s * 128 + i];
-#pragma unroll 1
-                    for (int c16 = 0; c16 < C / 16; ++c16) {
-                        float va[16], vd[16];
-                        tmem_ld16(tA + lane_off + c16 * 16, va);
-                        tmem_ld16(tD + lane_off + c16 * 16, vd);
-                        tmem_wait_regs<16>(va);
-                        tmem_wait_regs<16>(vd);
-                        uint32_t wa[8], wd[8];
+            if (ok && CAUSAL)
 #pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            const int j = c16 * 16 + e;
-                            const bool m0 = j <= ti, m1 = j + 1 <= ti;
-                            wa[e / 2] = pack_bf16x2(m0 ? va[e] : 0.f, m1 ? va[e + 1] : 0.f);
-                            wd[e / 2] = pack_bf16x2(m0 ? vd[e] + gdi : 0.f, m1 ? vd[e + 1] + gdi : 0.f);
-                        }
-                        uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
-                        uint8_t *q0 = dpbuf + swz_chunk(128, i, 2 * c16), *q1 = dpbuf + swz_chunk(128, i, 2 * c16 + 1);
-                        if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi) &&
-                                         in_smem(q0, 16, sm_lo, sm_hi) && in_smem(q1, 16, sm_lo, sm_hi),
-                                     431, smem_u32(p0) - sm_lo, c16)) {
-                            *reinterpret_cast<uint4 *>(p0) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-                            *reinterpret_cast<uint4 *>(p1) = make_uint4(wa[4], wa[5], wa[6], wa[7]);
-                            *reinterpret_cast<uint4 *>(q0) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-                            *reinterpret_cast<uint4 *>(q1) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
-                        }
-                    }
-                    fence_proxy_async();
+                for (int n = 0; n < NR; ++n) {
+                    const int row = r0 + n * RPP;
+                    uint8_t *ch = st + offq + row * 128;
+                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 421, smem_u32(ch) - sm_lo, row))
+                        feat8_scaled_inplace(ch, row % C < nvalid, p.phi, 1.f / den[n]);
                 }
-                tc_fence_before();
-                mbar_arrive_warp(&bar_pready);
-            }
-            ok = ok && warp_wait(&bar_outfull, k & 1, &abort_flag);
-            tc_fence_after();
-            if (ok && wq * 32 < D) {
-                __nv_bfloat16 *dkb = static_cast<__nv_bfloat16 *>(p.dk) + (size_t)bg * p.N * D;
-                __nv_bfloat16 *dvb = static_cast<__nv_bfloat16 *>(p.dv) + (size_t)bg * p.N * D;
-                const uint8_t *kt = st + OFF_K;
-#pragma unroll 1
-                for (int c16 = 0; c16 < C / 16; ++c16) {
-                    float vb[16], vv[16];
-                    tmem_ld16(tA + lane_off + c16 * 16, vb);
-                    tmem_ld16(tD + lane_off + c16 * 16, vv);
-                    tmem_wait_regs<16>(vb);
-                    tmem_wait_regs<16>(vv);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int j = c16 * 16 + e, tok = c0 + j;
-                        if (tok < t1 && LA_CHECK(((size_t)bg * p.N + tok) * D + d < (size_t)p.B * p.Hkv * p.N * D, 432,
-                                                 tok, d)) {
-                            const float f = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kt + swz_offset(C, j, d)));
-                            dkb[(size_t)tok * D + d] = __float2bfloat16_rn(feat_grad_from_feat(f, p.phi) * (vb[e] + r_d));
-                            dvb[(size_t)tok * D + d] = __float2bfloat16_rn(vv[e]);
-                        }
-                    }
+            ok = ok && warp_wait(&bar_fullkv[s], (k / NS) & 1, &abort_flag);
+            if (ok) {
+                for (int j = r0; j < C; j += RPP) {
+                    uint8_t *ch = st + OFF_K + offk + j * 128;
+                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 422, smem_u32(ch) - sm_lo, j))
+                        feat8_inplace2(ch, j < nvalid, p.phi);
                 }
             }
-            tc_fence_before();
-            mbar_arrive_warp(&bar_outfree);
-            if (CAUSAL && ok && d < D) {   // this chunk's rows join r for the earlier chunks
-                const float *gsd = gds + s * 128;
-                for (int row = 0; row < 128; ++row)
-                    r_d += gsd[row] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(st + swz_offset(128, row, d)));
-            }
-            mbar_arrive_warp(&bar_empty[s]);
+            fence_proxy_async();
+            if (pi == 0) LA_TL2(k, 2);
+            mbar_arrive_warp(&bar_ready[s]);
         }
-    } else if (warp >= 12) {
-        // ---------------- R conversion: TMEM R (fp32) -> R_bf (bf16 operand tile)
-        const int d = threadIdx.x - 384;
+    } else if (warp >= 8 && warp < 12) {
+        // ---------------- warpgroup A (thread = feature d): R conversion and dk
         const int wq = warp % 4;
+        const int d = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        if (wq * 32 < D) {
+        float r_prev = 0.f;   // r before the current chunk
+        if (d < D) {
             const float *row = rstate + (size_t)d * (D + 1);
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
@@ -871,40 +899,168 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < 16; ++e) v[e] = row[c16 * 16 + e];
                 if (CAUSAL) tmem_st16(tR + lane_off + c16 * 16, v);
-                uint32_t w[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-                *reinterpret_cast<uint4 *>(rbf + swz_chunk(128, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(rbf + swz_chunk(128, d, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+                store_rbf_row<D>(rbf, d, v, c16);
             }
-            if (CAUSAL) tmem_st_wait();
+            r_prev = row[D];
+            if (CAUSAL) {
+                float rv[16];
+                rv[0] = r_prev;
+#pragma unroll
+                for (int e = 1; e < 16; ++e) rv[e] = 0.f;
+                tmem_st16(tR + lane_off + D, rv);
+                tmem_st_wait();
+            }
         }
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive_warp(&bar_rbf);
-        if (CAUSAL) {
-            bool ok = true;
-            for (int k = 0; k < nchunk; ++k) {
-                ok = ok && warp_wait(&bar_rfull, k & 1, &abort_flag);
-                tc_fence_after();
-                if (ok && wq * 32 < D) {
-#pragma unroll 1
+        bool ok = true;
+        for (int k = 0; k < nchunk; ++k) {
+            const int s = k % NS, bb = k % NB;
+            ok = ok && warp_wait(&bar_outfull[bb], (k / NB) & 1, &abort_flag);
+            tc_fence_after();
+            if (d == 0) LA_TL2(k, 7);
+            float r_next = r_prev;
+            if (CAUSAL && d < D) {   // R and r after this chunk -> R_bf and r for the next one
+                if (ok) {
+#pragma unroll
                     for (int c16 = 0; c16 < D / 16; ++c16) {
                         float v[16];
                         tmem_ld16(tR + lane_off + c16 * 16, v);
                         tmem_wait_regs<16>(v);
-                        uint32_t w[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-                        *reinterpret_cast<uint4 *>(rbf + swz_chunk(128, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4 *>(rbf + swz_chunk(128, d, 2 * c16 + 1)) =
-                            make_uint4(w[4], w[5], w[6], w[7]);
+                        store_rbf_row<D>(rbf, d, v, c16);
                     }
+                    float rv[2];
+                    tmem_ld2(tR + lane_off + D, rv);
+                    tmem_wait_regs<2>(rv);
+                    r_next = rv[0] + rv[1];
                 }
+            }
+            if (CAUSAL) {
                 fence_proxy_async();
                 tc_fence_before();
                 mbar_arrive_warp(&bar_rbf);
             }
+            if (d == 0) LA_TL2(k, 8);
+            // dk = phi'(k) * (dk^T + r) for column d of the chunk's C keys, written over phi(K)
+            // (each thread reads and writes only its own column) for the TMA store
+            uint8_t *kw = stage0 + s * K::STAGE + OFF_K;
+#pragma unroll 1
+            for (int c16 = 0; c16 < C / 16; ++c16) {
+                float v[16];
+                if (ok && d < D) {
+                    tmem_ld16(tA(bb) + lane_off + c16 * 16, v);
+                    tmem_wait_regs<16>(v);
+                }
+                if (c16 + 1 == C / 16) {
+                    tc_fence_before();
+                    mbar_arrive_warp(&bar_outfree[bb]);
+                }
+                if (!ok || d >= D) continue;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    __nv_bfloat16 *x = reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d));
+                    *x = __float2bfloat16_rn(feat_grad_from_feat(__bfloat162float(*x), p.phi) * (v[e] + r_prev));
+                }
+            }
+            fence_proxy_async();
+            mbar_arrive_warp(&bar_dkready[s]);
+            if (d == 0) LA_TL2(k, 9);
+            r_prev = r_next;
+        }
+    } else if (warp >= 12 && warp < 16) {
+        // ---------------- warpgroup B: P' and dP' (thread = query row i) and dv (thread = e)
+        const int wq = warp % 4;
+        const int i = wq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const int ti = i % C, bh = bh0 + i / C;
+        bool ok = true;
+        float hv = 0.f;   // h of this thread's row in chunk k, loaded one step ahead
+        if (CAUSAL && nchunk > 0) {
+            const int t = t0 + (nchunk - 1) * C + ti;
+            if (t < t1 && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 434, bh, t)) hv = p.gd[(size_t)bh * p.N + t];
+        }
+        for (int k = 0; k <= nchunk; ++k) {
+            // dv of chunk k - 1, written over its V tile (dead once its MMAs are done, which
+            // outfull says; P' is then free too) for the TMA store
+            if (k > 0) {
+                const int kp = k - 1, bb = kp % NB, sp = kp % NS;
+                uint8_t *vw = stage0 + sp * K::STAGE + OFF_V;
+                ok = ok && warp_wait(&bar_outfull[bb], (kp / NB) & 1, &abort_flag);
+                tc_fence_after();
+#pragma unroll 1
+                for (int c16 = 0; c16 < C / 16; ++c16) {
+                    float v[16];
+                    if (ok && i < D) {
+                        tmem_ld16(tD(bb) + lane_off + c16 * 16, v);
+                        tmem_wait_regs<16>(v);
+                    }
+                    if (c16 + 1 == C / 16) {
+                        tc_fence_before();
+                        mbar_arrive_warp(&bar_outfree[bb]);
+                    }
+                    if (!ok || i >= D) continue;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, c16 * 16 + e, i)) = __float2bfloat16_rn(v[e]);
+                }
+                fence_proxy_async();
+                mbar_arrive_warp(&bar_dvready[sp]);
+            }
+            if (k == nchunk || !CAUSAL) continue;
+            // P' = mask(A_s), dP' = mask(dA' + h) for chunk k, and h (split) for the r product
+            const int bb = k % NB;
+            ok = ok && warp_wait(&bar_afull[bb], (k / NB) & 1, &abort_flag);
+            tc_fence_after();
+            if (i == 0) LA_TL2(k, 10);
+            float hnext = 0.f;
+            if (k + 1 < nchunk) {
+                const int tn = t0 + (nchunk - 2 - k) * C + ti;
+                if (tn < t1 && LA_CHECK((size_t)bh * p.N + tn < (size_t)p.B * p.Hq * p.N, 435, bh, tn))
+                    hnext = p.gd[(size_t)bh * p.N + tn];
+            }
+            if (ok) {
+                const __nv_bfloat16 hh = __float2bfloat16_rn(hv);
+                const __nv_bfloat16 hl = __float2bfloat16_rn(hv - __bfloat162float(hh));
+                if (K::H_IN_DP) {
+                    *reinterpret_cast<__nv_bfloat16 *>(dpbuf + swz_offset(128, i, C)) = hh;
+                    *reinterpret_cast<__nv_bfloat16 *>(dpbuf + swz_offset(128, i, C + 1)) = hl;
+                } else {
+                    *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 0, i)) = hh;
+                    *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 1, i)) = hl;
+                }
+#pragma unroll 1
+                for (int c16 = 0; c16 < C / 16; ++c16) {
+                    float va[16], vd[16];
+                    tmem_ld16(tA(bb) + lane_off + c16 * 16, va);
+                    tmem_ld16(tD(bb) + lane_off + c16 * 16, vd);
+                    tmem_wait_regs<16>(va);
+                    tmem_wait_regs<16>(vd);
+                    uint32_t wa[8], wd[8];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        const int j = c16 * 16 + e;
+                        const bool m0 = j <= ti, m1 = j + 1 <= ti;
+                        wa[e / 2] = pack_bf16x2(m0 ? va[e] : 0.f, m1 ? va[e + 1] : 0.f);
+                        wd[e / 2] = pack_bf16x2(m0 ? vd[e] + hv : 0.f, m1 ? vd[e + 1] + hv : 0.f);
+                    }
+                    uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
+                    uint8_t *q0 = dpbuf + swz_chunk(128, i, 2 * c16), *q1 = dpbuf + swz_chunk(128, i, 2 * c16 + 1);
+                    if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi) &&
+                                     in_smem(q0, 16, sm_lo, sm_hi) && in_smem(q1, 16, sm_lo, sm_hi),
+                                 431, smem_u32(p0) - sm_lo, c16)) {
+                        *reinterpret_cast<uint4 *>(p0) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+                        *reinterpret_cast<uint4 *>(p1) = make_uint4(wa[4], wa[5], wa[6], wa[7]);
+                        *reinterpret_cast<uint4 *>(q0) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                        *reinterpret_cast<uint4 *>(q1) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+                    }
+                }
+                fence_proxy_async();
+            }
+            tc_fence_before();
+            if (i == 0) LA_TL2(k, 11);
+            mbar_arrive_warp(&bar_pready);
+            hv = hnext;
         }
     }
     tc_fence_before();
@@ -919,12 +1075,14 @@ __global__ void __launch_bounds__(512, 1) k_tc_bwd_dkdv(const __grid_constant__ 
 template <int D, int G, bool CAUSAL>
 cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     using K = BwdCfg<D, G>;
-    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{};
+    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{};
     cudaError_t e = make_map(&mq, p.q, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mg, p.g, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mdq, p.dq, p.B * p.Hq, p.N, D, K::C);
+    if (e == cudaSuccess) e = make_map(&mdk, p.dk, p.B * p.Hkv, p.N, D, K::C);
+    if (e == cudaSuccess) e = make_map(&mdv, p.dv, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = prepare(k_tc_bwd_dq<D, G, CAUSAL>, K::DQ_SMEM);
     if (e == cudaSuccess) e = prepare(k_tc_bwd_dkdv<D, G, CAUSAL>, K::DKDV_SMEM);
     if (e != cudaSuccess) return e;
@@ -938,7 +1096,7 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
         e = scan_segments(p.rstate, p, CAUSAL ? kScanSuffix : kScanTotal, (size_t)D * (D + 1), s);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_bwd_dkdv_causal" : "tc_bwd_dkdv_bidir", s);
-    k_tc_bwd_dkdv<D, G, CAUSAL><<<grid, 512, K::DKDV_SMEM, s>>>(mq, mk, mv, mg, p);
+    k_tc_bwd_dkdv<D, G, CAUSAL><<<grid, kBwdThreads, K::DKDV_SMEM, s>>>(mq, mk, mv, mg, mdk, mdv, p);
     return cudaGetLastError();
 }
 
@@ -984,6 +1142,10 @@ cudaError_t tc_backward(const Params &p, cudaStream_t s) {
 // Timeline builds only: the dq kernel's event clocks ([64][16] long long).
 extern "C" int la_timeline_read_bwd(long long *out) {
     return cudaMemcpyFromSymbol(out, la::g_la_tl, sizeof(long long) * 64 * 16) == cudaSuccess ? 0 : 1;
+}
+// ... and the dk/dv kernel's.
+extern "C" int la_timeline_read_bwd2(long long *out) {
+    return cudaMemcpyFromSymbol(out, la::g_la_tl2, sizeof(long long) * 64 * 16) == cudaSuccess ? 0 : 1;
 }
 #endif
 

@@ -69,13 +69,21 @@ __device__ __noinline__ bool dbg_fail(int id, long long a, long long b) {
 // fixed events of its first 64 chunks, read back with la_timeline_read().
 #ifdef LA_TIMELINE
 __device__ long long g_la_tl[64][16];
+__device__ long long g_la_tl2[64][16];   // a second kernel of the same translation unit
 #define LA_TL(k, ev)                                                  \
     do {                                                              \
         if (blockIdx.x == 0 && (k) < 64) g_la_tl[(k)][(ev)] = clock64(); \
     } while (0)
+#define LA_TL2(k, ev)                                                  \
+    do {                                                               \
+        if (blockIdx.x == 0 && (k) < 64) g_la_tl2[(k)][(ev)] = clock64(); \
+    } while (0)
 #else
 #define LA_TL(k, ev) \
     do {             \
+    } while (0)
+#define LA_TL2(k, ev) \
+    do {              \
     } while (0)
 #endif
 
@@ -110,6 +118,24 @@ __device__ __forceinline__ uint32_t feat_bf16x2(uint32_t u, int phi) {
         y = __hadd2(y, e);
     }
     return *reinterpret_cast<uint32_t *>(&y);
+}
+
+// phi applied to 8 bf16 values in place and scaled by s (bf16x2 multiply by bf16(s)), or
+// zeros for a row past the end.
+__device__ __forceinline__ void feat8_scaled_inplace(uint8_t *chunk, bool valid, int phi, float s) {
+    uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
+    uint4 x = valid ? *ptr : make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+        const __nv_bfloat162 s2 = __float2bfloat162_rn(s);
+        uint32_t *xi = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t f = feat_bf16x2(xi[q], phi);
+            const __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&f), s2);
+            xi[q] = *reinterpret_cast<const uint32_t *>(&y);
+        }
+    }
+    *ptr = x;
 }
 
 // phi applied to 8 bf16 values (16 bytes) in place, or zeros for a row past the end.

@@ -59,6 +59,19 @@ __device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar) {
     if ((threadIdx.x & 31u) == 0u) mbar_arrive_cnt(bar, 32u);
 }
 
+// Non-blocking test: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Test the phase; the thread may be suspended inside for up to kSuspendNs waiting for it,
 // so that waiting warps do not spin on the issue slots.
 constexpr uint32_t kSuspendNs = 200000u;
@@ -206,8 +219,8 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
 }
 
 // The same MMA with the A operand kept in the collector buffer for the next MMA
-// (`fill`), or taken from it and released (`lastuse`): two consecutive MMAs that share A
-// read it from shared memory once.  The A descriptor of the `lastuse` MMA must describe
+// (`fill`), taken from it and kept (`use`), or taken from it and released (`lastuse`):
+// consecutive MMAs that share A read it from shared memory once.  The A descriptor of the `lastuse` MMA must describe
 // the same matrix as the `fill` before it, with the same major-ness.
 __device__ __forceinline__ void mma_bf16_fill(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                               uint32_t accumulate) {
@@ -215,6 +228,16 @@ __device__ __forceinline__ void mma_bf16_fill(uint32_t d_tmem, uint64_t a_desc, 
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16.collector::a::fill [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_use(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16.collector::a::use [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

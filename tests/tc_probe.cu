@@ -8,7 +8,9 @@
 // kept in the collector buffer and then taking A from it, into two accumulators (D is
 // then [M][2N]: both halves must equal A B^T); with `collector` = 2 the second MMA has
 // N = 16 and takes the first 16 rows (n) of B (D is [M][N + 16]).  `dcol` places the
-// accumulator at that TMEM column of a 512-column allocation.  Built by
+// accumulator at that TMEM column of a 512-column allocation.  `b_off` (MN-major B only)
+// starts B's descriptor `b_off` columns into its tile, inside the first 64-column block:
+// B is then stored with N + b_off columns and the product uses columns b_off .. b_off+N-1.  Built by
 // tests/test_gpu_tc_layouts.py into tests/_build.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -27,7 +29,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
                                                     const __grid_constant__ CUtensorMap map_b,
                                                     const __nv_bfloat16 *a_src, const __nv_bfloat16 *b_src,
                                                     float *d, int N, int K, int a_mn, int b_mn, int a_manual,
-                                                    int b_manual, int collector, int dcol, int *err) {
+                                                    int b_manual, int collector, int dcol, int b_off, int *err) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[2];
     __shared__ uint32_t tmem_slot;
@@ -35,7 +37,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
     const int M = 128;
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const int rows_a = a_mn ? K : M, cols_a = a_mn ? M : K;
-    const int rows_b = b_mn ? K : N, cols_b = b_mn ? N : K;
+    const int rows_b = b_mn ? K : N, cols_b = b_mn ? N + b_off : K;
     const int nblk_a = (cols_a + 63) / 64, nblk_b = (cols_b + 63) / 64;
     uint8_t *tile_a = smem;
     uint8_t *tile_b = smem + nblk_a * rows_a * 128;
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
         const uint32_t ta = smem_u32(tile_a), tb = smem_u32(tile_b);
         for (int ks = 0; ks < K / 16; ++ks) {
             const uint64_t da = a_mn ? desc_mnmajor(ta, rows_a, 0, ks) : desc_kmajor(ta, rows_a, 0, ks);
-            const uint64_t db = b_mn ? desc_mnmajor(tb, rows_b, 0, ks) : desc_kmajor(tb, rows_b, 0, ks);
+            const uint64_t db = b_mn ? desc_mnmajor(tb + (uint32_t)b_off * 2u, rows_b, 0, ks) : desc_kmajor(tb, rows_b, 0, ks);
             if (collector == 1) {
                 mma_bf16_fill(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
                 mma_bf16_lastuse(tmem + (uint32_t)N, da, db, idesc, ks > 0 ? 1u : 0u);
@@ -101,6 +103,11 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
                 mma_bf16_fill(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
                 mma_bf16_lastuse(tmem + (uint32_t)N, da, db, idesc_bf16(M, 16, a_mn != 0, b_mn != 0),
                                  ks > 0 ? 1u : 0u);
+            } else if (collector == 3) {   // fill, use (N = 16), lastuse (N = 16)
+                const uint32_t id16 = idesc_bf16(M, 16, a_mn != 0, b_mn != 0);
+                mma_bf16_fill(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+                mma_bf16_use(tmem + (uint32_t)N, da, db, id16, ks > 0 ? 1u : 0u);
+                mma_bf16_lastuse(tmem + (uint32_t)N + 16u, da, db, id16, ks > 0 ? 1u : 0u);
             } else {
                 mma_bf16(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
             }
@@ -112,7 +119,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
     tc_fence_after();
     if (ok) {
         const int row = warp * 32 + lane;
-        const int nout = collector == 1 ? 2 * N : (collector == 2 ? N + 16 : N);
+        const int nout = collector == 1 ? 2 * N : (collector == 2 ? N + 16 : (collector == 3 ? N + 32 : N));
         for (int c0 = 0; c0 < nout; c0 += 16) {
             float v[16];
             tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
@@ -157,13 +164,15 @@ bool make_map(CUtensorMap *map, const void *ptr, int rows, int cols) {
 // Returns 0 on success, 1 bad arguments, 2 tensor-map failure, 3 launch failure,
 // 4 a bounded wait ran out.
 extern "C" int tc_probe_mma(const void *a, const void *b, float *d, int N, int K, int a_mn, int b_mn,
-                            int a_manual, int b_manual, int collector, int dcol, int *err_dev) {
+                            int a_manual, int b_manual, int collector, int dcol, int b_off, int *err_dev) {
     const int M = 128;
     if (N < 16 || N > 256 || N % 16 || K < 16 || K > 256 || K % 16) return 1;
-    if (collector < 0 || collector > 2) return 1;
-    if (dcol < 0 || dcol % 16 || dcol + (collector == 1 ? 2 * N : (collector == 2 ? N + 16 : N)) > 512) return 1;
+    if (collector < 0 || collector > 3) return 1;
+    if (b_off < 0 || b_off % 8 || (b_off && (!b_mn || !b_manual || (b_off % 64) + N > 64))) return 1;
+    const int nout = collector == 1 ? 2 * N : (collector == 2 ? N + 16 : (collector == 3 ? N + 32 : N));
+    if (dcol < 0 || dcol % 16 || dcol + nout > 512) return 1;
     const int rows_a = a_mn ? K : M, cols_a = a_mn ? M : K;
-    const int rows_b = b_mn ? K : N, cols_b = b_mn ? N : K;
+    const int rows_b = b_mn ? K : N, cols_b = b_mn ? N + b_off : K;
     if ((!a_manual && cols_a % 64) || (!b_manual && cols_b % 64)) return 1;   // TMA: whole blocks
     if (rows_a % 8 || rows_b % 8) return 1;
     CUtensorMap ma{}, mb{};
@@ -173,7 +182,7 @@ extern "C" int tc_probe_mma(const void *a, const void *b, float *d, int N, int K
         return 3;
     probe_kernel<<<1, 128, kSmemBytes>>>(ma, mb, static_cast<const __nv_bfloat16 *>(a),
                                          static_cast<const __nv_bfloat16 *>(b), d, N, K, a_mn, b_mn, a_manual,
-                                         b_manual, collector, dcol, err_dev);
+                                         b_manual, collector, dcol, b_off, err_dev);
     if (cudaGetLastError() != cudaSuccess) return 3;
     if (cudaDeviceSynchronize() != cudaSuccess) return 3;
     int err = 0;

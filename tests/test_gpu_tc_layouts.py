@@ -28,13 +28,13 @@ def probe():
                        check=True)
     lib = ctypes.CDLL(LIB)
     vp, i = ctypes.c_void_p, ctypes.c_int
-    lib.tc_probe_mma.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
+    lib.tc_probe_mma.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, i, vp]
     lib.tc_probe_mma.restype = i
     return lib
 
 
 CASES = [
-    # N, K, a_mn, b_mn, a_manual, b_manual[, collector, dcol]   (M = 128)
+    # N, K, a_mn, b_mn, a_manual, b_manual[, collector, dcol[, b_off]]   (M = 128)
     (32, 128, 0, 0, 0, 0),     # scores: phi(q) rows x phi(k) rows, 32 keys
     (128, 128, 0, 0, 0, 0),    # scores, 128 keys
     (64, 128, 0, 0, 0, 0),
@@ -55,31 +55,40 @@ CASES = [
     (32, 128, 0, 0, 0, 0, 2, 160),    # A (N = 32) then den (N = 16) from one read of phi(Q)
     (128, 128, 1, 0, 0, 0, 2, 352),   # R (N = 128) then r (N = 16), K-major B
     (128, 128, 0, 1, 0, 0, 2, 224),   # X then a narrower product from one read of g
+    (16, 128, 1, 1, 0, 1, 0, 0, 32),  # gd as a column of the dP tile (MN-major B mid-block)
+    (32, 128, 1, 1, 0, 1, 2, 0, 32),  # the same after a wider product that filled the collector
+    (16, 128, 1, 1, 0, 1, 0, 0, 16),
+    (32, 128, 1, 1, 0, 1, 3, 0),      # dk^T, r and R from one read of phi_s (fill, use, lastuse)
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "N{}_K{}_amn{}_bmn{}_am{}_bm{}".format(*c[:6])
-                         + ("_coll{}_dcol{}".format(*c[6:]) if len(c) > 6 else ""))
+                         + ("_coll{}_dcol{}".format(*c[6:8]) if len(c) > 6 else "")
+                         + ("_boff{}".format(c[8]) if len(c) > 8 else ""))
 def test_mma_layout(probe, case):
     N, K, a_mn, b_mn, a_man, b_man = case[:6]
-    collector, dcol = case[6:] if len(case) > 6 else (0, 0)
+    collector, dcol = case[6:8] if len(case) > 6 else (0, 0)
+    b_off = case[8] if len(case) > 8 else 0
     M = 128
     g = torch.Generator().manual_seed(N * 1000 + K + 7 * a_mn + 13 * b_mn)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)    # logical A (m, k)
-    B = torch.randn(N, K, generator=g).to(torch.bfloat16)    # logical B (n, k)
+    B_all = torch.randn(N + b_off, K, generator=g).to(torch.bfloat16)
+    B = B_all[b_off:]                                        # logical B (n, k)
     a_store = (A.t() if a_mn else A).contiguous().cuda()
-    b_store = (B.t() if b_mn else B).contiguous().cuda()
-    nout = {0: N, 1: 2 * N, 2: N + 16}[collector]
+    b_store = (B_all.t() if b_mn else B).contiguous().cuda()
+    nout = {0: N, 1: 2 * N, 2: N + 16, 3: N + 32}[collector]
     d = torch.full((M, nout), float("nan"), dtype=torch.float32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = probe.tc_probe_mma(a_store.data_ptr(), b_store.data_ptr(), d.data_ptr(), N, K, a_mn, b_mn,
-                            a_man, b_man, collector, dcol, err.data_ptr())
+                            a_man, b_man, collector, dcol, b_off, err.data_ptr())
     assert rc == 0, f"probe returned {rc}"
     want = A.double() @ B.double().t()
     if collector == 1:
         want = torch.cat([want, want], dim=1)
     elif collector == 2:
         want = torch.cat([want, want[:, :16]], dim=1)
+    elif collector == 3:
+        want = torch.cat([want, want[:, :16], want[:, :16]], dim=1)
     got = d.cpu().double()
     assert torch.isfinite(got).all()
     rel = float((got - want).abs().max() / want.abs().max())
