@@ -60,6 +60,11 @@ struct FwdCfg {
     static_assert(T_A + C <= 512, "TMEM budget");
 };
 
+// k_tc_state: warp 0 TMA, warp 1 MMA, warps 4-15 the feature map (all of them on every
+// chunk) and, at the end, warps 4-7 the TMEM readout.
+constexpr int kStateThreads = 512;
+constexpr int kStatePro = kStateThreads - 128;
+
 template <int D>
 struct StateCfg {
     static constexpr int C = 64;
@@ -75,7 +80,7 @@ struct StateCfg {
 // Per-segment state: S = phi(K)^T V and z = phi(K)^T 1 over the segment's tokens (fp32 in
 // TMEM), written to the workspace as [D][D+1] (z in column D).
 template <int D>
-__global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUtensorMap map_k,
+__global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_constant__ CUtensorMap map_k,
                                                      const __grid_constant__ CUtensorMap map_v, Params p) {
     using K = StateCfg<D>;
     constexpr int C = K::C, NS = K::NS;
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
         abort_flag = 0;
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_ready[s], 128);
+            mbar_init(&bar_ready[s], kStatePro);
             mbar_init(&bar_empty[s], 1);
         }
         mbar_init(&bar_done, 1);
@@ -154,7 +159,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
             mbar_drain(&bar_done, 0);
         }
     } else if (warp >= 4) {
-        const int i = threadIdx.x - 128;
+        const int i = threadIdx.x - 128;   // 0 .. kStatePro - 1
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
@@ -162,8 +167,8 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
             if (ok) {
                 uint8_t *kt = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
-#pragma unroll 4
-                for (int idx = i; idx < C * (D / 8); idx += 128) {
+#pragma unroll 2
+                for (int idx = i; idx < C * (D / 8); idx += kStatePro) {
                     const int j = idx / (D / 8), c = idx % (D / 8);
                     uint8_t *ch = kt + swz_chunk(C, j, c);
                     if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 121, smem_u32(ch) - sm_lo, idx))
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(const __grid_constant__ CUt
         ok = ok && warp_wait(&bar_done, 0, &abort_flag);
         tc_fence_after();
         const int wq = warp % 4;
-        if (ok && wq * 32 < D) {
+        if (ok && warp < 8 && wq * 32 < D) {
             const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
             float *row = p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1)) + (size_t)i * (D + 1);
 #pragma unroll 1
@@ -545,7 +550,7 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
     if (e == cudaSuccess) e = prepare(k_tc_state<D>, StateCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     TraceScope ts("tc_seg_state", s);
-    k_tc_state<D><<<p.B * p.Hkv * p.nseg, 256, StateCfg<D>::SMEM, s>>>(mk, mv, p);
+    k_tc_state<D><<<p.B * p.Hkv * p.nseg, kStateThreads, StateCfg<D>::SMEM, s>>>(mk, mv, p);
     return cudaGetLastError();
 }
 
