@@ -267,6 +267,7 @@ def config_of(w: gen.Workload, world: int):
             "causal": w.causal, "phi": w.phi, "eps": w.eps, "cos_sin_weights": w.weights,
             "input_scale": w.scale, "global_batch": w.B * world, "seq_len": w.N,
             "parallelism": f"replicas{world}",
+            "step": "la_fwd, then la_bwd_from_fwd (the backward reads the forward's segment states)",
             "l2": f"no explicit flush: inputs larger than L2 ({path_bytes(w) / 2**20:.0f} MiB moved "
                   f"per step vs {L2_BYTES / 2**20:.0f} MiB L2)"}
 
@@ -323,7 +324,7 @@ def run_ours(args, world, rank, local):
         la.fwd(x["q"], x["k"], x["v"], w.causal, w.phi, w.eps, x["cos_weight"], x["sin_weight"],
                out=out, workspace=ws_f, stream=stream)
         la.bwd(x["q"], x["k"], x["v"], x["grad_out"], w.causal, w.phi, w.eps, x["cos_weight"],
-               x["sin_weight"], dq=dq, dk=dk, dv=dv, workspace=ws_b, stream=stream)
+               x["sin_weight"], dq=dq, dk=dk, dv=dv, workspace=ws_b, stream=stream, fwd_workspace=ws_f)
 
     clocks = ClockSampler(nvsmi_id(dev, local))
     clocks.start()
@@ -390,7 +391,8 @@ def run_ours(args, world, rank, local):
                 la.fwd(x["q"], x["k"], x["v"], w.causal, w.phi, w.eps, x["cos_weight"], x["sin_weight"],
                        out=o["out"], workspace=st["wf"], stream=s_cmp)
                 la.bwd(x["q"], x["k"], x["v"], x["grad_out"], w.causal, w.phi, w.eps, x["cos_weight"],
-                       x["sin_weight"], dq=o["dq"], dk=o["dk"], dv=o["dv"], workspace=st["wb"], stream=s_cmp)
+                       x["sin_weight"], dq=o["dq"], dk=o["dk"], dv=o["dv"], workspace=st["wb"], stream=s_cmp,
+                       fwd_workspace=st["wf"])
                 ev_cmp[i % 2] = torch.cuda.Event()
                 ev_cmp[i % 2].record(s_cmp)
                 s_out.wait_event(ev_cmp[i % 2])

@@ -110,7 +110,7 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
 la_status run(bool bwd, const void *q, const void *k, const void *v, const void *g, void *out,
               void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int D, la_dtype dt,
               int causal, la_phi phi, float eps, const float *cw, const float *sw, void *ws,
-              size_t ws_bytes, void *stream) {
+              size_t ws_bytes, void *stream, const void *fwd_ws = nullptr, size_t fwd_ws_bytes = 0) {
     la_status st = check_shape(B, Hq, Hkv, N, D, dt, phi, eps, cw, sw);
     if (st != LA_OK) return st;
     if (!q || !k || !v) return LA_ERR_ARG;
@@ -136,6 +136,16 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     p.rstate = bwd ? reinterpret_cast<float *>(base + pl.off_rstate) : nullptr;
     p.den = bwd ? reinterpret_cast<float *>(base + pl.off_den) : nullptr;
     p.gd = bwd ? reinterpret_cast<float *>(base + pl.off_gd) : nullptr;
+    if (bwd && fwd_ws) {
+        // the forward's workspace holds its scanned segment states; they are the backward's
+        // when both plans cut the sequence the same way
+        const Plan pf = make_plan(B, Hq, Hkv, N, D, dt, causal, cw != nullptr, 0);
+        if (pf.path == pl.path && pf.chunk == pl.chunk && pf.seg_len == pl.seg_len && pf.nseg == pl.nseg &&
+            pf.P == pl.P && pf.state_elems == pl.state_elems && fwd_ws_bytes >= pf.ws_bytes && aligned(fwd_ws, 256)) {
+            p.state = reinterpret_cast<float *>(const_cast<char *>(static_cast<const char *>(fwd_ws)) + pf.off_state);
+            p.state_given = 1;
+        }
+    }
     cudaError_t e = error_word(&p.err);
     if (e != cudaSuccess) return cuda_fail(e);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -220,6 +230,15 @@ la_status la_bwd(const void *q, const void *k, const void *v, const void *grad_o
                  const float *sin_weight, void *workspace, size_t ws_bytes, void *stream) {
     return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, dtype, is_causal,
                phi, eps, cos_weight, sin_weight, workspace, ws_bytes, stream);
+}
+
+la_status la_bwd_from_fwd(const void *q, const void *k, const void *v, const void *grad_out, void *dq, void *dk,
+                          void *dv, int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal, la_phi phi,
+                          float eps, const float *cos_weight, const float *sin_weight, const void *fwd_workspace,
+                          size_t fwd_ws_bytes, void *workspace, size_t ws_bytes, void *stream) {
+    if (!fwd_workspace) return LA_ERR_ARG;
+    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, dtype, is_causal, phi, eps,
+               cos_weight, sin_weight, workspace, ws_bytes, stream, fwd_workspace, fwd_ws_bytes);
 }
 
 la_status la_get_status(void *stream) {

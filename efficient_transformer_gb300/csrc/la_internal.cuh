@@ -31,6 +31,7 @@ struct Params {
     float eps;
     int chunk, seg_len, nseg;    // work split along the sequence
     float *state;                // per (b, kv head, segment) forward state partials
+    int state_given;             // backward: `state` already holds the scanned forward states
     float *rstate;               // per (b, kv head, segment) backward state partials
     float *den;                  // [B, Hq, N] row denominators (backward)
     float *gd;                   // [B, Hq, N] per-row denominator terms (backward; see each kernel)

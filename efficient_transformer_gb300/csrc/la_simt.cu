@@ -521,8 +521,11 @@ template <typename T, int D, int P>
 cudaError_t backward_impl(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
     const size_t elems = (size_t)P * D * (D + 1);
-    cudaError_t e = launch("simt_seg_state", k_seg_state<T, D, P>, smem_state<D, P>() + (P + 1) * smem_row<D>(), grid, p, s);
-    if (e == cudaSuccess) e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
+    cudaError_t e = cudaSuccess;
+    if (!p.state_given) {
+        e = launch("simt_seg_state", k_seg_state<T, D, P>, smem_state<D, P>() + (P + 1) * smem_row<D>(), grid, p, s);
+        if (e == cudaSuccess) e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
+    }
     if (e == cudaSuccess)
         e = launch("simt_bwd_dq", k_bwd_dq<T, D, P>, smem_state<D, P>() + (2 * P + 3) * smem_row<D>() + 2 * smem_tile(), grid, p, s);
     if (e == cudaSuccess)

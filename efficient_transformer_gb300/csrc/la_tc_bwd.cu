@@ -1105,10 +1105,12 @@ cudaError_t backward_dg(const Params &p, cudaStream_t s) {
     if constexpr (!BwdCfg<D, G>::FITS || !BwdCfg<D, G>::TMEM_FITS) {
         return cudaErrorNotSupported;
     } else {
-        cudaError_t e = tc_launch_state(p, s);
-        if (e == cudaSuccess)
-            e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, (size_t)D * (D + 1), s);
-        if (e != cudaSuccess) return e;
+        if (!p.state_given) {
+            cudaError_t e = tc_launch_state(p, s);
+            if (e == cudaSuccess)
+                e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, (size_t)D * (D + 1), s);
+            if (e != cudaSuccess) return e;
+        }
         return p.causal ? launch_bwd_kernels<D, G, true>(p, s) : launch_bwd_kernels<D, G, false>(p, s);
     }
 }

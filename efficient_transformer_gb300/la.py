@@ -56,6 +56,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.la_fwd.restype = i
     lib.la_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
     lib.la_bwd.restype = i
+    lib.la_bwd_from_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp, sz,
+                                    vp]
+    lib.la_bwd_from_fwd.restype = i
     lib.la_get_status.argtypes = [vp]
     lib.la_get_status.restype = i
     lib.la_status_str.argtypes = [i]
@@ -179,8 +182,13 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tenso
         is_causal: bool = False, phi: str = "elu+1", eps: float = 1e-6,
         cos_weight: torch.Tensor | None = None, sin_weight: torch.Tensor | None = None, *,
         dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
-        dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
-    """Linear-attention backward; returns ``(dq, dk, dv)`` (dk, dv with k's shape)."""
+        dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None,
+        fwd_workspace: torch.Tensor | None = None):
+    """Linear-attention backward; returns ``(dq, dk, dv)`` (dk, dv with k's shape).
+
+    ``fwd_workspace``: the workspace of the ``fwd`` call just made on the same inputs (ordered
+    before this call); its per-segment states are then reused instead of recomputed
+    (``la_bwd_from_fwd``).  The results are the same either way."""
     lib = load()
     B, Hq, Hkv, N, D = _check_inputs(q, k, v, cos_weight, sin_weight, (("grad_out", grad_out),))
     if grad_out.shape != q.shape:
@@ -194,12 +202,23 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tenso
     dt = _dtype_code(q)
     ws = _workspace(lib.la_workspace_size(B, Hq, Hkv, N, D, dt, int(is_causal),
                                           int(cos_weight is not None), 1), q.device, workspace)
-    st = lib.la_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
-                    B, Hq, Hkv, N, D, dt, int(is_causal), _phi_code(phi), float(eps),
-                    _ptr(cos_weight), _ptr(sin_weight), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
-                    _stream_handle(stream))
+    nws = 0 if ws is None else ws.numel() * ws.element_size()
+    if fwd_workspace is None:
+        st = lib.la_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, Hq, Hkv, N, D, dt, int(is_causal), _phi_code(phi), float(eps),
+                        _ptr(cos_weight), _ptr(sin_weight), _ptr(ws), nws, _stream_handle(stream))
+        call = "la_bwd"
+    else:
+        if fwd_workspace.device != q.device:
+            raise ValueError("fwd_workspace must be on q's device")
+        st = lib.la_bwd_from_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 B, Hq, Hkv, N, D, dt, int(is_causal), _phi_code(phi), float(eps),
+                                 _ptr(cos_weight), _ptr(sin_weight), _ptr(fwd_workspace),
+                                 fwd_workspace.numel() * fwd_workspace.element_size(), _ptr(ws), nws,
+                                 _stream_handle(stream))
+        call = "la_bwd_from_fwd"
     if st != LA_OK:
-        _raise(lib, st, "la_bwd")
+        _raise(lib, st, call)
     return dq, dk, dv
 
 

@@ -102,6 +102,25 @@ la_status la_bwd(const void *q, const void *k, const void *v, const void *grad_o
                  int is_causal, la_phi phi, float eps, const float *cos_weight,
                  const float *sin_weight, void *workspace, size_t ws_bytes, void *stream);
 
+/* The same backward (same operation, same results) for a caller that has just run la_fwd
+ * on these inputs: fwd_workspace / fwd_ws_bytes are that call's workspace, still holding
+ * what la_fwd left there (its scanned per-segment states S, z).  When the forward and the
+ * backward cut the sequence the same way (the same kernel family, chunk and segments; true
+ * whenever both run on the tensor-core path) the backward reads those states instead of
+ * recomputing them, which saves one pass over k and v; otherwise it recomputes them and
+ * fwd_workspace is not read.  The pages' `bwd` recomputes the forward through autograd;
+ * keeping the forward's states is this library's design.  The caller guarantees that
+ * la_fwd ran with the same q, k, v, sizes, mode, phi and weights, that its workspace was
+ * not written since, and that the forward is ordered before this call (same stream, or an
+ * event).  fwd_workspace is read only.  Errors as la_bwd; LA_ERR_ARG if fwd_workspace is
+ * NULL. */
+la_status la_bwd_from_fwd(const void *q, const void *k, const void *v, const void *grad_out,
+                          void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int D,
+                          la_dtype dtype, int is_causal, la_phi phi, float eps,
+                          const float *cos_weight, const float *sin_weight,
+                          const void *fwd_workspace, size_t fwd_ws_bytes, void *workspace,
+                          size_t ws_bytes, void *stream);
+
 /* Synchronises `stream`, then returns and clears the device-side error word of the
  * current device: LA_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call,
  * LA_ERR_CUDA if the synchronisation failed, else LA_OK. */

@@ -110,3 +110,17 @@ def test_python_binding_rejects_unbuilt_phi():
         la._phi_code("identity")
     with pytest.raises(ValueError):
         la._phi_code("gelu")
+
+
+def test_bwd_from_fwd_argument_errors(lib):
+    """la_bwd_from_fwd checks its arguments like la_bwd, and needs the forward's workspace."""
+    i, f = ctypes.c_int, ctypes.c_float
+    base = [FAKE] * 7 + [i(1), i(4), i(2), i(64), i(64), i(la.LA_BF16), i(1), i(0), f(1e-6), None, None]
+    # no forward workspace
+    assert lib.la_bwd_from_fwd(*(base + [None, ctypes.c_size_t(0), FAKE, ctypes.c_size_t(1 << 30), None])) == la.LA_ERR_ARG
+    # a forward workspace but no backward workspace
+    assert lib.la_bwd_from_fwd(*(base + [FAKE, ctypes.c_size_t(1 << 30), None, ctypes.c_size_t(0), None])) == la.LA_ERR_WORKSPACE
+    # Hq not a multiple of Hkv
+    bad = list(base)
+    bad[8] = i(3)
+    assert lib.la_bwd_from_fwd(*(bad + [FAKE, ctypes.c_size_t(1 << 30), FAKE, ctypes.c_size_t(1 << 30), None])) == la.LA_ERR_ARG

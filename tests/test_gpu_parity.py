@@ -172,3 +172,25 @@ def test_kernel_family(name, fwd_path):
     """The bf16 workloads without position weights run the tcgen05 forward."""
     w = gen.WORKLOADS[name]
     assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, False) == fwd_path
+
+
+# la_bwd_from_fwd reuses the forward's segment states when the two plans agree (and
+# recomputes them otherwise); either way it must give exactly la_bwd's results.
+@pytest.mark.parametrize("shape", [
+    (1, 8, 2, 1000, 128, "bf16", True),     # tensor-core forward and backward: states reused
+    (1, 4, 4, 700, 64, "bf16", False),      # bidirectional, tensor cores
+    (1, 4, 2, 600, 128, "bf16", True),      # tensor-core forward, CUDA-core backward: recomputed
+    (1, 2, 2, 300, 32, "f32", True),        # CUDA-core path: states reused
+], ids=lambda s: "x".join(map(str, s)))
+def test_bwd_from_fwd_matches_bwd(shape):
+    B, Hq, Hkv, N, D, dt, causal = shape
+    w = gen.Workload("ctx", B, Hq, Hkv, N, D, dt, causal, "elu+1", scale=0.5)
+    d = H.to_dev(gen.make_inputs(w, seed=5))
+    ws_f = torch.empty(la.workspace_size(B, Hq, Hkv, N, D, d["q"].dtype, causal, False, False),
+                       dtype=torch.uint8, device="cuda")
+    la.fwd(d["q"], d["k"], d["v"], causal, "elu+1", 1e-6, workspace=ws_f)
+    ref = la.bwd(d["q"], d["k"], d["v"], d["grad_out"], causal, "elu+1", 1e-6)
+    got = la.bwd(d["q"], d["k"], d["v"], d["grad_out"], causal, "elu+1", 1e-6, fwd_workspace=ws_f)
+    la.get_status()
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.equal(a, b), f"{name} differs from la_bwd"
