@@ -168,22 +168,23 @@ __global__ void k_scan(float *X, int nseg, size_t elems, int mode) {
     float *base = X + (size_t)blockIdx.y * nseg * elems + e;
     if (mode == kScanTotal) {
         float acc = 0.f;
-#pragma unroll 8
+#pragma unroll 32
         for (int s = 0; s < nseg; ++s) acc += base[(size_t)s * elems];
         for (int s = 0; s < nseg; ++s) base[(size_t)s * elems] = acc;
         return;
     }
-    // batches of 8 segments: all loads of a batch are issued before its stores
+    // batches of 32 segments (one batch for up to 32 segments per sequence): all loads of a
+    // batch are issued before its stores
     float acc = 0.f;
-    for (int k0 = 0; k0 < nseg; k0 += 8) {
-        float t[8];
+    for (int k0 = 0; k0 < nseg; k0 += 32) {
+        float t[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 32; ++u) {
             const int k = k0 + u, s = (mode == kScanPrefix) ? k : nseg - 1 - k;
             t[u] = k < nseg ? base[(size_t)s * elems] : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 32; ++u) {
             const int k = k0 + u, s = (mode == kScanPrefix) ? k : nseg - 1 - k;
             if (k < nseg) base[(size_t)s * elems] = acc;
             acc += t[u];

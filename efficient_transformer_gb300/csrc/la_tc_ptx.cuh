@@ -140,6 +140,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Bring one box of a 3-D tensor map into L2 (no shared memory, no completion to wait for),
+// so that a later tma_load_3d of the same box finds it there.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // Store one box of a 3-D tensor map from shared memory (bulk-group completion).  The
 // caller commits the group and waits for it before reusing the shared-memory source.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
