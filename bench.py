@@ -262,6 +262,13 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def workload_of(args) -> gen.Workload:
+    w = gen.WORKLOADS[args.workload]
+    if args.seq_len:
+        w = w.with_(name=f"{w.name}@n{args.seq_len}", N=args.seq_len)
+    return w
+
+
 def config_of(w: gen.Workload, world: int):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "D": w.D,
             "causal": w.causal, "phi": w.phi, "eps": w.eps, "cos_sin_weights": w.weights,
@@ -276,7 +283,7 @@ def run_reference(args, world, rank):
     """Reference arm: the float64 oracle as it stands, on the host cores, rank 0 only."""
     if rank != 0:
         return 0
-    w = gen.WORKLOADS[args.workload]
+    w = workload_of(args)
     budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step, whole run ~2.5 min
     tokens = oracle_tokens_for(w, min(10.0, budget))
     for _ in range(args.warmup):
@@ -305,7 +312,7 @@ def run_ours(args, world, rank, local):
         la_build.build()
     barrier(world)
     la.load()
-    w = gen.WORKLOADS[args.workload]
+    w = workload_of(args)
     dev = torch.device("cuda", local)
     host = gen.make_inputs(w, seed=rank)
     d = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
@@ -496,6 +503,8 @@ def main(argv=None):
                     help="approximate length of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="run the workload at this sequence length instead (small cases for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps; the number is not a valid measurement",

@@ -180,10 +180,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
         }
         ok = ok && warp_wait(&bar_done, 0, &abort_flag);
         tc_fence_after();
+        // TMEM rows (lane d: S[d][0..D-1], z[d]) -> shared memory [D][D + 1] floats (the
+        // stages are idle now; stride D + 1 is odd, so a warp's writes hit distinct banks)
         const int wq = warp % 4;
+        float *srow = reinterpret_cast<float *>(stage0);
         if (ok && warp < 8 && wq * 32 < D) {
             const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-            float *row = p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1)) + (size_t)i * (D + 1);
 #pragma unroll 1
             for (int c16 = 0; c16 <= D / 16; ++c16) {
                 float v[16];
@@ -191,15 +193,23 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
                 tmem_wait_regs<16>(v);
                 if (c16 < D / 16) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) row[c16 * 16 + e] = v[e];
+                    for (int e = 0; e < 16; ++e) srow[i * (D + 1) + c16 * 16 + e] = v[e];
                 } else {
-                    row[D] = v[0];
+                    srow[i * (D + 1) + D] = v[0];
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
+    // the segment's D (D + 1) floats are contiguous (and 16-byte aligned) in the workspace:
+    // every thread copies 16-byte pieces
+    if (!abort_flag) {
+        const float4 *src4 = reinterpret_cast<const float4 *>(stage0);
+        float4 *dst4 = reinterpret_cast<float4 *>(p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1)));
+        static_assert(D * (D + 1) % 4 == 0, "whole 16-byte pieces");
+        for (int idx = threadIdx.x; idx < D * (D + 1) / 4; idx += blockDim.x) dst4[idx] = src4[idx];
+    }
     if (warp == 1) tmem_dealloc(tS, 256);
     if (threadIdx.x == 0 && abort_flag) atomicExch(p.err, kErrTimeout);
 }
