@@ -268,8 +268,6 @@ def max_over_ranks(x: float, world: int) -> float:
 MEASURED_TRAFFIC = {
     "tc_bwd_dq_causal": (1353168640 + 527591680,
                          "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
-    "tc_bwd_dkdv_causal": (1369095936 + 250065920,
-                           "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
 }
 
 

@@ -30,7 +30,11 @@
 namespace la {
 namespace {
 
-constexpr int kBwdThreads = 640;
+// Threads per CTA and feature-map threads (warps 4-7 and 16 up): the dq kernel keeps 96
+// registers a thread for its row pool; the dk/dv kernel's pool fits 80 and takes more
+// feature-map warps.
+constexpr int kDqThreads = 640, kDqPro = 256;
+constexpr int kKvThreads = 768, kKvPro = 384;
 
 template <int D, int G>
 struct BwdCfg {
@@ -121,7 +125,7 @@ __device__ __forceinline__ uint4 dq_piece(uint4 u, const float *x, float inv) {
 
 // ---------------------------------------------------------------------------------------
 template <int D, int G, bool CAUSAL>
-__global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_constant__ CUtensorMap map_q,
+__global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_constant__ CUtensorMap map_q,
                                                               const __grid_constant__ CUtensorMap map_k,
                                                               const __grid_constant__ CUtensorMap map_v,
                                                               const __grid_constant__ CUtensorMap map_g,
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bar_fulla[s], 1);
             mbar_init(&bar_fullg[s], 1);
-            mbar_init(&bar_ready[s], 256);
+            mbar_init(&bar_ready[s], kDqPro);
             mbar_init(&bar_empty[s], 1);
             mbar_init(&bar_dqready[s][0], 128);
             mbar_init(&bar_dqready[s][1], 128);
@@ -351,10 +355,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
     } else if ((warp >= 4 && warp < 8) || warp >= 16) {
         // ---------------- phi prologue, in place on phi(Q) and phi(K): both warpgroups share
         // every chunk (16-byte pieces dealt round-robin)
-        const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0..255
+        const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0 .. kDqPro - 1
         // thread pi owns 16-byte column piece c of rows r0, r0 + RPP, ...; RPP is a multiple
         // of 8, so the piece's swizzled position is the same in all of them
-        constexpr int CPR = D / 8, RPP = 256 / CPR;
+        constexpr int CPR = D / 8, RPP = kDqPro / CPR;
         static_assert(RPP % 8 == 0, "rows per pass");
         const int c = pi % CPR, r0 = pi / CPR;
         const uint32_t pos = (uint32_t)(((c & 7) ^ (r0 & 7)) << 4);
@@ -612,7 +616,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dq(const __grid_const
 
 // ---------------------------------------------------------------------------------------
 template <int D, int G, bool CAUSAL>
-__global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dkdv(const __grid_constant__ CUtensorMap map_q,
+__global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_constant__ CUtensorMap map_q,
                                                                 const __grid_constant__ CUtensorMap map_k,
                                                                 const __grid_constant__ CUtensorMap map_v,
                                                                 const __grid_constant__ CUtensorMap map_g,
@@ -659,7 +663,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dkdv(const __grid_con
             mbar_init(&bar_fullq[s], 1);
             mbar_init(&bar_fullg[s], 1);
             mbar_init(&bar_fullkv[s], 1);
-            mbar_init(&bar_ready[s], 256);
+            mbar_init(&bar_ready[s], kKvPro);
             mbar_init(&bar_emptyqg[s], 1);
             mbar_init(&bar_emptykv[s], 1);
             mbar_init(&bar_dkready[s], 128);
@@ -841,13 +845,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dkdv(const __grid_con
     } else if ((warp >= 4 && warp < 8) || warp >= 16) {
         // ---------------- prologue (both warpgroups on every chunk): phi_s = phi(q) / den over
         // the Q tile, phi(K) over the K tile, in place
-        const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0..255
-        constexpr int CPR = D / 8, RPP = 256 / CPR;
+        const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0 .. kKvPro - 1
+        constexpr int CPR = D / 8, RPP = kKvPro / CPR;
         static_assert(RPP % 8 == 0, "rows per pass");
         const int c = pi % CPR, r0 = pi / CPR;
         const uint32_t pos = (uint32_t)(((c & 7) ^ (r0 & 7)) << 4);
         const uint32_t offq = (uint32_t)(c >> 3) * 128u * 128u + pos, offk = (uint32_t)(c >> 3) * C * 128u + pos;
-        constexpr int NR = 128 / RPP;
+        constexpr int NR = (128 + RPP - 1) / RPP;
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
@@ -860,7 +864,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dkdv(const __grid_con
                 for (int n = 0; n < NR; ++n) {
                     const int row = r0 + n * RPP, ti = row % C;
                     const size_t at = (size_t)(bh0 + row / C) * p.N + c0 + ti;
-                    den[n] = (ti < nvalid && LA_CHECK(at < (size_t)p.B * p.Hq * p.N, 423, row, c0)) ? p.den[at] : 1.f;
+                    den[n] = (row < 128 && ti < nvalid && LA_CHECK(at < (size_t)p.B * p.Hq * p.N, 423, row, c0)) ? p.den[at] : 1.f;
                 }
             if (CAUSAL) ok = ok && warp_wait(&bar_fullq[s], (k / NS) & 1, &abort_flag);
             if (pi == 0) LA_TL2(k, 1);
@@ -869,6 +873,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd_dkdv(const __grid_con
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
                     const int row = r0 + n * RPP;
+                    if (row >= 128) break;
                     uint8_t *ch = st + offq + row * 128;
                     if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 421, smem_u32(ch) - sm_lo, row))
                         feat8_scaled_inplace(ch, row % C < nvalid, p.phi, 1.f / den[n]);
@@ -1089,14 +1094,14 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
     {
         TraceScope ts(CAUSAL ? "tc_bwd_dq_causal" : "tc_bwd_dq_bidir", s);
-        k_tc_bwd_dq<D, G, CAUSAL><<<grid, kBwdThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, p);
+        k_tc_bwd_dq<D, G, CAUSAL><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, p);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess)
         e = scan_segments(p.rstate, p, CAUSAL ? kScanSuffix : kScanTotal, (size_t)D * (D + 1), s);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_bwd_dkdv_causal" : "tc_bwd_dkdv_bidir", s);
-    k_tc_bwd_dkdv<D, G, CAUSAL><<<grid, kBwdThreads, K::DKDV_SMEM, s>>>(mq, mk, mv, mg, mdk, mdv, p);
+    k_tc_bwd_dkdv<D, G, CAUSAL><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mq, mk, mv, mg, mdk, mdv, p);
     return cudaGetLastError();
 }
 
