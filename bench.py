@@ -266,8 +266,6 @@ def max_over_ranks(x: float, world: int) -> float:
 # on the benchmark workload, from one ncu capture of the current kernels; a kernel changed
 # since its capture must be removed from this table (its traffic is then reported as null).
 MEASURED_TRAFFIC = {
-    "tc_bwd_dq_causal": (1353168640 + 527591680,
-                         "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
 }
 
 

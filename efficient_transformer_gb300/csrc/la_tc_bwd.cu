@@ -30,10 +30,8 @@
 namespace la {
 namespace {
 
-// Threads per CTA and feature-map threads (warps 4-7 and 16 up): the dq kernel keeps 96
-// registers a thread for its row pool; the dk/dv kernel's pool fits 80 and takes more
-// feature-map warps.
-constexpr int kDqThreads = 640, kDqPro = 256;
+// Threads per CTA (80 registers a thread) and feature-map threads (warps 4-7 and 16-23).
+constexpr int kDqThreads = 768, kDqPro = 384;
 constexpr int kKvThreads = 768, kKvPro = 384;
 
 template <int D, int G>
@@ -466,15 +464,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 }
                 den += p.eps;
                 inv = 1.f / den;
-                // X in 16-column pieces, the next piece loading while this one is used
-                float xb[2][16];
-                tmem_ld16(tX + lane_off + h * HALF, xb[0]);
-#pragma unroll
+                // X in 16-column pieces
+#pragma unroll 1
                 for (int c16 = 0; c16 < HALF / 16; ++c16) {
                     const int col0 = h * HALF + c16 * 16;
-                    float *xv = xb[c16 & 1];
+                    float xv[16];
+                    tmem_ld16(tX + lane_off + col0, xv);
                     tmem_wait_regs<16>(xv);
-                    if (c16 + 1 < HALF / 16) tmem_ld16(tX + lane_off + col0 + 16, xb[(c16 + 1) & 1]);
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8) {
                         uint8_t *ch = st + swz_chunk(128, i, col0 / 8 + q8);
@@ -559,15 +555,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
             tc_fence_after();
             if (i == 0 && h == 0) LA_TL(k, 11);
-            float xb[2][16];
-            if (ok) tmem_ld16(tX + lane_off + h * HALF, xb[0]);
-#pragma unroll
+#pragma unroll 1
             for (int c16 = 0; c16 < HALF / 16; ++c16) {
                 const int col0 = h * HALF + c16 * 16;
-                float *xv = xb[c16 & 1];
+                float xv[16];
                 if (ok) {
+                    tmem_ld16(tX + lane_off + col0, xv);
                     tmem_wait_regs<16>(xv);
-                    if (c16 + 1 < HALF / 16) tmem_ld16(tX + lane_off + col0 + 16, xb[(c16 + 1) & 1]);
                 }
                 if (c16 + 1 == HALF / 16) {   // every column of X is in registers
                     tc_fence_before();
