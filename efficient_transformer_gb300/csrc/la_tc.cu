@@ -30,7 +30,7 @@
 namespace la {
 namespace {
 
-constexpr int kFwdThreads = 640;
+constexpr int kFwdThreads = 768, kFwdPro = 384;   // feature map: warps 4-7 and 16-23
 
 template <int D, int G>
 struct FwdCfg {
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
         abort_flag = 0;
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_ready[s], 128);
+            mbar_init(&bar_ready[s], kFwdPro);
             mbar_init(&bar_empty[s], 1);
         }
         for (int o = 0; o < 2; ++o) {
@@ -363,32 +363,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             mbar_drain(&bar_fin, 0);
         }
     } else if ((warp >= 4 && warp < 8) || warp >= 16) {
-        // ---------------- phi prologue, in place on the swizzled Q and K tiles; two
-        // warpgroups take alternate chunks
-        const int pg = warp >= 16 ? 1 : 0;
-        const int i = threadIdx.x - (pg ? 512 : 128);
+        // ---------------- phi prologue, in place on the swizzled Q and K tiles; all its
+        // warps on every chunk, thread pi owning 16-byte piece c of rows r0, r0 + RPP, ...
+        // (RPP a multiple of 8, so the piece's swizzled position is the same in all of them)
+        const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0 .. kFwdPro - 1
+        const int i = pi;
+        constexpr int CPR = D / 8, RPP = kFwdPro / CPR;
+        static_assert(RPP % 8 == 0, "rows per pass");
+        const int c = pi % CPR, r0 = pi / CPR;
+        const uint32_t pos = (uint32_t)(((c & 7) ^ (r0 & 7)) << 4);
+        const uint32_t offq = (uint32_t)(c >> 3) * 128u * 128u + pos, offk = (uint32_t)(c >> 3) * C * 128u + pos;
         bool ok = true;
-        for (int k = pg; k < nchunk; k += 2) {
+        for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
             ok = ok && warp_wait(&bar_full[s], (k / NS) & 1, &abort_flag);
             if (i == 0) LA_TL(k, 1);
             if (ok) {
                 uint8_t *st = stage0 + s * K::STAGE;
-                const int c0 = t0 + k * C;
-                const bool qvalid = c0 + (i % C) < t1;
+                const int nvalid = t1 - (t0 + k * C);
 #pragma unroll 4
-                for (int c = 0; c < D / 8; ++c) {
-                    uint8_t *ch = st + swz_chunk(128, i, c);
-                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, c))
-                        feat8_inplace2(ch, qvalid, p.phi);
+                for (int row = r0; row < 128; row += RPP) {
+                    uint8_t *ch = st + offq + row * 128;
+                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, row))
+                        feat8_inplace2(ch, row % C < nvalid, p.phi);
                 }
                 if (CAUSAL)
-#pragma unroll 2
-                    for (int idx = i; idx < C * (D / 8); idx += 128) {
-                        const int j = idx / (D / 8), c = idx % (D / 8);
-                        uint8_t *ch = st + OFF_K + swz_chunk(C, j, c);
-                        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 222, smem_u32(ch) - sm_lo, idx))
-                            feat8_inplace2(ch, c0 + j < t1, p.phi);
+                    for (int j = r0; j < C; j += RPP) {
+                        uint8_t *ch = st + OFF_K + offk + j * 128;
+                        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 222, smem_u32(ch) - sm_lo, j))
+                            feat8_inplace2(ch, j < nvalid, p.phi);
                     }
                 fence_proxy_async();
             }
