@@ -370,18 +370,24 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
                 const int nvalid = t1 - c0;   // tokens of this chunk inside the segment
-#pragma unroll 4
-                for (int row = r0; row < 128; row += RPP) {
-                    uint8_t *ch = st + offq + row * 128;
-                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 321, smem_u32(ch) - sm_lo, row))
-                        feat8_inplace2(ch, row % C < nvalid, p.phi);
+                constexpr int NQ = (128 + RPP - 1) / RPP, NK = CAUSAL ? (C + RPP - 1) / RPP : 0;
+                uint8_t *pp[NQ + NK + 1];
+                bool pres[NQ + NK + 1], val[NQ + NK + 1];
+#pragma unroll
+                for (int n = 0; n < NQ; ++n) {
+                    const int row = r0 + n * RPP;
+                    pp[n] = st + offq + row * 128;
+                    pres[n] = row < 128 && LA_CHECK(in_smem(pp[n], 16, sm_lo, sm_hi), 321, smem_u32(pp[n]) - sm_lo, row);
+                    val[n] = row % C < nvalid;
                 }
-                if (CAUSAL)
-                    for (int j = r0; j < C; j += RPP) {
-                        uint8_t *ch = st + OFF_K + offk + j * 128;
-                        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 322, smem_u32(ch) - sm_lo, j))
-                            feat8_inplace2(ch, j < nvalid, p.phi);
-                    }
+#pragma unroll
+                for (int n = 0; n < NK; ++n) {
+                    const int j = r0 + n * RPP;
+                    pp[NQ + n] = st + OFF_K + offk + j * 128;
+                    pres[NQ + n] = j < C && LA_CHECK(in_smem(pp[NQ + n], 16, sm_lo, sm_hi), 322, smem_u32(pp[NQ + n]) - sm_lo, j);
+                    val[NQ + n] = j < nvalid;
+                }
+                feat8_batch<NQ + NK, false>(pp, pres, val, p.phi, nullptr);
                 fence_proxy_async();
             }
             if (pi == 0) LA_TL(k, 2);
@@ -471,12 +477,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     float xv[16];
                     tmem_ld16(tX + lane_off + col0, xv);
                     tmem_wait_regs<16>(xv);
+                    uint8_t *ch[2];
+                    uint4 u[2];
+#pragma unroll
+                    for (int q8 = 0; q8 < 2; ++q8) {   // both loads before either store
+                        ch[q8] = st + swz_chunk(128, i, col0 / 8 + q8);
+                        u[q8] = *reinterpret_cast<const uint4 *>(ch[q8]);
+                    }
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8) {
-                        uint8_t *ch = st + swz_chunk(128, i, col0 / 8 + q8);
-                        if (!LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 331, smem_u32(ch) - sm_lo, col0)) continue;
-                        uint4 u = *reinterpret_cast<uint4 *>(ch);
-                        uint32_t *ui = reinterpret_cast<uint32_t *>(&u);
+                        uint32_t *ui = reinterpret_cast<uint32_t *>(&u[q8]);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float2 f = unpack_bf16x2(ui[q]);
@@ -484,7 +494,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                             acc[q] = fmaf(f.y, xv[q8 * 8 + 2 * q + 1], acc[q]);
                             ui[q] = pack_bf16x2(f.x * inv, f.y * inv);
                         }
-                        *reinterpret_cast<uint4 *>(ch) = u;
+                        if (LA_CHECK(in_smem(ch[q8], 16, sm_lo, sm_hi), 331, smem_u32(ch[q8]) - sm_lo, col0))
+                            *reinterpret_cast<uint4 *>(ch[q8]) = u[q8];
                     }
                 }
                 xch[h * 128 + i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
@@ -568,14 +579,18 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     mbar_arrive_warp(&bar_xfree);
                 }
                 if (!ok) continue;
+                uint8_t *ch[2];
+                uint4 u[2];
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8) {
-                    uint8_t *ch = st + swz_chunk(128, i, col0 / 8 + q8);
-                    if (!LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 341, smem_u32(ch) - sm_lo, q8)) continue;
-                    uint4 *cp = reinterpret_cast<uint4 *>(ch);
-                    *cp = p.phi == LA_PHI_ELU1 ? dq_piece<true>(*cp, xv + q8 * 8, inv)
-                                               : dq_piece<false>(*cp, xv + q8 * 8, inv);
+                for (int q8 = 0; q8 < 2; ++q8) {   // both loads before either store
+                    ch[q8] = st + swz_chunk(128, i, col0 / 8 + q8);
+                    u[q8] = *reinterpret_cast<const uint4 *>(ch[q8]);
                 }
+#pragma unroll
+                for (int q8 = 0; q8 < 2; ++q8)
+                    if (LA_CHECK(in_smem(ch[q8], 16, sm_lo, sm_hi), 341, smem_u32(ch[q8]) - sm_lo, q8))
+                        *reinterpret_cast<uint4 *>(ch[q8]) = p.phi == LA_PHI_ELU1 ? dq_piece<true>(u[q8], xv + q8 * 8, inv)
+                                                                                  : dq_piece<false>(u[q8], xv + q8 * 8, inv);
             }
             fence_proxy_async();
             if (i == 0 && h == 0) LA_TL(k, 12);
@@ -863,22 +878,33 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             if (CAUSAL) ok = ok && warp_wait(&bar_fullq[s], (k / NS) & 1, &abort_flag);
             if (pi == 0) LA_TL2(k, 1);
             uint8_t *st = stage0 + s * K::STAGE;
-            if (ok && CAUSAL)
+            if (ok && CAUSAL) {
+                uint8_t *pp[NR];
+                bool pres[NR], val[NR];
+                float sc[NR];
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
                     const int row = r0 + n * RPP;
-                    if (row >= 128) break;
-                    uint8_t *ch = st + offq + row * 128;
-                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 421, smem_u32(ch) - sm_lo, row))
-                        feat8_scaled_inplace(ch, row % C < nvalid, p.phi, 1.f / den[n]);
+                    pp[n] = st + offq + row * 128;
+                    pres[n] = row < 128 && LA_CHECK(in_smem(pp[n], 16, sm_lo, sm_hi), 421, smem_u32(pp[n]) - sm_lo, row);
+                    val[n] = row % C < nvalid;
+                    sc[n] = 1.f / den[n];
                 }
+                feat8_batch<NR, true>(pp, pres, val, p.phi, sc);
+            }
             ok = ok && warp_wait(&bar_fullkv[s], (k / NS) & 1, &abort_flag);
             if (ok) {
-                for (int j = r0; j < C; j += RPP) {
-                    uint8_t *ch = st + OFF_K + offk + j * 128;
-                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 422, smem_u32(ch) - sm_lo, j))
-                        feat8_inplace2(ch, j < nvalid, p.phi);
+                constexpr int NK = (C + RPP - 1) / RPP;
+                uint8_t *pp[NK];
+                bool pres[NK], val[NK];
+#pragma unroll
+                for (int n = 0; n < NK; ++n) {
+                    const int j = r0 + n * RPP;
+                    pp[n] = st + OFF_K + offk + j * 128;
+                    pres[n] = j < C && LA_CHECK(in_smem(pp[n], 16, sm_lo, sm_hi), 422, smem_u32(pp[n]) - sm_lo, j);
+                    val[n] = j < nvalid;
                 }
+                feat8_batch<NK, false>(pp, pres, val, p.phi, nullptr);
             }
             fence_proxy_async();
             if (pi == 0) LA_TL2(k, 2);
@@ -956,11 +982,14 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     mbar_arrive_warp(&bar_outfree[bb]);
                 }
                 if (!ok || d >= D) continue;
+                float fk[16];   // the column's 16 phi(k) values, all loaded before any store
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    __nv_bfloat16 *x = reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d));
-                    *x = __float2bfloat16_rn(feat_grad_from_feat(__bfloat162float(*x), p.phi) * (v[e] + r_prev));
-                }
+                for (int e = 0; e < 16; ++e)
+                    fk[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)));
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    *reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)) =
+                        __float2bfloat16_rn(feat_grad_from_feat(fk[e], p.phi) * (v[e] + r_prev));
             }
             fence_proxy_async();
             mbar_arrive_warp(&bar_dkready[s]);

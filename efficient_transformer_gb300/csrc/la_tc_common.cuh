@@ -138,6 +138,38 @@ __device__ __forceinline__ void feat8_scaled_inplace(uint8_t *chunk, bool valid,
     *ptr = x;
 }
 
+// phi (scaled by s[n] when SCALED) on up to NB 16-byte pieces in place (piece n exists when
+// present[n]; it becomes zeros when !valid[n], its row being past the end).  Every load is
+// issued before any store: in-place updates through computed addresses would otherwise
+// serialise, the compiler being unable to tell a later load from an earlier store's address.
+template <int NB, bool SCALED>
+__device__ __forceinline__ void feat8_batch(uint8_t *const *ptr, const bool *present, const bool *valid, int phi,
+                                            const float *s) {
+    uint4 x[NB];
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+        x[n] = present[n] && valid[n] ? *reinterpret_cast<const uint4 *>(ptr[n]) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int n = 0; n < NB; ++n) {
+        if (!(present[n] && valid[n])) continue;
+        uint32_t *xi = reinterpret_cast<uint32_t *>(&x[n]);
+        __nv_bfloat162 s2;
+        if (SCALED) s2 = __float2bfloat162_rn(s[n]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t f = feat_bf16x2(xi[q], phi);
+            if (SCALED) {
+                const __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&f), s2);
+                f = *reinterpret_cast<const uint32_t *>(&y);
+            }
+            xi[q] = f;
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+        if (present[n]) *reinterpret_cast<uint4 *>(ptr[n]) = x[n];
+}
+
 // phi applied to 8 bf16 values (16 bytes) in place, or zeros for a row past the end.
 __device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid, int phi) {
     uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
