@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
     const uint32_t sm_lo = smem_u32(smem_raw), sm_hi = sm_lo + K::SMEM;
     (void)sm_lo;
     (void)sm_hi;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int warp = threadIdx.x / 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
     const int t0 = seg * p.seg_len, t1 = min(p.N, t0 + p.seg_len);
     const int nchunk = (t1 - t0 + C - 1) / C;
@@ -120,43 +120,43 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
     const uint32_t tS = tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) {
+        {   // the whole warp, one lane issuing
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
-                if (k >= NS && !mbar_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
+                if (k >= NS && !warp_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
                 if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N, 101, smem_u32(st) - sm_lo, c0)) break;
-                mbar_arrive_expect_tx(&bar_full[s], K::STAGE);
+                mbar_arrive_expect_tx_w(&bar_full[s], K::STAGE);
                 for (int blk = 0; blk < K::DB; ++blk) {
-                    tma_load_3d(st + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
-                    tma_load_3d(st + K::K_BYTES + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
+                    tma_load_3d_w(st + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
+                    tma_load_3d_w(st + K::K_BYTES + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
                 }
                 issued = k + 1;
             }
-            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) mbar_drain(&bar_full[k % NS], (k / NS) & 1);
+            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) warp_drain(&bar_full[k % NS], (k / NS) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        {   // the whole warp, one lane issuing
             constexpr uint32_t idS = idesc_bf16(128, D, true, true);
             constexpr uint32_t idZ = idesc_bf16(128, 16, true, false);
             const uint32_t on = smem_u32(ones);
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
-                if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
+                if (!warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
                 tc_fence_after();
                 const uint32_t ks_ = smem_u32(stage0 + s * K::STAGE), vs_ = ks_ + K::K_BYTES;
                 if (!LA_CHECK(ks_ >= sm_lo && ks_ + (uint32_t)K::STAGE <= sm_hi, 111, ks_ - sm_lo, k)) break;
                 for (int kk = 0; kk < C / 16; ++kk) {
                     const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
-                    mma_bf16(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs_, C, 0, kk), idS, acc);
-                    mma_bf16(tS + D, desc_mnmajor(ks_, C, 0, kk), desc_kmajor(on, 16, 0, kk), idZ, acc);
+                    mma_bf16_w(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs_, C, 0, kk), idS, acc);
+                    mma_bf16_w(tS + D, desc_mnmajor(ks_, C, 0, kk), desc_kmajor(on, 16, 0, kk), idZ, acc);
                 }
-                mma_commit(&bar_empty[s]);
+                mma_commit_w(&bar_empty[s]);
             }
-            mma_commit(&bar_done);
-            mbar_drain(&bar_done, 0);
+            mma_commit_w(&bar_done);
+            warp_drain(&bar_done, 0);
         }
     } else if (warp >= 4) {
         const int i = threadIdx.x - 128;   // 0 .. kStatePro - 1
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
     uint8_t *ones = ztile + K::Z_BYTES;
     uint8_t *obuf = ones + K::ONES_BYTES;
 
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int warp = threadIdx.x / 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int t0 = seg * p.seg_len, t1 = min(p.N, t0 + p.seg_len);
@@ -283,84 +283,104 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
 
     if (warp == 0) {
         // ---------------- TMA producer
-        if (lane == 0) {
+        {   // the whole warp, one lane issuing
             constexpr uint32_t bytes = CAUSAL ? K::STAGE : K::Q_BYTES;
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
-                if (k >= NS && !mbar_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
+                if (k >= NS && !warp_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
                 if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N && bh0 + G <= p.B * p.Hq, 201,
                               smem_u32(st) - sm_lo, c0))
                     break;
                 LA_TL(k, 0);
-                mbar_arrive_expect_tx(&bar_full[s], bytes);
+                mbar_arrive_expect_tx_w(&bar_full[s], bytes);
                 for (int r = 0; r < G; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_full[s], blk * 64, c0, bh0 + r);
+                        tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_full[s], blk * 64, c0, bh0 + r);
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk) {
-                        tma_load_3d(st + OFF_K + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
-                        tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
+                        tma_load_3d_w(st + OFF_K + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
+                        tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
                     }
                 issued = k + 1;
             }
-            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) mbar_drain(&bar_full[k % NS], (k / NS) & 1);
+            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) warp_drain(&bar_full[k % NS], (k / NS) & 1);
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
+        // ---------------- MMA issuer.  Per chunk k: the inter-chunk part of O (with S_bf and z)
+        // and the state update, which the pool then converts for chunk k + 1; once P is ready,
+        // chunk k + 1's scores A (when its feature map is done) and the intra-chunk part of O.
+        // The epilogue turns A into P as soon as O no longer reads the P tile.
+        {   // the whole warp, one lane issuing
             constexpr uint32_t idA = idesc_bf16(128, C, false, false);
             constexpr uint32_t idO = idesc_bf16(128, D, false, true);
             constexpr uint32_t idDen = idesc_bf16(128, 16, false, false);
             constexpr uint32_t idS = idesc_bf16(128, D, true, true);
             constexpr uint32_t idZ = idesc_bf16(128, 16, true, false);
             const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf), zt = smem_u32(ztile), on = smem_u32(ones);
-            for (int k = 0; k < nchunk; ++k) {
+            // A for chunk k (causal), into the single A buffer once chunk k - 1's P has been read
+            auto issue_a = [&](int k) -> bool {
+                const int s = k % NS;
+                if (!warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) return false;
+                LA_TL(k, 3);
+                tc_fence_after();
+                const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K;
+                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi, 212, qs - sm_lo, k)) return false;
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_w(tA, desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                mma_commit_w(&bar_afull);
+                return true;
+            };
+            bool okm = !CAUSAL || nchunk == 0 || issue_a(0);
+            for (int k = 0; okm && k < nchunk; ++k) {
                 const int s = k % NS, o = k % NO;
                 const uint32_t tO = o ? tO1 : tO0;
-                if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
-                LA_TL(k, 3);
+                if (!CAUSAL && !warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
+                if ((CAUSAL || k == 0) && !warp_wait(&bar_sbf, k & 1, &abort_flag)) break;
+                LA_TL(k, 5);
+                if (k >= NO && !warp_wait(&bar_ofree[o], ((k / NO) - 1) & 1, &abort_flag)) break;
+                LA_TL(k, 6);
                 tc_fence_after();
                 const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V;
                 if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && smem_u32(obuf) + K::OUT_BYTES <= sm_hi, 211,
                               qs - sm_lo, k))
                     break;
-                if (CAUSAL) {
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_bf16(tA, desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
-                    mma_commit(&bar_afull);
-                    if (!mbar_wait(&bar_pready, k & 1, &abort_flag)) break;
-                }
-                LA_TL(k, 4);
-                if ((CAUSAL || k == 0) && !mbar_wait(&bar_sbf, k & 1, &abort_flag)) break;
-                LA_TL(k, 5);
-                if (k >= NO && !mbar_wait(&bar_ofree[o], ((k / NO) - 1) & 1, &abort_flag)) break;
-                LA_TL(k, 6);
-                tc_fence_after();
+                // O = phi(Q) S_bf^T, den = phi(Q) z (the state before this chunk)
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    mma_bf16(tO, desc_kmajor(qs, 128, 0, kk), desc_mnmajor(sbf_u, D, 0, kk), idO, kk > 0 ? 1u : 0u);
-                    mma_bf16(tO + D, desc_kmajor(qs, 128, 0, kk), desc_kmajor(zt, 16, 0, kk), idDen, kk > 0 ? 1u : 0u);
+                    mma_bf16_w(tO, desc_kmajor(qs, 128, 0, kk), desc_mnmajor(sbf_u, D, 0, kk), idO, kk > 0 ? 1u : 0u);
+                    mma_bf16_w(tO + D, desc_kmajor(qs, 128, 0, kk), desc_kmajor(zt, 16, 0, kk), idDen, kk > 0 ? 1u : 0u);
                 }
-                if (CAUSAL)
-                    for (int kk = 0; kk < C / 16; ++kk) {
-                        mma_bf16(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(vs, C, 0, kk), idO, 1u);
-                        mma_bf16(tO + D, desc_kmajor(pb, 128, 0, kk), desc_kmajor(on, 16, 0, kk), idDen, 1u);
-                    }
-                mma_commit(&bar_ofull[o]);
+                bool a_next = false;
                 if (CAUSAL) {
+                    // S += phi(K)^T V, z += phi(K)^T 1; the commit also covers the reads of S_bf and z
                     for (int kk = 0; kk < C / 16; ++kk) {
-                        mma_bf16(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs, C, 0, kk), idS, 1u);
-                        mma_bf16(tS + D, desc_mnmajor(ks_, C, 0, kk), desc_kmajor(on, 16, 0, kk), idZ, 1u);
+                        mma_bf16_w(tS, desc_mnmajor(ks_, C, 0, kk), desc_mnmajor(vs, C, 0, kk), idS, 1u);
+                        mma_bf16_w(tS + D, desc_mnmajor(ks_, C, 0, kk), desc_kmajor(on, 16, 0, kk), idZ, 1u);
                     }
-                    mma_commit(&bar_sfull);
+                    mma_commit_w(&bar_sfull);
+                    if (!warp_wait(&bar_pready, k & 1, &abort_flag)) break;
+                    LA_TL(k, 4);
+                    tc_fence_after();
+                    // chunk k + 1's scores go first when its feature map is ready (A is free now)
+                    if (k + 1 < nchunk && warp_test(&bar_ready[(k + 1) % NS], ((k + 1) / NS) & 1)) {
+                        if (!issue_a(k + 1)) break;
+                        a_next = true;
+                    }
+                    // O += P V, den += P 1 (within the chunk)
+                    for (int kk = 0; kk < C / 16; ++kk) {
+                        mma_bf16_w(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(vs, C, 0, kk), idO, 1u);
+                        mma_bf16_w(tO + D, desc_kmajor(pb, 128, 0, kk), desc_kmajor(on, 16, 0, kk), idDen, 1u);
+                    }
                 }
-                mma_commit(&bar_empty[s]);
+                mma_commit_w(&bar_ofull[o]);
+                mma_commit_w(&bar_empty[s]);
                 LA_TL(k, 7);
+                if (CAUSAL && k + 1 < nchunk && !a_next && !issue_a(k + 1)) break;
             }
-            mma_commit(&bar_fin);
-            mbar_drain(&bar_fin, 0);
+            mma_commit_w(&bar_fin);
+            warp_drain(&bar_fin, 0);
         }
     } else if ((warp >= 4 && warp < 8) || warp >= 16) {
         // ---------------- phi prologue, in place on the swizzled Q and K tiles; all its
@@ -399,7 +419,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             mbar_arrive_warp(&bar_ready[s]);
         }
     } else if (warp >= 8 && warp < 12) {
-        // ---------------- state conversion (thread = d) and P conversion (thread = row i)
+        // ---------------- state conversion (thread = d) and P conversion (thread = query row
+        // i): S, z after chunk k for chunk k + 1, then P = mask(A) for chunk k + 1 as soon as
+        // chunk k's O products (the readers of the P tile) are done
         const int i = threadIdx.x - 256;
         const int wq = warp % 4;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -430,8 +452,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
         mbar_arrive_warp(&bar_sbf);
         if (CAUSAL) {
             bool ok = true;
-            for (int k = 0; k < nchunk; ++k) {
-                // P for chunk k
+            auto p_conv = [&](int k) {
                 ok = ok && warp_wait(&bar_afull, k & 1, &abort_flag);
                 tc_fence_after();
                 if (i == 0) LA_TL(k, 8);
@@ -451,8 +472,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 const int j = c32 * 32 + h * 16 + e;
-                                w[e / 2] = pack_bf16x2((j <= ti) ? v[h * 16 + e] : 0.f,
-                                                       (j + 1 <= ti) ? v[h * 16 + e + 1] : 0.f);
+                                w[e / 2] = pack_bf16x2((j <= ti) ? v[h * 16 + e] : 0.f, (j + 1 <= ti) ? v[h * 16 + e + 1] : 0.f);
                             }
                             const int c16 = c32 * 2 + h;
                             uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
@@ -468,6 +488,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 tc_fence_before();
                 if (i == 0) LA_TL(k, 9);
                 mbar_arrive_warp(&bar_pready);
+            };
+            if (nchunk > 0) p_conv(0);
+            for (int k = 0; k < nchunk; ++k) {
                 // S, z after chunk k -> operand tiles for chunk k + 1
                 ok = ok && warp_wait(&bar_sfull, k & 1, &abort_flag);
                 tc_fence_after();
@@ -490,6 +513,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 tc_fence_before();
                 if (i == 0) LA_TL(k, 11);
                 mbar_arrive_warp(&bar_sbf);
+                if (k + 1 < nchunk) {
+                    ok = ok && warp_wait(&bar_ofull[k % NO], (k / NO) & 1, &abort_flag);
+                    p_conv(k + 1);
+                }
             }
         }
     } else if (warp >= 12 && warp < 16) {
@@ -511,32 +538,41 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 den = tmem_ld1(tO + lane_off + D);
                 tmem_wait_regs<1>(&den);
             }
-#pragma unroll
+            const float inv = 1.f / (den + p.eps);
+#pragma unroll 1
             for (int c64 = 0; c64 < D / 64; ++c64) {
-                float v[64];
+                float v[32];   // 32 columns at a time
                 if (ok) {
                     tmem_ld32(tO + lane_off + c64 * 64, v);
-                    tmem_ld32(tO + lane_off + c64 * 64 + 32, v + 32);
-                    tmem_wait_regs<64>(v);
+                    tmem_wait_regs<32>(v);
                 }
-                if (i == 0) bulk_wait_read();   // previous stores have read the staging tile
+                if (i < 32) {   // previous stores (lane 0's) have read the staging tile
+                    bulk_wait_read();
+                    __syncwarp();
+                }
                 named_barrier(2, 128);
-                if (ok) {
-                    const float inv = 1.f / (den + p.eps);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        uint4 w;
-                        w.x = pack_bf16x2(v[8 * q + 0] * inv, v[8 * q + 1] * inv);
-                        w.y = pack_bf16x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv);
-                        w.z = pack_bf16x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv);
-                        w.w = pack_bf16x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv);
-                        *reinterpret_cast<uint4 *>(obuf + swz_chunk(128, i, q)) = w;
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (ok && hh == 1) {
+                        tmem_ld32(tO + lane_off + c64 * 64 + 32, v);
+                        tmem_wait_regs<32>(v);
+                    }
+                    if (ok) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w;
+                            w.x = pack_bf16x2(v[8 * q + 0] * inv, v[8 * q + 1] * inv);
+                            w.y = pack_bf16x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv);
+                            w.z = pack_bf16x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv);
+                            w.w = pack_bf16x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv);
+                            *reinterpret_cast<uint4 *>(obuf + swz_chunk(128, i, hh * 4 + q)) = w;
+                        }
                     }
                 }
                 fence_proxy_async();
                 named_barrier(2, 128);
-                if (i == 0 && ok) {
-                    for (int r = 0; r < G; ++r) tma_store_3d(&map_o, obuf + r * C * 128, c64 * 64, c0, bh0 + r);
+                if (i < 32 && ok) {   // the first warp, lane 0 issuing
+                    for (int r = 0; r < G; ++r) tma_store_3d_w(&map_o, obuf + r * C * 128, c64 * 64, c0, bh0 + r);
                     bulk_commit();
                 }
             }
@@ -544,7 +580,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             if (i == 0) LA_TL(k, 13);
             mbar_arrive_warp(&bar_ofree[o]);
         }
-        if (i == 0) bulk_wait_all();
+        if (i < 32) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();

@@ -62,10 +62,16 @@ struct BwdCfg {
     static constexpr int NS = 3 * STAGE + KV_FIXED <= kSmemLimit - 512 ? 3 : 2;
     static constexpr int DKDV_SMEM = NS * STAGE + KV_FIXED;
     static constexpr bool FITS = DQ_SMEM <= kSmemLimit - 512 && DKDV_SMEM <= kSmemLimit - 512;
-    // dk/dv kernel TMEM columns: [R | r], then NB_KV buffers of [A_s then dk^T | dA' then dv^T]
+    // dk/dv kernel TMEM columns: R, then NB_KV buffers of [A_s | dA' | dk^T | r part | dv^T]
+    // when dk^T and dv^T fit in columns of their own (KV_SEP), else of
+    // [A_s then dk^T | dA' then dv^T | r part]; the r part (16 columns) takes phi_s^T h
     static constexpr int KT_R = 0;
-    static constexpr int KT_AD = D + 16;
-    static constexpr int NB_KV = KT_AD + 4 * C <= 512 ? 2 : 1;
+    static constexpr int KT_AD = D;
+    static constexpr bool KV_SEP = KT_AD + 4 * C + 16 <= 512;
+    static constexpr int KV_BW = KV_SEP ? 4 * C + 16 : 2 * C + 16;
+    static constexpr int NB_KV = KT_AD + 2 * KV_BW <= 512 ? 2 : 1;
+    // phi_s^T h rides on the dk^T product as 16 extra columns of dP' (h in dP')
+    static constexpr bool MERGE_H = KV_SEP && H_IN_DP;
     // dq kernel TMEM columns: [S | z], den, A, dA', X (then den * da - h z), [R | r]
     static constexpr int T_S = 0;
     static constexpr int T_DEN = D + 16;
@@ -73,7 +79,7 @@ struct BwdCfg {
     static constexpr int T_A2 = T_A + C;
     static constexpr int T_X = T_A2 + C;
     static constexpr int T_R = T_X + D;
-    static constexpr bool TMEM_FITS = T_R + D + 16 <= 512 && KT_AD + 2 * C <= 512;
+    static constexpr bool TMEM_FITS = T_R + D + 16 <= 512 && KT_AD + KV_BW <= 512;
     static_assert(T_S == 0 && KT_R == 0, "S (dq kernel) and R (dk/dv kernel) start the TMEM allocation");
     static_assert(NB_KV == 1 || NB_KV == 2, "one or two dk/dv TMEM buffers");
 };
@@ -200,46 +206,46 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     if (warp == 0) {
         // ---------------- TMA producer: K and Q (what the feature map needs) on one barrier,
         // V and grad_out on another
-        if (lane == 0) {
+        {   // the whole warp, one lane issuing
             constexpr uint32_t bytes_a = CAUSAL ? K::Q_BYTES + K::K_BYTES : K::Q_BYTES;
             constexpr uint32_t bytes_g = CAUSAL ? K::V_BYTES + K::G_BYTES : K::G_BYTES;
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
-                if (k >= NS && !mbar_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
+                if (k >= NS && !warp_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
                 if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N && bh0 + G <= p.B * p.Hq, 301,
                               smem_u32(st) - sm_lo, c0))
                     break;
                 LA_TL(k, 0);
-                mbar_arrive_expect_tx(&bar_fulla[s], bytes_a);
+                mbar_arrive_expect_tx_w(&bar_fulla[s], bytes_a);
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d(st + OFF_K + blk * C * 128, &map_k, &bar_fulla[s], blk * 64, c0, bg);
+                        tma_load_3d_w(st + OFF_K + blk * C * 128, &map_k, &bar_fulla[s], blk * 64, c0, bg);
                 for (int r = 0; r < G; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fulla[s], blk * 64, c0, bh0 + r);
-                mbar_arrive_expect_tx(&bar_fullg[s], bytes_g);
+                        tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fulla[s], blk * 64, c0, bh0 + r);
+                mbar_arrive_expect_tx_w(&bar_fullg[s], bytes_g);
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_fullg[s], blk * 64, c0, bg);
+                        tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fullg[s], blk * 64, c0, bg);
                 for (int r = 0; r < G; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64, c0,
+                        tma_load_3d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64, c0,
                                     bh0 + r);
                 issued = k + 1;
             }
             for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) {
-                mbar_drain(&bar_fulla[k % NS], (k / NS) & 1);
-                mbar_drain(&bar_fullg[k % NS], (k / NS) & 1);
+                warp_drain(&bar_fulla[k % NS], (k / NS) & 1);
+                warp_drain(&bar_fullg[k % NS], (k / NS) & 1);
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer.  Iteration k finishes chunk k - 1 (da, R, r) and
         // starts chunk k (A, den, X, dA', then the state update).  Products that share an
         // A operand are issued back to back so that A is read from shared memory once.
-        if (lane == 0) {
+        {   // the whole warp, one lane issuing
             constexpr uint32_t idA = idesc_bf16(128, C, false, false);
             constexpr uint32_t idX = idesc_bf16(128, D, false, false);
             constexpr uint32_t idDK = idesc_bf16(128, D, false, true);
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             for (int k = 0; k <= nchunk; ++k) {
                 if (k > 0) {
                     const int kp = k - 1, sp = kp % NS;
-                    if (!mbar_wait(&bar_gnready, kp & 1, &abort_flag)) break;
+                    if (!warp_wait(&bar_gnready, kp & 1, &abort_flag)) break;
                     LA_TL(kp, 5);
                     tc_fence_after();
                     const uint32_t qs = smem_u32(stage0 + sp * K::STAGE), ks_ = qs + OFF_K, gs = qs + OFF_G;
@@ -259,22 +265,22 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     const uint32_t zt = smem_u32(ztile + (CAUSAL ? (kp & 1) : 0) * K::Z_BYTES);
                     if (CAUSAL)
                         for (int kk = 0; kk < C / 16; ++kk)
-                            mma_bf16(tX, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(ks_, C, 0, kk), idDK, 1u);
-                    mma_bf16(tX, desc_mnmajor(ht, 16, 0, 0), desc_mnmajor(zt, 16, 0, 0), idHZ, 1u);
+                            mma_bf16_w(tX, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(ks_, C, 0, kk), idDK, 1u);
+                    mma_bf16_w(tX, desc_mnmajor(ht, 16, 0, 0), desc_mnmajor(zt, 16, 0, 0), idHZ, 1u);
                     // R += phi_s^T g, r += phi_s^T h  (phi_s = phi(Q) / den)
                     for (int kk = 0; kk < 128 / 16; ++kk) {
                         const uint32_t acc = (kp > 0 || kk > 0) ? 1u : 0u;
                         const uint64_t as = desc_mnmajor(qs, 128, 0, kk);
-                        mma_bf16_fill(tR, as, desc_mnmajor(gs, 128, 0, kk), idR, acc);
-                        mma_bf16_lastuse(tR + D, as, desc_kmajor(ht, 16, 0, kk), idR16, acc);
+                        mma_bf16_fill_w(tR, as, desc_mnmajor(gs, 128, 0, kk), idR, acc);
+                        mma_bf16_lastuse_w(tR + D, as, desc_kmajor(ht, 16, 0, kk), idR16, acc);
                     }
-                    mma_commit(&bar_dqfull);
+                    mma_commit_w(&bar_dqfull);
                 }
                 if (k == nchunk) break;
                 const int s = k % NS;
-                if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
-                if (!mbar_wait(&bar_fullg[s], (k / NS) & 1, &abort_flag)) break;
-                if ((CAUSAL || k == 0) && !mbar_wait(&bar_sbf, k & 1, &abort_flag)) break;
+                if (!warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) break;
+                if (!warp_wait(&bar_fullg[s], (k / NS) & 1, &abort_flag)) break;
+                if ((CAUSAL || k == 0) && !warp_wait(&bar_sbf, k & 1, &abort_flag)) break;
                 LA_TL(k, 3);
                 tc_fence_after();
                 const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V, gs = qs + OFF_G;
@@ -285,44 +291,44 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t aq = desc_kmajor(qs, 128, 0, kk);
                     if (CAUSAL) {
-                        mma_bf16_fill(tA, aq, desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
-                        mma_bf16_lastuse(tDen, aq, desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
+                        mma_bf16_fill_w(tA, aq, desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                        mma_bf16_lastuse_w(tDen, aq, desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
                     } else {
-                        mma_bf16(tDen, aq, desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
+                        mma_bf16_w(tDen, aq, desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
                     }
                 }
-                if (k > 0 && !mbar_wait(&bar_xfree, (k - 1) & 1, &abort_flag)) break;
+                if (k > 0 && !warp_wait(&bar_xfree, (k - 1) & 1, &abort_flag)) break;
                 LA_TL(k, 4);
                 tc_fence_after();
                 // X = g S_bf^T and dA' = g V^T share g
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t ag = desc_kmajor(gs, 128, 0, kk);
                     if (CAUSAL) {
-                        mma_bf16_fill(tX, ag, desc_kmajor(sbf_u, D, 0, kk), idX, kk > 0 ? 1u : 0u);
-                        mma_bf16_lastuse(tA2, ag, desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                        mma_bf16_fill_w(tX, ag, desc_kmajor(sbf_u, D, 0, kk), idX, kk > 0 ? 1u : 0u);
+                        mma_bf16_lastuse_w(tA2, ag, desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : 0u);
                     } else {
-                        mma_bf16(tX, ag, desc_kmajor(sbf_u, D, 0, kk), idX, kk > 0 ? 1u : 0u);
+                        mma_bf16_w(tX, ag, desc_kmajor(sbf_u, D, 0, kk), idX, kk > 0 ? 1u : 0u);
                     }
                 }
-                mma_commit(&bar_mfull);
+                mma_commit_w(&bar_mfull);
                 if (CAUSAL) {   // S += phi(K)^T V, z += phi(K)^T 1 (one read of phi(K))
                     for (int kk = 0; kk < C / 16; ++kk) {
                         const uint64_t ak = desc_mnmajor(ks_, C, 0, kk);
-                        mma_bf16_fill(tS, ak, desc_mnmajor(vs, C, 0, kk), idR, 1u);
-                        mma_bf16_lastuse(tS + D, ak, desc_kmajor(on, 16, 0, kk), idR16, 1u);
+                        mma_bf16_fill_w(tS, ak, desc_mnmajor(vs, C, 0, kk), idR, 1u);
+                        mma_bf16_lastuse_w(tS + D, ak, desc_kmajor(on, 16, 0, kk), idR16, 1u);
                     }
-                    mma_commit(&bar_sfull);
+                    mma_commit_w(&bar_sfull);
                 }
                 LA_TL(k, 6);
             }
-            mma_commit(&bar_fin);
-            mbar_drain(&bar_fin, 0);
+            mma_commit_w(&bar_fin);
+            warp_drain(&bar_fin, 0);
         }
     } else if (warp == 2) {
         // ---------------- dq store: each pool half leaves its D/2 columns of dq over the
         // phi_s tile; TMA writes them out, and the stage is released once the copies have
         // read it
-        if (lane == 0) {
+        {   // the whole warp, one lane issuing
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 uint8_t *st = stage0 + s * K::STAGE;
@@ -331,13 +337,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 // with D = 128 each half is one 64-column block and goes out on its own;
                 // with D = 64 both halves share the block
                 for (int hh = 0; hh < 2; ++hh) {
-                    ok = ok && mbar_wait(&bar_dqready[s][hh], (k / NS) & 1, &abort_flag);
+                    ok = ok && warp_wait(&bar_dqready[s][hh], (k / NS) & 1, &abort_flag);
                     if (!ok) break;
                     if (hh == 0) LA_TL(k, 13);
                     if (K::DB == 2 || hh == 1) {
                         const int blk = K::DB == 2 ? hh : 0;
                         for (int r = 0; r < G; ++r)
-                            tma_store_3d(&map_dq, st + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
+                            tma_store_3d_w(&map_dq, st + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
                     }
                 }
                 if (ok) {
@@ -345,7 +351,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     bulk_wait_read();
                     LA_TL(k, 14);
                 }
-                mbar_arrive(&bar_empty[s]);
+                mbar_arrive_w(&bar_empty[s]);
                 if (!ok) break;
             }
             bulk_wait_all();
@@ -641,7 +647,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     __shared__ uint64_t bar_fullq[NS], bar_fullg[NS], bar_fullkv[NS], bar_ready[NS], bar_emptyqg[NS],
         bar_emptykv[NS], bar_dkready[NS], bar_dvready[NS];
     __shared__ uint64_t bar_afull[2], bar_outfull[2], bar_outfree[2];
-    __shared__ uint64_t bar_pready, bar_rbf, bar_fin;
+    __shared__ uint64_t bar_pready, bar_rbf, bar_rfull, bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
@@ -683,9 +689,10 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
         mbar_init(&bar_pready, 128);
         for (int bb = 0; bb < 2; ++bb) {
             mbar_init(&bar_outfull[bb], 1);
-            mbar_init(&bar_outfree[bb], 256);
+            mbar_init(&bar_outfree[bb], 128);
         }
         mbar_init(&bar_rbf, 128);
+        mbar_init(&bar_rfull, 1);
         mbar_init(&bar_fin, 1);
         fence_barrier_init();
     }
@@ -696,160 +703,239 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // TMEM: [R | r (two columns: phi_s^T h_hi, phi_s^T h_lo)], then per buffer b:
-    // tA[b] = A_s then dk^T, tD[b] = dA' then dv^T (C columns each)
-    const uint32_t tR = tmem_base + K::KT_R, tAD = tmem_base + K::KT_AD;
-    auto tA = [=](int bb) { return tAD + (uint32_t)(bb * 2 * C); };
-    auto tD = [=](int bb) { return tAD + (uint32_t)(bb * 2 * C + C); };
+    // TMEM: R, then per buffer bb the scores A_s (tA), dA' (tD), the outputs dk^T (tK), dv^T
+    // (tV) and the r part phi_s^T [h_hi h_lo] (tRp, two of 16 columns).  With KV_SEP the
+    // outputs have columns of their own and tRp follows dk^T; otherwise dk^T overwrites A_s
+    // and dv^T overwrites dA'.
+    constexpr bool SEP = K::KV_SEP, MERGE_H = K::MERGE_H;
+    const uint32_t tR = tmem_base + K::KT_R;
+    auto tBuf = [=](int bb) { return tmem_base + (uint32_t)(K::KT_AD + bb * K::KV_BW); };
+    auto tA = [=](int bb) { return tBuf(bb); };
+    auto tD = [=](int bb) { return tBuf(bb) + (uint32_t)C; };
+    auto tK = [=](int bb) { return tBuf(bb) + (uint32_t)(SEP ? 2 * C : 0); };
+    auto tRp = [=](int bb) { return tBuf(bb) + (uint32_t)(SEP ? 3 * C : 2 * C); };
+    auto tV = [=](int bb) { return tBuf(bb) + (uint32_t)(SEP ? 3 * C + 16 : C); };
 
     if (warp == 0) {
         // ---------------- TMA producer (chunks in reverse order)
-        if (lane == 0) {
+        {   // the whole warp, one lane issuing
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + (nchunk - 1 - k) * C;
                 if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N, 401, smem_u32(st) - sm_lo, c0)) break;
-                if (CAUSAL && k >= NS && !mbar_wait(&bar_emptyqg[s], ((k / NS) - 1) & 1, &abort_flag)) break;
+                if (CAUSAL && k >= NS && !warp_wait(&bar_emptyqg[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 LA_TL2(k, 0);
                 if (CAUSAL) {
-                    mbar_arrive_expect_tx(&bar_fullq[s], K::Q_BYTES);
+                    mbar_arrive_expect_tx_w(&bar_fullq[s], K::Q_BYTES);
                     for (int r = 0; r < G; ++r)
                         for (int blk = 0; blk < K::DB; ++blk)
-                            tma_load_3d(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fullq[s], blk * 64, c0,
+                            tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fullq[s], blk * 64, c0,
                                         bh0 + r);
-                    mbar_arrive_expect_tx(&bar_fullg[s], K::G_BYTES);
+                    mbar_arrive_expect_tx_w(&bar_fullg[s], K::G_BYTES);
                     for (int r = 0; r < G; ++r)
                         for (int blk = 0; blk < K::DB; ++blk)
-                            tma_load_3d(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64,
+                            tma_load_3d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64,
                                         c0, bh0 + r);
                 }
-                if (k >= NS && !mbar_wait(&bar_emptykv[s], ((k / NS) - 1) & 1, &abort_flag)) break;
-                mbar_arrive_expect_tx(&bar_fullkv[s], K::K_BYTES + K::V_BYTES);
+                if (k >= NS && !warp_wait(&bar_emptykv[s], ((k / NS) - 1) & 1, &abort_flag)) break;
+                mbar_arrive_expect_tx_w(&bar_fullkv[s], K::K_BYTES + K::V_BYTES);
                 for (int blk = 0; blk < K::DB; ++blk) {
-                    tma_load_3d(st + OFF_K + blk * C * 128, &map_k, &bar_fullkv[s], blk * 64, c0, bg);
-                    tma_load_3d(st + OFF_V + blk * C * 128, &map_v, &bar_fullkv[s], blk * 64, c0, bg);
+                    tma_load_3d_w(st + OFF_K + blk * C * 128, &map_k, &bar_fullkv[s], blk * 64, c0, bg);
+                    tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fullkv[s], blk * 64, c0, bg);
                 }
                 issued = k + 1;
             }
             // a chunk whose K, V wait gave up has Q and g in flight: wait for those too
             for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) {
                 if (CAUSAL) {
-                    mbar_drain(&bar_fullq[k % NS], (k / NS) & 1);
-                    mbar_drain(&bar_fullg[k % NS], (k / NS) & 1);
+                    warp_drain(&bar_fullq[k % NS], (k / NS) & 1);
+                    warp_drain(&bar_fullg[k % NS], (k / NS) & 1);
                 }
-                mbar_drain(&bar_fullkv[k % NS], (k / NS) & 1);
+                warp_drain(&bar_fullkv[k % NS], (k / NS) & 1);
             }
             if (issued < nchunk && CAUSAL) {
                 const int k = issued;
-                mbar_drain(&bar_fullq[k % NS], (k / NS) & 1);
-                mbar_drain(&bar_fullg[k % NS], (k / NS) & 1);
+                warp_drain(&bar_fullq[k % NS], (k / NS) & 1);
+                warp_drain(&bar_fullg[k % NS], (k / NS) & 1);
             }
         }
     } else if (warp == 2) {
         // ---------------- dk, dv stores: TMA writes the two tiles left over phi(K) and V,
         // and the [K | V] region is released once the copies have read it
-        if (lane == 0) {
+        {   // the whole warp, one lane issuing
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + (nchunk - 1 - k) * C;
-                const bool ok = mbar_wait(&bar_dkready[s], (k / NS) & 1, &abort_flag) &&
-                                mbar_wait(&bar_dvready[s], (k / NS) & 1, &abort_flag);
+                bool ok = warp_wait(&bar_dkready[s], (k / NS) & 1, &abort_flag);
                 if (ok) {
                     LA_TL2(k, 12);
-                    for (int blk = 0; blk < K::DB; ++blk) {
-                        tma_store_3d(&map_dk, st + OFF_K + blk * C * 128, blk * 64, c0, bg);
-                        tma_store_3d(&map_dv, st + OFF_V + blk * C * 128, blk * 64, c0, bg);
-                    }
+                    for (int blk = 0; blk < K::DB; ++blk) tma_store_3d_w(&map_dk, st + OFF_K + blk * C * 128, blk * 64, c0, bg);
                     bulk_commit();
-                    bulk_wait_read();
-                    LA_TL2(k, 13);
                 }
-                mbar_arrive(&bar_emptykv[s]);
+                ok = ok && warp_wait(&bar_dvready[s], (k / NS) & 1, &abort_flag);
+                if (ok) {
+                    for (int blk = 0; blk < K::DB; ++blk) tma_store_3d_w(&map_dv, st + OFF_V + blk * C * 128, blk * 64, c0, bg);
+                    bulk_commit();
+                }
+                bulk_wait_read();
+                if (ok) LA_TL2(k, 13);
+                mbar_arrive_w(&bar_emptykv[s]);
                 if (!ok) break;
             }
             bulk_wait_all();
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer.  Iteration k starts chunk k (A_s, dA') and finishes
-        // chunk k - 1 (dk^T, dv^T, R, r).  With two TMEM buffers the start goes first when its
-        // inputs are already there, so that the tensor pipe works while the pool converts P'
-        // of chunk k - 1; otherwise (and always with one buffer, where chunk k's products
-        // overwrite chunk k - 1's outputs) the finish comes first.
-        if (lane == 0) {
+        // ---------------- MMA issuer.  Per chunk k: start (A_s, dA'; causal), the R part
+        // (dk^T = R_bf V^T, dv^T = R_bf^T phi(K)^T and R += phi_s^T g, none of which needs P'),
+        // which the tensor pipe works on while the pool converts P' and dP', then the finish
+        // (dk^T += phi_s^T [dP' | h], dv^T += g^T P').  With two buffers, chunk k + 1's start
+        // goes before chunk k's finish when its inputs are already there.  Without KV_SEP the
+        // outputs share columns with A_s and dA', and the whole chunk runs after P' (finish_alias).
+        {   // the whole warp, one lane issuing
             constexpr uint32_t idA = idesc_bf16(128, C, false, false);
             constexpr uint32_t idMM = idesc_bf16(128, C, true, true);
+            constexpr uint32_t idMH = idesc_bf16(128, MERGE_H ? C + 16 : C, true, true);
             constexpr uint32_t idMK = idesc_bf16(128, C, true, false);
             constexpr uint32_t idR = idesc_bf16(128, D, true, true);
             constexpr uint32_t idH = idesc_bf16(128, 16, true, K::H_IN_DP);
             const uint32_t pb = smem_u32(pbuf), dpb = smem_u32(dpbuf), rb = smem_u32(rbf), ht = smem_u32(htile);
+            auto stage_ok = [&](uint32_t qs, int k) {
+                return LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && rb + K::RBF_BYTES <= sm_hi, 411, qs - sm_lo, k);
+            };
             auto start = [&](int k) -> bool {
-                if (!CAUSAL) return true;
                 const int s = k % NS, bb = k % NB;
-                if (!mbar_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) return false;
-                if (!mbar_wait(&bar_fullg[s], (k / NS) & 1, &abort_flag)) return false;
-                if (k >= NB && !mbar_wait(&bar_outfree[bb], ((k - NB) / NB) & 1, &abort_flag)) return false;
+                if (!warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) return false;
+                if (!warp_wait(&bar_fullg[s], (k / NS) & 1, &abort_flag)) return false;
+                // sharing columns, A_s and dA' overwrite dk^T and dv^T of chunk k - NB
+                if (!SEP && k >= NB && !warp_wait(&bar_outfree[bb], ((k - NB) / NB) & 1, &abort_flag)) return false;
                 LA_TL2(k, 3);
                 tc_fence_after();
                 const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V, gs = qs + OFF_G;
+                if (!stage_ok(qs, k)) return false;
                 for (int kk = 0; kk < D / 16; ++kk)   // A_s = phi_s phi(K)^T
-                    mma_bf16(tA(bb), desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                    mma_bf16_w(tA(bb), desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
                 for (int kk = 0; kk < D / 16; ++kk)   // dA' = g V^T
-                    mma_bf16(tD(bb), desc_kmajor(gs, 128, 0, kk), desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : 0u);
-                mma_commit(&bar_afull[bb]);
+                    mma_bf16_w(tD(bb), desc_kmajor(gs, 128, 0, kk), desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : 0u);
+                mma_commit_w(&bar_afull[bb]);
                 LA_TL2(k, 4);
                 return true;
             };
-            auto finish = [&](int kp) -> bool {
-                const int sp = kp % NS, bb = kp % NB;
-                if (CAUSAL && !mbar_wait(&bar_pready, kp & 1, &abort_flag)) return false;
-                if ((CAUSAL || kp == 0) && !mbar_wait(&bar_rbf, kp & 1, &abort_flag)) return false;
-                if (!CAUSAL) {
-                    if (!mbar_wait(&bar_ready[sp], (kp / NS) & 1, &abort_flag)) return false;
-                    if (kp >= NB && !mbar_wait(&bar_outfree[bb], ((kp - NB) / NB) & 1, &abort_flag)) return false;
-                }
-                LA_TL2(kp, 5);
+            // dk^T (+)= R_bf V^T, dv^T (+)= R_bf^T phi(K)^T
+            auto rbf_terms = [&](uint32_t qs, int bb, uint32_t acc_k, uint32_t acc_v) {
+                const uint32_t ks_ = qs + OFF_K, vs = qs + OFF_V;
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_w(tK(bb), desc_kmajor(rb, D, 0, kk), desc_kmajor(vs, C, 0, kk), idA, kk > 0 ? 1u : acc_k);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_w(tV(bb), desc_mnmajor(rb, D, 0, kk), desc_kmajor(ks_, C, 0, kk), idMK, kk > 0 ? 1u : acc_v);
+            };
+            // R += phi_s^T g
+            auto r_update = [&](uint32_t qs) {
+                for (int kk = 0; kk < 128 / 16; ++kk)
+                    mma_bf16_w(tR, desc_mnmajor(qs, 128, 0, kk), desc_mnmajor(qs + OFF_G, 128, 0, kk), idR, 1u);
+            };
+            auto rpart = [&](int k) -> bool {
+                const int s = k % NS, bb = k % NB;
+                if ((CAUSAL || k == 0) && !warp_wait(&bar_rbf, k & 1, &abort_flag)) return false;
+                if (!CAUSAL && !warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) return false;
+                if (k >= NB && !warp_wait(&bar_outfree[bb], ((k - NB) / NB) & 1, &abort_flag)) return false;
+                LA_TL2(k, 14);
                 tc_fence_after();
-                const uint32_t qs = smem_u32(stage0 + sp * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V,
-                               gs = qs + OFF_G;
-                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && rb + K::RBF_BYTES <= sm_hi, 411, qs - sm_lo, kp))
-                    return false;
-                uint32_t acc = 0;
-                if (CAUSAL)   // dk^T = phi_s^T dP', r += phi_s^T h, R += phi_s^T g
-                    for (int kk = 0; kk < 128 / 16; ++kk, acc = 1) {
-                        const uint64_t as = desc_mnmajor(qs, 128, 0, kk);
-                        const uint64_t bh = K::H_IN_DP ? desc_mnmajor(dpb + C * 2, 128, 0, kk) : desc_kmajor(ht, 16, 0, kk);
-                        mma_bf16(tA(bb), as, desc_mnmajor(dpb, 128, 0, kk), idMM, acc);
-                        mma_bf16(tR + D, as, bh, idH, 1u);
-                        mma_bf16(tR, as, desc_mnmajor(gs, 128, 0, kk), idR, 1u);
-                    }
-                for (int kk = 0; kk < D / 16; ++kk, acc = 1)   // dk^T += R_bf V^T
-                    mma_bf16(tA(bb), desc_kmajor(rb, D, 0, kk), desc_kmajor(vs, C, 0, kk), idA, acc);
-                acc = 0;
-                if (CAUSAL)   // dv^T = g^T P'
-                    for (int kk = 0; kk < 128 / 16; ++kk, acc = 1)
-                        mma_bf16(tD(bb), desc_mnmajor(gs, 128, 0, kk), desc_mnmajor(pb, 128, 0, kk), idMM, acc);
-                for (int kk = 0; kk < D / 16; ++kk, acc = 1)   // dv^T += R_bf^T phi(K)^T
-                    mma_bf16(tD(bb), desc_mnmajor(rb, D, 0, kk), desc_kmajor(ks_, C, 0, kk), idMK, acc);
-                mma_commit(&bar_outfull[bb]);
-                if (CAUSAL) mma_commit(&bar_emptyqg[sp]);
-                LA_TL2(kp, 6);
+                const uint32_t qs = smem_u32(stage0 + s * K::STAGE);
+                if (!stage_ok(qs, k)) return false;
+                rbf_terms(qs, bb, 0u, 0u);
+                if (CAUSAL) {
+                    r_update(qs);
+                    mma_commit_w(&bar_rfull);
+                } else {
+                    mma_commit_w(&bar_outfull[bb]);
+                }
                 return true;
             };
-            for (int k = 0; k <= nchunk; ++k) {
-                // start first only when it will not wait (its stage is ready and its buffer free)
-                const bool early = NB == 2 && k < nchunk && CAUSAL &&
-                                   mbar_test(&bar_ready[k % NS], (k / NS) & 1) &&
-                                   mbar_test(&bar_fullg[k % NS], (k / NS) & 1) &&
-                                   (k < NB || mbar_test(&bar_outfree[k % NB], ((k - NB) / NB) & 1));
-                if (early && !start(k)) break;
-                if (k > 0 && !finish(k - 1)) break;
-                if (!early && k < nchunk && !start(k)) break;
+            auto finish = [&](int k) -> bool {   // causal, KV_SEP
+                const int s = k % NS, bb = k % NB;
+                if (!warp_wait(&bar_pready, k & 1, &abort_flag)) return false;
+                LA_TL2(k, 5);
+                tc_fence_after();
+                const uint32_t qs = smem_u32(stage0 + s * K::STAGE), gs = qs + OFF_G;
+                if (!stage_ok(qs, k)) return false;
+                for (int kk = 0; kk < 128 / 16; ++kk) {   // dk^T += phi_s^T dP', r part = phi_s^T h
+                    const uint64_t as = desc_mnmajor(qs, 128, 0, kk);
+                    mma_bf16_w(tK(bb), as, desc_mnmajor(dpb, 128, 0, kk), idMH, 1u);
+                    if (!MERGE_H)
+                        mma_bf16_w(tRp(bb), as, K::H_IN_DP ? desc_mnmajor(dpb + C * 2, 128, 0, kk) : desc_kmajor(ht, 16, 0, kk),
+                                 idH, kk > 0 ? 1u : 0u);
+                }
+                for (int kk = 0; kk < 128 / 16; ++kk)   // dv^T += g^T P'
+                    mma_bf16_w(tV(bb), desc_mnmajor(gs, 128, 0, kk), desc_mnmajor(pb, 128, 0, kk), idMM, 1u);
+                mma_commit_w(&bar_outfull[bb]);
+                mma_commit_w(&bar_emptyqg[s]);
+                LA_TL2(k, 6);
+                return true;
+            };
+            auto finish_alias = [&](int k) -> bool {   // !KV_SEP: everything after P' (one buffer)
+                const int s = k % NS, bb = k % NB;
+                if (CAUSAL && !warp_wait(&bar_pready, k & 1, &abort_flag)) return false;
+                if ((CAUSAL || k == 0) && !warp_wait(&bar_rbf, k & 1, &abort_flag)) return false;
+                if (!CAUSAL) {
+                    if (!warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) return false;
+                    if (k >= NB && !warp_wait(&bar_outfree[bb], ((k - NB) / NB) & 1, &abort_flag)) return false;
+                }
+                LA_TL2(k, 5);
+                tc_fence_after();
+                const uint32_t qs = smem_u32(stage0 + s * K::STAGE), gs = qs + OFF_G;
+                if (!stage_ok(qs, k)) return false;
+                if (CAUSAL) {
+                    for (int kk = 0; kk < 128 / 16; ++kk) {   // dk^T = phi_s^T dP', r part = phi_s^T h
+                        const uint64_t as = desc_mnmajor(qs, 128, 0, kk);
+                        mma_bf16_w(tK(bb), as, desc_mnmajor(dpb, 128, 0, kk), idMM, kk > 0 ? 1u : 0u);
+                        mma_bf16_w(tRp(bb), as, K::H_IN_DP ? desc_mnmajor(dpb + C * 2, 128, 0, kk) : desc_kmajor(ht, 16, 0, kk),
+                                 idH, kk > 0 ? 1u : 0u);
+                    }
+                    r_update(qs);
+                    for (int kk = 0; kk < 128 / 16; ++kk)   // dv^T = g^T P'
+                        mma_bf16_w(tV(bb), desc_mnmajor(gs, 128, 0, kk), desc_mnmajor(pb, 128, 0, kk), idMM, kk > 0 ? 1u : 0u);
+                }
+                rbf_terms(qs, bb, CAUSAL ? 1u : 0u, CAUSAL ? 1u : 0u);
+                mma_commit_w(&bar_outfull[bb]);
+                if (CAUSAL) {
+                    mma_commit_w(&bar_rfull);
+                    mma_commit_w(&bar_emptyqg[s]);
+                }
+                LA_TL2(k, 6);
+                return true;
+            };
+            if (SEP) {
+                int started = -1;
+                bool okm = true;
+                if (CAUSAL && nchunk > 0) {
+                    okm = start(0);
+                    started = 0;
+                }
+                for (int k = 0; okm && k < nchunk; ++k) {
+                    if (!rpart(k)) break;
+                    const int kn = k + 1, sn = kn % NS;
+                    if (CAUSAL && NB == 2 && kn < nchunk && warp_test(&bar_ready[sn], (kn / NS) & 1) &&
+                        warp_test(&bar_fullg[sn], (kn / NS) & 1)) {
+                        if (!start(kn)) break;
+                        started = kn;
+                    }
+                    if (CAUSAL && !finish(k)) break;
+                    if (CAUSAL && kn < nchunk && started < kn) {
+                        if (!start(kn)) break;
+                        started = kn;
+                    }
+                }
+            } else {
+                for (int k = 0; k < nchunk; ++k) {
+                    if (CAUSAL && !start(k)) break;
+                    if (!finish_alias(k)) break;
+                }
             }
-            mma_commit(&bar_fin);
-            mbar_drain(&bar_fin, 0);
+            mma_commit_w(&bar_fin);
+            warp_drain(&bar_fin, 0);
         }
     } else if ((warp >= 4 && warp < 8) || warp >= 16) {
         // ---------------- prologue (both warpgroups on every chunk): phi_s = phi(q) / den over
@@ -911,7 +997,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             mbar_arrive_warp(&bar_ready[s]);
         }
     } else if (warp >= 8 && warp < 12) {
-        // ---------------- warpgroup A (thread = feature d): R conversion and dk
+        // ---------------- warpgroup A (thread = feature d): R conversion, dk and dv
         const int wq = warp % 4;
         const int d = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -927,27 +1013,21 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                 store_rbf_row<D>(rbf, d, v, c16);
             }
             r_prev = row[D];
-            if (CAUSAL) {
-                float rv[16];
-                rv[0] = r_prev;
-#pragma unroll
-                for (int e = 1; e < 16; ++e) rv[e] = 0.f;
-                tmem_st16(tR + lane_off + D, rv);
-                tmem_st_wait();
-            }
         }
+        if (MERGE_H)   // the r part (its two read columns) accumulates onto dk^T's product: clear it
+            for (int bb = 0; bb < NB; ++bb) tmem_zero2(tRp(bb) + lane_off);
+        if (CAUSAL || MERGE_H) tmem_st_wait();
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive_warp(&bar_rbf);
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS, bb = k % NB;
-            ok = ok && warp_wait(&bar_outfull[bb], (k / NB) & 1, &abort_flag);
-            tc_fence_after();
-            if (d == 0) LA_TL2(k, 7);
-            float r_next = r_prev;
-            if (CAUSAL && d < D) {   // R and r after this chunk -> R_bf and r for the next one
-                if (ok) {
+            if (CAUSAL) {   // R after this chunk (its update is the chunk's first product) -> R_bf
+                ok = ok && warp_wait(&bar_rfull, k & 1, &abort_flag);
+                tc_fence_after();
+                if (d == 0) LA_TL2(k, 15);
+                if (ok && d < D) {
 #pragma unroll
                     for (int c16 = 0; c16 < D / 16; ++c16) {
                         float v[16];
@@ -955,33 +1035,34 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                         tmem_wait_regs<16>(v);
                         store_rbf_row<D>(rbf, d, v, c16);
                     }
-                    float rv[2];
-                    tmem_ld2(tR + lane_off + D, rv);
-                    tmem_wait_regs<2>(rv);
-                    r_next = rv[0] + rv[1];
                 }
-            }
-            if (CAUSAL) {
                 fence_proxy_async();
                 tc_fence_before();
                 mbar_arrive_warp(&bar_rbf);
+                if (d == 0) LA_TL2(k, 8);
             }
-            if (d == 0) LA_TL2(k, 8);
-            // dk = phi'(k) * (dk^T + r) for column d of the chunk's C keys, written over phi(K)
-            // (each thread reads and writes only its own column) for the TMA store
-            uint8_t *kw = stage0 + s * K::STAGE + OFF_K;
+            ok = ok && warp_wait(&bar_outfull[bb], (k / NB) & 1, &abort_flag);
+            tc_fence_after();
+            if (d == 0) LA_TL2(k, 7);
+            float r_chunk = 0.f;   // phi_s^T h of this chunk (h split in two bf16 parts)
+            if (CAUSAL && ok && d < D) {
+                float rv[2];
+                tmem_ld2(tRp(bb) + lane_off, rv);
+                tmem_wait_regs<2>(rv);
+                r_chunk = rv[0] + rv[1];
+            }
+            // the r part accumulates onto the next dk^T product of this buffer: clear it
+            if (MERGE_H && ok) tmem_zero2(tRp(bb) + lane_off);
+            // dk = phi'(k) * (dk^T + r) for column d of the chunk's C keys, written over phi(K),
+            // then dv (row e = d of dv^T) over V (each thread reads and writes only its own
+            // column), for the TMA stores
+            uint8_t *kw = stage0 + s * K::STAGE + OFF_K, *vw = stage0 + s * K::STAGE + OFF_V;
 #pragma unroll 1
             for (int c16 = 0; c16 < C / 16; ++c16) {
+                if (!ok || d >= D) break;
                 float v[16];
-                if (ok && d < D) {
-                    tmem_ld16(tA(bb) + lane_off + c16 * 16, v);
-                    tmem_wait_regs<16>(v);
-                }
-                if (c16 + 1 == C / 16) {
-                    tc_fence_before();
-                    mbar_arrive_warp(&bar_outfree[bb]);
-                }
-                if (!ok || d >= D) continue;
+                tmem_ld16(tK(bb) + lane_off + c16 * 16, v);
+                tmem_wait_regs<16>(v);
                 float fk[16];   // the column's 16 phi(k) values, all loaded before any store
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -993,11 +1074,30 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             }
             fence_proxy_async();
             mbar_arrive_warp(&bar_dkready[s]);
+#pragma unroll 1
+            for (int c16 = 0; c16 < C / 16; ++c16) {
+                float v[16];
+                if (ok && d < D) {
+                    tmem_ld16(tV(bb) + lane_off + c16 * 16, v);
+                    tmem_wait_regs<16>(v);
+                }
+                if (c16 + 1 == C / 16) {
+                    if (MERGE_H && ok) tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive_warp(&bar_outfree[bb]);
+                }
+                if (!ok || d >= D) continue;
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, c16 * 16 + e, d)) = __float2bfloat16_rn(v[e]);
+            }
+            fence_proxy_async();
+            mbar_arrive_warp(&bar_dvready[s]);
             if (d == 0) LA_TL2(k, 9);
-            r_prev = r_next;
+            r_prev += r_chunk;
         }
     } else if (warp >= 12 && warp < 16) {
-        // ---------------- warpgroup B: P' and dP' (thread = query row i) and dv (thread = e)
+        // ---------------- warpgroup B (thread = query row i): P' and dP'
         const int wq = warp % 4;
         const int i = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -1008,35 +1108,13 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             const int t = t0 + (nchunk - 1) * C + ti;
             if (t < t1 && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 434, bh, t)) hv = p.gd[(size_t)bh * p.N + t];
         }
-        for (int k = 0; k <= nchunk; ++k) {
-            // dv of chunk k - 1, written over its V tile (dead once its MMAs are done, which
-            // outfull says; P' is then free too) for the TMA store
+        for (int k = 0; k < nchunk && CAUSAL; ++k) {
+            // P' = mask(A_s), dP' = mask(dA' + h) for chunk k, and h (split) for the r part,
+            // once chunk k - 1's finish has read P' and dP'
             if (k > 0) {
-                const int kp = k - 1, bb = kp % NB, sp = kp % NS;
-                uint8_t *vw = stage0 + sp * K::STAGE + OFF_V;
-                ok = ok && warp_wait(&bar_outfull[bb], (kp / NB) & 1, &abort_flag);
+                ok = ok && warp_wait(&bar_outfull[(k - 1) % NB], ((k - 1) / NB) & 1, &abort_flag);
                 tc_fence_after();
-#pragma unroll 1
-                for (int c16 = 0; c16 < C / 16; ++c16) {
-                    float v[16];
-                    if (ok && i < D) {
-                        tmem_ld16(tD(bb) + lane_off + c16 * 16, v);
-                        tmem_wait_regs<16>(v);
-                    }
-                    if (c16 + 1 == C / 16) {
-                        tc_fence_before();
-                        mbar_arrive_warp(&bar_outfree[bb]);
-                    }
-                    if (!ok || i >= D) continue;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, c16 * 16 + e, i)) = __float2bfloat16_rn(v[e]);
-                }
-                fence_proxy_async();
-                mbar_arrive_warp(&bar_dvready[sp]);
             }
-            if (k == nchunk || !CAUSAL) continue;
-            // P' = mask(A_s), dP' = mask(dA' + h) for chunk k, and h (split) for the r product
             const int bb = k % NB;
             ok = ok && warp_wait(&bar_afull[bb], (k / NB) & 1, &abort_flag);
             tc_fence_after();

@@ -27,10 +27,23 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > kWaitNs) return;
 }
 
-// Warp-uniform bounded wait.
+// Warp-uniform bounded wait.  A phase that has already completed is seen by one
+// non-blocking test; only a wait that has to block reads the abort flag and the timer.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
     const bool ok = (*abort == 0) && mbar_wait(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-uniform non-blocking test (lane 0's view of the phase).
+__device__ __forceinline__ bool warp_test(uint64_t *bar, uint32_t parity) {
+    return __shfl_sync(0xffffffffu, mbar_test(bar, parity) ? 1 : 0, 0) != 0;
+}
+
+// Warp-uniform drain of a barrier phase (bounded; for the exit paths).
+__device__ __forceinline__ void warp_drain(uint64_t *bar, uint32_t parity) {
+    mbar_drain(bar, parity);
+    __syncwarp();
 }
 
 __device__ __forceinline__ float feat(float x, int phi) {

@@ -96,6 +96,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Wait for the phase with the given parity to complete.  Gives up (returns false and
 // raises *abort) after kWaitNs, or early once another thread raised *abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_test(bar, parity)) return true;
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
@@ -261,6 +262,87 @@ __device__ __forceinline__ void mma_bf16_lastuse(uint32_t d_tmem, uint64_t a_des
         : "memory");
 }
 
+// ---- warp-collective issue ----------------------------------------------------------
+// The *_w forms are called by all 32 lanes of a warp in warp-uniform control flow with
+// warp-uniform arguments; lane 0, selected by a predicate inside the instruction block,
+// issues the operation (always the same lane, so a commit covers the lane's MMAs).  Keeping the control flow uniform lets the compiler hold the
+// descriptors and coordinates in uniform registers: measured on sm_103a, an MMA issued
+// from inside a one-lane branch cost 80 cycles of issue alone and over 300 next to busy
+// warps, against 47 and 60 for the warp-collective form.
+
+#define LA_LANE0_MMA(QUAL)                                                        \
+    asm volatile(                                                                 \
+        "{\n\t.reg .pred p, e;\n\t.reg .u32 l;\n\t"                                 \
+        "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"                            \
+        "setp.ne.b32 p, %4, 0;\n\t"                                                 \
+        "@e tcgen05.mma.cta_group::1.kind::f16" QUAL " [%0], %1, %2, %3, p;\n\t}" \
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)      \
+        : "memory")
+
+__device__ __forceinline__ void mma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    LA_LANE0_MMA("");
+}
+__device__ __forceinline__ void mma_bf16_fill_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    LA_LANE0_MMA(".collector::a::fill");
+}
+__device__ __forceinline__ void mma_bf16_use_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    LA_LANE0_MMA(".collector::a::use");
+}
+__device__ __forceinline__ void mma_bf16_lastuse_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+    LA_LANE0_MMA(".collector::a::lastuse");
+}
+#undef LA_LANE0_MMA
+
+// Arrive once on *bar when every tcgen05 operation issued so far by the issuing lane is done.
+__device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint64_t *bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+// One arrival (count 1) on behalf of the warp.
+__device__ __forceinline__ void mbar_arrive_w(uint64_t *bar) {
+    __syncwarp();
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+        "[%2];\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// Store one box from shared memory (bulk-group completion) from lane 0.  Every lane then
+// runs bulk_commit() and bulk_wait_read() / bulk_wait_all() (empty groups for the lanes
+// that issued nothing) and __syncwarp(), so the warp waits for lane 0's copies.
+__device__ __forceinline__ void tma_store_3d_w(const CUtensorMap *map, const void *src, int x, int y, int z) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "@e cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n\t}" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // Arrive once on *bar when every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -335,6 +417,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
         "r"(__float_as_uint(v[15]))
         : "memory");
+}
+
+// Zero two consecutive columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_zero2(uint32_t taddr) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %1};" ::"r"(taddr), "r"(0u) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
