@@ -102,6 +102,10 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
         off += row_bytes;
         pl.off_gd = off;
         off += row_bytes;
+        if (pl.path == LA_PATH_TCGEN05 && causal) {   // phi(q) / den rows, bf16
+            pl.off_phis = off;
+            off += align_up((size_t)B * Hq * N * D * 2, 256);
+        }
     }
     pl.ws_bytes = off;
     return pl;
@@ -136,6 +140,7 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     p.rstate = bwd ? reinterpret_cast<float *>(base + pl.off_rstate) : nullptr;
     p.den = bwd ? reinterpret_cast<float *>(base + pl.off_den) : nullptr;
     p.gd = bwd ? reinterpret_cast<float *>(base + pl.off_gd) : nullptr;
+    p.phis = bwd && pl.off_phis ? static_cast<void *>(base + pl.off_phis) : nullptr;
     if (bwd && fwd_ws) {
         // the forward's workspace holds its scanned segment states; they are the backward's
         // when both plans cut the sequence the same way

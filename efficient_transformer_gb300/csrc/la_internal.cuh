@@ -35,6 +35,8 @@ struct Params {
     float *rstate;               // per (b, kv head, segment) backward state partials
     float *den;                  // [B, Hq, N] row denominators (backward)
     float *gd;                   // [B, Hq, N] per-row denominator terms (backward; see each kernel)
+    void *phis;                  // [B, Hq, N, D] bf16 phi(q) / den, written by the tensor-core dq
+                                 // kernel for the dk/dv kernel (causal tensor-core backward; else null)
     int *err;                    // device error word
 };
 
@@ -46,7 +48,7 @@ struct Plan {
     int seg_len;      // tokens per segment (a multiple of chunk)
     int nseg;         // segments per (batch, kv head)
     size_t state_elems;   // floats of one segment state (all terms)
-    size_t off_state, off_rstate, off_den, off_gd;   // workspace byte offsets
+    size_t off_state, off_rstate, off_den, off_gd, off_phis;   // workspace byte offsets
     size_t ws_bytes;
 };
 

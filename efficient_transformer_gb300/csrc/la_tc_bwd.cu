@@ -58,7 +58,13 @@ struct BwdCfg {
     // columns of dP' next to the C keys)
     static constexpr bool H_IN_DP = C % 64 != 0 && C % 64 + 16 <= 64;
     static constexpr int RBF_BYTES = D * 128 * 2;           // R_bf: D rows x 128 columns
-    static constexpr int KV_FIXED = 2 * P_BYTES + RBF_BYTES + (H_IN_DP ? 0 : H_BYTES) + 1024;
+    static constexpr int PT_BYTES = C * 256;                // P'^T: C rows (keys) x 128 columns
+    // dk and dv leave through a staging tile of their own (C rows x D columns, one after the
+    // other), so that the [K | V] region goes back to the loader before the epilogue; for
+    // C > 32 the outputs are written over phi(K) and V instead
+    static constexpr bool OUT_STAGE = C <= 32;
+    static constexpr int OUT_BYTES = OUT_STAGE ? C * D * 2 : 0;
+    static constexpr int KV_FIXED = PT_BYTES + P_BYTES + RBF_BYTES + (H_IN_DP ? 0 : H_BYTES) + OUT_BYTES + 1024;
     static constexpr int NS = 3 * STAGE + KV_FIXED <= kSmemLimit - 512 ? 3 : 2;
     static constexpr int DKDV_SMEM = NS * STAGE + KV_FIXED;
     static constexpr bool FITS = DQ_SMEM <= kSmemLimit - 512 && DKDV_SMEM <= kSmemLimit - 512;
@@ -133,14 +139,15 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                                                               const __grid_constant__ CUtensorMap map_k,
                                                               const __grid_constant__ CUtensorMap map_v,
                                                               const __grid_constant__ CUtensorMap map_g,
-                                                              const __grid_constant__ CUtensorMap map_dq, Params p) {
+                                                              const __grid_constant__ CUtensorMap map_dq,
+                                                              const __grid_constant__ CUtensorMap map_ps, Params p) {
     using K = BwdCfg<D, G>;
     constexpr int C = K::C, NS = K::NS_DQ;
     constexpr int OFF_K = K::Q_BYTES, OFF_V = OFF_K + K::K_BYTES, OFF_G = OFF_V + K::V_BYTES;
     constexpr int HALF = D / 2;   // feature columns per pool half
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar_fulla[NS], bar_fullg[NS], bar_ready[NS], bar_empty[NS], bar_dqready[NS][2];
-    __shared__ uint64_t bar_mfull, bar_sfull, bar_gnready, bar_dqfull, bar_xfree, bar_sbf, bar_fin;
+    __shared__ uint64_t bar_mfull, bar_sfull, bar_gnready, bar_dqfull, bar_xfree, bar_sbf, bar_psread, bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
@@ -188,6 +195,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         mbar_init(&bar_sfull, 1);
         mbar_init(&bar_gnready, 256);
         mbar_init(&bar_dqfull, 1);
+        mbar_init(&bar_psread, 1);
         mbar_init(&bar_xfree, 256);
         mbar_init(&bar_sbf, 256);
         mbar_init(&bar_fin, 1);
@@ -325,15 +333,28 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             warp_drain(&bar_fin, 0);
         }
     } else if (warp == 2) {
-        // ---------------- dq store: each pool half leaves its D/2 columns of dq over the
-        // phi_s tile; TMA writes them out, and the stage is released once the copies have
-        // read it
+        // ---------------- stores.  Causal: once the row pass has left phi_s = phi(q) / den in
+        // the Q tile, TMA copies it to the workspace for the dk/dv kernel, and the pool may
+        // overwrite the tile once the copy has read it.  Then each pool half leaves its D/2
+        // columns of dq over the phi_s tile; TMA writes them out, and the stage is released
+        // once the copies have read it
         {   // the whole warp, one lane issuing
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
                 bool ok = true;
+                if (CAUSAL) {
+                    ok = warp_wait(&bar_gnready, k & 1, &abort_flag);
+                    if (ok) {
+                        for (int r = 0; r < G; ++r)
+                            for (int blk = 0; blk < K::DB; ++blk)
+                                tma_store_3d_w(&map_ps, st + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
+                        bulk_commit();
+                    }
+                    bulk_wait_read();
+                    mbar_arrive_w(&bar_psread);
+                }
                 // with D = 128 each half is one 64-column block and goes out on its own;
                 // with D = 64 both halves share the block
                 for (int hh = 0; hh < 2; ++hh) {
@@ -569,7 +590,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 mbar_arrive_warp(&bar_sbf);
             }
             // ---- dq = phi'(q) / den * (den da), written over the phi_s tile for the TMA store
+            // (causal: after the copy of phi_s to the workspace has read the tile)
             ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
+            if (CAUSAL) ok = ok && warp_wait(&bar_psread, k & 1, &abort_flag);
             tc_fence_after();
             if (i == 0 && h == 0) LA_TL(k, 11);
 #pragma unroll 1
@@ -647,17 +670,19 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     __shared__ uint64_t bar_fullq[NS], bar_fullg[NS], bar_fullkv[NS], bar_ready[NS], bar_emptyqg[NS],
         bar_emptykv[NS], bar_dkready[NS], bar_dvready[NS];
     __shared__ uint64_t bar_afull[2], bar_outfull[2], bar_outfree[2];
-    __shared__ uint64_t bar_pready, bar_rbf, bar_rfull, bar_fin;
+    __shared__ uint64_t bar_pready, bar_rbf, bar_rfull, bar_stfree, bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
     const uint32_t sm_lo = smem_u32(smem_raw), sm_hi = sm_lo + K::DKDV_SMEM;
     (void)sm_lo;
     (void)sm_hi;
-    uint8_t *pbuf = stage0 + NS * K::STAGE;       // P' = mask(phi_s phi(K)^T)      [query rows][keys]
-    uint8_t *dpbuf = pbuf + K::P_BYTES;          // dP' = mask(g V^T + h), then h  [query rows][keys | h_hi h_lo]
+    uint8_t *ptbuf = stage0 + NS * K::STAGE;     // P'^T = mask(phi_s phi(K)^T)^T  [keys][query rows]
+    uint8_t *dpbuf = ptbuf + K::PT_BYTES;        // dP' = mask(g V^T + h), then h  [query rows][keys | h_hi h_lo]
     uint8_t *rbf = dpbuf + K::P_BYTES;           // R_bf [D rows d][128 columns e]
     uint8_t *htile = rbf + K::RBF_BYTES;         // h as 16 x 128 (rows h_hi, h_lo) when it is not in dP'
+    uint8_t *obuf = htile + (K::H_IN_DP ? 0 : K::H_BYTES);   // dk, then dv [keys][D] (OUT_STAGE)
+    constexpr bool OUT_STAGE = K::OUT_STAGE;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
@@ -680,7 +705,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             mbar_init(&bar_fullkv[s], 1);
             mbar_init(&bar_ready[s], kKvPro);
             mbar_init(&bar_emptyqg[s], 1);
-            mbar_init(&bar_emptykv[s], 1);
+            mbar_init(&bar_emptykv[s], OUT_STAGE ? 128 : 1);
             mbar_init(&bar_dkready[s], 128);
             mbar_init(&bar_dvready[s], 128);
         }
@@ -693,6 +718,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
         }
         mbar_init(&bar_rbf, 128);
         mbar_init(&bar_rfull, 1);
+        mbar_init(&bar_stfree, 1);
         mbar_init(&bar_fin, 1);
         fence_barrier_init();
     }
@@ -762,27 +788,34 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             }
         }
     } else if (warp == 2) {
-        // ---------------- dk, dv stores: TMA writes the two tiles left over phi(K) and V,
-        // and the [K | V] region is released once the copies have read it
+        // ---------------- dk, dv stores.  With OUT_STAGE both go out of the staging tile,
+        // dk first, and each copy frees the tile for the next output; otherwise TMA writes the
+        // two tiles left over phi(K) and V, and the [K | V] region is released once the copies
+        // have read it
         {   // the whole warp, one lane issuing
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 uint8_t *st = stage0 + s * K::STAGE;
+                uint8_t *src_k = OUT_STAGE ? obuf : st + OFF_K, *src_v = OUT_STAGE ? obuf : st + OFF_V;
                 const int c0 = t0 + (nchunk - 1 - k) * C;
                 bool ok = warp_wait(&bar_dkready[s], (k / NS) & 1, &abort_flag);
                 if (ok) {
                     LA_TL2(k, 12);
-                    for (int blk = 0; blk < K::DB; ++blk) tma_store_3d_w(&map_dk, st + OFF_K + blk * C * 128, blk * 64, c0, bg);
+                    for (int blk = 0; blk < K::DB; ++blk) tma_store_3d_w(&map_dk, src_k + blk * C * 128, blk * 64, c0, bg);
                     bulk_commit();
+                }
+                if (OUT_STAGE) {
+                    bulk_wait_read();
+                    mbar_arrive_w(&bar_stfree);
                 }
                 ok = ok && warp_wait(&bar_dvready[s], (k / NS) & 1, &abort_flag);
                 if (ok) {
-                    for (int blk = 0; blk < K::DB; ++blk) tma_store_3d_w(&map_dv, st + OFF_V + blk * C * 128, blk * 64, c0, bg);
+                    for (int blk = 0; blk < K::DB; ++blk) tma_store_3d_w(&map_dv, src_v + blk * C * 128, blk * 64, c0, bg);
                     bulk_commit();
                 }
                 bulk_wait_read();
                 if (ok) LA_TL2(k, 13);
-                mbar_arrive_w(&bar_emptykv[s]);
+                mbar_arrive_w(OUT_STAGE ? &bar_stfree : &bar_emptykv[s]);
                 if (!ok) break;
             }
             bulk_wait_all();
@@ -801,13 +834,14 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             constexpr uint32_t idMK = idesc_bf16(128, C, true, false);
             constexpr uint32_t idR = idesc_bf16(128, D, true, true);
             constexpr uint32_t idH = idesc_bf16(128, 16, true, K::H_IN_DP);
-            const uint32_t pb = smem_u32(pbuf), dpb = smem_u32(dpbuf), rb = smem_u32(rbf), ht = smem_u32(htile);
+            const uint32_t pb = smem_u32(ptbuf), dpb = smem_u32(dpbuf), rb = smem_u32(rbf), ht = smem_u32(htile);
             auto stage_ok = [&](uint32_t qs, int k) {
                 return LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && rb + K::RBF_BYTES <= sm_hi, 411, qs - sm_lo, k);
             };
             auto start = [&](int k) -> bool {
                 const int s = k % NS, bb = k % NB;
                 if (!warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag)) return false;
+                if (!warp_wait(&bar_fullq[s], (k / NS) & 1, &abort_flag)) return false;
                 if (!warp_wait(&bar_fullg[s], (k / NS) & 1, &abort_flag)) return false;
                 // sharing columns, A_s and dA' overwrite dk^T and dv^T of chunk k - NB
                 if (!SEP && k >= NB && !warp_wait(&bar_outfree[bb], ((k - NB) / NB) & 1, &abort_flag)) return false;
@@ -869,7 +903,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                                  idH, kk > 0 ? 1u : 0u);
                 }
                 for (int kk = 0; kk < 128 / 16; ++kk)   // dv^T += g^T P'
-                    mma_bf16_w(tV(bb), desc_mnmajor(gs, 128, 0, kk), desc_mnmajor(pb, 128, 0, kk), idMM, 1u);
+                    mma_bf16_w(tV(bb), desc_mnmajor(gs, 128, 0, kk), desc_kmajor(pb, C, 0, kk), idMK, 1u);
                 mma_commit_w(&bar_outfull[bb]);
                 mma_commit_w(&bar_emptyqg[s]);
                 LA_TL2(k, 6);
@@ -896,7 +930,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     }
                     r_update(qs);
                     for (int kk = 0; kk < 128 / 16; ++kk)   // dv^T = g^T P'
-                        mma_bf16_w(tV(bb), desc_mnmajor(gs, 128, 0, kk), desc_mnmajor(pb, 128, 0, kk), idMM, kk > 0 ? 1u : 0u);
+                        mma_bf16_w(tV(bb), desc_mnmajor(gs, 128, 0, kk), desc_kmajor(pb, C, 0, kk), idMK, kk > 0 ? 1u : 0u);
                 }
                 rbf_terms(qs, bb, CAUSAL ? 1u : 0u, CAUSAL ? 1u : 0u);
                 mma_commit_w(&bar_outfull[bb]);
@@ -918,7 +952,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     if (!rpart(k)) break;
                     const int kn = k + 1, sn = kn % NS;
                     if (CAUSAL && NB == 2 && kn < nchunk && warp_test(&bar_ready[sn], (kn / NS) & 1) &&
-                        warp_test(&bar_fullg[sn], (kn / NS) & 1)) {
+                        warp_test(&bar_fullq[sn], (kn / NS) & 1) && warp_test(&bar_fullg[sn], (kn / NS) & 1)) {
                         if (!start(kn)) break;
                         started = kn;
                     }
@@ -938,47 +972,22 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             warp_drain(&bar_fin, 0);
         }
     } else if ((warp >= 4 && warp < 8) || warp >= 16) {
-        // ---------------- prologue (both warpgroups on every chunk): phi_s = phi(q) / den over
-        // the Q tile, phi(K) over the K tile, in place
+        // ---------------- prologue (both warpgroups on every chunk): phi(K) over the K tile, in
+        // place (the Q tile arrives as phi_s = phi(q) / den, written by the dq kernel)
         const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0 .. kKvPro - 1
         constexpr int CPR = D / 8, RPP = kKvPro / CPR;
         static_assert(RPP % 8 == 0, "rows per pass");
         const int c = pi % CPR, r0 = pi / CPR;
         const uint32_t pos = (uint32_t)(((c & 7) ^ (r0 & 7)) << 4);
-        const uint32_t offq = (uint32_t)(c >> 3) * 128u * 128u + pos, offk = (uint32_t)(c >> 3) * C * 128u + pos;
-        constexpr int NR = (128 + RPP - 1) / RPP;
+        const uint32_t offk = (uint32_t)(c >> 3) * C * 128u + pos;
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
             const int c0 = t0 + (nchunk - 1 - k) * C;
             const int nvalid = t1 - c0;
-            // this thread's rows' denominators, loaded while the chunk's tiles arrive
-            float den[NR];
-            if (CAUSAL)
-#pragma unroll
-                for (int n = 0; n < NR; ++n) {
-                    const int row = r0 + n * RPP, ti = row % C;
-                    const size_t at = (size_t)(bh0 + row / C) * p.N + c0 + ti;
-                    den[n] = (row < 128 && ti < nvalid && LA_CHECK(at < (size_t)p.B * p.Hq * p.N, 423, row, c0)) ? p.den[at] : 1.f;
-                }
-            if (CAUSAL) ok = ok && warp_wait(&bar_fullq[s], (k / NS) & 1, &abort_flag);
-            if (pi == 0) LA_TL2(k, 1);
             uint8_t *st = stage0 + s * K::STAGE;
-            if (ok && CAUSAL) {
-                uint8_t *pp[NR];
-                bool pres[NR], val[NR];
-                float sc[NR];
-#pragma unroll
-                for (int n = 0; n < NR; ++n) {
-                    const int row = r0 + n * RPP;
-                    pp[n] = st + offq + row * 128;
-                    pres[n] = row < 128 && LA_CHECK(in_smem(pp[n], 16, sm_lo, sm_hi), 421, smem_u32(pp[n]) - sm_lo, row);
-                    val[n] = row % C < nvalid;
-                    sc[n] = 1.f / den[n];
-                }
-                feat8_batch<NR, true>(pp, pres, val, p.phi, sc);
-            }
             ok = ok && warp_wait(&bar_fullkv[s], (k / NS) & 1, &abort_flag);
+            if (pi == 0) LA_TL2(k, 1);
             if (ok) {
                 constexpr int NK = (C + RPP - 1) / RPP;
                 uint8_t *pp[NK];
@@ -986,7 +995,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
 #pragma unroll
                 for (int n = 0; n < NK; ++n) {
                     const int j = r0 + n * RPP;
-                    pp[n] = st + OFF_K + offk + j * 128;
+                    pp[n] = st + OFF_K + offk + (j < C ? j : 0) * 128;
                     pres[n] = j < C && LA_CHECK(in_smem(pp[n], 16, sm_lo, sm_hi), 422, smem_u32(pp[n]) - sm_lo, j);
                     val[n] = j < nvalid;
                 }
@@ -1041,8 +1050,27 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                 mbar_arrive_warp(&bar_rbf);
                 if (d == 0) LA_TL2(k, 8);
             }
-            ok = ok && warp_wait(&bar_outfull[bb], (k / NB) & 1, &abort_flag);
-            tc_fence_after();
+            // OUT_STAGE: phi(k) of column d, kept in registers so that the [K | V] region goes
+            // back to the loader as soon as no MMA reads it (causal: after the R part, which
+            // rfull says; bidirectional: after the chunk's products)
+            const uint8_t *kr = stage0 + s * K::STAGE + OFF_K;
+            uint32_t fk2[OUT_STAGE ? C / 2 : 1];
+            if constexpr (OUT_STAGE) {
+                if (!CAUSAL) {
+                    ok = ok && warp_wait(&bar_outfull[bb], (k / NB) & 1, &abort_flag);
+                    tc_fence_after();
+                }
+                const int dd = d < D ? d : 0;
+#pragma unroll
+                for (int j = 0; j < C; j += 2)
+                    fk2[j / 2] = pack_bf16x2(__bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kr + swz_offset(C, j, dd))),
+                                             __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kr + swz_offset(C, j + 1, dd))));
+                mbar_arrive_warp(&bar_emptykv[s]);
+            }
+            if (!OUT_STAGE || CAUSAL) {
+                ok = ok && warp_wait(&bar_outfull[bb], (k / NB) & 1, &abort_flag);
+                tc_fence_after();
+            }
             if (d == 0) LA_TL2(k, 7);
             float r_chunk = 0.f;   // phi_s^T h of this chunk (h split in two bf16 parts)
             if (CAUSAL && ok && d < D) {
@@ -1053,10 +1081,13 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             }
             // the r part accumulates onto the next dk^T product of this buffer: clear it
             if (MERGE_H && ok) tmem_zero2(tRp(bb) + lane_off);
-            // dk = phi'(k) * (dk^T + r) for column d of the chunk's C keys, written over phi(K),
-            // then dv (row e = d of dv^T) over V (each thread reads and writes only its own
-            // column), for the TMA stores
-            uint8_t *kw = stage0 + s * K::STAGE + OFF_K, *vw = stage0 + s * K::STAGE + OFF_V;
+            // dk = phi'(k) * (dk^T + r) for column d of the chunk's C keys, then dv (row e = d
+            // of dv^T), each written into the staging tile once the previous copy out of it
+            // has read it (OUT_STAGE), else over phi(K) and V; each thread reads and writes only
+            // its own column
+            uint8_t *kw = OUT_STAGE ? obuf : stage0 + s * K::STAGE + OFF_K;
+            uint8_t *vw = OUT_STAGE ? obuf : stage0 + s * K::STAGE + OFF_V;
+            if (OUT_STAGE && k > 0) ok = ok && warp_wait(&bar_stfree, 1u, &abort_flag);   // dv of chunk k - 1
 #pragma unroll 1
             for (int c16 = 0; c16 < C / 16; ++c16) {
                 if (!ok || d >= D) break;
@@ -1065,8 +1096,14 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                 tmem_wait_regs<16>(v);
                 float fk[16];   // the column's 16 phi(k) values, all loaded before any store
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    fk[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)));
+                for (int e = 0; e < 16; ++e) {
+                    if constexpr (OUT_STAGE) {
+                        const float2 u = unpack_bf16x2(fk2[(c16 * 16 + e) / 2 % (OUT_STAGE ? C / 2 : 1)]);
+                        fk[e] = (e & 1) ? u.y : u.x;
+                    } else {
+                        fk[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)));
+                    }
+                }
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     *reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)) =
@@ -1074,6 +1111,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             }
             fence_proxy_async();
             mbar_arrive_warp(&bar_dkready[s]);
+            if (OUT_STAGE) ok = ok && warp_wait(&bar_stfree, 0u, &abort_flag);   // dk of chunk k
 #pragma unroll 1
             for (int c16 = 0; c16 < C / 16; ++c16) {
                 float v[16];
@@ -1109,7 +1147,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             if (t < t1 && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 434, bh, t)) hv = p.gd[(size_t)bh * p.N + t];
         }
         for (int k = 0; k < nchunk && CAUSAL; ++k) {
-            // P' = mask(A_s), dP' = mask(dA' + h) for chunk k, and h (split) for the r part,
+            // P'^T = mask(A_s)^T, dP' = mask(dA' + h) for chunk k, and h (split) for the r part,
             // once chunk k - 1's finish has read P' and dP'
             if (k > 0) {
                 ok = ok && warp_wait(&bar_outfull[(k - 1) % NB], ((k - 1) / NB) & 1, &abort_flag);
@@ -1142,23 +1180,27 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     tmem_ld16(tD(bb) + lane_off + c16 * 16, vd);
                     tmem_wait_regs<16>(va);
                     tmem_wait_regs<16>(vd);
-                    uint32_t wa[8], wd[8];
+                    uint32_t wd[8];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
                         const int j = c16 * 16 + e;
                         const bool m0 = j <= ti, m1 = j + 1 <= ti;
-                        wa[e / 2] = pack_bf16x2(m0 ? va[e] : 0.f, m1 ? va[e + 1] : 0.f);
                         wd[e / 2] = pack_bf16x2(m0 ? vd[e] + hv : 0.f, m1 ? vd[e + 1] + hv : 0.f);
                     }
-                    uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
                     uint8_t *q0 = dpbuf + swz_chunk(128, i, 2 * c16), *q1 = dpbuf + swz_chunk(128, i, 2 * c16 + 1);
-                    if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi) &&
-                                     in_smem(q0, 16, sm_lo, sm_hi) && in_smem(q1, 16, sm_lo, sm_hi),
-                                 431, smem_u32(p0) - sm_lo, c16)) {
-                        *reinterpret_cast<uint4 *>(p0) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-                        *reinterpret_cast<uint4 *>(p1) = make_uint4(wa[4], wa[5], wa[6], wa[7]);
+                    uint8_t *pt = ptbuf + swz_offset(C, c16 * 16, i);
+                    if (LA_CHECK(in_smem(q0, 16, sm_lo, sm_hi) && in_smem(q1, 16, sm_lo, sm_hi) &&
+                                     in_smem(pt, 2, sm_lo, sm_hi) && in_smem(ptbuf + swz_offset(C, c16 * 16 + 15, i), 2, sm_lo, sm_hi),
+                                 431, smem_u32(q0) - sm_lo, c16)) {
                         *reinterpret_cast<uint4 *>(q0) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
                         *reinterpret_cast<uint4 *>(q1) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+                        // P'^T: row j (key), column i; a warp writes 64 contiguous bytes of a row
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = c16 * 16 + e;
+                            *reinterpret_cast<__nv_bfloat16 *>(ptbuf + swz_offset(C, j, i)) =
+                                __float2bfloat16_rn(j <= ti ? va[e] : 0.f);
+                        }
                     }
                 }
                 fence_proxy_async();
@@ -1181,8 +1223,10 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
 template <int D, int G, bool CAUSAL>
 cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     using K = BwdCfg<D, G>;
-    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{};
+    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{}, mps{};
     cudaError_t e = make_map(&mq, p.q, p.B * p.Hq, p.N, D, K::C);
+    // phi(q) / den rows: written by the dq kernel, read by the dk/dv kernel in place of q
+    if (e == cudaSuccess) e = make_map(&mps, CAUSAL ? p.phis : p.q, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mg, p.g, p.B * p.Hq, p.N, D, K::C);
@@ -1195,14 +1239,14 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
     {
         TraceScope ts(CAUSAL ? "tc_bwd_dq_causal" : "tc_bwd_dq_bidir", s);
-        k_tc_bwd_dq<D, G, CAUSAL><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, p);
+        k_tc_bwd_dq<D, G, CAUSAL><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, mps, p);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess)
         e = scan_segments(p.rstate, p, CAUSAL ? kScanSuffix : kScanTotal, (size_t)D * (D + 1), s);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_bwd_dkdv_causal" : "tc_bwd_dkdv_bidir", s);
-    k_tc_bwd_dkdv<D, G, CAUSAL><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mq, mk, mv, mg, mdk, mdv, p);
+    k_tc_bwd_dkdv<D, G, CAUSAL><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mps, mk, mv, mg, mdk, mdv, p);
     return cudaGetLastError();
 }
 
