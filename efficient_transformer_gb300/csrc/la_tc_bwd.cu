@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     constexpr int HALF = D / 2;   // feature columns per pool half
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar_fulla[NS], bar_fullg[NS], bar_ready[NS], bar_empty[NS], bar_dqready[NS][2];
-    __shared__ uint64_t bar_mfull, bar_sfull, bar_gnready, bar_dqfull, bar_xfree, bar_sbf, bar_psread, bar_fin;
+    __shared__ uint64_t bar_mfull, bar_sfull, bar_gnready, bar_dqfull, bar_xfree, bar_sbf, bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
@@ -195,7 +195,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         mbar_init(&bar_sfull, 1);
         mbar_init(&bar_gnready, 256);
         mbar_init(&bar_dqfull, 1);
-        mbar_init(&bar_psread, 1);
         mbar_init(&bar_xfree, 256);
         mbar_init(&bar_sbf, 256);
         mbar_init(&bar_fin, 1);
@@ -334,10 +333,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         }
     } else if (warp == 2) {
         // ---------------- stores.  Causal: once the row pass has left phi_s = phi(q) / den in
-        // the Q tile, TMA copies it to the workspace for the dk/dv kernel, and the pool may
-        // overwrite the tile once the copy has read it.  Then each pool half leaves its D/2
-        // columns of dq over the phi_s tile; TMA writes them out, and the stage is released
-        // once the copies have read it
+        // the Q tile, TMA copies it to the workspace for the dk/dv kernel.  Then each pool
+        // half leaves its D/2 columns of dq over the g tile; TMA writes them out, and the
+        // stage is released once all the copies have read it
         {   // the whole warp, one lane issuing
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
@@ -352,8 +350,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                                 tma_store_3d_w(&map_ps, st + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
                         bulk_commit();
                     }
-                    bulk_wait_read();
-                    mbar_arrive_w(&bar_psread);
                 }
                 // with D = 128 each half is one 64-column block and goes out on its own;
                 // with D = 64 both halves share the block
@@ -364,7 +360,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     if (K::DB == 2 || hh == 1) {
                         const int blk = K::DB == 2 ? hh : 0;
                         for (int r = 0; r < G; ++r)
-                            tma_store_3d_w(&map_dq, st + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
+                            tma_store_3d_w(&map_dq, st + OFF_G + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
                     }
                 }
                 if (ok) {
@@ -419,10 +415,38 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             }
             if (pi == 0) LA_TL(k, 2);
             mbar_arrive_warp(&bar_ready[s]);
+            // ---- warps 16-23: S, z after chunk k -> operand tiles for chunk k + 1, in two
+            // halves of D/2 columns (thread = TMEM lane), between this chunk's feature map and
+            // the next one's
+            if (CAUSAL && warp >= 16) {
+                const int h = (warp - 16) / 4, wq = warp % 4, i = wq * 32 + lane;
+                const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+                ok = ok && warp_wait(&bar_sfull, k & 1, &abort_flag);
+                tc_fence_after();
+                if (i == 0 && h == 0) LA_TL(k, 9);
+                if (ok && wq * 32 < D) {
+#pragma unroll
+                    for (int c16 = 0; c16 < HALF / 16; ++c16) {
+                        float v[16];
+                        tmem_ld16(tS + lane_off + h * HALF + c16 * 16, v);
+                        tmem_wait_regs<16>(v);
+                        store_state_row<D>(sbf, i, v, (h * HALF) / 16 + c16);
+                    }
+                    if (h == 0) {
+                        float zd = tmem_ld1(tS + lane_off + D);
+                        tmem_wait_regs<1>(&zd);
+                        store_split_z<D>(ztile + ((k + 1) & 1) * K::Z_BYTES, i, zd);
+                    }
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                if (i == 0 && h == 0) LA_TL(k, 10);
+                mbar_arrive_warp(&bar_sbf);
+            }
         }
     } else if (warp >= 8 && warp < 16) {
         // ---------------- row pool: two warpgroups, thread = query row i (TMEM lane), each
-        // half owning D/2 feature columns.  Per chunk: row work, state conversion, dq.
+        // half owning D/2 feature columns.  Per chunk: row work, dq.
         const int h = (warp - 8) / 4;
         const int wq = warp % 4;
         const int i = wq * 32 + lane;
@@ -565,34 +589,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             tc_fence_before();
             if (i == 0 && h == 0) LA_TL(k, 8);
             mbar_arrive_warp(&bar_gnready);
-            // ---- S, z after chunk k -> operand tiles for chunk k + 1
-            if (CAUSAL) {
-                ok = ok && warp_wait(&bar_sfull, k & 1, &abort_flag);
-                tc_fence_after();
-                if (i == 0 && h == 0) LA_TL(k, 9);
-                if (ok && wq * 32 < D) {
-#pragma unroll
-                    for (int c16 = 0; c16 < HALF / 16; ++c16) {
-                        float v[16];
-                        tmem_ld16(tS + lane_off + h * HALF + c16 * 16, v);
-                        tmem_wait_regs<16>(v);
-                        store_state_row<D>(sbf, i, v, (h * HALF) / 16 + c16);
-                    }
-                    if (h == 0) {
-                        float zd = tmem_ld1(tS + lane_off + D);
-                        tmem_wait_regs<1>(&zd);
-                        store_split_z<D>(ztile + ((k + 1) & 1) * K::Z_BYTES, i, zd);
-                    }
-                }
-                fence_proxy_async();
-                tc_fence_before();
-                if (i == 0 && h == 0) LA_TL(k, 10);
-                mbar_arrive_warp(&bar_sbf);
-            }
-            // ---- dq = phi'(q) / den * (den da), written over the phi_s tile for the TMA store
-            // (causal: after the copy of phi_s to the workspace has read the tile)
+            // ---- dq = phi'(q) / den * (den da), written over the g tile (dead once the chunk's
+            // products are done, which dqfull says) for the TMA store; phi_s stays in place for
+            // its own copy to the workspace
             ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
-            if (CAUSAL) ok = ok && warp_wait(&bar_psread, k & 1, &abort_flag);
             tc_fence_after();
             if (i == 0 && h == 0) LA_TL(k, 11);
 #pragma unroll 1
@@ -617,9 +617,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 }
 #pragma unroll
                 for (int q8 = 0; q8 < 2; ++q8)
-                    if (LA_CHECK(in_smem(ch[q8], 16, sm_lo, sm_hi), 341, smem_u32(ch[q8]) - sm_lo, q8))
-                        *reinterpret_cast<uint4 *>(ch[q8]) = p.phi == LA_PHI_ELU1 ? dq_piece<true>(u[q8], xv + q8 * 8, inv)
-                                                                                  : dq_piece<false>(u[q8], xv + q8 * 8, inv);
+                    if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 341, smem_u32(ch[q8]) - sm_lo, q8))
+                        *reinterpret_cast<uint4 *>(ch[q8] + OFF_G) =
+                            p.phi == LA_PHI_ELU1 ? dq_piece<true>(u[q8], xv + q8 * 8, inv) : dq_piece<false>(u[q8], xv + q8 * 8, inv);
             }
             fence_proxy_async();
             if (i == 0 && h == 0) LA_TL(k, 12);
