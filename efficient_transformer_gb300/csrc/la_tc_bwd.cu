@@ -30,9 +30,10 @@
 namespace la {
 namespace {
 
-// Threads per CTA (80 registers a thread) and feature-map threads (warps 4-7 and 16-23).
+// Threads per CTA (80 registers a thread) and feature-map threads (dq: warps 4-7 and 16-23;
+// dk/dv: warps 16-23).
 constexpr int kDqThreads = 768, kDqPro = 384;
-constexpr int kKvThreads = 768, kKvPro = 384;
+constexpr int kKvThreads = 768, kKvPro = 256;
 
 template <int D, int G>
 struct BwdCfg {
@@ -683,6 +684,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     uint8_t *htile = rbf + K::RBF_BYTES;         // h as 16 x 128 (rows h_hi, h_lo) when it is not in dP'
     uint8_t *obuf = htile + (K::H_IN_DP ? 0 : K::H_BYTES);   // dk, then dv [keys][D] (OUT_STAGE)
     constexpr bool OUT_STAGE = K::OUT_STAGE;
+    constexpr bool PSPLIT = CAUSAL && C / 16 >= 2;   // two warpgroups convert P' and dP'
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
@@ -711,7 +713,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
         }
         mbar_init(&bar_afull[0], 1);
         mbar_init(&bar_afull[1], 1);
-        mbar_init(&bar_pready, 128);
+        mbar_init(&bar_pready, PSPLIT ? 256 : 128);
         for (int bb = 0; bb < 2; ++bb) {
             mbar_init(&bar_outfull[bb], 1);
             mbar_init(&bar_outfree[bb], 128);
@@ -971,10 +973,10 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             mma_commit_w(&bar_fin);
             warp_drain(&bar_fin, 0);
         }
-    } else if ((warp >= 4 && warp < 8) || warp >= 16) {
-        // ---------------- prologue (both warpgroups on every chunk): phi(K) over the K tile, in
+    } else if (warp >= 16) {
+        // ---------------- prologue (warps 16-23 on every chunk): phi(K) over the K tile, in
         // place (the Q tile arrives as phi_s = phi(q) / den, written by the dq kernel)
-        const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0 .. kKvPro - 1
+        const int pi = threadIdx.x - 512;   // 0 .. kKvPro - 1
         constexpr int CPR = D / 8, RPP = kKvPro / CPR;
         static_assert(RPP % 8 == 0, "rows per pass");
         const int c = pi % CPR, r0 = pi / CPR;
@@ -1134,8 +1136,11 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             if (d == 0) LA_TL2(k, 9);
             r_prev += r_chunk;
         }
-    } else if (warp >= 12 && warp < 16) {
-        // ---------------- warpgroup B (thread = query row i): P' and dP'
+    } else if ((warp >= 12 && warp < 16) || (PSPLIT && warp >= 4 && warp < 8)) {
+        // ---------------- warpgroup B (warps 12-15, thread = query row i): P' and dP'; with
+        // PSPLIT warps 4-7 take every second 16-key piece of the same rows
+        const bool wgb = warp >= 12;
+        const int c16_0 = PSPLIT && !wgb ? 1 : 0, c16_step = PSPLIT ? 2 : 1;
         const int wq = warp % 4;
         const int i = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -1156,14 +1161,14 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             const int bb = k % NB;
             ok = ok && warp_wait(&bar_afull[bb], (k / NB) & 1, &abort_flag);
             tc_fence_after();
-            if (i == 0) LA_TL2(k, 10);
+            if (i == 0 && wgb) LA_TL2(k, 10);
             float hnext = 0.f;
             if (k + 1 < nchunk) {
                 const int tn = t0 + (nchunk - 2 - k) * C + ti;
                 if (tn < t1 && LA_CHECK((size_t)bh * p.N + tn < (size_t)p.B * p.Hq * p.N, 435, bh, tn))
                     hnext = p.gd[(size_t)bh * p.N + tn];
             }
-            if (ok) {
+            if (ok && wgb) {
                 const __nv_bfloat16 hh = __float2bfloat16_rn(hv);
                 const __nv_bfloat16 hl = __float2bfloat16_rn(hv - __bfloat162float(hh));
                 if (K::H_IN_DP) {
@@ -1173,8 +1178,10 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 0, i)) = hh;
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 1, i)) = hl;
                 }
+            }
+            if (ok) {
 #pragma unroll 1
-                for (int c16 = 0; c16 < C / 16; ++c16) {
+                for (int c16 = c16_0; c16 < C / 16; c16 += c16_step) {
                     float va[16], vd[16];
                     tmem_ld16(tA(bb) + lane_off + c16 * 16, va);
                     tmem_ld16(tD(bb) + lane_off + c16 * 16, vd);
@@ -1206,7 +1213,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                 fence_proxy_async();
             }
             tc_fence_before();
-            if (i == 0) LA_TL2(k, 11);
+            if (i == 0 && wgb) LA_TL2(k, 11);
             mbar_arrive_warp(&bar_pready);
             hv = hnext;
         }
