@@ -1034,23 +1034,10 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS, bb = k % NB;
-            if (CAUSAL) {   // R after this chunk (its update is the chunk's first product) -> R_bf
+            if (CAUSAL) {   // the chunk's R part (its first products) is done
                 ok = ok && warp_wait(&bar_rfull, k & 1, &abort_flag);
                 tc_fence_after();
                 if (d == 0) LA_TL2(k, 15);
-                if (ok && d < D) {
-#pragma unroll
-                    for (int c16 = 0; c16 < D / 16; ++c16) {
-                        float v[16];
-                        tmem_ld16(tR + lane_off + c16 * 16, v);
-                        tmem_wait_regs<16>(v);
-                        store_rbf_row<D>(rbf, d, v, c16);
-                    }
-                }
-                fence_proxy_async();
-                tc_fence_before();
-                mbar_arrive_warp(&bar_rbf);
-                if (d == 0) LA_TL2(k, 8);
             }
             // OUT_STAGE: phi(k) of column d, kept in registers so that the [K | V] region goes
             // back to the loader as soon as no MMA reads it (causal: after the R part, which
@@ -1068,6 +1055,21 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     fk2[j / 2] = pack_bf16x2(__bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kr + swz_offset(C, j, dd))),
                                              __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kr + swz_offset(C, j + 1, dd))));
                 mbar_arrive_warp(&bar_emptykv[s]);
+            }
+            if (CAUSAL) {   // R after this chunk -> R_bf for the next one
+                if (ok && d < D) {
+#pragma unroll
+                    for (int c16 = 0; c16 < D / 16; ++c16) {
+                        float v[16];
+                        tmem_ld16(tR + lane_off + c16 * 16, v);
+                        tmem_wait_regs<16>(v);
+                        store_rbf_row<D>(rbf, d, v, c16);
+                    }
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive_warp(&bar_rbf);
+                if (d == 0) LA_TL2(k, 8);
             }
             if (!OUT_STAGE || CAUSAL) {
                 ok = ok && warp_wait(&bar_outfull[bb], (k / NB) & 1, &abort_flag);
