@@ -266,11 +266,11 @@ def max_over_ranks(x: float, world: int) -> float:
 # on the benchmark workload, from one ncu capture of the current kernels; a kernel changed
 # since its capture must be removed from this table (its traffic is then reported as null).
 MEASURED_TRAFFIC = {
-    "tc_bwd_dq_causal": (1352314368 + 1048551680,
+    "tc_bwd_dq_causal": (1352376320 + 1048392192,
                          "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
-    "tc_bwd_dkdv_causal": (1360861440 + 249664000,
+    "tc_bwd_dkdv_causal": (1360859904 + 249645824,
                            "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
-    "tc_fwd_causal": (815456000 + 490747136,
+    "tc_fwd_causal": (815448832 + 490749696,
                       "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
 }
 
