@@ -7,11 +7,12 @@
 // suffix state R = sum_{i after} phi(q_i) gn_i^T, r = sum gd_i phi(q_i) carries the rows
 // that come later.  Launch order:
 //
-//   k_tc_state -> scan (prefix S)
-//   k_tc_bwd_dq   forward over chunks: dq, per-row den and gd, and each segment's
-//                 R (tensor cores) and r (fp32)
+//   k_tc_state -> scan (prefix S)   (skipped when the forward's states are given)
+//   k_tc_bwd_dq   forward over chunks: dq, per-row den and h, each segment's R and r,
+//                 and (causal) the rows phi_s = phi(q) / den for the next kernel
 //   scan (suffix R)
-//   k_tc_bwd_dkdv reverse over chunks: dk, dv (summed over the n_rep heads of the group)
+//   k_tc_bwd_dkdv reverse over chunks: dk, dv (summed over the n_rep heads of the group),
+//                 reading phi_s where the dq kernel read q
 //
 // Per chunk of k_tc_bwd_dq (128 stacked query rows, C keys), with the raw grad_out g:
 //   A = phi(Q) phi(K)^T,  dA' = g V^T,  X = g S_bf^T,  den = phi(Q) z + rowsum mask(A) + eps
@@ -23,8 +24,10 @@
 // Per chunk of k_tc_bwd_dkdv, computed transposed so the 128 query rows stay on the MMA's
 // K dimension (and the sum over the group's heads comes for free):
 //   dk^T = phi(Q)^T dP + R_bf V^T (+ r),  dv^T = gn^T P + R_bf^T phi(K)^T,  R += phi(Q)^T gn
-// Warp roles: warp 0 TMA, warp 1 MMA, warp 2 (dq kernel) dq store; the dq kernel runs the
-// feature map on warps 4-7 and 16-19 together and its row work on a pool of warps 8-15.
+// Warp roles: warp 0 TMA, warp 1 MMA, warp 2 the TMA stores.  The dq kernel runs the feature
+// map on warps 4-7 and 16-23 (16-23 also convert S), its row work and dq on a pool of warps
+// 8-15; the dk/dv kernel runs the feature map of K on warps 16-23, R conversion and the dk,
+// dv epilogues on warps 8-11, and P' / dP' on warps 12-15 with warps 4-7.
 #include "la_tc_common.cuh"
 
 namespace la {
