@@ -98,6 +98,14 @@ def test_workspace_sizes(lib):
     assert lib.la_workspace_size(1, 3, 2, 64, 64, la.LA_BF16, 1, 0, 0) == 0     # invalid
     # deterministic plan
     assert f == lib.la_workspace_size(1, 32, 8, 65536, 128, la.LA_BF16, 1, 0, 0)
+    # the causal tensor-core backward also holds a bf16 row of phi(q)/den per query position
+    # (written by its dq kernel for its dk/dv kernel); the bidirectional one does not
+    assert lib.la_kernel_path(1, 32, 8, 65536, 128, la.LA_BF16, 1, 0, 1) == la.LA_PATH_TCGEN05
+    bidir = lib.la_workspace_size(1, 32, 8, 65536, 128, la.LA_BF16, 0, 0, 1)
+    assert b - bidir >= 32 * 65536 * 128 * 2
+    # the float32 (CUDA-core) backward keeps no such array
+    b32 = lib.la_workspace_size(1, 32, 8, 65536, 128, la.LA_F32, 1, 0, 1)
+    assert b32 < 32 * 65536 * 128 * 2
 
 
 def test_float32_always_takes_simt(lib):
