@@ -2,6 +2,9 @@
 oracle on the same inputs, and compare per output tensor."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -17,11 +20,18 @@ def to_dev(inp: dict) -> dict:
     return {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
 
 
-def run_gpu(w: gen.Workload, dev: dict):
+def run_gpu(w: gen.Workload, dev: dict, from_fwd: bool = False):
+    """la_fwd, then la_bwd (from_fwd=False: the backward recomputes the forward's states) or
+    la_bwd_from_fwd on the forward's workspace (from_fwd=True: the benchmark's step)."""
+    has_w = dev["cos_weight"] is not None
+    ws_f = None
+    if from_fwd:
+        n = la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, has_w, False)
+        ws_f = torch.empty(max(n, 1), dtype=torch.uint8, device=dev["q"].device)
     out = la.fwd(dev["q"], dev["k"], dev["v"], w.causal, w.phi, w.eps, dev["cos_weight"],
-                 dev["sin_weight"])
+                 dev["sin_weight"], workspace=ws_f)
     dq, dk, dv = la.bwd(dev["q"], dev["k"], dev["v"], dev["grad_out"], w.causal, w.phi, w.eps,
-                        dev["cos_weight"], dev["sin_weight"])
+                        dev["cos_weight"], dev["sin_weight"], fwd_workspace=ws_f)
     la.get_status()
     return out, dq, dk, dv
 
@@ -42,9 +52,29 @@ def rel_err(got: torch.Tensor, ref: np.ndarray) -> float:
     return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-30))
 
 
-def compare(w: gen.Workload, got, ref, label: str = ""):
+def record(w: gen.Workload, errs: dict, label: str = "") -> None:
+    """Append the achieved errors to the JSON-lines file named by LA_PARITY_RECORD (if set),
+    so that the margin below the bar can be read after a run."""
+    path = os.environ.get("LA_PARITY_RECORD")
+    if not path:
+        return
+    fwd_path = la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, False)
+    bwd_path = la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, True)
+    names = {la.LA_PATH_SIMT: "simt", la.LA_PATH_TCGEN05: "tcgen05"}
+    row = {"workload": w.name, "label": label, "dtype": w.dtype, "tol": TOL[w.dtype],
+           "fwd_path": names[fwd_path], "bwd_path": names[bwd_path],
+           "shape": [w.B, w.Hq, w.Hkv, w.N, w.D], "causal": w.causal, "phi": w.phi, "eps": w.eps,
+           "weights": w.weights, "errors": errs}
+    d = os.path.dirname(os.path.abspath(path))
+    os.makedirs(d, exist_ok=True)
+    with open(path, "a") as f:
+        f.write(json.dumps(row) + "\n")
+
+
+def compare(w: gen.Workload, got, ref, label: str = "", names=("out", "dq", "dk", "dv")):
     tol = TOL[w.dtype]
-    errs = {n: rel_err(a, b) for n, a, b in zip(("out", "dq", "dk", "dv"), got, ref)}
+    errs = {n: rel_err(a, b) for n, a, b in zip(names, got, ref)}
+    record(w, errs, label)
     bad = {n: e for n, e in errs.items() if not e <= tol}
     assert not bad, f"{label} {w.name}: errors {errs} exceed {tol}"
     return errs

@@ -25,42 +25,78 @@ def built():
 # Workloads small enough for the full oracle.
 SMALL = ["causal_b1_h2_n256_d32_f32", "bidir_b2_h8_n2048_d64_bf16_elu1",
          "bidir_b2_h8_n2048_d64_bf16_relu", "causal_b4_h16_n4096_d64_bf16"]
-# Full-size workloads checked on whole key/value groups (b, g): groups are independent,
-# so the oracle on a group's slice gives exactly those rows of the full result.
-LARGE = {"cosformer_causal_b2_h16_n8192_d128_bf16": [(0, 0), (1, 15)],
-         "gqa_causal_b1_hq32_hkv8_n65536_d128_bf16": [(0, 0), (0, 7)]}
+# Full-size workloads, compared with the oracle on every (batch, key/value head) group.
+LARGE = ["cosformer_causal_b2_h16_n8192_d128_bf16", "gqa_causal_b1_hq32_hkv8_n65536_d128_bf16"]
+
+_oracle_cache = {}
 
 
-def groups_slice(inp, w, groups):
-    """Concatenate several (b, g) slices along the head axes (one oracle call, more threads)."""
-    parts = [gen.kv_group_slice(inp, w, b, g) for b, g in groups]
-    cat = {n: torch.cat([p[n] for p in parts], dim=1) for n in ("q", "k", "v", "grad_out")}
-    cat["cos_weight"], cat["sin_weight"] = inp["cos_weight"], inp["sin_weight"]
-    return cat
+def oracle_of(w, inp, key):
+    """The oracle's (out, dq, dk, dv) for one workload's seeded inputs, computed once."""
+    if key not in _oracle_cache:
+        _oracle_cache.clear()   # hold one full-size result at a time
+        _oracle_cache[key] = H.run_oracle(w, inp)
+    return _oracle_cache[key]
 
 
-def groups_rows(w, results, groups):
-    parts = [H.group_rows(w, results, b, g) for b, g in groups]
-    return tuple(torch.cat([p[i] for p in parts], dim=1) for i in range(4))
-
-
+@pytest.mark.parametrize("from_fwd", [False, True], ids=["bwd", "bwd_from_fwd"])
 @pytest.mark.parametrize("name", SMALL)
-def test_workload_full(name):
+def test_workload_full(name, from_fwd):
     w = gen.WORKLOADS[name]
     inp = gen.make_inputs(w)
-    got = H.run_gpu(w, H.to_dev(inp))
+    got = H.run_gpu(w, H.to_dev(inp), from_fwd=from_fwd)
+    H.compare(w, got, oracle_of(w, inp, name), label="bwd_from_fwd" if from_fwd else "bwd")
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_workload_large(name):
+    """The benchmark's step (la_fwd, then la_bwd_from_fwd on its workspace) at full size,
+    every output element against the oracle."""
+    w = gen.WORKLOADS[name]
+    inp = gen.make_inputs(w)
+    got = H.run_gpu(w, H.to_dev(inp), from_fwd=True)
+    ref = oracle_of(w, inp, name)
+    H.compare(w, got, ref, label="bwd_from_fwd, every group")
+
+
+def test_large_bwd_matches_bwd_from_fwd():
+    """At the benchmark's size, la_bwd (states recomputed) gives the same bits as
+    la_bwd_from_fwd (the forward's states reused)."""
+    w = gen.WORKLOADS["gqa_causal_b1_hq32_hkv8_n65536_d128_bf16"]
+    dev = H.to_dev(gen.make_inputs(w))
+    a = H.run_gpu(w, dev, from_fwd=True)
+    b = H.run_gpu(w, dev, from_fwd=False)
+    for n, x, y in zip(("out", "dq", "dk", "dv"), a, b):
+        assert torch.equal(x, y), n
+
+
+# Every tensor-core instantiation that the plan selects, at sizes with several segments of
+# several chunks per (batch, key/value head) and a ragged last chunk (N % C != 0).
+TC_CASES = [
+    # B, Hq, Hkv, N, D, causal, phi
+    (2, 16, 8, 3000, 64, False, "elu+1"),     # n_rep 2
+    (2, 16, 4, 3000, 64, False, "relu"),      # n_rep 4
+    (2, 16, 2, 3000, 64, False, "elu+1"),     # n_rep 8
+    (2, 16, 8, 3000, 128, False, "relu"),
+    (2, 16, 4, 3000, 128, False, "elu+1"),
+    (2, 16, 2, 3000, 128, False, "relu"),
+    (2, 16, 2, 3000, 128, True, "elu+1"),     # causal, n_rep 8
+    (2, 16, 8, 3000, 128, True, "relu"),      # causal, n_rep 2
+    (1, 8, 8, 1500, 64, False, "relu"),       # n_rep 1
+    (1, 4, 4, 2100, 128, True, "elu+1"),      # n_rep 1, D = 128
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_tensor_core_instantiations(case):
+    B, Hq, Hkv, N, D, causal, phi = case
+    w = gen.Workload(f"tc_b{B}_hq{Hq}_hkv{Hkv}_n{N}_d{D}_{'causal' if causal else 'bidir'}_{phi}",
+                     B, Hq, Hkv, N, D, "bf16", causal, phi, scale=0.5)
+    inp = gen.make_inputs(w, seed=13)
+    dev = H.to_dev(inp)
     ref = H.run_oracle(w, inp)
-    H.compare(w, got, ref)
-
-
-@pytest.mark.parametrize("name", sorted(LARGE))
-def test_workload_groups(name):
-    w = gen.WORKLOADS[name]
-    inp = gen.make_inputs(w)
-    got = H.run_gpu(w, H.to_dev(inp))
-    groups = LARGE[name]
-    ref = H.run_oracle(w, groups_slice(inp, w, groups))
-    H.compare(w, groups_rows(w, got, groups), ref, label=f"groups {groups}")
+    H.compare(w, H.run_gpu(w, dev, from_fwd=True), ref, label="bwd_from_fwd")
+    H.compare(w, H.run_gpu(w, dev, from_fwd=False), ref, label="bwd")
 
 
 # With a single visible key (N = 1) the exact dq and dk equal b (g . v) eps / den^2: the
@@ -121,10 +157,21 @@ def test_deterministic():
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_no_writes_outside_outputs(dtype):
-    """Guard bands around every output buffer stay untouched."""
-    w = gen.Workload("guard", 1, 4, 2, 77, 64, dtype, True, "elu+1", weights=True)
+GUARD_CASES = [
+    # B, Hq, Hkv, N, D, dtype, weights   (N leaves a ragged last chunk on every path)
+    (1, 4, 2, 77, 64, "f32", True),      # CUDA-core kernels
+    (1, 4, 2, 77, 64, "bf16", True),     # CUDA-core kernels (position weights)
+    (1, 8, 2, 205, 128, "bf16", False),  # tensor-core kernels, n_rep 4, TMA-store epilogues
+    (1, 2, 2, 141, 64, "bf16", False),   # tensor-core kernels, n_rep 1
+]
+
+
+@pytest.mark.parametrize("case", GUARD_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_no_writes_outside_outputs(case):
+    """Guard bands around every output buffer stay untouched (forward, la_bwd and
+    la_bwd_from_fwd)."""
+    B, Hq, Hkv, N, D, dtype, weights = case
+    w = gen.Workload("guard", B, Hq, Hkv, N, D, dtype, True, "elu+1", weights=weights)
     dev = H.to_dev(gen.make_inputs(w, seed=9))
     pad = 4096
     canary = 1234.5
@@ -133,18 +180,41 @@ def test_no_writes_outside_outputs(dtype):
         buf = torch.full((like.numel() + 2 * pad,), canary, dtype=like.dtype, device="cuda")
         return buf, buf[pad:pad + like.numel()].view(like.shape)
 
+    ws_f = torch.empty(max(1, la.workspace_size(B, Hq, Hkv, N, D, dev["q"].dtype, True, weights, False)),
+                       dtype=torch.uint8, device="cuda")
     ob, out = guarded(dev["q"])
-    qb, dq = guarded(dev["q"])
-    kb, dk = guarded(dev["k"])
-    vb, dv = guarded(dev["v"])
-    la.fwd(dev["q"], dev["k"], dev["v"], True, "elu+1", 1e-6, dev["cos_weight"], dev["sin_weight"], out=out)
-    la.bwd(dev["q"], dev["k"], dev["v"], dev["grad_out"], True, "elu+1", 1e-6, dev["cos_weight"],
-           dev["sin_weight"], dq=dq, dk=dk, dv=dv)
-    la.get_status()
-    for buf in (ob, qb, kb, vb):
-        assert torch.all(buf[:pad] == canary) and torch.all(buf[-pad:] == canary)
+    la.fwd(dev["q"], dev["k"], dev["v"], True, "elu+1", 1e-6, dev["cos_weight"], dev["sin_weight"], out=out,
+           workspace=ws_f)
     ref = H.run_oracle(w, {n: (t.cpu() if t is not None else None) for n, t in dev.items()})
-    H.compare(w, (out, dq, dk, dv), ref)
+    for fwd_ws in (None, ws_f):
+        qb, dq = guarded(dev["q"])
+        kb, dk = guarded(dev["k"])
+        vb, dv = guarded(dev["v"])
+        la.bwd(dev["q"], dev["k"], dev["v"], dev["grad_out"], True, "elu+1", 1e-6, dev["cos_weight"],
+               dev["sin_weight"], dq=dq, dk=dk, dv=dv, fwd_workspace=fwd_ws)
+        la.get_status()
+        for buf in (ob, qb, kb, vb):
+            assert torch.all(buf[:pad] == canary) and torch.all(buf[-pad:] == canary)
+        H.compare(w, (out, dq, dk, dv), ref, label="guard bands")
+
+
+# N = 1 at the stated eps = 1e-6: the output out_0 = v_0 s / (s + eps) is well conditioned
+# (only the gradients are not; they are checked above at eps = 100).
+@pytest.mark.parametrize("case", [
+    (1, 1, 1, 1, 32, "f32", True, "elu+1", False),
+    (1, 2, 1, 1, 64, "bf16", True, "relu", False),
+    (1, 4, 1, 1, 128, "bf16", False, "elu+1", False),
+    (2, 2, 2, 1, 128, "bf16", True, "relu", True),
+], ids=lambda c: "x".join(map(str, c)))
+def test_single_token_output_at_small_eps(case):
+    B, Hq, Hkv, N, D, dt, causal, phi, weights = case
+    w = gen.Workload("n1_eps1e-6", B, Hq, Hkv, N, D, dt, causal, phi, eps=1e-6, weights=weights)
+    inp = gen.make_inputs(w, seed=4)
+    dev = H.to_dev(inp)
+    out = la.fwd(dev["q"], dev["k"], dev["v"], causal, phi, 1e-6, dev["cos_weight"], dev["sin_weight"])
+    la.get_status()
+    ref = H.run_oracle(w, inp)[0]
+    H.compare(w, (out,), (ref,), label="out only", names=("out",))
 
 
 def test_status_clean_after_runs():
@@ -169,9 +239,10 @@ def test_binding_errors_are_raised():
     ("gqa_causal_b1_hq32_hkv8_n65536_d128_bf16", la.LA_PATH_TCGEN05),
 ])
 def test_kernel_family(name, fwd_path):
-    """The bf16 workloads without position weights run the tcgen05 forward."""
+    """The bf16 workloads without position weights run the tcgen05 forward and backward."""
     w = gen.WORKLOADS[name]
     assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, False) == fwd_path
+    assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, True) == fwd_path
 
 
 # la_bwd_from_fwd reuses the forward's segment states when the two plans agree (and
