@@ -266,12 +266,9 @@ def max_over_ranks(x: float, world: int) -> float:
 # on the benchmark workload, from one ncu capture of the current kernels; a kernel changed
 # since its capture must be removed from this table (its traffic is then reported as null).
 MEASURED_TRAFFIC = {
-    "tc_bwd_dq_causal": (1352376320 + 1048392192,
-                         "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
-    "tc_bwd_dkdv_causal": (1360859904 + 249645824,
-                           "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
-    "tc_fwd_causal": (815448832 + 490749696,
-                      "ncu one-pass capture, profiles/tc_gqa_causal_b1_hq32_hkv8_n65536_d128.md"),
+    "tc_bwd_dq_causal": (1352376320 + 1048392192, "ncu one-pass capture of the current kernels (commit c245c31)"),
+    "tc_bwd_dkdv_causal": (1360859904 + 249645824, "ncu one-pass capture of the current kernels (commit c245c31)"),
+    "tc_fwd_causal": (815448832 + 490749696, "ncu one-pass capture of the current kernels (commit c245c31)"),
 }
 
 
@@ -289,7 +286,8 @@ def config_of(w: gen.Workload, world: int):
             "parallelism": f"replicas{world}",
             "step": "la_fwd, then la_bwd_from_fwd (the backward reads the forward's segment states)",
             "l2": f"no explicit flush: inputs larger than L2 ({path_bytes(w) / 2**20:.0f} MiB moved "
-                  f"per step vs {L2_BYTES / 2**20:.0f} MiB L2)"}
+                  f"per step vs {L2_BYTES / 2**20:.0f} MiB L2); the per-workload table flushes L2 "
+                  f"before each step of workloads that fit in it"}
 
 
 def run_reference(args, world, rank):
@@ -317,6 +315,143 @@ def run_reference(args, world, rank):
     return 0
 
 
+# The HBM bandwidth of the operation's stated roofline (the slower of the tensor-core peak and
+# HBM bytes at 8 TB/s); the measured copy bandwidth gives a second, stricter-looking fraction.
+ROOFLINE_HBM_GBS = 8000.0
+FLUSH_BYTES = 512 * 2**20   # written between timed steps of workloads that fit in L2
+
+
+def path_roofline(w: gen.Workload, peaks: dict, ms_step: float, peak_src: str):
+    nbytes, flops = path_bytes(w), path_flops(w)
+    t_tc = flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_8 = max(nbytes / (ROOFLINE_HBM_GBS * 1e9), t_tc)
+    t_m = max(nbytes / (peaks["hbm_gbs"] * 1e9), t_tc)
+    return {"bytes_per_step": nbytes, "flops_per_step": flops,
+            "t_roofline_ms": t_8 * 1e3, "frac": t_8 * 1e3 / ms_step,
+            "basis": f"max(bytes / {ROOFLINE_HBM_GBS:.0f} GB/s, flops / {peak_src} bf16 sustained "
+                     f"{peaks['bf16_tflops_sustained']} TFLOP/s)",
+            "t_roofline_measured_hbm_ms": t_m * 1e3, "frac_measured_hbm": t_m * 1e3 / ms_step,
+            "measured_hbm_gbs": peaks["hbm_gbs"]}
+
+
+class Problem:
+    """Device inputs, outputs and workspaces of one workload, and its step: la_fwd, then
+    la_bwd_from_fwd on the forward's workspace."""
+
+    def __init__(self, la, w: gen.Workload, dev, seed: int = 0, host=None):
+        self.la, self.w = la, w
+        host = host if host is not None else gen.make_inputs(w, seed=seed)
+        self.d = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
+        d = self.d
+        self.out = torch.empty_like(d["q"])
+        self.dq, self.dk, self.dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+        has_w = d["cos_weight"] is not None
+        self.ws_f = torch.empty(max(1, la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, d["q"].dtype, w.causal, has_w,
+                                                         False)), dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(max(1, la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, d["q"].dtype, w.causal, has_w,
+                                                         True)), dtype=torch.uint8, device=dev)
+
+    def step(self, stream, x=None):
+        la, w = self.la, self.w
+        x = x or self.d
+        la.fwd(x["q"], x["k"], x["v"], w.causal, w.phi, w.eps, x["cos_weight"], x["sin_weight"],
+               out=self.out, workspace=self.ws_f, stream=stream)
+        la.bwd(x["q"], x["k"], x["v"], x["grad_out"], w.causal, w.phi, w.eps, x["cos_weight"],
+               x["sin_weight"], dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws_b, stream=stream,
+               fwd_workspace=self.ws_f)
+
+    def paths(self):
+        la, w = self.la, self.w
+        names = {la.LA_PATH_SIMT: "simt", la.LA_PATH_TCGEN05: "tcgen05"}
+        return {p: names[la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, p == "bwd")]
+                for p in ("fwd", "bwd")}
+
+
+def time_blocks(step, dev, stream, steps: int, repeats: int, world: int):
+    """`repeats` blocks of exactly `steps` steps; each block between two events on the
+    stream, with a barrier and a synchronisation on both sides.  Returns ms per step of
+    each block (max over ranks)."""
+    per = []
+    for _ in range(repeats):
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per.append(e0.elapsed_time(e1) / steps)
+    barrier(world)
+    return [max_over_ranks(x, world) for x in per]
+
+
+def time_flushed(run, dev, stream, steps: int, flush: torch.Tensor):
+    """`steps` single steps, L2 flushed (a 512 MiB write) before each; ms of each step."""
+    per = []
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per.append(e0.elapsed_time(e1))
+    return per
+
+
+def summary_ms(per):
+    return {"ms_per_step": statistics.median(per), "ms_min": min(per), "ms_max": max(per),
+            "samples": len(per)}
+
+
+def measure_config(la, w: gen.Workload, dev, steps: int, warmup: int, peaks, peak_src, flush):
+    """One row of the per-workload table: the workload's step timed on its own."""
+    pr = Problem(la, w, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, warmup)):
+        pr.step(stream)
+    la.get_status(stream)
+    small = path_bytes(w) < 4 * L2_BYTES
+    row = {"workload": w.name, "paths": pr.paths()}
+    if small:
+        # launch-bound sizes: one step captured in a CUDA graph and replayed, L2 flushed first
+        run, how = (lambda: pr.step(stream)), "library calls"
+        try:
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cap):
+                pr.step(torch.cuda.current_stream(dev))
+            stream.wait_stream(cap)
+            torch.cuda.synchronize(dev)
+            run, how = g.replay, "one step captured in a CUDA graph, replayed"
+        except RuntimeError as e:   # capture refused: time the plain calls
+            how = f"library calls (graph capture failed: {str(e)[:80]})"
+        run()
+        torch.cuda.synchronize(dev)
+        per = time_flushed(run, dev, stream, max(steps, 20), flush)
+        row["timing"] = f"{how}; L2 flushed ({FLUSH_BYTES >> 20} MiB write) before each timed step"
+    else:
+        per = time_blocks(lambda: pr.step(stream), dev, stream, steps, 5, 1)
+        row["timing"] = f"5 blocks of {steps} steps; inputs larger than L2"
+    la.get_status(stream)
+    row.update(summary_ms(per))
+    ms = row["ms_per_step"]
+    row["tokens_per_s"] = w.tokens / (ms / 1e3)
+    row["tflops"] = path_flops(w) / (ms / 1e3) / 1e12
+    rl = path_roofline(w, peaks, ms, peak_src)
+    row["roofline_frac"] = rl["frac"]
+    row["roofline_frac_measured_hbm"] = rl["frac_measured_hbm"]
+    row["t_roofline_ms"] = rl["t_roofline_ms"]
+    if w.dtype == "f32":
+        row["note"] = "float32, 0.6 MiB per step: launch-bound, reported only"
+    del pr
+    torch.cuda.empty_cache()
+    return row
+
+
 def run_ours(args, world, rank, local):
     from efficient_transformer_gb300 import build as la_build
     from efficient_transformer_gb300 import la
@@ -328,57 +463,43 @@ def run_ours(args, world, rank, local):
     w = workload_of(args)
     dev = torch.device("cuda", local)
     host = gen.make_inputs(w, seed=rank)
-    d = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
     pinned = {n: (t.pin_memory() if t is not None else None) for n, t in host.items()}
+    pr = Problem(la, w, dev, host=host)
     del host
-    out = torch.empty_like(d["q"])
-    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
-    has_w = d["cos_weight"] is not None
-    ws_f = torch.empty(max(1, la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, d["q"].dtype, w.causal, has_w, False)),
-                       dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(max(1, la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, d["q"].dtype, w.causal, has_w, True)),
-                       dtype=torch.uint8, device=dev)
+    d = pr.d
     stream = torch.cuda.current_stream(dev)
-
-    def step(x):
-        la.fwd(x["q"], x["k"], x["v"], w.causal, w.phi, w.eps, x["cos_weight"], x["sin_weight"],
-               out=out, workspace=ws_f, stream=stream)
-        la.bwd(x["q"], x["k"], x["v"], x["grad_out"], w.causal, w.phi, w.eps, x["cos_weight"],
-               x["sin_weight"], dq=dq, dk=dk, dv=dv, workspace=ws_b, stream=stream, fwd_workspace=ws_f)
+    peaks, peak_src = load_peaks()
 
     clocks = ClockSampler(nvsmi_id(dev, local))
     clocks.start()
     time.sleep(0.3)
     for _ in range(args.warmup):
-        step(d)
+        pr.step(stream)
     la.get_status(stream)
 
-    # Device-timed region: inputs resident in HBM, K steps between two events on the stream.
-    barrier(world)
-    torch.cuda.synchronize(dev)
+    # Device-timed region: inputs resident in HBM.  Blocks of exactly K steps, each between
+    # two events on the launching stream; repeated for a few seconds of sustained load, the
+    # reported step time being the median block.
+    first = time_blocks(lambda: pr.step(stream), dev, stream, args.steps, 1, world)[0]
+    repeats = args.repeats or max(5, min(200, int(math.ceil(3000.0 / max(first * args.steps, 1e-3)))))
     t_wall0 = time.time()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step(d)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    per = time_blocks(lambda: pr.step(stream), dev, stream, args.steps, repeats, world)
     t_wall1 = time.time()
-    barrier(world)
     la.get_status(stream)
-    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
-    ms_step = ms_total / args.steps
+    ms_step = statistics.median(per)
     # The same K steps again with every library launch bracketed by events (per-kernel shares
     # and the dominant kernel's launch time); kept apart so the events cost the timing nothing.
     barrier(world)
     torch.cuda.synchronize(dev)
     la.trace_start()
     for _ in range(args.steps):
-        step(d)
+        pr.step(stream)
     torch.cuda.synchronize(dev)
     kernels = la.trace_stop()
     barrier(world)
     la.get_status(stream)
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
 
     # End to end: pinned host inputs -> device, fwd + bwd, every output back to pinned host.
     # Every step copies its own inputs in and all of its outputs out inside the timed region;
@@ -386,7 +507,7 @@ def run_ours(args, world, rank, local):
     # step i's input copy and step i-1's output copy overlap step i's kernels.
     e2e = None
     if not args.no_e2e:
-        outs = (("out", out), ("dq", dq), ("dk", dk), ("dv", dv))
+        outs = (("out", pr.out), ("dq", pr.dq), ("dk", pr.dk), ("dv", pr.dv))
         h2d = sum(t.numel() * t.element_size() for t in pinned.values() if t is not None)
         d2h = sum(t.numel() * t.element_size() for _, t in outs)
         e2e_steps = max(2, min(args.steps, 10))
@@ -396,7 +517,7 @@ def run_ours(args, world, rank, local):
                 "x": {n: (torch.empty_like(t) if t is not None else None) for n, t in d.items()},
                 "o": {n: torch.empty_like(t) for n, t in outs},
                 "h": {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs},
-                "wf": torch.empty_like(ws_f), "wb": torch.empty_like(ws_b)})
+                "wf": torch.empty_like(pr.ws_f), "wb": torch.empty_like(pr.ws_b)})
         s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
 
         def e2e_run(nsteps, e_start=None, e_end=None):
@@ -445,17 +566,25 @@ def run_ours(args, world, rank, local):
         e2e = {"value": world * w.tokens / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "overlap": "input copy, kernels and output copy on three streams, two buffer sets"}
-    clocks.stop()
-    clk = clocks.summary(t_wall0, t_wall1)
+        del sets
+
+    # Per-workload table (one GPU): every workload's step timed on its own.
+    table = None
+    if world == 1 and not args.no_configs and not args.seq_len:
+        del pinned
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        table = []
+        for name, wc in gen.WORKLOADS.items():
+            if name == w.name:
+                continue
+            table.append(measure_config(la, wc, dev, args.steps, args.warmup, peaks, peak_src, flush))
+        del flush
 
     if rank != 0:
         return 0
 
-    peaks, peak_src = load_peaks()
     tokens_per_s = world * w.tokens / (ms_step / 1e3)
     flops = path_flops(w)
-    nbytes = path_bytes(w)
-    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops_sustained"] * 1e12))
 
     # Dominant kernel: the one with the largest share of traced device time.
     launches = sum(n for n, _ in kernels.values())
@@ -478,7 +607,9 @@ def run_ours(args, world, rank, local):
         peak = peaks["hbm_gbs"]
         peak_note = f"{peak_src} hbm_gbs"
     traffic = MEASURED_TRAFFIC.get(top_name) if w.name == gen.BENCH_WORKLOAD else None
-    roofline = {"bound": bound, "kernel": top_name, "achieved": achieved, "peak": peak, "unit": unit,
+    roofline = {"bound": bound, "kernel": top_name,
+                "scope": "the dominant kernel alone (largest share of traced device time)",
+                "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": traffic[0] if traffic else None,
                 "traffic_source": traffic[1] if traffic else None, "peak_source": peak_note,
                 "launch_ms": per_launch_s * 1e3,
@@ -492,18 +623,19 @@ def run_ours(args, world, rank, local):
                "sample": f"first {tokens} of {w.N} positions of every (batch, head), one fwd+bwd "
                          f"({t:.1f} s); tokens/s = B*{tokens} / seconds"}
 
+    cfg = config_of(w, world)
+    cfg["timing"] = (f"median of {repeats} blocks of {args.steps} steps (each block between two CUDA events, "
+                     f"synchronised on both sides)")
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) inputs, scale per workload)",
-        "config": config_of(w, world),
+        "config": cfg,
+        "ms_spread": {"min": min(per), "max": max(per), "blocks": len(per)},
         "tflops": world * flops / (ms_step / 1e3) / 1e12,
-        "path_roofline": {"bytes_per_step": nbytes, "flops_per_step": flops,
-                          "t_roofline_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
-                          "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s, bf16 sustained "
-                                   f"{peaks['bf16_tflops_sustained']} TFLOP/s"},
+        "path_roofline": path_roofline(w, peaks, ms_step, peak_src),
         "roofline": roofline,
         "kernels": {k: {"launches": n, "ms_per_launch": ms / n, "share": ms / total_ms if total_ms else None}
                     for k, (n, ms) in sorted(kernels.items(), key=lambda kv: -kv[1][1])},
@@ -511,6 +643,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,
+        "workloads": table,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -527,6 +660,10 @@ def main(argv=None):
                     help="approximate length of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table (every workload's step timed on its own)")
+    ap.add_argument("--repeats", type=int, default=0,
+                    help="timed blocks of --steps steps (default: enough for about 3 s)")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="run the workload at this sequence length instead (small cases for profilers)")
     args = ap.parse_args(argv)

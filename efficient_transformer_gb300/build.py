@@ -2,6 +2,11 @@
 
 Each CUDA source compiles to its own object in parallel; the objects link into
 ``efficient_transformer_gb300/_lib/libla.so`` (git-ignored).  Nothing is installed.
+
+``build(variant="test")`` builds the same sources with ``-DLA_TEST_HOOKS`` into
+``_lib/libla_test.so``: bounded waits give up after 5 ms instead of 2 s, and one exported
+switch makes a kernel withhold a barrier arrival, so that a test can check the timeout
+path end to end.  The product library never contains these hooks.
 """
 from __future__ import annotations
 
@@ -47,16 +52,27 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile every ``csrc/*.cu`` and link ``libla.so``; returns the library path."""
+VARIANTS = {"": [], "test": ["-DLA_TEST_HOOKS"]}
+
+
+def lib_path(variant: str = "") -> str:
+    return LIB_PATH if not variant else os.path.join(LIB_DIR, f"libla_{variant}.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          variant: str = "") -> str:
+    """Compile every ``csrc/*.cu`` and link ``libla.so`` (or the named variant); returns
+    the library path."""
     nvcc = _nvcc()
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    obj_dir = OBJ_DIR if not variant else OBJ_DIR + "_" + variant
+    out_lib = lib_path(variant)
+    os.makedirs(obj_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     common = _deps()
-    flags = NVCC_FLAGS + (extra_flags or [])
+    flags = NVCC_FLAGS + VARIANTS[variant] + (extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(obj, common + [src]):
             cmd = [nvcc] + ARCH + flags + ["-c", src, "-o", obj + ".tmp.o"]
             if verbose:
@@ -68,11 +84,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    if force or _stale(LIB_PATH, objs):
-        cmd = [nvcc] + ARCH + ["-shared", "-o", LIB_PATH + ".tmp", *objs]
+    if force or _stale(out_lib, objs):
+        cmd = [nvcc] + ARCH + ["-shared", "-o", out_lib + ".tmp", *objs]
         subprocess.run(cmd, check=True)
-        os.replace(LIB_PATH + ".tmp", LIB_PATH)
-    return LIB_PATH
+        os.replace(out_lib + ".tmp", out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":

@@ -32,6 +32,10 @@ namespace {
 
 constexpr int kFwdThreads = 768, kFwdPro = 384;   // feature map: warps 4-7 and 16-23
 
+#ifdef LA_TEST_HOOKS
+__device__ int g_la_test_skip;   // test build: withhold one arrival in k_tc_fwd (see there)
+#endif
+
 template <int D, int G>
 struct FwdCfg {
     static constexpr int C = 128 / G;                  // tokens per chunk
@@ -416,6 +420,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 fence_proxy_async();
             }
             if (i == 0) LA_TL(k, 2);
+#ifdef LA_TEST_HOOKS
+            // test build only: while armed, warp 4 of block 0 withholds its arrival for the
+            // first chunk, so the MMA warp's bounded wait for that chunk runs out
+            if (g_la_test_skip && blockIdx.x == 0 && k == 0 && warp == 4) continue;
+#endif
             mbar_arrive_warp(&bar_ready[s]);
         }
     } else if (warp >= 8 && warp < 12) {
@@ -671,6 +680,13 @@ cudaError_t tc_launch_state(const Params &p, cudaStream_t s) {
 }
 
 }  // namespace la
+
+#ifdef LA_TEST_HOOKS
+// Test builds only: arm (1) or disarm (0) the withheld arrival of k_tc_fwd.
+extern "C" int la_test_withhold_arrival(int on) {
+    return cudaMemcpyToSymbol(la::g_la_test_skip, &on, sizeof(int)) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 #ifdef LA_TIMELINE
 // Timeline builds only: copy out the forward kernel's event clocks ([64][16] long long).

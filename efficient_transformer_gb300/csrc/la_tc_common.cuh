@@ -24,7 +24,7 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kWaitNs) return;
+        if (globaltimer_ns() - t0 > kDrainNs) return;
 }
 
 // Warp-uniform bounded wait.  A phase that has already completed is seen by one
@@ -111,7 +111,10 @@ __device__ long long g_la_tl2[64][16];   // a second kernel of the same translat
 // exp(m) = 2^y with y = m log2(e).  y is formed as yh = bf16(m * c_hi) (c_hi = log2(e)
 // rounded to bf16) plus the small remainder r = (m c_hi - yh) + m (log2(e) - c_hi), the
 // first term exact in one fused multiply-add; then 2^y = 2^yh 2^r ~ 2^yh (1 + r ln 2),
-// with 2^yh from the packed bf16 ex2 instruction.  About ten packed operations per pair.
+// with 2^yh from the packed bf16 ex2 instruction.  About ten packed operations per pair;
+// at most 0.9 % relative error over bf16 x in [-12, 4].  (A float32 version with a single
+// rounding was measured: it lowers the tensor-core dq error by at most 20 % and makes the
+// long-context step 10 % slower, the feature map being on every kernel's chunk path.)
 __device__ __forceinline__ uint32_t feat_bf16x2(uint32_t u, int phi) {
     __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&u);
     const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);

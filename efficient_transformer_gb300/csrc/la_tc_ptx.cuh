@@ -19,8 +19,15 @@ namespace la {
 namespace tc {
 
 // A bounded mbarrier wait gives up after this many nanoseconds (every legitimate wait in
-// the library's kernels is shorter than a whole kernel, far below this).
+// the library's kernels is shorter than a whole kernel, far below this).  The test build
+// (LA_TEST_HOOKS) shortens it to 5 ms so that a test can make a wait run out quickly; the
+// drain of copies already in flight on the exit path keeps the long bound (kDrainNs).
+#ifdef LA_TEST_HOOKS
+constexpr uint64_t kWaitNs = 5000000ull;
+#else
 constexpr uint64_t kWaitNs = 2000000000ull;
+#endif
+constexpr uint64_t kDrainNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
