@@ -52,7 +52,9 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-VARIANTS = {"": [], "test": ["-DLA_TEST_HOOKS"]}
+# "timeline": block 0 of the forward and backward kernels records clock64() at fixed events
+# of its first 64 chunks (read back with la_timeline_read*), for pipeline studies.
+VARIANTS = {"": [], "test": ["-DLA_TEST_HOOKS"], "timeline": ["-DLA_TIMELINE"]}
 
 
 def lib_path(variant: str = "") -> str:

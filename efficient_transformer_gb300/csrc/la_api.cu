@@ -94,18 +94,28 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
     const size_t state_bytes = align_up((size_t)bg * pl.nseg * pl.state_elems * sizeof(float), 256);
     pl.off_state = 0;
     size_t off = state_bytes;
+    const bool tc = pl.path == LA_PATH_TCGEN05;
+    const size_t row_bytes = align_up((size_t)B * Hq * N * sizeof(float), 256);
+    // tensor-core path: den rows padded to a 16-byte multiple (TMA row stride)
+    const size_t den_bytes = tc ? align_up((size_t)B * Hq * tc_den_stride(N) * sizeof(float), 256) : row_bytes;
     if (is_bwd) {
         pl.off_rstate = off;
         off += state_bytes;
-        const size_t row_bytes = align_up((size_t)B * Hq * N * sizeof(float), 256);
         pl.off_den = off;
-        off += row_bytes;
+        off += den_bytes;
         pl.off_gd = off;
         off += row_bytes;
-        if (pl.path == LA_PATH_TCGEN05 && causal) {   // phi(q) / den rows, bf16
+        if (tc && causal) {   // phi(q) / den rows, bf16
             pl.off_phis = off;
             off += align_up((size_t)B * Hq * N * D * 2, 256);
         }
+    } else if (tc) {   // the forward leaves its per-row dens for the backward
+        pl.off_den = off;
+        off += den_bytes;
+    }
+    if (tc) {   // and a record of what it was run on
+        pl.off_hdr = off;
+        off += 256;
     }
     pl.ws_bytes = off;
     return pl;
@@ -136,18 +146,27 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     p.P = pl.P; p.phi = phi; p.causal = causal ? 1 : 0; p.eps = eps;
     p.chunk = pl.chunk; p.seg_len = pl.seg_len; p.nseg = pl.nseg;
     char *base = static_cast<char *>(ws);
+    const bool tc = pl.path == LA_PATH_TCGEN05;
     p.state = reinterpret_cast<float *>(base + pl.off_state);
     p.rstate = bwd ? reinterpret_cast<float *>(base + pl.off_rstate) : nullptr;
-    p.den = bwd ? reinterpret_cast<float *>(base + pl.off_den) : nullptr;
+    p.den = (bwd || tc) ? reinterpret_cast<float *>(base + pl.off_den) : nullptr;
+    p.den_stride = tc ? tc_den_stride(N) : N;
+    p.hdr = tc ? reinterpret_cast<int *>(base + pl.off_hdr) : nullptr;
     p.gd = bwd ? reinterpret_cast<float *>(base + pl.off_gd) : nullptr;
     p.phis = bwd && pl.off_phis ? static_cast<void *>(base + pl.off_phis) : nullptr;
     if (bwd && fwd_ws) {
-        // the forward's workspace holds its scanned segment states; they are the backward's
-        // when both plans cut the sequence the same way
+        // the forward's workspace holds its scanned segment states (and, on the tensor-core
+        // path, its per-row dens and its record); they are the backward's when both plans cut
+        // the sequence the same way
         const Plan pf = make_plan(B, Hq, Hkv, N, D, dt, causal, cw != nullptr, 0);
         if (pf.path == pl.path && pf.chunk == pl.chunk && pf.seg_len == pl.seg_len && pf.nseg == pl.nseg &&
             pf.P == pl.P && pf.state_elems == pl.state_elems && fwd_ws_bytes >= pf.ws_bytes && aligned(fwd_ws, 256)) {
-            p.state = reinterpret_cast<float *>(const_cast<char *>(static_cast<const char *>(fwd_ws)) + pf.off_state);
+            char *f = const_cast<char *>(static_cast<const char *>(fwd_ws));
+            p.state = reinterpret_cast<float *>(f + pf.off_state);
+            if (tc) {
+                p.den = reinterpret_cast<float *>(f + pf.off_den);
+                p.hdr = reinterpret_cast<int *>(f + pf.off_hdr);
+            }
             p.state_given = 1;
         }
     }
@@ -256,7 +275,7 @@ la_status la_get_status(void *stream) {
         const int zero = 0;
         e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
         if (e != cudaSuccess) return cuda_fail(e);
-        return LA_ERR_TIMEOUT;
+        return word == kErrStaleWorkspace ? LA_ERR_WORKSPACE : LA_ERR_TIMEOUT;
     }
     return LA_OK;
 }

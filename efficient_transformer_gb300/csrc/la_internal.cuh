@@ -20,6 +20,12 @@ constexpr int kPlanSms = 152;
 // Device error word values (latched by kernels, read by la_get_status).
 constexpr int kErrNone = 0;
 constexpr int kErrTimeout = 1;
+constexpr int kErrStaleWorkspace = 2;   // la_bwd_from_fwd got a workspace another call wrote
+
+// Words of the record that the tensor-core forward leaves in its workspace (what it was run
+// on), checked by the backward kernels when they take the forward's states and dens.
+constexpr int kHdrWords = 16;
+constexpr int kHdrMagic = 0x4c414631;
 
 // Everything a kernel needs.  Tensor pointers are typed void: the element type is a
 // template parameter of each kernel.
@@ -33,7 +39,13 @@ struct Params {
     float *state;                // per (b, kv head, segment) forward state partials
     int state_given;             // backward: `state` already holds the scanned forward states
     float *rstate;               // per (b, kv head, segment) backward state partials
-    float *den;                  // [B, Hq, N] row denominators (backward)
+    float *den;                  // [B, Hq, N] row denominators incl. eps: written by the tensor-core
+                                 // forward and read by the tensor-core dq kernel; written and read by
+                                 // the CUDA-core backward kernels
+    int den_stride;              // floats between the den rows of consecutive heads (N, or N rounded
+                                 // up to 32 on the tensor-core path, for 16-byte TMA strides)
+    int *hdr;                    // tensor-core forward: its record (kHdrWords); backward: the record
+                                 // to check (null: nothing to check)
     float *gd;                   // [B, Hq, N] per-row denominator terms (backward; see each kernel)
     void *phis;                  // [B, Hq, N, D] bf16 phi(q) / den, written by the tensor-core dq
                                  // kernel for the dk/dv kernel (causal tensor-core backward; else null)
@@ -48,9 +60,12 @@ struct Plan {
     int seg_len;      // tokens per segment (a multiple of chunk)
     int nseg;         // segments per (batch, kv head)
     size_t state_elems;   // floats of one segment state (all terms)
-    size_t off_state, off_rstate, off_den, off_gd, off_phis;   // workspace byte offsets
+    size_t off_state, off_rstate, off_den, off_gd, off_phis, off_hdr;   // workspace byte offsets
     size_t ws_bytes;
 };
+
+// Row stride of the per-row den array on the tensor-core path (16-byte aligned rows).
+inline int tc_den_stride(int N) { return (N + 31) / 32 * 32; }
 
 // --- device helpers --------------------------------------------------------------------
 

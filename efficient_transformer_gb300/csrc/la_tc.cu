@@ -18,7 +18,8 @@
 //   conv  P   = bf16(A masked j <= i)                                      (causal)
 //   MMA2  O   = phi(Q) S_bf + P V                              [128 x D]
 //         den = phi(Q) z_bf + P 1        (column D of O)       [128 x 16]
-//   epi   out = O / (den + eps)  -> staged in shared memory -> TMA store
+//   epi   out = O / (den + eps)  -> staged in shared memory -> TMA store; den + eps per row
+//         to the workspace (the backward's dq kernel reads it)
 //   MMA3  S  += phi(K)^T V,  z += phi(K)^T 1                              (causal)
 //   conv  S_bf, z_bf = bf16(S, z) for the next chunk
 // Warp roles (640 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
@@ -252,6 +253,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
     const int bh0 = b * p.Hq + g * G;
     const float *state = p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
 
+    // the record of this call, checked by a backward that takes this workspace's states and dens
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.hdr) {
+        const int rec[kHdrWords] = {kHdrMagic, p.B, p.Hq, p.Hkv, p.N, p.D, p.causal, p.phi, p.P,
+                                    __float_as_int(p.eps), p.nseg, p.chunk,
+                                    (int)reinterpret_cast<uintptr_t>(p.q), (int)(reinterpret_cast<uintptr_t>(p.q) >> 32),
+                                    (int)reinterpret_cast<uintptr_t>(p.k), (int)reinterpret_cast<uintptr_t>(p.v)};
+        for (int w = 0; w < kHdrWords; ++w) p.hdr[w] = rec[w];
+    }
     // constant tiles: ones (row 0 = 1 over C columns) and the zero rows of the z tile
     fill_ones_tile(ones, C);
     for (int idx = threadIdx.x; idx < K::Z_BYTES / 16; idx += blockDim.x)
@@ -548,6 +557,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 tmem_wait_regs<1>(&den);
             }
             const float inv = 1.f / (den + p.eps);
+            if (ok && p.den && c0 + i % C < t1)
+                p.den[(size_t)(bh0 + i / C) * p.den_stride + c0 + i % C] = den + p.eps;
 #pragma unroll 1
             for (int c64 = 0; c64 < D / 64; ++c64) {
                 float v[32];   // 32 columns at a time

@@ -7,20 +7,22 @@
 // suffix state R = sum_{i after} phi(q_i) gn_i^T, r = sum gd_i phi(q_i) carries the rows
 // that come later.  Launch order:
 //
-//   k_tc_state -> scan (prefix S)   (skipped when the forward's states are given)
-//   k_tc_bwd_dq   forward over chunks: dq, per-row den and h, each segment's R and r,
-//                 and (causal) the rows phi_s = phi(q) / den for the next kernel
+//   (the forward: k_tc_state -> scan -> k_tc_fwd, with dq as its output scratch; skipped
+//    when the caller's forward workspace gives the states and the per-row den)
+//   k_tc_bwd_dq   forward over chunks: dq, per-row h, each segment's R and r, and (causal)
+//                 the rows phi_s = phi(q) / den for the next kernel
 //   scan (suffix R)
 //   k_tc_bwd_dkdv reverse over chunks: dk, dv (summed over the n_rep heads of the group),
 //                 reading phi_s where the dq kernel read q
 //
-// Per chunk of k_tc_bwd_dq (128 stacked query rows, C keys), with the raw grad_out g:
-//   A = phi(Q) phi(K)^T,  dA' = g V^T,  X = g S_bf^T,  den = phi(Q) z + rowsum mask(A) + eps
-//   g . num = phi(q) . X + sum_j mask(A) dA'      (no O product is needed)
+// Per chunk of k_tc_bwd_dq (128 stacked query rows, C keys), with the raw grad_out g and
+// the forward's den (incl. eps) per row:
+//   phi_s = phi(q) / den (bf16, the feature map scales Q's rows in place)
+//   A_s = phi_s phi(K)^T,  dA' = g V^T,  X = g S_bf^T,  R += phi_s^T g (= phi(Q)^T gn)
+//   g . num / den = phi_s . X + sum_j mask(A_s) dA'      (no O product is needed)
 //   h = -(g . num) / den,  gd = h / den,  dP' = mask(dA' + h) = den * dP
-//   phi_s = phi(q) / den (bf16, in place over phi(Q))
-//   X += dP' phi(K),  den * da = X + h z (fp32),  dq = phi'(q) / den * (X + h z)
-//   R += phi_s^T g (= phi(Q)^T gn),  r += phi_s^T h (= phi(Q)^T gd),  S += phi(K)^T V
+//   X += dP' phi(K) + h z = den * da,  dq = phi'(q) / den * X
+//   r += phi_s^T h (= phi(Q)^T gd),  S += phi(K)^T V
 // Per chunk of k_tc_bwd_dkdv, computed transposed so the 128 query rows stay on the MMA's
 // K dimension (and the sum over the group's heads comes for free):
 //   dk^T = phi(Q)^T dP + R_bf V^T (+ r),  dv^T = gn^T P + R_bf^T phi(K)^T,  R += phi(Q)^T gn
@@ -54,10 +56,17 @@ struct BwdCfg {
     static constexpr int ONES_BYTES = CB * 16 * 128;        // ones: 16 rows x C columns
     static constexpr int H_BYTES = 2 * 16 * 128;            // h: 16 rows x 128 query rows (rows 0-2: hi, hi, lo)
     static constexpr int XCH_BYTES = 2 * 128 * 4;           // partial row dots of the two pool halves
-    // dq kernel: stages, dP', S_bf, two z slots, ones, h, exchange
+    // dq kernel: stages (with the rows' den: 128 floats, padded to keep the stages 1024-byte
+    // aligned), dP', S_bf, two z slots, ones, h, exchange
+    static constexpr int DEN_BYTES = 1024;
+    // each head's C dens land at a 128-byte aligned slot of DPAD floats (a TMA destination in
+    // shared memory must be 128-byte aligned): row i = r C + ti sits at r DPAD + ti
+    static constexpr int DPAD = C < 32 ? 32 : C;
+    static_assert(G * DPAD * 4 <= DEN_BYTES, "den slots");
+    static constexpr int STAGE_DQ = STAGE + DEN_BYTES;   // [phi_s | phi(K) | V | g | den]
     static constexpr int DQ_FIXED = P_BYTES + S_BYTES + 2 * Z_BYTES + ONES_BYTES + H_BYTES + XCH_BYTES + 1024;
-    static constexpr int NS_DQ = 3 * STAGE + DQ_FIXED <= kSmemLimit - 512 ? 3 : 2;
-    static constexpr int DQ_SMEM = NS_DQ * STAGE + DQ_FIXED;
+    static constexpr int NS_DQ = 3 * STAGE_DQ + DQ_FIXED <= kSmemLimit - 512 ? 3 : 2;
+    static constexpr int DQ_SMEM = NS_DQ * STAGE_DQ + DQ_FIXED;
     // dk/dv kernel: stages, P', dP', R_bf, h (a 16 x 128 tile unless it fits as two spare
     // columns of dP' next to the C keys)
     static constexpr bool H_IN_DP = C % 64 != 0 && C % 64 + 16 <= 64;
@@ -82,10 +91,9 @@ struct BwdCfg {
     static constexpr int NB_KV = KT_AD + 2 * KV_BW <= 512 ? 2 : 1;
     // phi_s^T h rides on the dk^T product as 16 extra columns of dP' (h in dP')
     static constexpr bool MERGE_H = KV_SEP && H_IN_DP;
-    // dq kernel TMEM columns: [S | z], den, A, dA', X (then den * da - h z), [R | r]
+    // dq kernel TMEM columns: [S | z], (16 free), A_s, dA', X (then den * da), [R | r]
     static constexpr int T_S = 0;
-    static constexpr int T_DEN = D + 16;
-    static constexpr int T_A = T_DEN + 16;
+    static constexpr int T_A = D + 32;
     static constexpr int T_A2 = T_A + C;
     static constexpr int T_X = T_A2 + C;
     static constexpr int T_R = T_X + D;
@@ -144,13 +152,17 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                                                               const __grid_constant__ CUtensorMap map_v,
                                                               const __grid_constant__ CUtensorMap map_g,
                                                               const __grid_constant__ CUtensorMap map_dq,
-                                                              const __grid_constant__ CUtensorMap map_ps, Params p) {
+                                                              const __grid_constant__ CUtensorMap map_ps,
+                                                              const __grid_constant__ CUtensorMap map_den, Params p) {
     using K = BwdCfg<D, G>;
-    constexpr int C = K::C, NS = K::NS_DQ;
+    constexpr int C = K::C, NS = K::NS_DQ, STAGE = K::STAGE_DQ;
     constexpr int OFF_K = K::Q_BYTES, OFF_V = OFF_K + K::K_BYTES, OFF_G = OFF_V + K::V_BYTES;
+    constexpr int OFF_DEN = OFF_G + K::G_BYTES;   // den + eps of the 128 rows (fp32)
     constexpr int HALF = D / 2;   // feature columns per pool half
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_fulla[NS], bar_fullg[NS], bar_ready[NS], bar_empty[NS], bar_dqready[NS][2];
+    // rdone is per stage: the store warp waits for chunk k's r product, and a single barrier could
+    // run two phases ahead of it (the next chunk's product may finish first)
+    __shared__ uint64_t bar_fulla[NS], bar_fullg[NS], bar_ready[NS], bar_empty[NS], bar_dqready[NS][2], bar_rdone[NS];
     __shared__ uint64_t bar_mfull, bar_sfull, bar_gnready, bar_dqfull, bar_xfree, bar_sbf, bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -158,12 +170,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     const uint32_t sm_lo = smem_u32(smem_raw), sm_hi = sm_lo + K::DQ_SMEM;
     (void)sm_lo;
     (void)sm_hi;
-    uint8_t *pbuf = stage0 + NS * K::STAGE;       // dP' (query rows x keys)
+    uint8_t *pbuf = stage0 + NS * STAGE;         // dP' (query rows x keys)
     uint8_t *sbf = pbuf + K::P_BYTES;            // S_bf [D][D]
     // z and h enter the products as two-term bf16 splits (v = v_hi + v_lo): the z tile holds
     // rows (z_hi, z_lo, z_hi) and the h tile rows (h_hi, h_hi, h_lo), so that one K = 16
-    // product gives h_hi z_hi + h_hi z_lo + h_lo z_hi, and phi(q) . z comes out as two
-    // columns (z_hi, z_lo) that are added in fp32
+    // product gives h_hi z_hi + h_hi z_lo + h_lo z_hi
     uint8_t *ztile = sbf + K::S_BYTES;           // two slots of 16 x D
     uint8_t *ones = ztile + 2 * K::Z_BYTES;      // 16 x C, row 0 = 1
     uint8_t *htile = ones + K::ONES_BYTES;       // 16 x 128 (query rows)
@@ -194,6 +205,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             mbar_init(&bar_empty[s], 1);
             mbar_init(&bar_dqready[s][0], 128);
             mbar_init(&bar_dqready[s][1], 128);
+            mbar_init(&bar_rdone[s], 1);
         }
         mbar_init(&bar_mfull, 1);
         mbar_init(&bar_sfull, 1);
@@ -203,6 +215,18 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         mbar_init(&bar_sbf, 256);
         mbar_init(&bar_fin, 1);
         fence_barrier_init();
+        // the forward's record of what it was run on: a workspace that another call wrote is
+        // reported through the device error word (la_get_status: LA_ERR_WORKSPACE)
+        if (blockIdx.x == 0 && p.hdr) {
+            const int want[kHdrWords] = {kHdrMagic, p.B, p.Hq, p.Hkv, p.N, p.D, p.causal, p.phi, p.P,
+                                         __float_as_int(p.eps), p.nseg, p.chunk,
+                                         (int)reinterpret_cast<uintptr_t>(p.q),
+                                         (int)(reinterpret_cast<uintptr_t>(p.q) >> 32),
+                                         (int)reinterpret_cast<uintptr_t>(p.k), (int)reinterpret_cast<uintptr_t>(p.v)};
+            bool same = true;
+            for (int w = 0; w < kHdrWords; ++w) same = same && p.hdr[w] == want[w];
+            if (!same) atomicExch(p.err, kErrStaleWorkspace);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&tmem_base, 512);
@@ -211,22 +235,22 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = tmem_base + K::T_S, tDen = tmem_base + K::T_DEN, tA = tmem_base + K::T_A,
-                   tA2 = tmem_base + K::T_A2, tX = tmem_base + K::T_X, tR = tmem_base + K::T_R;
+    const uint32_t tS = tmem_base + K::T_S, tA = tmem_base + K::T_A, tA2 = tmem_base + K::T_A2,
+                   tX = tmem_base + K::T_X, tR = tmem_base + K::T_R;
 
     if (warp == 0) {
-        // ---------------- TMA producer: K and Q (what the feature map needs) on one barrier,
-        // V and grad_out on another
+        // ---------------- TMA producer: K, Q, V and the rows' den (what the feature map and the
+        // first products need) on one barrier, grad_out on another
         {   // the whole warp, one lane issuing
-            constexpr uint32_t bytes_a = CAUSAL ? K::Q_BYTES + K::K_BYTES : K::Q_BYTES;
-            constexpr uint32_t bytes_g = CAUSAL ? K::V_BYTES + K::G_BYTES : K::G_BYTES;
+            constexpr uint32_t bytes_a = (CAUSAL ? K::Q_BYTES + K::K_BYTES + K::V_BYTES : K::Q_BYTES) + G * C * 4;
+            constexpr uint32_t bytes_g = K::G_BYTES;
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 if (k >= NS && !warp_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
-                uint8_t *st = stage0 + s * K::STAGE;
+                uint8_t *st = stage0 + s * STAGE;
                 const int c0 = t0 + k * C;
-                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N && bh0 + G <= p.B * p.Hq, 301,
+                if (!LA_CHECK(in_smem(st, STAGE, sm_lo, sm_hi) && c0 < p.N && bh0 + G <= p.B * p.Hq, 301,
                               smem_u32(st) - sm_lo, c0))
                     break;
                 LA_TL(k, 0);
@@ -234,17 +258,19 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d_w(st + OFF_K + blk * C * 128, &map_k, &bar_fulla[s], blk * 64, c0, bg);
-                for (int r = 0; r < G; ++r)
+                for (int r = 0; r < G; ++r) {
+                    tma_load_2d_w(st + OFF_DEN + r * K::DPAD * 4, &map_den, &bar_fulla[s], c0, bh0 + r);
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fulla[s], blk * 64, c0, bh0 + r);
-                mbar_arrive_expect_tx_w(&bar_fullg[s], bytes_g);
+                }
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fullg[s], blk * 64, c0, bg);
+                        tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fulla[s], blk * 64, c0, bg);
+                mbar_arrive_expect_tx_w(&bar_fullg[s], bytes_g);
                 for (int r = 0; r < G; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64, c0,
-                                    bh0 + r);
+                                      bh0 + r);
                 issued = k + 1;
             }
             for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) {
@@ -253,15 +279,14 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer.  Iteration k finishes chunk k - 1 (da, R, r) and
-        // starts chunk k (A, den, X, dA', then the state update).  Products that share an
-        // A operand are issued back to back so that A is read from shared memory once.
+        // ---------------- MMA issuer.  Iteration k finishes chunk k - 1 (X += dP' phi(K) + h z,
+        // then r) and starts chunk k (A_s, X, dA', then R and the state update).  Products that
+        // share an A operand are issued back to back so that A is read from shared memory once.
         {   // the whole warp, one lane issuing
             constexpr uint32_t idA = idesc_bf16(128, C, false, false);
             constexpr uint32_t idX = idesc_bf16(128, D, false, false);
             constexpr uint32_t idDK = idesc_bf16(128, D, false, true);
             constexpr uint32_t idHZ = idesc_bf16(128, D, true, true);
-            constexpr uint32_t id16 = idesc_bf16(128, 16, false, false);
             constexpr uint32_t idR = idesc_bf16(128, D, true, true);
             constexpr uint32_t idR16 = idesc_bf16(128, 16, true, false);
             const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf), on = smem_u32(ones), ht = smem_u32(htile);
@@ -271,21 +296,19 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     if (!warp_wait(&bar_gnready, kp & 1, &abort_flag)) break;
                     LA_TL(kp, 5);
                     tc_fence_after();
-                    const uint32_t qs = smem_u32(stage0 + sp * K::STAGE), ks_ = qs + OFF_K, gs = qs + OFF_G;
+                    const uint32_t qs = smem_u32(stage0 + sp * STAGE), ks_ = qs + OFF_K;
                     // X += dP' phi(K) + h z^T   (X becomes den * da)
                     const uint32_t zt = smem_u32(ztile + (CAUSAL ? (kp & 1) : 0) * K::Z_BYTES);
                     if (CAUSAL)
                         for (int kk = 0; kk < C / 16; ++kk)
                             mma_bf16_w(tX, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(ks_, C, 0, kk), idDK, 1u);
                     mma_bf16_w(tX, desc_mnmajor(ht, 16, 0, 0), desc_mnmajor(zt, 16, 0, 0), idHZ, 1u);
-                    // R += phi_s^T g, r += phi_s^T h  (phi_s = phi(Q) / den)
-                    for (int kk = 0; kk < 128 / 16; ++kk) {
-                        const uint32_t acc = (kp > 0 || kk > 0) ? 1u : 0u;
-                        const uint64_t as = desc_mnmajor(qs, 128, 0, kk);
-                        mma_bf16_fill_w(tR, as, desc_mnmajor(gs, 128, 0, kk), idR, acc);
-                        mma_bf16_lastuse_w(tR + D, as, desc_kmajor(ht, 16, 0, kk), idR16, acc);
-                    }
                     mma_commit_w(&bar_dqfull);
+                    // r += phi_s^T h  (phi_s = phi(Q) / den)
+                    for (int kk = 0; kk < 128 / 16; ++kk)
+                        mma_bf16_w(tR + D, desc_mnmajor(qs, 128, 0, kk), desc_kmajor(ht, 16, 0, kk), idR16,
+                                   (kp > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_w(&bar_rdone[sp]);
                 }
                 if (k == nchunk) break;
                 const int s = k % NS;
@@ -294,20 +317,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 if ((CAUSAL || k == 0) && !warp_wait(&bar_sbf, k & 1, &abort_flag)) break;
                 LA_TL(k, 3);
                 tc_fence_after();
-                const uint32_t qs = smem_u32(stage0 + s * K::STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V, gs = qs + OFF_G;
-                const uint32_t zt = smem_u32(ztile + (CAUSAL ? (k & 1) : 0) * K::Z_BYTES);
-                if (!LA_CHECK(qs >= sm_lo && qs + K::STAGE <= sm_hi && ht + K::H_BYTES <= sm_hi, 311, qs - sm_lo, k))
+                const uint32_t qs = smem_u32(stage0 + s * STAGE), ks_ = qs + OFF_K, vs = qs + OFF_V, gs = qs + OFF_G;
+                if (!LA_CHECK(qs >= sm_lo && qs + STAGE <= sm_hi && ht + K::H_BYTES <= sm_hi, 311, qs - sm_lo, k))
                     break;
-                // A = phi(Q) phi(K)^T and den = phi(Q) z share phi(Q)
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t aq = desc_kmajor(qs, 128, 0, kk);
-                    if (CAUSAL) {
-                        mma_bf16_fill_w(tA, aq, desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
-                        mma_bf16_lastuse_w(tDen, aq, desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
-                    } else {
-                        mma_bf16_w(tDen, aq, desc_kmajor(zt, 16, 0, kk), id16, kk > 0 ? 1u : 0u);
-                    }
-                }
+                // A_s = phi_s phi(K)^T
+                if (CAUSAL)
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_w(tA, desc_kmajor(qs, 128, 0, kk), desc_kmajor(ks_, C, 0, kk), idA, kk > 0 ? 1u : 0u);
                 if (k > 0 && !warp_wait(&bar_xfree, (k - 1) & 1, &abort_flag)) break;
                 LA_TL(k, 4);
                 tc_fence_after();
@@ -322,7 +338,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     }
                 }
                 mma_commit_w(&bar_mfull);
-                if (CAUSAL) {   // S += phi(K)^T V, z += phi(K)^T 1 (one read of phi(K))
+                if (CAUSAL) {   // S += phi(K)^T V, z += phi(K)^T 1 (one read of phi(K)), after X has
+                                // read S_bf; the state conversion for the next chunk waits for it
                     for (int kk = 0; kk < C / 16; ++kk) {
                         const uint64_t ak = desc_mnmajor(ks_, C, 0, kk);
                         mma_bf16_fill_w(tS, ak, desc_mnmajor(vs, C, 0, kk), idR, 1u);
@@ -330,24 +347,29 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     }
                     mma_commit_w(&bar_sfull);
                 }
+                // R += phi_s^T g (= phi(Q)^T gn); done before this chunk's dqfull, after which the
+                // dq epilogue writes over the g tile
+                for (int kk = 0; kk < 128 / 16; ++kk)
+                    mma_bf16_w(tR, desc_mnmajor(qs, 128, 0, kk), desc_mnmajor(gs, 128, 0, kk), idR,
+                               (k > 0 || kk > 0) ? 1u : 0u);
                 LA_TL(k, 6);
             }
             mma_commit_w(&bar_fin);
             warp_drain(&bar_fin, 0);
         }
     } else if (warp == 2) {
-        // ---------------- stores.  Causal: once the row pass has left phi_s = phi(q) / den in
-        // the Q tile, TMA copies it to the workspace for the dk/dv kernel.  Then each pool
-        // half leaves its D/2 columns of dq over the g tile; TMA writes them out, and the
-        // stage is released once all the copies have read it
+        // ---------------- stores.  Causal: phi_s = phi(q) / den, left in the Q tile by the
+        // feature map, goes to the workspace for the dk/dv kernel.  Then each pool half leaves
+        // its D/2 columns of dq over the g tile; TMA writes them out, and the stage is released
+        // once the copies have read it and the chunk's last products (r) are done
         {   // the whole warp, one lane issuing
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
-                uint8_t *st = stage0 + s * K::STAGE;
+                uint8_t *st = stage0 + s * STAGE;
                 const int c0 = t0 + k * C;
                 bool ok = true;
                 if (CAUSAL) {
-                    ok = warp_wait(&bar_gnready, k & 1, &abort_flag);
+                    ok = warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag);
                     if (ok) {
                         for (int r = 0; r < G; ++r)
                             for (int blk = 0; blk < K::DB; ++blk)
@@ -372,14 +394,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     bulk_wait_read();
                     LA_TL(k, 14);
                 }
+                ok = ok && warp_wait(&bar_rdone[s], (k / NS) & 1, &abort_flag);
                 mbar_arrive_w(&bar_empty[s]);
                 if (!ok) break;
             }
             bulk_wait_all();
         }
     } else if ((warp >= 4 && warp < 8) || warp >= 16) {
-        // ---------------- phi prologue, in place on phi(Q) and phi(K): both warpgroups share
-        // every chunk (16-byte pieces dealt round-robin)
+        // ---------------- phi prologue, in place: phi_s = phi(q) / den on the Q tile (den from
+        // the forward, in the stage) and phi(k) on the K tile; both warpgroups share every chunk
+        // (16-byte pieces dealt round-robin)
         const int pi = warp >= 16 ? threadIdx.x - 384 : threadIdx.x - 128;   // 0 .. kDqPro - 1
         // thread pi owns 16-byte column piece c of rows r0, r0 + RPP, ...; RPP is a multiple
         // of 8, so the piece's swizzled position is the same in all of them
@@ -394,7 +418,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             ok = ok && warp_wait(&bar_fulla[s], (k / NS) & 1, &abort_flag);
             if (pi == 0) LA_TL(k, 1);
             if (ok) {
-                uint8_t *st = stage0 + s * K::STAGE;
+                uint8_t *st = stage0 + s * STAGE;
+                const float *dent = reinterpret_cast<const float *>(st + OFF_DEN);
                 const int c0 = t0 + k * C;
                 const int nvalid = t1 - c0;   // tokens of this chunk inside the segment
                 constexpr int NQ = (128 + RPP - 1) / RPP, NK = CAUSAL ? (C + RPP - 1) / RPP : 0;
@@ -414,7 +439,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     pres[NQ + n] = j < C && LA_CHECK(in_smem(pp[NQ + n], 16, sm_lo, sm_hi), 322, smem_u32(pp[NQ + n]) - sm_lo, j);
                     val[NQ + n] = j < nvalid;
                 }
-                feat8_batch<NQ + NK, false>(pp, pres, val, p.phi, nullptr);
+                // the Q pieces' rows r0 + n RPP, each divided by its den
+                feat8_batch_rowscale<NQ + NK, C, K::DPAD>(pp, pres, val, p.phi, dent, r0, RPP, NQ);
                 fence_proxy_async();
             }
             if (pi == 0) LA_TL(k, 2);
@@ -450,7 +476,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         }
     } else if (warp >= 8 && warp < 16) {
         // ---------------- row pool: two warpgroups, thread = query row i (TMEM lane), each
-        // half owning D/2 feature columns.  Per chunk: row work, dq.
+        // half owning D/2 feature columns and every second 16-key piece of the chunk.  Per
+        // chunk: row work (g . num / den, h, dP'), then dq.
         const int h = (warp - 8) / 4;
         const int wq = warp % 4;
         const int i = wq * 32 + lane;
@@ -486,79 +513,58 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             const int s = k % NS;
             const int t = t0 + k * C + ti;
             const bool valid = t < t1;
-            uint8_t *st = stage0 + s * K::STAGE;
-            // ---- row work: den, phi_s = phi(q) / den in place, g . num, h, dP'
+            uint8_t *st = stage0 + s * STAGE;
+            // ---- row work: with phi_s = phi(q) / den and A_s = phi_s phi(K)^T,
+            // g . num / den = phi_s . X + sum_j mask(A_s) dA';  h = -(g . num) / den;
+            // dP' = mask(dA' + h)
             ok = ok && warp_wait(&bar_mfull, k & 1, &abort_flag);
             tc_fence_after();
             if (i == 0 && h == 0) LA_TL(k, 7);
-            float inv = 0.f, hval = 0.f, den = 1.f;
+            float hval = 0.f, inv = 0.f;
             if (ok) {
-                float dz[2];   // phi(q) . z_hi, phi(q) . z_lo
-                tmem_ld2(tDen + lane_off, dz);
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};   // g . num partials
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 if (CAUSAL) {
-                    float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                     for (int c16 = 0; c16 < C / 16; ++c16) {
+                        if ((c16 & 1) != h) continue;
                         float va[16], vd[16];
                         tmem_ld16(tA + lane_off + c16 * 16, va);
-                        if (h == 0) tmem_ld16(tA2 + lane_off + c16 * 16, vd);
+                        tmem_ld16(tA2 + lane_off + c16 * 16, vd);
                         tmem_wait_regs<16>(va);
-                        if (h == 0) {
-                            tmem_wait_regs<16>(vd);
+                        tmem_wait_regs<16>(vd);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const float a = (c16 * 16 + e <= ti) ? va[e] : 0.f;
-                                rs[e & 3] += a;
-                                acc[e & 3] = fmaf(a, vd[e], acc[e & 3]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) rs[e & 3] += (c16 * 16 + e <= ti) ? va[e] : 0.f;
-                        }
+                        for (int e = 0; e < 16; ++e)
+                            if (c16 * 16 + e <= ti) acc[e & 3] = fmaf(va[e], vd[e], acc[e & 3]);
                     }
-                    tmem_wait_regs<2>(dz);
-                    den = (dz[0] + dz[1]) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-                } else {
-                    tmem_wait_regs<2>(dz);
-                    den = dz[0] + dz[1];
                 }
-                den += p.eps;
-                inv = 1.f / den;
-                // X in 16-column pieces
+                // phi_s . X over this half's feature columns, 16 at a time
 #pragma unroll 1
                 for (int c16 = 0; c16 < HALF / 16; ++c16) {
                     const int col0 = h * HALF + c16 * 16;
                     float xv[16];
                     tmem_ld16(tX + lane_off + col0, xv);
-                    tmem_wait_regs<16>(xv);
-                    uint8_t *ch[2];
                     uint4 u[2];
 #pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8) {   // both loads before either store
-                        ch[q8] = st + swz_chunk(128, i, col0 / 8 + q8);
-                        u[q8] = *reinterpret_cast<const uint4 *>(ch[q8]);
-                    }
+                    for (int q8 = 0; q8 < 2; ++q8) u[q8] = *reinterpret_cast<const uint4 *>(st + swz_chunk(128, i, col0 / 8 + q8));
+                    tmem_wait_regs<16>(xv);
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8) {
-                        uint32_t *ui = reinterpret_cast<uint32_t *>(&u[q8]);
+                        const uint32_t *ui = reinterpret_cast<const uint32_t *>(&u[q8]);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float2 f = unpack_bf16x2(ui[q]);
                             acc[q] = fmaf(f.x, xv[q8 * 8 + 2 * q], acc[q]);
                             acc[q] = fmaf(f.y, xv[q8 * 8 + 2 * q + 1], acc[q]);
-                            ui[q] = pack_bf16x2(f.x * inv, f.y * inv);
                         }
-                        if (LA_CHECK(in_smem(ch[q8], 16, sm_lo, sm_hi), 331, smem_u32(ch[q8]) - sm_lo, col0))
-                            *reinterpret_cast<uint4 *>(ch[q8]) = u[q8];
                     }
                 }
                 xch[h * 128 + i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                inv = 1.f / reinterpret_cast<const float *>(st + OFF_DEN)[r * K::DPAD + ti];
             }
             named_barrier(3, 256);
             if (ok) {
-                const float gdot = xch[i] + xch[128 + i];
-                hval = valid ? -gdot * inv : 0.f;
+                const float gnum = xch[i] + xch[128 + i];   // g . num / den
+                hval = valid ? -gnum : 0.f;
                 if (CAUSAL)
                     for (int c16 = h; c16 < C / 16; c16 += 2) {
                         float vd[16];
@@ -583,19 +589,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 0, i)) = hh;
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 1, i)) = hh;
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 2, i)) = hl;
-                    if (valid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 334, bh, t)) {
-                        p.den[(size_t)bh * p.N + t] = den;
+                    if (valid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 334, bh, t))
                         p.gd[(size_t)bh * p.N + t] = hval;   // h = den * gd for the dk/dv kernel
-                    }
                 }
                 fence_proxy_async();
             }
             tc_fence_before();
             if (i == 0 && h == 0) LA_TL(k, 8);
             mbar_arrive_warp(&bar_gnready);
-            // ---- dq = phi'(q) / den * (den da), written over the g tile (dead once the chunk's
-            // products are done, which dqfull says) for the TMA store; phi_s stays in place for
-            // its own copy to the workspace
+            // ---- dq = phi'(q) / den * (den da), written over the g tile (its last reader, the R
+            // product, is done before dqfull) for the TMA store
             ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
             tc_fence_after();
             if (i == 0 && h == 0) LA_TL(k, 11);
@@ -603,15 +606,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             for (int c16 = 0; c16 < HALF / 16; ++c16) {
                 const int col0 = h * HALF + c16 * 16;
                 float xv[16];
-                if (ok) {
-                    tmem_ld16(tX + lane_off + col0, xv);
-                    tmem_wait_regs<16>(xv);
-                }
-                if (c16 + 1 == HALF / 16) {   // every column of X is in registers
-                    tc_fence_before();
-                    mbar_arrive_warp(&bar_xfree);
-                }
-                if (!ok) continue;
+                if (ok) tmem_ld16(tX + lane_off + col0, xv);
                 uint8_t *ch[2];
                 uint4 u[2];
 #pragma unroll
@@ -619,6 +614,12 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     ch[q8] = st + swz_chunk(128, i, col0 / 8 + q8);
                     u[q8] = *reinterpret_cast<const uint4 *>(ch[q8]);
                 }
+                if (ok) tmem_wait_regs<16>(xv);
+                if (c16 + 1 == HALF / 16) {   // every column of X is in registers
+                    tc_fence_before();
+                    mbar_arrive_warp(&bar_xfree);
+                }
+                if (!ok) continue;
 #pragma unroll
                 for (int q8 = 0; q8 < 2; ++q8)
                     if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 341, smem_u32(ch[q8]) - sm_lo, q8))
@@ -1235,8 +1236,9 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
 template <int D, int G, bool CAUSAL>
 cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     using K = BwdCfg<D, G>;
-    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{}, mps{};
+    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{}, mps{}, mden{};
     cudaError_t e = make_map(&mq, p.q, p.B * p.Hq, p.N, D, K::C);
+    if (e == cudaSuccess) e = make_map_rows_f32(&mden, p.den, p.B * p.Hq, p.N, p.den_stride, K::C);
     // phi(q) / den rows: written by the dq kernel, read by the dk/dv kernel in place of q
     if (e == cudaSuccess) e = make_map(&mps, CAUSAL ? p.phis : p.q, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
@@ -1251,7 +1253,7 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
     {
         TraceScope ts(CAUSAL ? "tc_bwd_dq_causal" : "tc_bwd_dq_bidir", s);
-        k_tc_bwd_dq<D, G, CAUSAL><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, mps, p);
+        k_tc_bwd_dq<D, G, CAUSAL><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, mps, mden, p);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess)
@@ -1268,9 +1270,11 @@ cudaError_t backward_dg(const Params &p, cudaStream_t s) {
         return cudaErrorNotSupported;
     } else {
         if (!p.state_given) {
-            cudaError_t e = tc_launch_state(p, s);
-            if (e == cudaSuccess)
-                e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, (size_t)D * (D + 1), s);
+            // the forward gives the segment states, the per-row den and the record; its output
+            // goes to dq, which the dq kernel overwrites
+            Params pf = p;
+            pf.out = p.dq;
+            cudaError_t e = tc_forward(pf, s);
             if (e != cudaSuccess) return e;
         }
         return p.causal ? launch_bwd_kernels<D, G, true>(p, s) : launch_bwd_kernels<D, G, false>(p, s);

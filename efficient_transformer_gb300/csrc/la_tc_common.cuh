@@ -186,6 +186,39 @@ __device__ __forceinline__ void feat8_batch(uint8_t *const *ptr, const bool *pre
         if (present[n]) *reinterpret_cast<uint4 *>(ptr[n]) = x[n];
 }
 
+// phi on up to NB 16-byte pieces in place, as feat8_batch; the first NSCALED of them (rows
+// r0, r0 + step, ... of a stacked tile whose row r C + ti has its den at den_tile[r DPAD + ti])
+// are then divided by their row's den in float32 and rounded to bf16 once more: phi(q) / den.
+// (A bf16 multiply by bf16(1 / den) is cheaper but leaves a rounding error shared by the whole
+// row, which the h z term of dq amplifies: measured, it doubles the dq error.)
+template <int NB, int C, int DPAD>
+__device__ __forceinline__ void feat8_batch_rowscale(uint8_t *const *ptr, const bool *present, const bool *valid,
+                                                     int phi, const float *den_tile, int r0, int step, int nscaled) {
+    uint4 x[NB];
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+        x[n] = present[n] && valid[n] ? *reinterpret_cast<const uint4 *>(ptr[n]) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int n = 0; n < NB; ++n) {
+        if (!(present[n] && valid[n])) continue;
+        uint32_t *xi = reinterpret_cast<uint32_t *>(&x[n]);
+        const int row = r0 + n * step;
+        const float sc = n < nscaled ? 1.f / den_tile[(row / C) * DPAD + row % C] : 1.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t f = feat_bf16x2(xi[q], phi);
+            if (n < nscaled) {
+                const float2 v = unpack_bf16x2(f);
+                f = pack_bf16x2(v.x * sc, v.y * sc);
+            }
+            xi[q] = f;
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+        if (present[n]) *reinterpret_cast<uint4 *>(ptr[n]) = x[n];
+}
+
 // phi applied to 8 bf16 values (16 bytes) in place, or zeros for a row past the end.
 __device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid, int phi) {
     uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
@@ -270,6 +303,21 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int heads, int N, int D,
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// 2-D map over float32 rows [heads][N] with a row stride of `stride` floats (a multiple of
+// 4): box {cols, 1}, no swizzle; columns past N read as zeros.
+cudaError_t make_map_rows_f32(CUtensorMap *map, const void *ptr, int heads, int N, int stride, int cols) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)heads};
+    cuuint64_t strides[1] = {(cuuint64_t)stride * 4};
+    cuuint32_t box[2] = {(cuuint32_t)cols, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

@@ -44,7 +44,9 @@
  *                       overflows 64 bits
  *   LA_ERR_UNSUPPORTED  D not in {32, 64, 128}
  *   LA_ERR_ALIGN        a pointer that is not 16-byte aligned (workspace: 256-byte)
- *   LA_ERR_WORKSPACE    ws_bytes < la_workspace_size(...) or workspace NULL while needed
+ *   LA_ERR_WORKSPACE    ws_bytes < la_workspace_size(...) or workspace NULL while needed;
+ *                       (from la_get_status) la_bwd_from_fwd got a workspace that another
+ *                       la_fwd call wrote
  *   LA_ERR_CUDA         a CUDA launch or runtime error (see la_last_cuda_error())
  *   LA_ERR_TIMEOUT      (from la_get_status) a kernel's bounded wait ran out
  * All argument checks run on the host before any CUDA call.
@@ -104,16 +106,23 @@ la_status la_bwd(const void *q, const void *k, const void *v, const void *grad_o
 
 /* The same backward (same operation, same results) for a caller that has just run la_fwd
  * on these inputs: fwd_workspace / fwd_ws_bytes are that call's workspace, still holding
- * what la_fwd left there (its scanned per-segment states S, z).  When the forward and the
- * backward cut the sequence the same way (the same kernel family, chunk and segments; true
- * whenever both run on the tensor-core path) the backward reads those states instead of
- * recomputing them, which saves one pass over k and v; otherwise it recomputes them and
- * fwd_workspace is not read.  The pages' `bwd` recomputes the forward through autograd;
- * keeping the forward's states is this library's design.  The caller guarantees that
- * la_fwd ran with the same q, k, v, sizes, mode, phi and weights, that its workspace was
- * not written since, and that the forward is ordered before this call (same stream, or an
- * event).  fwd_workspace is read only.  Errors as la_bwd; LA_ERR_ARG if fwd_workspace is
- * NULL. */
+ * what la_fwd left there: its scanned per-segment states S, z and, on the tensor-core path,
+ * every row's denominator den_i = sum_p a_i^p . z_i^p + eps and a record of the call.  When
+ * the forward and the backward cut the sequence the same way (the same kernel family, chunk
+ * and segments; true whenever both run on the tensor-core path) the backward reads those
+ * instead of recomputing them, which saves the forward's pass over q, k and v (la_bwd on the
+ * tensor-core path runs that forward itself, with dq as its output scratch); otherwise it
+ * recomputes them and fwd_workspace is not read.  The pages' `bwd` recomputes the forward
+ * through autograd; keeping the forward's context is this library's design.
+ *
+ * The caller guarantees that la_fwd ran with the same q, k, v (same buffers and values),
+ * sizes, mode, phi, eps and weights, that its workspace was not written since, and that
+ * the forward is ordered before this call (same stream, or an event).  On the tensor-core
+ * path the backward checks the forward's record (sizes, mode, phi, eps, segments and the
+ * q, k, v addresses): a workspace that another call wrote makes la_get_status() return
+ * LA_ERR_WORKSPACE (the gradients of that call are then not valid).  Values changed in the
+ * same buffers cannot be detected.  fwd_workspace is read only.  Errors as la_bwd;
+ * LA_ERR_ARG if fwd_workspace is NULL. */
 la_status la_bwd_from_fwd(const void *q, const void *k, const void *v, const void *grad_out,
                           void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int D,
                           la_dtype dtype, int is_causal, la_phi phi, float eps,
@@ -123,7 +132,8 @@ la_status la_bwd_from_fwd(const void *q, const void *k, const void *v, const voi
 
 /* Synchronises `stream`, then returns and clears the device-side error word of the
  * current device: LA_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call,
- * LA_ERR_CUDA if the synchronisation failed, else LA_OK. */
+ * LA_ERR_WORKSPACE if la_bwd_from_fwd was given a forward workspace that another call
+ * wrote, LA_ERR_CUDA if the synchronisation failed, else LA_OK. */
 la_status la_get_status(void *stream);
 
 /* Static, NUL-terminated description of a status code (host). */

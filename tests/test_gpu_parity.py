@@ -245,6 +245,25 @@ def test_kernel_family(name, fwd_path):
     assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, True) == fwd_path
 
 
+def test_bwd_from_fwd_reports_a_workspace_written_for_other_inputs():
+    """The tensor-core forward leaves a record of its call in its workspace; a backward given
+    that workspace for other tensors reports LA_ERR_WORKSPACE through la_get_status, and the
+    next matching call is clean."""
+    w = gen.Workload("stale", 1, 8, 2, 500, 128, "bf16", True, "elu+1", scale=0.5)
+    a = H.to_dev(gen.make_inputs(w, seed=1))
+    b = H.to_dev(gen.make_inputs(w, seed=2))
+    ws_f = torch.empty(la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, torch.bfloat16, True, False, False),
+                       dtype=torch.uint8, device="cuda")
+    la.fwd(a["q"], a["k"], a["v"], True, "elu+1", 1e-6, workspace=ws_f)
+    la.get_status()
+    la.bwd(b["q"], b["k"], b["v"], b["grad_out"], True, "elu+1", 1e-6, fwd_workspace=ws_f)
+    with pytest.raises(la.LinearAttentionError) as err:
+        la.get_status()
+    assert err.value.status == la.LA_ERR_WORKSPACE
+    la.bwd(a["q"], a["k"], a["v"], a["grad_out"], True, "elu+1", 1e-6, fwd_workspace=ws_f)
+    la.get_status()
+
+
 # la_bwd_from_fwd reuses the forward's segment states when the two plans agree (and
 # recomputes them otherwise); either way it must give exactly la_bwd's results.
 @pytest.mark.parametrize("shape", [
