@@ -76,18 +76,31 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
     pl.P = has_w ? 2 : 1;
     pl.path = tc_supported(Hq, Hkv, N, D, dt, pl.P, causal, is_bwd) ? LA_PATH_TCGEN05 : LA_PATH_SIMT;
     const int bg = B * Hkv;
-    int want;
+    int slots;   // CTAs that run at once on kPlanSms SMs
     if (pl.path == LA_PATH_TCGEN05) {
         pl.chunk = tc_chunk(Hq / Hkv);
-        want = (kPlanSms + bg - 1) / bg;            // one CTA per SM (shared memory bound)
+        slots = kPlanSms;                            // one CTA per SM (shared memory bound)
     } else {
         pl.chunk = 16;
-        want = (2 * kPlanSms + bg - 1) / bg;        // about two CTAs per SM in total
+        slots = 2 * kPlanSms;                        // about two CTAs per SM
     }
     const int nchunks = (N + pl.chunk - 1) / pl.chunk;
-    if (want > nchunks) want = nchunks;
-    if (want < 1) want = 1;
-    const int chunks_per_seg = (nchunks + want - 1) / want;
+    // segments per (batch, kv head): the count whose schedule ends first, counting waves of
+    // `slots` CTAs that each run their segment's chunks in turn plus about two chunks' worth of
+    // pipeline fill and drain (the fewest segments on a tie)
+    int chunks_per_seg = nchunks;
+    long long best = -1;
+    const int max_want = nchunks < 4 * slots ? nchunks : 4 * slots;
+    for (int want = 1; want <= max_want; ++want) {
+        const int cps = (nchunks + want - 1) / want;
+        const int nseg = (nchunks + cps - 1) / cps;
+        const long long waves = ((long long)bg * nseg + slots - 1) / slots;
+        const long long cost = waves * (cps + 2);
+        if (best < 0 || cost < best) {
+            best = cost;
+            chunks_per_seg = cps;
+        }
+    }
     pl.seg_len = chunks_per_seg * pl.chunk;
     pl.nseg = (N + pl.seg_len - 1) / pl.seg_len;
     pl.state_elems = (size_t)pl.P * D * (D + 1);

@@ -82,7 +82,7 @@ TC_CASES = [
     (2, 16, 2, 3000, 128, False, "relu"),
     (2, 16, 2, 3000, 128, True, "elu+1"),     # causal, n_rep 8
     (2, 16, 8, 3000, 128, True, "relu"),      # causal, n_rep 2
-    (1, 8, 8, 1500, 64, False, "relu"),       # n_rep 1
+    (1, 8, 8, 8000, 64, False, "relu"),       # n_rep 1
     (1, 4, 4, 2100, 128, True, "elu+1"),      # n_rep 1, D = 128
 ]
 

@@ -20,9 +20,9 @@ from efficient_transformer_gb300 import la
 
 pytestmark = pytest.mark.gpu
 
-# causal tensor-core forward, n_rep 2 (C = 64), 64 key/value heads: three segments of three
+# causal tensor-core forward, n_rep 2 (C = 64), 64 key/value heads: two segments of three
 # chunks per head, fewer chunks than pipeline stages
-W = gen.Workload("timeout_case", 1, 128, 64, 576, 64, "bf16", True, "elu+1", scale=0.5)
+W = gen.Workload("timeout_case", 1, 128, 64, 384, 64, "bf16", True, "elu+1", scale=0.5)
 
 
 @pytest.fixture(scope="module")
