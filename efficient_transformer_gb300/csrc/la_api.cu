@@ -59,7 +59,7 @@ la_status check_shape(int B, int Hq, int Hkv, int N, int D, int dtype, int phi, 
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || D <= 0) return LA_ERR_ARG;
     if (Hq % Hkv != 0) return LA_ERR_ARG;
     if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_ARG;
-    if (phi != LA_PHI_ELU1 && phi != LA_PHI_RELU) return LA_ERR_ARG;
+    if (phi != LA_PHI_ELU1 && phi != LA_PHI_RELU && phi != LA_PHI_IDENTITY) return LA_ERR_ARG;
     if (!(eps >= 0.f) || !std::isfinite(eps)) return LA_ERR_ARG;
     if ((cw == nullptr) != (sw == nullptr)) return LA_ERR_ARG;
     // element counts must fit comfortably in 64 bits

@@ -78,13 +78,15 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(x);
 }
 
-// phi and its derivative (phi = 0: elu(x) + 1, alpha = 1; phi = 1: relu).
+// phi and its derivative (phi = 0: elu(x) + 1, alpha = 1; phi = 1: relu; phi = 2: x).
 __device__ __forceinline__ float feature(float x, int phi) {
     if (phi == LA_PHI_ELU1) return x > 0.f ? x + 1.f : expf(x);
+    if (phi == LA_PHI_IDENTITY) return x;
     return x > 0.f ? x : 0.f;
 }
 __device__ __forceinline__ float feature_grad(float x, int phi) {
     if (phi == LA_PHI_ELU1) return x > 0.f ? 1.f : expf(x);
+    if (phi == LA_PHI_IDENTITY) return 1.f;
     return x > 0.f ? 1.f : 0.f;
 }
 

@@ -104,8 +104,8 @@ struct BwdCfg {
 
 __device__ __forceinline__ float feat_grad_from_feat(float f, int phi) {
     // elu+1: phi = x + 1 > 1 for x > 0 (derivative 1), phi = exp(x) <= 1 otherwise
-    // (derivative exp(x) = phi); relu: derivative 1 where phi > 0.
-    return phi == LA_PHI_ELU1 ? (f > 1.f ? 1.f : f) : (f > 0.f ? 1.f : 0.f);
+    // (derivative exp(x) = phi); relu: derivative 1 where phi > 0; identity: 1.
+    return phi == LA_PHI_ELU1 ? (f > 1.f ? 1.f : f) : phi == LA_PHI_IDENTITY ? 1.f : (f > 0.f ? 1.f : 0.f);
 }
 
 // z (fp32) into column d of a z tile as the rows (z_hi, z_lo, z_hi), z = z_hi + z_lo.
@@ -130,16 +130,16 @@ __device__ __forceinline__ void store_rbf_row(uint8_t *rbf, int d, const float *
 
 // Eight dq values from eight phi_s = phi(q) / den (bf16) and the matching den * da (fp32):
 // dq = phi'(q) / den * (den da), with phi'(q) / den = min(phi_s, 1 / den) for elu+1
-// (phi' = min(phi, 1)) and 1 / den where phi_s > 0 for relu.
-template <bool ELU>
+// (phi' = min(phi, 1)), 1 / den where phi_s > 0 for relu and 1 / den for identity.
+template <int PHI>
 __device__ __forceinline__ uint4 dq_piece(uint4 u, const float *x, float inv) {
     const uint32_t *ui = reinterpret_cast<const uint32_t *>(&u);
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float2 f = unpack_bf16x2(ui[q]);
-        const float m0 = ELU ? fminf(f.x, inv) : (f.x > 0.f ? inv : 0.f);
-        const float m1 = ELU ? fminf(f.y, inv) : (f.y > 0.f ? inv : 0.f);
+        const float m0 = PHI == LA_PHI_ELU1 ? fminf(f.x, inv) : PHI == LA_PHI_IDENTITY ? inv : (f.x > 0.f ? inv : 0.f);
+        const float m1 = PHI == LA_PHI_ELU1 ? fminf(f.y, inv) : PHI == LA_PHI_IDENTITY ? inv : (f.y > 0.f ? inv : 0.f);
         w[q] = pack_bf16x2(m0 * x[2 * q], m1 * x[2 * q + 1]);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
@@ -624,7 +624,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 for (int q8 = 0; q8 < 2; ++q8)
                     if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 341, smem_u32(ch[q8]) - sm_lo, q8))
                         *reinterpret_cast<uint4 *>(ch[q8] + OFF_G) =
-                            p.phi == LA_PHI_ELU1 ? dq_piece<true>(u[q8], xv + q8 * 8, inv) : dq_piece<false>(u[q8], xv + q8 * 8, inv);
+                            p.phi == LA_PHI_ELU1   ? dq_piece<LA_PHI_ELU1>(u[q8], xv + q8 * 8, inv)
+                            : p.phi == LA_PHI_RELU ? dq_piece<LA_PHI_RELU>(u[q8], xv + q8 * 8, inv)
+                                                   : dq_piece<LA_PHI_IDENTITY>(u[q8], xv + q8 * 8, inv);
             }
             fence_proxy_async();
             if (i == 0 && h == 0) LA_TL(k, 12);

@@ -47,7 +47,7 @@ __device__ __forceinline__ void warp_drain(uint64_t *bar, uint32_t parity) {
 }
 
 __device__ __forceinline__ float feat(float x, int phi) {
-    return phi == LA_PHI_ELU1 ? (x > 0.f ? x + 1.f : __expf(x)) : fmaxf(x, 0.f);
+    return phi == LA_PHI_ELU1 ? (x > 0.f ? x + 1.f : __expf(x)) : phi == LA_PHI_IDENTITY ? x : fmaxf(x, 0.f);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -107,7 +107,7 @@ __device__ long long g_la_tl2[64][16];   // a second kernel of the same translat
 }
 
 // phi on two bf16 values in bf16x2 arithmetic, branch-free:
-// elu(x) + 1 = max(x, 0) + exp(m), m = min(x, 0); relu(x) = max(x, 0).
+// elu(x) + 1 = max(x, 0) + exp(m), m = min(x, 0); relu(x) = max(x, 0); identity: x.
 // exp(m) = 2^y with y = m log2(e).  y is formed as yh = bf16(m * c_hi) (c_hi = log2(e)
 // rounded to bf16) plus the small remainder r = (m c_hi - yh) + m (log2(e) - c_hi), the
 // first term exact in one fused multiply-add; then 2^y = 2^yh 2^r ~ 2^yh (1 + r ln 2),
@@ -116,6 +116,7 @@ __device__ long long g_la_tl2[64][16];   // a second kernel of the same translat
 // rounding was measured: it lowers the tensor-core dq error by at most 20 % and makes the
 // long-context step 10 % slower, the feature map being on every kernel's chunk path.)
 __device__ __forceinline__ uint32_t feat_bf16x2(uint32_t u, int phi) {
+    if (phi == LA_PHI_IDENTITY) return u;
     __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&u);
     const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
     __nv_bfloat162 y = __hmax2(x, zero);

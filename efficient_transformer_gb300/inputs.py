@@ -8,6 +8,8 @@ cosFormer position weights, which are inputs of the operation.  The recipe:
 * float32 standard normal draws in the order q, k, v, grad_out, each of its own shape
   ([B, Hq, N, D] for q and grad_out, [B, Hkv, N, D] for k and v);
 * q, k and v multiplied by ``scale`` (grad_out is not scaled);
+* for workloads marked ``positive`` (the identity feature map, whose features the pages
+  call non-negative), q and k replaced by their absolute values;
 * a cast to the workload's dtype (round to nearest even for bf16);
 * cosFormer weights cos(pi*i/(2N)) and sin(pi*i/(2N)) for i = 0..N-1, evaluated in
   float64 and stored as float32.
@@ -34,6 +36,7 @@ class Workload:
     eps: float = 1e-6
     weights: bool = False   # cosFormer cos/sin position weights
     scale: float = 1.0
+    positive: bool = False  # |q|, |k| (non-negative features for phi = identity)
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -91,6 +94,9 @@ def make_inputs(w: Workload, seed: int = 0, device: str | torch.device = "cpu"):
         q.mul_(w.scale)
         k.mul_(w.scale)
         v.mul_(w.scale)
+    if w.positive:
+        q.abs_()
+        k.abs_()
     dt = w.torch_dtype
     out = {"q": q.to(dt), "k": k.to(dt), "v": v.to(dt), "grad_out": g.to(dt),
            "cos_weight": None, "sin_weight": None}

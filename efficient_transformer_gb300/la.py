@@ -25,8 +25,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libla.so")
 LA_OK, LA_ERR_ARG, LA_ERR_UNSUPPORTED, LA_ERR_ALIGN, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(7)
 LA_F32, LA_BF16 = 0, 1
 LA_PATH_SIMT, LA_PATH_TCGEN05 = 0, 1
-PHI = {"elu+1": 0, "relu": 1}
-_NOT_BUILT = {"identity", "softmax_free"}
+PHI = {"elu+1": 0, "relu": 1, "identity": 2}
+_NOT_BUILT = {"softmax_free"}
 
 _lib = None
 
@@ -96,7 +96,7 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def _phi_code(phi: str) -> int:
     if phi in _NOT_BUILT:
-        raise NotImplementedError(f"phi={phi!r} is not built (only 'elu+1' and 'relu')")
+        raise NotImplementedError(f"phi={phi!r} is not built (only 'elu+1', 'relu' and 'identity')")
     if phi not in PHI:
         raise ValueError(f"unknown phi {phi!r}")
     return PHI[phi]

@@ -9,7 +9,7 @@
  *   S_i^p = sum_{j in J(i)} b_j^p v_j^T,  z_i^p = sum_{j in J(i)} b_j^p
  *   out_i = (sum_p (a_i^p)^T S_i^p) / (sum_p a_i^p . z_i^p + eps)
  *
- * J(i) = {j <= i} (causal) or all j (bidirectional); phi(x) = elu(x) + 1 or relu(x);
+ * J(i) = {j <= i} (causal) or all j (bidirectional); phi(x) = elu(x) + 1, relu(x) or x;
  * without position weights there is one term p with w = 1, with them there are two:
  * w^cos = cos_weight and w^sin = sin_weight.  la_bwd returns the exact gradient of la_fwd
  * (the page's `bwd` differentiates `fwd`).
@@ -70,8 +70,11 @@ typedef enum {
     LA_ERR_WORKSPACE = 6
 } la_status;
 
-/* Feature map phi: elu(x) + 1 with alpha = 1, or max(x, 0). */
-typedef enum { LA_PHI_ELU1 = 0, LA_PHI_RELU = 1 } la_phi;
+/* Feature map phi: elu(x) + 1 with alpha = 1, max(x, 0), or x itself (identity: the
+ * caller's q and k are the features; the linear_attn page lists the maps as non-negative,
+ * so identity expects non-negative q and k: with signed features the denominator can
+ * vanish and the result is ill-conditioned or non-finite). */
+typedef enum { LA_PHI_ELU1 = 0, LA_PHI_RELU = 1, LA_PHI_IDENTITY = 2 } la_phi;
 
 /* Element type of q, k, v, grad_out and of every output. */
 typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;

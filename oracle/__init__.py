@@ -25,7 +25,7 @@ _SRC = os.path.join(_HERE, "la_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libla_oracle.so")
 
-PHI = {"elu+1": 0, "relu": 1}
+PHI = {"elu+1": 0, "relu": 1, "identity": 2}
 
 _lock = threading.Lock()
 _lib = None

@@ -14,8 +14,8 @@
  *   num_i = sum_p (a_i^p)^T S_i^p            den_i = sum_p a_i^p . z_i^p + eps
  *   out_i = num_i / den_i
  *
- * with J(i) = {j <= i} when causal and all j otherwise, phi(x) = elu(x)+1 (alpha = 1) or
- * relu(x), and w^p = 1 without position weights, else w^cos = cos_weight, w^sin =
+ * with J(i) = {j <= i} when causal and all j otherwise, phi(x) = elu(x)+1 (alpha = 1),
+ * relu(x) or x ("identity": the caller's features are used as they are), and w^p = 1 without position weights, else w^cos = cos_weight, w^sin =
  * sin_weight (cosFormer modulation: one weight per position, applied to phi(q_i) and
  * phi(k_i), never to v).  The state is the running prefix sum, taken in token order, so
  * this is the plain recurrent definition with no chunking, blocking or reordering.
@@ -33,7 +33,8 @@
  *   db_j^p = R_j^p v_j + r_j^p,   dv_j = sum_p (R_j^p)^T b_j^p
  *   dq_i = phi'(q_i) * sum_p w_i^p da_i^p,   dk_j = phi'(k_j) * sum_p w_j^p db_j^p
  * obtained by differentiating the definition above by hand (chain rule through out =
- * num/den).  phi'(x) = (x > 0 ? 1 : exp(x)) for elu+1 and (x > 0 ? 1 : 0) for relu.
+ * num/den).  phi'(x) = (x > 0 ? 1 : exp(x)) for elu+1, (x > 0 ? 1 : 0) for relu and 1 for
+ * identity.
  *
  * Layout: every tensor is a contiguous row-major float64 array [B, H, N, D]; Dv = D.
  * The weights, when given, are float64 arrays of length N (both or neither).
@@ -48,17 +49,19 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_PHI_ELU1 = 0, ORACLE_PHI_RELU = 1 };
+enum { ORACLE_PHI_ELU1 = 0, ORACLE_PHI_RELU = 1, ORACLE_PHI_IDENTITY = 2 };
 
 static double feature(double x, int phi)
 {
     if (phi == ORACLE_PHI_ELU1) return x > 0.0 ? x + 1.0 : exp(x);
+    if (phi == ORACLE_PHI_IDENTITY) return x;
     return x > 0.0 ? x : 0.0;
 }
 
 static double feature_grad(double x, int phi)
 {
     if (phi == ORACLE_PHI_ELU1) return x > 0.0 ? 1.0 : exp(x);
+    if (phi == ORACLE_PHI_IDENTITY) return 1.0;
     return x > 0.0 ? 1.0 : 0.0;
 }
 

@@ -30,12 +30,16 @@ import oracle
 def phi_np(x, phi):
     if phi == "elu+1":
         return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+    if phi == "identity":
+        return x
     return np.maximum(x, 0.0)
 
 
 def phi_torch(x, phi):
     if phi == "elu+1":
         return torch.nn.functional.elu(x) + 1.0
+    if phi == "identity":
+        return x
     return torch.relu(x)
 
 
@@ -86,10 +90,14 @@ def autograd_backward(q, k, v, g, causal, phi, eps, cw=None, sw=None):
     return tuple(x.numpy() for x in grads)
 
 
-def rand_case(B, Hq, Hkv, N, D, seed, weights=False, scale=1.0, avoid_kink=False):
+def rand_case(B, Hq, Hkv, N, D, seed, weights=False, scale=1.0, avoid_kink=False, positive=False):
+    """Random case; positive=True draws |N(0,1)| for q and k (identity feature map, whose
+    features the pages call non-negative)."""
     rng = np.random.default_rng(seed)
     q = rng.standard_normal((B, Hq, N, D)) * scale
     k = rng.standard_normal((B, Hkv, N, D)) * scale
+    if positive:
+        q, k = np.abs(q), np.abs(k)
     v = rng.standard_normal((B, Hkv, N, D))
     g = rng.standard_normal((B, Hq, N, D))
     if avoid_kink:  # keep relu inputs away from 0 for finite differences
@@ -117,13 +125,16 @@ MODES = [
     (False, "elu+1", True, 2, 2),
     (True, "elu+1", False, 4, 2),
     (False, "relu", True, 6, 2),
+    (True, "identity", False, 2, 2),
+    (False, "identity", True, 4, 2),
 ]
 
 
 def check_forward_brute(lib=None, tol=1e-12):
     fails = []
     for idx, (causal, phi, weights, Hq, Hkv) in enumerate(MODES):
-        q, k, v, g, cw, sw = rand_case(2, Hq, Hkv, 9, 5, seed=100 + idx, weights=weights)
+        q, k, v, g, cw, sw = rand_case(2, Hq, Hkv, 9, 5, seed=100 + idx, weights=weights,
+                                       positive=phi == "identity")
         ref = brute_forward(q, k, v, causal, phi, 1e-6, cw, sw)
         got = oracle.fwd(q, k, v, causal, phi, 1e-6, cw, sw, lib=lib)
         e = rel_err(got, ref)
@@ -135,7 +146,8 @@ def check_forward_brute(lib=None, tol=1e-12):
 def check_backward_autograd(lib=None, tol=1e-10):
     fails = []
     for idx, (causal, phi, weights, Hq, Hkv) in enumerate(MODES):
-        q, k, v, g, cw, sw = rand_case(2, Hq, Hkv, 7, 4, seed=200 + idx, weights=weights)
+        q, k, v, g, cw, sw = rand_case(2, Hq, Hkv, 7, 4, seed=200 + idx, weights=weights,
+                                       positive=phi == "identity")
         ref = autograd_backward(q, k, v, g, causal, phi, 1e-6, cw, sw)
         got = oracle.bwd(q, k, v, g, causal, phi, 1e-6, cw, sw, lib=lib)
         for name, a, b in zip(("dq", "dk", "dv"), got, ref):
@@ -176,7 +188,7 @@ def check_gqa_rule(lib=None, tol=1e-13):
 def check_closed_forms(lib=None):
     fails = []
     eps = 1e-6
-    for phi in ("elu+1", "relu"):
+    for phi in ("elu+1", "relu", "identity"):
         q, k, v, g, _, _ = rand_case(1, 1, 1, 5, 4, seed=400, scale=1.0)
         q[..., 0, :] = np.abs(q[..., 0, :]) + 0.1  # keep row 0 alive under relu
         k[..., 0, :] = np.abs(k[..., 0, :]) + 0.1
@@ -189,6 +201,14 @@ def check_closed_forms(lib=None):
             o1 = oracle.fwd(q[:, :, :1], k[:, :, :1], v[:, :, :1], causal, phi, eps, lib=lib)
             if rel_err(o1[0, 0, 0], want) > 1e-14:
                 fails.append(f"N=1 closed form phi={phi} causal={causal}")
+    # identity uses the features as given, signs included: row 0 with mixed signs and
+    # s = q_0 . k_0 = 1.75 > 0, eps = 1: out_0 = v_0 s / (s + 1)
+    q0 = np.array([[[[1.0, -0.5, 2.0, -1.0]]]])
+    k0 = np.array([[[[0.5, 1.0, 1.0, 0.25]]]])
+    v0 = np.array([[[[3.0, -1.0, 0.5, 2.0]]]])
+    o = oracle.fwd(q0, k0, v0, True, "identity", 1.0, lib=lib)
+    if rel_err(o[0, 0, 0], v0[0, 0, 0] * 1.75 / 2.75) > 1e-14:
+        fails.append("identity row0 closed form with mixed signs")
     return fails
 
 
@@ -247,10 +267,10 @@ def check_gradient_identities(lib=None):
 def check_finite_differences(lib=None, h=1e-6, tol=1e-6):
     fails = []
     cases = [(True, "elu+1", False, 2, 1), (False, "relu", False, 1, 1), (True, "relu", True, 2, 2),
-             (False, "elu+1", True, 2, 1)]
+             (False, "elu+1", True, 2, 1), (True, "identity", False, 2, 1)]
     for idx, (causal, phi, weights, Hq, Hkv) in enumerate(cases):
         q, k, v, g, cw, sw = rand_case(1, Hq, Hkv, 5, 3, seed=700 + idx, weights=weights,
-                                       avoid_kink=True)
+                                       avoid_kink=True, positive=phi == "identity")
         dq, dk, dv = oracle.bwd(q, k, v, g, causal, phi, 1e-6, cw, sw, lib=lib)
         for name, x, dx in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
             fd = np.zeros_like(x)

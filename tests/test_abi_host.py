@@ -113,9 +113,10 @@ def test_float32_always_takes_simt(lib):
     assert lib.la_kernel_path(1, 32, 8, 65536, 128, la.LA_F32, 1, 0, 1) == la.LA_PATH_SIMT
 
 
-def test_python_binding_rejects_unbuilt_phi():
+def test_python_binding_phi_codes():
+    assert la._phi_code("identity") == 2
     with pytest.raises(NotImplementedError):
-        la._phi_code("identity")
+        la._phi_code("softmax_free")
     with pytest.raises(ValueError):
         la._phi_code("gelu")
 

@@ -138,6 +138,26 @@ def test_edge_shapes(case):
     H.compare(w, got, H.run_oracle(w, inp))
 
 
+@pytest.mark.parametrize("case", [
+    # B, Hq, Hkv, N, D, dtype, causal, weights
+    (1, 2, 2, 300, 32, "f32", True, False),       # CUDA-core kernels
+    (2, 4, 2, 257, 64, "f32", False, True),
+    (1, 8, 2, 1000, 128, "bf16", True, False),    # tensor-core kernels (n_rep 4)
+    (2, 4, 4, 3000, 64, "bf16", False, False),   # tensor-core kernels (n_rep 1, bidirectional)
+    (1, 4, 4, 700, 128, "bf16", True, True),      # CUDA-core kernels, position weights
+], ids=lambda c: "x".join(map(str, c)))
+def test_identity_feature_map(case):
+    """phi = identity on non-negative features (the pages' feature maps are non-negative)."""
+    B, Hq, Hkv, N, D, dt, causal, weights = case
+    w = gen.Workload("identity", B, Hq, Hkv, N, D, dt, causal, "identity", weights=weights, scale=0.5,
+                     positive=True)
+    inp = gen.make_inputs(w, seed=23)
+    ref = H.run_oracle(w, inp)
+    dev = H.to_dev(inp)
+    H.compare(w, H.run_gpu(w, dev, from_fwd=True), ref, label="bwd_from_fwd")
+    H.compare(w, H.run_gpu(w, dev, from_fwd=False), ref, label="bwd")
+
+
 def test_dead_relu_rows():
     w = gen.Workload("dead_rows", 1, 2, 1, 96, 64, "bf16", True, "relu")
     inp = gen.make_inputs(w, seed=3)

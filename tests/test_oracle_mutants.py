@@ -26,6 +26,8 @@ MUTANTS = {
     "elu_derivative": ("if (phi == ORACLE_PHI_ELU1) return x > 0.0 ? 1.0 : exp(x);",
                        "if (phi == ORACLE_PHI_ELU1) return 1.0;"),
     "drop_r_term": ("double db = r[p * D + d];", "double db = 0.0;"),
+    "identity_derivative": ("if (phi == ORACLE_PHI_IDENTITY) return 1.0;", "if (phi == ORACLE_PHI_IDENTITY) return 0.0;"),
+    "identity_as_relu": ("if (phi == ORACLE_PHI_IDENTITY) return x;", "if (phi == ORACLE_PHI_IDENTITY) return x > 0.0 ? x : 0.0;"),
     "causal_exclusive_R": ("if (causal)\n            for (int p = 0; p < P; ++p) {  /* row i = j attends to j */",
                            "if (0)\n            for (int p = 0; p < P; ++p) {  /* row i = j attends to j */"),
 }
