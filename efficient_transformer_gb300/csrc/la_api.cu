@@ -362,6 +362,39 @@ la_status la_trace_kernel(int index, const char **name, int *launches, double *t
 
 }  // extern "C"
 
+// ---- low-rank projection ------------------------------------------------------------------
+
+namespace {
+
+// Host-only checks of the low-rank projection's arguments.
+la_status lowrank_check(int M, int K_in, int r, int K_out, int dtype) {
+    if (M <= 0 || K_in <= 0 || r <= 0 || K_out <= 0) return LA_ERR_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_ARG;
+    const unsigned long long big = (unsigned long long)M * (unsigned long long)(K_in > K_out ? K_in : K_out);
+    if (big >> 60) return LA_ERR_ARG;
+    if (dtype != LA_BF16 || r > 256) return LA_ERR_UNSUPPORTED;
+    // rows of x, y, U and V must start on 16-byte boundaries (TMA row strides)
+    if (K_in % 8 || K_out % 8 || r % 8) return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
+}  // namespace
+
+extern "C" la_status la_lowrank_fwd(const void *x, const void *U, const void *V, const void *bias, void *y, int M,
+                                    int K_in, int r, int K_out, la_dtype dtype, void *stream) {
+    la_status st = lowrank_check(M, K_in, r, K_out, dtype);
+    if (st != LA_OK) return st;
+    if (!x || !U || !V || !y) return LA_ERR_ARG;
+    const void *ptrs[] = {x, U, V, bias, y};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned(ptr, 16)) return LA_ERR_ALIGN;
+    int *err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e == cudaSuccess)
+        e = lowrank_forward(x, U, V, bias, y, M, K_in, r, K_out, err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LA_OK : cuda_fail(e);
+}
+
 // ---- forward without a caller workspace ------------------------------------------------
 //
 // For callers that cannot allocate device memory (plugin hosts that only pass input and

@@ -127,4 +127,8 @@ int tc_chunk(int n_rep);   // tokens per chunk of the tensor-core kernels
 bool tc_bwd_supported(int n_rep, int D);
 cudaError_t tc_launch_state(const Params &p, cudaStream_t s);   // per-segment (S, z) on tensor cores
 
+// Low-rank projection y = (x V^T) U^T + bias (bf16, tensor cores).
+cudaError_t lowrank_forward(const void *x, const void *U, const void *V, const void *bias, void *y, int M, int K_in,
+                            int r, int K_out, int *err, cudaStream_t s);
+
 }  // namespace la

@@ -1,0 +1,339 @@
+// la_lowrank.cu -- the low-rank projection on tensor cores (tcgen05 / TMEM / TMA):
+//
+//   y = (x V^T) U^T + bias        (module neuralops.core.triton_kernels.low_rank, `fwd`)
+//
+// with x [M, K_in], V [r, K_in], U [K_out, r], bias [K_out] (bf16, row-major), and its
+// gradient (the page's `bwd` differentiates `fwd`):
+//
+//   t = x V^T,  dt = g U,  dx = dt V,  dU = g^T t,  dV = dt^T x,  dbias = sum_m g[m].
+//
+// One kernel template does the two chained products of a 128-row tile of A1 [M, K1]:
+//
+//   T = A1 B1^T  (fp32 in TMEM, K1 in 64-column blocks)  ->  bf16 T in shared memory
+//   Y = T B2^T (+ bias)  (fp32 in TMEM, 128 output columns at a time)  ->  bf16 Y by TMA
+//
+// so the rank-r bottleneck T never leaves the SM.  B1 is [R, K1] (K-major) or [K1, R]
+// (MN-major: the same bytes read as rows of K), likewise B2 is [N2, R] or [R, N2]; the
+// forward takes x, V, U as they are (both K-major), the backward's dx = (g U) V takes U and
+// V as MN-major operands and also stores T (= dt) for the weight gradients.  The weight
+// gradients dU = g^T t and dV = dt^T x reduce over the M rows: a second kernel sums them in
+// row slices (fp32 partials in the workspace) and a fixed-order reduction finishes them, so
+// results never depend on scheduling.
+//
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps
+// 4-7 epilogue (thread = row of the tile).  Every wait is bounded; a wait that runs out
+// raises the block's abort flag and the call reports LA_ERR_TIMEOUT through la_get_status.
+#include "la_tc_common.cuh"
+
+namespace la {
+namespace {
+
+constexpr int kLrThreads = 256;
+
+// 2-D map over a row-major bf16 matrix [rows][cols]: box {64 columns, box_rows rows},
+// 128-byte swizzle; elements past either edge read as zeros.
+cudaError_t make_map_2d(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// RP: the inner (rank) dimension padded to a multiple of 64, at most 256.
+template <int RP, bool B1_MN, bool B2_MN>
+struct ChainCfg {
+    static constexpr int RB = RP / 64;                        // 64-wide rank blocks
+    static constexpr int A_BYTES = 128 * 64 * 2;              // A1 block: 128 rows x 64 columns of K1
+    static constexpr int B1_BYTES = RP * 64 * 2;              // B1 block: RP x 64 (either layout)
+    static constexpr int B2_BYTES = 128 * 64 * 2;             // B2 block: 128 outputs x 64 rank columns
+    static constexpr int STAGE = A_BYTES + (B1_BYTES > B2_BYTES ? B1_BYTES : B2_BYTES);
+    static constexpr int TBF_BYTES = 128 * RP * 2;            // T (bf16): 128 rows x RP, K-major
+    static constexpr int OUT_BYTES = 128 * 64 * 2;            // Y (or T) staging: 128 rows x 64 columns
+    static constexpr int FIXED = TBF_BYTES + OUT_BYTES + 1024;
+    static constexpr int NS = (kSmemLimit - 1024 - FIXED) / STAGE > 4 ? 4 : (kSmemLimit - 1024 - FIXED) / STAGE;
+    static constexpr int SMEM = NS * STAGE + FIXED;
+    static_assert(NS >= 2, "two pipeline stages");
+    // TMEM: T in [0, RP), the two Y buffers at 256 and 384 (128 columns each)
+    static constexpr int T_T = 0, T_Y0 = 256, T_Y1 = 384;
+};
+
+struct ChainArgs {
+    int M, K1, R, N2;      // A1 [M, K1], the rank R (<= RP), N2 output columns
+    const void *bias;      // [N2] bf16 or null
+    int write_t, write_y;  // which products leave the SM
+    int *err;
+};
+
+template <int RP, bool B1_MN, bool B2_MN>
+__global__ void __launch_bounds__(kLrThreads, 1) k_lr_chain(const __grid_constant__ CUtensorMap map_a1,
+                                                             const __grid_constant__ CUtensorMap map_b1,
+                                                             const __grid_constant__ CUtensorMap map_b2,
+                                                             const __grid_constant__ CUtensorMap map_t,
+                                                             const __grid_constant__ CUtensorMap map_y, ChainArgs a) {
+    using K = ChainCfg<RP, B1_MN, B2_MN>;
+    constexpr int NS = K::NS;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_tfull, bar_tbf, bar_yfull[2], bar_yfree[2], bar_fin;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    uint8_t *stage0 = align1024(smem_raw);
+    uint8_t *tbf = stage0 + NS * K::STAGE;
+    uint8_t *obuf = tbf + K::TBF_BYTES;
+    const int warp = threadIdx.x / 32;
+    const int ntiles = (a.M + 127) / 128;
+    const int nk1 = (a.K1 + 63) / 64;
+    const int nn2 = a.write_y ? (a.N2 + 127) / 128 : 0;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
+        }
+        mbar_init(&bar_tfull, 1);
+        mbar_init(&bar_tbf, 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar_yfull[b], 1);
+            mbar_init(&bar_yfree[b], 128);
+        }
+        mbar_init(&bar_fin, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tT = tmem_base + K::T_T;
+
+    if (warp == 0) {
+        // ---------------- TMA producer: per tile, the K1 blocks of A1 and B1, then the
+        // (output tile, rank block) blocks of B2, all through one ring of stages
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+            for (int kb = 0; ok && kb < nk1; ++kb, ++it) {
+                const int s = it % NS;
+                if (it >= NS && !warp_wait(&bar_empty[s], ((it / NS) - 1) & 1, &abort_flag)) { ok = false; break; }
+                uint8_t *st = stage0 + s * K::STAGE;
+                mbar_arrive_expect_tx_w(&bar_full[s], K::A_BYTES + K::B1_BYTES);
+                tma_load_2d_w(st, &map_a1, &bar_full[s], kb * 64, tile * 128);
+                if (B1_MN)   // B1 stored [K1][R]: RP/64 boxes of 64 K rows x 64 rank columns
+                    for (int rb = 0; rb < K::RB; ++rb)
+                        tma_load_2d_w(st + K::A_BYTES + rb * 64 * 128, &map_b1, &bar_full[s], rb * 64, kb * 64);
+                else         // B1 stored [R][K1]: one box of RP rows x 64 K columns
+                    tma_load_2d_w(st + K::A_BYTES, &map_b1, &bar_full[s], kb * 64, 0);
+            }
+            for (int nt = 0; ok && nt < nn2; ++nt)
+                for (int rb = 0; ok && rb < K::RB; ++rb, ++it) {
+                    const int s = it % NS;
+                    if (it >= NS && !warp_wait(&bar_empty[s], ((it / NS) - 1) & 1, &abort_flag)) { ok = false; break; }
+                    uint8_t *st = stage0 + s * K::STAGE + K::A_BYTES;
+                    mbar_arrive_expect_tx_w(&bar_full[s], K::B2_BYTES);
+                    if (B2_MN)   // B2 stored [R][N2]: two boxes of 64 rank rows x 64 output columns
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_2d_w(st + h * 64 * 128, &map_b2, &bar_full[s], nt * 128 + h * 64, rb * 64);
+                    else         // B2 stored [N2][R]: one box of 128 output rows x 64 rank columns
+                        tma_load_2d_w(st, &map_b2, &bar_full[s], rb * 64, nt * 128);
+                }
+        }
+        // drain the copies still in flight
+        for (int j = it > NS ? it - NS : 0; j < it; ++j) warp_drain(&bar_full[j % NS], (j / NS) & 1);
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        constexpr uint32_t id1 = idesc_bf16(128, RP, false, B1_MN);
+        constexpr uint32_t id2 = idesc_bf16(128, 128, false, B2_MN);
+        const uint32_t tb = smem_u32(tbf);
+        int it = 0, yc = 0, tc = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++tc) {
+            // T's columns are free once the epilogue has read the previous tile's T (tbf)
+            if (tc > 0 && !warp_wait(&bar_tbf, (tc - 1) & 1, &abort_flag)) break;
+            tc_fence_after();
+            for (int kb = 0; kb < nk1; ++kb, ++it) {
+                const int s = it % NS;
+                if (!warp_wait(&bar_full[s], (it / NS) & 1, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t as = smem_u32(stage0 + s * K::STAGE), bs = as + K::A_BYTES;
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t bd = B1_MN ? desc_mnmajor(bs, 64, 0, kk) : desc_kmajor(bs, RP, 0, kk);
+                    mma_bf16_w(tT, desc_kmajor(as, 128, 0, kk), bd, id1, (kb > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit_w(&bar_empty[s]);
+            }
+            if (!ok) break;
+            mma_commit_w(&bar_tfull);
+            if (nn2 == 0) continue;
+            if (!warp_wait(&bar_tbf, tc & 1, &abort_flag)) break;   // bf16 T is in shared memory
+            tc_fence_after();
+            for (int nt = 0; ok && nt < nn2; ++nt, ++yc) {
+                const int yb = yc & 1;
+                const uint32_t tY = tmem_base + (yb ? K::T_Y1 : K::T_Y0);
+                if (yc >= 2 && !warp_wait(&bar_yfree[yb], ((yc / 2) - 1) & 1, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                for (int rb = 0; rb < K::RB; ++rb, ++it) {
+                    const int s = it % NS;
+                    if (!warp_wait(&bar_full[s], (it / NS) & 1, &abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t bs = smem_u32(stage0 + s * K::STAGE + K::A_BYTES);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = B2_MN ? desc_mnmajor(bs, 64, 0, kk) : desc_kmajor(bs, 128, 0, kk);
+                        mma_bf16_w(tY, desc_kmajor(tb, 128, 0, rb * 4 + kk), bd, id2, (rb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit_w(&bar_empty[s]);
+                }
+                if (!ok) break;
+                mma_commit_w(&bar_yfull[yb]);
+            }
+        }
+        mma_commit_w(&bar_fin);
+        warp_drain(&bar_fin, 0);
+    } else if (warp >= 4) {
+        // ---------------- epilogue: thread i = row i of the tile (TMEM lane i)
+        const int i = threadIdx.x - 128;
+        const int wq = warp - 4;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        int yc = 0, tc = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tc) {
+            ok = ok && warp_wait(&bar_tfull, tc & 1, &abort_flag);
+            tc_fence_after();
+            // T (fp32) -> bf16 T in shared memory (the operand of the second product), and
+            // when asked, out to global memory through the staging tile
+#pragma unroll 1
+            for (int c16 = 0; c16 < RP / 16; ++c16) {
+                float v[16];
+                if (ok) {
+                    tmem_ld16(tT + lane_off + c16 * 16, v);
+                    tmem_wait_regs<16>(v);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = 0.f;
+                }
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+                *reinterpret_cast<uint4 *>(tbf + swz_chunk(128, i, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(tbf + swz_chunk(128, i, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            tc_fence_before();
+            fence_proxy_async();
+            mbar_arrive_warp(&bar_tbf);
+            if (a.write_t) {   // T leaves from the bf16 copy, 64 columns at a time
+                for (int rb = 0; rb < (a.R + 63) / 64; ++rb) {
+                    named_barrier(2, 128);
+                    if (ok && i < 32) {
+                        tma_store_2d_w(&map_t, tbf + rb * 128 * 128, rb * 64, tile * 128);
+                        bulk_commit();
+                        bulk_wait_read();
+                    }
+                    __syncwarp();
+                }
+            }
+            for (int nt = 0; nt < nn2; ++nt, ++yc) {
+                const int yb = yc & 1;
+                const uint32_t tY = tmem_base + (yb ? K::T_Y1 : K::T_Y0);
+                ok = ok && warp_wait(&bar_yfull[yb], (yc / 2) & 1, &abort_flag);
+                tc_fence_after();
+                for (int c64 = 0; c64 < 2; ++c64) {
+                    float v[32];
+                    if (i < 32) {   // the staging tile's previous store has read it
+                        bulk_wait_read();
+                        __syncwarp();
+                    }
+                    named_barrier(2, 128);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int col0 = nt * 128 + c64 * 64 + hh * 32;
+                        if (ok) {
+                            tmem_ld32(tY + lane_off + c64 * 64 + hh * 32, v);
+                            tmem_wait_regs<32>(v);
+                            if (a.bias)
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    v[e] += col0 + e < a.N2
+                                                ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.bias)[col0 + e])
+                                                : 0.f;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint4 w;
+                                w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+                                w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+                                w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+                                w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+                                *reinterpret_cast<uint4 *>(obuf + swz_chunk(128, i, hh * 4 + q)) = w;
+                            }
+                        }
+                    }
+                    if (c64 == 1) {   // every column of this Y buffer is in registers
+                        tc_fence_before();
+                        mbar_arrive_warp(&bar_yfree[yb]);
+                    }
+                    fence_proxy_async();
+                    named_barrier(2, 128);
+                    if (ok && i < 32) {
+                        tma_store_2d_w(&map_y, obuf, nt * 128 + c64 * 64, tile * 128);
+                        bulk_commit();
+                    }
+                }
+            }
+        }
+        if (i < 32) bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+    if (threadIdx.x == 0 && abort_flag) atomicExch(a.err, kErrTimeout);
+}
+
+template <int RP, bool B1_MN, bool B2_MN>
+cudaError_t launch_chain(const void *a1, const void *b1, const void *b2, void *t, void *y, const ChainArgs &ca,
+                         cudaStream_t s, const char *name) {
+    using K = ChainCfg<RP, B1_MN, B2_MN>;
+    CUtensorMap m_a1{}, m_b1{}, m_b2{}, m_t{}, m_y{};
+    cudaError_t e = make_map_2d(&m_a1, a1, ca.M, ca.K1, 128);
+    // B1 as stored: [R][K1] (box RP rows) or [K1][R] (box 64 rows)
+    if (e == cudaSuccess) e = B1_MN ? make_map_2d(&m_b1, b1, ca.K1, ca.R, 64) : make_map_2d(&m_b1, b1, ca.R, ca.K1, RP);
+    if (e == cudaSuccess && ca.write_y)
+        e = B2_MN ? make_map_2d(&m_b2, b2, ca.R, ca.N2, 64) : make_map_2d(&m_b2, b2, ca.N2, ca.R, 128);
+    if (e == cudaSuccess && ca.write_t) e = make_map_2d(&m_t, t, ca.M, ca.R, 128);
+    if (e == cudaSuccess && ca.write_y) e = make_map_2d(&m_y, y, ca.M, ca.N2, 128);
+    if (e == cudaSuccess) e = prepare(k_lr_chain<RP, B1_MN, B2_MN>, K::SMEM);
+    if (e != cudaSuccess) return e;
+    const int ntiles = (ca.M + 127) / 128;
+    const int grid = ntiles < kPlanSms ? ntiles : kPlanSms;
+    TraceScope ts(name, s);
+    k_lr_chain<RP, B1_MN, B2_MN><<<grid, kLrThreads, K::SMEM, s>>>(m_a1, m_b1, m_b2, m_t, m_y, ca);
+    return cudaGetLastError();
+}
+
+template <bool B1_MN, bool B2_MN>
+cudaError_t chain_dispatch(const void *a1, const void *b1, const void *b2, void *t, void *y, const ChainArgs &ca,
+                           cudaStream_t s, const char *name) {
+    const int rp = (ca.R + 63) / 64 * 64;
+    switch (rp) {
+        case 64: return launch_chain<64, B1_MN, B2_MN>(a1, b1, b2, t, y, ca, s, name);
+        case 128: return launch_chain<128, B1_MN, B2_MN>(a1, b1, b2, t, y, ca, s, name);
+        case 192: return launch_chain<192, B1_MN, B2_MN>(a1, b1, b2, t, y, ca, s, name);
+        case 256: return launch_chain<256, B1_MN, B2_MN>(a1, b1, b2, t, y, ca, s, name);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace
+
+cudaError_t lowrank_forward(const void *x, const void *U, const void *V, const void *bias, void *y, int M, int K_in,
+                            int r, int K_out, int *err, cudaStream_t s) {
+    ChainArgs ca{M, K_in, r, K_out, bias, 0, 1, err};
+    return chain_dispatch<false, false>(x, V, U, nullptr, y, ca, s, "lr_fwd");
+}
+
+}  // namespace la

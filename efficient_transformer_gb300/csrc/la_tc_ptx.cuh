@@ -381,6 +381,17 @@ __device__ __forceinline__ void tma_store_3d_w(const CUtensorMap *map, const voi
         : "memory");
 }
 
+// Store one box of a 2-D tensor map from shared memory from lane 0 (bulk-group completion;
+// see tma_store_3d_w for the commit and wait that follow).
+__device__ __forceinline__ void tma_store_2d_w(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "@e cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n\t}" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y)
+        : "memory");
+}
+
 // Arrive once on *bar when every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

@@ -107,6 +107,48 @@ def make_inputs(w: Workload, seed: int = 0, device: str | torch.device = "cpu"):
     return out
 
 
+@dataclass(frozen=True)
+class LowRankWorkload:
+    """y = (x V^T) U^T + bias over M rows."""
+    name: str
+    M: int
+    K_in: int
+    r: int
+    K_out: int
+    dtype: str = "bf16"
+    bias: bool = True
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+# The low-rank projection measured beside the attention: 64 K rows (a batch of long
+# sequences) projected through a rank-256 bottleneck between 4096-wide activations.
+LOWRANK_WORKLOADS = {
+    w.name: w
+    for w in [
+        LowRankWorkload("lowrank_m65536_kin4096_r256_kout4096_bf16", 65536, 4096, 256, 4096),
+    ]
+}
+
+
+def make_lowrank_inputs(w: LowRankWorkload, seed: int = 0):
+    """x ~ N(0, 1); V ~ N(0, 1/K_in) and U ~ N(0, 1/r), so that t and y stay of order one;
+    bias and grad_out ~ N(0, 1); drawn in the order x, V, U, bias, grad_out on a CPU
+    generator seeded with `seed`, then cast to the workload's dtype."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    x = torch.randn((w.M, w.K_in), generator=gen)
+    V = torch.randn((w.r, w.K_in), generator=gen) / math.sqrt(w.K_in)
+    U = torch.randn((w.K_out, w.r), generator=gen) / math.sqrt(w.r)
+    b = torch.randn((w.K_out,), generator=gen)
+    g = torch.randn((w.M, w.K_out), generator=gen)
+    dt = w.torch_dtype
+    return {"x": x.to(dt), "U": U.to(dt), "V": V.to(dt), "bias": b.to(dt) if w.bias else None,
+            "grad_out": g.to(dt)}
+
+
 def kv_group_slice(inputs: dict, w: Workload, b: int, g: int):
     """Inputs restricted to batch ``b`` and key/value head ``g`` with its n_rep query
     heads.  Groups are independent, so the oracle on this slice gives exactly the

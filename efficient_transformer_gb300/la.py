@@ -65,6 +65,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.la_status_str.restype = ctypes.c_char_p
     lib.la_last_cuda_error.argtypes = []
     lib.la_last_cuda_error.restype = ctypes.c_char_p
+    lib.la_lowrank_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.la_lowrank_fwd.restype = i
     lib.la_trace_start.argtypes = []
     lib.la_trace_start.restype = i
     lib.la_trace_stop.argtypes = []
@@ -220,6 +222,38 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tenso
     if st != LA_OK:
         _raise(lib, st, call)
     return dq, dk, dv
+
+
+def _check_lowrank(x, U, V, bias):
+    for name, t in (("x", x), ("U", U), ("V", V)) + ((("bias", bias),) if bias is not None else ()):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.dtype != x.dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, x has {x.dtype}")
+    if U.dim() != 2 or V.dim() != 2 or x.shape[-1] != V.shape[1] or U.shape[1] != V.shape[0]:
+        raise ValueError(f"shapes disagree: x {tuple(x.shape)}, U {tuple(U.shape)}, V {tuple(V.shape)}")
+    if bias is not None and bias.shape != (U.shape[0],):
+        raise ValueError("bias must have K_out = U.shape[0] elements")
+    M = x.numel() // x.shape[-1]
+    return M, V.shape[1], V.shape[0], U.shape[0]
+
+
+def lowrank_fwd(x: torch.Tensor, U: torch.Tensor, V: torch.Tensor, bias: torch.Tensor | None = None, *,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Low-rank projection ``y = (x @ V.T) @ U.T + bias`` (module
+    neuralops.core.triton_kernels.low_rank, ``fwd``): x [..., K_in], U [K_out, r], V [r, K_in];
+    returns y [..., K_out]."""
+    lib = load()
+    M, K_in, r, K_out = _check_lowrank(x, U, V, bias)
+    if out is None:
+        out = torch.empty(x.shape[:-1] + (K_out,), dtype=x.dtype, device=x.device)
+    elif out.shape != x.shape[:-1] + (K_out,) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor [..., K_out] of x's dtype")
+    st = lib.la_lowrank_fwd(_ptr(x), _ptr(U), _ptr(V), _ptr(bias), _ptr(out), M, K_in, r, K_out,
+                            _dtype_code(x), _stream_handle(stream))
+    if st != LA_OK:
+        _raise(lib, st, "la_lowrank_fwd")
+    return out
 
 
 def get_status(stream=None) -> None:

@@ -158,6 +158,23 @@ la_status la_trace_stop(void);
 int la_trace_collect(void);
 la_status la_trace_kernel(int index, const char **name, int *launches, double *total_ms);
 
+/* Low-rank projection (module neuralops.core.triton_kernels.low_rank, `fwd`):
+ *
+ *   y = (x V^T) U^T + bias
+ *
+ * x [M, K_in], V [r, K_in], U [K_out, r], bias [K_out] (NULL: no bias), y [M, K_out]; every
+ * tensor row-major and contiguous, bfloat16 (LA_BF16), on the device; the leading
+ * dimensions of a caller's x (batch, sequence) are the M rows.  Arithmetic: float32
+ * accumulation on the tensor cores; the bottleneck t = x V^T is rounded to bf16 once before
+ * the second product (as a bf16 framework computes the two products).  One kernel does both
+ * products per 128-row tile, so t never goes to memory.  No workspace.
+ * Errors: LA_ERR_ARG for sizes <= 0, a null x, U, V or y or an unknown dtype;
+ * LA_ERR_UNSUPPORTED for LA_F32, r > 256, or K_in, K_out or r not a multiple of 8 (rows
+ * must start on 16-byte boundaries); LA_ERR_ALIGN for a pointer that is not 16-byte
+ * aligned.  Asynchronous on `stream`, like la_fwd. */
+la_status la_lowrank_fwd(const void *x, const void *U, const void *V, const void *bias, void *y, int M,
+                         int K_in, int r, int K_out, la_dtype dtype, void *stream);
+
 /* Forward for callers that cannot allocate device memory.
  *
  * Some callers have no way to obtain scratch memory on the GPU: a plugin host that hands

@@ -71,6 +71,17 @@ def record(w: gen.Workload, errs: dict, label: str = "") -> None:
         f.write(json.dumps(row) + "\n")
 
 
+def record_named(name: str, label: str, errs: dict) -> None:
+    """record() for workloads of other operations (the low-rank projection)."""
+    path = os.environ.get("LA_PARITY_RECORD")
+    if not path:
+        return
+    os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
+    with open(path, "a") as f:
+        f.write(json.dumps({"workload": name, "label": label, "dtype": "bf16", "tol": TOL["bf16"],
+                            "errors": errs}) + "\n")
+
+
 def compare(w: gen.Workload, got, ref, label: str = "", names=("out", "dq", "dk", "dv")):
     tol = TOL[w.dtype]
     errs = {n: rel_err(a, b) for n, a, b in zip(names, got, ref)}
