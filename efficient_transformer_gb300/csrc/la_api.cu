@@ -395,6 +395,31 @@ extern "C" la_status la_lowrank_fwd(const void *x, const void *U, const void *V,
     return e == cudaSuccess ? LA_OK : cuda_fail(e);
 }
 
+extern "C" size_t la_lowrank_workspace_size(int M, int K_in, int r, int K_out, la_dtype dtype, int is_bwd) {
+    if (lowrank_check(M, K_in, r, K_out, dtype) != LA_OK || !is_bwd) return 0;
+    return lowrank_bwd_workspace(M, K_in, r, K_out);
+}
+
+extern "C" la_status la_lowrank_bwd(const void *x, const void *U, const void *V, const void *grad_out, void *dx,
+                                    void *dU, void *dV, void *dbias, int M, int K_in, int r, int K_out,
+                                    la_dtype dtype, void *workspace, size_t ws_bytes, void *stream) {
+    la_status st = lowrank_check(M, K_in, r, K_out, dtype);
+    if (st != LA_OK) return st;
+    if (!x || !U || !V || !grad_out || !dx || !dU || !dV) return LA_ERR_ARG;
+    const void *ptrs[] = {x, U, V, grad_out, dx, dU, dV, dbias};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned(ptr, 16)) return LA_ERR_ALIGN;
+    const size_t need = lowrank_bwd_workspace(M, K_in, r, K_out);
+    if (!workspace || ws_bytes < need) return LA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return LA_ERR_ALIGN;
+    int *err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e == cudaSuccess)
+        e = lowrank_backward(x, U, V, grad_out, dx, dU, dV, dbias, M, K_in, r, K_out, workspace, err,
+                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LA_OK : cuda_fail(e);
+}
+
 // ---- forward without a caller workspace ------------------------------------------------
 //
 // For callers that cannot allocate device memory (plugin hosts that only pass input and

@@ -328,12 +328,226 @@ cudaError_t chain_dispatch(const void *a1, const void *b1, const void *b2, void 
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Weight gradients: C = A^T B summed over the M rows, A [M, Mc] and B [M, Nc] row-major (both
+// read as MN-major operands: rows are the reduction index).  Grid: (Mc / 128) x (Nc / NT)
+// output tiles x S row slices; each CTA sums its slice's rows into TMEM and writes an fp32
+// partial tile; k_lr_reduce adds the S partials in slice order.  With ROWSUM the CTA also
+// sums A over its rows (an N = 16 product against a ones tile): dbias = sum_m g[m].
+constexpr int kWgNT = 256;   // output columns per tile
+
+struct WgradArgs {
+    int M, Mc, Nc, S, rows_per;   // rows_per: rows of one slice (a multiple of 64)
+    float *part;                  // [S][Mc][Nc]
+    float *rsum;                  // [S][Mc] (ROWSUM) or null
+    int *err;
+};
+
+template <bool ROWSUM>
+struct WgCfg {
+    static constexpr int A_BYTES = 64 * 128 * 2;     // 64 rows x 128 columns (two 64-column blocks)
+    static constexpr int B_BYTES = 64 * kWgNT * 2;   // 64 rows x 256 columns (four blocks)
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int ONES_BYTES = 16 * 128;      // 16 x 64 K-major, row 0 = 1
+    static constexpr int NS = 4;
+    static constexpr int SMEM = NS * STAGE + ONES_BYTES + 1024;
+    static constexpr int T_C = 0, T_RS = kWgNT;      // TMEM: C tile, then the row sums (16 columns)
+};
+
+template <bool ROWSUM>
+__global__ void __launch_bounds__(kLrThreads, 1) k_lr_wgrad(const __grid_constant__ CUtensorMap map_a,
+                                                             const __grid_constant__ CUtensorMap map_b, WgradArgs w) {
+    using K = WgCfg<ROWSUM>;
+    constexpr int NS = K::NS;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_done;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    uint8_t *stage0 = align1024(smem_raw);
+    uint8_t *ones = stage0 + NS * K::STAGE;
+    const int warp = threadIdx.x / 32;
+    const int ntn = (w.Nc + kWgNT - 1) / kWgNT;
+    const int sl = blockIdx.x % w.S, tile = blockIdx.x / w.S;
+    const int nt = tile % ntn, mt = tile / ntn;
+    const int m0 = sl * w.rows_per, m1 = min(w.M, m0 + w.rows_per);
+    const int nblk = m1 > m0 ? (m1 - m0 + 63) / 64 : 0;
+
+    if (ROWSUM) fill_ones_tile(ones, 64);
+    fence_proxy_async();
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
+        }
+        mbar_init(&bar_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tC = tmem_base + K::T_C, tRS = tmem_base + K::T_RS;
+
+    if (warp == 0) {
+        int issued = 0;
+        for (int kb = 0; kb < nblk; ++kb) {
+            const int s = kb % NS;
+            if (kb >= NS && !warp_wait(&bar_empty[s], ((kb / NS) - 1) & 1, &abort_flag)) break;
+            uint8_t *st = stage0 + s * K::STAGE;
+            const int r0 = m0 + kb * 64;
+            mbar_arrive_expect_tx_w(&bar_full[s], K::STAGE);
+            for (int h = 0; h < 2; ++h) tma_load_2d_w(st + h * 64 * 128, &map_a, &bar_full[s], mt * 128 + h * 64, r0);
+            for (int h = 0; h < kWgNT / 64; ++h)
+                tma_load_2d_w(st + K::A_BYTES + h * 64 * 128, &map_b, &bar_full[s], nt * kWgNT + h * 64, r0);
+            issued = kb + 1;
+        }
+        for (int j = issued > NS ? issued - NS : 0; j < issued; ++j) warp_drain(&bar_full[j % NS], (j / NS) & 1);
+    } else if (warp == 1) {
+        constexpr uint32_t idC = idesc_bf16(128, kWgNT, true, true);
+        constexpr uint32_t idR = idesc_bf16(128, 16, true, false);
+        const uint32_t on = smem_u32(ones);
+        for (int kb = 0; kb < nblk; ++kb) {
+            const int s = kb % NS;
+            if (!warp_wait(&bar_full[s], (kb / NS) & 1, &abort_flag)) break;
+            tc_fence_after();
+            const uint32_t as = smem_u32(stage0 + s * K::STAGE), bs = as + K::A_BYTES;
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                const uint64_t ad = desc_mnmajor(as, 64, 0, kk);
+                mma_bf16_w(tC, ad, desc_mnmajor(bs, 64, 0, kk), idC, acc);
+                if (ROWSUM) mma_bf16_w(tRS, ad, desc_kmajor(on, 16, 0, 0), idR, acc);
+            }
+            mma_commit_w(&bar_empty[s]);
+        }
+        mma_commit_w(&bar_done);
+        warp_drain(&bar_done, 0);
+    } else if (warp >= 4) {
+        // epilogue: thread i = row i of the C tile; fp32 partials to the workspace
+        const int i = threadIdx.x - 128, wq = warp - 4;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const bool ok = warp_wait(&bar_done, 0, &abort_flag);
+        tc_fence_after();
+        const int row = mt * 128 + i;
+        float *dst = w.part + ((size_t)sl * w.Mc + row) * (size_t)w.Nc;
+#pragma unroll 1
+        for (int c16 = 0; c16 < kWgNT / 16; ++c16) {
+            float v[16];
+            if (ok) {
+                tmem_ld16(tC + lane_off + c16 * 16, v);
+                tmem_wait_regs<16>(v);
+            }
+            if (!ok || row >= w.Mc) continue;
+            const int col0 = nt * kWgNT + c16 * 16;
+            for (int e = 0; e < 16; ++e)
+                if (col0 + e < w.Nc) dst[col0 + e] = nblk > 0 ? v[e] : 0.f;
+        }
+        if (ROWSUM && nt == 0) {
+            float v[16];
+            if (ok) {
+                tmem_ld16(tRS + lane_off, v);
+                tmem_wait_regs<16>(v);
+            }
+            if (ok && row < w.Mc) w.rsum[(size_t)sl * w.Mc + row] = nblk > 0 ? v[0] : 0.f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+    if (threadIdx.x == 0 && abort_flag) atomicExch(w.err, kErrTimeout);
+}
+
+// out[e] = bf16(sum over the S slices of part[s][e]), slices in order (deterministic).
+__global__ void k_lr_reduce(const float *part, int S, size_t elems, __nv_bfloat16 *out) {
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < elems; e += (size_t)gridDim.x * blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < S; ++s) acc += part[(size_t)s * elems + e];
+        out[e] = __float2bfloat16_rn(acc);
+    }
+}
+
+// Slices of the M rows for a weight gradient: as many as keep the CTAs within one wave.
+int wgrad_slices(int M, int tiles) {
+    int S = kPlanSms / tiles;
+    const int blocks = (M + 63) / 64;
+    if (S > blocks) S = blocks;
+    return S < 1 ? 1 : S;
+}
+
+// C = A^T B over M rows into bf16 `out` [Mc][Nc] (and, with rsum_out, the row sums of A).
+cudaError_t wgrad(const void *A, const void *Bm, int M, int Mc, int Nc, float *part, float *rsum,
+                  void *out, void *rsum_out, int *err, cudaStream_t s, const char *name) {
+    CUtensorMap ma{}, mb{};
+    cudaError_t e = make_map_2d(&ma, A, M, Mc, 64);
+    if (e == cudaSuccess) e = make_map_2d(&mb, Bm, M, Nc, 64);
+    const bool rs = rsum_out != nullptr;
+    if (e == cudaSuccess) e = rs ? prepare(k_lr_wgrad<true>, WgCfg<true>::SMEM) : prepare(k_lr_wgrad<false>, WgCfg<false>::SMEM);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((Mc + 127) / 128) * ((Nc + kWgNT - 1) / kWgNT);
+    const int S = wgrad_slices(M, tiles);
+    const int rows_per = ((M + S - 1) / S + 63) / 64 * 64;
+    WgradArgs w{M, Mc, Nc, S, rows_per, part, rsum, err};
+    {
+        TraceScope ts(name, s);
+        if (rs)
+            k_lr_wgrad<true><<<tiles * S, kLrThreads, WgCfg<true>::SMEM, s>>>(ma, mb, w);
+        else
+            k_lr_wgrad<false><<<tiles * S, kLrThreads, WgCfg<false>::SMEM, s>>>(ma, mb, w);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
+    TraceScope ts("lr_reduce", s);
+    const size_t elems = (size_t)Mc * Nc;
+    k_lr_reduce<<<kPlanSms * 4, 256, 0, s>>>(part, S, elems, static_cast<__nv_bfloat16 *>(out));
+    e = cudaGetLastError();
+    if (e == cudaSuccess && rs) {
+        k_lr_reduce<<<(Mc + 255) / 256, 256, 0, s>>>(rsum, S, (size_t)Mc, static_cast<__nv_bfloat16 *>(rsum_out));
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
 }  // namespace
 
 cudaError_t lowrank_forward(const void *x, const void *U, const void *V, const void *bias, void *y, int M, int K_in,
                             int r, int K_out, int *err, cudaStream_t s) {
     ChainArgs ca{M, K_in, r, K_out, bias, 0, 1, err};
     return chain_dispatch<false, false>(x, V, U, nullptr, y, ca, s, "lr_fwd");
+}
+
+size_t lowrank_bwd_workspace(int M, int K_in, int r, int K_out) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t tb = up((size_t)M * r * 2);   // t and dt, bf16 [M][r]
+    const int su = wgrad_slices(M, ((K_out + 127) / 128) * ((r + kWgNT - 1) / kWgNT));
+    const int sv = wgrad_slices(M, ((r + 127) / 128) * ((K_in + kWgNT - 1) / kWgNT));
+    const size_t pu = up((size_t)su * K_out * r * 4) + up((size_t)su * K_out * 4);
+    const size_t pv = up((size_t)sv * r * K_in * 4);
+    return 2 * tb + (pu > pv ? pu : pv);
+}
+
+cudaError_t lowrank_backward(const void *x, const void *U, const void *V, const void *g, void *dx, void *dU, void *dV,
+                             void *dbias, int M, int K_in, int r, int K_out, void *ws, int *err, cudaStream_t s) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    char *base = static_cast<char *>(ws);
+    void *t = base, *dt = base + up((size_t)M * r * 2);
+    float *part = reinterpret_cast<float *>(base + 2 * up((size_t)M * r * 2));
+    // t = x V^T (kept for dU = g^T t)
+    ChainArgs ct{M, K_in, r, 0, nullptr, 1, 0, err};
+    cudaError_t e = chain_dispatch<false, false>(x, V, nullptr, t, nullptr, ct, s, "lr_bwd_t");
+    // dt = g U (kept for dV = dt^T x), dx = dt V: U and V read as MN-major operands
+    ChainArgs cx{M, K_out, r, K_in, nullptr, 1, 1, err};
+    if (e == cudaSuccess) e = chain_dispatch<true, true>(g, U, V, dt, dx, cx, s, "lr_bwd_dx");
+    // dU = g^T t (and dbias = the row sums of g), then dV = dt^T x
+    if (e == cudaSuccess) {
+        const int su = wgrad_slices(M, ((K_out + 127) / 128) * ((r + kWgNT - 1) / kWgNT));
+        float *rsum = reinterpret_cast<float *>(reinterpret_cast<char *>(part) + up((size_t)su * K_out * r * 4));
+        e = wgrad(g, t, M, K_out, r, part, rsum, dU, dbias, err, s, "lr_bwd_dU");
+    }
+    if (e == cudaSuccess) e = wgrad(dt, x, M, r, K_in, part, nullptr, dV, nullptr, err, s, "lr_bwd_dV");
+    return e;
 }
 
 }  // namespace la

@@ -67,6 +67,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.la_last_cuda_error.restype = ctypes.c_char_p
     lib.la_lowrank_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.la_lowrank_fwd.restype = i
+    lib.la_lowrank_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.la_lowrank_workspace_size.restype = sz
+    lib.la_lowrank_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
+    lib.la_lowrank_bwd.restype = i
     lib.la_trace_start.argtypes = []
     lib.la_trace_start.restype = i
     lib.la_trace_stop.argtypes = []
@@ -254,6 +258,26 @@ def lowrank_fwd(x: torch.Tensor, U: torch.Tensor, V: torch.Tensor, bias: torch.T
     if st != LA_OK:
         _raise(lib, st, "la_lowrank_fwd")
     return out
+
+
+def lowrank_bwd(x: torch.Tensor, U: torch.Tensor, V: torch.Tensor, grad_out: torch.Tensor,
+                bias: torch.Tensor | None = None, *, workspace: torch.Tensor | None = None, stream=None):
+    """Backward of ``lowrank_fwd`` (module neuralops.core.triton_kernels.low_rank, ``bwd``):
+    returns ``(dx, dU, dV, dbias)``, dbias None without a bias."""
+    lib = load()
+    M, K_in, r, K_out = _check_lowrank(x, U, V, bias)
+    if grad_out.shape != x.shape[:-1] + (K_out,) or grad_out.dtype != x.dtype or not grad_out.is_contiguous():
+        raise ValueError("grad_out must be a contiguous tensor [..., K_out] of x's dtype")
+    dt = _dtype_code(x)
+    dx, dU, dV = torch.empty_like(x), torch.empty_like(U), torch.empty_like(V)
+    db = torch.empty_like(bias) if bias is not None else None
+    ws = _workspace(lib.la_lowrank_workspace_size(M, K_in, r, K_out, dt, 1), x.device, workspace)
+    st = lib.la_lowrank_bwd(_ptr(x), _ptr(U), _ptr(V), _ptr(grad_out), _ptr(dx), _ptr(dU), _ptr(dV), _ptr(db),
+                            M, K_in, r, K_out, dt, _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                            _stream_handle(stream))
+    if st != LA_OK:
+        _raise(lib, st, "la_lowrank_bwd")
+    return dx, dU, dV, db
 
 
 def get_status(stream=None) -> None:

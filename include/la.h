@@ -175,6 +175,23 @@ la_status la_trace_kernel(int index, const char **name, int *launches, double *t
 la_status la_lowrank_fwd(const void *x, const void *U, const void *V, const void *bias, void *y, int M,
                          int K_in, int r, int K_out, la_dtype dtype, void *stream);
 
+/* Bytes of workspace that la_lowrank_bwd (is_bwd = 1) needs; 0 for the forward or for
+ * arguments the calls reject.  Host-only. */
+size_t la_lowrank_workspace_size(int M, int K_in, int r, int K_out, la_dtype dtype, int is_bwd);
+
+/* Backward of la_lowrank_fwd (the page's `bwd`: gradients for x, U, V and bias) for the
+ * output gradient grad_out [M, K_out]:
+ *   t = x V^T,  dt = grad_out U,  dx = dt V,  dU = grad_out^T t,  dV = dt^T x,
+ *   dbias = sum over the M rows of grad_out.
+ * Writes dx [M, K_in], dU [K_out, r], dV [r, K_in] and, when dbias is not NULL, dbias
+ * [K_out] (bf16).  t and dt (bf16, rounded once like the forward's t) and the float32
+ * partial sums of the row reductions live in the workspace (la_lowrank_workspace_size, 256-
+ * byte aligned); the row reductions are summed in a fixed order, so results are
+ * deterministic.  Errors as la_lowrank_fwd, plus LA_ERR_WORKSPACE. */
+la_status la_lowrank_bwd(const void *x, const void *U, const void *V, const void *grad_out, void *dx, void *dU,
+                         void *dV, void *dbias, int M, int K_in, int r, int K_out, la_dtype dtype,
+                         void *workspace, size_t ws_bytes, void *stream);
+
 /* Forward for callers that cannot allocate device memory.
  *
  * Some callers have no way to obtain scratch memory on the GPU: a plugin host that hands

@@ -44,6 +44,27 @@ def test_lowrank_forward(case):
     assert err <= H.TOL["bf16"], err
 
 
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+def test_lowrank_backward(case):
+    M, K_in, r, K_out, bias = case
+    w = gen.LowRankWorkload(f"lr_m{M}_kin{K_in}_r{r}_kout{K_out}", M, K_in, r, K_out, bias=bias)
+    inp = gen.make_lowrank_inputs(w, seed=37)
+    dev = H.to_dev(inp)
+    got = la.lowrank_bwd(dev["x"], dev["U"], dev["V"], dev["grad_out"], dev["bias"])
+    again = la.lowrank_bwd(dev["x"], dev["U"], dev["V"], dev["grad_out"], dev["bias"])
+    la.get_status()
+    ref = lr_oracle.bwd(inp["x"], inp["U"], inp["V"], inp["grad_out"], inp["bias"])
+    errs = {}
+    for name, a, b, c in zip(("dx", "dU", "dV", "dbias"), got, ref, again):
+        if b is None:
+            assert a is None
+            continue
+        errs[name] = H.rel_err(a, b)
+        assert torch.equal(a, c), f"{name} differs between two runs"
+    H.record_named(w.name, "lowrank bwd", errs)
+    assert all(e <= H.TOL["bf16"] for e in errs.values()), errs
+
+
 def test_lowrank_leading_dims_and_deterministic():
     w = gen.LowRankWorkload("lr_lead", 2 * 300, 256, 64, 256)
     inp = gen.make_lowrank_inputs(w, seed=5)
