@@ -452,6 +452,64 @@ def measure_config(la, w: gen.Workload, dev, steps: int, warmup: int, peaks, pea
     return row
 
 
+def lowrank_counts(w: gen.LowRankWorkload):
+    """(bytes, flops) of one low-rank forward and of one forward + backward: compulsory bytes
+    (every input read once, every output written once) and the products' 2 m n k flops."""
+    el = 2
+    x_b, y_b = w.M * w.K_in * el, w.M * w.K_out * el
+    wts = (w.K_in + w.K_out) * w.r * el + (w.K_out * el if w.bias else 0)
+    f_fwd = 2.0 * w.M * w.r * (w.K_in + w.K_out)
+    f_bwd = 2.0 * w.M * w.r * (2 * w.K_in + 3 * w.K_out)   # t, dt, dx, dU, dV
+    b_fwd = x_b + y_b + wts
+    b_bwd = x_b + y_b + x_b + 2 * wts                      # x, g in; dx, dU, dV, dbias out
+    return (b_fwd, f_fwd), (b_fwd + b_bwd, f_fwd + f_bwd)
+
+
+def measure_lowrank(la, w: gen.LowRankWorkload, dev, steps: int, warmup: int, peaks, peak_src):
+    """One row of the per-workload table for the low-rank projection: forward alone and
+    forward + backward, each as blocks of `steps` calls between CUDA events."""
+    host = gen.make_lowrank_inputs(w)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
+    y = torch.empty((w.M, w.K_out), dtype=d["x"].dtype, device=dev)
+    ws = torch.empty(max(1, la.load().la_lowrank_workspace_size(w.M, w.K_in, w.r, w.K_out, la.LA_BF16, 1)),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        la.lowrank_fwd(d["x"], d["U"], d["V"], d["bias"], out=y, stream=stream)
+
+    def step():
+        fwd()
+        la.lowrank_bwd(d["x"], d["U"], d["V"], d["grad_out"], d["bias"], workspace=ws, stream=stream)
+
+    for _ in range(max(3, warmup)):
+        step()
+    la.get_status(stream)
+    per_f = time_blocks(fwd, dev, stream, steps, 5, 1)
+    per = time_blocks(step, dev, stream, steps, 5, 1)
+    la.get_status(stream)
+    (bf, ff), (bs, fs) = lowrank_counts(w)
+    row = {"workload": w.name, "paths": {"fwd": "tcgen05", "bwd": "tcgen05"},
+           "timing": f"5 blocks of {steps} steps; inputs larger than L2", "metric": "TFLOP/s"}
+    row.update(summary_ms(per))
+    ms, ms_f = row["ms_per_step"], statistics.median(per_f)
+    tc_peak = peaks["bf16_tflops_sustained"] * 1e12
+
+    def frac(nbytes, flops, t_ms):
+        t_roof = max(nbytes / (ROOFLINE_HBM_GBS * 1e9), flops / tc_peak)
+        return t_roof * 1e3 / t_ms, ("tensor" if flops / tc_peak >= nbytes / (ROOFLINE_HBM_GBS * 1e9) else "hbm")
+
+    row["tflops"] = fs / (ms / 1e3) / 1e12
+    row["roofline_frac"], row["bound"] = frac(bs, fs, ms)
+    row["fwd"] = {"ms": ms_f, "tflops": ff / (ms_f / 1e3) / 1e12, "roofline_frac": frac(bf, ff, ms_f)[0]}
+    row["tokens_per_s"] = w.M / (ms / 1e3)
+    row["roofline_basis"] = (f"max(bytes / {ROOFLINE_HBM_GBS:.0f} GB/s, flops / {peak_src} bf16 sustained "
+                             f"{peaks['bf16_tflops_sustained']} TFLOP/s)")
+    del d, y, ws
+    torch.cuda.empty_cache()
+    return row
+
+
 def run_ours(args, world, rank, local):
     from efficient_transformer_gb300 import build as la_build
     from efficient_transformer_gb300 import la
@@ -579,6 +637,8 @@ def run_ours(args, world, rank, local):
                 continue
             table.append(measure_config(la, wc, dev, args.steps, args.warmup, peaks, peak_src, flush))
         del flush
+        for wl in gen.LOWRANK_WORKLOADS.values():
+            table.append(measure_lowrank(la, wl, dev, args.steps, args.warmup, peaks, peak_src))
 
     if rank != 0:
         return 0

@@ -81,6 +81,39 @@ struct StateCfg {
     static constexpr int SMEM = NS * STAGE + ONES_BYTES + 1024;
 };
 
+// The state kernel's feature map over a K tile: thread i of kStatePro takes 16-byte pieces
+// idx = i, i + kStatePro, ... (row j = idx / (D / 8)); rows at or past t1 become zeros.
+template <int PHI, int C, int D>
+__device__ __forceinline__ void state_feature_map(uint8_t *kt, int i, int c0, int t1, uint32_t sm_lo, uint32_t sm_hi) {
+    (void)sm_lo;
+    (void)sm_hi;
+#pragma unroll 2
+    for (int idx = i; idx < C * (D / 8); idx += kStatePro) {
+        const int j = idx / (D / 8), c = idx % (D / 8);
+        uint8_t *ch = kt + swz_chunk(C, j, c);
+        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 121, smem_u32(ch) - sm_lo, idx)) feat8_inplace2<PHI>(ch, c0 + j < t1);
+    }
+}
+
+// The forward's feature map over one stage: 16-byte piece `offq` of Q rows r0, r0 + RPP, ...
+// (valid while row % C < nvalid) and, causal, piece `kpiece` of K rows r0, r0 + RPP, ...
+template <int PHI, int C, int RPP, bool CAUSAL>
+__device__ __forceinline__ void fwd_feature_map(uint8_t *st, uint32_t offq, uint8_t *kpiece, int r0, int nvalid,
+                                                uint32_t sm_lo, uint32_t sm_hi) {
+    (void)sm_lo;
+    (void)sm_hi;
+#pragma unroll 4
+    for (int row = r0; row < 128; row += RPP) {
+        uint8_t *ch = st + offq + row * 128;
+        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, row)) feat8_inplace2<PHI>(ch, row % C < nvalid);
+    }
+    if (CAUSAL)
+        for (int j = r0; j < C; j += RPP) {
+            uint8_t *ch = kpiece + j * 128;
+            if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 222, smem_u32(ch) - sm_lo, j)) feat8_inplace2<PHI>(ch, j < nvalid);
+        }
+}
+
 // ---------------------------------------------------------------------------------------
 // Per-segment state: S = phi(K)^T V and z = phi(K)^T 1 over the segment's tokens (fp32 in
 // TMEM), written to the workspace as [D][D+1] (z in column D).
@@ -172,13 +205,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
             if (ok) {
                 uint8_t *kt = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
-#pragma unroll 2
-                for (int idx = i; idx < C * (D / 8); idx += kStatePro) {
-                    const int j = idx / (D / 8), c = idx % (D / 8);
-                    uint8_t *ch = kt + swz_chunk(C, j, c);
-                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 121, smem_u32(ch) - sm_lo, idx))
-                        feat8_inplace2(ch, c0 + j < t1, p.phi);
-                }
+                if (p.phi == LA_PHI_ELU1)
+                    state_feature_map<LA_PHI_ELU1, C, D>(kt, i, c0, t1, sm_lo, sm_hi);
+                else if (p.phi == LA_PHI_RELU)
+                    state_feature_map<LA_PHI_RELU, C, D>(kt, i, c0, t1, sm_lo, sm_hi);
+                else
+                    state_feature_map<LA_PHI_IDENTITY, C, D>(kt, i, c0, t1, sm_lo, sm_hi);
                 fence_proxy_async();
             }
             mbar_arrive_warp(&bar_ready[s]);
@@ -414,18 +446,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             if (ok) {
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int nvalid = t1 - (t0 + k * C);
-#pragma unroll 4
-                for (int row = r0; row < 128; row += RPP) {
-                    uint8_t *ch = st + offq + row * 128;
-                    if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, row))
-                        feat8_inplace2(ch, row % C < nvalid, p.phi);
-                }
-                if (CAUSAL)
-                    for (int j = r0; j < C; j += RPP) {
-                        uint8_t *ch = st + OFF_K + offk + j * 128;
-                        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 222, smem_u32(ch) - sm_lo, j))
-                            feat8_inplace2(ch, j < nvalid, p.phi);
-                    }
+                if (p.phi == LA_PHI_ELU1)
+                    fwd_feature_map<LA_PHI_ELU1, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, sm_lo, sm_hi);
+                else if (p.phi == LA_PHI_RELU)
+                    fwd_feature_map<LA_PHI_RELU, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, sm_lo, sm_hi);
+                else
+                    fwd_feature_map<LA_PHI_IDENTITY, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, sm_lo,
+                                                                     sm_hi);
                 fence_proxy_async();
             }
             if (i == 0) LA_TL(k, 2);

@@ -102,10 +102,12 @@ struct BwdCfg {
     static_assert(NB_KV == 1 || NB_KV == 2, "one or two dk/dv TMEM buffers");
 };
 
-__device__ __forceinline__ float feat_grad_from_feat(float f, int phi) {
-    // elu+1: phi = x + 1 > 1 for x > 0 (derivative 1), phi = exp(x) <= 1 otherwise
-    // (derivative exp(x) = phi); relu: derivative 1 where phi > 0; identity: 1.
-    return phi == LA_PHI_ELU1 ? (f > 1.f ? 1.f : f) : phi == LA_PHI_IDENTITY ? 1.f : (f > 0.f ? 1.f : 0.f);
+// phi'(k) from phi(k): elu+1: phi = x + 1 > 1 for x > 0 (derivative 1), phi = exp(x) <= 1
+// otherwise (derivative exp(x) = phi); relu: 1 where phi > thr = 0; identity: 1 (thr = -inf,
+// so that relu and identity share one comparison).
+__device__ __forceinline__ float feat_grad_threshold(int phi) { return phi == LA_PHI_IDENTITY ? -INFINITY : 0.f; }
+__device__ __forceinline__ float feat_grad_from_feat(float f, bool elu, float thr) {
+    return elu ? fminf(f, 1.f) : (f > thr ? 1.f : 0.f);
 }
 
 // z (fp32) into column d of a z tile as the rows (z_hi, z_lo, z_hi), z = z_hi + z_lo.
@@ -440,7 +442,12 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     val[NQ + n] = j < nvalid;
                 }
                 // the Q pieces' rows r0 + n RPP, each divided by its den
-                feat8_batch_rowscale<NQ + NK, C, K::DPAD>(pp, pres, val, p.phi, dent, r0, RPP, NQ);
+                if (p.phi == LA_PHI_ELU1)
+                    feat8_batch_rowscale<LA_PHI_ELU1, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
+                else if (p.phi == LA_PHI_RELU)
+                    feat8_batch_rowscale<LA_PHI_RELU, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
+                else
+                    feat8_batch_rowscale<LA_PHI_IDENTITY, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
                 fence_proxy_async();
             }
             if (pi == 0) LA_TL(k, 2);
@@ -1007,7 +1014,12 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     pres[n] = j < C && LA_CHECK(in_smem(pp[n], 16, sm_lo, sm_hi), 422, smem_u32(pp[n]) - sm_lo, j);
                     val[n] = j < nvalid;
                 }
-                feat8_batch<NK, false>(pp, pres, val, p.phi, nullptr);
+                if (p.phi == LA_PHI_ELU1)
+                    feat8_batch<LA_PHI_ELU1, NK>(pp, pres, val);
+                else if (p.phi == LA_PHI_RELU)
+                    feat8_batch<LA_PHI_RELU, NK>(pp, pres, val);
+                else
+                    feat8_batch<LA_PHI_IDENTITY, NK>(pp, pres, val);
             }
             fence_proxy_async();
             if (pi == 0) LA_TL2(k, 2);
@@ -1019,6 +1031,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
         const int d = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         float r_prev = 0.f;   // r before the current chunk
+        const float grad_thr = feat_grad_threshold(p.phi);
         if (d < D) {
             const float *row = rstate + (size_t)d * (D + 1);
 #pragma unroll 1
@@ -1117,7 +1130,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     *reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)) =
-                        __float2bfloat16_rn(feat_grad_from_feat(fk[e], p.phi) * (v[e] + r_prev));
+                        __float2bfloat16_rn(feat_grad_from_feat(fk[e], p.phi == LA_PHI_ELU1, grad_thr) * (v[e] + r_prev));
             }
             fence_proxy_async();
             mbar_arrive_warp(&bar_dkready[s]);

@@ -46,10 +46,6 @@ __device__ __forceinline__ void warp_drain(uint64_t *bar, uint32_t parity) {
     __syncwarp();
 }
 
-__device__ __forceinline__ float feat(float x, int phi) {
-    return phi == LA_PHI_ELU1 ? (x > 0.f ? x + 1.f : __expf(x)) : phi == LA_PHI_IDENTITY ? x : fmaxf(x, 0.f);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -106,21 +102,23 @@ __device__ long long g_la_tl2[64][16];   // a second kernel of the same translat
     return a >= lo && a + bytes <= hi;
 }
 
-// phi on two bf16 values in bf16x2 arithmetic, branch-free:
-// elu(x) + 1 = max(x, 0) + exp(m), m = min(x, 0); relu(x) = max(x, 0); identity: x.
-// exp(m) = 2^y with y = m log2(e).  y is formed as yh = bf16(m * c_hi) (c_hi = log2(e)
-// rounded to bf16) plus the small remainder r = (m c_hi - yh) + m (log2(e) - c_hi), the
-// first term exact in one fused multiply-add; then 2^y = 2^yh 2^r ~ 2^yh (1 + r ln 2),
-// with 2^yh from the packed bf16 ex2 instruction.  About ten packed operations per pair;
-// at most 0.9 % relative error over bf16 x in [-12, 4].  (A float32 version with a single
-// rounding was measured: it lowers the tensor-core dq error by at most 20 % and makes the
-// long-context step 10 % slower, the feature map being on every kernel's chunk path.)
-__device__ __forceinline__ uint32_t feat_bf16x2(uint32_t u, int phi) {
-    if (phi == LA_PHI_IDENTITY) return u;
+// phi on two bf16 values in bf16x2 arithmetic, branch-free, for the feature map PHI (a
+// compile-time constant: the kernels branch on the call's phi once per chunk, outside their
+// unrolled loops, which a per-pair branch on a runtime phi slows by ~6 %): elu(x) + 1 = max(x, 0) + exp(m), m = min(x, 0); relu(x) = max(x, 0);
+// identity: x.  exp(m) = 2^y with y = m log2(e).  y is formed as yh = bf16(m * c_hi)
+// (c_hi = log2(e) rounded to bf16) plus the small remainder r = (m c_hi - yh) + m (log2(e) -
+// c_hi), the first term exact in one fused multiply-add; then 2^y = 2^yh 2^r ~ 2^yh (1 + r
+// ln 2), with 2^yh from the packed bf16 ex2 instruction.  About ten packed operations per
+// pair; at most 0.9 % relative error over bf16 x in [-12, 4].  (A float32 version with a
+// single rounding was measured: it lowers the tensor-core dq error by at most 20 % and makes
+// the long-context step 10 % slower, the feature map being on every kernel's chunk path.)
+template <int PHI>
+__device__ __forceinline__ uint32_t feat_bf16x2(uint32_t u) {
+    if (PHI == LA_PHI_IDENTITY) return u;
     __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&u);
     const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
     __nv_bfloat162 y = __hmax2(x, zero);
-    if (phi == LA_PHI_ELU1) {
+    if (PHI == LA_PHI_ELU1) {
         const __nv_bfloat162 c_hi = __float2bfloat162_rn(1.4453125f);   // bf16(log2 e)
         const __nv_bfloat162 c_lo = __float2bfloat162_rn(1.4426950408889634f - 1.4453125f);
         const __nv_bfloat162 ln2 = __float2bfloat162_rn(0.6931471805599453f);
@@ -137,31 +135,12 @@ __device__ __forceinline__ uint32_t feat_bf16x2(uint32_t u, int phi) {
     return *reinterpret_cast<uint32_t *>(&y);
 }
 
-// phi applied to 8 bf16 values in place and scaled by s (bf16x2 multiply by bf16(s)), or
-// zeros for a row past the end.
-__device__ __forceinline__ void feat8_scaled_inplace(uint8_t *chunk, bool valid, int phi, float s) {
-    uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
-    uint4 x = valid ? *ptr : make_uint4(0u, 0u, 0u, 0u);
-    if (valid) {
-        const __nv_bfloat162 s2 = __float2bfloat162_rn(s);
-        uint32_t *xi = reinterpret_cast<uint32_t *>(&x);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t f = feat_bf16x2(xi[q], phi);
-            const __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&f), s2);
-            xi[q] = *reinterpret_cast<const uint32_t *>(&y);
-        }
-    }
-    *ptr = x;
-}
-
-// phi (scaled by s[n] when SCALED) on up to NB 16-byte pieces in place (piece n exists when
-// present[n]; it becomes zeros when !valid[n], its row being past the end).  Every load is
-// issued before any store: in-place updates through computed addresses would otherwise
-// serialise, the compiler being unable to tell a later load from an earlier store's address.
-template <int NB, bool SCALED>
-__device__ __forceinline__ void feat8_batch(uint8_t *const *ptr, const bool *present, const bool *valid, int phi,
-                                            const float *s) {
+// phi on up to NB 16-byte pieces in place (piece n exists when present[n]; it becomes zeros
+// when !valid[n], its row being past the end).  Every load is issued before any store:
+// in-place updates through computed addresses would otherwise serialise, the compiler being
+// unable to tell a later load from an earlier store's address.
+template <int PHI, int NB>
+__device__ __forceinline__ void feat8_batch(uint8_t *const *ptr, const bool *present, const bool *valid) {
     uint4 x[NB];
 #pragma unroll
     for (int n = 0; n < NB; ++n)
@@ -170,17 +149,8 @@ __device__ __forceinline__ void feat8_batch(uint8_t *const *ptr, const bool *pre
     for (int n = 0; n < NB; ++n) {
         if (!(present[n] && valid[n])) continue;
         uint32_t *xi = reinterpret_cast<uint32_t *>(&x[n]);
-        __nv_bfloat162 s2;
-        if (SCALED) s2 = __float2bfloat162_rn(s[n]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint32_t f = feat_bf16x2(xi[q], phi);
-            if (SCALED) {
-                const __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&f), s2);
-                f = *reinterpret_cast<const uint32_t *>(&y);
-            }
-            xi[q] = f;
-        }
+        for (int q = 0; q < 4; ++q) xi[q] = feat_bf16x2<PHI>(xi[q]);
     }
 #pragma unroll
     for (int n = 0; n < NB; ++n)
@@ -192,9 +162,9 @@ __device__ __forceinline__ void feat8_batch(uint8_t *const *ptr, const bool *pre
 // are then divided by their row's den in float32 and rounded to bf16 once more: phi(q) / den.
 // (A bf16 multiply by bf16(1 / den) is cheaper but leaves a rounding error shared by the whole
 // row, which the h z term of dq amplifies: measured, it doubles the dq error.)
-template <int NB, int C, int DPAD>
+template <int PHI, int NB, int C, int DPAD>
 __device__ __forceinline__ void feat8_batch_rowscale(uint8_t *const *ptr, const bool *present, const bool *valid,
-                                                     int phi, const float *den_tile, int r0, int step, int nscaled) {
+                                                     const float *den_tile, int r0, int step, int nscaled) {
     uint4 x[NB];
 #pragma unroll
     for (int n = 0; n < NB; ++n)
@@ -207,7 +177,7 @@ __device__ __forceinline__ void feat8_batch_rowscale(uint8_t *const *ptr, const 
         const float sc = n < nscaled ? 1.f / den_tile[(row / C) * DPAD + row % C] : 1.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            uint32_t f = feat_bf16x2(xi[q], phi);
+            uint32_t f = feat_bf16x2<PHI>(xi[q]);
             if (n < nscaled) {
                 const float2 v = unpack_bf16x2(f);
                 f = pack_bf16x2(v.x * sc, v.y * sc);
@@ -221,14 +191,15 @@ __device__ __forceinline__ void feat8_batch_rowscale(uint8_t *const *ptr, const 
 }
 
 // phi applied to 8 bf16 values (16 bytes) in place, or zeros for a row past the end.
-__device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid, int phi) {
+template <int PHI>
+__device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid) {
     uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
     uint4 x = valid ? *ptr : make_uint4(0u, 0u, 0u, 0u);
     if (valid) {
-        x.x = feat_bf16x2(x.x, phi);
-        x.y = feat_bf16x2(x.y, phi);
-        x.z = feat_bf16x2(x.z, phi);
-        x.w = feat_bf16x2(x.w, phi);
+        x.x = feat_bf16x2<PHI>(x.x);
+        x.y = feat_bf16x2<PHI>(x.y);
+        x.z = feat_bf16x2<PHI>(x.z);
+        x.w = feat_bf16x2<PHI>(x.w);
     }
     *ptr = x;
 }
@@ -261,23 +232,6 @@ __device__ __forceinline__ void store_state_row(uint8_t *sbf, int d, const float
     for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
     *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4 *>(sbf + swz_chunk(D, d, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-// phi applied to 8 bf16 values in place (or zeros for a row past the end).
-__device__ __forceinline__ void feat8_inplace(uint8_t *chunk, bool valid, int phi) {
-    uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
-    uint4 x = *ptr, y;
-    if (valid) {
-        uint32_t *xi = reinterpret_cast<uint32_t *>(&x), *yi = reinterpret_cast<uint32_t *>(&y);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = unpack_bf16x2(xi[i]);
-            yi[i] = pack_bf16x2(feat(f.x, phi), feat(f.y, phi));
-        }
-    } else {
-        y = make_uint4(0u, 0u, 0u, 0u);
-    }
-    *ptr = y;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
