@@ -8,8 +8,15 @@
 // heads x C = 128 / G tokens), so one key/value tile serves the whole group (the gqa
 // page's head sharing, fused: no expanded k, v).
 //
-// z and the denominator also run on the tensor cores, through N = 16 products against two
-// small constant K-major tiles: ONES (row 0 all ones) and Z (row 0 = z_bf16).
+// z and the inter-chunk part of the denominator also run on the tensor cores, through N = 16
+// products against two small K-major tiles: ONES (row 0 all ones) and Z (rows 0 and 1: z
+// split into two bf16 terms, z = z_hi + z_lo, so phi(q) . z comes out as two fp32 columns
+// with the accuracy of float32).  The intra-chunk part of the denominator, the row sum of
+// mask(A), is taken twice: through the bf16 P (a product with a second ones tile whose row 2
+// is ones, landing in column D + 2), for out = O / den with the same P in numerator and
+// denominator; and in float32 by the warps that build P, which also write the den left to
+// the backward: that one must be accurate to float32 rounding (a den error is amplified
+// there by the h z term; measured, the bf16 row sum raises the dq error by 30 %).
 //
 // Forward = k_tc_state (per-segment S = phi(K)^T V, z = phi(K)^T 1) -> k_scan (exclusive
 // prefix, or total when bidirectional; CUDA cores) -> k_tc_fwd.  Per chunk of k_tc_fwd
@@ -17,7 +24,7 @@
 //   MMA1  A   = phi(Q) phi(K)^T                                [128 x C]   (causal)
 //   conv  P   = bf16(A masked j <= i)                                      (causal)
 //   MMA2  O   = phi(Q) S_bf + P V                              [128 x D]
-//         den = phi(Q) z_bf + P 1        (column D of O)       [128 x 16]
+//         den = phi(Q) z_hi + phi(Q) z_lo + P 1    (columns D, D + 1, D + 2)
 //   epi   out = O / (den + eps)  -> staged in shared memory -> TMA store; den + eps per row
 //         to the workspace (the backward's dq kernel reads it)
 //   MMA3  S  += phi(K)^T V,  z += phi(K)^T 1                              (causal)
@@ -51,7 +58,7 @@ struct FwdCfg {
     static constexpr int Z_BYTES = DB * 16 * 128;      // z_bf: 16 rows x D columns, K-major
     static constexpr int ONES_BYTES = CB * 16 * 128;   // ones: 16 rows x C columns, K-major
     static constexpr int OUT_BYTES = 128 * 128;        // output staging: 128 rows x 64 columns
-    static constexpr int FIXED = P_BYTES + S_BYTES + Z_BYTES + ONES_BYTES + OUT_BYTES + 1024;
+    static constexpr int FIXED = P_BYTES + S_BYTES + Z_BYTES + 2 * ONES_BYTES + OUT_BYTES + 1024;
     static constexpr int NS = (kSmemLimit - 1024 - FIXED) / STAGE > 4 ? 4 : (kSmemLimit - 1024 - FIXED) / STAGE;
     static constexpr int SMEM = NS * STAGE + FIXED;
     static_assert(NS >= 2, "not enough shared memory for two stages");
@@ -275,7 +282,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
     uint8_t *sbf = pbuf + K::P_BYTES;
     uint8_t *ztile = sbf + K::S_BYTES;
     uint8_t *ones = ztile + K::Z_BYTES;
-    uint8_t *obuf = ones + K::ONES_BYTES;
+    uint8_t *ones2 = ones + K::ONES_BYTES;   // row 2 = 1: P 1 into column D + 2
+    uint8_t *obuf = ones2 + K::ONES_BYTES;
 
     const int warp = threadIdx.x / 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
@@ -293,8 +301,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                                     (int)reinterpret_cast<uintptr_t>(p.k), (int)reinterpret_cast<uintptr_t>(p.v)};
         for (int w = 0; w < kHdrWords; ++w) p.hdr[w] = rec[w];
     }
-    // constant tiles: ones (row 0 = 1 over C columns) and the zero rows of the z tile
+    // constant tiles: ones (row 0 = 1 over C columns), ones2 (row 2 = 1) and the zero rows of
+    // the z tile
     fill_ones_tile(ones, C);
+    fill_ones_tile(ones2, C, 2);
     for (int idx = threadIdx.x; idx < K::Z_BYTES / 16; idx += blockDim.x)
         reinterpret_cast<uint4 *>(ztile)[idx] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async();
@@ -364,7 +374,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             constexpr uint32_t idDen = idesc_bf16(128, 16, false, false);
             constexpr uint32_t idS = idesc_bf16(128, D, true, true);
             constexpr uint32_t idZ = idesc_bf16(128, 16, true, false);
-            const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf), zt = smem_u32(ztile), on = smem_u32(ones);
+            const uint32_t sbf_u = smem_u32(sbf), pb = smem_u32(pbuf), zt = smem_u32(ztile), on = smem_u32(ones),
+                           on2 = smem_u32(ones2);
             // A for chunk k (causal), into the single A buffer once chunk k - 1's P has been read
             auto issue_a = [&](int k) -> bool {
                 const int s = k % NS;
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                     // O += P V, den += P 1 (within the chunk)
                     for (int kk = 0; kk < C / 16; ++kk) {
                         mma_bf16_w(tO, desc_kmajor(pb, 128, 0, kk), desc_mnmajor(vs, C, 0, kk), idO, 1u);
-                        mma_bf16_w(tO + D, desc_kmajor(pb, 128, 0, kk), desc_kmajor(on, 16, 0, kk), idDen, 1u);
+                        mma_bf16_w(tO + D, desc_kmajor(pb, 128, 0, kk), desc_kmajor(on2, 16, 0, kk), idDen, 1u);
                     }
                 }
                 mma_commit_w(&bar_ofull[o]);
@@ -490,17 +501,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 tmem_st16(tS + lane_off + D, zv);
                 tmem_st_wait();
             }
-            *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zv[0]);
+            store_z_split(ztile, i, zv[0]);
         }
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive_warp(&bar_sbf);
         if (CAUSAL) {
             bool ok = true;
+            float rs_cur = 0.f;   // fp32 row sum of mask(A) of the chunk last converted
             auto p_conv = [&](int k) {
                 ok = ok && warp_wait(&bar_afull, k & 1, &abort_flag);
                 tc_fence_after();
                 if (i == 0) LA_TL(k, 8);
+                float rs = 0.f;
                 if (ok) {
 #pragma unroll
                     for (int c32 = 0; c32 < (C + 31) / 32; ++c32) {
@@ -514,11 +527,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
 #pragma unroll
                         for (int h = 0; h < (C >= 32 ? 2 : 1); ++h) {
                             uint32_t w[8];
+                            float pair[8];
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 const int j = c32 * 32 + h * 16 + e;
-                                w[e / 2] = pack_bf16x2((j <= ti) ? v[h * 16 + e] : 0.f, (j + 1 <= ti) ? v[h * 16 + e + 1] : 0.f);
+                                const float a0 = (j <= ti) ? v[h * 16 + e] : 0.f, a1 = (j + 1 <= ti) ? v[h * 16 + e + 1] : 0.f;
+                                pair[e / 2] = a0 + a1;
+                                w[e / 2] = pack_bf16x2(a0, a1);
                             }
+                            rs += ((pair[0] + pair[1]) + (pair[2] + pair[3])) + ((pair[4] + pair[5]) + (pair[6] + pair[7]));
                             const int c16 = c32 * 2 + h;
                             uint8_t *p0 = pbuf + swz_chunk(128, i, 2 * c16), *p1 = pbuf + swz_chunk(128, i, 2 * c16 + 1);
                             if (LA_CHECK(in_smem(p0, 16, sm_lo, sm_hi) && in_smem(p1, 16, sm_lo, sm_hi), 241,
@@ -530,9 +547,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                     }
                     fence_proxy_async();
                 }
+                rs_cur = rs;
                 tc_fence_before();
                 if (i == 0) LA_TL(k, 9);
                 mbar_arrive_warp(&bar_pready);
+            };
+            // the backward's den of chunk k: phi(q) . z (columns D, D + 1 of chunk k's O buffer,
+            // read once its products are done and before this warpgroup's next state conversion
+            // lets chunk k + 2 reuse the buffer) plus this thread's fp32 row sum of mask(A)
+            auto write_den = [&](int k, float rsum) {
+                float dz[2] = {0.f, 0.f};
+                if (ok) {
+                    tmem_ld2((k % NO ? tO1 : tO0) + lane_off + D, dz);
+                    tmem_wait_regs<2>(dz);
+                }
+                const int t = t0 + k * C + ti;
+                if (ok && p.den && t < t1) p.den[(size_t)(bh0 + i / C) * p.den_stride + t] = (dz[0] + dz[1]) + rsum + p.eps;
             };
             if (nchunk > 0) p_conv(0);
             for (int k = 0; k < nchunk; ++k) {
@@ -541,18 +571,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 tc_fence_after();
                 if (i == 0) LA_TL(k, 10);
                 if (ok && wq * 32 < D) {
+#pragma unroll 1
+                    for (int c32 = 0; c32 < D / 32; ++c32) {
+                        float v[32];
+                        tmem_ld32(tS + lane_off + c32 * 32, v);
+                        tmem_wait_regs<32>(v);
 #pragma unroll
-                    for (int c64 = 0; c64 < D / 64; ++c64) {
-                        float v[64];
-                        tmem_ld32(tS + lane_off + c64 * 64, v);
-                        tmem_ld32(tS + lane_off + c64 * 64 + 32, v + 32);
-                        tmem_wait_regs<64>(v);
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) store_state_row<D>(sbf, i, v + 16 * h, c64 * 4 + h);
+                        for (int h = 0; h < 2; ++h) store_state_row<D>(sbf, i, v + 16 * h, c32 * 2 + h);
                     }
                     float zd = tmem_ld1(tS + lane_off + D);
                     tmem_wait_regs<1>(&zd);
-                    *reinterpret_cast<__nv_bfloat16 *>(ztile + swz_offset(16, 0, i)) = __float2bfloat16_rn(zd);
+                    store_z_split(ztile, i, zd);
                 }
                 fence_proxy_async();
                 tc_fence_before();
@@ -560,8 +589,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 mbar_arrive_warp(&bar_sbf);
                 if (k + 1 < nchunk) {
                     ok = ok && warp_wait(&bar_ofull[k % NO], (k / NO) & 1, &abort_flag);
+                    tc_fence_after();
+                    write_den(k, rs_cur);
                     p_conv(k + 1);
                 }
+            }
+            if (nchunk > 0) {
+                ok = ok && warp_wait(&bar_ofull[(nchunk - 1) % NO], ((nchunk - 1) / NO) & 1, &abort_flag);
+                tc_fence_after();
+                write_den(nchunk - 1, rs_cur);
             }
         }
     } else if (warp >= 12 && warp < 16) {
@@ -578,14 +614,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             ok = ok && warp_wait(&bar_ofull[o], (k / NO) & 1, &abort_flag);
             tc_fence_after();
             if (i == 0) LA_TL(k, 12);
-            float den = 0.f;
+            float den = 0.f, dzz = 0.f;   // dzz = phi(q) . z (hi + lo)
             if (ok) {
-                den = tmem_ld1(tO + lane_off + D);
-                tmem_wait_regs<1>(&den);
+                float dz[4];   // phi(q) . z_hi, phi(q) . z_lo, P 1 (bf16 P), unused
+                tmem_ld4(tO + lane_off + D, dz);
+                tmem_wait_regs<4>(dz);
+                dzz = dz[0] + dz[1];
+                den = dzz + dz[2];
+                // bidirectional: the backward's den (causal: written by the P conversion warps)
+                if (!CAUSAL && p.den && c0 + i % C < t1)
+                    p.den[(size_t)(bh0 + i / C) * p.den_stride + c0 + i % C] = den + p.eps;
             }
             const float inv = 1.f / (den + p.eps);
-            if (ok && p.den && c0 + i % C < t1)
-                p.den[(size_t)(bh0 + i / C) * p.den_stride + c0 + i % C] = den + p.eps;
 #pragma unroll 1
             for (int c64 = 0; c64 < D / 64; ++c64) {
                 float v[32];   // 32 columns at a time

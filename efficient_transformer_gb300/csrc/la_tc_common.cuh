@@ -206,13 +206,23 @@ __device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid) {
 
 __host__ __device__ constexpr int align32(int x) { return (x + 31) / 32 * 32; }
 
-// A 16-row K-major tile with `cols` columns: row 0 = 1 for columns < cols, zero elsewhere.
-__device__ __forceinline__ void fill_ones_tile(uint8_t *t, int cols) {
+// z (fp32) into column d of a 16-row K-major z tile as rows 0 and 1: z_hi = bf16(z) and
+// z_lo = bf16(z - z_hi), so that a product with the tile gives phi . z_hi and phi . z_lo in two
+// fp32 columns whose sum carries z to about 16 bits.
+__device__ __forceinline__ void store_z_split(uint8_t *zt, int d, float z) {
+    const __nv_bfloat16 zh = __float2bfloat16_rn(z);
+    *reinterpret_cast<__nv_bfloat16 *>(zt + swz_offset(16, 0, d)) = zh;
+    *reinterpret_cast<__nv_bfloat16 *>(zt + swz_offset(16, 1, d)) = __float2bfloat16_rn(z - __bfloat162float(zh));
+}
+
+// A 16-row K-major tile with `cols` columns: row `one_row` = 1 for columns < cols, zero
+// elsewhere.
+__device__ __forceinline__ void fill_ones_tile(uint8_t *t, int cols, int one_row = 0) {
     const int nblk = (cols + 63) / 64;
     for (int idx = threadIdx.x; idx < nblk * 16 * 8; idx += blockDim.x) {
         const int blk = idx / 128, rc = idx % 128, row = rc / 8, c = rc % 8;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row == 0) {
+        if (row == one_row) {
             const int col0 = blk * 64 + c * 8;
             uint32_t w[4];
 #pragma unroll

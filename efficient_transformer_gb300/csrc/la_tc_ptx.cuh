@@ -428,6 +428,18 @@ __device__ __forceinline__ void tmem_ld2(uint32_t taddr, float *v) {
     v[1] = __uint_as_float(r1);
 }
 
+// Warp-wide: thread t gets TMEM lane (lane of taddr) + t, four consecutive columns.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float *v) {
+    uint32_t r0, r1, r2, r3;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(taddr));
+    v[0] = __uint_as_float(r0);
+    v[1] = __uint_as_float(r1);
+    v[2] = __uint_as_float(r2);
+    v[3] = __uint_as_float(r3);
+}
+
 // Warp-wide: thread t gets TMEM lane (lane of taddr) + t, 32 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
     uint32_t r[32];
