@@ -78,7 +78,7 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
     const int bg = B * Hkv;
     int slots;   // CTAs that run at once on kPlanSms SMs
     if (pl.path == LA_PATH_TCGEN05) {
-        pl.chunk = tc_chunk(Hq / Hkv);
+        pl.chunk = tc_chunk(Hq / Hkv, D);
         slots = kPlanSms;                            // one CTA per SM (shared memory bound)
     } else {
         pl.chunk = 16;

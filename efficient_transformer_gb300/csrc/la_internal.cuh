@@ -123,7 +123,7 @@ cudaError_t simt_backward(const Params &p, la_dtype dt, cudaStream_t s);
 cudaError_t tc_forward(const Params &p, cudaStream_t s);
 cudaError_t tc_backward(const Params &p, cudaStream_t s);
 bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal, int is_bwd);
-int tc_chunk(int n_rep);   // tokens per chunk of the tensor-core kernels
+int tc_chunk(int n_rep, int D);   // tokens per chunk of the tensor-core forward (the plan's chunk)
 bool tc_bwd_supported(int n_rep, int D);
 cudaError_t tc_launch_state(const Params &p, cudaStream_t s);   // per-segment (S, z) on tensor cores
 

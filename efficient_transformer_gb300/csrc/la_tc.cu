@@ -103,16 +103,18 @@ __device__ __forceinline__ void state_feature_map(uint8_t *kt, int i, int c0, in
 }
 
 // The forward's feature map over one stage: 16-byte piece `offq` of Q rows r0, r0 + RPP, ...
-// (valid while row % C < nvalid) and, causal, piece `kpiece` of K rows r0, r0 + RPP, ...
+// (valid while row < qrows, the rows of the group's real heads, and row % C < nvalid; the
+// other rows become zeros) and, causal, piece `kpiece` of K rows r0, r0 + RPP, ...
 template <int PHI, int C, int RPP, bool CAUSAL>
 __device__ __forceinline__ void fwd_feature_map(uint8_t *st, uint32_t offq, uint8_t *kpiece, int r0, int nvalid,
-                                                uint32_t sm_lo, uint32_t sm_hi) {
+                                                int qrows, uint32_t sm_lo, uint32_t sm_hi) {
     (void)sm_lo;
     (void)sm_hi;
 #pragma unroll 4
     for (int row = r0; row < 128; row += RPP) {
         uint8_t *ch = st + offq + row * 128;
-        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, row)) feat8_inplace2<PHI>(ch, row % C < nvalid);
+        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, row))
+            feat8_inplace2<PHI>(ch, row < qrows && row % C < nvalid);
     }
     if (CAUSAL)
         for (int j = r0; j < C; j += RPP) {
@@ -259,8 +261,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------------------
-// Chunked forward (see the file comment for the per-chunk steps and warp roles).
-template <int D, int G, bool CAUSAL>
+// Chunked forward (see the file comment for the per-chunk steps and warp roles).  MASK: the
+// group has fewer heads (n_rep) than the tile's G, and the rows past them are masked.
+template <int D, int G, bool CAUSAL, bool MASK>
 __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant__ CUtensorMap map_q,
                                                            const __grid_constant__ CUtensorMap map_k,
                                                            const __grid_constant__ CUtensorMap map_v,
@@ -290,7 +293,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int t0 = seg * p.seg_len, t1 = min(p.N, t0 + p.seg_len);
     const int nchunk = (t1 - t0 + C - 1) / C;
-    const int bh0 = b * p.Hq + g * G;
+    // the group's gr = n_rep heads fill rows [0, gr C) of the G C = 128 MMA rows; with gr < G
+    // (a group smaller than the tile's) the other rows stay zero and nothing is stored for them
+    const int gr = MASK ? p.n_rep : G;
+    const int bh0 = b * p.Hq + g * gr;
     const float *state = p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
 
     // the record of this call, checked by a backward that takes this workspace's states and dens
@@ -339,19 +345,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
     if (warp == 0) {
         // ---------------- TMA producer
         {   // the whole warp, one lane issuing
-            constexpr uint32_t bytes = CAUSAL ? K::STAGE : K::Q_BYTES;
+            const uint32_t bytes = (uint32_t)(gr * C * D * 2) + (CAUSAL ? (uint32_t)(K::K_BYTES + K::V_BYTES) : 0u);
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 if (k >= NS && !warp_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
-                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N && bh0 + G <= p.B * p.Hq, 201,
+                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N && gr <= G && bh0 + gr <= p.B * p.Hq, 201,
                               smem_u32(st) - sm_lo, c0))
                     break;
                 LA_TL(k, 0);
                 mbar_arrive_expect_tx_w(&bar_full[s], bytes);
-                for (int r = 0; r < G; ++r)
+                for (int r = 0; r < gr; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_full[s], blk * 64, c0, bh0 + r);
                 if (CAUSAL)
@@ -458,12 +464,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int nvalid = t1 - (t0 + k * C);
                 if (p.phi == LA_PHI_ELU1)
-                    fwd_feature_map<LA_PHI_ELU1, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, sm_lo, sm_hi);
+                    fwd_feature_map<LA_PHI_ELU1, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C, sm_lo,
+                                                                 sm_hi);
                 else if (p.phi == LA_PHI_RELU)
-                    fwd_feature_map<LA_PHI_RELU, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, sm_lo, sm_hi);
+                    fwd_feature_map<LA_PHI_RELU, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C, sm_lo,
+                                                                 sm_hi);
                 else
-                    fwd_feature_map<LA_PHI_IDENTITY, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, sm_lo,
-                                                                     sm_hi);
+                    fwd_feature_map<LA_PHI_IDENTITY, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C,
+                                                                     sm_lo, sm_hi);
                 fence_proxy_async();
             }
             if (i == 0) LA_TL(k, 2);
@@ -562,7 +570,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                     tmem_wait_regs<2>(dz);
                 }
                 const int t = t0 + k * C + ti;
-                if (ok && p.den && t < t1) p.den[(size_t)(bh0 + i / C) * p.den_stride + t] = (dz[0] + dz[1]) + rsum + p.eps;
+                if (ok && p.den && t < t1 && i / C < gr)
+                    p.den[(size_t)(bh0 + i / C) * p.den_stride + t] = (dz[0] + dz[1]) + rsum + p.eps;
             };
             if (nchunk > 0) p_conv(0);
             for (int k = 0; k < nchunk; ++k) {
@@ -622,7 +631,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 dzz = dz[0] + dz[1];
                 den = dzz + dz[2];
                 // bidirectional: the backward's den (causal: written by the P conversion warps)
-                if (!CAUSAL && p.den && c0 + i % C < t1)
+                if (!CAUSAL && p.den && c0 + i % C < t1 && i / C < gr)
                     p.den[(size_t)(bh0 + i / C) * p.den_stride + c0 + i % C] = den + p.eps;
             }
             const float inv = 1.f / (den + p.eps);
@@ -659,7 +668,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 fence_proxy_async();
                 named_barrier(2, 128);
                 if (i < 32 && ok) {   // the first warp, lane 0 issuing
-                    for (int r = 0; r < G; ++r) tma_store_3d_w(&map_o, obuf + r * C * 128, c64 * 64, c0, bh0 + r);
+                    for (int r = 0; r < gr; ++r) tma_store_3d_w(&map_o, obuf + r * C * 128, c64 * 64, c0, bh0 + r);
                     bulk_commit();
                 }
             }
@@ -690,7 +699,7 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int D, int G, bool CAUSAL>
+template <int D, int G, bool CAUSAL, bool MASK>
 cudaError_t launch_fwd(const Params &p, cudaStream_t s) {
     using K = FwdCfg<D, G>;
     CUtensorMap mq{}, mk{}, mv{}, mo{};
@@ -698,14 +707,14 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t s) {
     if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mo, p.out, p.B * p.Hq, p.N, D, K::C);
-    if (e == cudaSuccess) e = prepare(k_tc_fwd<D, G, CAUSAL>, K::SMEM);
+    if (e == cudaSuccess) e = prepare(k_tc_fwd<D, G, CAUSAL, MASK>, K::SMEM);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_fwd_causal" : "tc_fwd_bidir", s);
-    k_tc_fwd<D, G, CAUSAL><<<p.B * p.Hkv * p.nseg, kFwdThreads, K::SMEM, s>>>(mq, mk, mv, mo, p);
+    k_tc_fwd<D, G, CAUSAL, MASK><<<p.B * p.Hkv * p.nseg, kFwdThreads, K::SMEM, s>>>(mq, mk, mv, mo, p);
     return cudaGetLastError();
 }
 
-template <int D, int G>
+template <int D, int G, bool MASK = false>
 cudaError_t forward_dg(const Params &p, cudaStream_t s) {
     cudaError_t e = launch_state<D>(p, s);
 #ifdef LA_DEBUG
@@ -718,15 +727,15 @@ cudaError_t forward_dg(const Params &p, cudaStream_t s) {
     if (stop && stop[0] == 's' && stop[1] == 'c') return e;      // "scan"
 #endif
     if (e != cudaSuccess) return e;
-    return p.causal ? launch_fwd<D, G, true>(p, s) : launch_fwd<D, G, false>(p, s);
+    return p.causal ? launch_fwd<D, G, true, MASK>(p, s) : launch_fwd<D, G, false, MASK>(p, s);
 }
 
 template <int D>
 cudaError_t forward_d(const Params &p, cudaStream_t s) {
     switch (p.n_rep) {
-        case 1:
+        case 1:   // D = 128: the n_rep = 2 tiles with half the rows masked (see k_tc_fwd)
             if constexpr (D == 64) return forward_dg<D, 1>(p, s);
-            return cudaErrorNotSupported;
+            else return forward_dg<D, 2, true>(p, s);
         case 2: return forward_dg<D, 2>(p, s);
         case 4: return forward_dg<D, 4>(p, s);
         case 8: return forward_dg<D, 8>(p, s);
@@ -736,7 +745,9 @@ cudaError_t forward_d(const Params &p, cudaStream_t s) {
 
 }  // namespace
 
-int tc_chunk(int n_rep) { return 128 / n_rep; }
+// Tokens per chunk of the forward's tiles (the plan's chunk): 128 / n_rep, except for D = 128
+// with n_rep = 1, whose one head takes half of the n_rep = 2 tiles.
+int tc_chunk(int n_rep, int D) { return D == 128 && n_rep == 1 ? 64 : 128 / n_rep; }
 
 bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal, int is_bwd) {
     (void)N;
@@ -744,9 +755,7 @@ bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal,
     if (dt != LA_BF16 || P != 1) return false;
     const int n_rep = Hq / Hkv;
     if (is_bwd) return tc_bwd_supported(n_rep, D);
-    if (D == 128) return n_rep == 2 || n_rep == 4 || n_rep == 8;
-    if (D == 64) return n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8;
-    return false;
+    return (D == 64 || D == 128) && (n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8);
 }
 
 cudaError_t tc_forward(const Params &p, cudaStream_t s) {

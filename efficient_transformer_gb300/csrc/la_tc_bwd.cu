@@ -148,7 +148,8 @@ __device__ __forceinline__ uint4 dq_piece(uint4 u, const float *x, float inv) {
 }
 
 // ---------------------------------------------------------------------------------------
-template <int D, int G, bool CAUSAL>
+// MASK: the group has fewer heads (n_rep) than the tile's G; the rows past them are masked.
+template <int D, int G, bool CAUSAL, bool MASK>
 __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_constant__ CUtensorMap map_q,
                                                               const __grid_constant__ CUtensorMap map_k,
                                                               const __grid_constant__ CUtensorMap map_v,
@@ -187,7 +188,12 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int t0 = seg * p.seg_len, t1 = min(p.N, t0 + p.seg_len);
     const int nchunk = (t1 - t0 + C - 1) / C;
-    const int bh0 = b * p.Hq + g * G;
+    // the group's gr = n_rep heads fill rows [0, gr C) of the 128 MMA rows; with gr < G the
+    // other rows are masked: their phi_s rows are zeros (feature map), their g rows zeros
+    // (cleared here, never loaded, and the dq epilogue writes zeros back), so every product
+    // over them adds nothing, and nothing is stored for them
+    const int gr = MASK ? p.n_rep : G;
+    const int bh0 = b * p.Hq + g * gr;
     const size_t seg_state = ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
     const float *state = p.state + seg_state;
     float *rstate = p.rstate + seg_state;
@@ -196,6 +202,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     for (int idx = threadIdx.x; idx < (2 * K::Z_BYTES + K::H_BYTES) / 16; idx += blockDim.x) {
         uint8_t *t = idx < 2 * K::Z_BYTES / 16 ? ztile + idx * 16 : htile + (idx - 2 * K::Z_BYTES / 16) * 16;
         *reinterpret_cast<uint4 *>(t) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if constexpr (MASK) {
+        if (gr < G) {   // the masked g rows of every stage: NS stages x DB blocks x (128 - gr C) rows
+            const int mrows = 128 - gr * C;
+            for (int idx = threadIdx.x; idx < NS * K::DB * mrows * 8; idx += blockDim.x) {
+                const int row = gr * C + (idx / 8) % mrows, blk = (idx / (8 * mrows)) % K::DB, s = idx / (8 * mrows * K::DB);
+                *reinterpret_cast<uint4 *>(stage0 + s * STAGE + OFF_G + blk * 128 * 128 + row * 128 + (idx % 8) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
     }
     fence_proxy_async();
     if (threadIdx.x == 0) {
@@ -244,15 +260,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         // ---------------- TMA producer: K, Q, V and the rows' den (what the feature map and the
         // first products need) on one barrier, grad_out on another
         {   // the whole warp, one lane issuing
-            constexpr uint32_t bytes_a = (CAUSAL ? K::Q_BYTES + K::K_BYTES + K::V_BYTES : K::Q_BYTES) + G * C * 4;
-            constexpr uint32_t bytes_g = K::G_BYTES;
+            const uint32_t bytes_a = (uint32_t)(gr * C * D * 2 + gr * C * 4) +
+                                     (CAUSAL ? (uint32_t)(K::K_BYTES + K::V_BYTES) : 0u);
+            const uint32_t bytes_g = (uint32_t)(gr * C * D * 2);
             int issued = 0;
             for (int k = 0; k < nchunk; ++k) {
                 const int s = k % NS;
                 if (k >= NS && !warp_wait(&bar_empty[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 uint8_t *st = stage0 + s * STAGE;
                 const int c0 = t0 + k * C;
-                if (!LA_CHECK(in_smem(st, STAGE, sm_lo, sm_hi) && c0 < p.N && bh0 + G <= p.B * p.Hq, 301,
+                if (!LA_CHECK(in_smem(st, STAGE, sm_lo, sm_hi) && c0 < p.N && gr <= G && bh0 + gr <= p.B * p.Hq, 301,
                               smem_u32(st) - sm_lo, c0))
                     break;
                 LA_TL(k, 0);
@@ -260,7 +277,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d_w(st + OFF_K + blk * C * 128, &map_k, &bar_fulla[s], blk * 64, c0, bg);
-                for (int r = 0; r < G; ++r) {
+                for (int r = 0; r < gr; ++r) {
                     tma_load_2d_w(st + OFF_DEN + r * K::DPAD * 4, &map_den, &bar_fulla[s], c0, bh0 + r);
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fulla[s], blk * 64, c0, bh0 + r);
@@ -269,7 +286,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fulla[s], blk * 64, c0, bg);
                 mbar_arrive_expect_tx_w(&bar_fullg[s], bytes_g);
-                for (int r = 0; r < G; ++r)
+                for (int r = 0; r < gr; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
                         tma_load_3d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64, c0,
                                       bh0 + r);
@@ -373,7 +390,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 if (CAUSAL) {
                     ok = warp_wait(&bar_ready[s], (k / NS) & 1, &abort_flag);
                     if (ok) {
-                        for (int r = 0; r < G; ++r)
+                        for (int r = 0; r < gr; ++r)
                             for (int blk = 0; blk < K::DB; ++blk)
                                 tma_store_3d_w(&map_ps, st + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
                         bulk_commit();
@@ -387,7 +404,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     if (hh == 0) LA_TL(k, 13);
                     if (K::DB == 2 || hh == 1) {
                         const int blk = K::DB == 2 ? hh : 0;
-                        for (int r = 0; r < G; ++r)
+                        for (int r = 0; r < gr; ++r)
                             tma_store_3d_w(&map_dq, st + OFF_G + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
                     }
                 }
@@ -432,7 +449,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     const int row = r0 + n * RPP;
                     pp[n] = st + offq + row * 128;
                     pres[n] = row < 128 && LA_CHECK(in_smem(pp[n], 16, sm_lo, sm_hi), 321, smem_u32(pp[n]) - sm_lo, row);
-                    val[n] = row % C < nvalid;
+                    val[n] = row < gr * C && row % C < nvalid;
                 }
 #pragma unroll
                 for (int n = 0; n < NK; ++n) {
@@ -519,7 +536,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         for (int k = 0; k < nchunk; ++k) {
             const int s = k % NS;
             const int t = t0 + k * C + ti;
-            const bool valid = t < t1;
+            const bool valid = t < t1 && r < gr;
             uint8_t *st = stage0 + s * STAGE;
             // ---- row work: with phi_s = phi(q) / den and A_s = phi_s phi(K)^T,
             // g . num / den = phi_s . X + sum_j mask(A_s) dA';  h = -(g . num) / den;
@@ -566,7 +583,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     }
                 }
                 xch[h * 128 + i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-                inv = 1.f / reinterpret_cast<const float *>(st + OFF_DEN)[r * K::DPAD + ti];
+                // (masked rows: 0, so that their dq is zeros, which keeps their g rows zero)
+                inv = r < gr ? 1.f / reinterpret_cast<const float *>(st + OFF_DEN)[r * K::DPAD + ti] : 0.f;
             }
             named_barrier(3, 256);
             if (ok) {
@@ -667,7 +685,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
 }
 
 // ---------------------------------------------------------------------------------------
-template <int D, int G, bool CAUSAL>
+template <int D, int G, bool CAUSAL, bool MASK>
 __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_constant__ CUtensorMap map_q,
                                                                 const __grid_constant__ CUtensorMap map_k,
                                                                 const __grid_constant__ CUtensorMap map_v,
@@ -704,12 +722,26 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int t0 = seg * p.seg_len, t1 = min(p.N, t0 + p.seg_len);
     const int nchunk = (t1 - t0 + C - 1) / C;
-    const int bh0 = b * p.Hq + g * G;
+    // rows of masked heads (gr < G; see k_tc_bwd_dq): zero phi_s and g rows, never loaded, and
+    // a zero h, so that they add nothing to dk, dv, R or r
+    const int gr = MASK ? p.n_rep : G;
+    const int bh0 = b * p.Hq + g * gr;
     const float *rstate = p.rstate + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
 
     for (int idx = threadIdx.x; idx < (K::P_BYTES + (K::H_IN_DP ? 0 : K::H_BYTES)) / 16; idx += blockDim.x) {
         uint8_t *t = idx < K::P_BYTES / 16 ? dpbuf + idx * 16 : htile + (idx - K::P_BYTES / 16) * 16;
         *reinterpret_cast<uint4 *>(t) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if constexpr (MASK) {
+        if (gr < G) {   // NS stages x {phi_s, g} x DB blocks x (128 - gr C) rows
+            const int mrows = 128 - gr * C;
+            for (int idx = threadIdx.x; idx < NS * 2 * K::DB * mrows * 8; idx += blockDim.x) {
+                const int row = gr * C + (idx / 8) % mrows, blk = (idx / (8 * mrows)) % K::DB;
+                const int which = (idx / (8 * mrows * K::DB)) % 2, s = idx / (8 * mrows * K::DB * 2);
+                *reinterpret_cast<uint4 *>(stage0 + s * K::STAGE + (which ? OFF_G : 0) + blk * 128 * 128 + row * 128 +
+                                           (idx % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
     }
     fence_proxy_async();
     if (threadIdx.x == 0) {
@@ -765,17 +797,19 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                 const int s = k % NS;
                 uint8_t *st = stage0 + s * K::STAGE;
                 const int c0 = t0 + (nchunk - 1 - k) * C;
-                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N, 401, smem_u32(st) - sm_lo, c0)) break;
+                if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N && gr <= G && bh0 + gr <= p.B * p.Hq, 401,
+                              smem_u32(st) - sm_lo, c0))
+                    break;
                 if (CAUSAL && k >= NS && !warp_wait(&bar_emptyqg[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 LA_TL2(k, 0);
                 if (CAUSAL) {
-                    mbar_arrive_expect_tx_w(&bar_fullq[s], K::Q_BYTES);
-                    for (int r = 0; r < G; ++r)
+                    mbar_arrive_expect_tx_w(&bar_fullq[s], (uint32_t)(gr * C * D * 2));
+                    for (int r = 0; r < gr; ++r)
                         for (int blk = 0; blk < K::DB; ++blk)
                             tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fullq[s], blk * 64, c0,
                                         bh0 + r);
-                    mbar_arrive_expect_tx_w(&bar_fullg[s], K::G_BYTES);
-                    for (int r = 0; r < G; ++r)
+                    mbar_arrive_expect_tx_w(&bar_fullg[s], (uint32_t)(gr * C * D * 2));
+                    for (int r = 0; r < gr; ++r)
                         for (int blk = 0; blk < K::DB; ++blk)
                             tma_load_3d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64,
                                         c0, bh0 + r);
@@ -1170,7 +1204,8 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
         float hv = 0.f;   // h of this thread's row in chunk k, loaded one step ahead
         if (CAUSAL && nchunk > 0) {
             const int t = t0 + (nchunk - 1) * C + ti;
-            if (t < t1 && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 434, bh, t)) hv = p.gd[(size_t)bh * p.N + t];
+            if (t < t1 && i / C < gr && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 434, bh, t))
+                hv = p.gd[(size_t)bh * p.N + t];
         }
         for (int k = 0; k < nchunk && CAUSAL; ++k) {
             // P'^T = mask(A_s)^T, dP' = mask(dA' + h) for chunk k, and h (split) for the r part,
@@ -1186,7 +1221,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             float hnext = 0.f;
             if (k + 1 < nchunk) {
                 const int tn = t0 + (nchunk - 2 - k) * C + ti;
-                if (tn < t1 && LA_CHECK((size_t)bh * p.N + tn < (size_t)p.B * p.Hq * p.N, 435, bh, tn))
+                if (tn < t1 && i / C < gr && LA_CHECK((size_t)bh * p.N + tn < (size_t)p.B * p.Hq * p.N, 435, bh, tn))
                     hnext = p.gd[(size_t)bh * p.N + tn];
             }
             if (ok && wgb) {
@@ -1248,7 +1283,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
 // ---------------------------------------------------------------------------------------
 // Host side
 
-template <int D, int G, bool CAUSAL>
+template <int D, int G, bool CAUSAL, bool MASK>
 cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     using K = BwdCfg<D, G>;
     CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{}, mps{}, mden{};
@@ -1262,24 +1297,24 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     if (e == cudaSuccess) e = make_map(&mdq, p.dq, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mdk, p.dk, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mdv, p.dv, p.B * p.Hkv, p.N, D, K::C);
-    if (e == cudaSuccess) e = prepare(k_tc_bwd_dq<D, G, CAUSAL>, K::DQ_SMEM);
-    if (e == cudaSuccess) e = prepare(k_tc_bwd_dkdv<D, G, CAUSAL>, K::DKDV_SMEM);
+    if (e == cudaSuccess) e = prepare(k_tc_bwd_dq<D, G, CAUSAL, MASK>, K::DQ_SMEM);
+    if (e == cudaSuccess) e = prepare(k_tc_bwd_dkdv<D, G, CAUSAL, MASK>, K::DKDV_SMEM);
     if (e != cudaSuccess) return e;
     const int grid = p.B * p.Hkv * p.nseg;
     {
         TraceScope ts(CAUSAL ? "tc_bwd_dq_causal" : "tc_bwd_dq_bidir", s);
-        k_tc_bwd_dq<D, G, CAUSAL><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, mps, mden, p);
+        k_tc_bwd_dq<D, G, CAUSAL, MASK><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, mps, mden, p);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess)
         e = scan_segments(p.rstate, p, CAUSAL ? kScanSuffix : kScanTotal, (size_t)D * (D + 1), s);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_bwd_dkdv_causal" : "tc_bwd_dkdv_bidir", s);
-    k_tc_bwd_dkdv<D, G, CAUSAL><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mps, mk, mv, mg, mdk, mdv, p);
+    k_tc_bwd_dkdv<D, G, CAUSAL, MASK><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mps, mk, mv, mg, mdk, mdv, p);
     return cudaGetLastError();
 }
 
-template <int D, int G>
+template <int D, int G, bool MASK = false>
 cudaError_t backward_dg(const Params &p, cudaStream_t s) {
     if constexpr (!BwdCfg<D, G>::FITS || !BwdCfg<D, G>::TMEM_FITS) {
         return cudaErrorNotSupported;
@@ -1292,15 +1327,19 @@ cudaError_t backward_dg(const Params &p, cudaStream_t s) {
             cudaError_t e = tc_forward(pf, s);
             if (e != cudaSuccess) return e;
         }
-        return p.causal ? launch_bwd_kernels<D, G, true>(p, s) : launch_bwd_kernels<D, G, false>(p, s);
+        return p.causal ? launch_bwd_kernels<D, G, true, MASK>(p, s) : launch_bwd_kernels<D, G, false, MASK>(p, s);
     }
 }
 
 template <int D>
 cudaError_t backward_d(const Params &p, cudaStream_t s) {
-    switch (p.n_rep) {
-        case 1: return backward_dg<D, 1>(p, s);
-        case 2: return backward_dg<D, 2>(p, s);
+    switch (p.n_rep) {   // D = 128, n_rep <= 2: the n_rep = 4 tiles with rows masked (k_tc_bwd_dq)
+        case 1:
+            if constexpr (D == 128) return backward_dg<D, 4, true>(p, s);
+            else return backward_dg<D, 1>(p, s);
+        case 2:
+            if constexpr (D == 128) return backward_dg<D, 4, true>(p, s);
+            else return backward_dg<D, 2>(p, s);
         case 4: return backward_dg<D, 4>(p, s);
         case 8: return backward_dg<D, 8>(p, s);
         default: return cudaErrorNotSupported;
@@ -1310,9 +1349,7 @@ cudaError_t backward_d(const Params &p, cudaStream_t s) {
 }  // namespace
 
 bool tc_bwd_supported(int n_rep, int D) {
-    if (D == 128) return n_rep == 4 || n_rep == 8;
-    if (D == 64) return n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8;
-    return false;
+    return (D == 64 || D == 128) && (n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8);
 }
 
 cudaError_t tc_backward(const Params &p, cudaStream_t s) {

@@ -88,7 +88,10 @@ typedef enum { LA_PATH_SIMT = 0, LA_PATH_TCGEN05 = 1 } la_path;
 size_t la_workspace_size(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
                          int has_weights, int is_bwd);
 
-/* Kernel family chosen for these arguments (host-only; for tests and reports). */
+/* Kernel family chosen for these arguments (host-only; for tests and reports): the
+ * tensor-core kernels (LA_PATH_TCGEN05) for bfloat16 without cos/sin weights at D = 64 or 128
+ * with n_rep = Hq / Hkv in {1, 2, 4, 8}, forward and backward; the CUDA-core kernels
+ * (LA_PATH_SIMT) otherwise. */
 la_path la_kernel_path(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
                        int has_weights, int is_bwd);
 

@@ -83,7 +83,11 @@ TC_CASES = [
     (2, 16, 2, 3000, 128, True, "elu+1"),     # causal, n_rep 8
     (2, 16, 8, 3000, 128, True, "relu"),      # causal, n_rep 2
     (1, 8, 8, 8000, 64, False, "relu"),       # n_rep 1
-    (1, 4, 4, 2100, 128, True, "elu+1"),      # n_rep 1, D = 128
+    # D = 128 with n_rep 1 or 2: the forward takes the n_rep 2 tiles and the backward the
+    # n_rep 4 tiles, with the rows past the group's heads masked
+    (1, 4, 4, 2100, 128, True, "elu+1"),      # n_rep 1
+    (2, 8, 8, 3000, 128, False, "relu"),      # n_rep 1, bidirectional
+    (1, 6, 3, 2500, 128, True, "identity"),   # n_rep 2
 ]
 
 
@@ -91,7 +95,7 @@ TC_CASES = [
 def test_tensor_core_instantiations(case):
     B, Hq, Hkv, N, D, causal, phi = case
     w = gen.Workload(f"tc_b{B}_hq{Hq}_hkv{Hkv}_n{N}_d{D}_{'causal' if causal else 'bidir'}_{phi}",
-                     B, Hq, Hkv, N, D, "bf16", causal, phi, scale=0.5)
+                     B, Hq, Hkv, N, D, "bf16", causal, phi, scale=0.5, positive=phi == "identity")
     inp = gen.make_inputs(w, seed=13)
     dev = H.to_dev(inp)
     ref = H.run_oracle(w, inp)
@@ -183,6 +187,8 @@ GUARD_CASES = [
     (1, 4, 2, 77, 64, "bf16", True),     # CUDA-core kernels (position weights)
     (1, 8, 2, 205, 128, "bf16", False),  # tensor-core kernels, n_rep 4, TMA-store epilogues
     (1, 2, 2, 141, 64, "bf16", False),   # tensor-core kernels, n_rep 1
+    (1, 4, 2, 205, 128, "bf16", False),  # tensor-core kernels with masked rows (n_rep 2)
+    (1, 2, 2, 141, 128, "bf16", False),  # ... and n_rep 1
 ]
 
 
@@ -289,7 +295,7 @@ def test_bwd_from_fwd_reports_a_workspace_written_for_other_inputs():
 @pytest.mark.parametrize("shape", [
     (1, 8, 2, 1000, 128, "bf16", True),     # tensor-core forward and backward: states reused
     (1, 4, 4, 700, 64, "bf16", False),      # bidirectional, tensor cores
-    (1, 4, 2, 600, 128, "bf16", True),      # tensor-core forward, CUDA-core backward: recomputed
+    (1, 4, 2, 600, 128, "bf16", True),      # tensor cores with masked rows (n_rep 2 at D = 128)
     (1, 2, 2, 300, 32, "f32", True),        # CUDA-core path: states reused
 ], ids=lambda s: "x".join(map(str, s)))
 def test_bwd_from_fwd_matches_bwd(shape):
