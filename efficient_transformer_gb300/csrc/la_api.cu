@@ -125,6 +125,12 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
     } else if (tc) {   // the forward leaves its per-row dens for the backward
         pl.off_den = off;
         off += den_bytes;
+        if (pl.P == 2) {   // cos pass -> sin pass: numerator rows and dens of the cos terms
+            pl.off_pnum = off;
+            off += align_up((size_t)B * Hq * N * D * sizeof(float), 256);
+            pl.off_pden = off;
+            off += row_bytes;
+        }
     }
     if (tc) {   // and a record of what it was run on
         pl.off_hdr = off;
@@ -167,6 +173,8 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     p.hdr = tc ? reinterpret_cast<int *>(base + pl.off_hdr) : nullptr;
     p.gd = bwd ? reinterpret_cast<float *>(base + pl.off_gd) : nullptr;
     p.phis = bwd && pl.off_phis ? static_cast<void *>(base + pl.off_phis) : nullptr;
+    p.part_num = pl.off_pnum ? reinterpret_cast<float *>(base + pl.off_pnum) : nullptr;
+    p.part_den = pl.off_pden ? reinterpret_cast<float *>(base + pl.off_pden) : nullptr;
     if (bwd && fwd_ws) {
         // the forward's workspace holds its scanned segment states (and, on the tensor-core
         // path, its per-row dens and its record); they are the backward's when both plans cut

@@ -49,6 +49,11 @@ struct Params {
     float *gd;                   // [B, Hq, N] per-row denominator terms (backward; see each kernel)
     void *phis;                  // [B, Hq, N, D] bf16 phi(q) / den, written by the tensor-core dq
                                  // kernel for the dk/dv kernel (causal tensor-core backward; else null)
+    // tensor-core forward with cos/sin weights, run as two passes (cos, then sin)
+    int pass;                    // 0: one pass; 1: the cos pass; 2: the sin pass
+    const float *wrow;           // this pass's position weights (cw or sw), on phi(q) and phi(k) rows
+    float *part_num;             // [B, Hq, N, D] fp32: the cos pass's numerator rows (unnormalised)
+    float *part_den;             // [B, Hq, N] fp32: the cos pass's denominators (without eps)
     int *err;                    // device error word
 };
 
@@ -61,6 +66,7 @@ struct Plan {
     int nseg;         // segments per (batch, kv head)
     size_t state_elems;   // floats of one segment state (all terms)
     size_t off_state, off_rstate, off_den, off_gd, off_phis, off_hdr;   // workspace byte offsets
+    size_t off_pnum, off_pden;    // tensor-core forward with cos/sin weights: the cos pass's partials
     size_t ws_bytes;
 };
 
@@ -125,7 +131,6 @@ cudaError_t tc_backward(const Params &p, cudaStream_t s);
 bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal, int is_bwd);
 int tc_chunk(int n_rep, int D);   // tokens per chunk of the tensor-core forward (the plan's chunk)
 bool tc_bwd_supported(int n_rep, int D);
-cudaError_t tc_launch_state(const Params &p, cudaStream_t s);   // per-segment (S, z) on tensor cores
 
 // Low-rank projection y = (x V^T) U^T + bias (bf16, tensor cores).
 cudaError_t lowrank_forward(const void *x, const void *U, const void *V, const void *bias, void *y, int M, int K_in,

@@ -89,44 +89,67 @@ struct StateCfg {
 };
 
 // The state kernel's feature map over a K tile: thread i of kStatePro takes 16-byte pieces
-// idx = i, i + kStatePro, ... (row j = idx / (D / 8)); rows at or past t1 become zeros.
-template <int PHI, int C, int D>
-__device__ __forceinline__ void state_feature_map(uint8_t *kt, int i, int c0, int t1, uint32_t sm_lo, uint32_t sm_hi) {
+// idx = i, i + kStatePro, ... (row j = idx / (D / 8)); rows at or past t1 become zeros.  WT:
+// each row times its position weight w[token].
+template <int PHI, int C, int D, bool WT>
+__device__ __forceinline__ void state_feature_map(uint8_t *kt, int i, int c0, int t1, const float *w, uint32_t sm_lo,
+                                                  uint32_t sm_hi) {
     (void)sm_lo;
     (void)sm_hi;
+    (void)w;
 #pragma unroll 2
     for (int idx = i; idx < C * (D / 8); idx += kStatePro) {
         const int j = idx / (D / 8), c = idx % (D / 8);
         uint8_t *ch = kt + swz_chunk(C, j, c);
-        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 121, smem_u32(ch) - sm_lo, idx)) feat8_inplace2<PHI>(ch, c0 + j < t1);
+        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 121, smem_u32(ch) - sm_lo, idx)) {
+            const bool valid = c0 + j < t1;
+            if constexpr (WT)
+                feat8_weighted<PHI>(ch, valid, valid ? w[c0 + j] : 0.f);
+            else
+                feat8_inplace2<PHI>(ch, valid);
+        }
     }
 }
 
 // The forward's feature map over one stage: 16-byte piece `offq` of Q rows r0, r0 + RPP, ...
 // (valid while row < qrows, the rows of the group's real heads, and row % C < nvalid; the
-// other rows become zeros) and, causal, piece `kpiece` of K rows r0, r0 + RPP, ...
-template <int PHI, int C, int RPP, bool CAUSAL>
+// other rows become zeros) and, causal, piece `kpiece` of K rows r0, r0 + RPP, ...  WT: each
+// row times the position weight w[c0 + token].
+template <int PHI, int C, int RPP, bool CAUSAL, bool WT>
 __device__ __forceinline__ void fwd_feature_map(uint8_t *st, uint32_t offq, uint8_t *kpiece, int r0, int nvalid,
-                                                int qrows, uint32_t sm_lo, uint32_t sm_hi) {
+                                                int qrows, int c0, const float *w, uint32_t sm_lo, uint32_t sm_hi) {
     (void)sm_lo;
     (void)sm_hi;
+    (void)c0;
+    (void)w;
 #pragma unroll 4
     for (int row = r0; row < 128; row += RPP) {
         uint8_t *ch = st + offq + row * 128;
-        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, row))
-            feat8_inplace2<PHI>(ch, row < qrows && row % C < nvalid);
+        if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 221, smem_u32(ch) - sm_lo, row)) {
+            const bool valid = row < qrows && row % C < nvalid;
+            if constexpr (WT)
+                feat8_weighted<PHI>(ch, valid, valid ? w[c0 + row % C] : 0.f);
+            else
+                feat8_inplace2<PHI>(ch, valid);
+        }
     }
     if (CAUSAL)
         for (int j = r0; j < C; j += RPP) {
             uint8_t *ch = kpiece + j * 128;
-            if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 222, smem_u32(ch) - sm_lo, j)) feat8_inplace2<PHI>(ch, j < nvalid);
+            if (LA_CHECK(in_smem(ch, 16, sm_lo, sm_hi), 222, smem_u32(ch) - sm_lo, j)) {
+                if constexpr (WT)
+                    feat8_weighted<PHI>(ch, j < nvalid, j < nvalid ? w[c0 + j] : 0.f);
+                else
+                    feat8_inplace2<PHI>(ch, j < nvalid);
+            }
         }
 }
 
 // ---------------------------------------------------------------------------------------
 // Per-segment state: S = phi(K)^T V and z = phi(K)^T 1 over the segment's tokens (fp32 in
-// TMEM), written to the workspace as [D][D+1] (z in column D).
-template <int D>
+// TMEM), written to the workspace as [D][D+1] (z in column D).  WT: phi(k) rows weighted by
+// the pass's position weights (cos or sin).
+template <int D, bool WT>
 __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_constant__ CUtensorMap map_k,
                                                      const __grid_constant__ CUtensorMap map_v, Params p) {
     using K = StateCfg<D>;
@@ -215,11 +238,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
                 uint8_t *kt = stage0 + s * K::STAGE;
                 const int c0 = t0 + k * C;
                 if (p.phi == LA_PHI_ELU1)
-                    state_feature_map<LA_PHI_ELU1, C, D>(kt, i, c0, t1, sm_lo, sm_hi);
+                    state_feature_map<LA_PHI_ELU1, C, D, WT>(kt, i, c0, t1, p.wrow, sm_lo, sm_hi);
                 else if (p.phi == LA_PHI_RELU)
-                    state_feature_map<LA_PHI_RELU, C, D>(kt, i, c0, t1, sm_lo, sm_hi);
+                    state_feature_map<LA_PHI_RELU, C, D, WT>(kt, i, c0, t1, p.wrow, sm_lo, sm_hi);
                 else
-                    state_feature_map<LA_PHI_IDENTITY, C, D>(kt, i, c0, t1, sm_lo, sm_hi);
+                    state_feature_map<LA_PHI_IDENTITY, C, D, WT>(kt, i, c0, t1, p.wrow, sm_lo, sm_hi);
                 fence_proxy_async();
             }
             mbar_arrive_warp(&bar_ready[s]);
@@ -262,8 +285,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
 
 // ---------------------------------------------------------------------------------------
 // Chunked forward (see the file comment for the per-chunk steps and warp roles).  MASK: the
-// group has fewer heads (n_rep) than the tile's G, and the rows past them are masked.
-template <int D, int G, bool CAUSAL, bool MASK>
+// group has fewer heads (n_rep) than the tile's G, and the rows past them are masked.  WT: one
+// of the two passes of the cos/sin-weighted forward (p.pass: 1 cos, 2 sin; see forward_dg).
+template <int D, int G, bool CAUSAL, bool MASK, bool WT>
 __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant__ CUtensorMap map_q,
                                                            const __grid_constant__ CUtensorMap map_k,
                                                            const __grid_constant__ CUtensorMap map_v,
@@ -462,16 +486,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             if (i == 0) LA_TL(k, 1);
             if (ok) {
                 uint8_t *st = stage0 + s * K::STAGE;
-                const int nvalid = t1 - (t0 + k * C);
+                const int c0 = t0 + k * C, nvalid = t1 - c0;
                 if (p.phi == LA_PHI_ELU1)
-                    fwd_feature_map<LA_PHI_ELU1, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C, sm_lo,
-                                                                 sm_hi);
+                    fwd_feature_map<LA_PHI_ELU1, C, RPP, CAUSAL, WT>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C, c0,
+                                                                     p.wrow, sm_lo, sm_hi);
                 else if (p.phi == LA_PHI_RELU)
-                    fwd_feature_map<LA_PHI_RELU, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C, sm_lo,
-                                                                 sm_hi);
+                    fwd_feature_map<LA_PHI_RELU, C, RPP, CAUSAL, WT>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C, c0,
+                                                                     p.wrow, sm_lo, sm_hi);
                 else
-                    fwd_feature_map<LA_PHI_IDENTITY, C, RPP, CAUSAL>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C,
-                                                                     sm_lo, sm_hi);
+                    fwd_feature_map<LA_PHI_IDENTITY, C, RPP, CAUSAL, WT>(st, offq, st + OFF_K + offk, r0, nvalid, gr * C,
+                                                                         c0, p.wrow, sm_lo, sm_hi);
                 fence_proxy_async();
             }
             if (i == 0) LA_TL(k, 2);
@@ -623,18 +647,42 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             ok = ok && warp_wait(&bar_ofull[o], (k / NO) & 1, &abort_flag);
             tc_fence_after();
             if (i == 0) LA_TL(k, 12);
-            float den = 0.f, dzz = 0.f;   // dzz = phi(q) . z (hi + lo)
+            const bool rowok = c0 + i % C < t1 && i / C < gr;
+            const size_t rg = (size_t)(bh0 + i / C) * p.N + (c0 + i % C);   // the row's index (when rowok)
+            float pden = 0.f;   // sin pass: the cos terms' den of the row
+            if constexpr (WT)
+                if (p.pass == 2 && ok && rowok) pden = p.part_den[rg];
+            float den = 0.f;
             if (ok) {
                 float dz[4];   // phi(q) . z_hi, phi(q) . z_lo, P 1 (bf16 P), unused
                 tmem_ld4(tO + lane_off + D, dz);
                 tmem_wait_regs<4>(dz);
-                dzz = dz[0] + dz[1];
-                den = dzz + dz[2];
+                den = (dz[0] + dz[1]) + dz[2];
                 // bidirectional: the backward's den (causal: written by the P conversion warps)
-                if (!CAUSAL && p.den && c0 + i % C < t1 && i / C < gr)
-                    p.den[(size_t)(bh0 + i / C) * p.den_stride + c0 + i % C] = den + p.eps;
+                if (!CAUSAL && p.den && rowok) p.den[(size_t)(bh0 + i / C) * p.den_stride + c0 + i % C] = den + p.eps;
             }
-            const float inv = 1.f / (den + p.eps);
+            if constexpr (WT) {
+                if (p.pass == 1) {   // cos pass: the row's numerator (fp32, unnormalised) and den
+#pragma unroll 1
+                    for (int c32 = 0; c32 < D / 32; ++c32) {
+                        float v[32];
+                        if (ok) {
+                            tmem_ld32(tO + lane_off + c32 * 32, v);
+                            tmem_wait_regs<32>(v);
+                        }
+                        if (ok && rowok) {
+                            float4 *dst = reinterpret_cast<float4 *>(p.part_num + rg * D + c32 * 32);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        }
+                    }
+                    if (ok && rowok) p.part_den[rg] = den;
+                    tc_fence_before();
+                    mbar_arrive_warp(&bar_ofree[o]);
+                    continue;
+                }
+            }
+            const float inv = 1.f / (den + pden + p.eps);
 #pragma unroll 1
             for (int c64 = 0; c64 < D / 64; ++c64) {
                 float v[32];   // 32 columns at a time
@@ -652,6 +700,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                     if (ok && hh == 1) {
                         tmem_ld32(tO + lane_off + c64 * 64 + 32, v);
                         tmem_wait_regs<32>(v);
+                    }
+                    if constexpr (WT) {   // sin pass: plus the cos terms' numerator
+                        if (p.pass == 2 && ok && rowok) {
+                            const float4 *src = reinterpret_cast<const float4 *>(p.part_num + rg * D + c64 * 64 + hh * 32);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 a = src[q];
+                                v[4 * q] += a.x;
+                                v[4 * q + 1] += a.y;
+                                v[4 * q + 2] += a.z;
+                                v[4 * q + 3] += a.w;
+                            }
+                        }
                     }
                     if (ok) {
 #pragma unroll
@@ -687,19 +748,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
 // ---------------------------------------------------------------------------------------
 // Host side
 
-template <int D>
+template <int D, bool WT>
 cudaError_t launch_state(const Params &p, cudaStream_t s) {
     CUtensorMap mk{}, mv{};
     cudaError_t e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, StateCfg<D>::C);
     if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, StateCfg<D>::C);
-    if (e == cudaSuccess) e = prepare(k_tc_state<D>, StateCfg<D>::SMEM);
+    if (e == cudaSuccess) e = prepare(k_tc_state<D, WT>, StateCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     TraceScope ts("tc_seg_state", s);
-    k_tc_state<D><<<p.B * p.Hkv * p.nseg, kStateThreads, StateCfg<D>::SMEM, s>>>(mk, mv, p);
+    k_tc_state<D, WT><<<p.B * p.Hkv * p.nseg, kStateThreads, StateCfg<D>::SMEM, s>>>(mk, mv, p);
     return cudaGetLastError();
 }
 
-template <int D, int G, bool CAUSAL, bool MASK>
+template <int D, int G, bool CAUSAL, bool MASK, bool WT>
 cudaError_t launch_fwd(const Params &p, cudaStream_t s) {
     using K = FwdCfg<D, G>;
     CUtensorMap mq{}, mk{}, mv{}, mo{};
@@ -707,16 +768,43 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t s) {
     if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mo, p.out, p.B * p.Hq, p.N, D, K::C);
-    if (e == cudaSuccess) e = prepare(k_tc_fwd<D, G, CAUSAL, MASK>, K::SMEM);
+    if (e == cudaSuccess) e = prepare(k_tc_fwd<D, G, CAUSAL, MASK, WT>, K::SMEM);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_fwd_causal" : "tc_fwd_bidir", s);
-    k_tc_fwd<D, G, CAUSAL, MASK><<<p.B * p.Hkv * p.nseg, kFwdThreads, K::SMEM, s>>>(mq, mk, mv, mo, p);
+    k_tc_fwd<D, G, CAUSAL, MASK, WT><<<p.B * p.Hkv * p.nseg, kFwdThreads, K::SMEM, s>>>(mq, mk, mv, mo, p);
     return cudaGetLastError();
+}
+
+// The forward with cos/sin weights (the cosFormer modulation of the linear_attn page:
+// W_ij = c_i c_j + s_i s_j) as two passes of the one-term kernels, each with its own (S, z)
+// and the features c_t phi(x_t), then s_t phi(x_t): out = (num_c + num_s) / (den_c + den_s +
+// eps).  The cos pass leaves num_c and den_c (fp32) in the workspace; the sin pass adds them
+// in its epilogue.  Each pass's states sit in their own half of the state array.
+template <int D, int G, bool MASK>
+cudaError_t forward_two_pass(const Params &p, cudaStream_t s) {
+    const size_t pass_elems = (size_t)p.B * p.Hkv * p.nseg * D * (D + 1);
+    cudaError_t e = cudaSuccess;
+    for (int pass = 1; pass <= 2 && e == cudaSuccess; ++pass) {
+        Params pp = p;
+        pp.pass = pass;
+        pp.wrow = pass == 1 ? p.cw : p.sw;
+        pp.state = p.state + (size_t)(pass - 1) * pass_elems;
+        pp.den = nullptr;   // the weighted backward runs on the CUDA cores and forms its own
+        e = launch_state<D, true>(pp, s);
+        if (e == cudaSuccess) e = scan_segments(pp.state, pp, pp.causal ? kScanPrefix : kScanTotal, (size_t)D * (D + 1), s);
+        if (e == cudaSuccess)
+            e = pp.causal ? launch_fwd<D, G, true, MASK, true>(pp, s) : launch_fwd<D, G, false, MASK, true>(pp, s);
+    }
+    return e;
 }
 
 template <int D, int G, bool MASK = false>
 cudaError_t forward_dg(const Params &p, cudaStream_t s) {
-    cudaError_t e = launch_state<D>(p, s);
+    if (p.P == 2) {
+        if (!p.cw || !p.sw || !p.part_num || !p.part_den) return cudaErrorInvalidValue;
+        return forward_two_pass<D, G, MASK>(p, s);
+    }
+    cudaError_t e = launch_state<D, false>(p, s);
 #ifdef LA_DEBUG
     const char *stop = getenv("LA_DEBUG_STOP");
     if (stop && stop[0] == 's' && stop[1] == 't') return e;      // "state"
@@ -727,7 +815,7 @@ cudaError_t forward_dg(const Params &p, cudaStream_t s) {
     if (stop && stop[0] == 's' && stop[1] == 'c') return e;      // "scan"
 #endif
     if (e != cudaSuccess) return e;
-    return p.causal ? launch_fwd<D, G, true, MASK>(p, s) : launch_fwd<D, G, false, MASK>(p, s);
+    return p.causal ? launch_fwd<D, G, true, MASK, false>(p, s) : launch_fwd<D, G, false, MASK, false>(p, s);
 }
 
 template <int D>
@@ -752,9 +840,9 @@ int tc_chunk(int n_rep, int D) { return D == 128 && n_rep == 1 ? 64 : 128 / n_re
 bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal, int is_bwd) {
     (void)N;
     (void)causal;
-    if (dt != LA_BF16 || P != 1) return false;
+    if (dt != LA_BF16 || (P != 1 && P != 2)) return false;
     const int n_rep = Hq / Hkv;
-    if (is_bwd) return tc_bwd_supported(n_rep, D);
+    if (is_bwd) return P == 1 && tc_bwd_supported(n_rep, D);   // weighted backward: CUDA cores
     return (D == 64 || D == 128) && (n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8);
 }
 
@@ -762,9 +850,6 @@ cudaError_t tc_forward(const Params &p, cudaStream_t s) {
     return p.D == 128 ? forward_d<128>(p, s) : (p.D == 64 ? forward_d<64>(p, s) : cudaErrorNotSupported);
 }
 
-cudaError_t tc_launch_state(const Params &p, cudaStream_t s) {
-    return p.D == 128 ? launch_state<128>(p, s) : (p.D == 64 ? launch_state<64>(p, s) : cudaErrorNotSupported);
-}
 
 }  // namespace la
 

@@ -190,6 +190,33 @@ __device__ __forceinline__ void feat8_batch_rowscale(uint8_t *const *ptr, const 
         if (present[n]) *reinterpret_cast<uint4 *>(ptr[n]) = x[n];
 }
 
+// w phi(x) on 8 bf16 values (16 bytes) in place, or zeros for a row past the end: phi in
+// float32 (expf for elu+1), times the row's position weight w, rounded to bf16 once.  (The
+// cos/sin passes of the forward; one rounding keeps the weighted features as accurate as
+// bf16 allows, where the unweighted maps trade that for the packed bf16 arithmetic above.)
+template <int PHI>
+__device__ __forceinline__ void feat8_weighted(uint8_t *chunk, bool valid, float w) {
+    uint4 *ptr = reinterpret_cast<uint4 *>(chunk);
+    uint4 x = valid ? *ptr : make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+        uint32_t *xi = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = unpack_bf16x2(xi[q]);
+            float a = f.x, b = f.y;
+            if (PHI == LA_PHI_ELU1) {
+                a = a > 0.f ? a + 1.f : expf(a);
+                b = b > 0.f ? b + 1.f : expf(b);
+            } else if (PHI == LA_PHI_RELU) {
+                a = fmaxf(a, 0.f);
+                b = fmaxf(b, 0.f);
+            }
+            xi[q] = pack_bf16x2(a * w, b * w);
+        }
+    }
+    *ptr = x;
+}
+
 // phi applied to 8 bf16 values (16 bytes) in place, or zeros for a row past the end.
 template <int PHI>
 __device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid) {

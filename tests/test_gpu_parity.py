@@ -103,6 +103,33 @@ def test_tensor_core_instantiations(case):
     H.compare(w, H.run_gpu(w, dev, from_fwd=False), ref, label="bwd")
 
 
+# The cos/sin-weighted forward on tensor cores (two passes, cos then sin) at shapes with several
+# segments, ragged last chunks, every tile layout (n_rep 1 on masked rows at D = 128) and each
+# feature map; the backward of these runs on the CUDA cores.
+WEIGHTED_TC_CASES = [
+    # B, Hq, Hkv, N, D, causal, phi
+    (2, 4, 4, 3000, 128, True, "relu"),       # n_rep 1, masked rows
+    (1, 8, 8, 2500, 128, False, "elu+1"),     # n_rep 1, bidirectional
+    (1, 8, 2, 2900, 128, True, "elu+1"),      # n_rep 4
+    (2, 8, 1, 1500, 128, True, "relu"),       # n_rep 8
+    (2, 8, 8, 3000, 64, True, "elu+1"),       # n_rep 1, D = 64
+    (1, 8, 4, 2100, 64, False, "relu"),       # n_rep 2, bidirectional
+    (1, 6, 3, 2000, 64, True, "identity"),    # n_rep 2
+]
+
+
+@pytest.mark.parametrize("case", WEIGHTED_TC_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_weighted_tensor_core_forward(case):
+    B, Hq, Hkv, N, D, causal, phi = case
+    w = gen.Workload(f"tcw_b{B}_hq{Hq}_hkv{Hkv}_n{N}_d{D}_{'causal' if causal else 'bidir'}_{phi}",
+                     B, Hq, Hkv, N, D, "bf16", causal, phi, scale=0.5, weights=True, positive=phi == "identity")
+    assert la.kernel_path(B, Hq, Hkv, N, D, torch.bfloat16, causal, True, False) == la.LA_PATH_TCGEN05
+    inp = gen.make_inputs(w, seed=17)
+    dev = H.to_dev(inp)
+    ref = H.run_oracle(w, inp)
+    H.compare(w, H.run_gpu(w, dev, from_fwd=True), ref, label="weighted forward on tensor cores")
+
+
 # With a single visible key (N = 1) the exact dq and dk equal b (g . v) eps / den^2: the
 # recurrence forms them as the difference of two terms of size ~1/den that agree up to a
 # relative eps/den, so the result carries the terms' rounding error amplified by den/eps.
@@ -257,18 +284,19 @@ def test_binding_errors_are_raised():
         la.fwd(q, q, q)          # unsupported head dimension
 
 
-@pytest.mark.parametrize("name,fwd_path", [
-    ("causal_b1_h2_n256_d32_f32", la.LA_PATH_SIMT),
-    ("bidir_b2_h8_n2048_d64_bf16_elu1", la.LA_PATH_TCGEN05),
-    ("causal_b4_h16_n4096_d64_bf16", la.LA_PATH_TCGEN05),
-    ("cosformer_causal_b2_h16_n8192_d128_bf16", la.LA_PATH_SIMT),
-    ("gqa_causal_b1_hq32_hkv8_n65536_d128_bf16", la.LA_PATH_TCGEN05),
+@pytest.mark.parametrize("name,fwd_path,bwd_path", [
+    ("causal_b1_h2_n256_d32_f32", la.LA_PATH_SIMT, la.LA_PATH_SIMT),
+    ("bidir_b2_h8_n2048_d64_bf16_elu1", la.LA_PATH_TCGEN05, la.LA_PATH_TCGEN05),
+    ("causal_b4_h16_n4096_d64_bf16", la.LA_PATH_TCGEN05, la.LA_PATH_TCGEN05),
+    ("cosformer_causal_b2_h16_n8192_d128_bf16", la.LA_PATH_TCGEN05, la.LA_PATH_SIMT),
+    ("gqa_causal_b1_hq32_hkv8_n65536_d128_bf16", la.LA_PATH_TCGEN05, la.LA_PATH_TCGEN05),
 ])
-def test_kernel_family(name, fwd_path):
-    """The bf16 workloads without position weights run the tcgen05 forward and backward."""
+def test_kernel_family(name, fwd_path, bwd_path):
+    """The bf16 workloads run the tcgen05 forward (with cos/sin weights as two passes) and,
+    without weights, the tcgen05 backward."""
     w = gen.WORKLOADS[name]
     assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, False) == fwd_path
-    assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, True) == fwd_path
+    assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, True) == bwd_path
 
 
 def test_bwd_from_fwd_reports_a_workspace_written_for_other_inputs():
