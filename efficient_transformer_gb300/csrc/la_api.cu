@@ -122,6 +122,19 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
             pl.off_phis = off;
             off += align_up((size_t)B * Hq * N * D * 2, 256);
         }
+        if (tc && pl.P == 2) {   // cos/sin passes: the forward's partials (when the backward runs
+                                 // it) and the cos pass's dq, dk, dv (fp32)
+            pl.off_pnum = off;
+            off += align_up((size_t)B * Hq * N * D * sizeof(float), 256);
+            pl.off_pden = off;
+            off += row_bytes;
+            pl.off_pdq = off;
+            off += align_up((size_t)B * Hq * N * D * sizeof(float), 256);
+            pl.off_pdk = off;
+            off += align_up((size_t)B * Hkv * N * D * sizeof(float), 256);
+            pl.off_pdv = off;
+            off += align_up((size_t)B * Hkv * N * D * sizeof(float), 256);
+        }
     } else if (tc) {   // the forward leaves its per-row dens for the backward
         pl.off_den = off;
         off += den_bytes;
@@ -175,6 +188,9 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     p.phis = bwd && pl.off_phis ? static_cast<void *>(base + pl.off_phis) : nullptr;
     p.part_num = pl.off_pnum ? reinterpret_cast<float *>(base + pl.off_pnum) : nullptr;
     p.part_den = pl.off_pden ? reinterpret_cast<float *>(base + pl.off_pden) : nullptr;
+    p.part_dq = pl.off_pdq ? reinterpret_cast<float *>(base + pl.off_pdq) : nullptr;
+    p.part_dk = pl.off_pdk ? reinterpret_cast<float *>(base + pl.off_pdk) : nullptr;
+    p.part_dv = pl.off_pdv ? reinterpret_cast<float *>(base + pl.off_pdv) : nullptr;
     if (bwd && fwd_ws) {
         // the forward's workspace holds its scanned segment states (and, on the tensor-core
         // path, its per-row dens and its record); they are the backward's when both plans cut
@@ -187,6 +203,10 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
             if (tc) {
                 p.den = reinterpret_cast<float *>(f + pf.off_den);
                 p.hdr = reinterpret_cast<int *>(f + pf.off_hdr);
+                if (pl.P == 2) {   // the forward's float32 output rows (for h) and its partials
+                    p.part_num = reinterpret_cast<float *>(f + pf.off_pnum);
+                    p.part_den = reinterpret_cast<float *>(f + pf.off_pden);
+                }
             }
             p.state_given = 1;
         }

@@ -54,6 +54,11 @@ struct Params {
     const float *wrow;           // this pass's position weights (cw or sw), on phi(q) and phi(k) rows
     float *part_num;             // [B, Hq, N, D] fp32: the cos pass's numerator rows (unnormalised)
     float *part_den;             // [B, Hq, N] fp32: the cos pass's denominators (without eps)
+    // ... and its backward: the cos pass's gradients (fp32), added in by the sin pass; the
+    // forward's float32 output rows (part_num after the sin pass) give h = -g . out, read
+    // from `gd`
+    float *part_dq;              // [B, Hq, N, D]
+    float *part_dk, *part_dv;    // [B, Hkv, N, D]
     int *err;                    // device error word
 };
 
@@ -67,6 +72,7 @@ struct Plan {
     size_t state_elems;   // floats of one segment state (all terms)
     size_t off_state, off_rstate, off_den, off_gd, off_phis, off_hdr;   // workspace byte offsets
     size_t off_pnum, off_pden;    // tensor-core forward with cos/sin weights: the cos pass's partials
+    size_t off_pdq, off_pdk, off_pdv;   // ... and backward
     size_t ws_bytes;
 };
 

@@ -594,8 +594,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                     tmem_wait_regs<2>(dz);
                 }
                 const int t = t0 + k * C + ti;
-                if (ok && p.den && t < t1 && i / C < gr)
-                    p.den[(size_t)(bh0 + i / C) * p.den_stride + t] = (dz[0] + dz[1]) + rsum + p.eps;
+                if (ok && p.den && t < t1 && i / C < gr) {
+                    float *dp = p.den + (size_t)(bh0 + i / C) * p.den_stride + t;
+                    if (WT && p.pass == 2)   // the sin terms onto the cos pass's den (which has eps)
+                        *dp += (dz[0] + dz[1]) + rsum;
+                    else
+                        *dp = (dz[0] + dz[1]) + rsum + p.eps;
+                }
             };
             if (nchunk > 0) p_conv(0);
             for (int k = 0; k < nchunk; ++k) {
@@ -658,8 +663,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 tmem_ld4(tO + lane_off + D, dz);
                 tmem_wait_regs<4>(dz);
                 den = (dz[0] + dz[1]) + dz[2];
-                // bidirectional: the backward's den (causal: written by the P conversion warps)
-                if (!CAUSAL && p.den && rowok) p.den[(size_t)(bh0 + i / C) * p.den_stride + c0 + i % C] = den + p.eps;
+                // bidirectional: the backward's den (causal: written by the P conversion warps;
+                // the sin pass adds its terms to the cos pass's)
+                if (!CAUSAL && p.den && rowok) {
+                    float *dp = p.den + (size_t)(bh0 + i / C) * p.den_stride + c0 + i % C;
+                    if (WT && p.pass == 2)
+                        *dp += den;
+                    else
+                        *dp = den + p.eps;
+                }
             }
             if constexpr (WT) {
                 if (p.pass == 1) {   // cos pass: the row's numerator (fp32, unnormalised) and den
@@ -701,9 +713,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                         tmem_ld32(tO + lane_off + c64 * 64 + 32, v);
                         tmem_wait_regs<32>(v);
                     }
-                    if constexpr (WT) {   // sin pass: plus the cos terms' numerator
+                    if constexpr (WT) {   // sin pass: plus the cos terms' numerator; the float32
+                                          // output row goes back in its place (the backward's h)
                         if (p.pass == 2 && ok && rowok) {
-                            const float4 *src = reinterpret_cast<const float4 *>(p.part_num + rg * D + c64 * 64 + hh * 32);
+                            float4 *src = reinterpret_cast<float4 *>(p.part_num + rg * D + c64 * 64 + hh * 32);
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
                                 const float4 a = src[q];
@@ -711,6 +724,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                                 v[4 * q + 1] += a.y;
                                 v[4 * q + 2] += a.z;
                                 v[4 * q + 3] += a.w;
+                                src[q] = make_float4(v[4 * q] * inv, v[4 * q + 1] * inv, v[4 * q + 2] * inv, v[4 * q + 3] * inv);
                             }
                         }
                     }
@@ -779,7 +793,9 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t s) {
 // W_ij = c_i c_j + s_i s_j) as two passes of the one-term kernels, each with its own (S, z)
 // and the features c_t phi(x_t), then s_t phi(x_t): out = (num_c + num_s) / (den_c + den_s +
 // eps).  The cos pass leaves num_c and den_c (fp32) in the workspace; the sin pass adds them
-// in its epilogue.  Each pass's states sit in their own half of the state array.
+// in its epilogue, and leaves the float32 output rows where num_c was (the backward's h =
+// -g . out).  Each pass's states sit in their own half of the state array; the den left for
+// the backward (incl. eps) is the cos pass's plus the sin pass's.
 template <int D, int G, bool MASK>
 cudaError_t forward_two_pass(const Params &p, cudaStream_t s) {
     const size_t pass_elems = (size_t)p.B * p.Hkv * p.nseg * D * (D + 1);
@@ -789,7 +805,6 @@ cudaError_t forward_two_pass(const Params &p, cudaStream_t s) {
         pp.pass = pass;
         pp.wrow = pass == 1 ? p.cw : p.sw;
         pp.state = p.state + (size_t)(pass - 1) * pass_elems;
-        pp.den = nullptr;   // the weighted backward runs on the CUDA cores and forms its own
         e = launch_state<D, true>(pp, s);
         if (e == cudaSuccess) e = scan_segments(pp.state, pp, pp.causal ? kScanPrefix : kScanTotal, (size_t)D * (D + 1), s);
         if (e == cudaSuccess)
@@ -842,7 +857,7 @@ bool tc_supported(int Hq, int Hkv, int N, int D, la_dtype dt, int P, int causal,
     (void)causal;
     if (dt != LA_BF16 || (P != 1 && P != 2)) return false;
     const int n_rep = Hq / Hkv;
-    if (is_bwd) return P == 1 && tc_bwd_supported(n_rep, D);   // weighted backward: CUDA cores
+    if (is_bwd) return tc_bwd_supported(n_rep, D);
     return (D == 64 || D == 128) && (n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8);
 }
 

@@ -109,6 +109,10 @@ __device__ __forceinline__ float feat_grad_threshold(int phi) { return phi == LA
 __device__ __forceinline__ float feat_grad_from_feat(float f, bool elu, float thr) {
     return elu ? fminf(f, 1.f) : (f > thr ? 1.f : 0.f);
 }
+// ... and w phi'(k) from the weighted feature f = w phi(k) (w >= 0): min(f, w) for elu+1.
+__device__ __forceinline__ float feat_grad_from_feat_w(float f, bool elu, float thr, float w) {
+    return elu ? fminf(f, w) : (f > thr ? w : 0.f);
+}
 
 // z (fp32) into column d of a z tile as the rows (z_hi, z_lo, z_hi), z = z_hi + z_lo.
 template <int D>
@@ -147,9 +151,27 @@ __device__ __forceinline__ uint4 dq_piece(uint4 u, const float *x, float inv) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// dq_piece's eight values in float32 (the cos/sin passes add the two terms before rounding);
+// with position weights, inv = w / den: the feature is w phi(q), whose derivative is w phi'(q),
+// and min(phi_s, w / den) = w min(phi, 1) / den for elu+1.
+template <int PHI>
+__device__ __forceinline__ void dq_vals(uint4 u, const float *x, float inv, float *o) {
+    const uint32_t *ui = reinterpret_cast<const uint32_t *>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = unpack_bf16x2(ui[q]);
+        const float m0 = PHI == LA_PHI_ELU1 ? fminf(f.x, inv) : PHI == LA_PHI_IDENTITY ? inv : (f.x > 0.f ? inv : 0.f);
+        const float m1 = PHI == LA_PHI_ELU1 ? fminf(f.y, inv) : PHI == LA_PHI_IDENTITY ? inv : (f.y > 0.f ? inv : 0.f);
+        o[2 * q] = m0 * x[2 * q];
+        o[2 * q + 1] = m1 * x[2 * q + 1];
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // MASK: the group has fewer heads (n_rep) than the tile's G; the rows past them are masked.
-template <int D, int G, bool CAUSAL, bool MASK>
+// WT: one of the two passes of the cos/sin-weighted backward (p.pass: 1 cos, 2 sin; see
+// backward_two_pass): features w phi, h = -g . out given in p.gd, and dq summed over the passes.
+template <int D, int G, bool CAUSAL, bool MASK, bool WT>
 __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_constant__ CUtensorMap map_q,
                                                               const __grid_constant__ CUtensorMap map_k,
                                                               const __grid_constant__ CUtensorMap map_v,
@@ -402,7 +424,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     ok = ok && warp_wait(&bar_dqready[s][hh], (k / NS) & 1, &abort_flag);
                     if (!ok) break;
                     if (hh == 0) LA_TL(k, 13);
-                    if (K::DB == 2 || hh == 1) {
+                    if ((K::DB == 2 || hh == 1) && !(WT && p.pass == 1)) {   // (cos pass: dq partials in fp32)
                         const int blk = K::DB == 2 ? hh : 0;
                         for (int r = 0; r < gr; ++r)
                             tma_store_3d_w(&map_dq, st + OFF_G + blk * 128 * 128 + r * C * 128, blk * 64, c0, bh0 + r);
@@ -458,13 +480,29 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     pres[NQ + n] = j < C && LA_CHECK(in_smem(pp[NQ + n], 16, sm_lo, sm_hi), 322, smem_u32(pp[NQ + n]) - sm_lo, j);
                     val[NQ + n] = j < nvalid;
                 }
-                // the Q pieces' rows r0 + n RPP, each divided by its den
-                if (p.phi == LA_PHI_ELU1)
-                    feat8_batch_rowscale<LA_PHI_ELU1, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
-                else if (p.phi == LA_PHI_RELU)
-                    feat8_batch_rowscale<LA_PHI_RELU, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
-                else
-                    feat8_batch_rowscale<LA_PHI_IDENTITY, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
+                if constexpr (WT) {   // w phi(q) / den and w phi(k), phi in float32
+                    float sc[NQ + NK + 1];
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n) {
+                        const int row = r0 + n * RPP;
+                        sc[n] = val[n] ? p.wrow[c0 + row % C] / dent[(row / C) * K::DPAD + row % C] : 0.f;
+                    }
+#pragma unroll
+                    for (int n = 0; n < NK; ++n) sc[NQ + n] = val[NQ + n] ? p.wrow[c0 + r0 + n * RPP] : 0.f;
+                    if (p.phi == LA_PHI_ELU1)
+                        feat8_batch_scaled<LA_PHI_ELU1, NQ + NK>(pp, pres, val, sc);
+                    else if (p.phi == LA_PHI_RELU)
+                        feat8_batch_scaled<LA_PHI_RELU, NQ + NK>(pp, pres, val, sc);
+                    else
+                        feat8_batch_scaled<LA_PHI_IDENTITY, NQ + NK>(pp, pres, val, sc);
+                } else {   // the Q pieces' rows r0 + n RPP, each divided by its den
+                    if (p.phi == LA_PHI_ELU1)
+                        feat8_batch_rowscale<LA_PHI_ELU1, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
+                    else if (p.phi == LA_PHI_RELU)
+                        feat8_batch_rowscale<LA_PHI_RELU, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
+                    else
+                        feat8_batch_rowscale<LA_PHI_IDENTITY, NQ + NK, C, K::DPAD>(pp, pres, val, dent, r0, RPP, NQ);
+                }
                 fence_proxy_async();
             }
             if (pi == 0) LA_TL(k, 2);
@@ -545,9 +583,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             tc_fence_after();
             if (i == 0 && h == 0) LA_TL(k, 7);
             float hval = 0.f, inv = 0.f;
+            if (WT && ok && valid) hval = p.gd[(size_t)bh * p.N + t];   // h = -g . out, given
             if (ok) {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                if (CAUSAL) {
+                if (CAUSAL && !WT) {
 #pragma unroll 1
                     for (int c16 = 0; c16 < C / 16; ++c16) {
                         if ((c16 & 1) != h) continue;
@@ -563,7 +602,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 }
                 // phi_s . X over this half's feature columns, 16 at a time
 #pragma unroll 1
-                for (int c16 = 0; c16 < HALF / 16; ++c16) {
+                for (int c16 = 0; c16 < (WT ? 0 : HALF / 16); ++c16) {
                     const int col0 = h * HALF + c16 * 16;
                     float xv[16];
                     tmem_ld16(tX + lane_off + col0, xv);
@@ -583,13 +622,19 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     }
                 }
                 xch[h * 128 + i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-                // (masked rows: 0, so that their dq is zeros, which keeps their g rows zero)
-                inv = r < gr ? 1.f / reinterpret_cast<const float *>(st + OFF_DEN)[r * K::DPAD + ti] : 0.f;
+                // (masked rows: 0, so that their dq is zeros, which keeps their g rows zero; with
+                // weights w / den, for rows inside the sequence)
+                if constexpr (WT)
+                    inv = valid ? p.wrow[t] / reinterpret_cast<const float *>(st + OFF_DEN)[r * K::DPAD + ti] : 0.f;
+                else
+                    inv = r < gr ? 1.f / reinterpret_cast<const float *>(st + OFF_DEN)[r * K::DPAD + ti] : 0.f;
             }
             named_barrier(3, 256);
             if (ok) {
-                const float gnum = xch[i] + xch[128 + i];   // g . num / den
-                hval = valid ? -gnum : 0.f;
+                if (!WT) {
+                    const float gnum = xch[i] + xch[128 + i];   // g . num / den
+                    hval = valid ? -gnum : 0.f;
+                }
                 if (CAUSAL)
                     for (int c16 = h; c16 < C / 16; c16 += 2) {
                         float vd[16];
@@ -614,7 +659,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 0, i)) = hh;
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 1, i)) = hh;
                     *reinterpret_cast<__nv_bfloat16 *>(htile + swz_offset(16, 2, i)) = hl;
-                    if (valid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 334, bh, t))
+                    if (!WT && valid && LA_CHECK((size_t)bh * p.N + t < (size_t)p.B * p.Hq * p.N, 334, bh, t))
                         p.gd[(size_t)bh * p.N + t] = hval;   // h = den * gd for the dk/dv kernel
                 }
                 fence_proxy_async();
@@ -645,13 +690,43 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     mbar_arrive_warp(&bar_xfree);
                 }
                 if (!ok) continue;
+                if constexpr (WT) {   // cos pass: dq terms (fp32) to the workspace; sin pass: plus those
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8)
-                    if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 341, smem_u32(ch[q8]) - sm_lo, q8))
-                        *reinterpret_cast<uint4 *>(ch[q8] + OFF_G) =
-                            p.phi == LA_PHI_ELU1   ? dq_piece<LA_PHI_ELU1>(u[q8], xv + q8 * 8, inv)
-                            : p.phi == LA_PHI_RELU ? dq_piece<LA_PHI_RELU>(u[q8], xv + q8 * 8, inv)
-                                                   : dq_piece<LA_PHI_IDENTITY>(u[q8], xv + q8 * 8, inv);
+                    for (int q8 = 0; q8 < 2; ++q8) {
+                        float o[8];
+                        if (p.phi == LA_PHI_ELU1)
+                            dq_vals<LA_PHI_ELU1>(u[q8], xv + q8 * 8, inv, o);
+                        else if (p.phi == LA_PHI_RELU)
+                            dq_vals<LA_PHI_RELU>(u[q8], xv + q8 * 8, inv, o);
+                        else
+                            dq_vals<LA_PHI_IDENTITY>(u[q8], xv + q8 * 8, inv, o);
+                        float4 *pq = reinterpret_cast<float4 *>(p.part_dq + ((size_t)bh * p.N + t) * D + col0 + q8 * 8);
+                        if (p.pass == 1) {
+                            if (valid) {
+                                pq[0] = make_float4(o[0], o[1], o[2], o[3]);
+                                pq[1] = make_float4(o[4], o[5], o[6], o[7]);
+                            }
+                        } else {
+                            if (valid) {
+                                const float4 a = pq[0], b2 = pq[1];
+                                o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
+                                o[4] += b2.x; o[5] += b2.y; o[6] += b2.z; o[7] += b2.w;
+                            }
+                            if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 342, smem_u32(ch[q8]) - sm_lo, q8))
+                                *reinterpret_cast<uint4 *>(ch[q8] + OFF_G) =
+                                    make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                                               pack_bf16x2(o[6], o[7]));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int q8 = 0; q8 < 2; ++q8)
+                        if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 341, smem_u32(ch[q8]) - sm_lo, q8))
+                            *reinterpret_cast<uint4 *>(ch[q8] + OFF_G) =
+                                p.phi == LA_PHI_ELU1   ? dq_piece<LA_PHI_ELU1>(u[q8], xv + q8 * 8, inv)
+                                : p.phi == LA_PHI_RELU ? dq_piece<LA_PHI_RELU>(u[q8], xv + q8 * 8, inv)
+                                                       : dq_piece<LA_PHI_IDENTITY>(u[q8], xv + q8 * 8, inv);
+                }
             }
             fence_proxy_async();
             if (i == 0 && h == 0) LA_TL(k, 12);
@@ -685,7 +760,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
 }
 
 // ---------------------------------------------------------------------------------------
-template <int D, int G, bool CAUSAL, bool MASK>
+template <int D, int G, bool CAUSAL, bool MASK, bool WT>
 __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_constant__ CUtensorMap map_q,
                                                                 const __grid_constant__ CUtensorMap map_k,
                                                                 const __grid_constant__ CUtensorMap map_v,
@@ -848,7 +923,8 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                 uint8_t *src_k = OUT_STAGE ? obuf : st + OFF_K, *src_v = OUT_STAGE ? obuf : st + OFF_V;
                 const int c0 = t0 + (nchunk - 1 - k) * C;
                 bool ok = warp_wait(&bar_dkready[s], (k / NS) & 1, &abort_flag);
-                if (ok) {
+                const bool store = !(WT && p.pass == 1);   // cos pass: dk, dv partials in fp32
+                if (ok && store) {
                     LA_TL2(k, 12);
                     for (int blk = 0; blk < K::DB; ++blk) tma_store_3d_w(&map_dk, src_k + blk * C * 128, blk * 64, c0, bg);
                     bulk_commit();
@@ -858,7 +934,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     mbar_arrive_w(&bar_stfree);
                 }
                 ok = ok && warp_wait(&bar_dvready[s], (k / NS) & 1, &abort_flag);
-                if (ok) {
+                if (ok && store) {
                     for (int blk = 0; blk < K::DB; ++blk) tma_store_3d_w(&map_dv, src_v + blk * C * 128, blk * 64, c0, bg);
                     bulk_commit();
                 }
@@ -1048,12 +1124,24 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     pres[n] = j < C && LA_CHECK(in_smem(pp[n], 16, sm_lo, sm_hi), 422, smem_u32(pp[n]) - sm_lo, j);
                     val[n] = j < nvalid;
                 }
-                if (p.phi == LA_PHI_ELU1)
-                    feat8_batch<LA_PHI_ELU1, NK>(pp, pres, val);
-                else if (p.phi == LA_PHI_RELU)
-                    feat8_batch<LA_PHI_RELU, NK>(pp, pres, val);
-                else
-                    feat8_batch<LA_PHI_IDENTITY, NK>(pp, pres, val);
+                if constexpr (WT) {   // w phi(k), phi in float32
+                    float sc[NK];
+#pragma unroll
+                    for (int n = 0; n < NK; ++n) sc[n] = pres[n] && val[n] ? p.wrow[c0 + r0 + n * RPP] : 0.f;
+                    if (p.phi == LA_PHI_ELU1)
+                        feat8_batch_scaled<LA_PHI_ELU1, NK>(pp, pres, val, sc);
+                    else if (p.phi == LA_PHI_RELU)
+                        feat8_batch_scaled<LA_PHI_RELU, NK>(pp, pres, val, sc);
+                    else
+                        feat8_batch_scaled<LA_PHI_IDENTITY, NK>(pp, pres, val, sc);
+                } else {
+                    if (p.phi == LA_PHI_ELU1)
+                        feat8_batch<LA_PHI_ELU1, NK>(pp, pres, val);
+                    else if (p.phi == LA_PHI_RELU)
+                        feat8_batch<LA_PHI_RELU, NK>(pp, pres, val);
+                    else
+                        feat8_batch<LA_PHI_IDENTITY, NK>(pp, pres, val);
+                }
             }
             fence_proxy_async();
             if (pi == 0) LA_TL2(k, 2);
@@ -1161,10 +1249,29 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                         fk[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)));
                     }
                 }
+                if constexpr (WT) {   // w phi'(k) (dk^T + r); cos pass: to the workspace (fp32),
+                                      // sin pass: plus the cos pass's
+                    const int c0 = t0 + (nchunk - 1 - k) * C;
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    *reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)) =
-                        __float2bfloat16_rn(feat_grad_from_feat(fk[e], p.phi == LA_PHI_ELU1, grad_thr) * (v[e] + r_prev));
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = c16 * 16 + e;
+                        const bool kv = c0 + j < t1;
+                        float val = feat_grad_from_feat_w(fk[e], p.phi == LA_PHI_ELU1, grad_thr, kv ? p.wrow[c0 + j] : 0.f) *
+                                    (v[e] + r_prev);
+                        float *pk = p.part_dk + ((size_t)bg * p.N + c0 + j) * D + d;
+                        if (p.pass == 1) {
+                            if (kv) *pk = val;
+                        } else {
+                            if (kv) val += *pk;
+                            *reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, j, d)) = __float2bfloat16_rn(val);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        *reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, c16 * 16 + e, d)) =
+                            __float2bfloat16_rn(feat_grad_from_feat(fk[e], p.phi == LA_PHI_ELU1, grad_thr) * (v[e] + r_prev));
+                }
             }
             fence_proxy_async();
             mbar_arrive_warp(&bar_dkready[s]);
@@ -1182,9 +1289,26 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     mbar_arrive_warp(&bar_outfree[bb]);
                 }
                 if (!ok || d >= D) continue;
+                if constexpr (WT) {   // cos pass: dv terms to the workspace; sin pass: plus those
+                    const int c0 = t0 + (nchunk - 1 - k) * C;
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, c16 * 16 + e, d)) = __float2bfloat16_rn(v[e]);
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = c16 * 16 + e;
+                        const bool kv = c0 + j < t1;
+                        float val = v[e];
+                        float *pv = p.part_dv + ((size_t)bg * p.N + c0 + j) * D + d;
+                        if (p.pass == 1) {
+                            if (kv) *pv = val;
+                        } else {
+                            if (kv) val += *pv;
+                            *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, j, d)) = __float2bfloat16_rn(val);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, c16 * 16 + e, d)) = __float2bfloat16_rn(v[e]);
+                }
             }
             fence_proxy_async();
             mbar_arrive_warp(&bar_dvready[s]);
@@ -1283,7 +1407,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
 // ---------------------------------------------------------------------------------------
 // Host side
 
-template <int D, int G, bool CAUSAL, bool MASK>
+template <int D, int G, bool CAUSAL, bool MASK, bool WT>
 cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     using K = BwdCfg<D, G>;
     CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{}, mps{}, mden{};
@@ -1297,21 +1421,69 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     if (e == cudaSuccess) e = make_map(&mdq, p.dq, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mdk, p.dk, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mdv, p.dv, p.B * p.Hkv, p.N, D, K::C);
-    if (e == cudaSuccess) e = prepare(k_tc_bwd_dq<D, G, CAUSAL, MASK>, K::DQ_SMEM);
-    if (e == cudaSuccess) e = prepare(k_tc_bwd_dkdv<D, G, CAUSAL, MASK>, K::DKDV_SMEM);
+    if (e == cudaSuccess) e = prepare(k_tc_bwd_dq<D, G, CAUSAL, MASK, WT>, K::DQ_SMEM);
+    if (e == cudaSuccess) e = prepare(k_tc_bwd_dkdv<D, G, CAUSAL, MASK, WT>, K::DKDV_SMEM);
     if (e != cudaSuccess) return e;
     const int grid = p.B * p.Hkv * p.nseg;
     {
         TraceScope ts(CAUSAL ? "tc_bwd_dq_causal" : "tc_bwd_dq_bidir", s);
-        k_tc_bwd_dq<D, G, CAUSAL, MASK><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, mps, mden, p);
+        k_tc_bwd_dq<D, G, CAUSAL, MASK, WT><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, mps, mden, p);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess)
         e = scan_segments(p.rstate, p, CAUSAL ? kScanSuffix : kScanTotal, (size_t)D * (D + 1), s);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_bwd_dkdv_causal" : "tc_bwd_dkdv_bidir", s);
-    k_tc_bwd_dkdv<D, G, CAUSAL, MASK><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mps, mk, mv, mg, mdk, mdv, p);
+    k_tc_bwd_dkdv<D, G, CAUSAL, MASK, WT><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mps, mk, mv, mg, mdk, mdv, p);
     return cudaGetLastError();
+}
+
+// h = -g . out per row (out: the forward's float32 output rows), one warp per row: the h of
+// the cos/sin-weighted backward, shared by its two passes.
+__global__ void k_h_rows(const __nv_bfloat16 *__restrict__ g, const float *__restrict__ out, float *__restrict__ h,
+                         long long rows, int D) {
+    const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= rows) return;
+    float acc = 0.f;
+    for (int d = lane; d < D; d += 32) acc = fmaf(__bfloat162float(g[row * D + d]), out[row * D + d], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) h[row] = -acc;
+}
+
+// The backward with cos/sin weights, W_ij = c_i c_j + s_i s_j, as two passes (cos, then sin)
+// of the one-term kernels with the features w phi: with gn = g / den and gd = h / den shared
+// by both terms (den, the sum of both terms' plus eps, from the forward; h = -g . out), each
+// term's gradient is the one-term backward with those features and that h, times the weight
+// where the feature is differentiated (w phi'(q), w phi'(k)); the cos pass leaves dq, dk, dv
+// in float32 in the workspace and the sin pass adds its own before rounding.
+template <int D, int G, bool MASK>
+cudaError_t backward_two_pass(const Params &p, cudaStream_t s) {
+    if (!p.cw || !p.sw || !p.part_num || !p.part_dq || !p.part_dk || !p.part_dv) return cudaErrorInvalidValue;
+    cudaError_t e = cudaSuccess;
+    if (!p.state_given) {   // the forward (two passes), its output to dq as scratch
+        Params pf = p;
+        pf.out = p.dq;
+        e = tc_forward(pf, s);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const long long rows = (long long)p.B * p.Hq * p.N;
+        TraceScope ts("tc_bwd_h_rows", s);
+        k_h_rows<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.g), p.part_num, p.gd, rows,
+                                                           D);
+        e = cudaGetLastError();
+    }
+    const size_t pass_elems = (size_t)p.B * p.Hkv * p.nseg * D * (D + 1);
+    for (int pass = 1; pass <= 2 && e == cudaSuccess; ++pass) {
+        Params pp = p;
+        pp.pass = pass;
+        pp.wrow = pass == 1 ? p.cw : p.sw;
+        pp.state = p.state + (size_t)(pass - 1) * pass_elems;
+        e = p.causal ? launch_bwd_kernels<D, G, true, MASK, true>(pp, s) : launch_bwd_kernels<D, G, false, MASK, true>(pp, s);
+    }
+    return e;
 }
 
 template <int D, int G, bool MASK = false>
@@ -1319,6 +1491,7 @@ cudaError_t backward_dg(const Params &p, cudaStream_t s) {
     if constexpr (!BwdCfg<D, G>::FITS || !BwdCfg<D, G>::TMEM_FITS) {
         return cudaErrorNotSupported;
     } else {
+        if (p.P == 2) return backward_two_pass<D, G, MASK>(p, s);
         if (!p.state_given) {
             // the forward gives the segment states, the per-row den and the record; its output
             // goes to dq, which the dq kernel overwrites
@@ -1327,7 +1500,7 @@ cudaError_t backward_dg(const Params &p, cudaStream_t s) {
             cudaError_t e = tc_forward(pf, s);
             if (e != cudaSuccess) return e;
         }
-        return p.causal ? launch_bwd_kernels<D, G, true, MASK>(p, s) : launch_bwd_kernels<D, G, false, MASK>(p, s);
+        return p.causal ? launch_bwd_kernels<D, G, true, MASK, false>(p, s) : launch_bwd_kernels<D, G, false, MASK, false>(p, s);
     }
 }
 

@@ -190,6 +190,39 @@ __device__ __forceinline__ void feat8_batch_rowscale(uint8_t *const *ptr, const 
         if (present[n]) *reinterpret_cast<uint4 *>(ptr[n]) = x[n];
 }
 
+// phi on up to NB 16-byte pieces in place, each piece n then times sc[n], as feat8_batch
+// (loads first, stores last), with phi in float32 and one rounding to bf16: the weighted
+// features w phi(x) of the cos/sin passes, and w phi(q) / den where sc = w / den.
+template <int PHI, int NB>
+__device__ __forceinline__ void feat8_batch_scaled(uint8_t *const *ptr, const bool *present, const bool *valid,
+                                                   const float *sc) {
+    uint4 x[NB];
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+        x[n] = present[n] && valid[n] ? *reinterpret_cast<const uint4 *>(ptr[n]) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int n = 0; n < NB; ++n) {
+        if (!(present[n] && valid[n])) continue;
+        uint32_t *xi = reinterpret_cast<uint32_t *>(&x[n]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = unpack_bf16x2(xi[q]);
+            float a = f.x, b = f.y;
+            if (PHI == LA_PHI_ELU1) {
+                a = a > 0.f ? a + 1.f : expf(a);
+                b = b > 0.f ? b + 1.f : expf(b);
+            } else if (PHI == LA_PHI_RELU) {
+                a = fmaxf(a, 0.f);
+                b = fmaxf(b, 0.f);
+            }
+            xi[q] = pack_bf16x2(a * sc[n], b * sc[n]);
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+        if (present[n]) *reinterpret_cast<uint4 *>(ptr[n]) = x[n];
+}
+
 // w phi(x) on 8 bf16 values (16 bytes) in place, or zeros for a row past the end: phi in
 // float32 (expf for elu+1), times the row's position weight w, rounded to bf16 once.  (The
 // cos/sin passes of the forward; one rounding keeps the weighted features as accurate as

@@ -89,9 +89,9 @@ size_t la_workspace_size(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, i
                          int has_weights, int is_bwd);
 
 /* Kernel family chosen for these arguments (host-only; for tests and reports): the
- * tensor-core kernels (LA_PATH_TCGEN05) for bfloat16 without cos/sin weights at D = 64 or 128
- * with n_rep = Hq / Hkv in {1, 2, 4, 8}, forward and backward; the CUDA-core kernels
- * (LA_PATH_SIMT) otherwise. */
+ * tensor-core kernels (LA_PATH_TCGEN05) for bfloat16 at D = 64 or 128 with n_rep = Hq / Hkv
+ * in {1, 2, 4, 8}, forward and backward (with cos/sin weights as two passes, one per term);
+ * the CUDA-core kernels (LA_PATH_SIMT) otherwise. */
 la_path la_kernel_path(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
                        int has_weights, int is_bwd);
 
@@ -113,7 +113,8 @@ la_status la_bwd(const void *q, const void *k, const void *v, const void *grad_o
 /* The same backward (same operation, same results) for a caller that has just run la_fwd
  * on these inputs: fwd_workspace / fwd_ws_bytes are that call's workspace, still holding
  * what la_fwd left there: its scanned per-segment states S, z and, on the tensor-core path,
- * every row's denominator den_i = sum_p a_i^p . z_i^p + eps and a record of the call.  When
+ * every row's denominator den_i = sum_p a_i^p . z_i^p + eps, a record of the call and, with
+ * cos/sin weights, the output rows in float32.  When
  * the forward and the backward cut the sequence the same way (the same kernel family, chunk
  * and segments; true whenever both run on the tensor-core path) the backward reads those
  * instead of recomputing them, which saves the forward's pass over q, k and v (la_bwd on the

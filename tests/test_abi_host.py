@@ -111,8 +111,8 @@ def test_workspace_sizes(lib):
 def test_tensor_core_shapes(lib):
     """bf16 without position weights runs the tensor-core kernels, forward and backward, at
     D = 64 and 128 for every n_rep in {1, 2, 4, 8} (D = 128 with n_rep 1 or 2 on tiles of a
-    larger group, rows masked); other head dimensions and n_rep values do not; with cos/sin
-    weights only the forward does."""
+    larger group, rows masked), with cos/sin weights too (two passes); other head dimensions
+    and n_rep values do not."""
     for D in (64, 128):
         for n_rep in (1, 2, 4, 8):
             for causal in (0, 1):
@@ -123,9 +123,9 @@ def test_tensor_core_shapes(lib):
         assert lib.la_kernel_path(1, 3, 1, 512, 64, la.LA_BF16, 1, 0, is_bwd) == la.LA_PATH_SIMT   # n_rep 3
         assert lib.la_kernel_path(1, 16, 1, 512, 64, la.LA_BF16, 1, 0, is_bwd) == la.LA_PATH_SIMT  # n_rep 16
         assert lib.la_kernel_path(1, 4, 4, 512, 32, la.LA_BF16, 1, 0, is_bwd) == la.LA_PATH_SIMT   # D = 32
-    # cos/sin weights: the forward on tensor cores (two passes), the backward on CUDA cores
-    assert lib.la_kernel_path(2, 16, 16, 8192, 128, la.LA_BF16, 1, 1, 0) == la.LA_PATH_TCGEN05
-    assert lib.la_kernel_path(2, 16, 16, 8192, 128, la.LA_BF16, 1, 1, 1) == la.LA_PATH_SIMT
+    # cos/sin weights: tensor cores too (two passes, one per term)
+    for is_bwd in (0, 1):
+        assert lib.la_kernel_path(2, 16, 16, 8192, 128, la.LA_BF16, 1, 1, is_bwd) == la.LA_PATH_TCGEN05
 
 
 def test_float32_always_takes_simt(lib):

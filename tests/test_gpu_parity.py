@@ -103,15 +103,16 @@ def test_tensor_core_instantiations(case):
     H.compare(w, H.run_gpu(w, dev, from_fwd=False), ref, label="bwd")
 
 
-# The cos/sin-weighted forward on tensor cores (two passes, cos then sin) at shapes with several
-# segments, ragged last chunks, every tile layout (n_rep 1 on masked rows at D = 128) and each
-# feature map; the backward of these runs on the CUDA cores.
+# The cos/sin-weighted forward and backward on tensor cores (two passes, cos then sin) at shapes
+# with several segments, ragged last chunks, every tile layout (n_rep 1 and 2 on masked rows
+# at D = 128) and each feature map; through la_bwd_from_fwd and la_bwd.
 WEIGHTED_TC_CASES = [
     # B, Hq, Hkv, N, D, causal, phi
     (2, 4, 4, 3000, 128, True, "relu"),       # n_rep 1, masked rows
     (1, 8, 8, 2500, 128, False, "elu+1"),     # n_rep 1, bidirectional
     (1, 8, 2, 2900, 128, True, "elu+1"),      # n_rep 4
     (2, 8, 1, 1500, 128, True, "relu"),       # n_rep 8
+    (1, 8, 4, 2600, 128, True, "relu"),       # n_rep 2, masked rows
     (2, 8, 8, 3000, 64, True, "elu+1"),       # n_rep 1, D = 64
     (1, 8, 4, 2100, 64, False, "relu"),       # n_rep 2, bidirectional
     (1, 6, 3, 2000, 64, True, "identity"),    # n_rep 2
@@ -119,15 +120,17 @@ WEIGHTED_TC_CASES = [
 
 
 @pytest.mark.parametrize("case", WEIGHTED_TC_CASES, ids=lambda c: "x".join(map(str, c)))
-def test_weighted_tensor_core_forward(case):
+def test_weighted_tensor_cores(case):
     B, Hq, Hkv, N, D, causal, phi = case
     w = gen.Workload(f"tcw_b{B}_hq{Hq}_hkv{Hkv}_n{N}_d{D}_{'causal' if causal else 'bidir'}_{phi}",
                      B, Hq, Hkv, N, D, "bf16", causal, phi, scale=0.5, weights=True, positive=phi == "identity")
-    assert la.kernel_path(B, Hq, Hkv, N, D, torch.bfloat16, causal, True, False) == la.LA_PATH_TCGEN05
+    for is_bwd in (False, True):
+        assert la.kernel_path(B, Hq, Hkv, N, D, torch.bfloat16, causal, True, is_bwd) == la.LA_PATH_TCGEN05
     inp = gen.make_inputs(w, seed=17)
     dev = H.to_dev(inp)
     ref = H.run_oracle(w, inp)
-    H.compare(w, H.run_gpu(w, dev, from_fwd=True), ref, label="weighted forward on tensor cores")
+    H.compare(w, H.run_gpu(w, dev, from_fwd=True), ref, label="weighted, bwd_from_fwd")
+    H.compare(w, H.run_gpu(w, dev, from_fwd=False), ref, label="weighted, bwd")
 
 
 # With a single visible key (N = 1) the exact dq and dk equal b (g . v) eps / den^2: the
@@ -211,7 +214,7 @@ def test_deterministic():
 GUARD_CASES = [
     # B, Hq, Hkv, N, D, dtype, weights   (N leaves a ragged last chunk on every path)
     (1, 4, 2, 77, 64, "f32", True),      # CUDA-core kernels
-    (1, 4, 2, 77, 64, "bf16", True),     # CUDA-core kernels (position weights)
+    (1, 4, 2, 77, 64, "bf16", True),     # tensor-core kernels, cos/sin passes
     (1, 8, 2, 205, 128, "bf16", False),  # tensor-core kernels, n_rep 4, TMA-store epilogues
     (1, 2, 2, 141, 64, "bf16", False),   # tensor-core kernels, n_rep 1
     (1, 4, 2, 205, 128, "bf16", False),  # tensor-core kernels with masked rows (n_rep 2)
@@ -288,12 +291,12 @@ def test_binding_errors_are_raised():
     ("causal_b1_h2_n256_d32_f32", la.LA_PATH_SIMT, la.LA_PATH_SIMT),
     ("bidir_b2_h8_n2048_d64_bf16_elu1", la.LA_PATH_TCGEN05, la.LA_PATH_TCGEN05),
     ("causal_b4_h16_n4096_d64_bf16", la.LA_PATH_TCGEN05, la.LA_PATH_TCGEN05),
-    ("cosformer_causal_b2_h16_n8192_d128_bf16", la.LA_PATH_TCGEN05, la.LA_PATH_SIMT),
+    ("cosformer_causal_b2_h16_n8192_d128_bf16", la.LA_PATH_TCGEN05, la.LA_PATH_TCGEN05),
     ("gqa_causal_b1_hq32_hkv8_n65536_d128_bf16", la.LA_PATH_TCGEN05, la.LA_PATH_TCGEN05),
 ])
 def test_kernel_family(name, fwd_path, bwd_path):
-    """The bf16 workloads run the tcgen05 forward (with cos/sin weights as two passes) and,
-    without weights, the tcgen05 backward."""
+    """The bf16 workloads run the tcgen05 forward and backward (with cos/sin weights as two
+    passes, one per term)."""
     w = gen.WORKLOADS[name]
     assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, False) == fwd_path
     assert la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, True) == bwd_path
