@@ -715,15 +715,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                     }
                     if constexpr (WT) {   // sin pass: plus the cos terms' numerator; the float32
                                           // output row goes back in its place (the backward's h)
-                        if (p.pass == 2 && ok && rowok) {
+                        if (p.pass == 2 && ok && rowok) {   // (every load before any store)
                             float4 *src = reinterpret_cast<float4 *>(p.part_num + rg * D + c64 * 64 + hh * 32);
+                            float4 a[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) a[q] = src[q];
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
-                                const float4 a = src[q];
-                                v[4 * q] += a.x;
-                                v[4 * q + 1] += a.y;
-                                v[4 * q + 2] += a.z;
-                                v[4 * q + 3] += a.w;
+                                v[4 * q] += a[q].x;
+                                v[4 * q + 1] += a[q].y;
+                                v[4 * q + 2] += a[q].z;
+                                v[4 * q + 3] += a[q].w;
                                 src[q] = make_float4(v[4 * q] * inv, v[4 * q + 1] * inv, v[4 * q + 2] * inv, v[4 * q + 3] * inv);
                             }
                         }

@@ -691,6 +691,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 }
                 if (!ok) continue;
                 if constexpr (WT) {   // cos pass: dq terms (fp32) to the workspace; sin pass: plus those
+                    float4 *pq = reinterpret_cast<float4 *>(p.part_dq + ((size_t)bh * p.N + t) * D + col0);
+                    float4 prev[4] = {};
+                    if (p.pass == 2 && valid)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) prev[q] = __ldg(pq + q);
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8) {
                         float o[8];
@@ -700,18 +705,15 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                             dq_vals<LA_PHI_RELU>(u[q8], xv + q8 * 8, inv, o);
                         else
                             dq_vals<LA_PHI_IDENTITY>(u[q8], xv + q8 * 8, inv, o);
-                        float4 *pq = reinterpret_cast<float4 *>(p.part_dq + ((size_t)bh * p.N + t) * D + col0 + q8 * 8);
                         if (p.pass == 1) {
                             if (valid) {
-                                pq[0] = make_float4(o[0], o[1], o[2], o[3]);
-                                pq[1] = make_float4(o[4], o[5], o[6], o[7]);
+                                pq[2 * q8] = make_float4(o[0], o[1], o[2], o[3]);
+                                pq[2 * q8 + 1] = make_float4(o[4], o[5], o[6], o[7]);
                             }
                         } else {
-                            if (valid) {
-                                const float4 a = pq[0], b2 = pq[1];
-                                o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
-                                o[4] += b2.x; o[5] += b2.y; o[6] += b2.z; o[7] += b2.w;
-                            }
+                            const float4 a = prev[2 * q8], b2 = prev[2 * q8 + 1];
+                            o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
+                            o[4] += b2.x; o[5] += b2.y; o[6] += b2.z; o[7] += b2.w;
                             if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 342, smem_u32(ch[q8]) - sm_lo, q8))
                                 *reinterpret_cast<uint4 *>(ch[q8] + OFF_G) =
                                     make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
@@ -1250,20 +1252,28 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     }
                 }
                 if constexpr (WT) {   // w phi'(k) (dk^T + r); cos pass: to the workspace (fp32),
-                                      // sin pass: plus the cos pass's
+                                      // sin pass: plus the cos pass's (every load before any store)
                     const int c0 = t0 + (nchunk - 1 - k) * C;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int j = c16 * 16 + e;
-                        const bool kv = c0 + j < t1;
-                        float val = feat_grad_from_feat_w(fk[e], p.phi == LA_PHI_ELU1, grad_thr, kv ? p.wrow[c0 + j] : 0.f) *
-                                    (v[e] + r_prev);
-                        float *pk = p.part_dk + ((size_t)bg * p.N + c0 + j) * D + d;
-                        if (p.pass == 1) {
-                            if (kv) *pk = val;
-                        } else {
-                            if (kv) val += *pk;
-                            *reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, j, d)) = __float2bfloat16_rn(val);
+                    for (int e8 = 0; e8 < 16; e8 += 8) {
+                        float wv[8], prev[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = c16 * 16 + e8 + e;
+                            const bool kv = c0 + j < t1;
+                            wv[e] = kv ? __ldg(p.wrow + c0 + j) : 0.f;
+                            prev[e] = kv && p.pass == 2 ? __ldg(p.part_dk + ((size_t)bg * p.N + c0 + j) * D + d) : 0.f;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = c16 * 16 + e8 + e;
+                            const float val =
+                                feat_grad_from_feat_w(fk[e8 + e], p.phi == LA_PHI_ELU1, grad_thr, wv[e]) * (v[e8 + e] + r_prev);
+                            if (p.pass == 1) {
+                                if (c0 + j < t1) p.part_dk[((size_t)bg * p.N + c0 + j) * D + d] = val;
+                            } else {
+                                *reinterpret_cast<__nv_bfloat16 *>(kw + swz_offset(C, j, d)) = __float2bfloat16_rn(val + prev[e]);
+                            }
                         }
                     }
                 } else {
@@ -1291,17 +1301,23 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                 if (!ok || d >= D) continue;
                 if constexpr (WT) {   // cos pass: dv terms to the workspace; sin pass: plus those
                     const int c0 = t0 + (nchunk - 1 - k) * C;
+                    if (p.pass == 1) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int j = c16 * 16 + e;
-                        const bool kv = c0 + j < t1;
-                        float val = v[e];
-                        float *pv = p.part_dv + ((size_t)bg * p.N + c0 + j) * D + d;
-                        if (p.pass == 1) {
-                            if (kv) *pv = val;
-                        } else {
-                            if (kv) val += *pv;
-                            *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, j, d)) = __float2bfloat16_rn(val);
+                        for (int e = 0; e < 16; ++e)
+                            if (c0 + c16 * 16 + e < t1) p.part_dv[((size_t)bg * p.N + c0 + c16 * 16 + e) * D + d] = v[e];
+                    } else {
+#pragma unroll
+                        for (int e8 = 0; e8 < 16; e8 += 8) {
+                            float prev[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int j = c16 * 16 + e8 + e;
+                                prev[e] = c0 + j < t1 ? __ldg(p.part_dv + ((size_t)bg * p.N + c0 + j) * D + d) : 0.f;
+                            }
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, c16 * 16 + e8 + e, d)) =
+                                    __float2bfloat16_rn(v[e8 + e] + prev[e]);
                         }
                     }
                 } else {
