@@ -156,7 +156,8 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
 la_status run(bool bwd, const void *q, const void *k, const void *v, const void *g, void *out,
               void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int D, la_dtype dt,
               int causal, la_phi phi, float eps, const float *cw, const float *sw, void *ws,
-              size_t ws_bytes, void *stream, const void *fwd_ws = nullptr, size_t fwd_ws_bytes = 0) {
+              size_t ws_bytes, void *stream, const void *fwd_ws = nullptr, size_t fwd_ws_bytes = 0,
+              const la_strides *const *strides = nullptr) {
     la_status st = check_shape(B, Hq, Hkv, N, D, dt, phi, eps, cw, sw);
     if (st != LA_OK) return st;
     if (!q || !k || !v) return LA_ERR_ARG;
@@ -164,14 +165,26 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     const void *ptrs[] = {q, k, v, g, out, dq, dk, dv, cw, sw};
     for (const void *ptr : ptrs)
         if (ptr && !aligned(ptr, 16)) return LA_ERR_ALIGN;
+    // input strides (q, k, v, grad_out): contiguous unless given
+    Strides ist[4] = {contiguous_strides(Hq, N, D), contiguous_strides(Hkv, N, D), contiguous_strides(Hkv, N, D),
+                     contiguous_strides(Hq, N, D)};
+    for (int i = 0; strides && i < 4; ++i)
+        if (strides[i]) {
+            if (strides[i]->b < 0 || strides[i]->h < 0 || strides[i]->n < 0) return LA_ERR_ARG;
+            ist[i] = Strides{strides[i]->b, strides[i]->h, strides[i]->n};
+        }
     const Plan pl = make_plan(B, Hq, Hkv, N, D, dt, causal, cw != nullptr, bwd);
     if (pl.ws_bytes > 0) {
         if (!ws || ws_bytes < pl.ws_bytes) return LA_ERR_WORKSPACE;
         if (!aligned(ws, 256)) return LA_ERR_ALIGN;
     }
+    if (pl.path == LA_PATH_TCGEN05)   // TMA: every stride a multiple of 16 bytes (8 bf16)
+        for (const Strides &x : ist)
+            if (x.b % 8 || x.h % 8 || x.n % 8) return LA_ERR_ALIGN;
 
     Params p{};
     p.q = q; p.k = k; p.v = v; p.g = g;
+    p.st_q = ist[0]; p.st_k = ist[1]; p.st_v = ist[2]; p.st_g = ist[3];
     p.out = out; p.dq = dq; p.dk = dk; p.dv = dv;
     p.cw = cw; p.sw = sw;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.D = D; p.n_rep = Hq / Hkv;
@@ -304,6 +317,25 @@ la_status la_bwd_from_fwd(const void *q, const void *k, const void *v, const voi
     if (!fwd_workspace) return LA_ERR_ARG;
     return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, dtype, is_causal, phi, eps,
                cos_weight, sin_weight, workspace, ws_bytes, stream, fwd_workspace, fwd_ws_bytes);
+}
+
+la_status la_fwd_strided(const void *q, const void *k, const void *v, void *out, int B, int Hq, int Hkv, int N, int D,
+                         la_dtype dtype, int is_causal, la_phi phi, float eps, const float *cos_weight,
+                         const float *sin_weight, const la_strides *q_strides, const la_strides *k_strides,
+                         const la_strides *v_strides, void *workspace, size_t ws_bytes, void *stream) {
+    const la_strides *st[4] = {q_strides, k_strides, v_strides, nullptr};
+    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, dtype, is_causal, phi, eps,
+               cos_weight, sin_weight, workspace, ws_bytes, stream, nullptr, 0, st);
+}
+la_status la_bwd_strided(const void *q, const void *k, const void *v, const void *grad_out, void *dq, void *dk, void *dv,
+                         int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal, la_phi phi, float eps,
+                         const float *cos_weight, const float *sin_weight, const la_strides *q_strides,
+                         const la_strides *k_strides, const la_strides *v_strides, const la_strides *g_strides,
+                         const void *fwd_workspace, size_t fwd_ws_bytes, void *workspace, size_t ws_bytes,
+                         void *stream) {
+    const la_strides *st[4] = {q_strides, k_strides, v_strides, g_strides};
+    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, dtype, is_causal, phi, eps, cos_weight,
+               sin_weight, workspace, ws_bytes, stream, fwd_workspace, fwd_ws_bytes, st);
 }
 
 la_status la_get_status(void *stream) {

@@ -27,10 +27,19 @@ constexpr int kErrStaleWorkspace = 2;   // la_bwd_from_fwd got a workspace anoth
 constexpr int kHdrWords = 16;
 constexpr int kHdrMagic = 0x4c414631;
 
+// Element strides of a [B, H, N, D] tensor along B, H and N (D is contiguous).
+struct Strides {
+    long long b, h, n;
+};
+inline Strides contiguous_strides(int H, int N, int D) {
+    return Strides{(long long)H * N * D, (long long)N * D, (long long)D};
+}
+
 // Everything a kernel needs.  Tensor pointers are typed void: the element type is a
 // template parameter of each kernel.
 struct Params {
     const void *q, *k, *v, *g;   // inputs ([B,Hq,N,D] for q, g; [B,Hkv,N,D] for k, v)
+    Strides st_q, st_k, st_v, st_g;   // their strides (outputs and workspace rows are contiguous)
     void *out, *dq, *dk, *dv;    // outputs
     const float *cw, *sw;        // position weights or null
     int B, Hq, Hkv, N, D, n_rep, P, phi, causal;

@@ -41,9 +41,10 @@ __device__ __forceinline__ Seg my_segment(const Params &p) {
     return r;
 }
 
+// Head bh = b H + h of an input with element strides st (rows t at t st.n).
 template <typename T>
-__device__ __forceinline__ const T *head_ptr(const void *base, int bh, int N, int D) {
-    return static_cast<const T *>(base) + (size_t)bh * N * D;
+__device__ __forceinline__ const T *head_ptr(const void *base, const Strides &st, int bh, int H) {
+    return static_cast<const T *>(base) + (long long)(bh / H) * st.b + (long long)(bh % H) * st.h;
 }
 
 // Key/value chunk [c0, c0 + kC) clipped to t1: bsm[term][j][d] = w_j^term phi(k_jd),
@@ -56,8 +57,8 @@ __device__ void load_kv(const Params &p, const T *kb, const T *vb, int c0, int t
     for (int idx = threadIdx.x; idx < kC * D; idx += kThreads) {
         const int j = idx / D, d = idx - j * D, t = c0 + j;
         const bool ok = t < t1;
-        const float kv = ok ? to_f32(kb[(size_t)t * D + d]) : 0.f;
-        const float vv = ok ? to_f32(vb[(size_t)t * D + d]) : 0.f;
+        const float kv = ok ? to_f32(kb[(long long)t * p.st_k.n + d]) : 0.f;
+        const float vv = ok ? to_f32(vb[(long long)t * p.st_v.n + d]) : 0.f;
         const float f = ok ? feature(kv, p.phi) : 0.f;
 #pragma unroll
         for (int term = 0; term < P; ++term)
@@ -75,7 +76,7 @@ __device__ void load_q(const Params &p, const T *qb, int c0, int t1, float *asm_
     for (int idx = threadIdx.x; idx < kC * D; idx += kThreads) {
         const int i = idx / D, d = idx - i * D, t = c0 + i;
         const bool ok = t < t1;
-        const float qv = ok ? to_f32(qb[(size_t)t * D + d]) : 0.f;
+        const float qv = ok ? to_f32(qb[(long long)t * p.st_q.n + d]) : 0.f;
         const float f = ok ? feature(qv, p.phi) : 0.f;
 #pragma unroll
         for (int term = 0; term < P; ++term)
@@ -92,7 +93,7 @@ __device__ void load_gx(const Params &p, const T *gb, const float *denb, const f
     for (int idx = threadIdx.x; idx < kC * DP; idx += kThreads) {
         const int i = idx / DP, e = idx - i * DP, t = c0 + i;
         float x = 0.f;
-        if (t < t1) x = (e < D) ? to_f32(gb[(size_t)t * D + e]) / denb[t] : gdb[t];
+        if (t < t1) x = (e < D) ? to_f32(gb[(long long)t * p.st_g.n + e]) / denb[t] : gdb[t];
         gx[idx] = x;
     }
 }
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) k_seg_state(Params p) {
     float *S = sm, *bsm = S + P * D * DP, *vsm = bsm + P * kC * DP;
     const Seg sg = my_segment(p);
     for (int i = threadIdx.x; i < P * D * DP; i += kThreads) S[i] = 0.f;
-    const T *kb = head_ptr<T>(p.k, sg.bg, p.N, D), *vb = head_ptr<T>(p.v, sg.bg, p.N, D);
+    const T *kb = head_ptr<T>(p.k, p.st_k, sg.bg, p.Hkv), *vb = head_ptr<T>(p.v, p.st_v, sg.bg, p.Hkv);
     for (int c0 = sg.t0; c0 < sg.t1; c0 += kC) {
         __syncthreads();
         load_kv<T, D, P>(p, kb, vb, c0, sg.t1, bsm, vsm, nullptr);
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kThreads) k_fwd(Params p) {
           *Asm = vsm + kC * DP;
     const Seg sg = my_segment(p);
     load_state<D, P>(S, p.state + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DP));
-    const T *kb = head_ptr<T>(p.k, sg.bg, p.N, D), *vb = head_ptr<T>(p.v, sg.bg, p.N, D);
+    const T *kb = head_ptr<T>(p.k, p.st_k, sg.bg, p.Hkv), *vb = head_ptr<T>(p.v, p.st_v, sg.bg, p.Hkv);
     const int i = threadIdx.x / 16, l = threadIdx.x % 16;
     for (int c0 = sg.t0; c0 < sg.t1; c0 += kC) {
         __syncthreads();
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) k_fwd(Params p) {
         for (int r = 0; r < p.n_rep; ++r) {
             const int bh = sg.b * p.Hq + sg.g * p.n_rep + r;
             __syncthreads();
-            load_q<T, D, P>(p, head_ptr<T>(p.q, bh, p.N, D), c0, sg.t1, asm_, nullptr);
+            load_q<T, D, P>(p, head_ptr<T>(p.q, p.st_q, bh, p.Hq), c0, sg.t1, asm_, nullptr);
             __syncthreads();
             if (p.causal) intra_scores<D, P>(asm_, bsm, Asm);
             __syncthreads();
@@ -265,16 +266,16 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
           *qraw = vsm + kC * DP, *gx = qraw + kC * DP, *Asm = gx + kC * DP, *dAsm = Asm + kC * kC;
     const Seg sg = my_segment(p);
     load_state<D, P>(S, p.state + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DP));
-    const T *kb = head_ptr<T>(p.k, sg.bg, p.N, D), *vb = head_ptr<T>(p.v, sg.bg, p.N, D);
+    const T *kb = head_ptr<T>(p.k, p.st_k, sg.bg, p.Hkv), *vb = head_ptr<T>(p.v, p.st_v, sg.bg, p.Hkv);
     const int i = threadIdx.x / 16, l = threadIdx.x % 16;
     for (int c0 = sg.t0; c0 < sg.t1; c0 += kC) {
         __syncthreads();
         load_kv<T, D, P>(p, kb, vb, c0, sg.t1, bsm, vsm, nullptr);
         for (int r = 0; r < p.n_rep; ++r) {
             const int bh = sg.b * p.Hq + sg.g * p.n_rep + r;
-            const T *gb = head_ptr<T>(p.g, bh, p.N, D);
+            const T *gb = head_ptr<T>(p.g, p.st_g, bh, p.Hq);
             __syncthreads();
-            load_q<T, D, P>(p, head_ptr<T>(p.q, bh, p.N, D), c0, sg.t1, asm_, qraw);
+            load_q<T, D, P>(p, head_ptr<T>(p.q, p.st_q, bh, p.Hq), c0, sg.t1, asm_, qraw);
             __syncthreads();
             if (p.causal) intra_scores<D, P>(asm_, bsm, Asm);
             __syncthreads();
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
             float gv[M], gdot = 0.f;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                gv[m] = ok ? to_f32(gb[(size_t)t * D + l + 16 * m]) : 0.f;
+                gv[m] = ok ? to_f32(gb[(long long)t * p.st_g.n + l + 16 * m]) : 0.f;
                 gdot += gv[m] * acc[m];
             }
             gdot = row_sum16(gdot);
@@ -390,8 +391,8 @@ __global__ void __launch_bounds__(kThreads) k_seg_rstate(Params p) {
         for (int r = 0; r < p.n_rep; ++r) {
             const int bh = sg.b * p.Hq + sg.g * p.n_rep + r;
             __syncthreads();
-            load_q<T, D, P>(p, head_ptr<T>(p.q, bh, p.N, D), c0, sg.t1, asm_, nullptr);
-            load_gx<T, D>(p, head_ptr<T>(p.g, bh, p.N, D), p.den + (size_t)bh * p.N,
+            load_q<T, D, P>(p, head_ptr<T>(p.q, p.st_q, bh, p.Hq), c0, sg.t1, asm_, nullptr);
+            load_gx<T, D>(p, head_ptr<T>(p.g, p.st_g, bh, p.Hq), p.den + (size_t)bh * p.N,
                           p.gd + (size_t)bh * p.N, c0, sg.t1, gx);
             __syncthreads();
             state_update<D, P>(R, asm_, gx);
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dkdv(Params p) {
           *kraw = vsm + kC * DP, *gx = kraw + kC * DP, *Asm = gx + kC * DP, *dAsm = Asm + kC * kC;
     const Seg sg = my_segment(p);
     load_state<D, P>(R, p.rstate + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DP));
-    const T *kb = head_ptr<T>(p.k, sg.bg, p.N, D), *vb = head_ptr<T>(p.v, sg.bg, p.N, D);
+    const T *kb = head_ptr<T>(p.k, p.st_k, sg.bg, p.Hkv), *vb = head_ptr<T>(p.v, p.st_v, sg.bg, p.Hkv);
     const int j = threadIdx.x / 16, l = threadIdx.x % 16;
     const int nchunks = (sg.t1 - sg.t0 + kC - 1) / kC;
     for (int c = nchunks - 1; c >= 0; --c) {
@@ -448,8 +449,8 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dkdv(Params p) {
         for (int r = 0; p.causal && r < p.n_rep; ++r) {
             const int bh = sg.b * p.Hq + sg.g * p.n_rep + r;
             __syncthreads();
-            load_q<T, D, P>(p, head_ptr<T>(p.q, bh, p.N, D), c0, sg.t1, asm_, nullptr);
-            load_gx<T, D>(p, head_ptr<T>(p.g, bh, p.N, D), p.den + (size_t)bh * p.N,
+            load_q<T, D, P>(p, head_ptr<T>(p.q, p.st_q, bh, p.Hq), c0, sg.t1, asm_, nullptr);
+            load_gx<T, D>(p, head_ptr<T>(p.g, p.st_g, bh, p.Hq), p.den + (size_t)bh * p.N,
                           p.gd + (size_t)bh * p.N, c0, sg.t1, gx);
             __syncthreads();
             {

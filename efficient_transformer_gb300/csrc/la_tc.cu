@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
     (void)sm_hi;
     const int warp = threadIdx.x / 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
+    const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int t0 = seg * p.seg_len, t1 = min(p.N, t0 + p.seg_len);
     const int nchunk = (t1 - t0 + C - 1) / C;
 
@@ -200,8 +201,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
                 if (!LA_CHECK(in_smem(st, K::STAGE, sm_lo, sm_hi) && c0 < p.N, 101, smem_u32(st) - sm_lo, c0)) break;
                 mbar_arrive_expect_tx_w(&bar_full[s], K::STAGE);
                 for (int blk = 0; blk < K::DB; ++blk) {
-                    tma_load_3d_w(st + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
-                    tma_load_3d_w(st + K::K_BYTES + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
+                    tma_load_4d_w(st + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, g, b);
+                    tma_load_4d_w(st + K::K_BYTES + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, g, b);
                 }
                 issued = k + 1;
             }
@@ -383,11 +384,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                 mbar_arrive_expect_tx_w(&bar_full[s], bytes);
                 for (int r = 0; r < gr; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_full[s], blk * 64, c0, bh0 + r);
+                        tma_load_4d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_full[s], blk * 64, c0, g * gr + r, b);
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk) {
-                        tma_load_3d_w(st + OFF_K + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, bg);
-                        tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, bg);
+                        tma_load_4d_w(st + OFF_K + blk * C * 128, &map_k, &bar_full[s], blk * 64, c0, g, b);
+                        tma_load_4d_w(st + OFF_V + blk * C * 128, &map_v, &bar_full[s], blk * 64, c0, g, b);
                     }
                 issued = k + 1;
             }
@@ -767,8 +768,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
 template <int D, bool WT>
 cudaError_t launch_state(const Params &p, cudaStream_t s) {
     CUtensorMap mk{}, mv{};
-    cudaError_t e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, StateCfg<D>::C);
-    if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, StateCfg<D>::C);
+    cudaError_t e = make_map_in(&mk, p.k, p.B, p.Hkv, p.N, D, p.st_k, StateCfg<D>::C);
+    if (e == cudaSuccess) e = make_map_in(&mv, p.v, p.B, p.Hkv, p.N, D, p.st_v, StateCfg<D>::C);
     if (e == cudaSuccess) e = prepare(k_tc_state<D, WT>, StateCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     TraceScope ts("tc_seg_state", s);
@@ -780,9 +781,9 @@ template <int D, int G, bool CAUSAL, bool MASK, bool WT>
 cudaError_t launch_fwd(const Params &p, cudaStream_t s) {
     using K = FwdCfg<D, G>;
     CUtensorMap mq{}, mk{}, mv{}, mo{};
-    cudaError_t e = make_map(&mq, p.q, p.B * p.Hq, p.N, D, K::C);
-    if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
-    if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, K::C);
+    cudaError_t e = make_map_in(&mq, p.q, p.B, p.Hq, p.N, D, p.st_q, K::C);
+    if (e == cudaSuccess) e = make_map_in(&mk, p.k, p.B, p.Hkv, p.N, D, p.st_k, K::C);
+    if (e == cudaSuccess) e = make_map_in(&mv, p.v, p.B, p.Hkv, p.N, D, p.st_v, K::C);
     if (e == cudaSuccess) e = make_map(&mo, p.out, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = prepare(k_tc_fwd<D, G, CAUSAL, MASK, WT>, K::SMEM);
     if (e != cudaSuccess) return e;

@@ -298,20 +298,20 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                 mbar_arrive_expect_tx_w(&bar_fulla[s], bytes_a);
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d_w(st + OFF_K + blk * C * 128, &map_k, &bar_fulla[s], blk * 64, c0, bg);
+                        tma_load_4d_w(st + OFF_K + blk * C * 128, &map_k, &bar_fulla[s], blk * 64, c0, g, b);
                 for (int r = 0; r < gr; ++r) {
                     tma_load_2d_w(st + OFF_DEN + r * K::DPAD * 4, &map_den, &bar_fulla[s], c0, bh0 + r);
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fulla[s], blk * 64, c0, bh0 + r);
+                        tma_load_4d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fulla[s], blk * 64, c0, g * gr + r, b);
                 }
                 if (CAUSAL)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fulla[s], blk * 64, c0, bg);
+                        tma_load_4d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fulla[s], blk * 64, c0, g, b);
                 mbar_arrive_expect_tx_w(&bar_fullg[s], bytes_g);
                 for (int r = 0; r < gr; ++r)
                     for (int blk = 0; blk < K::DB; ++blk)
-                        tma_load_3d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64, c0,
-                                      bh0 + r);
+                        tma_load_4d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64, c0,
+                                      g * gr + r, b);
                 issued = k + 1;
             }
             for (int k = issued > NS ? issued - NS : 0; k < issued; ++k) {
@@ -883,19 +883,19 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                     mbar_arrive_expect_tx_w(&bar_fullq[s], (uint32_t)(gr * C * D * 2));
                     for (int r = 0; r < gr; ++r)
                         for (int blk = 0; blk < K::DB; ++blk)
-                            tma_load_3d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fullq[s], blk * 64, c0,
-                                        bh0 + r);
+                            tma_load_4d_w(st + blk * 128 * 128 + r * C * 128, &map_q, &bar_fullq[s], blk * 64, c0,
+                                        g * gr + r, b);
                     mbar_arrive_expect_tx_w(&bar_fullg[s], (uint32_t)(gr * C * D * 2));
                     for (int r = 0; r < gr; ++r)
                         for (int blk = 0; blk < K::DB; ++blk)
-                            tma_load_3d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64,
-                                        c0, bh0 + r);
+                            tma_load_4d_w(st + OFF_G + blk * 128 * 128 + r * C * 128, &map_g, &bar_fullg[s], blk * 64,
+                                        c0, g * gr + r, b);
                 }
                 if (k >= NS && !warp_wait(&bar_emptykv[s], ((k / NS) - 1) & 1, &abort_flag)) break;
                 mbar_arrive_expect_tx_w(&bar_fullkv[s], K::K_BYTES + K::V_BYTES);
                 for (int blk = 0; blk < K::DB; ++blk) {
-                    tma_load_3d_w(st + OFF_K + blk * C * 128, &map_k, &bar_fullkv[s], blk * 64, c0, bg);
-                    tma_load_3d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fullkv[s], blk * 64, c0, bg);
+                    tma_load_4d_w(st + OFF_K + blk * C * 128, &map_k, &bar_fullkv[s], blk * 64, c0, g, b);
+                    tma_load_4d_w(st + OFF_V + blk * C * 128, &map_v, &bar_fullkv[s], blk * 64, c0, g, b);
                 }
                 issued = k + 1;
             }
@@ -1426,14 +1426,19 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
 template <int D, int G, bool CAUSAL, bool MASK, bool WT>
 cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     using K = BwdCfg<D, G>;
-    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{}, mps{}, mden{};
-    cudaError_t e = make_map(&mq, p.q, p.B * p.Hq, p.N, D, K::C);
+    CUtensorMap mq{}, mk{}, mv{}, mg{}, mdq{}, mdk{}, mdv{}, mps{}, mqs{}, mden{};
+    // inputs through 4-D maps with the caller's strides; outputs (and phi_s) contiguous
+    cudaError_t e = make_map_in(&mq, p.q, p.B, p.Hq, p.N, D, p.st_q, K::C);
     if (e == cudaSuccess) e = make_map_rows_f32(&mden, p.den, p.B * p.Hq, p.N, p.den_stride, K::C);
-    // phi(q) / den rows: written by the dq kernel, read by the dk/dv kernel in place of q
-    if (e == cudaSuccess) e = make_map(&mps, CAUSAL ? p.phis : p.q, p.B * p.Hq, p.N, D, K::C);
-    if (e == cudaSuccess) e = make_map(&mk, p.k, p.B * p.Hkv, p.N, D, K::C);
-    if (e == cudaSuccess) e = make_map(&mv, p.v, p.B * p.Hkv, p.N, D, K::C);
-    if (e == cudaSuccess) e = make_map(&mg, p.g, p.B * p.Hq, p.N, D, K::C);
+    // phi(q) / den rows: written by the dq kernel (mps), read by the dk/dv kernel in place of q
+    // (mqs; bidirectional: q itself, and mps is not used)
+    if (e == cudaSuccess) e = make_map(&mps, CAUSAL ? p.phis : p.dq, p.B * p.Hq, p.N, D, K::C);
+    if (e == cudaSuccess)
+        e = CAUSAL ? make_map_in(&mqs, p.phis, p.B, p.Hq, p.N, D, contiguous_strides(p.Hq, p.N, D), K::C)
+                   : make_map_in(&mqs, p.q, p.B, p.Hq, p.N, D, p.st_q, K::C);
+    if (e == cudaSuccess) e = make_map_in(&mk, p.k, p.B, p.Hkv, p.N, D, p.st_k, K::C);
+    if (e == cudaSuccess) e = make_map_in(&mv, p.v, p.B, p.Hkv, p.N, D, p.st_v, K::C);
+    if (e == cudaSuccess) e = make_map_in(&mg, p.g, p.B, p.Hq, p.N, D, p.st_g, K::C);
     if (e == cudaSuccess) e = make_map(&mdq, p.dq, p.B * p.Hq, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mdk, p.dk, p.B * p.Hkv, p.N, D, K::C);
     if (e == cudaSuccess) e = make_map(&mdv, p.dv, p.B * p.Hkv, p.N, D, K::C);
@@ -1450,19 +1455,21 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
         e = scan_segments(p.rstate, p, CAUSAL ? kScanSuffix : kScanTotal, (size_t)D * (D + 1), s);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_bwd_dkdv_causal" : "tc_bwd_dkdv_bidir", s);
-    k_tc_bwd_dkdv<D, G, CAUSAL, MASK, WT><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mps, mk, mv, mg, mdk, mdv, p);
+    k_tc_bwd_dkdv<D, G, CAUSAL, MASK, WT><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mqs, mk, mv, mg, mdk, mdv, p);
     return cudaGetLastError();
 }
 
 // h = -g . out per row (out: the forward's float32 output rows), one warp per row: the h of
 // the cos/sin-weighted backward, shared by its two passes.
-__global__ void k_h_rows(const __nv_bfloat16 *__restrict__ g, const float *__restrict__ out, float *__restrict__ h,
-                         long long rows, int D) {
-    const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+__global__ void k_h_rows(const __nv_bfloat16 *__restrict__ g, Strides sg, int H, int N, const float *__restrict__ out,
+                         float *__restrict__ h, long long rows, int D) {
+    const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;   // bh N + t
     const int lane = threadIdx.x % 32;
     if (row >= rows) return;
+    const long long bh = row / N, t = row % N;
+    const __nv_bfloat16 *gr = g + (bh / H) * sg.b + (bh % H) * sg.h + t * sg.n;
     float acc = 0.f;
-    for (int d = lane; d < D; d += 32) acc = fmaf(__bfloat162float(g[row * D + d]), out[row * D + d], acc);
+    for (int d = lane; d < D; d += 32) acc = fmaf(__bfloat162float(gr[d]), out[row * D + d], acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) h[row] = -acc;
@@ -1487,8 +1494,8 @@ cudaError_t backward_two_pass(const Params &p, cudaStream_t s) {
     {
         const long long rows = (long long)p.B * p.Hq * p.N;
         TraceScope ts("tc_bwd_h_rows", s);
-        k_h_rows<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.g), p.part_num, p.gd, rows,
-                                                           D);
+        k_h_rows<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.g), p.st_g, p.Hq, p.N,
+                                                           p.part_num, p.gd, rows, D);
         e = cudaGetLastError();
     }
     const size_t pass_elems = (size_t)p.B * p.Hkv * p.nseg * D * (D + 1);

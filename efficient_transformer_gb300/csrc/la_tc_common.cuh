@@ -332,6 +332,22 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int heads, int N, int D,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 4-D map over an input [B, H, N, D] (bf16) with element strides st (b, h, n; d contiguous,
+// each a multiple of 8 elements), dims (D, N, H, B): box {64, rows, 1, 1}, 128-byte swizzle;
+// loads give the coordinates (d, t, h, b) to tma_load_4d_w.
+cudaError_t make_map_in(CUtensorMap *map, const void *ptr, int B, int H, int N, int D, const Strides &st, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)st.n * 2, (cuuint64_t)st.h * 2, (cuuint64_t)st.b * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // 2-D map over float32 rows [heads][N] with a row stride of `stride` floats (a multiple of
 // 4): box {cols, 1}, no swizzle; columns past N read as zeros.
 cudaError_t make_map_rows_f32(CUtensorMap *map, const void *ptr, int heads, int N, int stride, int cols) {

@@ -341,6 +341,17 @@ __device__ __forceinline__ void tma_load_3d_w(void *dst, const CUtensorMap *map,
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z,
+                                              int w) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "@e cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+        "[%2];\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
+
 __device__ __forceinline__ void tma_load_2d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"

@@ -6,7 +6,9 @@ phi="elu+1", eps=1e-6, cos_weight=None, sin_weight=None)`` and ``bwd(q, k, v, gr
 ...) -> (dq, dk, dv)``.  The key/value head count is read from ``k.shape[1]``; when it is
 smaller than ``q.shape[1]`` the call is grouped-query attention (module
 neuralops.core.triton_kernels.gqa) with the expansion fused into the kernels, and dk, dv
-come back with the key/value shape, summed over each group.
+come back with the key/value shape, summed over each group.  Inputs may be strided views
+(last dimension contiguous, e.g. slices of a fused qkv projection): their strides go to
+``la_fwd_strided`` / ``la_bwd_strided``; outputs are contiguous.
 
 PyTorch supplies device memory and the current stream; every arithmetic step runs in
 the library's CUDA kernels.  There is no fallback: if libla.so is missing or a call
@@ -29,6 +31,11 @@ PHI = {"elu+1": 0, "relu": 1, "identity": 2}
 _NOT_BUILT = {"softmax_free"}
 
 _lib = None
+
+
+class LaStrides(ctypes.Structure):
+    """la_strides: element strides of a [B, H, N, D] input along B, H, N."""
+    _fields_ = [("b", ctypes.c_longlong), ("h", ctypes.c_longlong), ("n", ctypes.c_longlong)]
 
 
 class LinearAttentionError(RuntimeError):
@@ -59,6 +66,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.la_bwd_from_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp, sz,
                                     vp]
     lib.la_bwd_from_fwd.restype = i
+    sp = ctypes.POINTER(LaStrides)
+    lib.la_fwd_strided.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, sp, sp, sp, vp, sz, vp]
+    lib.la_fwd_strided.restype = i
+    lib.la_bwd_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, sp, sp, sp, sp,
+                                   vp, sz, vp, sz, vp]
+    lib.la_bwd_strided.restype = i
     lib.la_get_status.argtypes = [vp]
     lib.la_get_status.restype = i
     lib.la_status_str.argtypes = [i]
@@ -116,8 +129,8 @@ def _check_inputs(q, k, v, cos_weight, sin_weight, extra=()):
     for name, t in (("q", q), ("k", k), ("v", v)) + tuple(extra):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-        if t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous [B, H, N, D] tensor")
+        if t.dim() != 4 or (t.shape[3] > 1 and t.stride(3) != 1) or min(t.stride()) < 0:
+            raise ValueError(f"{name} must be a [B, H, N, D] tensor whose last dimension is contiguous")
         if t.dtype != q.dtype:
             raise TypeError(f"{name} has dtype {t.dtype}, q has {q.dtype}")
     B, Hq, N, D = q.shape
@@ -130,6 +143,13 @@ def _check_inputs(q, k, v, cos_weight, sin_weight, extra=()):
                               or not w.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous float32 CUDA vector of length N={N}")
     return B, Hq, k.shape[1], N, D
+
+
+def _strides(t):
+    """la_strides of an input (None when contiguous: the plain entry points take it)."""
+    if t.is_contiguous():
+        return None
+    return ctypes.pointer(LaStrides(t.stride(0), t.stride(1), t.stride(2)))
 
 
 def _stream_handle(stream) -> ctypes.c_void_p:
@@ -170,17 +190,26 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, is_causal: bool = Fal
     lib = load()
     B, Hq, Hkv, N, D = _check_inputs(q, k, v, cos_weight, sin_weight)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor like q")
     dt = _dtype_code(q)
     ws = _workspace(lib.la_workspace_size(B, Hq, Hkv, N, D, dt, int(is_causal),
                                           int(cos_weight is not None), 0), q.device, workspace)
-    st = lib.la_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, D, dt, int(is_causal),
-                    _phi_code(phi), float(eps), _ptr(cos_weight), _ptr(sin_weight), _ptr(ws),
-                    0 if ws is None else ws.numel() * ws.element_size(), _stream_handle(stream))
+    nws = 0 if ws is None else ws.numel() * ws.element_size()
+    strides = [_strides(t) for t in (q, k, v)]
+    if all(x is None for x in strides):
+        st = lib.la_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, D, dt, int(is_causal),
+                        _phi_code(phi), float(eps), _ptr(cos_weight), _ptr(sin_weight), _ptr(ws), nws,
+                        _stream_handle(stream))
+        call = "la_fwd"
+    else:
+        st = lib.la_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, D, dt, int(is_causal),
+                                _phi_code(phi), float(eps), _ptr(cos_weight), _ptr(sin_weight), *strides,
+                                _ptr(ws), nws, _stream_handle(stream))
+        call = "la_fwd_strided"
     if st != LA_OK:
-        _raise(lib, st, "la_fwd")
+        _raise(lib, st, call)
     return out
 
 
@@ -199,9 +228,9 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tenso
     B, Hq, Hkv, N, D = _check_inputs(q, k, v, cos_weight, sin_weight, (("grad_out", grad_out),))
     if grad_out.shape != q.shape:
         raise ValueError("grad_out must have the shape of q")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = torch.empty(q.shape, dtype=q.dtype, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=k.dtype, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=v.dtype, device=v.device) if dv is None else dv
     for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
         if t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous tensor like its input")
@@ -209,14 +238,22 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tenso
     ws = _workspace(lib.la_workspace_size(B, Hq, Hkv, N, D, dt, int(is_causal),
                                           int(cos_weight is not None), 1), q.device, workspace)
     nws = 0 if ws is None else ws.numel() * ws.element_size()
-    if fwd_workspace is None:
+    if fwd_workspace is not None and fwd_workspace.device != q.device:
+        raise ValueError("fwd_workspace must be on q's device")
+    strides = [_strides(t) for t in (q, k, v, grad_out)]
+    if any(x is not None for x in strides):
+        fws = 0 if fwd_workspace is None else fwd_workspace.numel() * fwd_workspace.element_size()
+        st = lib.la_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
+                                B, Hq, Hkv, N, D, dt, int(is_causal), _phi_code(phi), float(eps),
+                                _ptr(cos_weight), _ptr(sin_weight), *strides, _ptr(fwd_workspace), fws,
+                                _ptr(ws), nws, _stream_handle(stream))
+        call = "la_bwd_strided"
+    elif fwd_workspace is None:
         st = lib.la_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
                         B, Hq, Hkv, N, D, dt, int(is_causal), _phi_code(phi), float(eps),
                         _ptr(cos_weight), _ptr(sin_weight), _ptr(ws), nws, _stream_handle(stream))
         call = "la_bwd"
     else:
-        if fwd_workspace.device != q.device:
-            raise ValueError("fwd_workspace must be on q's device")
         st = lib.la_bwd_from_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
                                  B, Hq, Hkv, N, D, dt, int(is_causal), _phi_code(phi), float(eps),
                                  _ptr(cos_weight), _ptr(sin_weight), _ptr(fwd_workspace),

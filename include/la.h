@@ -82,6 +82,13 @@ typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 /* Which kernel family a call with these arguments runs. */
 typedef enum { LA_PATH_SIMT = 0, LA_PATH_TCGEN05 = 1 } la_path;
 
+/* Element strides of a [B, H, N, D] input along B, H and N; its last dimension (D) is
+ * contiguous.  E.g. q taken from a fused [B, N, 3, H, D] projection as qkv[:, :, 0]
+ * permuted to [B, H, N, D]: b = 3 N H D, h = D, n = 3 H D. */
+typedef struct {
+    long long b, h, n;
+} la_strides;
+
 /* Bytes of workspace that la_fwd (is_bwd = 0) or la_bwd (is_bwd = 1) needs for these
  * sizes.  Host-only, never fails: returns 0 for arguments la_fwd / la_bwd would reject.
  * has_weights: 1 when cos_weight and sin_weight are given. */
@@ -101,6 +108,19 @@ la_status la_fwd(const void *q, const void *k, const void *v, void *out, int B, 
                  int Hkv, int N, int D, la_dtype dtype, int is_causal, la_phi phi, float eps,
                  const float *cos_weight, const float *sin_weight, void *workspace,
                  size_t ws_bytes, void *stream);
+
+/* la_fwd on inputs with strides: q_strides, k_strides, v_strides (NULL: contiguous) give
+ * each input's element strides; out is contiguous.  The strides are used as given (the
+ * caller guarantees every element they reach lies in the input's allocation); negative
+ * strides: LA_ERR_ARG.  On the tensor-core path (la_kernel_path) every stride must be a
+ * multiple of 8 elements (TMA: 16-byte row strides), else LA_ERR_ALIGN; the CUDA-core
+ * path takes any.  The gqa page's wrapper passes strides to its kernel in the same way. */
+la_status la_fwd_strided(const void *q, const void *k, const void *v, void *out, int B, int Hq,
+                         int Hkv, int N, int D, la_dtype dtype, int is_causal, la_phi phi,
+                         float eps, const float *cos_weight, const float *sin_weight,
+                         const la_strides *q_strides, const la_strides *k_strides,
+                         const la_strides *v_strides, void *workspace, size_t ws_bytes,
+                         void *stream);
 
 /* Backward, `linear_attn.bwd(q, k, v, grad_out, is_causal, phi, eps, cos_weight,
  * sin_weight) -> (dq, dk, dv)`: writes dq [B, Hq, N, D] and the group-summed dk, dv
@@ -136,6 +156,19 @@ la_status la_bwd_from_fwd(const void *q, const void *k, const void *v, const voi
                           const float *cos_weight, const float *sin_weight,
                           const void *fwd_workspace, size_t fwd_ws_bytes, void *workspace,
                           size_t ws_bytes, void *stream);
+
+/* la_bwd (fwd_workspace NULL) or la_bwd_from_fwd (fwd_workspace given, from la_fwd_strided
+ * with the same inputs and strides) on inputs with strides: q, k, v, grad_out strides as in
+ * la_fwd_strided (NULL: contiguous); dq, dk, dv are contiguous.  Errors as la_fwd_strided
+ * and la_bwd. */
+la_status la_bwd_strided(const void *q, const void *k, const void *v, const void *grad_out,
+                         void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int D,
+                         la_dtype dtype, int is_causal, la_phi phi, float eps,
+                         const float *cos_weight, const float *sin_weight,
+                         const la_strides *q_strides, const la_strides *k_strides,
+                         const la_strides *v_strides, const la_strides *g_strides,
+                         const void *fwd_workspace, size_t fwd_ws_bytes, void *workspace,
+                         size_t ws_bytes, void *stream);
 
 /* Synchronises `stream`, then returns and clears the device-side error word of the
  * current device: LA_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call,

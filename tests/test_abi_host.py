@@ -153,3 +153,27 @@ def test_bwd_from_fwd_argument_errors(lib):
     bad = list(base)
     bad[8] = i(3)
     assert lib.la_bwd_from_fwd(*(bad + [FAKE, ctypes.c_size_t(1 << 30), FAKE, ctypes.c_size_t(1 << 30), None])) == la.LA_ERR_ARG
+
+
+def test_strided_argument_errors(lib):
+    """la_fwd_strided / la_bwd_strided reject negative strides (LA_ERR_ARG) and, on the
+    tensor-core path, strides that are not multiples of 8 elements (LA_ERR_ALIGN), before any
+    CUDA call."""
+    i, f, sz = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    S = la.LaStrides
+    neg = S(-1, 64 * 64, 64)
+    odd = S(4 * 64 * 64, 64 * 64 + 4, 64)
+    shape = [i(1), i(4), i(2), i(64), i(64), i(la.LA_BF16), i(1), i(0), f(1e-6), None, None]
+    assert lib.la_kernel_path(1, 4, 2, 64, 64, la.LA_BF16, 1, 0, 0) == la.LA_PATH_TCGEN05
+
+    def fwd(sq, sk):
+        return lib.la_fwd_strided(*([FAKE] * 4 + shape + [sq, sk, None, FAKE, sz(1 << 30), None]))
+
+    assert fwd(ctypes.byref(neg), None) == la.LA_ERR_ARG
+    assert fwd(None, ctypes.byref(odd)) == la.LA_ERR_ALIGN
+
+    def bwd(sg):
+        return lib.la_bwd_strided(*([FAKE] * 7 + shape + [None, None, None, sg, None, sz(0), FAKE, sz(1 << 30), None]))
+
+    assert bwd(ctypes.byref(neg)) == la.LA_ERR_ARG
+    assert bwd(ctypes.byref(odd)) == la.LA_ERR_ALIGN
