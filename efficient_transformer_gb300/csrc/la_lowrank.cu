@@ -29,6 +29,7 @@ namespace la {
 namespace {
 
 constexpr int kLrThreads = 256;
+constexpr int kLrChainThreads = 384;   // chain kernel: warp 0 TMA, warp 1 MMA, warps 4-11 epilogue
 
 // 2-D map over a row-major bf16 matrix [rows][cols]: box {64 columns, box_rows rows},
 // 128-byte swizzle; elements past either edge read as zeros.
@@ -54,13 +55,19 @@ struct ChainCfg {
     static constexpr int B2_BYTES = 128 * 64 * 2;             // B2 block: 128 outputs x 64 rank columns
     static constexpr int STAGE = A_BYTES + (B1_BYTES > B2_BYTES ? B1_BYTES : B2_BYTES);
     static constexpr int TBF_BYTES = 128 * RP * 2;            // T (bf16): 128 rows x RP, K-major
-    static constexpr int OUT_BYTES = 128 * 64 * 2;            // Y (or T) staging: 128 rows x 64 columns
+    static constexpr int OUT_BYTES = 2 * 128 * 32 * 2;        // Y staging: two tiles of 128 rows x 32 columns
     static constexpr int FIXED = TBF_BYTES + OUT_BYTES + 1024;
     static constexpr int NS = (kSmemLimit - 1024 - FIXED) / STAGE > 4 ? 4 : (kSmemLimit - 1024 - FIXED) / STAGE;
     static constexpr int SMEM = NS * STAGE + FIXED;
     static_assert(NS >= 2, "two pipeline stages");
-    // TMEM: T in [0, RP), the two Y buffers at 256 and 384 (128 columns each)
-    static constexpr int T_T = 0, T_Y0 = 256, T_Y1 = 384;
+    // the second product's B2 blocks are small: a stage carries BPS of them, so that as many
+    // bytes are in flight as in the first product (the ring runs into L2 latency otherwise)
+    static constexpr int BPS = STAGE / B2_BYTES;
+    // TMEM: T in [0, RP); four Y buffers of 128 columns: 256, 384 and, once T has been copied
+    // out in bf16 (until the next tile's first product), 0 and 128
+    static constexpr int T_T = 0;
+    static constexpr int NY = 4;
+    __host__ __device__ static constexpr int t_y(int b) { return b == 0 ? 256 : b == 1 ? 384 : b == 2 ? 0 : 128; }
 };
 
 struct ChainArgs {
@@ -68,18 +75,18 @@ struct ChainArgs {
     const void *bias;      // [N2] bf16 or null
     int write_t, write_y;  // which products leave the SM
     int *err;
+    void *y;               // [M, N2] bf16, written row by row from the epilogue (set by launch_chain)
 };
 
 template <int RP, bool B1_MN, bool B2_MN>
-__global__ void __launch_bounds__(kLrThreads, 1) k_lr_chain(const __grid_constant__ CUtensorMap map_a1,
+__global__ void __launch_bounds__(kLrChainThreads, 1) k_lr_chain(const __grid_constant__ CUtensorMap map_a1,
                                                              const __grid_constant__ CUtensorMap map_b1,
                                                              const __grid_constant__ CUtensorMap map_b2,
-                                                             const __grid_constant__ CUtensorMap map_t,
-                                                             const __grid_constant__ CUtensorMap map_y, ChainArgs a) {
+                                                             const __grid_constant__ CUtensorMap map_t, ChainArgs a) {
     using K = ChainCfg<RP, B1_MN, B2_MN>;
     constexpr int NS = K::NS;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_tfull, bar_tbf, bar_yfull[2], bar_yfree[2], bar_fin;
+    __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_tfull, bar_tbf, bar_yfull[K::NY], bar_yfree[K::NY], bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t *stage0 = align1024(smem_raw);
@@ -98,7 +105,7 @@ __global__ void __launch_bounds__(kLrThreads, 1) k_lr_chain(const __grid_constan
         }
         mbar_init(&bar_tfull, 1);
         mbar_init(&bar_tbf, 128);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < K::NY; ++b) {
             mbar_init(&bar_yfull[b], 1);
             mbar_init(&bar_yfree[b], 128);
         }
@@ -124,6 +131,7 @@ __global__ void __launch_bounds__(kLrThreads, 1) k_lr_chain(const __grid_constan
                 const int s = it % NS;
                 if (it >= NS && !warp_wait(&bar_empty[s], ((it / NS) - 1) & 1, &abort_flag)) { ok = false; break; }
                 uint8_t *st = stage0 + s * K::STAGE;
+                if (tile == blockIdx.x) LA_TL(kb, 0);
                 mbar_arrive_expect_tx_w(&bar_full[s], K::A_BYTES + K::B1_BYTES);
                 tma_load_2d_w(st, &map_a1, &bar_full[s], kb * 64, tile * 128);
                 if (B1_MN)   // B1 stored [K1][R]: RP/64 boxes of 64 K rows x 64 rank columns
@@ -132,18 +140,23 @@ __global__ void __launch_bounds__(kLrThreads, 1) k_lr_chain(const __grid_constan
                 else         // B1 stored [R][K1]: one box of RP rows x 64 K columns
                     tma_load_2d_w(st + K::A_BYTES, &map_b1, &bar_full[s], kb * 64, 0);
             }
-            for (int nt = 0; ok && nt < nn2; ++nt)
-                for (int rb = 0; ok && rb < K::RB; ++rb, ++it) {
-                    const int s = it % NS;
-                    if (it >= NS && !warp_wait(&bar_empty[s], ((it / NS) - 1) & 1, &abort_flag)) { ok = false; break; }
-                    uint8_t *st = stage0 + s * K::STAGE + K::A_BYTES;
-                    mbar_arrive_expect_tx_w(&bar_full[s], K::B2_BYTES);
+            // B2 blocks bi = nt RB + rb (output tile nt, rank block rb), BPS to a stage
+            const int nb2 = nn2 * K::RB;
+            for (int b0 = 0; ok && b0 < nb2; b0 += K::BPS, ++it) {
+                const int s = it % NS;
+                if (it >= NS && !warp_wait(&bar_empty[s], ((it / NS) - 1) & 1, &abort_flag)) { ok = false; break; }
+                const int nb = nb2 - b0 < K::BPS ? nb2 - b0 : K::BPS;
+                mbar_arrive_expect_tx_w(&bar_full[s], nb * K::B2_BYTES);
+                for (int j = 0; j < nb; ++j) {
+                    const int nt = (b0 + j) / K::RB, rb = (b0 + j) % K::RB;
+                    uint8_t *st = stage0 + s * K::STAGE + j * K::B2_BYTES;
                     if (B2_MN)   // B2 stored [R][N2]: two boxes of 64 rank rows x 64 output columns
                         for (int h = 0; h < 2; ++h)
                             tma_load_2d_w(st + h * 64 * 128, &map_b2, &bar_full[s], nt * 128 + h * 64, rb * 64);
                     else         // B2 stored [N2][R]: one box of 128 output rows x 64 rank columns
                         tma_load_2d_w(st, &map_b2, &bar_full[s], rb * 64, nt * 128);
                 }
+            }
         }
         // drain the copies still in flight
         for (int j = it > NS ? it - NS : 0; j < it; ++j) warp_drain(&bar_full[j % NS], (j / NS) & 1);
@@ -155,13 +168,20 @@ __global__ void __launch_bounds__(kLrThreads, 1) k_lr_chain(const __grid_constan
         int it = 0, yc = 0, tc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++tc) {
-            // T's columns are free once the epilogue has read the previous tile's T (tbf)
+            // T's columns are free once the epilogue has read the previous tile's T (tbf) and
+            // the Y buffers 2 and 3 that lie in them (their last uses)
             if (tc > 0 && !warp_wait(&bar_tbf, (tc - 1) & 1, &abort_flag)) break;
+            for (int b = 2; b < K::NY && ok; ++b) {
+                const int uses = yc > b ? (yc - 1 - b) / K::NY + 1 : 0;
+                if (uses > 0 && !warp_wait(&bar_yfree[b], (uses - 1) & 1, &abort_flag)) ok = false;
+            }
+            if (!ok) break;
             tc_fence_after();
             for (int kb = 0; kb < nk1; ++kb, ++it) {
                 const int s = it % NS;
                 if (!warp_wait(&bar_full[s], (it / NS) & 1, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                if (tc == 0) LA_TL(kb, 1);
                 const uint32_t as = smem_u32(stage0 + s * K::STAGE), bs = as + K::A_BYTES;
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t bd = B1_MN ? desc_mnmajor(bs, 64, 0, kk) : desc_kmajor(bs, RP, 0, kk);
@@ -171,122 +191,156 @@ __global__ void __launch_bounds__(kLrThreads, 1) k_lr_chain(const __grid_constan
             }
             if (!ok) break;
             mma_commit_w(&bar_tfull);
+            if (tc == 0) LA_TL(0, 7);
             if (nn2 == 0) continue;
             if (!warp_wait(&bar_tbf, tc & 1, &abort_flag)) break;   // bf16 T is in shared memory
             tc_fence_after();
-            for (int nt = 0; ok && nt < nn2; ++nt, ++yc) {
-                const int yb = yc & 1;
-                const uint32_t tY = tmem_base + (yb ? K::T_Y1 : K::T_Y0);
-                if (yc >= 2 && !warp_wait(&bar_yfree[yb], ((yc / 2) - 1) & 1, &abort_flag)) { ok = false; break; }
+            if (tc == 0) LA_TL(1, 7);
+            // B2 blocks as the producer packs them: BPS to a stage, output tile nt = bi / RB
+            // accumulating into Y buffer yc % NY over its RB rank blocks
+            const int nb2 = nn2 * K::RB;
+            for (int b0 = 0; ok && b0 < nb2; b0 += K::BPS, ++it) {
+                const int s = it % NS;
+                if (!warp_wait(&bar_full[s], (it / NS) & 1, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                for (int rb = 0; rb < K::RB; ++rb, ++it) {
-                    const int s = it % NS;
-                    if (!warp_wait(&bar_full[s], (it / NS) & 1, &abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t bs = smem_u32(stage0 + s * K::STAGE + K::A_BYTES);
+                const int nb = nb2 - b0 < K::BPS ? nb2 - b0 : K::BPS;
+                for (int j = 0; j < nb; ++j) {
+                    const int rb = (b0 + j) % K::RB, yb = yc % K::NY;
+                    const uint32_t tY = tmem_base + K::t_y(yb);
+                    if (rb == 0) {   // a new output tile: its Y buffer must have been read
+                        if (yc >= K::NY && !warp_wait(&bar_yfree[yb], ((yc / K::NY) - 1) & 1, &abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        if (tc == 0) LA_TL((b0 + j) / K::RB, 2);
+                    }
+                    const uint32_t bs = smem_u32(stage0 + s * K::STAGE + j * K::B2_BYTES);
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t bd = B2_MN ? desc_mnmajor(bs, 64, 0, kk) : desc_kmajor(bs, 128, 0, kk);
                         mma_bf16_w(tY, desc_kmajor(tb, 128, 0, rb * 4 + kk), bd, id2, (rb > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit_w(&bar_empty[s]);
+                    if (rb == K::RB - 1) {
+                        mma_commit_w(&bar_yfull[yb]);
+                        if (tc == 0) LA_TL((b0 + j) / K::RB, 3);
+                        ++yc;
+                    }
                 }
-                if (!ok) break;
-                mma_commit_w(&bar_yfull[yb]);
+                mma_commit_w(&bar_empty[s]);
             }
         }
         mma_commit_w(&bar_fin);
         warp_drain(&bar_fin, 0);
     } else if (warp >= 4) {
-        // ---------------- epilogue: thread i = row i of the tile (TMEM lane i)
-        const int i = threadIdx.x - 128;
-        const int wq = warp - 4;
+        // ---------------- epilogue: two warpgroups, thread i = row i of the tile (TMEM lane i).
+        // Group 0 (warps 4-7) turns T into its bf16 copy (and writes T out when asked); group g
+        // takes the output tiles of Y buffers g and g + 2 (yc % 4 of parity g), so two output
+        // tiles are written out at once while the MMA runs up to two more ahead.
+        const int grp = (warp - 4) / 4, wq = warp % 4;
+        const int i = wq * 32 + threadIdx.x % 32, lane = threadIdx.x % 32;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        uint8_t *stg = obuf + grp * (K::OUT_BYTES / 2);   // this group's staging: 128 rows x 32 columns
         int yc = 0, tc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tc) {
-            ok = ok && warp_wait(&bar_tfull, tc & 1, &abort_flag);
-            tc_fence_after();
-            // T (fp32) -> bf16 T in shared memory (the operand of the second product), and
-            // when asked, out to global memory through the staging tile
-#pragma unroll 1
-            for (int c16 = 0; c16 < RP / 16; ++c16) {
-                float v[16];
-                if (ok) {
-                    tmem_ld16(tT + lane_off + c16 * 16, v);
-                    tmem_wait_regs<16>(v);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = 0.f;
+            if (grp == 0) {
+                ok = ok && warp_wait(&bar_tfull, tc & 1, &abort_flag);
+                tc_fence_after();
+                if (a.write_t && tc > 0) {   // the previous tile's copies of T have read the bf16 tile
+                    if (i < 32) bulk_wait_read();
+                    named_barrier(2, 128);
                 }
-                uint32_t w[8];
+                // T (fp32) -> bf16 T in shared memory (the operand of the second product), and
+                // when asked, out to global memory from there
+#pragma unroll 1
+                for (int c16 = 0; c16 < RP / 16; ++c16) {
+                    float v[16];
+                    if (ok) {
+                        tmem_ld16(tT + lane_off + c16 * 16, v);
+                        tmem_wait_regs<16>(v);
+                    } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-                *reinterpret_cast<uint4 *>(tbf + swz_chunk(128, i, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(tbf + swz_chunk(128, i, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-            tc_fence_before();
-            fence_proxy_async();
-            mbar_arrive_warp(&bar_tbf);
-            if (a.write_t) {   // T leaves from the bf16 copy, 64 columns at a time
-                for (int rb = 0; rb < (a.R + 63) / 64; ++rb) {
+                        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+                    }
+                    uint32_t w[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+                    *reinterpret_cast<uint4 *>(tbf + swz_chunk(128, i, 2 * c16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(tbf + swz_chunk(128, i, 2 * c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                tc_fence_before();
+                fence_proxy_async();
+                if (tc == 0 && i == 0) LA_TL(2, 7);
+                mbar_arrive_warp(&bar_tbf);
+                if (a.write_t) {   // T leaves from the bf16 copy, every 64-column block at once
                     named_barrier(2, 128);
                     if (ok && i < 32) {
-                        tma_store_2d_w(&map_t, tbf + rb * 128 * 128, rb * 64, tile * 128);
+                        for (int rb = 0; rb < (a.R + 63) / 64; ++rb)
+                            tma_store_2d_w(&map_t, tbf + rb * 128 * 128, rb * 64, tile * 128);
                         bulk_commit();
-                        bulk_wait_read();
                     }
                     __syncwarp();
                 }
             }
             for (int nt = 0; nt < nn2; ++nt, ++yc) {
-                const int yb = yc & 1;
-                const uint32_t tY = tmem_base + (yb ? K::T_Y1 : K::T_Y0);
-                ok = ok && warp_wait(&bar_yfull[yb], (yc / 2) & 1, &abort_flag);
+                const int yb = yc % K::NY;
+                if ((yb & 1) != grp) continue;
+                const uint32_t tY = tmem_base + K::t_y(yb);
+                // the tile's 128 bias values before the wait for its products: their loads (L2
+                // latency, which each 32-column piece exposed) overlap the wait and the TMEM reads
+                uint4 bias16[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    bias16[q] = a.bias && nt * 128 + 8 * q < a.N2
+                                    ? __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.bias) + nt * 128 + 8 * q))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                ok = ok && warp_wait(&bar_yfull[yb], (yc / K::NY) & 1, &abort_flag);
                 tc_fence_after();
-                for (int c64 = 0; c64 < 2; ++c64) {
+                if (tc == 0 && i == 0) LA_TL(nt, 4);
+                // 32 columns at a time: thread i (row i) writes its 64 bytes into the staging tile
+                // (rows in pairs of 128-byte swizzled lines), then each warp copies 8 rows per
+                // store instruction, whole 64-byte row pieces.  (A TMA store out of a staging tile
+                // queued behind this SM's loads of the next blocks, and a store per thread per
+                // row wrote partial lines: 10 k and 7 k cycles per output tile, measured.)
+#pragma unroll
+                for (int c32 = 0; c32 < 4; ++c32) {
+                    const int col0 = nt * 128 + c32 * 32;
                     float v[32];
-                    if (i < 32) {   // the staging tile's previous store has read it
-                        bulk_wait_read();
-                        __syncwarp();
+                    if (ok) {
+                        tmem_ld32(tY + lane_off + c32 * 32, v);
+                        tmem_wait_regs<32>(v);
                     }
-                    named_barrier(2, 128);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int col0 = nt * 128 + c64 * 64 + hh * 32;
-                        if (ok) {
-                            tmem_ld32(tY + lane_off + c64 * 64 + hh * 32, v);
-                            tmem_wait_regs<32>(v);
-                            if (a.bias)
-#pragma unroll
-                                for (int e = 0; e < 32; ++e)
-                                    v[e] += col0 + e < a.N2
-                                                ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.bias)[col0 + e])
-                                                : 0.f;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                uint4 w;
-                                w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-                                w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-                                w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-                                w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-                                *reinterpret_cast<uint4 *>(obuf + swz_chunk(128, i, hh * 4 + q)) = w;
-                            }
-                        }
-                    }
-                    if (c64 == 1) {   // every column of this Y buffer is in registers
+                    if (c32 == 3) {   // every column of this Y buffer is in registers
                         tc_fence_before();
                         mbar_arrive_warp(&bar_yfree[yb]);
                     }
-                    fence_proxy_async();
-                    named_barrier(2, 128);
-                    if (ok && i < 32) {
-                        tma_store_2d_w(&map_y, obuf, nt * 128 + c64 * 64, tile * 128);
-                        bulk_commit();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t *bw = reinterpret_cast<const uint32_t *>(&bias16[c32 * 4 + q]);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_bf16x2(bw[e]);
+                            w[e] = pack_bf16x2(v[8 * q + 2 * e] + f.x, v[8 * q + 2 * e + 1] + f.y);
+                        }
+                        // row i: line i / 2, chunks (i % 2) 4 + q, swizzled by the line
+                        *reinterpret_cast<uint4 *>(stg + swz_chunk(64, i >> 1, (i & 1) * 4 + q)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
+                    named_barrier(2 + grp, 128);
+                    // warp wq copies rows wq 32 .. + 31: lane l takes 16-byte piece l % 4 of row
+                    // 8 r + l / 4 of its block, r = 0 .. 3
+                    const int piece = lane % 4, c = col0 + piece * 8;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int rr = wq * 32 + 8 * r + lane / 4, row = tile * 128 + rr;
+                        const uint4 w = *reinterpret_cast<const uint4 *>(stg + swz_chunk(64, rr >> 1, (rr & 1) * 4 + piece));
+                        if (ok && row < a.M && c < a.N2)
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.y) + (size_t)row * a.N2 + c) = w;
+                    }
+                    named_barrier(2 + grp, 128);   // the staging tile is read before the next piece
                 }
+                if (tc == 0 && i == 0) LA_TL(nt, 5);
             }
         }
-        if (i < 32) bulk_wait_all();
+        if (grp == 0 && i < 32) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -298,20 +352,21 @@ template <int RP, bool B1_MN, bool B2_MN>
 cudaError_t launch_chain(const void *a1, const void *b1, const void *b2, void *t, void *y, const ChainArgs &ca,
                          cudaStream_t s, const char *name) {
     using K = ChainCfg<RP, B1_MN, B2_MN>;
-    CUtensorMap m_a1{}, m_b1{}, m_b2{}, m_t{}, m_y{};
+    CUtensorMap m_a1{}, m_b1{}, m_b2{}, m_t{};
     cudaError_t e = make_map_2d(&m_a1, a1, ca.M, ca.K1, 128);
     // B1 as stored: [R][K1] (box RP rows) or [K1][R] (box 64 rows)
     if (e == cudaSuccess) e = B1_MN ? make_map_2d(&m_b1, b1, ca.K1, ca.R, 64) : make_map_2d(&m_b1, b1, ca.R, ca.K1, RP);
     if (e == cudaSuccess && ca.write_y)
         e = B2_MN ? make_map_2d(&m_b2, b2, ca.R, ca.N2, 64) : make_map_2d(&m_b2, b2, ca.N2, ca.R, 128);
     if (e == cudaSuccess && ca.write_t) e = make_map_2d(&m_t, t, ca.M, ca.R, 128);
-    if (e == cudaSuccess && ca.write_y) e = make_map_2d(&m_y, y, ca.M, ca.N2, 128);
     if (e == cudaSuccess) e = prepare(k_lr_chain<RP, B1_MN, B2_MN>, K::SMEM);
     if (e != cudaSuccess) return e;
+    ChainArgs a = ca;
+    a.y = y;
     const int ntiles = (ca.M + 127) / 128;
     const int grid = ntiles < kPlanSms ? ntiles : kPlanSms;
     TraceScope ts(name, s);
-    k_lr_chain<RP, B1_MN, B2_MN><<<grid, kLrThreads, K::SMEM, s>>>(m_a1, m_b1, m_b2, m_t, m_y, ca);
+    k_lr_chain<RP, B1_MN, B2_MN><<<grid, kLrChainThreads, K::SMEM, s>>>(m_a1, m_b1, m_b2, m_t, a);
     return cudaGetLastError();
 }
 
@@ -551,3 +606,10 @@ cudaError_t lowrank_backward(const void *x, const void *U, const void *V, const 
 }
 
 }  // namespace la
+
+#ifdef LA_TIMELINE
+// Timeline builds only: the low-rank chain kernel's event clocks ([64][16] long long).
+extern "C" int la_timeline_read_lr(long long *out) {
+    return cudaMemcpyFromSymbol(out, la::g_la_tl, sizeof(long long) * 64 * 16) == cudaSuccess ? 0 : 1;
+}
+#endif
