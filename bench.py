@@ -510,6 +510,21 @@ def measure_lowrank(la, w: gen.LowRankWorkload, dev, steps: int, warmup: int, pe
     return row
 
 
+def run_lowrank_only(args, local):
+    """The low-rank projection's step alone, at --lowrank-rows rows: one JSON line with its
+    forward and forward + backward times (the per-workload table's row)."""
+    from efficient_transformer_gb300 import la
+
+    la.load()
+    base = next(iter(gen.LOWRANK_WORKLOADS.values()))
+    wl = gen.LowRankWorkload(f"lowrank_m{args.lowrank_rows}_kin{base.K_in}_r{base.r}_kout{base.K_out}_bf16",
+                             args.lowrank_rows, base.K_in, base.r, base.K_out)
+    peaks, peak_src = load_peaks()
+    row = measure_lowrank(la, wl, torch.device("cuda", local), args.steps, args.warmup, peaks, peak_src)
+    print(json.dumps(row))
+    return 0
+
+
 def run_ours(args, world, rank, local):
     from efficient_transformer_gb300 import build as la_build
     from efficient_transformer_gb300 import la
@@ -726,6 +741,9 @@ def main(argv=None):
                     help="timed blocks of --steps steps (default: enough for about 3 s)")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="run the workload at this sequence length instead (small cases for profilers)")
+    ap.add_argument("--lowrank-rows", type=int, default=0,
+                    help="time only the low-rank projection's step (forward + backward) at this many "
+                         "rows, with the low-rank workload's other sizes (for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps; the number is not a valid measurement",
@@ -736,6 +754,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
+        if args.lowrank_rows:
+            return run_lowrank_only(args, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:
