@@ -454,12 +454,13 @@ def measure_config(la, w: gen.Workload, dev, steps: int, warmup: int, peaks, pea
 
 def lowrank_counts(w: gen.LowRankWorkload):
     """(bytes, flops) of one low-rank forward and of one forward + backward: compulsory bytes
-    (every input read once, every output written once) and the products' 2 m n k flops."""
+    (every input read once, every output written once) and the 2 m n k flops of the products
+    the operation needs (the forward's two; the backward's dt, dx, dU, dV: t is the forward's)."""
     el = 2
     x_b, y_b = w.M * w.K_in * el, w.M * w.K_out * el
     wts = (w.K_in + w.K_out) * w.r * el + (w.K_out * el if w.bias else 0)
     f_fwd = 2.0 * w.M * w.r * (w.K_in + w.K_out)
-    f_bwd = 2.0 * w.M * w.r * (2 * w.K_in + 3 * w.K_out)   # t, dt, dx, dU, dV
+    f_bwd = 2.0 * w.M * w.r * (2 * w.K_in + 2 * w.K_out)   # dt, dU (K_out); dx, dV (K_in)
     b_fwd = x_b + y_b + wts
     b_bwd = x_b + y_b + x_b + 2 * wts                      # x, g in; dx, dU, dV, dbias out
     return (b_fwd, f_fwd), (b_fwd + b_bwd, f_fwd + f_bwd)
@@ -467,10 +468,13 @@ def lowrank_counts(w: gen.LowRankWorkload):
 
 def measure_lowrank(la, w: gen.LowRankWorkload, dev, steps: int, warmup: int, peaks, peak_src):
     """One row of the per-workload table for the low-rank projection: forward alone and
-    forward + backward, each as blocks of `steps` calls between CUDA events."""
+    forward + backward, each as blocks of `steps` calls between CUDA events.  The step's
+    forward keeps the bottleneck t for its backward (la_lowrank_fwd_t / la_lowrank_bwd_t),
+    as a training step that keeps its forward's context does."""
     host = gen.make_lowrank_inputs(w)
     d = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
     y = torch.empty((w.M, w.K_out), dtype=d["x"].dtype, device=dev)
+    t = torch.empty((w.M, w.r), dtype=d["x"].dtype, device=dev)
     ws = torch.empty(max(1, la.load().la_lowrank_workspace_size(w.M, w.K_in, w.r, w.K_out, la.LA_BF16, 1)),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -479,8 +483,8 @@ def measure_lowrank(la, w: gen.LowRankWorkload, dev, steps: int, warmup: int, pe
         la.lowrank_fwd(d["x"], d["U"], d["V"], d["bias"], out=y, stream=stream)
 
     def step():
-        fwd()
-        la.lowrank_bwd(d["x"], d["U"], d["V"], d["grad_out"], d["bias"], workspace=ws, stream=stream)
+        la.lowrank_fwd(d["x"], d["U"], d["V"], d["bias"], out=y, t_out=t, stream=stream)
+        la.lowrank_bwd(d["x"], d["U"], d["V"], d["grad_out"], d["bias"], workspace=ws, t=t, stream=stream)
 
     for _ in range(max(3, warmup)):
         step()
@@ -505,7 +509,7 @@ def measure_lowrank(la, w: gen.LowRankWorkload, dev, steps: int, warmup: int, pe
     row["tokens_per_s"] = w.M / (ms / 1e3)
     row["roofline_basis"] = (f"max(bytes / {ROOFLINE_HBM_GBS:.0f} GB/s, flops / {peak_src} bf16 sustained "
                              f"{peaks['bf16_tflops_sustained']} TFLOP/s)")
-    del d, y, ws
+    del d, y, t, ws
     torch.cuda.empty_cache()
     return row
 

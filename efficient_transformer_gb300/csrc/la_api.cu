@@ -440,19 +440,51 @@ la_status lowrank_check(int M, int K_in, int r, int K_out, int dtype) {
 
 }  // namespace
 
-extern "C" la_status la_lowrank_fwd(const void *x, const void *U, const void *V, const void *bias, void *y, int M,
-                                    int K_in, int r, int K_out, la_dtype dtype, void *stream) {
+namespace {
+la_status lowrank_fwd_run(const void *x, const void *U, const void *V, const void *bias, void *y, void *t_out, int M,
+                          int K_in, int r, int K_out, la_dtype dtype, void *stream) {
     la_status st = lowrank_check(M, K_in, r, K_out, dtype);
     if (st != LA_OK) return st;
     if (!x || !U || !V || !y) return LA_ERR_ARG;
-    const void *ptrs[] = {x, U, V, bias, y};
+    const void *ptrs[] = {x, U, V, bias, y, t_out};
     for (const void *ptr : ptrs)
         if (ptr && !aligned(ptr, 16)) return LA_ERR_ALIGN;
     int *err = nullptr;
     cudaError_t e = error_word(&err);
     if (e == cudaSuccess)
-        e = lowrank_forward(x, U, V, bias, y, M, K_in, r, K_out, err, static_cast<cudaStream_t>(stream));
+        e = lowrank_forward(x, U, V, bias, y, t_out, M, K_in, r, K_out, err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LA_OK : cuda_fail(e);
+}
+
+la_status lowrank_bwd_run(const void *x, const void *U, const void *V, const void *t, const void *grad_out, void *dx,
+                          void *dU, void *dV, void *dbias, int M, int K_in, int r, int K_out, la_dtype dtype,
+                          void *workspace, size_t ws_bytes, void *stream) {
+    la_status st = lowrank_check(M, K_in, r, K_out, dtype);
+    if (st != LA_OK) return st;
+    if (!x || !U || !V || !grad_out || !dx || !dU || !dV) return LA_ERR_ARG;
+    const void *ptrs[] = {x, U, V, t, grad_out, dx, dU, dV, dbias};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned(ptr, 16)) return LA_ERR_ALIGN;
+    const size_t need = lowrank_bwd_workspace(M, K_in, r, K_out);
+    if (!workspace || ws_bytes < need) return LA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return LA_ERR_ALIGN;
+    int *err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e == cudaSuccess)
+        e = lowrank_backward(x, U, V, t, grad_out, dx, dU, dV, dbias, M, K_in, r, K_out, workspace, err,
+                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LA_OK : cuda_fail(e);
+}
+}  // namespace
+
+extern "C" la_status la_lowrank_fwd(const void *x, const void *U, const void *V, const void *bias, void *y, int M,
+                                    int K_in, int r, int K_out, la_dtype dtype, void *stream) {
+    return lowrank_fwd_run(x, U, V, bias, y, nullptr, M, K_in, r, K_out, dtype, stream);
+}
+extern "C" la_status la_lowrank_fwd_t(const void *x, const void *U, const void *V, const void *bias, void *y,
+                                      void *t_out, int M, int K_in, int r, int K_out, la_dtype dtype, void *stream) {
+    if (!t_out) return LA_ERR_ARG;
+    return lowrank_fwd_run(x, U, V, bias, y, t_out, M, K_in, r, K_out, dtype, stream);
 }
 
 extern "C" size_t la_lowrank_workspace_size(int M, int K_in, int r, int K_out, la_dtype dtype, int is_bwd) {
@@ -463,21 +495,15 @@ extern "C" size_t la_lowrank_workspace_size(int M, int K_in, int r, int K_out, l
 extern "C" la_status la_lowrank_bwd(const void *x, const void *U, const void *V, const void *grad_out, void *dx,
                                     void *dU, void *dV, void *dbias, int M, int K_in, int r, int K_out,
                                     la_dtype dtype, void *workspace, size_t ws_bytes, void *stream) {
-    la_status st = lowrank_check(M, K_in, r, K_out, dtype);
-    if (st != LA_OK) return st;
-    if (!x || !U || !V || !grad_out || !dx || !dU || !dV) return LA_ERR_ARG;
-    const void *ptrs[] = {x, U, V, grad_out, dx, dU, dV, dbias};
-    for (const void *ptr : ptrs)
-        if (ptr && !aligned(ptr, 16)) return LA_ERR_ALIGN;
-    const size_t need = lowrank_bwd_workspace(M, K_in, r, K_out);
-    if (!workspace || ws_bytes < need) return LA_ERR_WORKSPACE;
-    if (!aligned(workspace, 256)) return LA_ERR_ALIGN;
-    int *err = nullptr;
-    cudaError_t e = error_word(&err);
-    if (e == cudaSuccess)
-        e = lowrank_backward(x, U, V, grad_out, dx, dU, dV, dbias, M, K_in, r, K_out, workspace, err,
-                             static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? LA_OK : cuda_fail(e);
+    return lowrank_bwd_run(x, U, V, nullptr, grad_out, dx, dU, dV, dbias, M, K_in, r, K_out, dtype, workspace,
+                           ws_bytes, stream);
+}
+extern "C" la_status la_lowrank_bwd_t(const void *x, const void *U, const void *V, const void *t, const void *grad_out,
+                                      void *dx, void *dU, void *dV, void *dbias, int M, int K_in, int r, int K_out,
+                                      la_dtype dtype, void *workspace, size_t ws_bytes, void *stream) {
+    if (!t) return LA_ERR_ARG;
+    return lowrank_bwd_run(x, U, V, t, grad_out, dx, dU, dV, dbias, M, K_in, r, K_out, dtype, workspace, ws_bytes,
+                           stream);
 }
 
 // ---- forward without a caller workspace ------------------------------------------------

@@ -148,10 +148,11 @@ int tc_chunk(int n_rep, int D);   // tokens per chunk of the tensor-core forward
 bool tc_bwd_supported(int n_rep, int D);
 
 // Low-rank projection y = (x V^T) U^T + bias (bf16, tensor cores).
-cudaError_t lowrank_forward(const void *x, const void *U, const void *V, const void *bias, void *y, int M, int K_in,
-                            int r, int K_out, int *err, cudaStream_t s);
+cudaError_t lowrank_forward(const void *x, const void *U, const void *V, const void *bias, void *y, void *t_out, int M,
+                            int K_in, int r, int K_out, int *err, cudaStream_t s);
 size_t lowrank_bwd_workspace(int M, int K_in, int r, int K_out);
-cudaError_t lowrank_backward(const void *x, const void *U, const void *V, const void *g, void *dx, void *dU, void *dV,
-                             void *dbias, int M, int K_in, int r, int K_out, void *ws, int *err, cudaStream_t s);
+cudaError_t lowrank_backward(const void *x, const void *U, const void *V, const void *t_given, const void *g, void *dx,
+                             void *dU, void *dV, void *dbias, int M, int K_in, int r, int K_out, void *ws, int *err,
+                             cudaStream_t s);
 
 }  // namespace la

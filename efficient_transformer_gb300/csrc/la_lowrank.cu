@@ -567,10 +567,11 @@ cudaError_t wgrad(const void *A, const void *Bm, int M, int Mc, int Nc, float *p
 
 }  // namespace
 
-cudaError_t lowrank_forward(const void *x, const void *U, const void *V, const void *bias, void *y, int M, int K_in,
-                            int r, int K_out, int *err, cudaStream_t s) {
-    ChainArgs ca{M, K_in, r, K_out, bias, 0, 1, err};
-    return chain_dispatch<false, false>(x, V, U, nullptr, y, ca, s, "lr_fwd");
+cudaError_t lowrank_forward(const void *x, const void *U, const void *V, const void *bias, void *y, void *t_out, int M,
+                            int K_in, int r, int K_out, int *err, cudaStream_t s) {
+    // t_out: the bf16 T = x V^T of the first product leaves the SM too (the backward's t)
+    ChainArgs ca{M, K_in, r, K_out, bias, t_out ? 1 : 0, 1, err};
+    return chain_dispatch<false, false>(x, V, U, t_out, y, ca, s, "lr_fwd");
 }
 
 size_t lowrank_bwd_workspace(int M, int K_in, int r, int K_out) {
@@ -583,15 +584,19 @@ size_t lowrank_bwd_workspace(int M, int K_in, int r, int K_out) {
     return 2 * tb + (pu > pv ? pu : pv);
 }
 
-cudaError_t lowrank_backward(const void *x, const void *U, const void *V, const void *g, void *dx, void *dU, void *dV,
-                             void *dbias, int M, int K_in, int r, int K_out, void *ws, int *err, cudaStream_t s) {
+cudaError_t lowrank_backward(const void *x, const void *U, const void *V, const void *t_given, const void *g, void *dx,
+                             void *dU, void *dV, void *dbias, int M, int K_in, int r, int K_out, void *ws, int *err,
+                             cudaStream_t s) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     char *base = static_cast<char *>(ws);
-    void *t = base, *dt = base + up((size_t)M * r * 2);
+    const void *t = t_given ? t_given : static_cast<const void *>(base);
+    void *dt = base + up((size_t)M * r * 2);
     float *part = reinterpret_cast<float *>(base + 2 * up((size_t)M * r * 2));
-    // t = x V^T (kept for dU = g^T t)
-    ChainArgs ct{M, K_in, r, 0, nullptr, 1, 0, err};
-    cudaError_t e = chain_dispatch<false, false>(x, V, nullptr, t, nullptr, ct, s, "lr_bwd_t");
+    cudaError_t e = cudaSuccess;
+    if (!t_given) {   // t = x V^T (kept for dU = g^T t), unless the forward left it
+        ChainArgs ct{M, K_in, r, 0, nullptr, 1, 0, err};
+        e = chain_dispatch<false, false>(x, V, nullptr, base, nullptr, ct, s, "lr_bwd_t");
+    }
     // dt = g U (kept for dV = dt^T x), dx = dt V: U and V read as MN-major operands
     ChainArgs cx{M, K_out, r, K_in, nullptr, 1, 1, err};
     if (e == cudaSuccess) e = chain_dispatch<true, true>(g, U, V, dt, dx, cx, s, "lr_bwd_dx");

@@ -83,6 +83,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.la_lowrank_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.la_lowrank_workspace_size.restype = sz
     lib.la_lowrank_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
+    lib.la_lowrank_fwd_t.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.la_lowrank_fwd_t.restype = i
+    lib.la_lowrank_bwd_t.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
+    lib.la_lowrank_bwd_t.restype = i
     lib.la_lowrank_bwd.restype = i
     lib.la_trace_start.argtypes = []
     lib.la_trace_start.restype = i
@@ -280,27 +284,39 @@ def _check_lowrank(x, U, V, bias):
 
 
 def lowrank_fwd(x: torch.Tensor, U: torch.Tensor, V: torch.Tensor, bias: torch.Tensor | None = None, *,
-                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                out: torch.Tensor | None = None, t_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Low-rank projection ``y = (x @ V.T) @ U.T + bias`` (module
     neuralops.core.triton_kernels.low_rank, ``fwd``): x [..., K_in], U [K_out, r], V [r, K_in];
-    returns y [..., K_out]."""
+    returns y [..., K_out].  ``t_out`` ([M, r], x's dtype): also receives the bottleneck
+    t = x V^T for ``lowrank_bwd(..., t=t_out)`` (``la_lowrank_fwd_t``)."""
     lib = load()
     M, K_in, r, K_out = _check_lowrank(x, U, V, bias)
     if out is None:
         out = torch.empty(x.shape[:-1] + (K_out,), dtype=x.dtype, device=x.device)
     elif out.shape != x.shape[:-1] + (K_out,) or out.dtype != x.dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor [..., K_out] of x's dtype")
-    st = lib.la_lowrank_fwd(_ptr(x), _ptr(U), _ptr(V), _ptr(bias), _ptr(out), M, K_in, r, K_out,
-                            _dtype_code(x), _stream_handle(stream))
+    if t_out is None:
+        st = lib.la_lowrank_fwd(_ptr(x), _ptr(U), _ptr(V), _ptr(bias), _ptr(out), M, K_in, r, K_out,
+                                _dtype_code(x), _stream_handle(stream))
+        call = "la_lowrank_fwd"
+    else:
+        if t_out.shape != (M, r) or t_out.dtype != x.dtype or not t_out.is_contiguous() or not t_out.is_cuda:
+            raise ValueError(f"t_out must be a contiguous CUDA tensor [{M}, {r}] of x's dtype")
+        st = lib.la_lowrank_fwd_t(_ptr(x), _ptr(U), _ptr(V), _ptr(bias), _ptr(out), _ptr(t_out), M, K_in, r,
+                                  K_out, _dtype_code(x), _stream_handle(stream))
+        call = "la_lowrank_fwd_t"
     if st != LA_OK:
-        _raise(lib, st, "la_lowrank_fwd")
+        _raise(lib, st, call)
     return out
 
 
 def lowrank_bwd(x: torch.Tensor, U: torch.Tensor, V: torch.Tensor, grad_out: torch.Tensor,
-                bias: torch.Tensor | None = None, *, workspace: torch.Tensor | None = None, stream=None):
+                bias: torch.Tensor | None = None, *, workspace: torch.Tensor | None = None,
+                t: torch.Tensor | None = None, stream=None):
     """Backward of ``lowrank_fwd`` (module neuralops.core.triton_kernels.low_rank, ``bwd``):
-    returns ``(dx, dU, dV, dbias)``, dbias None without a bias."""
+    returns ``(dx, dU, dV, dbias)``, dbias None without a bias.  ``t``: the bottleneck that
+    ``lowrank_fwd(..., t_out=t)`` left for these x, V (``la_lowrank_bwd_t``: same results,
+    one pass over x fewer)."""
     lib = load()
     M, K_in, r, K_out = _check_lowrank(x, U, V, bias)
     if grad_out.shape != x.shape[:-1] + (K_out,) or grad_out.dtype != x.dtype or not grad_out.is_contiguous():
@@ -309,11 +325,19 @@ def lowrank_bwd(x: torch.Tensor, U: torch.Tensor, V: torch.Tensor, grad_out: tor
     dx, dU, dV = torch.empty_like(x), torch.empty_like(U), torch.empty_like(V)
     db = torch.empty_like(bias) if bias is not None else None
     ws = _workspace(lib.la_lowrank_workspace_size(M, K_in, r, K_out, dt, 1), x.device, workspace)
-    st = lib.la_lowrank_bwd(_ptr(x), _ptr(U), _ptr(V), _ptr(grad_out), _ptr(dx), _ptr(dU), _ptr(dV), _ptr(db),
-                            M, K_in, r, K_out, dt, _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
-                            _stream_handle(stream))
+    nws = 0 if ws is None else ws.numel() * ws.element_size()
+    if t is None:
+        st = lib.la_lowrank_bwd(_ptr(x), _ptr(U), _ptr(V), _ptr(grad_out), _ptr(dx), _ptr(dU), _ptr(dV), _ptr(db),
+                                M, K_in, r, K_out, dt, _ptr(ws), nws, _stream_handle(stream))
+        call = "la_lowrank_bwd"
+    else:
+        if t.shape != (M, r) or t.dtype != x.dtype or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"t must be a contiguous CUDA tensor [{M}, {r}] of x's dtype")
+        st = lib.la_lowrank_bwd_t(_ptr(x), _ptr(U), _ptr(V), _ptr(t), _ptr(grad_out), _ptr(dx), _ptr(dU), _ptr(dV),
+                                  _ptr(db), M, K_in, r, K_out, dt, _ptr(ws), nws, _stream_handle(stream))
+        call = "la_lowrank_bwd_t"
     if st != LA_OK:
-        _raise(lib, st, "la_lowrank_bwd")
+        _raise(lib, st, call)
     return dx, dU, dV, db
 
 

@@ -229,6 +229,22 @@ la_status la_lowrank_bwd(const void *x, const void *U, const void *V, const void
                          void *dV, void *dbias, int M, int K_in, int r, int K_out, la_dtype dtype,
                          void *workspace, size_t ws_bytes, void *stream);
 
+/* la_lowrank_fwd that also writes the bottleneck t = x V^T (bf16, [M, r], rounded once: the
+ * bits la_lowrank_bwd would recompute) to t_out, for la_lowrank_bwd_t.  LA_ERR_ARG if t_out
+ * is NULL; otherwise as la_lowrank_fwd. */
+la_status la_lowrank_fwd_t(const void *x, const void *U, const void *V, const void *bias, void *y,
+                           void *t_out, int M, int K_in, int r, int K_out, la_dtype dtype,
+                           void *stream);
+
+/* la_lowrank_bwd given the t that la_lowrank_fwd_t wrote for these x and V (ordered before
+ * this call): the same results, without the backward's own pass over x for t.  The caller
+ * guarantees t matches x and V.  LA_ERR_ARG if t is NULL; otherwise as la_lowrank_bwd (the
+ * workspace size is the same). */
+la_status la_lowrank_bwd_t(const void *x, const void *U, const void *V, const void *t,
+                           const void *grad_out, void *dx, void *dU, void *dV, void *dbias, int M,
+                           int K_in, int r, int K_out, la_dtype dtype, void *workspace,
+                           size_t ws_bytes, void *stream);
+
 /* Forward for callers that cannot allocate device memory.
  *
  * Some callers have no way to obtain scratch memory on the GPU: a plugin host that hands

@@ -65,6 +65,29 @@ def test_lowrank_backward(case):
     assert all(e <= H.TOL["bf16"] for e in errs.values()), errs
 
 
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+def test_lowrank_saved_t(case):
+    """la_lowrank_fwd_t writes the same y as la_lowrank_fwd plus t = bf16(x V^T), and
+    la_lowrank_bwd_t given that t returns exactly la_lowrank_bwd's gradients."""
+    M, K_in, r, K_out, bias = case
+    w = gen.LowRankWorkload(f"lr_m{M}_kin{K_in}_r{r}_kout{K_out}", M, K_in, r, K_out, bias=bias)
+    dev = H.to_dev(gen.make_lowrank_inputs(w, seed=41))
+    y = la.lowrank_fwd(dev["x"], dev["U"], dev["V"], dev["bias"])
+    t = torch.empty((M, r), dtype=torch.bfloat16, device="cuda")
+    y_t = la.lowrank_fwd(dev["x"], dev["U"], dev["V"], dev["bias"], t_out=t)
+    got = la.lowrank_bwd(dev["x"], dev["U"], dev["V"], dev["grad_out"], dev["bias"], t=t)
+    ref = la.lowrank_bwd(dev["x"], dev["U"], dev["V"], dev["grad_out"], dev["bias"])
+    la.get_status()
+    assert torch.equal(y, y_t)
+    # t is the bottleneck rounded once: within bf16 rounding of the exact x V^T
+    exact = dev["x"].double() @ dev["V"].double().T
+    assert float((t.double() - exact).abs().max() / exact.abs().max()) <= 2 ** -8
+    for name, a, b in zip(("dx", "dU", "dV", "dbias"), got, ref):
+        assert (a is None) == (b is None)
+        if a is not None:
+            assert torch.equal(a, b), f"{name} with the forward's t differs"
+
+
 def test_lowrank_leading_dims_and_deterministic():
     w = gen.LowRankWorkload("lr_lead", 2 * 300, 256, 64, 256)
     inp = gen.make_lowrank_inputs(w, seed=5)
