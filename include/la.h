@@ -20,7 +20,8 @@
  * expanded key/value tensors are never formed.
  *
  * Layout: q, out, grad_out, dq are contiguous [B, Hq, N, D]; k, v, dk, dv are contiguous
- * [B, Hkv, N, D] (row-major, D fastest; Dv = D).  Elements are float32 (LA_F32) or
+ * [B, Hkv, N, D] (row-major, D fastest; Dv = D); la_fwd_strided and la_bwd_strided take
+ * inputs with other strides (D still contiguous).  Elements are float32 (LA_F32) or
  * bfloat16 (LA_BF16); outputs use the input type.  Arithmetic is float32 accumulation in
  * both cases (bfloat16 tensor-core operands on the LA_BF16 fast path).  cos_weight and
  * sin_weight are float32 device vectors of length N, indexed by position, applied to
