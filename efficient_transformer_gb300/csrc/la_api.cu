@@ -125,11 +125,11 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
         if (tc && pl.P == 2) {   // cos/sin passes: the forward's partials (when the backward runs
                                  // it) and the cos pass's dq, dk, dv (fp32)
             pl.off_pnum = off;
-            off += align_up((size_t)B * Hq * N * D * sizeof(float), 256);
+            off += align_up(blocked_floats(B * Hq, N, D) * sizeof(float), 256);
             pl.off_pden = off;
             off += row_bytes;
             pl.off_pdq = off;
-            off += align_up((size_t)B * Hq * N * D * sizeof(float), 256);
+            off += align_up(blocked_floats(B * Hq, N, D) * sizeof(float), 256);
             pl.off_pdk = off;
             off += align_up((size_t)B * Hkv * N * D * sizeof(float), 256);
             pl.off_pdv = off;
@@ -140,7 +140,7 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
         off += den_bytes;
         if (pl.P == 2) {   // cos pass -> sin pass: numerator rows and dens of the cos terms
             pl.off_pnum = off;
-            off += align_up((size_t)B * Hq * N * D * sizeof(float), 256);
+            off += align_up(blocked_floats(B * Hq, N, D) * sizeof(float), 256);
             pl.off_pden = off;
             off += row_bytes;
         }

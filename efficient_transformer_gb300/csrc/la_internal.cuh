@@ -61,12 +61,13 @@ struct Params {
     // tensor-core forward with cos/sin weights, run as two passes (cos, then sin)
     int pass;                    // 0: one pass; 1: the cos pass; 2: the sin pass
     const float *wrow;           // this pass's position weights (cw or sw), on phi(q) and phi(k) rows
-    float *part_num;             // [B, Hq, N, D] fp32: the cos pass's numerator rows (unnormalised)
+    float *part_num;             // fp32, chunk-blocked (blocked_index, the forward's chunk): the cos
+                                 // pass's numerator rows (unnormalised), then the float32 output rows
     float *part_den;             // [B, Hq, N] fp32: the cos pass's denominators (without eps)
     // ... and its backward: the cos pass's gradients (fp32), added in by the sin pass; the
-    // forward's float32 output rows (part_num after the sin pass) give h = -g . out, read
-    // from `gd`
-    float *part_dq;              // [B, Hq, N, D]
+    // forward's float32 output rows (part_num after the sin pass) give h = -g . out, written
+    // to `gd`
+    float *part_dq;              // fp32, chunk-blocked (blocked_index, the dq kernel's chunk)
     float *part_dk, *part_dv;    // [B, Hkv, N, D]
     int *err;                    // device error word
 };
@@ -84,6 +85,17 @@ struct Plan {
     size_t off_pdq, off_pdk, off_pdv;   // ... and backward
     size_t ws_bytes;
 };
+
+// Element (row t of head bh, column e) of a chunk-blocked float32 array over C-token chunks,
+// [heads][ceil(N / C)][D][C]: for each column the C rows of a chunk are contiguous, so a warp
+// of consecutive rows stores or loads one run (the cos/sin passes' partials, which a thread
+// per row writes and reads).  At most heads (N + C - 1) D floats.
+__host__ __device__ inline size_t blocked_index(int bh, int t, int e, int N, int D, int C) {
+    const int nck = (N + C - 1) / C;
+    return (((size_t)bh * nck + t / C) * D + e) * C + (t % C);
+}
+// Floats of such an array for any chunk length up to 128.
+inline size_t blocked_floats(int heads, int N, int D) { return (size_t)heads * (N + 128) * D; }
 
 // Row stride of the per-row den array on the tensor-core path (16-byte aligned rows).
 inline int tc_den_stride(int N) { return (N + 31) / 32 * 32; }

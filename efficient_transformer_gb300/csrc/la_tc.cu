@@ -655,6 +655,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
             if (i == 0) LA_TL(k, 12);
             const bool rowok = c0 + i % C < t1 && i / C < gr;
             const size_t rg = (size_t)(bh0 + i / C) * p.N + (c0 + i % C);   // the row's index (when rowok)
+            if constexpr (WT)   // sin pass: the next chunk's cos partials (one contiguous block a head)
+                if (p.pass == 2 && i == 0 && k + 1 < nchunk)   // into L2 while this chunk is written out
+                    for (int r = 0; r < gr; ++r)
+                        prefetch_l2_bulk(p.part_num + blocked_index(bh0 + r, c0 + C, 0, p.N, D, C), (uint32_t)(D * C * 4));
             float pden = 0.f;   // sin pass: the cos terms' den of the row
             if constexpr (WT)
                 if (p.pass == 2 && ok && rowok) pden = p.part_den[rg];
@@ -683,10 +687,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                             tmem_ld32(tO + lane_off + c32 * 32, v);
                             tmem_wait_regs<32>(v);
                         }
-                        if (ok && rowok) {
-                            float4 *dst = reinterpret_cast<float4 *>(p.part_num + rg * D + c32 * 32);
+                        if (ok && rowok) {   // chunk-blocked: a warp's rows form one run per column
+                            float *dst = p.part_num + blocked_index(bh0 + i / C, c0 + i % C, c32 * 32, p.N, D, C);
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                            for (int e = 0; e < 32; ++e) dst[(size_t)e * C] = v[e];
                         }
                     }
                     if (ok && rowok) p.part_den[rg] = den;
@@ -717,17 +721,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
                     if constexpr (WT) {   // sin pass: plus the cos terms' numerator; the float32
                                           // output row goes back in its place (the backward's h)
                         if (p.pass == 2 && ok && rowok) {   // (every load before any store)
-                            float4 *src = reinterpret_cast<float4 *>(p.part_num + rg * D + c64 * 64 + hh * 32);
-                            float4 a[8];
+                            float *src = p.part_num + blocked_index(bh0 + i / C, c0 + i % C, c64 * 64 + hh * 32, p.N, D, C);
+                            float a[32];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) a[q] = src[q];
+                            for (int e = 0; e < 32; ++e) a[e] = src[(size_t)e * C];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                v[4 * q] += a[q].x;
-                                v[4 * q + 1] += a[q].y;
-                                v[4 * q + 2] += a[q].z;
-                                v[4 * q + 3] += a[q].w;
-                                src[q] = make_float4(v[4 * q] * inv, v[4 * q + 1] * inv, v[4 * q + 2] * inv, v[4 * q + 3] * inv);
+                            for (int e = 0; e < 32; ++e) {
+                                v[e] += a[e];
+                                src[(size_t)e * C] = v[e] * inv;
                             }
                         }
                     }

@@ -690,12 +690,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     mbar_arrive_warp(&bar_xfree);
                 }
                 if (!ok) continue;
-                if constexpr (WT) {   // cos pass: dq terms (fp32) to the workspace; sin pass: plus those
-                    float4 *pq = reinterpret_cast<float4 *>(p.part_dq + ((size_t)bh * p.N + t) * D + col0);
-                    float4 prev[4] = {};
-                    if (p.pass == 2 && valid)
+                if constexpr (WT) {   // cos pass: dq terms (fp32) to the workspace, chunk-blocked (a
+                                      // warp's rows form one run per column); sin pass: plus those
+                    if (p.pass == 2 && c16 == 0 && h == 0 && i == 0 && k + 1 < nchunk)   // the next chunk's block
+                        for (int r2 = 0; r2 < gr; ++r2)                                 // of them into L2
+                            prefetch_l2_bulk(p.part_dq + blocked_index(bh0 + r2, t0 + (k + 1) * C, 0, p.N, D, C),
+                                             (uint32_t)(D * C * 4));
+                    float *pq = p.part_dq + (valid ? blocked_index(bh, t, col0, p.N, D, C) : 0);
+                    float prev[16];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) prev[q] = __ldg(pq + q);
+                    for (int e = 0; e < 16; ++e) prev[e] = p.pass == 2 && valid ? __ldg(pq + (size_t)e * C) : 0.f;
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8) {
                         float o[8];
@@ -706,14 +710,12 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                         else
                             dq_vals<LA_PHI_IDENTITY>(u[q8], xv + q8 * 8, inv, o);
                         if (p.pass == 1) {
-                            if (valid) {
-                                pq[2 * q8] = make_float4(o[0], o[1], o[2], o[3]);
-                                pq[2 * q8 + 1] = make_float4(o[4], o[5], o[6], o[7]);
-                            }
+                            if (valid)
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) pq[(size_t)(q8 * 8 + e) * C] = o[e];
                         } else {
-                            const float4 a = prev[2 * q8], b2 = prev[2 * q8 + 1];
-                            o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
-                            o[4] += b2.x; o[5] += b2.y; o[6] += b2.z; o[7] += b2.w;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] += prev[q8 * 8 + e];
                             if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 342, smem_u32(ch[q8]) - sm_lo, q8))
                                 *reinterpret_cast<uint4 *>(ch[q8] + OFF_G) =
                                     make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
@@ -1459,20 +1461,28 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// h = -g . out per row (out: the forward's float32 output rows), one warp per row: the h of
-// the cos/sin-weighted backward, shared by its two passes.
-__global__ void k_h_rows(const __nv_bfloat16 *__restrict__ g, Strides sg, int H, int N, const float *__restrict__ out,
-                         float *__restrict__ h, long long rows, int D) {
-    const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;   // bh N + t
-    const int lane = threadIdx.x % 32;
-    if (row >= rows) return;
-    const long long bh = row / N, t = row % N;
-    const __nv_bfloat16 *gr = g + (bh / H) * sg.b + (bh % H) * sg.h + t * sg.n;
+// h = -g . out per row (out: the forward's float32 output rows, chunk-blocked over its
+// C-token chunks): the h of the cos/sin-weighted backward, shared by its two passes.  One
+// block per (head, chunk), thread = row, so the out reads of a column are one run.
+__global__ void k_h_rows(const __nv_bfloat16 *__restrict__ g, Strides sg, int H, int N, int C,
+                         const float *__restrict__ out, float *__restrict__ h, int D) {
+    const int nck = (N + C - 1) / C;
+    const int bh = blockIdx.x / nck, t = (blockIdx.x % nck) * C + threadIdx.x;
+    if (threadIdx.x >= C || t >= N) return;
+    const __nv_bfloat16 *gr = g + (long long)(bh / H) * sg.b + (long long)(bh % H) * sg.h + (long long)t * sg.n;
+    const float *orow = out + blocked_index(bh, t, 0, N, D, C);
     float acc = 0.f;
-    for (int d = lane; d < D; d += 32) acc = fmaf(__bfloat162float(gr[d]), out[row * D + d], acc);
+    for (int d = 0; d < D; d += 8) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(gr + d);
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(&u);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) h[row] = -acc;
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            acc = fmaf(f.x, orow[(size_t)(d + 2 * e) * C], acc);
+            acc = fmaf(f.y, orow[(size_t)(d + 2 * e + 1) * C], acc);
+        }
+    }
+    h[(size_t)bh * N + t] = -acc;
 }
 
 // The backward with cos/sin weights, W_ij = c_i c_j + s_i s_j, as two passes (cos, then sin)
@@ -1492,10 +1502,10 @@ cudaError_t backward_two_pass(const Params &p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     {
-        const long long rows = (long long)p.B * p.Hq * p.N;
         TraceScope ts("tc_bwd_h_rows", s);
-        k_h_rows<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.g), p.st_g, p.Hq, p.N,
-                                                           p.part_num, p.gd, rows, D);
+        const int nck = (p.N + p.chunk - 1) / p.chunk;   // the forward's chunks (p.chunk)
+        k_h_rows<<<(unsigned)(p.B * p.Hq * nck), p.chunk, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.g), p.st_g, p.Hq,
+                                                                  p.N, p.chunk, p.part_num, p.gd, D);
         e = cudaGetLastError();
     }
     const size_t pass_elems = (size_t)p.B * p.Hkv * p.nseg * D * (D + 1);

@@ -361,6 +361,12 @@ __device__ __forceinline__ void tma_load_2d_w(void *dst, const CUtensorMap *map,
         : "memory");
 }
 
+// Bring `bytes` (a multiple of 16) of global memory at p (16-byte aligned) into L2, from the
+// calling thread, without waiting.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Bring one box of a 3-D tensor map into L2 from lane 0 (warp-uniform call).
 __device__ __forceinline__ void tma_prefetch_3d_w(const CUtensorMap *map, int x, int y, int z) {
     asm volatile(
