@@ -1256,6 +1256,11 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
                 if constexpr (WT) {   // w phi'(k) (dk^T + r); cos pass: to the workspace (fp32),
                                       // sin pass: plus the cos pass's (every load before any store)
                     const int c0 = t0 + (nchunk - 1 - k) * C;
+                    if (p.pass == 2 && c16 == 0 && d == 0 && k + 1 < nchunk) {   // the next (earlier) chunk's
+                        const size_t nx = ((size_t)bg * p.N + (c0 - C)) * D;   // C x D blocks into L2
+                        prefetch_l2_bulk(p.part_dk + nx, (uint32_t)(C * D * 4));
+                        prefetch_l2_bulk(p.part_dv + nx, (uint32_t)(C * D * 4));
+                    }
 #pragma unroll
                     for (int e8 = 0; e8 < 16; e8 += 8) {
                         float wv[8], prev[8];
