@@ -155,6 +155,12 @@ EDGE = [
     (1, 2, 2, 129, 128, "bf16", True, "relu", True),
     (1, 16, 2, 300, 64, "bf16", True, "elu+1", False),
     (1, 3, 3, 200, 32, "f32", False, "elu+1", True),
+    # tensor cores: cos/sin passes and masked rows at a single token, a pair, and ragged chunks
+    (1, 1, 1, 1, 128, "bf16", True, "relu", True),
+    (1, 2, 2, 2, 64, "bf16", False, "elu+1", True),
+    (1, 2, 1, 33, 128, "bf16", True, "elu+1", True),
+    (2, 3, 3, 65, 128, "bf16", True, "elu+1", False),
+    (1, 8, 4, 31, 128, "bf16", False, "relu", False),
 ]
 
 
@@ -178,7 +184,7 @@ def test_edge_shapes(case):
     (2, 4, 2, 257, 64, "f32", False, True),
     (1, 8, 2, 1000, 128, "bf16", True, False),    # tensor-core kernels (n_rep 4)
     (2, 4, 4, 3000, 64, "bf16", False, False),   # tensor-core kernels (n_rep 1, bidirectional)
-    (1, 4, 4, 700, 128, "bf16", True, True),      # CUDA-core kernels, position weights
+    (1, 4, 4, 700, 128, "bf16", True, True),      # tensor-core cos/sin passes, masked rows
 ], ids=lambda c: "x".join(map(str, c)))
 def test_identity_feature_map(case):
     """phi = identity on non-negative features (the pages' feature maps are non-negative)."""
