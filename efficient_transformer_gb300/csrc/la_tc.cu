@@ -250,8 +250,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
         }
         ok = ok && warp_wait(&bar_done, 0, &abort_flag);
         tc_fence_after();
-        // TMEM rows (lane d: S[d][0..D-1], z[d]) -> shared memory [D][D + 1] floats (the
-        // stages are idle now; stride D + 1 is odd, so a warp's writes hit distinct banks)
+        // TMEM rows (lane d: S[d][0..D-1], z[d]) -> shared memory in the lane-blocked state
+        // layout (the stages are idle now; a warp's 16-byte stores are side by side)
         const int wq = warp % 4;
         float *srow = reinterpret_cast<float *>(stage0);
         if (ok && warp < 8 && wq * 32 < D) {
@@ -261,12 +261,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
                 float v[16];
                 tmem_ld16(tS + lane_off + c16 * 16, v);
                 tmem_wait_regs<16>(v);
-                if (c16 < D / 16) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) srow[i * (D + 1) + c16 * 16 + e] = v[e];
-                } else {
-                    srow[i * (D + 1) + D] = v[0];
-                }
+                if (c16 < D / 16)
+                    state_store16<D>(srow, i, c16, v);
+                else
+                    state_store_z<D>(srow, i, v[0]);
             }
         }
     }
@@ -517,17 +515,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
         const int ti = i % C;
         // initial S, z of the segment: TMEM (causal) and the bf16 operand tiles
         if (wq * 32 < D) {
-            const float *row = state + (size_t)i * (D + 1);
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 float v[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = row[c16 * 16 + e];
+                state_load16<D>(state, i, c16, v);
                 if (CAUSAL) tmem_st16(tS + lane_off + c16 * 16, v);
                 store_state_row<D>(sbf, i, v, c16);
             }
             float zv[16];
-            zv[0] = row[D];
+            zv[0] = state_z<D>(state, i);
 #pragma unroll
             for (int e = 1; e < 16; ++e) zv[e] = 0.f;
             if (CAUSAL) {

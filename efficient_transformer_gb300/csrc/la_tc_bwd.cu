@@ -548,18 +548,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         const int bh = bh0 + r;
         // initial S, z of the segment: TMEM (causal) and the operand tiles (slot 0)
         if (wq * 32 < D) {
-            const float *row = state + (size_t)i * (D + 1);
 #pragma unroll 1
             for (int c16 = h * (HALF / 16); c16 < (h + 1) * (HALF / 16); ++c16) {
                 float v[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = row[c16 * 16 + e];
+                state_load16<D>(state, i, c16, v);
                 if (CAUSAL) tmem_st16(tS + lane_off + c16 * 16, v);
                 store_state_row<D>(sbf, i, v, c16);
             }
             if (h == 0) {
                 float zv[16];
-                zv[0] = row[D];
+                zv[0] = state_z<D>(state, i);
 #pragma unroll
                 for (int e = 1; e < 16; ++e) zv[e] = 0.f;
                 if (CAUSAL) tmem_st16(tS + lane_off + D, zv);
@@ -740,20 +738,18 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         ok = ok && warp_wait(&bar_fin, 0, &abort_flag);
         tc_fence_after();
         if (ok && wq * 32 < D) {
-            float *row = rstate + (size_t)i * (D + 1);
 #pragma unroll 1
             for (int c16 = h * (HALF / 16); c16 < (h + 1) * (HALF / 16); ++c16) {
                 float v[16];
                 tmem_ld16(tR + lane_off + c16 * 16, v);
                 tmem_wait_regs<16>(v);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) row[c16 * 16 + e] = v[e];
+                state_store16<D>(rstate, i, c16, v);
             }
             if (h == 0) {
                 float rd[16];   // r = phi_s^T h_hi (column 0) + phi_s^T h_lo (column 2)
                 tmem_ld16(tR + lane_off + D, rd);
                 tmem_wait_regs<16>(rd);
-                row[D] = rd[0] + rd[2];
+                state_store_z<D>(rstate, i, rd[0] + rd[2]);
             }
         }
     }
@@ -1159,16 +1155,14 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
         float r_prev = 0.f;   // r before the current chunk
         const float grad_thr = feat_grad_threshold(p.phi);
         if (d < D) {
-            const float *row = rstate + (size_t)d * (D + 1);
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 float v[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = row[c16 * 16 + e];
+                state_load16<D>(rstate, d, c16, v);
                 if (CAUSAL) tmem_st16(tR + lane_off + c16 * 16, v);
                 store_rbf_row<D>(rbf, d, v, c16);
             }
-            r_prev = row[D];
+            r_prev = state_z<D>(rstate, d);
         }
         if (MERGE_H)   // the r part (its two read columns) accumulates onto dk^T's product: clear it
             for (int bb = 0; bb < NB; ++bb) tmem_zero2(tRp(bb) + lane_off);

@@ -266,6 +266,32 @@ __device__ __forceinline__ void feat8_inplace2(uint8_t *chunk, bool valid) {
 
 __host__ __device__ constexpr int align32(int x) { return (x + 31) / 32 * 32; }
 
+// Segment states of the tensor-core kernels (one (S, z) pair, D (D + 1) floats per segment)
+// are lane-blocked: S[d][e] sits at ((e / 4) D + d) 4 + e % 4 and z[d] at D D + d.  A warp
+// whose threads hold rows d (TMEM lanes d) then moves 16 columns as four runs of 512
+// contiguous bytes, where a row-major state costs one 4-byte access per lane and column.  The
+// segment scan adds states elementwise and does not depend on the layout.
+template <int D>
+__device__ __forceinline__ void state_load16(const float *st, int d, int c16, float *v) {
+    const float4 *p = reinterpret_cast<const float4 *>(st);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 x = p[(c16 * 4 + q) * D + d];
+        v[4 * q] = x.x;
+        v[4 * q + 1] = x.y;
+        v[4 * q + 2] = x.z;
+        v[4 * q + 3] = x.w;
+    }
+}
+template <int D>
+__device__ __forceinline__ void state_store16(float *st, int d, int c16, const float *v) {
+    float4 *p = reinterpret_cast<float4 *>(st);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) p[(c16 * 4 + q) * D + d] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+template <int D> __device__ __forceinline__ float state_z(const float *st, int d) { return st[D * D + d]; }
+template <int D> __device__ __forceinline__ void state_store_z(float *st, int d, float z) { st[D * D + d] = z; }
+
 // z (fp32) into column d of a 16-row K-major z tile as rows 0 and 1: z_hi = bf16(z) and
 // z_lo = bf16(z - z_hi), so that a product with the tile gives phi . z_hi and phi . z_lo in two
 // fp32 columns whose sum carries z to about 16 bits.
