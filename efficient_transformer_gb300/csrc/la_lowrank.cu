@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kLrChainThreads, 1) k_lr_chain(const __grid_co
     using K = ChainCfg<RP, B1_MN, B2_MN>;
     constexpr int NS = K::NS;
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();
     __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_tfull, bar_tbf, bar_yfull[K::NY], bar_yfree[K::NY], bar_fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -366,8 +367,7 @@ cudaError_t launch_chain(const void *a1, const void *b1, const void *b2, void *t
     const int ntiles = (ca.M + 127) / 128;
     const int grid = ntiles < kPlanSms ? ntiles : kPlanSms;
     TraceScope ts(name, s);
-    k_lr_chain<RP, B1_MN, B2_MN><<<grid, kLrChainThreads, K::SMEM, s>>>(m_a1, m_b1, m_b2, m_t, a);
-    return cudaGetLastError();
+    return launch_pdl(k_lr_chain<RP, B1_MN, B2_MN>, dim3(grid), dim3(kLrChainThreads), K::SMEM, s, m_a1, m_b1, m_b2, m_t, a);
 }
 
 template <bool B1_MN, bool B2_MN>
@@ -415,6 +415,7 @@ __global__ void __launch_bounds__(kLrThreads, 1) k_lr_wgrad(const __grid_constan
     using K = WgCfg<ROWSUM>;
     constexpr int NS = K::NS;
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();
     __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_done;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -517,6 +518,7 @@ __global__ void __launch_bounds__(kLrThreads, 1) k_lr_wgrad(const __grid_constan
 
 // out[e] = bf16(sum over the S slices of part[s][e]), slices in order (deterministic).
 __global__ void k_lr_reduce(const float *part, int S, size_t elems, __nv_bfloat16 *out) {
+    pdl_wait();
     for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < elems; e += (size_t)gridDim.x * blockDim.x) {
         float acc = 0.f;
         for (int s = 0; s < S; ++s) acc += part[(size_t)s * elems + e];
@@ -547,21 +549,17 @@ cudaError_t wgrad(const void *A, const void *Bm, int M, int Mc, int Nc, float *p
     WgradArgs w{M, Mc, Nc, S, rows_per, part, rsum, err};
     {
         TraceScope ts(name, s);
-        if (rs)
-            k_lr_wgrad<true><<<tiles * S, kLrThreads, WgCfg<true>::SMEM, s>>>(ma, mb, w);
-        else
-            k_lr_wgrad<false><<<tiles * S, kLrThreads, WgCfg<false>::SMEM, s>>>(ma, mb, w);
-        e = cudaGetLastError();
+        e = rs ? launch_pdl(k_lr_wgrad<true>, dim3(tiles * S), dim3(kLrThreads), WgCfg<true>::SMEM, s, ma, mb, w)
+               : launch_pdl(k_lr_wgrad<false>, dim3(tiles * S), dim3(kLrThreads), WgCfg<false>::SMEM, s, ma, mb, w);
     }
     if (e != cudaSuccess) return e;
     TraceScope ts("lr_reduce", s);
     const size_t elems = (size_t)Mc * Nc;
-    k_lr_reduce<<<kPlanSms * 4, 256, 0, s>>>(part, S, elems, static_cast<__nv_bfloat16 *>(out));
-    e = cudaGetLastError();
-    if (e == cudaSuccess && rs) {
-        k_lr_reduce<<<(Mc + 255) / 256, 256, 0, s>>>(rsum, S, (size_t)Mc, static_cast<__nv_bfloat16 *>(rsum_out));
-        e = cudaGetLastError();
-    }
+    e = launch_pdl(k_lr_reduce, dim3(kPlanSms * 4), dim3(256), 0, s, (const float *)part, S, elems,
+                   static_cast<__nv_bfloat16 *>(out));
+    if (e == cudaSuccess && rs)
+        e = launch_pdl(k_lr_reduce, dim3((unsigned)((Mc + 255) / 256)), dim3(256), 0, s, (const float *)rsum, S, (size_t)Mc,
+                       static_cast<__nv_bfloat16 *>(rsum_out));
     return e;
 }
 

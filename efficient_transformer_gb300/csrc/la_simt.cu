@@ -145,6 +145,7 @@ __device__ __forceinline__ float row_sum16(float x) {
 // Per-segment state S = sum_j b_j [v_j, 1]^T over the segment's tokens.
 template <typename T, int D, int P>
 __global__ void __launch_bounds__(kThreads) k_seg_state(Params p) {
+    pdl_wait();
     constexpr int DP = D + 1;
     extern __shared__ float sm[];
     float *S = sm, *bsm = S + P * D * DP, *vsm = bsm + P * kC * DP;
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(kThreads) k_seg_state(Params p) {
 
 // Scan of segment states along the sequence, per (batch, kv head), in a fixed order.
 __global__ void k_scan(float *X, int nseg, size_t elems, int mode) {
+    pdl_wait();
     const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= elems) return;
     float *base = X + (size_t)blockIdx.y * nseg * elems + e;
@@ -197,6 +199,7 @@ __global__ void k_scan(float *X, int nseg, size_t elems, int mode) {
 // Forward: out_i = (A V + a S)_i / (rowsum A + a . z + eps)_i per query head.
 template <typename T, int D, int P>
 __global__ void __launch_bounds__(kThreads) k_fwd(Params p) {
+    pdl_wait();
     constexpr int DP = D + 1, M = D / 16;
     extern __shared__ float sm[];
     float *S = sm, *asm_ = S + P * D * DP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
@@ -260,6 +263,7 @@ __global__ void __launch_bounds__(kThreads) k_fwd(Params p) {
 // Backward, pass 1: dq, and the per-row den_i and gd_i = -(g_i . num_i) / den_i^2.
 template <typename T, int D, int P>
 __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
+    pdl_wait();
     constexpr int DP = D + 1, M = D / 16;
     extern __shared__ float sm[];
     float *S = sm, *asm_ = S + P * D * DP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
@@ -382,6 +386,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
 // a_i [gn_i, gd_i]^T (column D holds r).
 template <typename T, int D, int P>
 __global__ void __launch_bounds__(kThreads) k_seg_rstate(Params p) {
+    pdl_wait();
     constexpr int DP = D + 1;
     extern __shared__ float sm[];
     float *R = sm, *asm_ = R + P * D * DP, *gx = asm_ + P * kC * DP;
@@ -406,6 +411,7 @@ __global__ void __launch_bounds__(kThreads) k_seg_rstate(Params p) {
 // Backward, pass 2 (reverse over chunks): dk, dv for the kv head, summed over the group.
 template <typename T, int D, int P>
 __global__ void __launch_bounds__(kThreads) k_bwd_dkdv(Params p) {
+    pdl_wait();
     constexpr int DP = D + 1, M = D / 16;
     extern __shared__ float sm[];
     float *R = sm, *asm_ = R + P * D * DP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
@@ -502,8 +508,7 @@ cudaError_t launch(const char *name, K kernel, size_t smem, int grid, const Para
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     TraceScope ts(name, s);
-    kernel<<<grid, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, s, p);
 }
 
 
@@ -558,8 +563,7 @@ cudaError_t dispatch_p(const Params &p, cudaStream_t s, bool bwd) {
 cudaError_t scan_segments(float *X, const Params &p, int mode, size_t elems, cudaStream_t s) {
     dim3 grid((unsigned)((elems + 255) / 256), (unsigned)(p.B * p.Hkv));
     TraceScope ts("scan", s);
-    k_scan<<<grid, 256, 0, s>>>(X, p.nseg, elems, mode);
-    return cudaGetLastError();
+    return launch_pdl(k_scan, grid, dim3(256), 0, s, X, p.nseg, elems, mode);
 }
 
 cudaError_t simt_forward(const Params &p, la_dtype dt, cudaStream_t s) {

@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
     using K = StateCfg<D>;
     constexpr int C = K::C, NS = K::NS;
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();
+    LA_SPAN(0, 0);
     __shared__ uint64_t bar_full[NS], bar_ready[NS], bar_empty[NS], bar_done;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(const __grid_cons
     }
     if (warp == 1) tmem_dealloc(tS, 256);
     if (threadIdx.x == 0 && abort_flag) atomicExch(p.err, kErrTimeout);
+    LA_SPAN(0, 1);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -296,6 +299,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
     constexpr int OFF_K = K::Q_BYTES, OFF_V = OFF_K + K::K_BYTES;
     constexpr int NO = K::O2 ? 2 : 1;   // O buffers
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();
+    LA_SPAN(1, 0);
     __shared__ uint64_t bar_full[NS], bar_ready[NS], bar_empty[NS], bar_ofull[2], bar_ofree[2];
     __shared__ uint64_t bar_afull, bar_pready, bar_sfull, bar_sbf, bar_fin;
     __shared__ uint32_t tmem_base;
@@ -757,6 +762,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
     if (threadIdx.x == 0 && abort_flag) atomicExch(p.err, kErrTimeout);
+    LA_SPAN(1, 1);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -770,8 +776,7 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
     if (e == cudaSuccess) e = prepare(k_tc_state<D, WT>, StateCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     TraceScope ts("tc_seg_state", s);
-    k_tc_state<D, WT><<<p.B * p.Hkv * p.nseg, kStateThreads, StateCfg<D>::SMEM, s>>>(mk, mv, p);
-    return cudaGetLastError();
+    return launch_pdl(k_tc_state<D, WT>, dim3(p.B * p.Hkv * p.nseg), dim3(kStateThreads), StateCfg<D>::SMEM, s, mk, mv, p);
 }
 
 template <int D, int G, bool CAUSAL, bool MASK, bool WT>
@@ -785,8 +790,8 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t s) {
     if (e == cudaSuccess) e = prepare(k_tc_fwd<D, G, CAUSAL, MASK, WT>, K::SMEM);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_fwd_causal" : "tc_fwd_bidir", s);
-    k_tc_fwd<D, G, CAUSAL, MASK, WT><<<p.B * p.Hkv * p.nseg, kFwdThreads, K::SMEM, s>>>(mq, mk, mv, mo, p);
-    return cudaGetLastError();
+    return launch_pdl(k_tc_fwd<D, G, CAUSAL, MASK, WT>, dim3(p.B * p.Hkv * p.nseg), dim3(kFwdThreads), K::SMEM, s, mq, mk, mv,
+                      mo, p);
 }
 
 // The forward with cos/sin weights (the cosFormer modulation of the linear_attn page:
@@ -879,6 +884,10 @@ extern "C" int la_test_withhold_arrival(int on) {
 // Timeline builds only: copy out the forward kernel's event clocks ([64][16] long long).
 extern "C" int la_timeline_read(long long *out) {
     return cudaMemcpyFromSymbol(out, la::g_la_tl, sizeof(long long) * 64 * 16) == cudaSuccess ? 0 : 1;
+}
+// ... and the per-block entry and exit times of this file's kernels ([4][256][2], ns).
+extern "C" int la_timeline_read_span(unsigned long long *out) {
+    return cudaMemcpyFromSymbol(out, la::g_la_span, sizeof(unsigned long long) * 4 * 256 * 2) == cudaSuccess ? 0 : 1;
 }
 #endif
 

@@ -185,6 +185,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     constexpr int OFF_DEN = OFF_G + K::G_BYTES;   // den + eps of the 128 rows (fp32)
     constexpr int HALF = D / 2;   // feature columns per pool half
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();
+    LA_SPAN(2, 0);
     // rdone is per stage: the store warp waits for chunk k's r product, and a single barrier could
     // run two phases ahead of it (the next chunk's product may finish first)
     __shared__ uint64_t bar_fulla[NS], bar_fullg[NS], bar_ready[NS], bar_empty[NS], bar_dqready[NS][2], bar_rdone[NS];
@@ -757,6 +759,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
     if (threadIdx.x == 0 && abort_flag) atomicExch(p.err, kErrTimeout);
+    LA_SPAN(2, 1);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -771,6 +774,8 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     constexpr int C = K::C, NS = K::NS, NB = K::NB_KV;
     constexpr int OFF_K = K::Q_BYTES, OFF_V = OFF_K + K::K_BYTES, OFF_G = OFF_V + K::V_BYTES;
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();
+    LA_SPAN(3, 0);
     // each stage is two regions: [Q | g] (free once the chunk's products are done) and
     // [K | V] (dk is written over phi(K) and dv over V, and the region is free once the TMA
     // stores of dk and dv have read it)
@@ -1419,6 +1424,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
     if (threadIdx.x == 0 && abort_flag) atomicExch(p.err, kErrTimeout);
+    LA_SPAN(3, 1);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1449,15 +1455,15 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
     {
         TraceScope ts(CAUSAL ? "tc_bwd_dq_causal" : "tc_bwd_dq_bidir", s);
-        k_tc_bwd_dq<D, G, CAUSAL, MASK, WT><<<grid, kDqThreads, K::DQ_SMEM, s>>>(mq, mk, mv, mg, mdq, mps, mden, p);
-        e = cudaGetLastError();
+        e = launch_pdl(k_tc_bwd_dq<D, G, CAUSAL, MASK, WT>, dim3(grid), dim3(kDqThreads), K::DQ_SMEM, s, mq, mk, mv, mg, mdq,
+                       mps, mden, p);
     }
     if (e == cudaSuccess)
         e = scan_segments(p.rstate, p, CAUSAL ? kScanSuffix : kScanTotal, (size_t)D * (D + 1), s);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_bwd_dkdv_causal" : "tc_bwd_dkdv_bidir", s);
-    k_tc_bwd_dkdv<D, G, CAUSAL, MASK, WT><<<grid, kKvThreads, K::DKDV_SMEM, s>>>(mqs, mk, mv, mg, mdk, mdv, p);
-    return cudaGetLastError();
+    return launch_pdl(k_tc_bwd_dkdv<D, G, CAUSAL, MASK, WT>, dim3(grid), dim3(kKvThreads), K::DKDV_SMEM, s, mqs, mk, mv, mg,
+                      mdk, mdv, p);
 }
 
 // h = -g . out per row (out: the forward's float32 output rows, chunk-blocked over its
@@ -1465,6 +1471,7 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
 // block per (head, chunk), thread = row, so the out reads of a column are one run.
 __global__ void k_h_rows(const __nv_bfloat16 *__restrict__ g, Strides sg, int H, int N, int C,
                          const float *__restrict__ out, float *__restrict__ h, int D) {
+    pdl_wait();
     const int nck = (N + C - 1) / C;
     const int bh = blockIdx.x / nck, t = (blockIdx.x % nck) * C + threadIdx.x;
     if (threadIdx.x >= C || t >= N) return;
@@ -1503,9 +1510,8 @@ cudaError_t backward_two_pass(const Params &p, cudaStream_t s) {
     {
         TraceScope ts("tc_bwd_h_rows", s);
         const int nck = (p.N + p.chunk - 1) / p.chunk;   // the forward's chunks (p.chunk)
-        k_h_rows<<<(unsigned)(p.B * p.Hq * nck), p.chunk, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.g), p.st_g, p.Hq,
-                                                                  p.N, p.chunk, p.part_num, p.gd, D);
-        e = cudaGetLastError();
+        e = launch_pdl(k_h_rows, dim3((unsigned)(p.B * p.Hq * nck)), dim3(p.chunk), 0, s,
+                       static_cast<const __nv_bfloat16 *>(p.g), p.st_g, p.Hq, p.N, p.chunk, (const float *)p.part_num, p.gd, D);
     }
     const size_t pass_elems = (size_t)p.B * p.Hkv * p.nseg * D * (D + 1);
     for (int pass = 1; pass <= 2 && e == cudaSuccess; ++pass) {
@@ -1571,6 +1577,10 @@ extern "C" int la_timeline_read_bwd(long long *out) {
 // ... and the dk/dv kernel's.
 extern "C" int la_timeline_read_bwd2(long long *out) {
     return cudaMemcpyFromSymbol(out, la::g_la_tl2, sizeof(long long) * 64 * 16) == cudaSuccess ? 0 : 1;
+}
+// ... and the per-block entry and exit times of this file's kernels ([4][256][2], ns).
+extern "C" int la_timeline_read_span_bwd(unsigned long long *out) {
+    return cudaMemcpyFromSymbol(out, la::g_la_span, sizeof(unsigned long long) * 4 * 256 * 2) == cudaSuccess ? 0 : 1;
 }
 #endif
 

@@ -87,12 +87,26 @@ __device__ long long g_la_tl2[64][16];   // a second kernel of the same translat
     do {                                                               \
         if (blockIdx.x == 0 && (k) < 64) g_la_tl2[(k)][(ev)] = clock64(); \
     } while (0)
+// ... and every block of kernel `kid` records the global timer (ns) at its entry (ev 0) and
+// exit (ev 1), read back with la_timeline_read_span()
+__device__ unsigned long long g_la_span[4][256][2];
+#define LA_SPAN(kid, ev)                                                                            \
+    do {                                                                                            \
+        if (threadIdx.x == 0 && blockIdx.x < 256) {                                                 \
+            unsigned long long t_;                                                                  \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                  \
+            g_la_span[(kid)][blockIdx.x][(ev)] = t_;                                                \
+        }                                                                                           \
+    } while (0)
 #else
 #define LA_TL(k, ev) \
     do {             \
     } while (0)
 #define LA_TL2(k, ev) \
     do {              \
+    } while (0)
+#define LA_SPAN(kid, ev) \
+    do {                 \
     } while (0)
 #endif
 
