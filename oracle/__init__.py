@@ -56,6 +56,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.la_oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, i,
                                   ctypes.c_double, dp, dp]
     lib.la_oracle_bwd.restype = ctypes.c_int
+    lib.la_oracle_fwd_v.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, i, ctypes.c_double, dp, dp]
+    lib.la_oracle_fwd_v.restype = None
+    lib.la_oracle_bwd_v.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, i, i,
+                                    ctypes.c_double, dp, dp]
+    lib.la_oracle_bwd_v.restype = ctypes.c_int
     lib.la_oracle_num_threads.argtypes = []
     lib.la_oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -93,11 +98,12 @@ def _ptr(a: np.ndarray | None):
 
 
 def _check(q, k, v, cos_weight, sin_weight):
+    """Shapes: q [B, Hq, N, D], k [B, Hkv, N, D], v [B, Hkv, N, Dv] (Dv may differ from D)."""
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
         raise ValueError("q, k, v must be [B, H, N, D]")
     B, Hq, N, D = q.shape
     Bk, Hkv, Nk, Dk = k.shape
-    if (Bk, Nk, Dk) != (B, N, D) or v.shape != k.shape:
+    if (Bk, Nk, Dk) != (B, N, D) or v.shape[:3] != k.shape[:3] or v.shape[3] < 1:
         raise ValueError("q, k, v shapes disagree")
     if Hkv <= 0 or Hq % Hkv != 0:
         raise ValueError("query heads must be a multiple of key/value heads")
@@ -105,17 +111,17 @@ def _check(q, k, v, cos_weight, sin_weight):
         raise ValueError("give both position weights or neither")
     if cos_weight is not None and (cos_weight.shape != (N,) or sin_weight.shape != (N,)):
         raise ValueError("position weights must have length N")
-    return B, Hq, Hkv, N, D
+    return B, Hq, Hkv, N, D, v.shape[3]
 
 
 def fwd(q, k, v, is_causal: bool = False, phi: str = "elu+1", eps: float = 1e-6,
         cos_weight=None, sin_weight=None, lib: ctypes.CDLL | None = None) -> np.ndarray:
-    """Oracle forward: ``out`` as float64 [B, Hq, N, D]."""
+    """Oracle forward: ``out`` as float64 [B, Hq, N, Dv]."""
     q, k, v, cw, sw = (_f64(x) for x in (q, k, v, cos_weight, sin_weight))
-    B, Hq, Hkv, N, D = _check(q, k, v, cw, sw)
-    out = np.empty_like(q)
-    (lib or load()).la_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, D,
-                                  int(bool(is_causal)), PHI[phi], float(eps), _ptr(cw), _ptr(sw))
+    B, Hq, Hkv, N, D, Dv = _check(q, k, v, cw, sw)
+    out = np.empty((B, Hq, N, Dv), dtype=np.float64)
+    (lib or load()).la_oracle_fwd_v(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, D, Dv,
+                                    int(bool(is_causal)), PHI[phi], float(eps), _ptr(cw), _ptr(sw))
     return out
 
 
@@ -123,15 +129,15 @@ def bwd(q, k, v, grad_out, is_causal: bool = False, phi: str = "elu+1", eps: flo
         cos_weight=None, sin_weight=None, lib: ctypes.CDLL | None = None):
     """Oracle backward: ``(dq, dk, dv)`` as float64; dk, dv have the key/value shape."""
     q, k, v, g, cw, sw = (_f64(x) for x in (q, k, v, grad_out, cos_weight, sin_weight))
-    B, Hq, Hkv, N, D = _check(q, k, v, cw, sw)
-    if g.shape != q.shape:
-        raise ValueError("grad_out must have the shape of q")
+    B, Hq, Hkv, N, D, Dv = _check(q, k, v, cw, sw)
+    if g.shape != (B, Hq, N, Dv):
+        raise ValueError("grad_out must have the shape of out ([B, Hq, N, Dv])")
     dq = np.empty_like(q)
     dk = np.empty_like(k)
     dv = np.empty_like(v)
-    rc = (lib or load()).la_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(dq), _ptr(dk),
-                                       _ptr(dv), B, Hq, Hkv, N, D, int(bool(is_causal)), PHI[phi],
-                                       float(eps), _ptr(cw), _ptr(sw))
+    rc = (lib or load()).la_oracle_bwd_v(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(dq), _ptr(dk),
+                                         _ptr(dv), B, Hq, Hkv, N, D, Dv, int(bool(is_causal)), PHI[phi],
+                                         float(eps), _ptr(cw), _ptr(sw))
     if rc != 0:
         raise MemoryError("oracle could not allocate its scratch arrays")
     return dq, dk, dv

@@ -36,7 +36,10 @@
  * num/den).  phi'(x) = (x > 0 ? 1 : exp(x)) for elu+1, (x > 0 ? 1 : 0) for relu and 1 for
  * identity.
  *
- * Layout: every tensor is a contiguous row-major float64 array [B, H, N, D]; Dv = D.
+ * Layout: every tensor is a contiguous row-major float64 array: q, k, dq, dk [B, H, N, D] and
+ * v, out, grad_out, dv [B, H, N, Dv].  The value width Dv may differ from D: `fwd` takes v
+ * as a tensor of its own and reads only q's head dimension, and the state S = sum b v^T is
+ * D x Dv (the `_v` entry points; la_oracle_fwd and la_oracle_bwd take Dv = D).
  * The weights, when given, are float64 arrays of length N (both or neither).
  * The outer loop over (batch, query head) runs under OpenMP when built with -fopenmp;
  * each iteration writes only its own rows, and the group sum runs afterwards in a fixed
@@ -81,103 +84,111 @@ static double weight(const double *cw, const double *sw, int p, int i)
     return p == 0 ? cw[i] : sw[i];
 }
 
-/* Add token j of one key/value head to the state: S^p += b_j^p v_j^T, z^p += b_j^p. */
+/* Add token j of one key/value head to the state: S^p += b_j^p v_j^T, z^p += b_j^p
+ * (S^p is D x Dv). */
 static void add_token(double *S, double *z, const double *kj, const double *vj, int D,
-                      int P, int phi, const double *cw, const double *sw, int j)
+                      int Dv, int P, int phi, const double *cw, const double *sw, int j)
 {
     for (int p = 0; p < P; ++p) {
         double w = weight(cw, sw, p, j);
         for (int d = 0; d < D; ++d) {
             double bd = w * feature(kj[d], phi);
             z[p * D + d] += bd;
-            for (int e = 0; e < D; ++e) S[(p * D + d) * D + e] += bd * vj[e];
+            for (int e = 0; e < Dv; ++e) S[(p * D + d) * Dv + e] += bd * vj[e];
         }
     }
 }
 
-/* num_i and den_i for query row i against the current state. */
-static void read_out(const double *S, const double *z, const double *qi, int D, int P,
+/* num_i (Dv values) and den_i for query row i against the current state. */
+static void read_out(const double *S, const double *z, const double *qi, int D, int Dv, int P,
                      int phi, const double *cw, const double *sw, int i, double eps,
                      double *num, double *den)
 {
-    for (int e = 0; e < D; ++e) num[e] = 0.0;
+    for (int e = 0; e < Dv; ++e) num[e] = 0.0;
     double dn = 0.0;
     for (int p = 0; p < P; ++p) {
         double w = weight(cw, sw, p, i);
         for (int d = 0; d < D; ++d) {
             double ad = w * feature(qi[d], phi);
             dn += ad * z[p * D + d];
-            for (int e = 0; e < D; ++e) num[e] += ad * S[(p * D + d) * D + e];
+            for (int e = 0; e < Dv; ++e) num[e] += ad * S[(p * D + d) * Dv + e];
         }
     }
     *den = dn + eps;
 }
 
 static void head_forward(const double *qh, const double *kh, const double *vh, double *oh,
-                         int N, int D, int causal, int phi, double eps, const double *cw,
+                         int N, int D, int Dv, int causal, int phi, double eps, const double *cw,
                          const double *sw)
 {
     int P = cw ? 2 : 1;
-    double *S = calloc((size_t)P * D * D, sizeof(double));
+    double *S = calloc((size_t)P * D * Dv, sizeof(double));
     double *z = calloc((size_t)P * D, sizeof(double));
-    double *num = malloc((size_t)D * sizeof(double));
+    double *num = malloc((size_t)Dv * sizeof(double));
     if (!causal)
         for (int j = 0; j < N; ++j)
-            add_token(S, z, kh + (size_t)j * D, vh + (size_t)j * D, D, P, phi, cw, sw, j);
+            add_token(S, z, kh + (size_t)j * D, vh + (size_t)j * Dv, D, Dv, P, phi, cw, sw, j);
     for (int i = 0; i < N; ++i) {
         if (causal)
-            add_token(S, z, kh + (size_t)i * D, vh + (size_t)i * D, D, P, phi, cw, sw, i);
+            add_token(S, z, kh + (size_t)i * D, vh + (size_t)i * Dv, D, Dv, P, phi, cw, sw, i);
         double den;
-        read_out(S, z, qh + (size_t)i * D, D, P, phi, cw, sw, i, eps, num, &den);
-        for (int e = 0; e < D; ++e) oh[(size_t)i * D + e] = num[e] / den;
+        read_out(S, z, qh + (size_t)i * D, D, Dv, P, phi, cw, sw, i, eps, num, &den);
+        for (int e = 0; e < Dv; ++e) oh[(size_t)i * Dv + e] = num[e] / den;
     }
     free(S);
     free(z);
     free(num);
 }
 
+void la_oracle_fwd_v(const double *q, const double *k, const double *v, double *out, int B,
+                     int Hq, int Hkv, int N, int D, int Dv, int causal, int phi, double eps,
+                     const double *cos_weight, const double *sin_weight)
+{
+    int n_rep = Hq / Hkv;
+    size_t head = (size_t)N * D, vhead = (size_t)N * Dv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * Hq; ++bh) {
+        int b = bh / Hq, h = bh % Hq, g = h / n_rep;
+        size_t kv = (size_t)b * Hkv + g;
+        head_forward(q + (size_t)bh * head, k + kv * head, v + kv * vhead, out + (size_t)bh * vhead,
+                     N, D, Dv, causal, phi, eps, cos_weight, sin_weight);
+    }
+}
+
 void la_oracle_fwd(const double *q, const double *k, const double *v, double *out, int B,
                    int Hq, int Hkv, int N, int D, int causal, int phi, double eps,
                    const double *cos_weight, const double *sin_weight)
 {
-    int n_rep = Hq / Hkv;
-    size_t head = (size_t)N * D;
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int bh = 0; bh < B * Hq; ++bh) {
-        int b = bh / Hq, h = bh % Hq, g = h / n_rep;
-        size_t kv_off = ((size_t)b * Hkv + g) * head;
-        head_forward(q + (size_t)bh * head, k + kv_off, v + kv_off, out + (size_t)bh * head,
-                     N, D, causal, phi, eps, cos_weight, sin_weight);
-    }
+    la_oracle_fwd_v(q, k, v, out, B, Hq, Hkv, N, D, D, causal, phi, eps, cos_weight, sin_weight);
 }
 
 /* Backward for one query head.  dk_h and dv_h receive this head's own contribution to
  * the gradient of its key/value head (summed over the group by the caller). */
 static void head_backward(const double *qh, const double *kh, const double *vh,
                           const double *gh, double *dqh, double *dkh, double *dvh, int N,
-                          int D, int causal, int phi, double eps, const double *cw,
+                          int D, int Dv, int causal, int phi, double eps, const double *cw,
                           const double *sw)
 {
     int P = cw ? 2 : 1;
-    double *S = calloc((size_t)P * D * D, sizeof(double));
+    double *S = calloc((size_t)P * D * Dv, sizeof(double));
     double *z = calloc((size_t)P * D, sizeof(double));
-    double *num = malloc((size_t)D * sizeof(double));
-    double *gn = malloc((size_t)N * D * sizeof(double));  /* gn_i per row */
-    double *gd = malloc((size_t)N * sizeof(double));      /* gd_i per row */
+    double *num = malloc((size_t)Dv * sizeof(double));
+    double *gn = malloc((size_t)N * Dv * sizeof(double));  /* gn_i per row */
+    double *gd = malloc((size_t)N * sizeof(double));       /* gd_i per row */
 
     /* Forward over i: the state S_i, z_i; the row gradients gn, gd; dq. */
     if (!causal)
         for (int j = 0; j < N; ++j)
-            add_token(S, z, kh + (size_t)j * D, vh + (size_t)j * D, D, P, phi, cw, sw, j);
+            add_token(S, z, kh + (size_t)j * D, vh + (size_t)j * Dv, D, Dv, P, phi, cw, sw, j);
     for (int i = 0; i < N; ++i) {
-        const double *qi = qh + (size_t)i * D, *gi = gh + (size_t)i * D;
+        const double *qi = qh + (size_t)i * D, *gi = gh + (size_t)i * Dv;
         if (causal)
-            add_token(S, z, kh + (size_t)i * D, vh + (size_t)i * D, D, P, phi, cw, sw, i);
+            add_token(S, z, kh + (size_t)i * D, vh + (size_t)i * Dv, D, Dv, P, phi, cw, sw, i);
         double den;
-        read_out(S, z, qi, D, P, phi, cw, sw, i, eps, num, &den);
+        read_out(S, z, qi, D, Dv, P, phi, cw, sw, i, eps, num, &den);
         double g_dot_num = 0.0;
-        for (int e = 0; e < D; ++e) {
-            gn[(size_t)i * D + e] = gi[e] / den;
+        for (int e = 0; e < Dv; ++e) {
+            gn[(size_t)i * Dv + e] = gi[e] / den;
             g_dot_num += gi[e] * num[e];
         }
         gd[i] = -g_dot_num / (den * den);
@@ -185,15 +196,15 @@ static void head_backward(const double *qh, const double *kh, const double *vh,
             double acc = 0.0;  /* sum_p w_i^p da_i^p[d] */
             for (int p = 0; p < P; ++p) {
                 double da = gd[i] * z[p * D + d];
-                for (int e = 0; e < D; ++e) da += S[(p * D + d) * D + e] * gn[(size_t)i * D + e];
+                for (int e = 0; e < Dv; ++e) da += S[(p * D + d) * Dv + e] * gn[(size_t)i * Dv + e];
                 acc += weight(cw, sw, p, i) * da;
             }
             dqh[(size_t)i * D + d] = feature_grad(qi[d], phi) * acc;
         }
     }
 
-    /* Backward over j: R_j^p, r_j^p summed over the rows i that attend to j. */
-    double *R = calloc((size_t)P * D * D, sizeof(double));
+    /* Backward over j: R_j^p (D x Dv), r_j^p summed over the rows i that attend to j. */
+    double *R = calloc((size_t)P * D * Dv, sizeof(double));
     double *r = calloc((size_t)P * D, sizeof(double));
     if (!causal)
         for (int i = 0; i < N; ++i)
@@ -202,7 +213,7 @@ static void head_backward(const double *qh, const double *kh, const double *vh,
                 for (int d = 0; d < D; ++d) {
                     double ad = w * feature(qh[(size_t)i * D + d], phi);
                     r[p * D + d] += gd[i] * ad;
-                    for (int e = 0; e < D; ++e) R[(p * D + d) * D + e] += ad * gn[(size_t)i * D + e];
+                    for (int e = 0; e < Dv; ++e) R[(p * D + d) * Dv + e] += ad * gn[(size_t)i * Dv + e];
                 }
             }
     for (int j = N - 1; j >= 0; --j) {
@@ -212,20 +223,20 @@ static void head_backward(const double *qh, const double *kh, const double *vh,
                 for (int d = 0; d < D; ++d) {
                     double ad = w * feature(qh[(size_t)j * D + d], phi);
                     r[p * D + d] += gd[j] * ad;
-                    for (int e = 0; e < D; ++e) R[(p * D + d) * D + e] += ad * gn[(size_t)j * D + e];
+                    for (int e = 0; e < Dv; ++e) R[(p * D + d) * Dv + e] += ad * gn[(size_t)j * Dv + e];
                 }
             }
-        const double *kj = kh + (size_t)j * D, *vj = vh + (size_t)j * D;
-        for (int e = 0; e < D; ++e) dvh[(size_t)j * D + e] = 0.0;
+        const double *kj = kh + (size_t)j * D, *vj = vh + (size_t)j * Dv;
+        for (int e = 0; e < Dv; ++e) dvh[(size_t)j * Dv + e] = 0.0;
         for (int d = 0; d < D; ++d) {
             double acc = 0.0;  /* sum_p w_j^p db_j^p[d] */
             for (int p = 0; p < P; ++p) {
                 double w = weight(cw, sw, p, j);
                 double bd = w * feature(kj[d], phi);
                 double db = r[p * D + d];
-                for (int e = 0; e < D; ++e) {
-                    db += R[(p * D + d) * D + e] * vj[e];
-                    dvh[(size_t)j * D + e] += R[(p * D + d) * D + e] * bd;
+                for (int e = 0; e < Dv; ++e) {
+                    db += R[(p * D + d) * Dv + e] * vj[e];
+                    dvh[(size_t)j * Dv + e] += R[(p * D + d) * Dv + e] * bd;
                 }
                 acc += w * db;
             }
@@ -237,37 +248,48 @@ static void head_backward(const double *qh, const double *kh, const double *vh,
 
 /* Returns 0 on success, 1 when scratch memory for the per-query-head key/value
  * gradients could not be allocated. */
-int la_oracle_bwd(const double *q, const double *k, const double *v, const double *grad_out,
-                  double *dq, double *dk, double *dv, int B, int Hq, int Hkv, int N, int D,
-                  int causal, int phi, double eps, const double *cos_weight,
-                  const double *sin_weight)
+int la_oracle_bwd_v(const double *q, const double *k, const double *v, const double *grad_out,
+                    double *dq, double *dk, double *dv, int B, int Hq, int Hkv, int N, int D,
+                    int Dv, int causal, int phi, double eps, const double *cos_weight,
+                    const double *sin_weight)
 {
     int n_rep = Hq / Hkv;
-    size_t head = (size_t)N * D;
-    /* Key/value gradients per query head, [B, Hq, N, D], as the expanded tensors of the
-     * gqa page before its group reduction. */
+    size_t head = (size_t)N * D, vhead = (size_t)N * Dv;
+    /* Key/value gradients per query head, [B, Hq, N, D] and [B, Hq, N, Dv], as the expanded
+     * tensors of the gqa page before its group reduction. */
     double *dk_x = malloc((size_t)B * Hq * head * sizeof(double));
-    double *dv_x = malloc((size_t)B * Hq * head * sizeof(double));
+    double *dv_x = malloc((size_t)B * Hq * vhead * sizeof(double));
     if (!dk_x || !dv_x) { free(dk_x); free(dv_x); return 1; }
 #pragma omp parallel for schedule(dynamic, 1)
     for (int bh = 0; bh < B * Hq; ++bh) {
         int b = bh / Hq, h = bh % Hq, g = h / n_rep;
-        size_t kv_off = ((size_t)b * Hkv + g) * head;
-        head_backward(q + (size_t)bh * head, k + kv_off, v + kv_off, grad_out + (size_t)bh * head,
-                      dq + (size_t)bh * head, dk_x + (size_t)bh * head, dv_x + (size_t)bh * head,
-                      N, D, causal, phi, eps, cos_weight, sin_weight);
+        size_t kv = (size_t)b * Hkv + g;
+        head_backward(q + (size_t)bh * head, k + kv * head, v + kv * vhead, grad_out + (size_t)bh * vhead,
+                      dq + (size_t)bh * head, dk_x + (size_t)bh * head, dv_x + (size_t)bh * vhead,
+                      N, D, Dv, causal, phi, eps, cos_weight, sin_weight);
     }
-    /* view(B, Hkv, n_rep, N, D).sum(2), in a fixed order. */
+    /* view(B, Hkv, n_rep, N, D).sum(2) (and N, Dv for dv), in a fixed order. */
     for (int b = 0; b < B; ++b)
         for (int g = 0; g < Hkv; ++g) {
-            double *dkg = dk + ((size_t)b * Hkv + g) * head, *dvg = dv + ((size_t)b * Hkv + g) * head;
-            for (size_t t = 0; t < head; ++t) { dkg[t] = 0.0; dvg[t] = 0.0; }
+            double *dkg = dk + ((size_t)b * Hkv + g) * head, *dvg = dv + ((size_t)b * Hkv + g) * vhead;
+            for (size_t t = 0; t < head; ++t) dkg[t] = 0.0;
+            for (size_t t = 0; t < vhead; ++t) dvg[t] = 0.0;
             for (int rr = 0; rr < n_rep; ++rr) {
-                size_t src = ((size_t)b * Hq + (size_t)g * n_rep + rr) * head;
-                for (size_t t = 0; t < head; ++t) { dkg[t] += dk_x[src + t]; dvg[t] += dv_x[src + t]; }
+                size_t src = (size_t)b * Hq + (size_t)g * n_rep + rr;
+                for (size_t t = 0; t < head; ++t) dkg[t] += dk_x[src * head + t];
+                for (size_t t = 0; t < vhead; ++t) dvg[t] += dv_x[src * vhead + t];
             }
         }
     free(dk_x);
     free(dv_x);
     return 0;
+}
+
+int la_oracle_bwd(const double *q, const double *k, const double *v, const double *grad_out,
+                  double *dq, double *dk, double *dv, int B, int Hq, int Hkv, int N, int D,
+                  int causal, int phi, double eps, const double *cos_weight,
+                  const double *sin_weight)
+{
+    return la_oracle_bwd_v(q, k, v, grad_out, dq, dk, dv, B, Hq, Hkv, N, D, D, causal, phi, eps,
+                           cos_weight, sin_weight);
 }

@@ -13,7 +13,11 @@ Each check compares the oracle with something that is not the oracle:
 * closed forms and symmetries (row 0, N = 1, key permutations, all-ones values, dead
   relu rows, causal last row equals bidirectional last row, the cos/sin identity);
 * the grouped-query rule of the gqa page: expand k, v with h -> h // n_rep, run every
-  query head on its own, then sum dk, dv with view(B, Hkv, n_rep, N, D).sum(2).
+  query head on its own, then sum dk, dv with view(B, Hkv, n_rep, N, D).sum(2);
+* a value width Dv different from the head dimension D: the quadratic form and its
+  autograd at Dv != D, and the independence of the value columns (splitting v and g into
+  column blocks gives out and dv block by block, and dq, dk as the sum over the blocks,
+  every block sharing one den).
 
 The helpers here never call the CUDA library.
 """
@@ -90,16 +94,17 @@ def autograd_backward(q, k, v, g, causal, phi, eps, cw=None, sw=None):
     return tuple(x.numpy() for x in grads)
 
 
-def rand_case(B, Hq, Hkv, N, D, seed, weights=False, scale=1.0, avoid_kink=False, positive=False):
+def rand_case(B, Hq, Hkv, N, D, seed, weights=False, scale=1.0, avoid_kink=False, positive=False, Dv=None):
     """Random case; positive=True draws |N(0,1)| for q and k (identity feature map, whose
-    features the pages call non-negative)."""
+    features the pages call non-negative); Dv is the value width (D when None)."""
     rng = np.random.default_rng(seed)
+    Dv = D if Dv is None else Dv
     q = rng.standard_normal((B, Hq, N, D)) * scale
     k = rng.standard_normal((B, Hkv, N, D)) * scale
     if positive:
         q, k = np.abs(q), np.abs(k)
-    v = rng.standard_normal((B, Hkv, N, D))
-    g = rng.standard_normal((B, Hq, N, D))
+    v = rng.standard_normal((B, Hkv, N, Dv))
+    g = rng.standard_normal((B, Hq, N, Dv))
     if avoid_kink:  # keep relu inputs away from 0 for finite differences
         for x in (q, k):
             x[np.abs(x) < 1e-2] += 0.05
@@ -264,13 +269,45 @@ def check_gradient_identities(lib=None):
     return fails
 
 
+def check_value_width(lib=None, tol_fwd=1e-12, tol_bwd=1e-10, tol_split=1e-13):
+    """Dv != D: quadratic form and its autograd, and the value columns' independence."""
+    fails = []
+    cases = [(True, "elu+1", False, 2, 2, 5, 3), (False, "relu", True, 4, 2, 4, 7), (True, "relu", True, 6, 2, 3, 8),
+             (False, "identity", False, 2, 1, 6, 2), (True, "elu+1", True, 2, 1, 2, 9)]
+    for idx, (causal, phi, weights, Hq, Hkv, D, Dv) in enumerate(cases):
+        q, k, v, g, cw, sw = rand_case(2, Hq, Hkv, 9, D, seed=800 + idx, weights=weights,
+                                       positive=phi == "identity", Dv=Dv)
+        out = oracle.fwd(q, k, v, causal, phi, 1e-6, cw, sw, lib=lib)
+        e = rel_err(out, brute_forward(q, k, v, causal, phi, 1e-6, cw, sw))
+        if not e <= tol_fwd:
+            fails.append(f"value width fwd brute case={idx} err={e:.3e}")
+        got = oracle.bwd(q, k, v, g, causal, phi, 1e-6, cw, sw, lib=lib)
+        for name, a, b in zip(("dq", "dk", "dv"), got, autograd_backward(q, k, v, g, causal, phi, 1e-6, cw, sw)):
+            e = rel_err(a, b)
+            if not e <= tol_bwd:
+                fails.append(f"value width bwd autograd case={idx} {name} err={e:.3e}")
+        # column blocks [0, c) and [c, Dv): out and dv side by side, dq and dk summed
+        c = Dv // 2
+        parts = [(v[..., :c], g[..., :c]), (v[..., c:], g[..., c:])]
+        outs = [oracle.fwd(q, k, vb, causal, phi, 1e-6, cw, sw, lib=lib) for vb, _ in parts]
+        grads = [oracle.bwd(q, k, vb, gb, causal, phi, 1e-6, cw, sw, lib=lib) for vb, gb in parts]
+        for name, a, b in (("out", out, np.concatenate(outs, -1)),
+                           ("dq", got[0], grads[0][0] + grads[1][0]),
+                           ("dk", got[1], grads[0][1] + grads[1][1]),
+                           ("dv", got[2], np.concatenate([grads[0][2], grads[1][2]], -1))):
+            e = rel_err(a, b)
+            if not e <= tol_split:
+                fails.append(f"value width column split case={idx} {name} err={e:.3e}")
+    return fails
+
+
 def check_finite_differences(lib=None, h=1e-6, tol=1e-6):
     fails = []
-    cases = [(True, "elu+1", False, 2, 1), (False, "relu", False, 1, 1), (True, "relu", True, 2, 2),
-             (False, "elu+1", True, 2, 1), (True, "identity", False, 2, 1)]
-    for idx, (causal, phi, weights, Hq, Hkv) in enumerate(cases):
+    cases = [(True, "elu+1", False, 2, 1, 3), (False, "relu", False, 1, 1, 3), (True, "relu", True, 2, 2, 3),
+             (False, "elu+1", True, 2, 1, 3), (True, "identity", False, 2, 1, 3), (True, "elu+1", True, 2, 1, 5)]
+    for idx, (causal, phi, weights, Hq, Hkv, Dv) in enumerate(cases):
         q, k, v, g, cw, sw = rand_case(1, Hq, Hkv, 5, 3, seed=700 + idx, weights=weights,
-                                       avoid_kink=True, positive=phi == "identity")
+                                       avoid_kink=True, positive=phi == "identity", Dv=Dv)
         dq, dk, dv = oracle.bwd(q, k, v, g, causal, phi, 1e-6, cw, sw, lib=lib)
         for name, x, dx in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
             fd = np.zeros_like(x)
@@ -293,7 +330,7 @@ def check_finite_differences(lib=None, h=1e-6, tol=1e-6):
 
 
 ALL_CHECKS = [check_forward_brute, check_backward_autograd, check_gqa_rule, check_closed_forms,
-              check_symmetries, check_gradient_identities, check_finite_differences]
+              check_symmetries, check_gradient_identities, check_value_width, check_finite_differences]
 
 
 def run_all(lib=None):

@@ -15,13 +15,14 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "la_oracle.c")
 MUTANTS = {
     "drop_eps": ("*den = dn + eps;", "*den = dn;"),
     "gd_sign": ("gd[i] = -g_dot_num / (den * den);", "gd[i] = g_dot_num / (den * den);"),
-    "readout_transposed_state": ("num[e] += ad * S[(p * D + d) * D + e];", "num[e] += ad * S[(p * D + e) * D + d];"),
-    "dq_transposed_state": ("da += S[(p * D + d) * D + e] * gn[(size_t)i * D + e];",
-                            "da += S[(p * D + e) * D + d] * gn[(size_t)i * D + e];"),
-    "dv_transposed_state": ("dvh[(size_t)j * D + e] += R[(p * D + d) * D + e] * bd;",
-                            "dvh[(size_t)j * D + e] += R[(p * D + e) * D + d] * bd;"),
-    "gqa_head_map": ("int b = bh / Hq, h = bh % Hq, g = h / n_rep;\n        size_t kv_off = ((size_t)b * Hkv + g) * head;\n        head_forward",
-                     "int b = bh / Hq, h = bh % Hq, g = h % Hkv;\n        size_t kv_off = ((size_t)b * Hkv + g) * head;\n        head_forward"),
+    # (the transposed reads stay inside the P D Dv state: (p Dv + e) D + d)
+    "readout_transposed_state": ("num[e] += ad * S[(p * D + d) * Dv + e];", "num[e] += ad * S[(p * Dv + e) * D + d];"),
+    "dq_transposed_state": ("da += S[(p * D + d) * Dv + e] * gn[(size_t)i * Dv + e];",
+                            "da += S[(p * Dv + e) * D + d] * gn[(size_t)i * Dv + e];"),
+    "dv_transposed_state": ("dvh[(size_t)j * Dv + e] += R[(p * D + d) * Dv + e] * bd;",
+                            "dvh[(size_t)j * Dv + e] += R[(p * Dv + e) * D + d] * bd;"),
+    "gqa_head_map": ("int b = bh / Hq, h = bh % Hq, g = h / n_rep;\n        size_t kv = (size_t)b * Hkv + g;\n        head_forward",
+                     "int b = bh / Hq, h = bh % Hq, g = h % Hkv;\n        size_t kv = (size_t)b * Hkv + g;\n        head_forward"),
     "sin_weight_ignored": ("return p == 0 ? cw[i] : sw[i];", "return p == 0 ? cw[i] : cw[i];"),
     "elu_derivative": ("if (phi == ORACLE_PHI_ELU1) return x > 0.0 ? 1.0 : exp(x);",
                        "if (phi == ORACLE_PHI_ELU1) return 1.0;"),
