@@ -54,9 +54,9 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Host-only argument checks shared by every entry point.
-la_status check_shape(int B, int Hq, int Hkv, int N, int D, int dtype, int phi, float eps,
+la_status check_shape(int B, int Hq, int Hkv, int N, int D, int Dv, int dtype, int phi, float eps,
                       const float *cw, const float *sw) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || D <= 0) return LA_ERR_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || D <= 0 || Dv <= 0) return LA_ERR_ARG;
     if (Hq % Hkv != 0) return LA_ERR_ARG;
     if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_ARG;
     if (phi != LA_PHI_ELU1 && phi != LA_PHI_RELU && phi != LA_PHI_IDENTITY) return LA_ERR_ARG;
@@ -64,17 +64,19 @@ la_status check_shape(int B, int Hq, int Hkv, int N, int D, int dtype, int phi, 
     if ((cw == nullptr) != (sw == nullptr)) return LA_ERR_ARG;
     // element counts must fit comfortably in 64 bits
     const unsigned long long elems = (unsigned long long)B * (unsigned long long)Hq *
-                                     (unsigned long long)N * (unsigned long long)D;
+                                     (unsigned long long)N * (unsigned long long)(D > Dv ? D : Dv);
     if (elems >> 60) return LA_ERR_ARG;
     if (D != 32 && D != 64 && D != 128) return LA_ERR_UNSUPPORTED;
+    if (Dv != 32 && Dv != 64 && Dv != 128) return LA_ERR_UNSUPPORTED;
     return LA_OK;
 }
 
 // The work plan, a pure function of the arguments.
-Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, int has_w, int is_bwd) {
+Plan make_plan(int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dt, int causal, int has_w, int is_bwd) {
     Plan pl{};
     pl.P = has_w ? 2 : 1;
-    pl.path = tc_supported(Hq, Hkv, N, D, dt, pl.P, causal, is_bwd) ? LA_PATH_TCGEN05 : LA_PATH_SIMT;
+    // the tensor-core kernels are written for Dv = D; other value widths run on the CUDA cores
+    pl.path = Dv == D && tc_supported(Hq, Hkv, N, D, dt, pl.P, causal, is_bwd) ? LA_PATH_TCGEN05 : LA_PATH_SIMT;
     const int bg = B * Hkv;
     int slots;   // CTAs that run at once on kPlanSms SMs
     if (pl.path == LA_PATH_TCGEN05) {
@@ -103,7 +105,7 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
     }
     pl.seg_len = chunks_per_seg * pl.chunk;
     pl.nseg = (N + pl.seg_len - 1) / pl.seg_len;
-    pl.state_elems = (size_t)pl.P * D * (D + 1);
+    pl.state_elems = (size_t)pl.P * D * (Dv + 1);
     const size_t state_bytes = align_up((size_t)bg * pl.nseg * pl.state_elems * sizeof(float), 256);
     pl.off_state = 0;
     size_t off = state_bytes;
@@ -154,11 +156,11 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, la_dtype dt, int causal, in
 }
 
 la_status run(bool bwd, const void *q, const void *k, const void *v, const void *g, void *out,
-              void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int D, la_dtype dt,
+              void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dt,
               int causal, la_phi phi, float eps, const float *cw, const float *sw, void *ws,
               size_t ws_bytes, void *stream, const void *fwd_ws = nullptr, size_t fwd_ws_bytes = 0,
               const la_strides *const *strides = nullptr) {
-    la_status st = check_shape(B, Hq, Hkv, N, D, dt, phi, eps, cw, sw);
+    la_status st = check_shape(B, Hq, Hkv, N, D, Dv, dt, phi, eps, cw, sw);
     if (st != LA_OK) return st;
     if (!q || !k || !v) return LA_ERR_ARG;
     if (bwd ? (!g || !dq || !dk || !dv) : !out) return LA_ERR_ARG;
@@ -166,14 +168,14 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     for (const void *ptr : ptrs)
         if (ptr && !aligned(ptr, 16)) return LA_ERR_ALIGN;
     // input strides (q, k, v, grad_out): contiguous unless given
-    Strides ist[4] = {contiguous_strides(Hq, N, D), contiguous_strides(Hkv, N, D), contiguous_strides(Hkv, N, D),
-                     contiguous_strides(Hq, N, D)};
+    Strides ist[4] = {contiguous_strides(Hq, N, D), contiguous_strides(Hkv, N, D), contiguous_strides(Hkv, N, Dv),
+                     contiguous_strides(Hq, N, Dv)};
     for (int i = 0; strides && i < 4; ++i)
         if (strides[i]) {
             if (strides[i]->b < 0 || strides[i]->h < 0 || strides[i]->n < 0) return LA_ERR_ARG;
             ist[i] = Strides{strides[i]->b, strides[i]->h, strides[i]->n};
         }
-    const Plan pl = make_plan(B, Hq, Hkv, N, D, dt, causal, cw != nullptr, bwd);
+    const Plan pl = make_plan(B, Hq, Hkv, N, D, Dv, dt, causal, cw != nullptr, bwd);
     if (pl.ws_bytes > 0) {
         if (!ws || ws_bytes < pl.ws_bytes) return LA_ERR_WORKSPACE;
         if (!aligned(ws, 256)) return LA_ERR_ALIGN;
@@ -187,7 +189,7 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     p.st_q = ist[0]; p.st_k = ist[1]; p.st_v = ist[2]; p.st_g = ist[3];
     p.out = out; p.dq = dq; p.dk = dk; p.dv = dv;
     p.cw = cw; p.sw = sw;
-    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.D = D; p.n_rep = Hq / Hkv;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.D = D; p.Dv = Dv; p.n_rep = Hq / Hkv;
     p.P = pl.P; p.phi = phi; p.causal = causal ? 1 : 0; p.eps = eps;
     p.chunk = pl.chunk; p.seg_len = pl.seg_len; p.nseg = pl.nseg;
     char *base = static_cast<char *>(ws);
@@ -208,7 +210,7 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
         // the forward's workspace holds its scanned segment states (and, on the tensor-core
         // path, its per-row dens and its record); they are the backward's when both plans cut
         // the sequence the same way
-        const Plan pf = make_plan(B, Hq, Hkv, N, D, dt, causal, cw != nullptr, 0);
+        const Plan pf = make_plan(B, Hq, Hkv, N, D, Dv, dt, causal, cw != nullptr, 0);
         if (pf.path == pl.path && pf.chunk == pl.chunk && pf.seg_len == pl.seg_len && pf.nseg == pl.nseg &&
             pf.P == pl.P && pf.state_elems == pl.state_elems && fwd_ws_bytes >= pf.ws_bytes && aligned(fwd_ws, 256)) {
             char *f = const_cast<char *>(static_cast<const char *>(fwd_ws));
@@ -282,23 +284,48 @@ extern "C" {
 
 size_t la_workspace_size(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
                          int has_weights, int is_bwd) {
-    const float *w = has_weights ? reinterpret_cast<const float *>(16) : nullptr;
-    if (check_shape(B, Hq, Hkv, N, D, dtype, LA_PHI_ELU1, 0.f, w, w) != LA_OK) return 0;
-    return make_plan(B, Hq, Hkv, N, D, dtype, is_causal, has_weights, is_bwd).ws_bytes;
+    return la_workspace_size_v(B, Hq, Hkv, N, D, D, dtype, is_causal, has_weights, is_bwd);
 }
 
 la_path la_kernel_path(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
                        int has_weights, int is_bwd) {
+    return la_kernel_path_v(B, Hq, Hkv, N, D, D, dtype, is_causal, has_weights, is_bwd);
+}
+
+size_t la_workspace_size_v(int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dtype, int is_causal,
+                           int has_weights, int is_bwd) {
     const float *w = has_weights ? reinterpret_cast<const float *>(16) : nullptr;
-    if (check_shape(B, Hq, Hkv, N, D, dtype, LA_PHI_ELU1, 0.f, w, w) != LA_OK) return LA_PATH_SIMT;
-    return make_plan(B, Hq, Hkv, N, D, dtype, is_causal, has_weights, is_bwd).path;
+    if (check_shape(B, Hq, Hkv, N, D, Dv, dtype, LA_PHI_ELU1, 0.f, w, w) != LA_OK) return 0;
+    return make_plan(B, Hq, Hkv, N, D, Dv, dtype, is_causal, has_weights, is_bwd).ws_bytes;
+}
+
+la_path la_kernel_path_v(int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dtype, int is_causal,
+                         int has_weights, int is_bwd) {
+    const float *w = has_weights ? reinterpret_cast<const float *>(16) : nullptr;
+    if (check_shape(B, Hq, Hkv, N, D, Dv, dtype, LA_PHI_ELU1, 0.f, w, w) != LA_OK) return LA_PATH_SIMT;
+    return make_plan(B, Hq, Hkv, N, D, Dv, dtype, is_causal, has_weights, is_bwd).path;
+}
+
+la_status la_fwd_v(const void *q, const void *k, const void *v, void *out, int B, int Hq, int Hkv, int N, int D,
+                   int Dv, la_dtype dtype, int is_causal, la_phi phi, float eps, const float *cos_weight,
+                   const float *sin_weight, void *workspace, size_t ws_bytes, void *stream) {
+    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, Dv, dtype, is_causal, phi,
+               eps, cos_weight, sin_weight, workspace, ws_bytes, stream);
+}
+
+la_status la_bwd_v(const void *q, const void *k, const void *v, const void *grad_out, void *dq, void *dk, void *dv,
+                   int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dtype, int is_causal, la_phi phi, float eps,
+                   const float *cos_weight, const float *sin_weight, const void *fwd_workspace, size_t fwd_ws_bytes,
+                   void *workspace, size_t ws_bytes, void *stream) {
+    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, Dv, dtype, is_causal, phi, eps,
+               cos_weight, sin_weight, workspace, ws_bytes, stream, fwd_workspace, fwd_ws_bytes);
 }
 
 la_status la_fwd(const void *q, const void *k, const void *v, void *out, int B, int Hq, int Hkv,
                  int N, int D, la_dtype dtype, int is_causal, la_phi phi, float eps,
                  const float *cos_weight, const float *sin_weight, void *workspace,
                  size_t ws_bytes, void *stream) {
-    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, dtype,
+    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, D, dtype,
                is_causal, phi, eps, cos_weight, sin_weight, workspace, ws_bytes, stream);
 }
 
@@ -306,7 +333,7 @@ la_status la_bwd(const void *q, const void *k, const void *v, const void *grad_o
                  void *dk, void *dv, int B, int Hq, int Hkv, int N, int D, la_dtype dtype,
                  int is_causal, la_phi phi, float eps, const float *cos_weight,
                  const float *sin_weight, void *workspace, size_t ws_bytes, void *stream) {
-    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, dtype, is_causal,
+    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, D, dtype, is_causal,
                phi, eps, cos_weight, sin_weight, workspace, ws_bytes, stream);
 }
 
@@ -315,7 +342,7 @@ la_status la_bwd_from_fwd(const void *q, const void *k, const void *v, const voi
                           float eps, const float *cos_weight, const float *sin_weight, const void *fwd_workspace,
                           size_t fwd_ws_bytes, void *workspace, size_t ws_bytes, void *stream) {
     if (!fwd_workspace) return LA_ERR_ARG;
-    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, dtype, is_causal, phi, eps,
+    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, D, dtype, is_causal, phi, eps,
                cos_weight, sin_weight, workspace, ws_bytes, stream, fwd_workspace, fwd_ws_bytes);
 }
 
@@ -324,7 +351,7 @@ la_status la_fwd_strided(const void *q, const void *k, const void *v, void *out,
                          const float *sin_weight, const la_strides *q_strides, const la_strides *k_strides,
                          const la_strides *v_strides, void *workspace, size_t ws_bytes, void *stream) {
     const la_strides *st[4] = {q_strides, k_strides, v_strides, nullptr};
-    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, dtype, is_causal, phi, eps,
+    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, D, dtype, is_causal, phi, eps,
                cos_weight, sin_weight, workspace, ws_bytes, stream, nullptr, 0, st);
 }
 la_status la_bwd_strided(const void *q, const void *k, const void *v, const void *grad_out, void *dq, void *dk, void *dv,
@@ -334,7 +361,7 @@ la_status la_bwd_strided(const void *q, const void *k, const void *v, const void
                          const void *fwd_workspace, size_t fwd_ws_bytes, void *workspace, size_t ws_bytes,
                          void *stream) {
     const la_strides *st[4] = {q_strides, k_strides, v_strides, g_strides};
-    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, dtype, is_causal, phi, eps, cos_weight,
+    return run(true, q, k, v, grad_out, nullptr, dq, dk, dv, B, Hq, Hkv, N, D, D, dtype, is_causal, phi, eps, cos_weight,
                sin_weight, workspace, ws_bytes, stream, fwd_workspace, fwd_ws_bytes, st);
 }
 
@@ -357,7 +384,7 @@ const char *la_status_str(la_status status) {
     switch (status) {
         case LA_OK: return "ok";
         case LA_ERR_ARG: return "invalid argument";
-        case LA_ERR_UNSUPPORTED: return "unsupported head dimension (D must be 32, 64 or 128)";
+        case LA_ERR_UNSUPPORTED: return "unsupported head dimension (D and Dv must be 32, 64 or 128)";
         case LA_ERR_ALIGN: return "misaligned pointer (16 bytes; workspace 256 bytes)";
         case LA_ERR_CUDA: return "CUDA error";
         case LA_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
@@ -543,14 +570,14 @@ extern "C" la_status la_fwd_static_ws(const void *q, const void *k, const void *
                                       int is_causal, la_phi phi, float eps,
                                       const float *cos_weight, const float *sin_weight,
                                       void *stream) {
-    la_status st = check_shape(B, Hq, Hkv, N, D, dtype, phi, eps, cos_weight, sin_weight);
+    la_status st = check_shape(B, Hq, Hkv, N, D, D, dtype, phi, eps, cos_weight, sin_weight);
     if (st != LA_OK) return st;
     const size_t need =
-        make_plan(B, Hq, Hkv, N, D, dtype, is_causal, cos_weight != nullptr, 0).ws_bytes;
+        make_plan(B, Hq, Hkv, N, D, D, dtype, is_causal, cos_weight != nullptr, 0).ws_bytes;
     if (need > LA_STATIC_WS_BYTES) return LA_ERR_STATIC_WS_LIMIT;
     void *ws = nullptr;
     cudaError_t e = static_ws_address(&ws);
     if (e != cudaSuccess) return cuda_fail(e);
-    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, dtype,
+    return run(false, q, k, v, nullptr, out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, D, D, dtype,
                is_causal, phi, eps, cos_weight, sin_weight, ws, LA_STATIC_WS_BYTES, stream);
 }

@@ -43,6 +43,7 @@ struct Params {
     void *out, *dq, *dk, *dv;    // outputs
     const float *cw, *sw;        // position weights or null
     int B, Hq, Hkv, N, D, n_rep, P, phi, causal;
+    int Dv;                      // value width (v, out, grad_out, dv rows); D on the tensor-core path
     float eps;
     int chunk, seg_len, nseg;    // work split along the sequence
     float *state;                // per (b, kv head, segment) forward state partials

@@ -16,8 +16,10 @@
 //   backward  k_seg_state -> k_scan -> k_bwd_dq (dq, and per-row den, gd)
 //             -> k_seg_rstate -> k_scan (exclusive suffix, or total) -> k_bwd_dkdv
 //
-// State layout in the workspace: [B*Hkv][nseg][P][D][D+1] float32, where column D holds
-// z (the value vector is augmented with a constant 1, so S and z update together).
+// State layout in the workspace: [B*Hkv][nseg][P][D][Dv+1] float32, where column Dv holds
+// z (the value vector is augmented with a constant 1, so S and z update together).  The
+// value width Dv (v, out, grad_out and dv rows) may differ from the head dimension D (q, k,
+// dq and dk rows); the kernels take both as template parameters D and DV.
 #include "la_internal.cuh"
 
 namespace la {
@@ -47,26 +49,28 @@ __device__ __forceinline__ const T *head_ptr(const void *base, const Strides &st
     return static_cast<const T *>(base) + (long long)(bh / H) * st.b + (long long)(bh % H) * st.h;
 }
 
-// Key/value chunk [c0, c0 + kC) clipped to t1: bsm[term][j][d] = w_j^term phi(k_jd),
-// vsm[j][e] = v_je with vsm[j][D] = 1; rows past t1 are all zero (phi(0) is not 0 for
-// elu+1, so padding must be explicit).  kraw (optional) gets k itself.
-template <typename T, int D, int P>
+// Key/value chunk [c0, c0 + kC) clipped to t1: bsm[term][j][d] = w_j^term phi(k_jd) (row
+// pitch D + 1), vsm[j][e] = v_je with vsm[j][DV] = 1 (row pitch DV + 1); rows past t1 are
+// all zero (phi(0) is not 0 for elu+1, so padding must be explicit).  kraw (optional) gets k
+// itself.
+template <typename T, int D, int DV, int P>
 __device__ void load_kv(const Params &p, const T *kb, const T *vb, int c0, int t1, float *bsm,
                         float *vsm, float *kraw) {
-    constexpr int DP = D + 1;
+    constexpr int DP = D + 1, DVP = DV + 1;
     for (int idx = threadIdx.x; idx < kC * D; idx += kThreads) {
         const int j = idx / D, d = idx - j * D, t = c0 + j;
         const bool ok = t < t1;
         const float kv = ok ? to_f32(kb[(long long)t * p.st_k.n + d]) : 0.f;
-        const float vv = ok ? to_f32(vb[(long long)t * p.st_v.n + d]) : 0.f;
         const float f = ok ? feature(kv, p.phi) : 0.f;
 #pragma unroll
         for (int term = 0; term < P; ++term)
             bsm[(term * kC + j) * DP + d] = ok ? pos_weight(p, term, t) * f : 0.f;
-        vsm[j * DP + d] = vv;
         if (kraw) kraw[j * DP + d] = kv;
     }
-    for (int j = threadIdx.x; j < kC; j += kThreads) vsm[j * DP + D] = (c0 + j < t1) ? 1.f : 0.f;
+    for (int idx = threadIdx.x; idx < kC * DVP; idx += kThreads) {
+        const int j = idx / DVP, e = idx - j * DVP, t = c0 + j;
+        vsm[idx] = t < t1 ? (e < DV ? to_f32(vb[(long long)t * p.st_v.n + e]) : 1.f) : 0.f;
+    }
 }
 
 // Query chunk: asm_[term][i][d] = w_i^term phi(q_id) (0 past t1); qraw gets q.
@@ -85,15 +89,15 @@ __device__ void load_q(const Params &p, const T *qb, int c0, int t1, float *asm_
     }
 }
 
-// gx[i][e] = g_ie / den_i and gx[i][D] = gd_i from the saved per-row den and gd.
-template <typename T, int D>
+// gx[i][e] = g_ie / den_i and gx[i][DV] = gd_i from the saved per-row den and gd.
+template <typename T, int DV>
 __device__ void load_gx(const Params &p, const T *gb, const float *denb, const float *gdb, int c0,
                         int t1, float *gx) {
-    constexpr int DP = D + 1;
-    for (int idx = threadIdx.x; idx < kC * DP; idx += kThreads) {
-        const int i = idx / DP, e = idx - i * DP, t = c0 + i;
+    constexpr int DVP = DV + 1;
+    for (int idx = threadIdx.x; idx < kC * DVP; idx += kThreads) {
+        const int i = idx / DVP, e = idx - i * DVP, t = c0 + i;
         float x = 0.f;
-        if (t < t1) x = (e < D) ? to_f32(gb[(long long)t * p.st_g.n + e]) / denb[t] : gdb[t];
+        if (t < t1) x = (e < DV) ? to_f32(gb[(long long)t * p.st_g.n + e]) / denb[t] : gdb[t];
         gx[idx] = x;
     }
 }
@@ -115,23 +119,24 @@ __device__ void intra_scores(const float *asm_, const float *bsm, float *Asm) {
     Asm[i * kC + j] = acc;
 }
 
-// S[term][d][e] += sum_j rows[term][j][d] * cols[j][e] over the whole state.
-template <int D, int P>
+// S[term][d][e] += sum_j rows[term][j][d] * cols[j][e] over the whole state (rows: feature
+// rows of pitch D + 1; cols: augmented value rows of pitch DV + 1).
+template <int D, int DV, int P>
 __device__ void state_update(float *S, const float *rows, const float *cols) {
-    constexpr int DP = D + 1;
-    for (int idx = threadIdx.x; idx < P * D * DP; idx += kThreads) {
-        const int pd = idx / DP, e = idx - pd * DP, term = pd / D, d = pd - term * D;
+    constexpr int DP = D + 1, DVP = DV + 1;
+    for (int idx = threadIdx.x; idx < P * D * DVP; idx += kThreads) {
+        const int pd = idx / DVP, e = idx - pd * DVP, term = pd / D, d = pd - term * D;
         const float *rc = rows + term * kC * DP + d;
         float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < kC; ++j) acc += rc[j * DP] * cols[j * DP + e];
+        for (int j = 0; j < kC; ++j) acc += rc[j * DP] * cols[j * DVP + e];
         S[idx] += acc;
     }
 }
 
-template <int D, int P>
+template <int D, int DV, int P>
 __device__ void load_state(float *S, const float *src) {
-    for (int i = threadIdx.x; i < P * D * (D + 1); i += kThreads) S[i] = src[i];
+    for (int i = threadIdx.x; i < P * D * (DV + 1); i += kThreads) S[i] = src[i];
 }
 
 // Sum over the 16 lanes that share a row (lanes 0-15 or 16-31 of a warp).
@@ -143,24 +148,24 @@ __device__ __forceinline__ float row_sum16(float x) {
 
 // ---------------------------------------------------------------------------------------
 // Per-segment state S = sum_j b_j [v_j, 1]^T over the segment's tokens.
-template <typename T, int D, int P>
+template <typename T, int D, int DV, int P>
 __global__ void __launch_bounds__(kThreads) k_seg_state(Params p) {
     pdl_wait();
-    constexpr int DP = D + 1;
+    constexpr int DP = D + 1, DVP = DV + 1;
     extern __shared__ float sm[];
-    float *S = sm, *bsm = S + P * D * DP, *vsm = bsm + P * kC * DP;
+    float *S = sm, *bsm = S + P * D * DVP, *vsm = bsm + P * kC * DP;
     const Seg sg = my_segment(p);
-    for (int i = threadIdx.x; i < P * D * DP; i += kThreads) S[i] = 0.f;
+    for (int i = threadIdx.x; i < P * D * DVP; i += kThreads) S[i] = 0.f;
     const T *kb = head_ptr<T>(p.k, p.st_k, sg.bg, p.Hkv), *vb = head_ptr<T>(p.v, p.st_v, sg.bg, p.Hkv);
     for (int c0 = sg.t0; c0 < sg.t1; c0 += kC) {
         __syncthreads();
-        load_kv<T, D, P>(p, kb, vb, c0, sg.t1, bsm, vsm, nullptr);
+        load_kv<T, D, DV, P>(p, kb, vb, c0, sg.t1, bsm, vsm, nullptr);
         __syncthreads();
-        state_update<D, P>(S, bsm, vsm);
+        state_update<D, DV, P>(S, bsm, vsm);
     }
     __syncthreads();
-    float *dst = p.state + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DP);
-    for (int i = threadIdx.x; i < P * D * DP; i += kThreads) dst[i] = S[i];
+    float *dst = p.state + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DVP);
+    for (int i = threadIdx.x; i < P * D * DVP; i += kThreads) dst[i] = S[i];
 }
 
 // Scan of segment states along the sequence, per (batch, kv head), in a fixed order.
@@ -196,21 +201,22 @@ __global__ void k_scan(float *X, int nseg, size_t elems, int mode) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Forward: out_i = (A V + a S)_i / (rowsum A + a . z + eps)_i per query head.
-template <typename T, int D, int P>
+// Forward: out_i = (A V + a S)_i / (rowsum A + a . z + eps)_i per query head.  Thread
+// (i, l): query row i of the chunk, output columns l + 16 m.
+template <typename T, int D, int DV, int P>
 __global__ void __launch_bounds__(kThreads) k_fwd(Params p) {
     pdl_wait();
-    constexpr int DP = D + 1, M = D / 16;
+    constexpr int DP = D + 1, DVP = DV + 1, M = D / 16, MV = DV / 16;
     extern __shared__ float sm[];
-    float *S = sm, *asm_ = S + P * D * DP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
-          *Asm = vsm + kC * DP;
+    float *S = sm, *asm_ = S + P * D * DVP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
+          *Asm = vsm + kC * DVP;
     const Seg sg = my_segment(p);
-    load_state<D, P>(S, p.state + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DP));
+    load_state<D, DV, P>(S, p.state + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DVP));
     const T *kb = head_ptr<T>(p.k, p.st_k, sg.bg, p.Hkv), *vb = head_ptr<T>(p.v, p.st_v, sg.bg, p.Hkv);
     const int i = threadIdx.x / 16, l = threadIdx.x % 16;
     for (int c0 = sg.t0; c0 < sg.t1; c0 += kC) {
         __syncthreads();
-        load_kv<T, D, P>(p, kb, vb, c0, sg.t1, bsm, vsm, nullptr);
+        load_kv<T, D, DV, P>(p, kb, vb, c0, sg.t1, bsm, vsm, nullptr);
         for (int r = 0; r < p.n_rep; ++r) {
             const int bh = sg.b * p.Hq + sg.g * p.n_rep + r;
             __syncthreads();
@@ -218,63 +224,63 @@ __global__ void __launch_bounds__(kThreads) k_fwd(Params p) {
             __syncthreads();
             if (p.causal) intra_scores<D, P>(asm_, bsm, Asm);
             __syncthreads();
-            float acc[M];
+            float acc[MV];
 #pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] = 0.f;
+            for (int m = 0; m < MV; ++m) acc[m] = 0.f;
             float dpart = 0.f;
             if (p.causal) {
                 for (int j = 0; j < kC; ++j) {
                     const float a = Asm[i * kC + j];
 #pragma unroll
-                    for (int m = 0; m < M; ++m) acc[m] += a * vsm[j * DP + l + 16 * m];
+                    for (int m = 0; m < MV; ++m) acc[m] += a * vsm[j * DVP + l + 16 * m];
                 }
                 dpart += Asm[i * kC + l];
             }
 #pragma unroll
             for (int term = 0; term < P; ++term) {
-                const float *ar = asm_ + (term * kC + i) * DP, *St = S + term * D * DP;
+                const float *ar = asm_ + (term * kC + i) * DP, *St = S + term * D * DVP;
                 for (int d = 0; d < D; ++d) {
                     const float a = ar[d];
 #pragma unroll
-                    for (int m = 0; m < M; ++m) acc[m] += a * St[d * DP + l + 16 * m];
+                    for (int m = 0; m < MV; ++m) acc[m] += a * St[d * DVP + l + 16 * m];
                 }
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     const int d = l + 16 * m;
-                    dpart += ar[d] * St[d * DP + D];
+                    dpart += ar[d] * St[d * DVP + DV];
                 }
             }
             const float den = row_sum16(dpart) + p.eps;
             const int t = c0 + i;
             if (t < sg.t1) {
-                T *ob = static_cast<T *>(p.out) + ((size_t)bh * p.N + t) * D;
+                T *ob = static_cast<T *>(p.out) + ((size_t)bh * p.N + t) * DV;
 #pragma unroll
-                for (int m = 0; m < M; ++m) ob[l + 16 * m] = from_f32<T>(acc[m] / den);
+                for (int m = 0; m < MV; ++m) ob[l + 16 * m] = from_f32<T>(acc[m] / den);
             }
         }
         if (p.causal) {
             __syncthreads();
-            state_update<D, P>(S, bsm, vsm);
+            state_update<D, DV, P>(S, bsm, vsm);
         }
     }
 }
 
 // ---------------------------------------------------------------------------------------
 // Backward, pass 1: dq, and the per-row den_i and gd_i = -(g_i . num_i) / den_i^2.
-template <typename T, int D, int P>
+template <typename T, int D, int DV, int P>
 __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
     pdl_wait();
-    constexpr int DP = D + 1, M = D / 16;
+    constexpr int DP = D + 1, DVP = DV + 1, M = D / 16, MV = DV / 16;
     extern __shared__ float sm[];
-    float *S = sm, *asm_ = S + P * D * DP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
-          *qraw = vsm + kC * DP, *gx = qraw + kC * DP, *Asm = gx + kC * DP, *dAsm = Asm + kC * kC;
+    float *S = sm, *asm_ = S + P * D * DVP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
+          *qraw = vsm + kC * DVP, *gx = qraw + kC * DP, *Asm = gx + kC * DVP, *dAsm = Asm + kC * kC;
     const Seg sg = my_segment(p);
-    load_state<D, P>(S, p.state + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DP));
+    load_state<D, DV, P>(S, p.state + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DVP));
     const T *kb = head_ptr<T>(p.k, p.st_k, sg.bg, p.Hkv), *vb = head_ptr<T>(p.v, p.st_v, sg.bg, p.Hkv);
     const int i = threadIdx.x / 16, l = threadIdx.x % 16;
     for (int c0 = sg.t0; c0 < sg.t1; c0 += kC) {
         __syncthreads();
-        load_kv<T, D, P>(p, kb, vb, c0, sg.t1, bsm, vsm, nullptr);
+        load_kv<T, D, DV, P>(p, kb, vb, c0, sg.t1, bsm, vsm, nullptr);
         for (int r = 0; r < p.n_rep; ++r) {
             const int bh = sg.b * p.Hq + sg.g * p.n_rep + r;
             const T *gb = head_ptr<T>(p.g, p.st_g, bh, p.Hq);
@@ -283,48 +289,48 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
             __syncthreads();
             if (p.causal) intra_scores<D, P>(asm_, bsm, Asm);
             __syncthreads();
-            // num, den for row i (lane l holds columns l + 16 m)
-            float acc[M];
+            // num, den for row i (lane l holds value columns l + 16 m)
+            float acc[MV];
 #pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] = 0.f;
+            for (int m = 0; m < MV; ++m) acc[m] = 0.f;
             float dpart = 0.f;
             if (p.causal) {
                 for (int j = 0; j < kC; ++j) {
                     const float a = Asm[i * kC + j];
 #pragma unroll
-                    for (int m = 0; m < M; ++m) acc[m] += a * vsm[j * DP + l + 16 * m];
+                    for (int m = 0; m < MV; ++m) acc[m] += a * vsm[j * DVP + l + 16 * m];
                 }
                 dpart += Asm[i * kC + l];
             }
 #pragma unroll
             for (int term = 0; term < P; ++term) {
-                const float *ar = asm_ + (term * kC + i) * DP, *St = S + term * D * DP;
+                const float *ar = asm_ + (term * kC + i) * DP, *St = S + term * D * DVP;
                 for (int d = 0; d < D; ++d) {
                     const float a = ar[d];
 #pragma unroll
-                    for (int m = 0; m < M; ++m) acc[m] += a * St[d * DP + l + 16 * m];
+                    for (int m = 0; m < MV; ++m) acc[m] += a * St[d * DVP + l + 16 * m];
                 }
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     const int d = l + 16 * m;
-                    dpart += ar[d] * St[d * DP + D];
+                    dpart += ar[d] * St[d * DVP + DV];
                 }
             }
             const float den = row_sum16(dpart) + p.eps;
             const int t = c0 + i;
             const bool ok = t < sg.t1;
-            float gv[M], gdot = 0.f;
+            float gv[MV], gdot = 0.f;
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
+            for (int m = 0; m < MV; ++m) {
                 gv[m] = ok ? to_f32(gb[(long long)t * p.st_g.n + l + 16 * m]) : 0.f;
                 gdot += gv[m] * acc[m];
             }
             gdot = row_sum16(gdot);
             const float gdi = ok ? -gdot / (den * den) : 0.f;
 #pragma unroll
-            for (int m = 0; m < M; ++m) gx[i * DP + l + 16 * m] = gv[m] / den;
+            for (int m = 0; m < MV; ++m) gx[i * DVP + l + 16 * m] = gv[m] / den;
             if (l == 0) {
-                gx[i * DP + D] = gdi;
+                gx[i * DVP + DV] = gdi;
                 if (ok) {
                     p.den[(size_t)bh * p.N + t] = den;
                     p.gd[(size_t)bh * p.N + t] = gdi;
@@ -335,11 +341,11 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
                 const int ii = threadIdx.x / kC, j = threadIdx.x % kC;
                 float x = 0.f;
                 if (j <= ii)
-                    for (int e = 0; e < DP; ++e) x += gx[ii * DP + e] * vsm[j * DP + e];
+                    for (int e = 0; e < DVP; ++e) x += gx[ii * DVP + e] * vsm[j * DVP + e];
                 dAsm[ii * kC + j] = x;
             }
             __syncthreads();
-            // da^term_i = sum_j dA_ij b_j^term + S^term gn_i + gd_i z^term
+            // da^term_i = sum_j dA_ij b_j^term + S^term gn_i + gd_i z^term (lane l: features l + 16 m)
             float wt[P];
 #pragma unroll
             for (int term = 0; term < P; ++term) wt[term] = ok ? pos_weight(p, term, t) : 0.f;
@@ -357,11 +363,11 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
 #pragma unroll
                         for (int m = 0; m < M; ++m) da[m] += x * bsm[(term * kC + j) * DP + l + 16 * m];
                     }
-                const float *St = S + term * D * DP;
-                for (int e = 0; e < DP; ++e) {
-                    const float x = gx[i * DP + e];
+                const float *St = S + term * D * DVP;
+                for (int e = 0; e < DVP; ++e) {
+                    const float x = gx[i * DVP + e];
 #pragma unroll
-                    for (int m = 0; m < M; ++m) da[m] += St[(l + 16 * m) * DP + e] * x;
+                    for (int m = 0; m < M; ++m) da[m] += St[(l + 16 * m) * DVP + e] * x;
                 }
 #pragma unroll
                 for (int m = 0; m < M; ++m) dqv[m] += wt[term] * da[m];
@@ -377,78 +383,79 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dq(Params p) {
         }
         if (p.causal) {
             __syncthreads();
-            state_update<D, P>(S, bsm, vsm);
+            state_update<D, DV, P>(S, bsm, vsm);
         }
     }
 }
 
 // Backward, per-segment R = sum over the group's query heads and the segment's rows of
-// a_i [gn_i, gd_i]^T (column D holds r).
-template <typename T, int D, int P>
+// a_i [gn_i, gd_i]^T (column DV holds r).
+template <typename T, int D, int DV, int P>
 __global__ void __launch_bounds__(kThreads) k_seg_rstate(Params p) {
     pdl_wait();
-    constexpr int DP = D + 1;
+    constexpr int DP = D + 1, DVP = DV + 1;
     extern __shared__ float sm[];
-    float *R = sm, *asm_ = R + P * D * DP, *gx = asm_ + P * kC * DP;
+    float *R = sm, *asm_ = R + P * D * DVP, *gx = asm_ + P * kC * DP;
     const Seg sg = my_segment(p);
-    for (int i = threadIdx.x; i < P * D * DP; i += kThreads) R[i] = 0.f;
+    for (int i = threadIdx.x; i < P * D * DVP; i += kThreads) R[i] = 0.f;
     for (int c0 = sg.t0; c0 < sg.t1; c0 += kC) {
         for (int r = 0; r < p.n_rep; ++r) {
             const int bh = sg.b * p.Hq + sg.g * p.n_rep + r;
             __syncthreads();
             load_q<T, D, P>(p, head_ptr<T>(p.q, p.st_q, bh, p.Hq), c0, sg.t1, asm_, nullptr);
-            load_gx<T, D>(p, head_ptr<T>(p.g, p.st_g, bh, p.Hq), p.den + (size_t)bh * p.N,
-                          p.gd + (size_t)bh * p.N, c0, sg.t1, gx);
+            load_gx<T, DV>(p, head_ptr<T>(p.g, p.st_g, bh, p.Hq), p.den + (size_t)bh * p.N,
+                           p.gd + (size_t)bh * p.N, c0, sg.t1, gx);
             __syncthreads();
-            state_update<D, P>(R, asm_, gx);
+            state_update<D, DV, P>(R, asm_, gx);
         }
     }
     __syncthreads();
-    float *dst = p.rstate + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DP);
-    for (int i = threadIdx.x; i < P * D * DP; i += kThreads) dst[i] = R[i];
+    float *dst = p.rstate + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DVP);
+    for (int i = threadIdx.x; i < P * D * DVP; i += kThreads) dst[i] = R[i];
 }
 
 // Backward, pass 2 (reverse over chunks): dk, dv for the kv head, summed over the group.
-template <typename T, int D, int P>
+// Thread (j, l): key row j of the chunk; features l + 16 m (dk) and value columns l + 16 m (dv).
+template <typename T, int D, int DV, int P>
 __global__ void __launch_bounds__(kThreads) k_bwd_dkdv(Params p) {
     pdl_wait();
-    constexpr int DP = D + 1, M = D / 16;
+    constexpr int DP = D + 1, DVP = DV + 1, M = D / 16, MV = DV / 16;
     extern __shared__ float sm[];
-    float *R = sm, *asm_ = R + P * D * DP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
-          *kraw = vsm + kC * DP, *gx = kraw + kC * DP, *Asm = gx + kC * DP, *dAsm = Asm + kC * kC;
+    float *R = sm, *asm_ = R + P * D * DVP, *bsm = asm_ + P * kC * DP, *vsm = bsm + P * kC * DP,
+          *kraw = vsm + kC * DVP, *gx = kraw + kC * DP, *Asm = gx + kC * DVP, *dAsm = Asm + kC * kC;
     const Seg sg = my_segment(p);
-    load_state<D, P>(R, p.rstate + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DP));
+    load_state<D, DV, P>(R, p.rstate + ((size_t)sg.bg * p.nseg + sg.s) * (P * D * DVP));
     const T *kb = head_ptr<T>(p.k, p.st_k, sg.bg, p.Hkv), *vb = head_ptr<T>(p.v, p.st_v, sg.bg, p.Hkv);
     const int j = threadIdx.x / 16, l = threadIdx.x % 16;
     const int nchunks = (sg.t1 - sg.t0 + kC - 1) / kC;
     for (int c = nchunks - 1; c >= 0; --c) {
         const int c0 = sg.t0 + c * kC;
         __syncthreads();
-        load_kv<T, D, P>(p, kb, vb, c0, sg.t1, bsm, vsm, kraw);
+        load_kv<T, D, DV, P>(p, kb, vb, c0, sg.t1, bsm, vsm, kraw);
         __syncthreads();
         // Inter-chunk part from the rows after this chunk: db^term_j = R^term [v_j, 1],
         // dv_j = sum_term (R^term)^T b_j^term.
-        float db[P][M], dvv[M];
+        float db[P][M], dvv[MV];
 #pragma unroll
         for (int term = 0; term < P; ++term) {
-            const float *Rt = R + term * D * DP;
+            const float *Rt = R + term * D * DVP;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const int d = l + 16 * m;
                 float x = 0.f;
-                for (int e = 0; e < DP; ++e) x += Rt[d * DP + e] * vsm[j * DP + e];
+                for (int e = 0; e < DVP; ++e) x += Rt[d * DVP + e] * vsm[j * DVP + e];
                 db[term][m] = x;
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) dvv[m] = 0.f;
+        for (int m = 0; m < MV; ++m) dvv[m] = 0.f;
 #pragma unroll
         for (int term = 0; term < P; ++term) {
-            const float *Rt = R + term * D * DP;
+            const float *Rt = R + term * D * DVP;
             for (int d = 0; d < D; ++d) {
                 const float bv = bsm[(term * kC + j) * DP + d];
 #pragma unroll
-                for (int m = 0; m < M; ++m) dvv[m] += Rt[d * DP + l + 16 * m] * bv;
+                for (int m = 0; m < MV; ++m) dvv[m] += Rt[d * DVP + l + 16 * m] * bv;
             }
         }
         // Intra-chunk part (causal only; bidirectional rows see every key through R).
@@ -456,15 +463,15 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dkdv(Params p) {
             const int bh = sg.b * p.Hq + sg.g * p.n_rep + r;
             __syncthreads();
             load_q<T, D, P>(p, head_ptr<T>(p.q, p.st_q, bh, p.Hq), c0, sg.t1, asm_, nullptr);
-            load_gx<T, D>(p, head_ptr<T>(p.g, p.st_g, bh, p.Hq), p.den + (size_t)bh * p.N,
-                          p.gd + (size_t)bh * p.N, c0, sg.t1, gx);
+            load_gx<T, DV>(p, head_ptr<T>(p.g, p.st_g, bh, p.Hq), p.den + (size_t)bh * p.N,
+                           p.gd + (size_t)bh * p.N, c0, sg.t1, gx);
             __syncthreads();
             {
                 intra_scores<D, P>(asm_, bsm, Asm);
                 const int ii = threadIdx.x / kC, jj = threadIdx.x % kC;
                 float x = 0.f;
                 if (jj <= ii)
-                    for (int e = 0; e < DP; ++e) x += gx[ii * DP + e] * vsm[jj * DP + e];
+                    for (int e = 0; e < DVP; ++e) x += gx[ii * DVP + e] * vsm[jj * DVP + e];
                 dAsm[ii * kC + jj] = x;
                 __syncthreads();
                 // intra: db^term_j += sum_{i >= j} dA_ij a_i^term; dv_j += sum_{i >= j} A_ij gn_i
@@ -475,16 +482,16 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dkdv(Params p) {
 #pragma unroll
                         for (int m = 0; m < M; ++m) db[term][m] += x1 * asm_[(term * kC + i) * DP + l + 16 * m];
 #pragma unroll
-                    for (int m = 0; m < M; ++m) dvv[m] += x2 * gx[i * DP + l + 16 * m];
+                    for (int m = 0; m < MV; ++m) dvv[m] += x2 * gx[i * DVP + l + 16 * m];
                 }
                 // rows of this chunk join the suffix state for earlier chunks
-                state_update<D, P>(R, asm_, gx);
+                state_update<D, DV, P>(R, asm_, gx);
             }
         }
         const int t = c0 + j;
         if (t < sg.t1) {
             T *dkb = static_cast<T *>(p.dk) + ((size_t)sg.bg * p.N + t) * D;
-            T *dvb = static_cast<T *>(p.dv) + ((size_t)sg.bg * p.N + t) * D;
+            T *dvb = static_cast<T *>(p.dv) + ((size_t)sg.bg * p.N + t) * DV;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const int d = l + 16 * m;
@@ -492,15 +499,16 @@ __global__ void __launch_bounds__(kThreads) k_bwd_dkdv(Params p) {
 #pragma unroll
                 for (int term = 0; term < P; ++term) x += pos_weight(p, term, t) * db[term][m];
                 dkb[d] = from_f32<T>(feature_grad(kraw[j * DP + d], p.phi) * x);
-                dvb[d] = from_f32<T>(dvv[m]);
             }
+#pragma unroll
+            for (int m = 0; m < MV; ++m) dvb[l + 16 * m] = from_f32<T>(dvv[m]);
         }
     }
 }
 
 // ---------------------------------------------------------------------------------------
-template <int D, int P> constexpr size_t smem_state() { return sizeof(float) * P * D * (D + 1); }
-template <int D> constexpr size_t smem_row() { return sizeof(float) * kC * (D + 1); }
+template <int D, int DV, int P> constexpr size_t smem_state() { return sizeof(float) * P * D * (DV + 1); }
+template <int W> constexpr size_t smem_row() { return sizeof(float) * kC * (W + 1); }   // kC rows of W + 1
 constexpr size_t smem_tile() { return sizeof(float) * kC * kC; }
 
 template <typename K>
@@ -511,44 +519,64 @@ cudaError_t launch(const char *name, K kernel, size_t smem, int grid, const Para
     return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, s, p);
 }
 
+// Dynamic shared memory of each kernel: its state, then its feature rows (pitch D + 1), value
+// rows (pitch DV + 1) and score tiles, in the order the kernel lays them out.
+template <int D, int DV, int P> constexpr size_t smem_seg_state() {
+    return smem_state<D, DV, P>() + P * smem_row<D>() + smem_row<DV>();
+}
+template <int D, int DV, int P> constexpr size_t smem_fwd() {
+    return smem_state<D, DV, P>() + 2 * P * smem_row<D>() + smem_row<DV>() + smem_tile();
+}
+template <int D, int DV, int P> constexpr size_t smem_bwd() {   // k_bwd_dq and k_bwd_dkdv
+    return smem_state<D, DV, P>() + (2 * P + 1) * smem_row<D>() + 2 * smem_row<DV>() + 2 * smem_tile();
+}
+template <int D, int DV, int P> constexpr size_t smem_seg_rstate() {
+    return smem_state<D, DV, P>() + P * smem_row<D>() + smem_row<DV>();
+}
 
-
-template <typename T, int D, int P>
+template <typename T, int D, int DV, int P>
 cudaError_t forward_impl(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
-    const size_t elems = (size_t)P * D * (D + 1);
-    cudaError_t e = launch("simt_seg_state", k_seg_state<T, D, P>, smem_state<D, P>() + (P + 1) * smem_row<D>(), grid, p, s);
+    const size_t elems = (size_t)P * D * (DV + 1);
+    cudaError_t e = launch("simt_seg_state", k_seg_state<T, D, DV, P>, smem_seg_state<D, DV, P>(), grid, p, s);
     if (e == cudaSuccess) e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
+    if (e == cudaSuccess) e = launch("simt_fwd", k_fwd<T, D, DV, P>, smem_fwd<D, DV, P>(), grid, p, s);
+    return e;
+}
+
+template <typename T, int D, int DV, int P>
+cudaError_t backward_impl(const Params &p, cudaStream_t s) {
+    const int grid = p.B * p.Hkv * p.nseg;
+    const size_t elems = (size_t)P * D * (DV + 1);
+    cudaError_t e = cudaSuccess;
+    if (!p.state_given) {
+        e = launch("simt_seg_state", k_seg_state<T, D, DV, P>, smem_seg_state<D, DV, P>(), grid, p, s);
+        if (e == cudaSuccess) e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
+    }
+    if (e == cudaSuccess) e = launch("simt_bwd_dq", k_bwd_dq<T, D, DV, P>, smem_bwd<D, DV, P>(), grid, p, s);
     if (e == cudaSuccess)
-        e = launch("simt_fwd", k_fwd<T, D, P>, smem_state<D, P>() + (2 * P + 1) * smem_row<D>() + smem_tile(), grid, p, s);
+        e = launch("simt_seg_rstate", k_seg_rstate<T, D, DV, P>, smem_seg_rstate<D, DV, P>(), grid, p, s);
+    if (e == cudaSuccess) e = scan_segments(p.rstate, p, p.causal ? kScanSuffix : kScanTotal, elems, s);
+    if (e == cudaSuccess) e = launch("simt_bwd_dkdv", k_bwd_dkdv<T, D, DV, P>, smem_bwd<D, DV, P>(), grid, p, s);
     return e;
 }
 
 template <typename T, int D, int P>
-cudaError_t backward_impl(const Params &p, cudaStream_t s) {
-    const int grid = p.B * p.Hkv * p.nseg;
-    const size_t elems = (size_t)P * D * (D + 1);
-    cudaError_t e = cudaSuccess;
-    if (!p.state_given) {
-        e = launch("simt_seg_state", k_seg_state<T, D, P>, smem_state<D, P>() + (P + 1) * smem_row<D>(), grid, p, s);
-        if (e == cudaSuccess) e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, elems, s);
+cudaError_t dispatch_dv(const Params &p, cudaStream_t s, bool bwd) {
+    switch (p.Dv) {
+        case 32: return bwd ? backward_impl<T, D, 32, P>(p, s) : forward_impl<T, D, 32, P>(p, s);
+        case 64: return bwd ? backward_impl<T, D, 64, P>(p, s) : forward_impl<T, D, 64, P>(p, s);
+        case 128: return bwd ? backward_impl<T, D, 128, P>(p, s) : forward_impl<T, D, 128, P>(p, s);
+        default: return cudaErrorInvalidValue;
     }
-    if (e == cudaSuccess)
-        e = launch("simt_bwd_dq", k_bwd_dq<T, D, P>, smem_state<D, P>() + (2 * P + 3) * smem_row<D>() + 2 * smem_tile(), grid, p, s);
-    if (e == cudaSuccess)
-        e = launch("simt_seg_rstate", k_seg_rstate<T, D, P>, smem_state<D, P>() + (P + 1) * smem_row<D>(), grid, p, s);
-    if (e == cudaSuccess) e = scan_segments(p.rstate, p, p.causal ? kScanSuffix : kScanTotal, elems, s);
-    if (e == cudaSuccess)
-        e = launch("simt_bwd_dkdv", k_bwd_dkdv<T, D, P>, smem_state<D, P>() + (2 * P + 3) * smem_row<D>() + 2 * smem_tile(), grid, p, s);
-    return e;
 }
 
 template <typename T, int P>
 cudaError_t dispatch_d(const Params &p, cudaStream_t s, bool bwd) {
     switch (p.D) {
-        case 32: return bwd ? backward_impl<T, 32, P>(p, s) : forward_impl<T, 32, P>(p, s);
-        case 64: return bwd ? backward_impl<T, 64, P>(p, s) : forward_impl<T, 64, P>(p, s);
-        case 128: return bwd ? backward_impl<T, 128, P>(p, s) : forward_impl<T, 128, P>(p, s);
+        case 32: return dispatch_dv<T, 32, P>(p, s, bwd);
+        case 64: return dispatch_dv<T, 64, P>(p, s, bwd);
+        case 128: return dispatch_dv<T, 128, P>(p, s, bwd);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -6,7 +6,8 @@ cosFormer position weights, which are inputs of the operation.  The recipe:
 
 * one CPU ``torch.Generator`` seeded with ``seed`` (0 by default);
 * float32 standard normal draws in the order q, k, v, grad_out, each of its own shape
-  ([B, Hq, N, D] for q and grad_out, [B, Hkv, N, D] for k and v);
+  ([B, Hq, N, D] for q, [B, Hkv, N, D] for k, [B, Hkv, N, Dv] for v and [B, Hq, N, Dv] for
+  grad_out, the value width Dv being D unless the workload sets it);
 * q, k and v multiplied by ``scale`` (grad_out is not scaled);
 * for workloads marked ``positive`` (the identity feature map, whose features the pages
   call non-negative), q and k replaced by their absolute values;
@@ -37,6 +38,11 @@ class Workload:
     weights: bool = False   # cosFormer cos/sin position weights
     scale: float = 1.0
     positive: bool = False  # |q|, |k| (non-negative features for phi = identity)
+    Dv: int | None = None   # value width (v, out, grad_out, dv); None: D
+
+    @property
+    def value_dim(self) -> int:
+        return self.D if self.Dv is None else self.Dv
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -88,8 +94,8 @@ def make_inputs(w: Workload, seed: int = 0, device: str | torch.device = "cpu"):
     ks = (w.B, w.Hkv, w.N, w.D)
     q = torch.randn(qs, generator=gen, dtype=torch.float32)
     k = torch.randn(ks, generator=gen, dtype=torch.float32)
-    v = torch.randn(ks, generator=gen, dtype=torch.float32)
-    g = torch.randn(qs, generator=gen, dtype=torch.float32)
+    v = torch.randn(ks[:3] + (w.value_dim,), generator=gen, dtype=torch.float32)
+    g = torch.randn(qs[:3] + (w.value_dim,), generator=gen, dtype=torch.float32)
     if w.scale != 1.0:
         q.mul_(w.scale)
         k.mul_(w.scale)

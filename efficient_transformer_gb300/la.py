@@ -59,6 +59,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.la_workspace_size.restype = sz
     lib.la_kernel_path.argtypes = [i, i, i, i, i, i, i, i, i]
     lib.la_kernel_path.restype = i
+    lib.la_workspace_size_v.argtypes = [i, i, i, i, i, i, i, i, i, i]
+    lib.la_workspace_size_v.restype = sz
+    lib.la_kernel_path_v.argtypes = [i, i, i, i, i, i, i, i, i, i]
+    lib.la_kernel_path_v.restype = i
+    lib.la_fwd_v.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
+    lib.la_fwd_v.restype = i
+    lib.la_bwd_v.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp, sz, vp]
+    lib.la_bwd_v.restype = i
     lib.la_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
     lib.la_fwd.restype = i
     lib.la_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
@@ -138,7 +146,7 @@ def _check_inputs(q, k, v, cos_weight, sin_weight, extra=()):
         if t.dtype != q.dtype:
             raise TypeError(f"{name} has dtype {t.dtype}, q has {q.dtype}")
     B, Hq, N, D = q.shape
-    if k.shape[0] != B or k.shape[2:] != (N, D) or v.shape != k.shape:
+    if k.shape[0] != B or k.shape[2:] != (N, D) or v.shape[:3] != k.shape[:3]:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
     if (cos_weight is None) != (sin_weight is None):
         raise ValueError("give both cos_weight and sin_weight or neither")
@@ -146,7 +154,7 @@ def _check_inputs(q, k, v, cos_weight, sin_weight, extra=()):
         if w is not None and (w.dtype != torch.float32 or not w.is_cuda or w.shape != (N,)
                               or not w.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous float32 CUDA vector of length N={N}")
-    return B, Hq, k.shape[1], N, D
+    return B, Hq, k.shape[1], N, D, v.shape[3]
 
 
 def _strides(t):
@@ -162,17 +170,17 @@ def _stream_handle(stream) -> ctypes.c_void_p:
 
 
 def workspace_size(B, Hq, Hkv, N, D, dtype: torch.dtype, is_causal: bool, has_weights: bool,
-                   is_bwd: bool) -> int:
+                   is_bwd: bool, Dv: int | None = None) -> int:
     code = LA_F32 if dtype == torch.float32 else LA_BF16
-    return int(load().la_workspace_size(B, Hq, Hkv, N, D, code, int(is_causal), int(has_weights),
-                                        int(is_bwd)))
+    return int(load().la_workspace_size_v(B, Hq, Hkv, N, D, D if Dv is None else Dv, code, int(is_causal),
+                                          int(has_weights), int(is_bwd)))
 
 
 def kernel_path(B, Hq, Hkv, N, D, dtype: torch.dtype, is_causal: bool, has_weights: bool,
-                is_bwd: bool) -> int:
+                is_bwd: bool, Dv: int | None = None) -> int:
     code = LA_F32 if dtype == torch.float32 else LA_BF16
-    return int(load().la_kernel_path(B, Hq, Hkv, N, D, code, int(is_causal), int(has_weights),
-                                     int(is_bwd)))
+    return int(load().la_kernel_path_v(B, Hq, Hkv, N, D, D if Dv is None else Dv, code, int(is_causal),
+                                       int(has_weights), int(is_bwd)))
 
 
 def _workspace(nbytes: int, device, given):
@@ -190,19 +198,28 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, is_causal: bool = Fal
         phi: str = "elu+1", eps: float = 1e-6, cos_weight: torch.Tensor | None = None,
         sin_weight: torch.Tensor | None = None, *, out: torch.Tensor | None = None,
         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Linear-attention forward; returns ``out`` with the shape and dtype of ``q``."""
+    """Linear-attention forward; returns ``out`` [B, Hq, N, Dv] in the dtype of ``q`` (Dv =
+    v's last dimension; with Dv != D the inputs must be contiguous)."""
     lib = load()
-    B, Hq, Hkv, N, D = _check_inputs(q, k, v, cos_weight, sin_weight)
+    B, Hq, Hkv, N, D, Dv = _check_inputs(q, k, v, cos_weight, sin_weight)
+    oshape = (B, Hq, N, Dv)
     if out is None:
-        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
-    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor like q")
+        out = torch.empty(oshape, dtype=q.dtype, device=q.device)
+    elif tuple(out.shape) != oshape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {oshape} tensor of q's dtype")
     dt = _dtype_code(q)
-    ws = _workspace(lib.la_workspace_size(B, Hq, Hkv, N, D, dt, int(is_causal),
-                                          int(cos_weight is not None), 0), q.device, workspace)
+    ws = _workspace(lib.la_workspace_size_v(B, Hq, Hkv, N, D, Dv, dt, int(is_causal),
+                                            int(cos_weight is not None), 0), q.device, workspace)
     nws = 0 if ws is None else ws.numel() * ws.element_size()
     strides = [_strides(t) for t in (q, k, v)]
-    if all(x is None for x in strides):
+    if Dv != D:
+        if any(x is not None for x in strides):
+            raise ValueError("with Dv != D, q, k and v must be contiguous")
+        st = lib.la_fwd_v(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, D, Dv, dt, int(is_causal),
+                          _phi_code(phi), float(eps), _ptr(cos_weight), _ptr(sin_weight), _ptr(ws), nws,
+                          _stream_handle(stream))
+        call = "la_fwd_v"
+    elif all(x is None for x in strides):
         st = lib.la_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, D, dt, int(is_causal),
                         _phi_code(phi), float(eps), _ptr(cos_weight), _ptr(sin_weight), _ptr(ws), nws,
                         _stream_handle(stream))
@@ -223,15 +240,15 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tenso
         dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
         dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None,
         fwd_workspace: torch.Tensor | None = None):
-    """Linear-attention backward; returns ``(dq, dk, dv)`` (dk, dv with k's shape).
+    """Linear-attention backward; returns ``(dq, dk, dv)`` with the shapes of q, k and v.
 
     ``fwd_workspace``: the workspace of the ``fwd`` call just made on the same inputs (ordered
     before this call); its per-segment states are then reused instead of recomputed
     (``la_bwd_from_fwd``).  The results are the same either way."""
     lib = load()
-    B, Hq, Hkv, N, D = _check_inputs(q, k, v, cos_weight, sin_weight, (("grad_out", grad_out),))
-    if grad_out.shape != q.shape:
-        raise ValueError("grad_out must have the shape of q")
+    B, Hq, Hkv, N, D, Dv = _check_inputs(q, k, v, cos_weight, sin_weight, (("grad_out", grad_out),))
+    if tuple(grad_out.shape) != (B, Hq, N, Dv):
+        raise ValueError("grad_out must have the shape of out ([B, Hq, N, Dv])")
     dq = torch.empty(q.shape, dtype=q.dtype, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=k.dtype, device=k.device) if dk is None else dk
     dv = torch.empty(v.shape, dtype=v.dtype, device=v.device) if dv is None else dv
@@ -239,13 +256,22 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tenso
         if t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous tensor like its input")
     dt = _dtype_code(q)
-    ws = _workspace(lib.la_workspace_size(B, Hq, Hkv, N, D, dt, int(is_causal),
-                                          int(cos_weight is not None), 1), q.device, workspace)
+    ws = _workspace(lib.la_workspace_size_v(B, Hq, Hkv, N, D, Dv, dt, int(is_causal),
+                                            int(cos_weight is not None), 1), q.device, workspace)
     nws = 0 if ws is None else ws.numel() * ws.element_size()
     if fwd_workspace is not None and fwd_workspace.device != q.device:
         raise ValueError("fwd_workspace must be on q's device")
     strides = [_strides(t) for t in (q, k, v, grad_out)]
-    if any(x is not None for x in strides):
+    if Dv != D:
+        if any(x is not None for x in strides):
+            raise ValueError("with Dv != D, q, k, v and grad_out must be contiguous")
+        fws = 0 if fwd_workspace is None else fwd_workspace.numel() * fwd_workspace.element_size()
+        st = lib.la_bwd_v(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
+                          B, Hq, Hkv, N, D, Dv, dt, int(is_causal), _phi_code(phi), float(eps),
+                          _ptr(cos_weight), _ptr(sin_weight), _ptr(fwd_workspace), fws,
+                          _ptr(ws), nws, _stream_handle(stream))
+        call = "la_bwd_v"
+    elif any(x is not None for x in strides):
         fws = 0 if fwd_workspace is None else fwd_workspace.numel() * fwd_workspace.element_size()
         st = lib.la_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv),
                                 B, Hq, Hkv, N, D, dt, int(is_causal), _phi_code(phi), float(eps),

@@ -20,8 +20,10 @@
  * expanded key/value tensors are never formed.
  *
  * Layout: q, out, grad_out, dq are contiguous [B, Hq, N, D]; k, v, dk, dv are contiguous
- * [B, Hkv, N, D] (row-major, D fastest; Dv = D); la_fwd_strided and la_bwd_strided take
- * inputs with other strides (D still contiguous).  Elements are float32 (LA_F32) or
+ * [B, Hkv, N, D] (row-major, D fastest); la_fwd_strided and la_bwd_strided take inputs with
+ * other strides (D still contiguous).  la_fwd_v and la_bwd_v take a value width Dv of its
+ * own: v, dv [B, Hkv, N, Dv] and out, grad_out [B, Hq, N, Dv] (`fwd` takes v as a tensor of
+ * its own and reads only q's head dimension; the state S = sum b v^T is then D x Dv).  Elements are float32 (LA_F32) or
  * bfloat16 (LA_BF16); outputs use the input type.  Arithmetic is float32 accumulation in
  * both cases (bfloat16 tensor-core operands on the LA_BF16 fast path).  cos_weight and
  * sin_weight are float32 device vectors of length N, indexed by position, applied to
@@ -43,7 +45,7 @@
  *                       eps negative or not finite, unknown dtype or phi, exactly one of
  *                       cos_weight / sin_weight given, sizes whose element count
  *                       overflows 64 bits
- *   LA_ERR_UNSUPPORTED  D not in {32, 64, 128}
+ *   LA_ERR_UNSUPPORTED  D (or Dv) not in {32, 64, 128}
  *   LA_ERR_ALIGN        a pointer that is not 16-byte aligned (workspace: 256-byte)
  *   LA_ERR_WORKSPACE    ws_bytes < la_workspace_size(...) or workspace NULL while needed;
  *                       (from la_get_status) la_bwd_from_fwd got a workspace that another
@@ -102,6 +104,13 @@ size_t la_workspace_size(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, i
  * the CUDA-core kernels (LA_PATH_SIMT) otherwise. */
 la_path la_kernel_path(int B, int Hq, int Hkv, int N, int D, la_dtype dtype, int is_causal,
                        int has_weights, int is_bwd);
+
+/* la_workspace_size and la_kernel_path for a value width Dv (la_fwd_v, la_bwd_v).  Dv != D
+ * runs on the CUDA-core kernels. */
+size_t la_workspace_size_v(int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dtype, int is_causal,
+                           int has_weights, int is_bwd);
+la_path la_kernel_path_v(int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dtype, int is_causal,
+                         int has_weights, int is_bwd);
 
 /* Forward, `linear_attn.fwd(q, k, v, is_causal, phi, eps, cos_weight, sin_weight)`:
  * writes out [B, Hq, N, D]. */
@@ -170,6 +179,21 @@ la_status la_bwd_strided(const void *q, const void *k, const void *v, const void
                          const la_strides *v_strides, const la_strides *g_strides,
                          const void *fwd_workspace, size_t fwd_ws_bytes, void *workspace,
                          size_t ws_bytes, void *stream);
+
+/* la_fwd with a value width Dv in {32, 64, 128} of its own: q, k [.., N, D]; v [B, Hkv, N,
+ * Dv]; writes out [B, Hq, N, Dv].  All contiguous.  The state S = sum_j b_j v_j^T is D x Dv;
+ * Dv = D is la_fwd.  Workspace: la_workspace_size_v.  Errors as la_fwd. */
+la_status la_fwd_v(const void *q, const void *k, const void *v, void *out, int B, int Hq, int Hkv, int N, int D,
+                   int Dv, la_dtype dtype, int is_causal, la_phi phi, float eps, const float *cos_weight,
+                   const float *sin_weight, void *workspace, size_t ws_bytes, void *stream);
+
+/* la_bwd (fwd_workspace NULL) or la_bwd_from_fwd (fwd_workspace from la_fwd_v with the same
+ * arguments) with a value width Dv: grad_out [B, Hq, N, Dv]; writes dq [B, Hq, N, D], dk
+ * [B, Hkv, N, D] and dv [B, Hkv, N, Dv].  All contiguous.  Errors as la_bwd. */
+la_status la_bwd_v(const void *q, const void *k, const void *v, const void *grad_out, void *dq, void *dk, void *dv,
+                   int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dtype, int is_causal, la_phi phi, float eps,
+                   const float *cos_weight, const float *sin_weight, const void *fwd_workspace, size_t fwd_ws_bytes,
+                   void *workspace, size_t ws_bytes, void *stream);
 
 /* Synchronises `stream`, then returns and clears the device-side error word of the
  * current device: LA_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call,

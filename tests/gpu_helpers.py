@@ -26,7 +26,7 @@ def run_gpu(w: gen.Workload, dev: dict, from_fwd: bool = False):
     has_w = dev["cos_weight"] is not None
     ws_f = None
     if from_fwd:
-        n = la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, has_w, False)
+        n = la.workspace_size(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, has_w, False, Dv=w.value_dim)
         ws_f = torch.empty(max(n, 1), dtype=torch.uint8, device=dev["q"].device)
     out = la.fwd(dev["q"], dev["k"], dev["v"], w.causal, w.phi, w.eps, dev["cos_weight"],
                  dev["sin_weight"], workspace=ws_f)
@@ -58,12 +58,12 @@ def record(w: gen.Workload, errs: dict, label: str = "") -> None:
     path = os.environ.get("LA_PARITY_RECORD")
     if not path:
         return
-    fwd_path = la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, False)
-    bwd_path = la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, True)
+    fwd_path = la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, False, Dv=w.value_dim)
+    bwd_path = la.kernel_path(w.B, w.Hq, w.Hkv, w.N, w.D, w.torch_dtype, w.causal, w.weights, True, Dv=w.value_dim)
     names = {la.LA_PATH_SIMT: "simt", la.LA_PATH_TCGEN05: "tcgen05"}
     row = {"workload": w.name, "label": label, "dtype": w.dtype, "tol": TOL[w.dtype],
            "fwd_path": names[fwd_path], "bwd_path": names[bwd_path],
-           "shape": [w.B, w.Hq, w.Hkv, w.N, w.D], "causal": w.causal, "phi": w.phi, "eps": w.eps,
+           "shape": [w.B, w.Hq, w.Hkv, w.N, w.D, w.value_dim], "causal": w.causal, "phi": w.phi, "eps": w.eps,
            "weights": w.weights, "errors": errs}
     d = os.path.dirname(os.path.abspath(path))
     os.makedirs(d, exist_ok=True)

@@ -177,3 +177,36 @@ def test_strided_argument_errors(lib):
 
     assert bwd(ctypes.byref(neg)) == la.LA_ERR_ARG
     assert bwd(ctypes.byref(odd)) == la.LA_ERR_ALIGN
+
+
+def test_value_width_entry_points(lib):
+    """la_*_v: a value width Dv of its own.  Dv = D is the plain call (same plan, same
+    workspace, same kernel family); Dv != D runs on the CUDA cores; Dv outside {32, 64, 128}
+    is unsupported and checked before any CUDA call."""
+    for D in (32, 64, 128):
+        for is_bwd in (0, 1):
+            assert lib.la_workspace_size_v(1, 8, 2, 3000, D, D, la.LA_BF16, 1, 0, is_bwd) == \
+                lib.la_workspace_size(1, 8, 2, 3000, D, la.LA_BF16, 1, 0, is_bwd)
+            assert lib.la_kernel_path_v(1, 8, 2, 3000, D, D, la.LA_BF16, 1, 0, is_bwd) == \
+                lib.la_kernel_path(1, 8, 2, 3000, D, la.LA_BF16, 1, 0, is_bwd)
+            for Dv in (32, 64, 128):
+                if Dv != D:
+                    assert lib.la_kernel_path_v(1, 8, 2, 3000, D, Dv, la.LA_BF16, 1, 0, is_bwd) == la.LA_PATH_SIMT
+                    assert lib.la_workspace_size_v(1, 8, 2, 3000, D, Dv, la.LA_BF16, 1, 0, is_bwd) > 0
+    # the states hold D (Dv + 1) floats per segment: a wider value grows the workspace
+    assert lib.la_workspace_size_v(1, 8, 2, 3000, 64, 128, la.LA_F32, 1, 0, 0) > \
+        lib.la_workspace_size_v(1, 8, 2, 3000, 64, 32, la.LA_F32, 1, 0, 0)
+    for Dv in (0, -1):
+        assert lib.la_workspace_size_v(1, 8, 2, 64, 64, Dv, la.LA_F32, 1, 0, 0) == 0
+    assert lib.la_workspace_size_v(1, 8, 2, 64, 64, 48, la.LA_F32, 1, 0, 0) == 0
+    fake = ctypes.c_void_p(256)   # never dereferenced: the checks fail first
+    args = (1, 2, 2, 64, 64)
+    assert lib.la_fwd_v(fake, fake, fake, fake, *args, 48, la.LA_F32, 1, 0, 1e-6, None, None, None, 0,
+                        None) == la.LA_ERR_UNSUPPORTED
+    assert lib.la_fwd_v(fake, fake, fake, fake, *args, 0, la.LA_F32, 1, 0, 1e-6, None, None, None, 0,
+                        None) == la.LA_ERR_ARG
+    assert lib.la_bwd_v(fake, fake, fake, fake, fake, fake, fake, *args, 256, la.LA_F32, 1, 0, 1e-6, None, None,
+                        None, 0, None, 0, None) == la.LA_ERR_UNSUPPORTED
+    # a valid Dv with no workspace is a workspace error, still before any CUDA call
+    assert lib.la_fwd_v(fake, fake, fake, fake, *args, 32, la.LA_F32, 1, 0, 1e-6, None, None, None, 0,
+                        None) == la.LA_ERR_WORKSPACE
