@@ -269,6 +269,49 @@ def check_gradient_identities(lib=None):
     return fails
 
 
+def phi_grad_np(x, phi):
+    if phi == "elu+1":
+        return np.where(x > 0, 1.0, np.exp(np.minimum(x, 0.0)))
+    if phi == "identity":
+        return np.ones_like(x)
+    return (x > 0).astype(np.float64)
+
+
+def check_scaling_identities(lib=None, tol=1e-11):
+    """Exact identities of the gradient with respect to the features a_i = w_i phi(q_i) and
+    b_j = w_j phi(k_j) (da = dq / phi'(q), db = dk / phi'(k) elementwise; phi' > 0 for elu+1
+    and identity).  num_i and den_i - eps are bilinear in (a, b), so
+      per row:  sum_d a_id da_id = eps (g_i . out_i) / den_i   (scale a_i alone),
+      overall:  sum_j b_j . db_j = sum_i a_i . da_i            (scale every a, or every b),
+    with den_i from the quadratic form, not from the oracle."""
+    fails = []
+    cases = [(True, "elu+1", False, 2, 2), (False, "elu+1", True, 4, 2), (True, "identity", True, 6, 3),
+             (False, "identity", False, 2, 1)]
+    for idx, (causal, phi, weights, Hq, Hkv) in enumerate(cases):
+        eps = 0.7
+        q, k, v, g, cw, sw = rand_case(2, Hq, Hkv, 7, 4, seed=900 + idx, weights=weights,
+                                       positive=phi == "identity", Dv=5)
+        out = oracle.fwd(q, k, v, causal, phi, eps, cw, sw, lib=lib)
+        dq, dk, _ = oracle.bwd(q, k, v, g, causal, phi, eps, cw, sw, lib=lib)
+        N = q.shape[2]
+        W = np.ones((N, N)) if cw is None else np.outer(cw, cw) + np.outer(sw, sw)
+        if causal:
+            W = np.tril(W)
+        n_rep = Hq // Hkv
+        A = np.einsum("bhid,bhjd->bhij", phi_np(q, phi), phi_np(expand_kv(k, n_rep), phi)) * W
+        den = A.sum(-1) + eps
+        # a . da with a = w phi(q) and da = dq / (w phi'(q)): the weights cancel
+        a_da = np.sum(phi_np(q, phi) * dq / phi_grad_np(q, phi), axis=-1)
+        b_db = np.sum(phi_np(k, phi) * dk / phi_grad_np(k, phi))
+        want = eps * np.sum(g * out, axis=-1) / den
+        e = rel_err(a_da, want)
+        if not e <= tol:
+            fails.append(f"per-row a.da identity case={idx} err={e:.3e}")
+        if abs(b_db - a_da.sum()) > tol * max(1.0, abs(a_da.sum()), np.abs(a_da).sum()):
+            fails.append(f"b.db = a.da identity case={idx}: {b_db} vs {a_da.sum()}")
+    return fails
+
+
 def check_value_width(lib=None, tol_fwd=1e-12, tol_bwd=1e-10, tol_split=1e-13):
     """Dv != D: quadratic form and its autograd, and the value columns' independence."""
     fails = []
@@ -330,7 +373,8 @@ def check_finite_differences(lib=None, h=1e-6, tol=1e-6):
 
 
 ALL_CHECKS = [check_forward_brute, check_backward_autograd, check_gqa_rule, check_closed_forms,
-              check_symmetries, check_gradient_identities, check_value_width, check_finite_differences]
+              check_symmetries, check_gradient_identities, check_scaling_identities, check_value_width,
+              check_finite_differences]
 
 
 def run_all(lib=None):
