@@ -796,6 +796,12 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     uint8_t *obuf = htile + (K::H_IN_DP ? 0 : K::H_BYTES);   // dk, then dv [keys][D] (OUT_STAGE)
     constexpr bool OUT_STAGE = K::OUT_STAGE;
     constexpr bool PSPLIT = CAUSAL && C / 16 >= 2;   // two warpgroups convert P' and dP'
+    // DVSPLIT: the dv epilogue runs on warps 20-23 beside the dk epilogue on warps 8-11 (and the
+    // feature map of K on warps 16-19 only).  With C > 32 (one buffer of TMEM outputs, outputs
+    // written over phi(K) and V) the two epilogues are the tail of a chain that the next
+    // chunk's products wait for: the TMEM buffer is free once both have read it.
+    constexpr bool DVSPLIT = !OUT_STAGE && !WT;
+    constexpr int KVPRO = DVSPLIT ? kKvPro / 2 : kKvPro;   // feature-map threads
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bg = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg;
@@ -830,7 +836,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             mbar_init(&bar_fullq[s], 1);
             mbar_init(&bar_fullg[s], 1);
             mbar_init(&bar_fullkv[s], 1);
-            mbar_init(&bar_ready[s], kKvPro);
+            mbar_init(&bar_ready[s], KVPRO);
             mbar_init(&bar_emptyqg[s], 1);
             mbar_init(&bar_emptykv[s], OUT_STAGE ? 128 : 1);
             mbar_init(&bar_dkready[s], 128);
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
         mbar_init(&bar_pready, PSPLIT ? 256 : 128);
         for (int bb = 0; bb < 2; ++bb) {
             mbar_init(&bar_outfull[bb], 1);
-            mbar_init(&bar_outfree[bb], 128);
+            mbar_init(&bar_outfree[bb], DVSPLIT ? 256 : 128);
         }
         mbar_init(&bar_rbf, 128);
         mbar_init(&bar_rfull, 1);
@@ -1101,11 +1107,43 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             mma_commit_w(&bar_fin);
             warp_drain(&bar_fin, 0);
         }
+    } else if (DVSPLIT && warp >= 20) {
+        // ---------------- warps 20-23 (thread = value column e = d): dv = row e of dv^T, written
+        // over V for the TMA store, beside warps 8-11's dk
+        const int wq = warp % 4;
+        const int d = wq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        bool ok = true;
+        for (int k = 0; k < nchunk; ++k) {
+            const int s = k % NS, bb = k % NB;
+            ok = ok && warp_wait(&bar_outfull[bb], (k / NB) & 1, &abort_flag);
+            tc_fence_after();
+            uint8_t *vw = stage0 + s * K::STAGE + OFF_V;
+#pragma unroll 1
+            for (int c16 = 0; c16 < C / 16; ++c16) {
+                float v[16];
+                if (ok && d < D) {
+                    tmem_ld16(tV(bb) + lane_off + c16 * 16, v);
+                    tmem_wait_regs<16>(v);
+                }
+                if (c16 + 1 == C / 16) {
+                    tc_fence_before();
+                    mbar_arrive_warp(&bar_outfree[bb]);
+                }
+                if (!ok || d >= D) continue;
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    *reinterpret_cast<__nv_bfloat16 *>(vw + swz_offset(C, c16 * 16 + e, d)) = __float2bfloat16_rn(v[e]);
+            }
+            fence_proxy_async();
+            mbar_arrive_warp(&bar_dvready[s]);
+        }
     } else if (warp >= 16) {
-        // ---------------- prologue (warps 16-23 on every chunk): phi(K) over the K tile, in
-        // place (the Q tile arrives as phi_s = phi(q) / den, written by the dq kernel)
-        const int pi = threadIdx.x - 512;   // 0 .. kKvPro - 1
-        constexpr int CPR = D / 8, RPP = kKvPro / CPR;
+        // ---------------- prologue (warps 16-23, or 16-19 with DVSPLIT, on every chunk): phi(K)
+        // over the K tile, in place (the Q tile arrives as phi_s = phi(q) / den, written by the
+        // dq kernel)
+        const int pi = threadIdx.x - 512;   // 0 .. KVPRO - 1
+        constexpr int CPR = D / 8, RPP = KVPRO / CPR;
         static_assert(RPP % 8 == 0, "rows per pass");
         const int c = pi % CPR, r0 = pi / CPR;
         const uint32_t pos = (uint32_t)(((c & 7) ^ (r0 & 7)) << 4);
@@ -1291,6 +1329,12 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
             }
             fence_proxy_async();
             mbar_arrive_warp(&bar_dkready[s]);
+            if constexpr (DVSPLIT) {   // dv is written by warps 20-23; dk^T has been read
+                tc_fence_before();
+                mbar_arrive_warp(&bar_outfree[bb]);
+                r_prev += r_chunk;
+                continue;
+            }
             if (OUT_STAGE) ok = ok && warp_wait(&bar_stfree, 0u, &abort_flag);   // dk of chunk k
 #pragma unroll 1
             for (int c16 = 0; c16 < C / 16; ++c16) {
