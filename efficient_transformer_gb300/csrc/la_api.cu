@@ -105,6 +105,7 @@ Plan make_plan(int B, int Hq, int Hkv, int N, int D, int Dv, la_dtype dt, int ca
     }
     pl.seg_len = chunks_per_seg * pl.chunk;
     pl.nseg = (N + pl.seg_len - 1) / pl.seg_len;
+    pl.scan_in_kernel = pl.path == LA_PATH_TCGEN05 && pl.nseg <= kScanInKernelMaxSeg;
     pl.state_elems = (size_t)pl.P * D * (Dv + 1);
     const size_t state_bytes = align_up((size_t)bg * pl.nseg * pl.state_elems * sizeof(float), 256);
     pl.off_state = 0;
@@ -191,7 +192,7 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
     p.cw = cw; p.sw = sw;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.D = D; p.Dv = Dv; p.n_rep = Hq / Hkv;
     p.P = pl.P; p.phi = phi; p.causal = causal ? 1 : 0; p.eps = eps;
-    p.chunk = pl.chunk; p.seg_len = pl.seg_len; p.nseg = pl.nseg;
+    p.chunk = pl.chunk; p.seg_len = pl.seg_len; p.nseg = pl.nseg; p.scan_in_kernel = pl.scan_in_kernel;
     char *base = static_cast<char *>(ws);
     const bool tc = pl.path == LA_PATH_TCGEN05;
     p.state = reinterpret_cast<float *>(base + pl.off_state);
@@ -212,6 +213,7 @@ la_status run(bool bwd, const void *q, const void *k, const void *v, const void 
         // the sequence the same way
         const Plan pf = make_plan(B, Hq, Hkv, N, D, Dv, dt, causal, cw != nullptr, 0);
         if (pf.path == pl.path && pf.chunk == pl.chunk && pf.seg_len == pl.seg_len && pf.nseg == pl.nseg &&
+            pf.scan_in_kernel == pl.scan_in_kernel &&
             pf.P == pl.P && pf.state_elems == pl.state_elems && fwd_ws_bytes >= pf.ws_bytes && aligned(fwd_ws, 256)) {
             char *f = const_cast<char *>(static_cast<const char *>(fwd_ws));
             p.state = reinterpret_cast<float *>(f + pf.off_state);

@@ -11,6 +11,11 @@
 
 namespace la {
 
+// Segments per sequence up to which the tensor-core kernels join segment states themselves
+// (summing at most this many states when they load a segment's starting state) instead of
+// launching the scan kernel.
+constexpr int kScanInKernelMaxSeg = 8;
+
 // Number of SMs the work split is planned for (GB300: 152).  The split only sets how a
 // head's sequence is cut into segments; results are correct on any device, and for a
 // given set of arguments the split (and so the float summation order) never depends on
@@ -46,6 +51,9 @@ struct Params {
     int Dv;                      // value width (v, out, grad_out, dv rows); D on the tensor-core path
     float eps;
     int chunk, seg_len, nseg;    // work split along the sequence
+    int scan_in_kernel;          // tensor-core path with few segments: the kernels that read a
+                                 // segment's starting state sum the per-segment states themselves
+                                 // (in the scan's order) and no scan kernel runs
     float *state;                // per (b, kv head, segment) forward state partials
     int state_given;             // backward: `state` already holds the scanned forward states
     float *rstate;               // per (b, kv head, segment) backward state partials
@@ -80,6 +88,7 @@ struct Plan {
     int chunk;        // tokens per chunk
     int seg_len;      // tokens per segment (a multiple of chunk)
     int nseg;         // segments per (batch, kv head)
+    int scan_in_kernel;   // see Params
     size_t state_elems;   // floats of one segment state (all terms)
     size_t off_state, off_rstate, off_den, off_gd, off_phis, off_hdr;   // workspace byte offsets
     size_t off_pnum, off_pden;    // tensor-core forward with cos/sin weights: the cos pass's partials

@@ -325,7 +325,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
     // (a group smaller than the tile's) the other rows stay zero and nothing is stored for them
     const int gr = MASK ? p.n_rep : G;
     const int bh0 = b * p.Hq + g * gr;
-    const float *state = p.state + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
+    const float *state_head = p.state + (size_t)bg * p.nseg * (size_t)(D * (D + 1));   // segment 0's state
+    constexpr int kJoin = CAUSAL ? kScanPrefix : kScanTotal;
 
     // the record of this call, checked by a backward that takes this workspace's states and dens
     if (blockIdx.x == 0 && threadIdx.x == 0 && p.hdr) {
@@ -523,12 +524,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 float v[16];
-                state_load16<D>(state, i, c16, v);
+                seg_state_load16<D>(state_head, seg, p.nseg, kJoin, p.scan_in_kernel, i, c16, v);
                 if (CAUSAL) tmem_st16(tS + lane_off + c16 * 16, v);
                 store_state_row<D>(sbf, i, v, c16);
             }
             float zv[16];
-            zv[0] = state_z<D>(state, i);
+            zv[0] = seg_state_z<D>(state_head, seg, p.nseg, kJoin, p.scan_in_kernel, i);
 #pragma unroll
             for (int e = 1; e < 16; ++e) zv[e] = 0.f;
             if (CAUSAL) {
@@ -811,7 +812,8 @@ cudaError_t forward_two_pass(const Params &p, cudaStream_t s) {
         pp.wrow = pass == 1 ? p.cw : p.sw;
         pp.state = p.state + (size_t)(pass - 1) * pass_elems;
         e = launch_state<D, true>(pp, s);
-        if (e == cudaSuccess) e = scan_segments(pp.state, pp, pp.causal ? kScanPrefix : kScanTotal, (size_t)D * (D + 1), s);
+        if (e == cudaSuccess && !pp.scan_in_kernel)
+            e = scan_segments(pp.state, pp, pp.causal ? kScanPrefix : kScanTotal, (size_t)D * (D + 1), s);
         if (e == cudaSuccess)
             e = pp.causal ? launch_fwd<D, G, true, MASK, true>(pp, s) : launch_fwd<D, G, false, MASK, true>(pp, s);
     }
@@ -829,7 +831,7 @@ cudaError_t forward_dg(const Params &p, cudaStream_t s) {
     const char *stop = getenv("LA_DEBUG_STOP");
     if (stop && stop[0] == 's' && stop[1] == 't') return e;      // "state"
 #endif
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !p.scan_in_kernel)
         e = scan_segments(p.state, p, p.causal ? kScanPrefix : kScanTotal, (size_t)D * (D + 1), s);
 #ifdef LA_DEBUG
     if (stop && stop[0] == 's' && stop[1] == 'c') return e;      // "scan"

@@ -219,7 +219,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
     const int gr = MASK ? p.n_rep : G;
     const int bh0 = b * p.Hq + g * gr;
     const size_t seg_state = ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
-    const float *state = p.state + seg_state;
+    const float *state_head = p.state + (size_t)bg * p.nseg * (size_t)(D * (D + 1));   // segment 0's state
+    constexpr int kJoin = CAUSAL ? kScanPrefix : kScanTotal;
     float *rstate = p.rstate + seg_state;
 
     fill_ones_tile(ones, C);
@@ -553,13 +554,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
 #pragma unroll 1
             for (int c16 = h * (HALF / 16); c16 < (h + 1) * (HALF / 16); ++c16) {
                 float v[16];
-                state_load16<D>(state, i, c16, v);
+                seg_state_load16<D>(state_head, seg, p.nseg, kJoin, p.scan_in_kernel, i, c16, v);
                 if (CAUSAL) tmem_st16(tS + lane_off + c16 * 16, v);
                 store_state_row<D>(sbf, i, v, c16);
             }
             if (h == 0) {
                 float zv[16];
-                zv[0] = state_z<D>(state, i);
+                zv[0] = seg_state_z<D>(state_head, seg, p.nseg, kJoin, p.scan_in_kernel, i);
 #pragma unroll
                 for (int e = 1; e < 16; ++e) zv[e] = 0.f;
                 if (CAUSAL) tmem_st16(tS + lane_off + D, zv);
@@ -812,7 +813,8 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
     // a zero h, so that they add nothing to dk, dv, R or r
     const int gr = MASK ? p.n_rep : G;
     const int bh0 = b * p.Hq + g * gr;
-    const float *rstate = p.rstate + ((size_t)bg * p.nseg + seg) * (size_t)(D * (D + 1));
+    const float *rstate_head = p.rstate + (size_t)bg * p.nseg * (size_t)(D * (D + 1));   // segment 0's R
+    constexpr int kJoinR = CAUSAL ? kScanSuffix : kScanTotal;
 
     for (int idx = threadIdx.x; idx < (K::P_BYTES + (K::H_IN_DP ? 0 : K::H_BYTES)) / 16; idx += blockDim.x) {
         uint8_t *t = idx < K::P_BYTES / 16 ? dpbuf + idx * 16 : htile + (idx - K::P_BYTES / 16) * 16;
@@ -1201,11 +1203,11 @@ __global__ void __launch_bounds__(kKvThreads, 1) k_tc_bwd_dkdv(const __grid_cons
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 float v[16];
-                state_load16<D>(rstate, d, c16, v);
+                seg_state_load16<D>(rstate_head, seg, p.nseg, kJoinR, p.scan_in_kernel, d, c16, v);
                 if (CAUSAL) tmem_st16(tR + lane_off + c16 * 16, v);
                 store_rbf_row<D>(rbf, d, v, c16);
             }
-            r_prev = state_z<D>(rstate, d);
+            r_prev = seg_state_z<D>(rstate_head, seg, p.nseg, kJoinR, p.scan_in_kernel, d);
         }
         if (MERGE_H)   // the r part (its two read columns) accumulates onto dk^T's product: clear it
             for (int bb = 0; bb < NB; ++bb) tmem_zero2(tRp(bb) + lane_off);
@@ -1502,7 +1504,7 @@ cudaError_t launch_bwd_kernels(const Params &p, cudaStream_t s) {
         e = launch_pdl(k_tc_bwd_dq<D, G, CAUSAL, MASK, WT>, dim3(grid), dim3(kDqThreads), K::DQ_SMEM, s, mq, mk, mv, mg, mdq,
                        mps, mden, p);
     }
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !p.scan_in_kernel)
         e = scan_segments(p.rstate, p, CAUSAL ? kScanSuffix : kScanTotal, (size_t)D * (D + 1), s);
     if (e != cudaSuccess) return e;
     TraceScope ts(CAUSAL ? "tc_bwd_dkdv_causal" : "tc_bwd_dkdv_bidir", s);

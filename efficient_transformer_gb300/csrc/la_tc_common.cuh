@@ -304,6 +304,40 @@ __device__ __forceinline__ void state_store16(float *st, int d, int c16, const f
     for (int q = 0; q < 4; ++q) p[(c16 * 4 + q) * D + d] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 template <int D> __device__ __forceinline__ float state_z(const float *st, int d) { return st[D * D + d]; }
+
+// A segment's starting state, 16 columns of row d (and z[d]): as the scan kernel left it in the
+// segment's slot, or (in_kernel) summed here from the per-segment states of its sequence (`head`:
+// segment 0's slot) in the scan's own order, so that the bits are the same: the segments before
+// `seg` ascending (kScanPrefix), after it descending (kScanSuffix), or all of them (kScanTotal).
+template <int D>
+__device__ __forceinline__ void seg_state_load16(const float *head, int seg, int nseg, int mode, bool in_kernel, int d,
+                                                 int c16, float *v) {
+    constexpr int E = D * (D + 1);
+    if (!in_kernel) {
+        state_load16<D>(head + (size_t)seg * E, d, c16, v);
+        return;
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = 0.f;
+    const bool down = mode == kScanSuffix;
+    const int n = mode == kScanPrefix ? seg : mode == kScanSuffix ? nseg - 1 - seg : nseg;
+    for (int u = 0; u < n; ++u) {
+        float x[16];
+        state_load16<D>(head + (size_t)(down ? nseg - 1 - u : u) * E, d, c16, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] += x[e];
+    }
+}
+template <int D>
+__device__ __forceinline__ float seg_state_z(const float *head, int seg, int nseg, int mode, bool in_kernel, int d) {
+    constexpr int E = D * (D + 1);
+    if (!in_kernel) return state_z<D>(head + (size_t)seg * E, d);
+    const bool down = mode == kScanSuffix;
+    const int n = mode == kScanPrefix ? seg : mode == kScanSuffix ? nseg - 1 - seg : nseg;
+    float z = 0.f;
+    for (int u = 0; u < n; ++u) z += state_z<D>(head + (size_t)(down ? nseg - 1 - u : u) * E, d);
+    return z;
+}
 template <int D> __device__ __forceinline__ void state_store_z(float *st, int d, float z) { st[D * D + d] = z; }
 
 // z (fp32) into column d of a 16-row K-major z tile as rows 0 and 1: z_hi = bf16(z) and
