@@ -114,6 +114,17 @@ __device__ __forceinline__ float feat_grad_from_feat_w(float f, bool elu, float 
     return elu ? fminf(f, w) : (f > thr ? w : 0.f);
 }
 
+// W (16 or 32) consecutive TMEM columns of the thread's lane into v; the caller's
+// tmem_wait_regs<W>(v) orders every use of v after the load.
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v) {
+    static_assert(W == 16 || W == 32, "16 or 32 columns");
+    if constexpr (W == 32)
+        tmem_ld32(taddr, v);
+    else
+        tmem_ld16(taddr, v);
+}
+
 // z (fp32) into column d of a z tile as the rows (z_hi, z_lo, z_hi), z = z_hi + z_lo.
 template <int D>
 __device__ __forceinline__ void store_split_z(uint8_t *zt, int d, float z) {
@@ -601,18 +612,19 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                             if (c16 * 16 + e <= ti) acc[e & 3] = fmaf(va[e], vd[e], acc[e & 3]);
                     }
                 }
-                // phi_s . X over this half's feature columns, 16 at a time
+                // phi_s . X over this half's feature columns, XW at a time (one TMEM round trip each)
+                constexpr int XW = HALF >= 32 ? 32 : 16;
 #pragma unroll 1
-                for (int c16 = 0; c16 < (WT ? 0 : HALF / 16); ++c16) {
-                    const int col0 = h * HALF + c16 * 16;
-                    float xv[16];
-                    tmem_ld16(tX + lane_off + col0, xv);
-                    uint4 u[2];
+                for (int cx = 0; cx < (WT ? 0 : HALF / XW); ++cx) {
+                    const int col0 = h * HALF + cx * XW;
+                    float xv[XW];
+                    tmem_ld_cols<XW>(tX + lane_off + col0, xv);
+                    uint4 u[XW / 8];
 #pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8) u[q8] = *reinterpret_cast<const uint4 *>(st + swz_chunk(128, i, col0 / 8 + q8));
-                    tmem_wait_regs<16>(xv);
+                    for (int q8 = 0; q8 < XW / 8; ++q8) u[q8] = *reinterpret_cast<const uint4 *>(st + swz_chunk(128, i, col0 / 8 + q8));
+                    tmem_wait_regs<XW>(xv);
 #pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8) {
+                    for (int q8 = 0; q8 < XW / 8; ++q8) {
                         const uint32_t *ui = reinterpret_cast<const uint32_t *>(&u[q8]);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -673,27 +685,30 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
             ok = ok && warp_wait(&bar_dqfull, k & 1, &abort_flag);
             tc_fence_after();
             if (i == 0 && h == 0) LA_TL(k, 11);
+            // 16 columns of X per TMEM round trip: 32 here (as in the row pass) spilled registers
+            // and made the long-context step 3 % slower
+            constexpr int XE = 16;
 #pragma unroll 1
-            for (int c16 = 0; c16 < HALF / 16; ++c16) {
-                const int col0 = h * HALF + c16 * 16;
-                float xv[16];
-                if (ok) tmem_ld16(tX + lane_off + col0, xv);
-                uint8_t *ch[2];
-                uint4 u[2];
+            for (int cx = 0; cx < HALF / XE; ++cx) {
+                const int col0 = h * HALF + cx * XE;
+                float xv[XE];
+                if (ok) tmem_ld_cols<XE>(tX + lane_off + col0, xv);
+                uint8_t *ch[XE / 8];
+                uint4 u[XE / 8];
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8) {   // both loads before either store
+                for (int q8 = 0; q8 < XE / 8; ++q8) {   // every load before any store
                     ch[q8] = st + swz_chunk(128, i, col0 / 8 + q8);
                     u[q8] = *reinterpret_cast<const uint4 *>(ch[q8]);
                 }
-                if (ok) tmem_wait_regs<16>(xv);
-                if (c16 + 1 == HALF / 16) {   // every column of X is in registers
+                if (ok) tmem_wait_regs<XE>(xv);
+                if (cx + 1 == HALF / XE) {   // every column of X is in registers
                     tc_fence_before();
                     mbar_arrive_warp(&bar_xfree);
                 }
                 if (!ok) continue;
                 if constexpr (WT) {   // cos pass: dq terms (fp32) to the workspace, chunk-blocked (a
                                       // warp's rows form one run per column); sin pass: plus those
-                    if (p.pass == 2 && c16 == 0 && h == 0 && i == 0 && k + 1 < nchunk)   // the next chunk's block
+                    if (p.pass == 2 && cx == 0 && h == 0 && i == 0 && k + 1 < nchunk)   // the next chunk's block
                         for (int r2 = 0; r2 < gr; ++r2)                                 // of them into L2
                             prefetch_l2_bulk(p.part_dq + blocked_index(bh0 + r2, t0 + (k + 1) * C, 0, p.N, D, C),
                                              (uint32_t)(D * C * 4));
@@ -725,7 +740,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
                     }
                 } else {
 #pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8)
+                    for (int q8 = 0; q8 < XE / 8; ++q8)
                         if (LA_CHECK(in_smem(ch[q8] + OFF_G, 16, sm_lo, sm_hi), 341, smem_u32(ch[q8]) - sm_lo, q8))
                             *reinterpret_cast<uint4 *>(ch[q8] + OFF_G) =
                                 p.phi == LA_PHI_ELU1   ? dq_piece<LA_PHI_ELU1>(u[q8], xv + q8 * 8, inv)
