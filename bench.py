@@ -266,9 +266,9 @@ def max_over_ranks(x: float, world: int) -> float:
 # on the benchmark workload, from one ncu capture of the current kernels; a kernel changed
 # since its capture must be removed from this table (its traffic is then reported as null).
 MEASURED_TRAFFIC = {
-    "tc_bwd_dq_causal": (1360735402 + 1040020992, "ncu one-pass capture of the current kernels (commit 90ccc69)"),
-    "tc_bwd_dkdv_causal": (1360885674 + 249568853, "ncu one-pass capture of the current kernels (commit 90ccc69)"),
-    "tc_fwd_causal": (815452416 + 498475349, "ncu one-pass capture of the current kernels (commit 90ccc69)"),
+    "tc_bwd_dq_causal": (1361156181 + 1041062826, "ncu one-pass capture of the current kernels (commit c663517)"),
+    "tc_bwd_dkdv_causal": (1361027157 + 249435050, "ncu one-pass capture of the current kernels (commit c663517)"),
+    "tc_fwd_causal": (815492352 + 498729642, "ncu one-pass capture of the current kernels (commit c663517)"),
 }
 
 
