@@ -36,7 +36,11 @@
  * can run at the same time.
  *
  * Execution: la_fwd and la_bwd only enqueue kernels on `stream` (a cudaStream_t; NULL is
- * the legacy default stream) and return; they never synchronise.  Their status covers
+ * the legacy default stream) and return; they never synchronise.  Kernels are launched with
+ * programmatic stream serialization, so a kernel's blocks may be placed while the previous
+ * kernel's last blocks finish; each kernel waits for the work before it on the stream to
+ * complete (griddepcontrol.wait) before it touches memory, so stream order holds as for
+ * plain launches.  Their status covers
  * argument checks and launch errors.  Errors found by a kernel while it runs (a bounded
  * wait that ran out) are latched in a device word that la_get_status() reads.
  *
