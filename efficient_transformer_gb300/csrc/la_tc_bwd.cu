@@ -581,6 +581,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) k_tc_bwd_dq(const __grid_consta
         }
         fence_proxy_async();
         tc_fence_before();
+        if (i == 0 && h == 0) LA_TL(0, 15);   // the segment's starting S, z are in TMEM and S_bf
         mbar_arrive_warp(&bar_sbf);
         bool ok = true;
         for (int k = 0; k < nchunk; ++k) {
