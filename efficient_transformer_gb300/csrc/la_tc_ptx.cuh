@@ -49,9 +49,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // One arrival of weight `count` (for a warp that arrives as a unit).
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count) {
@@ -126,9 +123,6 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 // ---- TMA --------------------------------------------------------------------------------
 
-__device__ __forceinline__ void tma_prefetch(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
 
 // Load one box of a 2-D tensor map at coordinates (x innermost, y) into shared memory,
 // completing `bytes` transaction bytes on *bar.
@@ -148,29 +142,10 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// Bring one box of a 3-D tensor map into L2 (no shared memory, no completion to wait for),
-// so that a later tma_load_3d of the same box finds it there.
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
 
-// Store one box of a 3-D tensor map from shared memory (bulk-group completion).  The
-// caller commits the group and waits for it before reusing the shared-memory source.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk group of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Wait until at most one committed bulk group of this thread (the most recent) may still be
-// reading shared memory.
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Wait until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -297,10 +272,6 @@ __device__ __forceinline__ void mma_bf16_fill_w(uint32_t d_tmem, uint64_t a_desc
                                                 uint32_t accumulate) {
     LA_LANE0_MMA(".collector::a::fill");
 }
-__device__ __forceinline__ void mma_bf16_use_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-    LA_LANE0_MMA(".collector::a::use");
-}
 __device__ __forceinline__ void mma_bf16_lastuse_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                    uint32_t idesc, uint32_t accumulate) {
     LA_LANE0_MMA(".collector::a::lastuse");
@@ -332,14 +303,6 @@ __device__ __forceinline__ void mbar_arrive_w(uint64_t *bar) {
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-        "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
-        "[%2];\n\t}" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
 
 __device__ __forceinline__ void tma_load_4d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z,
                                               int w) {
@@ -367,24 +330,7 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// Bring one box of a 3-D tensor map into L2 from lane 0 (warp-uniform call).
-__device__ __forceinline__ void tma_prefetch_3d_w(const CUtensorMap *map, int x, int y, int z) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-        "@e cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n\t}" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
 
-__device__ __forceinline__ void tma_prefetch_2d_w(const CUtensorMap *map, int x, int y) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-        "@e cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n\t}" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(y)
-        : "memory");
-}
 
 // Store one box from shared memory (bulk-group completion) from lane 0.  Every lane then
 // runs bulk_commit() and bulk_wait_read() / bulk_wait_all() (empty groups for the lanes
@@ -472,7 +418,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Wait for this warp's TMEM loads, then pin the N loaded registers behind the wait: the
 // empty asm "rewrites" each value, so no use of them can be scheduled before the wait.
