@@ -1,4 +1,4 @@
-"""GB300-native fused linear attention (forward and backward).
+"""GB300-native fused linear attention (forward and backward) and the low-rank projection.
 
 The compute path is a C-ABI shared library built from hand-written sm_103a CUDA
 (``csrc/``); ``efficient_transformer_gb300.la`` is its thin Python binding.  Importing
