@@ -534,6 +534,12 @@ template <int D, int DV, int P> constexpr size_t smem_seg_rstate() {
     return smem_state<D, DV, P>() + P * smem_row<D>() + smem_row<DV>();
 }
 
+// Every kernel's shared memory fits one block (227 KB) at the largest state, D = Dv = 128 with
+// cos/sin weights; the other (D, Dv, P) need less.
+static_assert(smem_bwd<128, 128, 2>() <= 227 * 1024 && smem_fwd<128, 128, 2>() <= 227 * 1024 &&
+                  smem_seg_state<128, 128, 2>() <= 227 * 1024 && smem_seg_rstate<128, 128, 2>() <= 227 * 1024,
+              "CUDA-core kernels' shared memory");
+
 template <typename T, int D, int DV, int P>
 cudaError_t forward_impl(const Params &p, cudaStream_t s) {
     const int grid = p.B * p.Hkv * p.nseg;
